@@ -1,0 +1,373 @@
+"""Plain fp64 CPU oracle for DKV decode attention over an anchor + low-rank
+differential KV cache.
+
+TEST INFRASTRUCTURE ONLY.  Imported by ``tests/``, ``__graft_entry__.smoke()``
+and the ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py``; the
+product path never imports, links or runs anything in this directory.  It
+shares no code, header, table or constant with the CUDA library.
+
+Sources (cited by page title and section):
+
+* [DKV-Z]   "DKV: Anchor + Low-Rank Differential KV-Cache Compression for
+            Scalable Long-Context Inference" (Zenodo record), abstract.
+* [README]  "Differential-KV (DKV): Anchor + Low-Rank KV-Cache Compression"
+            (project README), sections "Core Architecture & Paper Overview"
+            (Core), "Core Innovations" (Innov), "Key Environment Knobs"
+            (Knobs), "Measured Paper Benchmarks" (Bench).
+
+What is computed (and where the pages are silent, the reading taken):
+
+* compression of one 256-token block: exact anchor = first token; joint K|V
+  truncated SVD of the deltas to the anchor, S folded into U; exact residual
+  rows = the R rows whose key the low-rank part reconstructs worst (plain L2
+  key error, ties to the lower row); per-block key min/max (router bounds);
+* decode: top-K routing on the per-block upper bound of the GQA-averaged
+  query against the key box; attention over the routed blocks (anchor,
+  low-rank rows, exact residual rows) and the exact recency window.  The
+  plain definition is implemented by materialising the reconstructed keys and
+  values of the routed blocks and taking one softmax; the factored form
+  (low-rank scoring, low-rank value, split log-sum-exp merge) is implemented
+  separately so that the two can pin each other.
+
+Everything runs in float64 on float64 copies of the (fp16) inputs.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+BLOCK_SIZE = 256  # [README Core] fixed micro-blocks of B_s = 256 tokens
+
+
+# ---------------------------------------------------------------------------
+# compression
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class Block:
+    """One compressed block (all fields float64 except ``S``).
+
+    a_k, a_v   [d]        exact anchor token (the block's first token)
+    U          [255, r]   low-rank coefficients of tokens 1..255, S folded in
+    V_K, V_V   [r, d]     key / value halves of the joint right basis
+    S          [R]        token positions (1..255, ascending) kept exact
+    K_res,V_res[R, d]     the exact rows at those positions
+    kmin, kmax [d]        per-channel key extremes over the 256 tokens
+    sigma      [m]        singular values of the delta matrix (diagnostic)
+    err        [255]      key reconstruction error of tokens 1..255
+    """
+
+    a_k: np.ndarray
+    a_v: np.ndarray
+    U: np.ndarray
+    V_K: np.ndarray
+    V_V: np.ndarray
+    S: np.ndarray
+    K_res: np.ndarray
+    V_res: np.ndarray
+    kmin: np.ndarray
+    kmax: np.ndarray
+    sigma: np.ndarray | None = None
+    err: np.ndarray | None = None
+
+    @property
+    def rank(self) -> int:
+        return self.U.shape[1]
+
+
+def select_residuals(err: np.ndarray, n_residual: int) -> np.ndarray:
+    """Exact-residual selection by worst reconstruction.
+
+    [DKV-Z] keeps as exact residual tokens "the rows the low-rank basis
+    reconstructs worst"; [README Innov, "Content-Aware / Rarity-Aware Residual
+    Selection"] names the vanilla criterion arg max ||k - k_hat||_2.  ``err``
+    holds that error for tokens 1..255; the R largest are kept, equal errors
+    going to the lower token.  Returns token positions (1..255), ascending.
+    """
+    n = err.shape[0]
+    R = max(0, min(int(n_residual), n))
+    order = sorted(range(n), key=lambda i: (-float(err[i]), i))[:R]
+    return np.array(sorted(i + 1 for i in order), dtype=np.int64)
+
+
+def compress_block(Kb: np.ndarray, Vb: np.ndarray, rank: int, n_residual: int) -> Block:
+    """Anchor + joint K|V truncated SVD + exact residuals for one block.
+
+    [README Core] items 1-3 and [DKV-Z]: the anchor (a_k, a_v) is the block's
+    first token kept exact; the other 255 tokens are stored as a rank-r joint
+    K|V truncated SVD delta with U in R^{255 x r} and V_K, V_V in R^{r x d};
+    a budget of R exact residual rows is kept beside it.
+
+    Step by step:
+    1. a_k = K[0], a_v = V[0].
+    2. X_i = [K[i] - a_k | V[i] - a_v] for i = 1..255 (delta to the anchor).
+    3. X = U_hat diag(sigma) W^T (LAPACK, fp64); U = U_hat[:, :r] diag(sigma[:r])
+       (S folded into U); V_K = W^T[:r, :d], V_V = W^T[:r, d:].
+    4. err_i = ||(K[i] - a_k) - U_i V_K||_2 and the R worst rows are kept exact.
+    5. kmin, kmax = channel-wise min / max of the 256 exact keys ([README Bench],
+       table "Per-Block Memory Breakdown": "Key Min/Max ... Decode router bounds").
+    """
+    Kb = np.asarray(Kb, dtype=np.float64)
+    Vb = np.asarray(Vb, dtype=np.float64)
+    n, d = Kb.shape
+    if n != BLOCK_SIZE or Vb.shape != Kb.shape:
+        raise ValueError("a block is 256 tokens of K and V with the same head_dim")
+    a_k, a_v = Kb[0].copy(), Vb[0].copy()
+    dK = Kb[1:] - a_k
+    dV = Vb[1:] - a_v
+    X = np.concatenate([dK, dV], axis=1)                      # [255, 2d]
+    U_hat, sigma, Wt = np.linalg.svd(X, full_matrices=False)  # fp64 LAPACK
+    r = max(0, min(int(rank), sigma.shape[0]))
+    U = U_hat[:, :r] * sigma[:r]
+    V_K = Wt[:r, :d].copy()
+    V_V = Wt[:r, d:].copy()
+    err = np.sqrt(((dK - U @ V_K) ** 2).sum(axis=1))
+    S = select_residuals(err, n_residual)
+    return Block(a_k=a_k, a_v=a_v, U=U, V_K=V_K, V_V=V_V, S=S,
+                 K_res=Kb[S].copy(), V_res=Vb[S].copy(),
+                 kmin=Kb.min(axis=0), kmax=Kb.max(axis=0), sigma=sigma, err=err)
+
+
+@dataclasses.dataclass
+class Unit:
+    """Compressed cache of one (layer, sequence, KV head): blocks + window."""
+
+    blocks: list
+    win_K: np.ndarray  # [W, d] exact recency window ([README Core] item 4)
+    win_V: np.ndarray
+
+
+def compress_unit(K: np.ndarray, V: np.ndarray, n_blocks: int, rank: int, n_residual: int) -> Unit:
+    """Split a unit's T = n_blocks*256 + W tokens into compressed blocks and the
+    exact recency window ([DKV-Z]: recent tokens exact, older ones compressed)."""
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    nb = int(n_blocks)
+    blocks = [compress_block(K[b * BLOCK_SIZE:(b + 1) * BLOCK_SIZE], V[b * BLOCK_SIZE:(b + 1) * BLOCK_SIZE],
+                             rank, n_residual) for b in range(nb)]
+    return Unit(blocks=blocks, win_K=K[nb * BLOCK_SIZE:].copy(), win_V=V[nb * BLOCK_SIZE:].copy())
+
+
+def reconstruct_block(blk: Block) -> tuple[np.ndarray, np.ndarray]:
+    """K_hat, V_hat [256, d] of a compressed block: row 0 the anchor, rows in S
+    the stored exact rows, every other row a + U_i [V_K | V_V] ([README Core])."""
+    d = blk.a_k.shape[0]
+    Kh = np.empty((BLOCK_SIZE, d))
+    Vh = np.empty((BLOCK_SIZE, d))
+    Kh[0], Vh[0] = blk.a_k, blk.a_v
+    Kh[1:] = blk.a_k + blk.U @ blk.V_K
+    Vh[1:] = blk.a_v + blk.U @ blk.V_V
+    if blk.S.size:
+        Kh[blk.S] = blk.K_res
+        Vh[blk.S] = blk.V_res
+    return Kh, Vh
+
+
+# ---------------------------------------------------------------------------
+# routing
+# ---------------------------------------------------------------------------
+
+def effective_top_k(top_k: int, n_blocks: int) -> int:
+    """[README Knobs] DKV_TOPK_BLOCKS: blocks routed per decode step; the README's
+    benchmark section ("attend every block (DKV_TOPK_BLOCKS=0)") reads 0 as
+    every block.  K >= NB also attends every block."""
+    if top_k < 0:
+        raise ValueError("top_k must be >= 0")
+    return n_blocks if (top_k == 0 or top_k >= n_blocks) else int(top_k)
+
+
+def router_bounds(q: np.ndarray, kmin: np.ndarray, kmax: np.ndarray) -> np.ndarray:
+    """Per-block upper bound on the group-mean query score.
+
+    q [G, d] are the GQA group's queries (one KV head).  [README Knobs]
+    DKV_CB_GQA_ROUTE routes on the head-averaged query; [README Bench] stores
+    per-block key min/max as the "Decode router bounds".  With
+    qbar = mean_g (c q_g), c = 1/sqrt(d):
+        bound_b = sum_j max(qbar_j * kmax_bj, qbar_j * kmin_bj)
+    which is >= qbar . k for every key k in the block's box.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    d = q.shape[1]
+    qbar = (q / math.sqrt(d)).mean(axis=0)
+    kmin = np.asarray(kmin, dtype=np.float64)
+    kmax = np.asarray(kmax, dtype=np.float64)
+    return np.maximum(qbar[None, :] * kmax, qbar[None, :] * kmin).sum(axis=1)
+
+
+def route(bounds: np.ndarray, top_k: int) -> np.ndarray:
+    """Top-K blocks by (bound descending, block index ascending); the routed
+    indices are returned in ascending order ([DKV-Z]: "routes to the top-K
+    relevant blocks")."""
+    nb = bounds.shape[0]
+    k = effective_top_k(top_k, nb)
+    order = sorted(range(nb), key=lambda b: (-float(bounds[b]), b))[:k]
+    return np.array(sorted(order), dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# decode: plain definition
+# ---------------------------------------------------------------------------
+
+def softmax_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """o_g = softmax(c q_g K^T) V and lse_g = log sum exp(c q_g K^T), c = 1/sqrt(d)."""
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    s = (q / math.sqrt(q.shape[1])) @ K.T                   # [G, n]
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    l = e.sum(axis=1, keepdims=True)
+    return (e @ V) / l, (m + np.log(l))[:, 0]
+
+
+def decode_unit(q: np.ndarray, unit: Unit, top_k: int) -> dict:
+    """Decode attention of one unit, by definition.
+
+    [DKV-Z]: route to the top-K relevant blocks, attend them and the dense
+    recency window.  Token set = for each routed block its anchor, its
+    reconstructed low-rank rows and its exact residual rows; then the W window
+    tokens.  One softmax over that set (the split log-sum-exp merge the pages
+    describe reaches the same value; see ``decode_unit_factored``).
+    Returns o [G, d], lse [G], idx (routed blocks, ascending), bounds [NB].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    d = q.shape[1]
+    nb = len(unit.blocks)
+    if nb:
+        kmin = np.stack([b.kmin for b in unit.blocks])
+        kmax = np.stack([b.kmax for b in unit.blocks])
+        bounds = router_bounds(q, kmin, kmax)
+        idx = route(bounds, top_k)
+    else:
+        bounds = np.zeros(0)
+        idx = np.zeros(0, dtype=np.int64)
+    Ks, Vs = [], []
+    for b in idx:
+        Kh, Vh = reconstruct_block(unit.blocks[b])
+        Ks.append(Kh)
+        Vs.append(Vh)
+    Ks.append(np.asarray(unit.win_K, dtype=np.float64).reshape(-1, d))
+    Vs.append(np.asarray(unit.win_V, dtype=np.float64).reshape(-1, d))
+    Kall = np.concatenate(Ks)
+    Vall = np.concatenate(Vs)
+    if Kall.shape[0] == 0:
+        raise ValueError("nothing to attend: no routed block and an empty window")
+    o, lse = softmax_attention(q, Kall, Vall)
+    return {"o": o, "lse": lse, "idx": idx, "bounds": bounds}
+
+
+# ---------------------------------------------------------------------------
+# decode: factored form (low-rank scoring, low-rank value, split LSE merge)
+# ---------------------------------------------------------------------------
+
+def lse_merge(parts: list) -> tuple[np.ndarray, np.ndarray]:
+    """Flash-style log-sum-exp merge ([DKV-Z]; [README Core] "Flash-Style LSE
+    Combine").  Each part is (m [G], l [G], acc [G, d]) with
+    l = sum exp(s - m) and acc = sum exp(s - m) v over that part's tokens:
+        m* = max_j m_j,  l* = sum_j l_j e^{m_j - m*},
+        o  = sum_j acc_j e^{m_j - m*} / l*,  lse = m* + log l*.
+    """
+    ms = np.stack([p[0] for p in parts])                     # [P, G]
+    mstar = ms.max(axis=0)
+    w = np.exp(ms - mstar[None, :])
+    lstar = sum(wj * p[1] for wj, p in zip(w, parts))
+    acc = sum(wj[:, None] * p[2] for wj, p in zip(w, parts))
+    return acc / lstar[:, None], mstar + np.log(lstar)
+
+
+def _part(s: np.ndarray, V: np.ndarray) -> tuple:
+    m = s.max(axis=1)
+    e = np.exp(s - m[:, None])
+    return m, e.sum(axis=1), e @ V
+
+
+def block_partial(q: np.ndarray, blk: Block) -> tuple:
+    """Partial (m, l, acc) of one routed block without materialising K.
+
+    [README Core] "Low-Rank Space Query Scoring": with q~ = c q,
+      z   = V_K q~                              (r numbers per query)
+      s_0 = q~ . a_k                            (anchor)
+      s_i = q~ . a_k + U_i . z                  (low-rank rows i not in S)
+      s_j = q~ . k_j                            (exact residual rows j in S)
+    and the value side
+      acc = (sum_{low-rank incl. anchor} p) a_v + (sum p_i U_i) V_V + sum_{S} p_j v_j.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    qt = q / math.sqrt(q.shape[1])
+    z = qt @ blk.V_K.T                                        # [G, r]
+    base = qt @ blk.a_k                                       # [G]
+    lowrank = np.ones(BLOCK_SIZE, dtype=bool)
+    lowrank[blk.S] = False
+    lr_rows = np.nonzero(lowrank[1:])[0]                      # indices into U (token - 1)
+    s_lr = base[:, None] + z @ blk.U[lr_rows].T               # [G, n_lr]
+    s_anchor = base[:, None]                                  # [G, 1]
+    s_res = qt @ blk.K_res.T                                  # [G, R]
+    s_all = np.concatenate([s_anchor, s_lr, s_res], axis=1)
+    m = s_all.max(axis=1)
+    p_anchor = np.exp(s_anchor - m[:, None])
+    p_lr = np.exp(s_lr - m[:, None])
+    p_res = np.exp(s_res - m[:, None])
+    pa = p_anchor[:, 0] + p_lr.sum(axis=1)
+    w = p_lr @ blk.U[lr_rows]                                 # [G, r]
+    acc = pa[:, None] * blk.a_v[None, :] + w @ blk.V_V + p_res @ blk.V_res
+    l = pa + p_res.sum(axis=1)
+    return m, l, acc
+
+
+def decode_unit_factored(q: np.ndarray, unit: Unit, top_k: int, window_chunk: int = 256) -> dict:
+    """Same result as ``decode_unit`` through the factored steps: route, one
+    partial per routed block (``block_partial``), exact window partials in
+    chunks, then the split log-sum-exp merge."""
+    q = np.asarray(q, dtype=np.float64)
+    d = q.shape[1]
+    qt = q / math.sqrt(d)
+    nb = len(unit.blocks)
+    if nb:
+        bounds = router_bounds(q, np.stack([b.kmin for b in unit.blocks]), np.stack([b.kmax for b in unit.blocks]))
+        idx = route(bounds, top_k)
+    else:
+        bounds, idx = np.zeros(0), np.zeros(0, dtype=np.int64)
+    parts = [block_partial(q, unit.blocks[b]) for b in idx]
+    W = unit.win_K.shape[0]
+    for t0 in range(0, W, window_chunk):
+        Kc = np.asarray(unit.win_K[t0:t0 + window_chunk], dtype=np.float64)
+        Vc = np.asarray(unit.win_V[t0:t0 + window_chunk], dtype=np.float64)
+        parts.append(_part(qt @ Kc.T, Vc))
+    o, lse = lse_merge(parts)
+    return {"o": o, "lse": lse, "idx": idx, "bounds": bounds}
+
+
+# ---------------------------------------------------------------------------
+# byte accounting
+# ---------------------------------------------------------------------------
+
+def pages_block_bytes(d: int, u_rank: int, R: int, elem_bytes: int = 4,
+                      basis_bytes: int | None = None, meta_bytes: int = 8) -> dict:
+    """Per-block byte accounting in the layout of [README Bench] table
+    "Per-Block Memory Breakdown (B_s = 256 Tokens)": U coefficients [255, r],
+    V_K/V_V bases [2, r, d], anchors [2, d], key min/max [2, d], scalars,
+    exact residuals [R, 2, d]; the dense block is [256, 2, d] x 2.
+    ``basis_bytes`` overrides the V_K/V_V row (the table prints a figure that
+    does not follow from its own shape)."""
+    u = (BLOCK_SIZE - 1) * u_rank * elem_bytes
+    basis = basis_bytes if basis_bytes is not None else 2 * u_rank * d * elem_bytes
+    anchors = 2 * d * elem_bytes
+    minmax = 2 * d * elem_bytes
+    core = u + basis + anchors + minmax + meta_bytes
+    res = R * 2 * d * elem_bytes
+    dense = BLOCK_SIZE * 2 * d * elem_bytes
+    return {"U": u, "basis": basis, "anchors": anchors, "minmax": minmax, "meta": meta_bytes,
+            "core": core, "residual": res, "block": core + res, "dense": dense,
+            "ratio": dense / (core + res)}
+
+
+def residual_row_bytes(d: int, elem_bytes: int = 2) -> int:
+    """One exact residual token = its key and value rows."""
+    return 2 * d * elem_bytes
+
+
+def dense_kv_bytes(context: int, d: int, n_layers: int, n_kv_heads: int, elem_bytes: int = 2) -> int:
+    """Uncompressed K and V of every layer and KV head."""
+    return context * 2 * d * elem_bytes * n_layers * n_kv_heads

@@ -1,0 +1,390 @@
+"""Pins of the fp64 oracle to facts outside itself (CPU only).
+
+Each test checks the oracle against something it does not compute itself:
+a textbook routine it must reduce to (dense softmax attention via scipy), a
+closed form, an invariant, brute force on tiny inputs, or the numbers the
+pages print (tests/golden).  A plausible slip in the oracle (dropped anchor,
+wrong sign of a delta, transposed basis, residual rows not substituted,
+wrong tie order, a missing LSE rescale) fails at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+from oracle import dkv_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+BS = O.BLOCK_SIZE
+
+
+def _kv(rng, n_tok, d, lat=3, outliers=2):
+    """Small structured K/V: mean + low-rank latent + noise + a few outlier rows."""
+    mu = rng.standard_normal((2, d))
+    L = rng.standard_normal((2, n_tok, lat))
+    Wm = rng.standard_normal((2, lat, d)) / math.sqrt(lat)
+    X = mu[:, None, :] + L @ Wm + 0.05 * rng.standard_normal((2, n_tok, d))
+    rows = rng.choice(n_tok, size=outliers, replace=False)
+    X[:, rows, :] *= 8.0
+    return X[0], X[1]
+
+
+def _dense(q, K, V):
+    """Textbook softmax attention via scipy (the routine the method must reduce to)."""
+    s = (q / math.sqrt(q.shape[1])) @ K.T
+    return scipy.special.softmax(s, axis=1) @ V, scipy.special.logsumexp(s, axis=1)
+
+
+# ----------------------------------------------------------------- P1, P2
+
+@pytest.mark.parametrize("d,nb,W", [(16, 3, 40), (8, 2, 0), (32, 1, 7)])
+def test_full_rank_all_routed_equals_dense(d, nb, W):
+    """r = rank(X) = min(255, 2d), R = 0, K = NB: the cache is lossless and the
+    decode is dense softmax attention over the exact K, V."""
+    rng = np.random.default_rng(10 + d)
+    K, V = _kv(rng, nb * BS + W, d)
+    q = rng.standard_normal((3, d))
+    unit = O.compress_unit(K, V, nb, rank=min(255, 2 * d), n_residual=0)
+    for top_k in (0, nb, nb + 5):
+        got = O.decode_unit(q, unit, top_k)
+        o, lse = _dense(q, K, V)
+        np.testing.assert_allclose(got["o"], o, atol=1e-11, rtol=0)
+        np.testing.assert_allclose(got["lse"], lse, atol=1e-11, rtol=0)
+
+
+@pytest.mark.parametrize("rank", [0, 1, 5])
+def test_all_residual_rows_is_exact(rank):
+    """R = 255 keeps every non-anchor row exact: dense attention for any r."""
+    rng = np.random.default_rng(rank)
+    d, nb, W = 16, 2, 33
+    K, V = _kv(rng, nb * BS + W, d)
+    q = rng.standard_normal((2, d))
+    unit = O.compress_unit(K, V, nb, rank=rank, n_residual=255)
+    got = O.decode_unit(q, unit, 0)
+    o, lse = _dense(q, K, V)
+    np.testing.assert_allclose(got["o"], o, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(got["lse"], lse, atol=1e-12, rtol=0)
+    f = O.decode_unit_factored(q, unit, 0)
+    np.testing.assert_allclose(f["o"], o, atol=1e-12, rtol=0)
+
+
+# ----------------------------------------------------------------- P3
+
+def test_split_lse_merge_equals_single_softmax():
+    """Any partition of the token set merged by log-sum-exp = one softmax."""
+    rng = np.random.default_rng(3)
+    G, n, d = 4, 777, 12
+    q = rng.standard_normal((G, d)) * 3.0
+    K = rng.standard_normal((n, d)) * 2.0
+    V = rng.standard_normal((n, d))
+    s = (q / math.sqrt(d)) @ K.T
+    o_ref = scipy.special.softmax(s, axis=1) @ V
+    lse_ref = scipy.special.logsumexp(s, axis=1)
+    for trial in range(5):
+        cuts = np.sort(rng.choice(np.arange(1, n), size=trial + 1, replace=False))
+        parts = []
+        for a, b in zip(np.r_[0, cuts], np.r_[cuts, n]):
+            sp = s[:, a:b]
+            m = sp.max(axis=1)
+            e = np.exp(sp - m[:, None])
+            parts.append((m, e.sum(axis=1), e @ V[a:b]))
+        o, lse = O.lse_merge(parts)
+        np.testing.assert_allclose(o, o_ref, atol=1e-13, rtol=0)
+        np.testing.assert_allclose(lse, lse_ref, atol=1e-12, rtol=0)
+
+
+def test_lse_merge_single_part_and_order_invariance():
+    rng = np.random.default_rng(4)
+    parts = [(rng.standard_normal(2) * 5, rng.random(2) + 0.1, rng.standard_normal((2, 3))) for _ in range(4)]
+    o1, l1 = O.lse_merge(parts)
+    o2, l2 = O.lse_merge(parts[::-1])
+    np.testing.assert_allclose(o1, o2, atol=1e-14)
+    np.testing.assert_allclose(l1, l2, atol=1e-14)
+    m, l, acc = parts[0]
+    o, lse = O.lse_merge([parts[0]])
+    np.testing.assert_allclose(o, acc / l[:, None], atol=1e-15)
+    np.testing.assert_allclose(lse, m + np.log(l), atol=1e-15)
+
+
+# ----------------------------------------------------------------- P4
+
+@pytest.mark.parametrize("rank,R", [(3, 10), (8, 0), (0, 4), (12, 100)])
+def test_factored_equals_materialised(rank, R):
+    """Low-rank scoring q.a_k + U_i.z and value (sum p) a_v + (sum p U) V_V equal
+    attention over the reconstructed tokens, per block and per unit."""
+    rng = np.random.default_rng(40 + rank + R)
+    d, nb, W = 16, 4, 70
+    K, V = _kv(rng, nb * BS + W, d)
+    q = rng.standard_normal((6, d)) * 2
+    unit = O.compress_unit(K, V, nb, rank, R)
+    for blk in unit.blocks:
+        m, l, acc = O.block_partial(q, blk)
+        Kh, Vh = O.reconstruct_block(blk)
+        o_ref, lse_ref = _dense(q, Kh, Vh)
+        np.testing.assert_allclose(acc / l[:, None], o_ref, atol=1e-12, rtol=0)
+        np.testing.assert_allclose(m + np.log(l), lse_ref, atol=1e-12, rtol=0)
+    for top_k in (1, 2, 0):
+        a = O.decode_unit(q, unit, top_k)
+        b = O.decode_unit_factored(q, unit, top_k, window_chunk=32)
+        np.testing.assert_array_equal(a["idx"], b["idx"])
+        np.testing.assert_allclose(a["o"], b["o"], atol=1e-12, rtol=0)
+        np.testing.assert_allclose(a["lse"], b["lse"], atol=1e-12, rtol=0)
+
+
+# ----------------------------------------------------------------- P5
+
+def test_router_bound_is_an_upper_bound_on_every_key():
+    rng = np.random.default_rng(5)
+    d = 24
+    for _ in range(20):
+        keys = rng.standard_normal((BS, d)) * rng.uniform(0.1, 5)
+        q = rng.standard_normal((5, d))
+        b = O.router_bounds(q, keys.min(0)[None], keys.max(0)[None])[0]
+        qbar = (q / math.sqrt(d)).mean(0)
+        assert b >= (keys @ qbar).max() - 1e-12
+        # the bound is attained when the block's box corners are keys
+        corner = np.where(qbar >= 0, keys.max(0), keys.min(0))
+        np.testing.assert_allclose(b, corner @ qbar, atol=1e-12)
+
+
+def test_route_brute_force_and_ties():
+    rng = np.random.default_rng(6)
+    for nb in (1, 2, 5, 7):
+        for k in range(0, nb + 2):
+            bounds = rng.integers(0, 4, size=nb).astype(float)  # many ties
+            got = O.route(bounds, k)
+            kk = nb if (k == 0 or k >= nb) else k
+            # brute force: best subset by sum of bounds, ties broken toward lower indices
+            best = None
+            for sub in itertools.combinations(range(nb), kk):
+                key = (-sum(bounds[list(sub)]), list(sub))
+                if best is None or key < best[0]:
+                    best = (key, sub)
+            assert list(got) == sorted(best[1])
+    # explicit tie order: equal bounds keep the lower block index
+    assert list(O.route(np.array([1.0, 2.0, 2.0, 2.0]), 2)) == [1, 2]
+    assert list(O.route(np.array([5.0, 1.0, 5.0]), 1)) == [0]
+
+
+def test_all_routed_makes_routing_irrelevant():
+    rng = np.random.default_rng(7)
+    d, nb = 16, 5
+    K, V = _kv(rng, nb * BS + 20, d)
+    unit = O.compress_unit(K, V, nb, 4, 6)
+    q = rng.standard_normal((2, d))
+    a = O.decode_unit(q, unit, 0)
+    # permute the blocks: attending all of them gives the same answer
+    perm = O.Unit(blocks=unit.blocks[::-1], win_K=unit.win_K, win_V=unit.win_V)
+    b = O.decode_unit(q, perm, nb)
+    np.testing.assert_allclose(a["o"], b["o"], atol=1e-13)
+    assert list(a["idx"]) == list(range(nb))
+
+
+def test_routing_picks_blocks_with_the_largest_bound():
+    """A block whose keys align with the query must be routed."""
+    rng = np.random.default_rng(8)
+    d, nb = 16, 6
+    K, V = _kv(rng, nb * BS, d)
+    q = rng.standard_normal((3, d))
+    qbar = q.mean(0)
+    K[3 * BS + 17] = 40 * qbar / np.linalg.norm(qbar)  # one very aligned key in block 3
+    unit = O.compress_unit(K, V, nb, 4, 4)
+    assert 3 in O.decode_unit(q, unit, 1)["idx"]
+
+
+# ----------------------------------------------------------------- P6
+
+def test_rank_zero_closed_form():
+    """r = 0: every low-rank row is the anchor, so a block's partial is
+    (n_lr e^{s0}) a_v + sum_S e^{s_j} v_j over l = n_lr e^{s0} + sum_S e^{s_j}."""
+    rng = np.random.default_rng(9)
+    d = 16
+    K, V = _kv(rng, BS, d)
+    blk = O.compress_block(K, V, rank=0, n_residual=7)
+    q = rng.standard_normal((2, d))
+    qt = q / math.sqrt(d)
+    s0 = qt @ K[0]
+    sres = qt @ K[blk.S].T
+    n_lr = BS - len(blk.S)
+    num = (n_lr * np.exp(s0))[:, None] * V[0][None] + np.exp(sres) @ V[blk.S]
+    den = n_lr * np.exp(s0) + np.exp(sres).sum(1)
+    m, l, acc = O.block_partial(q, blk)
+    np.testing.assert_allclose(acc / l[:, None], num / den[:, None], atol=1e-12)
+    np.testing.assert_allclose(m + np.log(l), np.log(den), atol=1e-12)
+
+
+# ----------------------------------------------------------------- P7, P8 (the pages' printed numbers)
+
+def test_per_block_bytes_match_the_pages_table():
+    g = json.load(open(os.path.join(GOLDEN, "per_block_bytes.json")))
+    rows = g["rows"]
+    for R in (128, 64):
+        acc = O.pages_block_bytes(g["head_dim"], g["u_rank"], R, elem_bytes=g["elem_bytes"],
+                                  basis_bytes=g["basis_bytes_as_printed"])
+        assert acc["U"] == rows["U"]
+        assert acc["anchors"] == rows["anchors"]
+        assert acc["minmax"] == rows["minmax"]
+        assert acc["core"] == rows["core"]
+        assert acc["residual"] == rows[f"residual_R{R}"]
+        assert acc["block"] == rows[f"block_R{R}"]
+        assert acc["dense"] == rows["dense"]
+        assert round(acc["ratio"], 2) == g["ratios"][f"R{R}"]
+    # the printed basis row is not its own shape at 4-byte elements (a garble, passed through)
+    assert O.pages_block_bytes(128, 16, 0)["basis"] == rows["basis"] // 2
+
+
+def test_residual_sweep_store_sizes_match_fp16_rows():
+    """The store grows by one fp16 K+V row per residual slot per block, and the
+    3.80x ratio is dense fp16 KV at 16k over the R=8 store."""
+    g = json.load(open(os.path.join(GOLDEN, "residual_sweep_16k.json")))
+    R, store = np.array(g["R"], float), np.array(g["store_gb"]) * 1e9
+    slope = np.polyfit(R, store, 1)[0]
+    per_row = O.residual_row_bytes(g["head_dim"]) * g["n_blocks"] * g["n_layers"] * g["n_kv_heads"]
+    assert g["n_blocks"] == (g["context"] - 512) // BS
+    assert abs(slope / per_row - 1) < 0.01
+    dense = O.dense_kv_bytes(g["context"], g["head_dim"], g["n_layers"], g["n_kv_heads"])
+    for s, ratio in zip(store, g["ratio_vs_dense"]):
+        assert abs(dense / s - ratio) / ratio < 0.02
+
+
+# ----------------------------------------------------------------- P9 and compression invariants
+
+@pytest.mark.parametrize("rank", [1, 4, 9, 20])
+def test_eckart_young(rank):
+    """Truncation error = sum of the discarded squared singular values, taken
+    from an independent symmetric eigen-solve of X^T X; the joint basis rows
+    are orthonormal; no random rank-r factorisation does better."""
+    rng = np.random.default_rng(90 + rank)
+    d = 16
+    K, V = _kv(rng, BS, d, lat=5)
+    blk = O.compress_block(K, V, rank, 0)
+    X = np.concatenate([K[1:] - K[0], V[1:] - V[0]], axis=1)
+    Wr = np.concatenate([blk.V_K, blk.V_V], axis=1)
+    err = ((X - blk.U @ Wr) ** 2).sum()
+    ev = np.sort(np.linalg.eigvalsh(X.T @ X))[::-1]
+    np.testing.assert_allclose(err, ev[rank:].sum(), rtol=1e-9, atol=1e-9)
+    np.testing.assert_allclose(Wr @ Wr.T, np.eye(rank), atol=1e-12)
+    for _ in range(5):
+        Q, _ = np.linalg.qr(rng.standard_normal((2 * d, rank)))
+        assert ((X - (X @ Q) @ Q.T) ** 2).sum() >= err - 1e-9
+
+
+def test_anchor_is_first_token_and_deltas_are_to_it():
+    rng = np.random.default_rng(11)
+    d = 8
+    K, V = _kv(rng, BS, d)
+    blk = O.compress_block(K, V, rank=2 * d, n_residual=0)
+    np.testing.assert_array_equal(blk.a_k, K[0])
+    np.testing.assert_array_equal(blk.a_v, V[0])
+    Kh, Vh = O.reconstruct_block(blk)
+    np.testing.assert_allclose(Kh, K, atol=1e-11)
+    np.testing.assert_allclose(Vh, V, atol=1e-11)
+    # a constant shift of the whole block only moves the anchor: the deltas are unchanged
+    b1 = O.compress_block(K, V, rank=3, n_residual=0)
+    b2 = O.compress_block(K + 3.0, V - 2.0, rank=3, n_residual=0)
+    np.testing.assert_allclose(b2.a_k, K[0] + 3.0)
+    np.testing.assert_allclose(b2.U @ b2.V_K, b1.U @ b1.V_K, atol=1e-9)
+    np.testing.assert_allclose(b2.U @ b2.V_V, b1.U @ b1.V_V, atol=1e-9)
+
+
+def test_residuals_pick_the_worst_reconstructed_rows():
+    """A row far off the low-rank structure is kept exact; the kept rows are
+    exactly the R largest key errors, ties to the lower position."""
+    rng = np.random.default_rng(12)
+    d = 16
+    K, V = _kv(rng, BS, d, lat=2, outliers=0)
+    K[77] += rng.standard_normal(d) * 3.0   # off-structure key
+    K[200] += rng.standard_normal(d) * 2.0
+    blk = O.compress_block(K, V, rank=4, n_residual=2)   # rank 4 spans the K and V latents
+    assert list(blk.S) == [77, 200]
+    np.testing.assert_array_equal(blk.K_res, K[[77, 200]])
+    np.testing.assert_array_equal(blk.V_res, V[[77, 200]])
+    # brute-force the selection from the reconstruction
+    Kh_lr = K[0] + blk.U @ blk.V_K
+    err = np.linalg.norm(K[1:] - Kh_lr, axis=1)
+    for R in (0, 1, 5, 30, 255, 300):
+        S = O.select_residuals(err, R)
+        assert len(S) == min(R, 255)
+        if 0 < len(S) < 255:
+            kept = err[S - 1]
+            dropped = np.delete(err, S - 1)
+            assert kept.min() >= dropped.max()
+    # ties go to the lower token
+    assert list(O.select_residuals(np.array([1.0, 3.0, 3.0, 3.0, 0.5]), 2)) == [2, 3]
+
+
+def test_router_minmax_are_channel_extremes():
+    rng = np.random.default_rng(13)
+    K, V = _kv(rng, BS, 8)
+    blk = O.compress_block(K, V, 2, 3)
+    np.testing.assert_array_equal(blk.kmin, K.min(0))
+    np.testing.assert_array_equal(blk.kmax, K.max(0))
+
+
+# ----------------------------------------------------------------- P10: brute force, scalar loops
+
+def test_tiny_brute_force_loops():
+    """Scalar Python loops over tokens and channels agree with the vectorised oracle."""
+    rng = np.random.default_rng(14)
+    d, nb, W, G, r, R, top_k = 4, 3, 9, 2, 2, 5, 2
+    K, V = _kv(rng, nb * BS + W, d, lat=2, outliers=1)
+    q = rng.standard_normal((G, d))
+    unit = O.compress_unit(K, V, nb, r, R)
+    c = 1.0 / math.sqrt(d)
+    # routing by loops
+    bounds = []
+    for blk in unit.blocks:
+        tot = 0.0
+        for j in range(d):
+            qb = sum(c * q[g][j] for g in range(G)) / G
+            tot += max(qb * blk.kmax[j], qb * blk.kmin[j])
+        bounds.append(tot)
+    order = sorted(range(nb), key=lambda b: (-bounds[b], b))[:top_k]
+    routed = sorted(order)
+    # token list by loops
+    toks = []
+    for b in routed:
+        blk = unit.blocks[b]
+        S = set(int(x) for x in blk.S)
+        for i in range(BS):
+            if i == 0:
+                k, v = list(blk.a_k), list(blk.a_v)
+            elif i in S:
+                j = list(blk.S).index(i)
+                k, v = list(blk.K_res[j]), list(blk.V_res[j])
+            else:
+                k = [blk.a_k[t] + sum(blk.U[i - 1][a] * blk.V_K[a][t] for a in range(r)) for t in range(d)]
+                v = [blk.a_v[t] + sum(blk.U[i - 1][a] * blk.V_V[a][t] for a in range(r)) for t in range(d)]
+            toks.append((k, v))
+    for t in range(W):
+        toks.append((list(unit.win_K[t]), list(unit.win_V[t])))
+    got = O.decode_unit(q, unit, top_k)
+    assert list(got["idx"]) == routed
+    for g in range(G):
+        s = [c * sum(q[g][t] * k[t] for t in range(d)) for k, _ in toks]
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        den = sum(e)
+        o = [sum(e[n] * toks[n][1][t] for n in range(len(toks))) / den for t in range(d)]
+        np.testing.assert_allclose(got["o"][g], o, atol=1e-12)
+        assert abs(got["lse"][g] - (m + math.log(den))) < 1e-12
+
+
+def test_window_only_and_empty_inputs():
+    rng = np.random.default_rng(15)
+    d = 8
+    K, V = _kv(rng, 50, d)
+    q = rng.standard_normal((1, d))
+    unit = O.compress_unit(K, V, 0, 4, 4)
+    got = O.decode_unit(q, unit, 3)
+    o, lse = _dense(q, K, V)
+    np.testing.assert_allclose(got["o"], o, atol=1e-13)
+    assert got["idx"].size == 0
+    with pytest.raises(ValueError):
+        O.decode_unit(q, O.compress_unit(K[:0], V[:0], 0, 4, 4), 1)
+    with pytest.raises(ValueError):
+        O.route(np.zeros(3), -1)
