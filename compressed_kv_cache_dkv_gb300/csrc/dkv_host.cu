@@ -1,0 +1,221 @@
+// Host side of libdkv: descriptor validation, layout, argument checks and the
+// extern "C" entry points declared in include/dkv.h.  No kernel code here.
+#include <cstring>
+
+#include "dkv_internal.cuh"
+
+namespace dkv {
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool make_layout(const dkv_desc* d, Layout* L) {
+  if (!d || !L || d->total_bytes == 0) return false;
+  L->d = d->head_dim;
+  L->r = d->rank;
+  L->r8 = d->rank_pad;
+  L->R = d->n_residual;
+  L->R8 = d->res_pad;
+  L->W = d->window;
+  L->W16 = d->window_pad;
+  L->NB = d->n_blocks;
+  L->units = d->n_units;
+  L->off_mask = d->blk_off_mask;
+  L->off_vk = d->blk_off_vk;
+  L->off_u = d->blk_off_u;
+  L->off_res = d->blk_off_res;
+  L->off_vv = d->blk_off_vv;
+  L->block_bytes = d->block_bytes;
+  L->off_router = d->off_router;
+  L->off_blocks = d->off_blocks;
+  L->off_cold = d->off_cold;
+  L->off_window = d->off_window;
+  L->block_stride = d->block_stride;
+  L->unit_stride = d->unit_stride;
+  L->total = d->total_bytes;
+  return true;
+}
+
+// Recompute the layout from the caller-set fields and check that the filled
+// fields agree (a descriptor edited after dkv_layout() is rejected).
+static int check_desc(const dkv_desc* d, Layout* L) {
+  if (!d) return DKV_ERR_ARG;
+  dkv_desc c;
+  std::memcpy(&c, d, sizeof(c));
+  int st = dkv_layout(&c);
+  if (st != DKV_OK) return st;
+  if (std::memcmp(&c, d, sizeof(c)) != 0) return DKV_ERR_SHAPE;
+  make_layout(&c, L);
+  return DKV_OK;
+}
+
+}  // namespace dkv
+
+using namespace dkv;
+
+extern "C" {
+
+int dkv_version(void) { return DKV_VERSION; }
+
+const char* dkv_status_string(int status) {
+  switch (status) {
+    case DKV_OK: return "ok";
+    case DKV_ERR_ARG: return "invalid argument";
+    case DKV_ERR_SHAPE: return "inconsistent shape";
+    case DKV_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case DKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case DKV_ERR_CUDA: return "CUDA runtime error";
+    case DKV_ERR_TIMEOUT: return "device wait timed out";
+    case DKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case DKV_ERR_DEVICE: return "device error word set";
+    default: return "unknown status";
+  }
+}
+
+int dkv_layout(dkv_desc* d) {
+  if (!d) return DKV_ERR_ARG;
+  if (d->batch < 1 || d->n_q_heads < 1 || d->n_kv_heads < 1 || d->head_dim < 1 || d->n_blocks < 0 ||
+      d->window < 0 || d->rank < 0 || d->n_residual < 0 || d->block_size < 1)
+    return DKV_ERR_ARG;
+  if (d->n_q_heads % d->n_kv_heads != 0) return DKV_ERR_SHAPE;
+  if (d->n_blocks == 0 && d->window == 0) return DKV_ERR_SHAPE;  // nothing to attend
+  if (d->block_size != DKV_BLOCK_SIZE) return DKV_ERR_UNSUPPORTED;
+  if (d->head_dim != 64 && d->head_dim != 128) return DKV_ERR_UNSUPPORTED;
+  if (d->n_q_heads / d->n_kv_heads > 8) return DKV_ERR_UNSUPPORTED;
+  if (d->rank > 128 || d->n_residual > 255) return DKV_ERR_UNSUPPORTED;
+  if (d->n_blocks > 16384) return DKV_ERR_UNSUPPORTED;  // router keeps all block scores in shared memory
+  const uint64_t dd = (uint64_t)d->head_dim;
+  const int r8 = (d->rank + 7) / 8 * 8;
+  const int R8 = (d->n_residual + 7) / 8 * 8;
+  const int W16 = (d->window + 15) / 16 * 16;
+  d->rank_pad = r8;
+  d->res_pad = R8;
+  d->window_pad = W16;
+  d->n_units = d->batch * d->n_kv_heads;
+  d->blk_off_mask = 4 * dd;
+  d->blk_off_vk = 4 * dd + 32;
+  d->blk_off_u = d->blk_off_vk + 2ull * r8 * dd;
+  d->blk_off_res = d->blk_off_u + 2ull * 256 * r8;
+  d->blk_off_vv = d->blk_off_res + 4ull * R8 * dd;
+  d->block_bytes = d->blk_off_vv + 2ull * r8 * dd;
+  d->block_stride = round_up(d->block_bytes, 128);
+  const uint64_t nb = (uint64_t)d->n_blocks;
+  d->off_router = 0;
+  d->off_blocks = round_up(nb * 4 * dd, 128);
+  d->off_cold = d->off_blocks + nb * d->block_stride;
+  d->off_window = d->off_cold + round_up(nb * (uint64_t)R8 * 2, 128);
+  d->unit_stride = round_up(d->off_window + (uint64_t)W16 * 4 * dd, 128);
+  d->total_bytes = d->unit_stride * (uint64_t)d->n_units;
+  return DKV_OK;
+}
+
+size_t dkv_layout_bytes(dkv_desc* d) { return dkv_layout(d) == DKV_OK ? (size_t)d->total_bytes : 0; }
+
+size_t dkv_compress_workspace_bytes(const dkv_desc* d) {
+  Layout L;
+  if (check_desc(d, &L) != DKV_OK) return 0;
+  return compress_ws_bytes(L);
+}
+
+int dkv_compress_layout(const dkv_desc* d, const void* K, const void* V, void* cache, void* workspace,
+                        size_t ws_bytes, void* stream) {
+  Layout L;
+  int st = check_desc(d, &L);
+  if (st != DKV_OK) return st;
+  if (!K || !V || !cache || !workspace) return DKV_ERR_ARG;
+  if (!aligned16(K) || !aligned16(V) || !aligned16(cache) || !aligned16(workspace)) return DKV_ERR_ALIGN;
+  if (ws_bytes < compress_ws_bytes(L)) return DKV_ERR_WORKSPACE;
+  const int p_cap = L.d == 128 ? 64 : 128;
+  if (L.r > p_cap) return DKV_ERR_UNSUPPORTED;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = launch_compress(L, static_cast<const __half*>(K), static_cast<const __half*>(V),
+                                  static_cast<uint8_t*>(cache), ws, reinterpret_cast<uint32_t*>(ws),
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
+}
+
+int dkv_import_factors(const dkv_desc* d, const dkv_factors* f, void* cache, void* workspace, void* stream) {
+  Layout L;
+  int st = check_desc(d, &L);
+  if (st != DKV_OK) return st;
+  if (!f || !cache || !workspace) return DKV_ERR_ARG;
+  if (!aligned16(cache) || !aligned16(workspace)) return DKV_ERR_ALIGN;
+  if (L.NB > 0) {
+    if (!f->a_k || !f->a_v || !f->kmin || !f->kmax) return DKV_ERR_ARG;
+    if (L.r > 0 && (!f->U || !f->V_K || !f->V_V)) return DKV_ERR_ARG;
+    if (L.R > 0 && (!f->res_pos || !f->K_res || !f->V_res)) return DKV_ERR_ARG;
+  }
+  if (L.W > 0 && (!f->win_K || !f->win_V)) return DKV_ERR_ARG;
+  cudaError_t e = launch_pack(L, *f, static_cast<uint8_t*>(cache), static_cast<uint32_t*>(workspace),
+                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
+}
+
+size_t dkv_decode_workspace_bytes(const dkv_desc* d, int32_t top_k) {
+  Layout L;
+  if (top_k < 0 || check_desc(d, &L) != DKV_OK) return 0;
+  return plan_decode(L, d->n_q_heads, d->n_kv_heads, top_k).ws_bytes;
+}
+
+int dkv_decode_attend(const dkv_desc* d, const void* q, const void* cache, int32_t top_k, float* out, float* lse,
+                      int32_t* routed, void* workspace, size_t ws_bytes, void* stream) {
+  Layout L;
+  int st = check_desc(d, &L);
+  if (st != DKV_OK) return st;
+  if (top_k < 0) return DKV_ERR_ARG;
+  if (!q || !cache || !out || !workspace) return DKV_ERR_ARG;
+  if (!aligned16(q) || !aligned16(cache) || !aligned16(out) || !aligned16(workspace) || (lse && !aligned16(lse)) ||
+      (routed && !aligned16(routed)))
+    return DKV_ERR_ALIGN;
+  DecodePlan P = plan_decode(L, d->n_q_heads, d->n_kv_heads, top_k);
+  if (ws_bytes < P.ws_bytes) return DKV_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  int32_t* ridx = reinterpret_cast<int32_t*>(ws + P.off_routed);
+  float* parts = reinterpret_cast<float*>(ws + P.off_partials);
+  const __half* qh = static_cast<const __half*>(q);
+  const uint8_t* c = static_cast<const uint8_t*>(cache);
+  cudaError_t e = cudaSuccess;
+  if (P.K_eff > 0) e = launch_route(L, P, d->n_q_heads, d->n_kv_heads, qh, c, ridx, routed, s);
+  if (e == cudaSuccess) e = launch_attend(L, P, d->n_q_heads, d->n_kv_heads, qh, c, ridx, parts, err, s);
+  if (e == cudaSuccess) e = launch_combine(L, P, d->batch, d->n_q_heads, d->n_kv_heads, parts, out, lse, s);
+  return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
+}
+
+size_t dkv_dense_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t T) {
+  if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || T < 1 || n_q_heads % n_kv_heads) return 0;
+  if ((head_dim != 64 && head_dim != 128) || n_q_heads / n_kv_heads > 8) return 0;
+  return dense_ws_bytes(batch, n_q_heads, n_kv_heads, head_dim, T);
+}
+
+int dkv_dense_decode(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t T,
+                     const void* q, const void* K, const void* V, float* out, float* lse, void* workspace,
+                     size_t ws_bytes, void* stream) {
+  if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || T < 1) return DKV_ERR_ARG;
+  if (n_q_heads % n_kv_heads) return DKV_ERR_SHAPE;
+  if ((head_dim != 64 && head_dim != 128) || n_q_heads / n_kv_heads > 8) return DKV_ERR_UNSUPPORTED;
+  if (!q || !K || !V || !out || !workspace) return DKV_ERR_ARG;
+  if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) || !aligned16(workspace) ||
+      (lse && !aligned16(lse)))
+    return DKV_ERR_ALIGN;
+  if (ws_bytes < dense_ws_bytes(batch, n_q_heads, n_kv_heads, head_dim, T)) return DKV_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = launch_dense(batch, n_q_heads, n_kv_heads, head_dim, T, static_cast<const __half*>(q),
+                               static_cast<const __half*>(K), static_cast<const __half*>(V), out, lse, ws,
+                               reinterpret_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
+}
+
+int dkv_get_error(void* workspace, void* stream, uint32_t* word) {
+  if (!workspace || !word) return DKV_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t w = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DKV_ERR_CUDA;
+  if (cudaMemcpy(&w, workspace, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return DKV_ERR_CUDA;
+  if (w && cudaMemset(workspace, 0, sizeof(uint32_t) * 2) != cudaSuccess) return DKV_ERR_CUDA;
+  *word = w;
+  if (w & DKV_DEVERR_TIMEOUT) return DKV_ERR_TIMEOUT;
+  return w ? DKV_ERR_DEVICE : DKV_OK;
+}
+
+}  // extern "C"

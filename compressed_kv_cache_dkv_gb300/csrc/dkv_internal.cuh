@@ -1,0 +1,245 @@
+// Internal header of libdkv: packed-layout address math, PTX wrappers and
+// the launcher prototypes shared by the .cu files of the library.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dkv.h"
+
+namespace dkv {
+
+// ---------------------------------------------------------------------------
+// Packed layout of one block record (all sections 16-byte aligned):
+//
+//   [0, 4d)            a_k[d], a_v[d]                       fp16, plain
+//   [4d, 4d+32)        residual mask, 256 bits (bit i = token i kept exact)
+//   [off_vk, off_u)    V_K  [r8][d]   "B^T layout"  (B operand of z^T = q^T V_K^T)
+//   [off_u, off_res)   U    [256][r8] "A layout"    (row 0 = anchor, all zero)
+//   [off_res, off_vv)  residual groups of 16 tokens (last group may hold 8):
+//                      K_res tile in "A layout" then V_res^T tile in "A layout"
+//   [off_vv, bytes)    V_V^T [d][r8]  "A layout"    (A operand of o = V_V^T w)
+//
+// The router section of a unit is [NB][2][d] fp16 (kmin row, kmax row); the
+// cold section is [NB][R8] uint16 residual positions; the window is W16
+// tokens in 16-token groups laid out like the residual groups.
+//
+// "A layout" of an M x K fp16 matrix (M, K multiples of 8): 16-row m-tiles,
+// inside each m-tile 16-column k-tiles, inside each (m-tile, k-tile) the 8x8
+// sub-blocks of an mma.m16n8k16 A fragment, interleaved per lane:
+//   lane l holds, for each existing sub-block in the order a0 (rows 0-7,
+//   cols 0-7), a1 (rows 8-15, cols 0-7), a2 (rows 0-7, cols 8-15), a3 (rows
+//   8-15, cols 8-15), the two halves at (row l/4, cols 2(l%4), 2(l%4)+1).
+// A lane therefore reads its whole fragment with one 16-byte (full tile),
+// 8-byte (half tile) or 4-byte load.  "B^T layout" of an N x K matrix
+// (the transpose of an mma B operand): 8-row n-tiles, 32-column k-pairs,
+// lane l holds b0,b1 of k-tile 2p then b0,b1 of k-tile 2p+1 (16 bytes).
+// ---------------------------------------------------------------------------
+
+struct Layout {
+  int d, r, r8, R, R8, W, W16, NB, units;
+  uint64_t off_mask, off_vk, off_u, off_res, off_vv, block_bytes;
+  uint64_t off_router, off_blocks, off_cold, off_window, block_stride, unit_stride, total;
+};
+
+__host__ __device__ inline uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+// byte offset of element (row, col) inside an "A layout" matrix of rows x cols
+__host__ __device__ inline uint32_t a_layout_off(int rows, int cols, int row, int col) {
+  int mt = row >> 4, kt = col >> 4;
+  int rows_in = rows - (mt << 4); rows_in = rows_in > 16 ? 16 : rows_in;
+  int cols_in = cols - (kt << 4); cols_in = cols_in > 16 ? 16 : cols_in;
+  int nr = rows_in >> 3, nc = cols_in >> 3;
+  int nsb = nr * nc;
+  int rr = (row & 15) >> 3, cc = (col & 15) >> 3;
+  int sbi = cc * nr + rr;
+  int lane = ((row & 7) << 2) | ((col & 7) >> 1);
+  uint32_t base = (uint32_t)mt * 16u * (uint32_t)cols * 2u + (uint32_t)kt * 16u * (uint32_t)rows_in * 2u;
+  return base + (uint32_t)lane * (uint32_t)nsb * 4u + (uint32_t)sbi * 4u + (uint32_t)(col & 1) * 2u;
+}
+
+// byte offset of element (row=n, col=k) inside a "B^T layout" matrix of rows x cols (cols % 32 == 0)
+__host__ __device__ inline uint32_t bt_layout_off(int rows, int cols, int row, int col) {
+  (void)rows;
+  int nt = row >> 3, kp = col >> 5;
+  int lane = ((row & 7) << 2) | ((col & 7) >> 1);
+  int sb = (col & 31) >> 3;
+  return (uint32_t)nt * 8u * (uint32_t)cols * 2u + (uint32_t)kp * 512u + (uint32_t)lane * 16u +
+         (uint32_t)sb * 4u + (uint32_t)(col & 1) * 2u;
+}
+
+// offset of token t's K element / V element inside a run of 16-token exact groups
+// (residual store or window); n_tok = number of stored tokens (multiple of 8)
+__host__ __device__ inline uint32_t exact_k_off(int n_tok, int d, int t, int j) {
+  int g = t >> 4;
+  int in_g = n_tok - (g << 4); in_g = in_g > 16 ? 16 : in_g;
+  uint32_t gbase = (uint32_t)g * 64u * (uint32_t)d;
+  return gbase + a_layout_off(in_g, d, t & 15, j);
+}
+__host__ __device__ inline uint32_t exact_v_off(int n_tok, int d, int t, int j) {
+  int g = t >> 4;
+  int in_g = n_tok - (g << 4); in_g = in_g > 16 ? 16 : in_g;
+  uint32_t gbase = (uint32_t)g * 64u * (uint32_t)d + (uint32_t)in_g * (uint32_t)d * 2u;
+  return gbase + a_layout_off(d, in_g, j, t & 15);
+}
+
+bool make_layout(const dkv_desc* d, Layout* L);  // from a desc filled by dkv_layout()
+
+// ---------------------------------------------------------------------------
+// Workspace header (first 256 bytes of every workspace)
+// ---------------------------------------------------------------------------
+struct WsHeader {
+  uint32_t error_word;
+  uint32_t error_detail;
+  uint32_t reserved[62];
+};
+constexpr size_t kWsHeader = 256;
+
+__device__ inline void raise_error(uint32_t* err, uint32_t bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers (sm_90+ forms, used on sm_103a)
+// ---------------------------------------------------------------------------
+__device__ inline uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ inline void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ inline void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ inline void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ inline void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ inline void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ inline bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: gives up after `limit` polls (each try_wait itself suspends for
+// a hardware-defined time slice), raises DKV_DEVERR_TIMEOUT and returns false.
+constexpr uint32_t kWaitLimit = 1u << 22;
+__device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  raise_error(err, DKV_DEVERR_TIMEOUT);
+  return false;
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completion counted on `bar`
+__device__ inline void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ inline uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ inline void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ inline void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ inline void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// D += A(16x16, row) * B(16x8, col), fp16 inputs, fp32 accumulate
+__device__ inline void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// D += A(16x8, row) * B(8x8, col)
+__device__ inline void mma1688(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+// transpose an 8x8 b16 matrix held one 32-bit pair per lane
+__device__ inline uint32_t movtrans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ inline uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// split (x, y) into fp16 hi + fp16 lo pairs so that hi + lo carries ~22 bits
+__device__ inline void split_half2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  __half2 h = __floats2half2_rn(x, y);
+  float2 hf = __half22float2(h);
+  __half2 l = __floats2half2_rn(x - hf.x, y - hf.y);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+  lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+__device__ inline uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ inline uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ inline uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// launchers (host functions defined in the kernel .cu files)
+// ---------------------------------------------------------------------------
+cudaError_t launch_pack(const Layout& L, const dkv_factors& f, uint8_t* cache, uint32_t* err, cudaStream_t s);
+cudaError_t launch_compress(const Layout& L, const __half* K, const __half* V, uint8_t* cache, uint8_t* ws,
+                            uint32_t* err, cudaStream_t s);
+size_t compress_ws_bytes(const Layout& L);
+
+struct DecodePlan {
+  int K_eff, n_wchunks, wchunk_tokens, n_items;
+  size_t off_routed, off_partials, ws_bytes;
+};
+DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k);
+cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
+                         const uint8_t* cache, int32_t* routed, int32_t* routed_out, cudaStream_t s);
+cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
+                          const uint8_t* cache, const int32_t* routed, float* partials, uint32_t* err,
+                          cudaStream_t s);
+cudaError_t launch_combine(const Layout& L, const DecodePlan& P, int batch, int n_q_heads, int n_kv_heads,
+                           const float* partials, float* out, float* lse, cudaStream_t s);
+
+size_t dense_ws_bytes(int batch, int n_q_heads, int n_kv_heads, int d, int T);
+cudaError_t launch_dense(int batch, int n_q_heads, int n_kv_heads, int d, int T, const __half* q, const __half* K,
+                         const __half* V, float* out, float* lse, uint8_t* ws, uint32_t* err, cudaStream_t s);
+
+}  // namespace dkv

@@ -153,7 +153,7 @@ def unit_kv(w: Workload, layer: int, b: int, h: int) -> tuple[np.ndarray, np.nda
 
 def queries(w: Workload, layer: int) -> np.ndarray:
     """Decode queries q ~ N(0, 1), fp16 [batch, n_q_heads, head_dim]."""
-    rng = _unit_rng(w.seed, layer, -1, -1, 2)
+    rng = _unit_rng(w.seed, layer, 0xFFFF, 0xFFFF, 2)
     return rng.standard_normal((w.batch, w.n_q_heads, w.head_dim), dtype=np.float32).astype(np.float16)
 
 

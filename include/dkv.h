@@ -1,0 +1,215 @@
+/*
+ * dkv.h -- C ABI of libdkv: DKV decode-time attention over an anchor +
+ * low-rank differential KV cache, on one NVIDIA GB300 (sm_103a).
+ *
+ * Method (cited by page title and section):
+ *   [DKV-Z]  "DKV: Anchor + Low-Rank Differential KV-Cache Compression for
+ *            Scalable Long-Context Inference" (Zenodo record), abstract.
+ *   [README] "Differential-KV (DKV): Anchor + Low-Rank KV-Cache Compression"
+ *            (project README): "Core Architecture & Paper Overview" (Core),
+ *            "Key Environment Knobs" (Knobs), "Measured Paper Benchmarks"
+ *            (Bench), "Core Innovations" (Innov).
+ *
+ * Each 256-token block of a (sequence, KV head) is stored as an exact anchor
+ * token (a_k, a_v), a rank-r joint K|V truncated-SVD delta (U with the
+ * singular values folded in, V_K, V_V) and R exact residual rows; a dense
+ * recency window sits beside the blocks ([DKV-Z]; [README Core] items 1-4).
+ * At decode time each query group routes to the top-K blocks, scores them in
+ * low-rank space as q.a_k + U_i.(V_K q) without materialising K, forms the
+ * value as (sum p) a_v + (sum p U_i) V_V, attends the residual rows and the
+ * window exactly, and merges all partial results with an fp32 log-sum-exp
+ * reduction over fp16 operands ([DKV-Z]; [README Core] "Low-Rank Space Query
+ * Scoring", "Flash-Style LSE Combine").
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" point to CUDA device memory that the CALLER
+ *     allocated and owns; the library allocates nothing and keeps no pointer
+ *     after a call returns.  Buffers must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *     default stream.  Work is enqueued asynchronously on it; the call returns
+ *     before the GPU finishes.
+ *   - Return value: DKV_OK (0) or a negative DKV_ERR_* code.  When arguments
+ *     fail validation nothing is launched and no memory is touched.  Nothing
+ *     throws across the ABI.
+ *   - Faults found on the device (a bounded wait that gave up, an index out of
+ *     range) set bits in an error word kept in the workspace header; read and
+ *     clear it with dkv_get_error().
+ *   - Units: a unit is one (sequence b, KV head h), numbered u = b*n_kv_heads + h.
+ *     Query head j belongs to KV head j / G with G = n_q_heads / n_kv_heads.
+ */
+#ifndef DKV_H
+#define DKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DKV_VERSION 1
+
+#if defined(__GNUC__)
+#define DKV_API __attribute__((visibility("default")))
+#else
+#define DKV_API
+#endif
+
+/* status codes */
+#define DKV_OK               0
+#define DKV_ERR_ARG         -1  /* null pointer, negative count, bad value */
+#define DKV_ERR_SHAPE       -2  /* sizes inconsistent with each other or with the descriptor */
+#define DKV_ERR_ALIGN       -3  /* a pointer is not 16-byte aligned */
+#define DKV_ERR_UNSUPPORTED -4  /* well-formed but outside what the kernels implement */
+#define DKV_ERR_CUDA        -5  /* a CUDA runtime call failed */
+#define DKV_ERR_TIMEOUT     -6  /* a bounded device wait gave up (see dkv_get_error) */
+#define DKV_ERR_WORKSPACE   -7  /* workspace missing or smaller than required */
+#define DKV_ERR_DEVICE      -8  /* the device error word is non-zero (see dkv_get_error) */
+
+/* bits of the device error word */
+#define DKV_DEVERR_TIMEOUT  0x1u  /* an mbarrier wait exceeded its iteration limit */
+#define DKV_DEVERR_INDEX    0x2u  /* a routed block index or residual position was out of range */
+#define DKV_DEVERR_RANGE    0x4u  /* a compressed factor did not fit fp16 (saturated) */
+
+#define DKV_BLOCK_SIZE 256      /* [README Core]: fixed micro-blocks of B_s = 256 tokens */
+
+/*
+ * Descriptor of one layer's compressed cache.  The caller sets the first nine
+ * fields; dkv_layout() validates them and fills the rest.  Plain old data:
+ * pass it by pointer, copy it freely.
+ *
+ * Supported: head_dim 64 or 128; 1 <= n_q_heads/n_kv_heads <= 8; block_size
+ * 256; 0 <= rank <= 128; 0 <= n_residual <= 255; n_blocks >= 0; window >= 0;
+ * n_blocks + window > 0.
+ */
+typedef struct dkv_desc {
+  int32_t batch;        /* sequences B */
+  int32_t n_q_heads;    /* query heads Hq */
+  int32_t n_kv_heads;   /* KV heads Hkv (Hq % Hkv == 0) */
+  int32_t head_dim;     /* d */
+  int32_t block_size;   /* must be 256 */
+  int32_t n_blocks;     /* compressed blocks NB per unit */
+  int32_t window;       /* exact recency-window tokens W per unit */
+  int32_t rank;         /* r: rank of the joint K|V delta ([README Core] item 2) */
+  int32_t n_residual;   /* R: exact residual rows per block ([README Core] item 3) */
+  /* ---- filled by dkv_layout() ---- */
+  int32_t rank_pad;     /* r rounded up to a multiple of 8 (zero-padded) */
+  int32_t res_pad;      /* R rounded up to a multiple of 8 (zero-padded) */
+  int32_t window_pad;   /* W rounded up to a multiple of 16 (zero-padded) */
+  int32_t n_units;      /* B * Hkv */
+  /* byte offsets inside one block record */
+  uint64_t blk_off_mask, blk_off_vk, blk_off_u, blk_off_res, blk_off_vv, block_bytes;
+  /* byte offsets inside one unit record */
+  uint64_t off_router, off_blocks, off_cold, off_window;
+  uint64_t block_stride, unit_stride, total_bytes;
+} dkv_desc;
+
+/*
+ * Plain row-major factors of a whole layer, used by dkv_import_factors() to
+ * fill the packed cache from factors produced elsewhere (for instance a host
+ * reference implementation).  All device pointers; fp16 unless noted.
+ * Shapes use U_ = n_units, NB, r, R, W, d from the descriptor.
+ */
+typedef struct dkv_factors {
+  const void* a_k;        /* [U_][NB][d]      anchor keys (the block's first token) */
+  const void* a_v;        /* [U_][NB][d]      anchor values */
+  const void* U;          /* [U_][NB][255][r] low-rank coefficients of tokens 1..255, S folded in */
+  const void* V_K;        /* [U_][NB][r][d]   key half of the joint right basis */
+  const void* V_V;        /* [U_][NB][r][d]   value half */
+  const int32_t* res_pos; /* [U_][NB][R]      residual token positions, 1..255, strictly ascending */
+  const void* K_res;      /* [U_][NB][R][d]   exact residual keys */
+  const void* V_res;      /* [U_][NB][R][d]   exact residual values */
+  const void* kmin;       /* [U_][NB][d]      per-channel key minimum over the block */
+  const void* kmax;       /* [U_][NB][d]      per-channel key maximum */
+  const void* win_K;      /* [U_][W][d]       recency-window keys */
+  const void* win_V;      /* [U_][W][d]       recency-window values */
+} dkv_factors;
+
+/* Library version (DKV_VERSION). */
+DKV_API int dkv_version(void);
+
+/* Human-readable name of a status code; never NULL. */
+DKV_API const char* dkv_status_string(int status);
+
+/*
+ * Validate the caller-set fields of *d and fill the layout fields.
+ * Returns DKV_OK, DKV_ERR_ARG (null / negative), DKV_ERR_SHAPE (Hq % Hkv != 0,
+ * nothing to attend) or DKV_ERR_UNSUPPORTED.  Host only; needs no GPU.
+ */
+DKV_API int dkv_layout(dkv_desc* d);
+
+/* dkv_layout() then the total cache size in bytes; 0 when validation fails. */
+DKV_API size_t dkv_layout_bytes(dkv_desc* d);
+
+/*
+ * Compress a layer's exact K and V into the packed cache ([DKV-Z]; [README
+ * Core] items 1-4): per block the anchor = first token, a rank-r truncated
+ * SVD of the joint deltas [K_i - a_k | V_i - a_v] (i = 1..255) with the
+ * singular values folded into U, the R rows with the largest key
+ * reconstruction error ||k_i - k_hat_i||_2 kept exact (ties to the lower
+ * row; [README Innov] "vanilla L2" criterion), per-channel key min/max for
+ * the router; the last W tokens are copied as the exact window.
+ *   d      descriptor filled by dkv_layout()
+ *   K, V   device fp16 [B][Hkv][T][head_dim], T = n_blocks*256 + window
+ *   cache  device buffer of d->total_bytes bytes, written entirely
+ *   workspace / ws_bytes  device scratch of dkv_compress_workspace_bytes(d)
+ * The GPU compressor supports rank <= 64 at head_dim 128 (<= 112 at 64).
+ */
+DKV_API size_t dkv_compress_workspace_bytes(const dkv_desc* d);
+DKV_API int dkv_compress_layout(const dkv_desc* d, const void* K, const void* V, void* cache,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Fill the packed cache from plain factors (see dkv_factors).  Overwrites the
+ * whole cache.  `workspace` is a device buffer of at least 256 bytes whose
+ * header receives the device error word: residual positions must be strictly
+ * ascending in 1..255, else DKV_DEVERR_INDEX is raised and the offending
+ * block keeps no residual row (its mask is left empty).
+ */
+DKV_API int dkv_import_factors(const dkv_desc* d, const dkv_factors* f, void* cache, void* workspace, void* stream);
+
+/*
+ * Decode-time attention for one layer ([DKV-Z]; [README Core]; [README
+ * Knobs] DKV_TOPK_BLOCKS, DKV_CB_GQA_ROUTE).
+ *   q       device fp16 [B][Hq][head_dim], one decode query per (sequence, head)
+ *   cache   device packed cache (dkv_compress_layout / dkv_import_factors)
+ *   top_k   blocks routed per unit; 0 or >= n_blocks attends every block
+ *           (the README's DKV_TOPK_BLOCKS=0 reading); negative is DKV_ERR_ARG
+ *   out     device fp32 [B][Hq][head_dim]: softmax(c q K_hat^T) V_hat over the
+ *           routed blocks and the window, c = 1/sqrt(head_dim)
+ *   lse     optional device fp32 [B][Hq]: natural-log log-sum-exp of the scores
+ *   routed  optional device int32 [B][Hkv][K_eff]: routed block indices,
+ *           ascending, K_eff = top_k clipped to n_blocks
+ *   workspace / ws_bytes  device scratch of dkv_decode_workspace_bytes(d, top_k)
+ * Routing: qbar = mean over the group of c*q; block score
+ * sum_j max(qbar_j kmax_bj, qbar_j kmin_bj); top-K by (score desc, index asc).
+ */
+DKV_API size_t dkv_decode_workspace_bytes(const dkv_desc* d, int32_t top_k);
+DKV_API int dkv_decode_attend(const dkv_desc* d, const void* q, const void* cache, int32_t top_k,
+                      float* out, float* lse, int32_t* routed,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Dense fp16 decode attention over uncompressed K, V: the bytes/throughput
+ * reference the compressed path is compared with.
+ *   K, V   device fp16 [B][Hkv][T][head_dim]; T >= 1
+ *   q      device fp16 [B][Hq][head_dim];  out fp32 [B][Hq][head_dim];  lse optional fp32 [B][Hq]
+ */
+DKV_API size_t dkv_dense_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads,
+                                 int32_t head_dim, int32_t T);
+DKV_API int dkv_dense_decode(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t T,
+                     const void* q, const void* K, const void* V, float* out, float* lse,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, read the device error word kept in the header of
+ * `workspace` (any workspace passed to the calls above), store it in *word
+ * and clear it.  Returns DKV_OK, DKV_ERR_TIMEOUT when the timeout bit is set,
+ * DKV_ERR_DEVICE for other bits, DKV_ERR_CUDA when the stream failed.
+ */
+DKV_API int dkv_get_error(void* workspace, void* stream, uint32_t* word);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DKV_H */

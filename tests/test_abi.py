@@ -1,0 +1,86 @@
+"""The C-ABI library: loads, exports every symbol include/dkv.h declares, and
+validates descriptors and arguments on the host (no GPU needed here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from compressed_kv_cache_dkv_gb300 import dkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dkv_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = dkv.lib()
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(dkv.EXPORTED)
+    assert lib.dkv_version() == 1
+
+
+def test_status_strings():
+    for st in (0, -1, -2, -3, -4, -5, -6, -7, -8):
+        assert dkv.dkv_status_string(st)
+    assert dkv.dkv_status_string(-99) == "unknown status"
+
+
+def test_layout_validation():
+    ok = dict(batch=1, n_q_heads=12, n_kv_heads=2, head_dim=128, n_blocks=30, window=512, rank=32, n_residual=40)
+    dkv.dkv_layout(**ok)
+    bad = [
+        (dict(batch=0), dkv.DKV_ERR_ARG), (dict(rank=-1), dkv.DKV_ERR_ARG), (dict(n_blocks=-1), dkv.DKV_ERR_ARG),
+        (dict(n_q_heads=13), dkv.DKV_ERR_SHAPE), (dict(n_blocks=0, window=0), dkv.DKV_ERR_SHAPE),
+        (dict(head_dim=96), dkv.DKV_ERR_UNSUPPORTED), (dict(rank=129), dkv.DKV_ERR_UNSUPPORTED),
+        (dict(n_residual=256), dkv.DKV_ERR_UNSUPPORTED), (dict(n_q_heads=18), dkv.DKV_ERR_UNSUPPORTED),
+        (dict(block_size=128), dkv.DKV_ERR_UNSUPPORTED),
+    ]
+    for change, status in bad:
+        kw = dict(ok, **change)
+        with pytest.raises(dkv.DkvError) as e:
+            dkv.dkv_layout(**kw)
+        assert e.value.status == status, change
+
+
+@pytest.mark.parametrize("d,nb,W,r,R", [(128, 30, 512, 32, 40), (128, 252, 1024, 48, 128), (64, 3, 256, 8, 16),
+                                        (128, 5, 17, 24, 5), (64, 0, 100, 0, 0)])
+def test_layout_bytes(d, nb, W, r, R):
+    desc = dkv.dkv_layout(2, 6, 2, d, nb, W, r, R)
+    r8, R8, W16 = -(-r // 8) * 8, -(-R // 8) * 8, -(-W // 16) * 16
+    hot = 4 * d + 32 + 2 * r8 * d + 512 * r8 + 4 * R8 * d + 2 * r8 * d
+    assert desc.block_bytes == hot
+    assert desc.block_stride % 128 == 0 and desc.block_stride >= hot
+    for off in (desc.blk_off_mask, desc.blk_off_vk, desc.blk_off_u, desc.blk_off_res, desc.blk_off_vv,
+                desc.off_blocks, desc.off_cold, desc.off_window, desc.unit_stride):
+        assert off % 16 == 0
+    assert desc.unit_stride >= nb * (4 * d + desc.block_stride) + W16 * 4 * d
+    assert desc.total_bytes == desc.unit_stride * 2 * 2
+    assert dkv.dkv_layout_bytes(desc) == desc.total_bytes
+
+
+def test_calls_validate_before_touching_the_device():
+    """Bad arguments return an error code without any CUDA work."""
+    desc = dkv.dkv_layout(1, 6, 1, 64, 3, 100, 16, 24)
+    L = dkv.lib()
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    assert L.dkv_decode_attend(ctypes.byref(desc), None, fake, 2, fake, None, None, fake, 1 << 20, None) == dkv.DKV_ERR_ARG
+    assert L.dkv_decode_attend(ctypes.byref(desc), fake, fake, -3, fake, None, None, fake, 1 << 20, None) == dkv.DKV_ERR_ARG
+    assert L.dkv_decode_attend(ctypes.byref(desc), odd, fake, 2, fake, None, None, fake, 1 << 20, None) == dkv.DKV_ERR_ALIGN
+    assert L.dkv_decode_attend(ctypes.byref(desc), fake, fake, 2, fake, None, None, fake, 16, None) == dkv.DKV_ERR_WORKSPACE
+    edited = dkv.dkv_desc.from_buffer_copy(desc)
+    edited.rank = 24     # descriptor changed after dkv_layout()
+    assert L.dkv_decode_attend(ctypes.byref(edited), fake, fake, 2, fake, None, None, fake, 1 << 20, None) == dkv.DKV_ERR_SHAPE
+    assert L.dkv_compress_layout(ctypes.byref(desc), None, fake, fake, fake, 1 << 20, None) == dkv.DKV_ERR_ARG
+    assert L.dkv_dense_decode(1, 6, 4, 64, 10, fake, fake, fake, fake, None, fake, 1 << 20, None) == dkv.DKV_ERR_SHAPE
+    assert L.dkv_dense_decode(1, 6, 1, 80, 10, fake, fake, fake, fake, None, fake, 1 << 20, None) == dkv.DKV_ERR_UNSUPPORTED
+    assert dkv.dkv_decode_workspace_bytes(desc, -1) == 0
+    assert dkv.dkv_decode_workspace_bytes(desc, 2) > 0
