@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Decode-attention throughput over the DKV compressed cache on GB300.
+
+One step = one decode step of every layer of the workload: per layer one
+dkv_decode_attend (route -> block/window attention -> LSE combine) over that
+layer's packed cache, each layer with its own queries.  Default workload: the
+64k configuration (batch 16, 28 layers of 12 q / 2 KV heads, head_dim 128,
+252 blocks + 1024-token window per unit, layer-adaptive rank 24/48/16, 128
+residual rows, top-K 16).
+
+Prints ONE JSON line (rank 0).  `value` = queries/s of the device-timed
+steps (inputs resident in HBM, K steps replayed from a CUDA graph);
+`e2e` = the same metric through the C ABI with pinned host buffers (q copied
+in, out copied back, every step); `roofline` = the block/window attention
+kernel's algorithmic bytes per launch over its CUDA-event duration inside the
+timed region; `cpu_baseline` = the fp64 oracle timed on host cores on a
+bounded sample.  `--impl reference` times the oracle alone as the reference arm.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (weak
+scaling, no data-path collective); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attention queries/s and HBM GB/s (% of roofline) over DKV cache"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------------------- byte accounting
+
+def attend_bytes(w, layer: int, top_k: int) -> int:
+    """Algorithmic bytes the block/window attention kernel must read per launch:
+    per unit K routed blocks (anchors 4d + V_K,V_V 4rd + U 2*255*r + residual
+    rows 4Rd + mask 32) plus the window 4Wd; per launch the queries."""
+    d, r, R, W, NB = w.head_dim, w.rank(layer), w.n_residual, w.window, w.n_blocks
+    k = NB if (top_k == 0 or top_k >= NB) else top_k
+    per_block = 4 * d + 4 * r * d + 2 * 255 * r + 4 * R * d + 32
+    per_unit = k * per_block + W * 4 * d
+    return w.units_per_layer * per_unit + w.batch * w.n_q_heads * d * 2
+
+
+def call_bytes(w, layer: int, top_k: int) -> int:
+    """Algorithmic bytes of one dkv_decode_attend: the attention kernel's bytes,
+    the router rows NB*4d per unit, and the fp32 output."""
+    return (attend_bytes(w, layer, top_k) + w.units_per_layer * w.n_blocks * 4 * w.head_dim
+            + w.batch * w.n_q_heads * w.head_dim * 4)
+
+
+# ----------------------------------------------------------------------------- clocks (NVML, read only)
+
+REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+           0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+           0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event reasons of this process's GPU every few ms."""
+
+    def __init__(self, torch_device_index: int):
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._h = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            bus = self._bus_id(torch_device_index)
+            h = ctypes.c_void_p()
+            if bus is None or nv.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nv, self._h = nv, h
+            fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._reasons = fn
+        except OSError:
+            self._h = None
+
+    @staticmethod
+    def _bus_id(idx: int):
+        try:
+            import torch
+            rt = ctypes.CDLL("libcudart.so.13")
+            buf = ctypes.create_string_buffer(64)
+            dev = torch.cuda.current_device() if idx is None else idx
+            if rt.cudaDeviceGetPCIBusId(buf, 64, dev) != 0:
+                return None
+            return buf.value
+        except OSError:
+            return None
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self._nv.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0 and \
+                    self._reasons(self._h, ctypes.byref(rs)) == 0:
+                self.samples.append((clk.value, rs.value))
+            time.sleep(0.003)
+
+    def __enter__(self):
+        if self._h is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._h is not None:
+            self._t.join()
+
+    def summary(self) -> dict:
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"], "samples": 0}
+        busy = [s for s in self.samples if not (s[1] & 0x1)] or self.samples
+        reasons = 0
+        for _, r in busy:
+            reasons |= r
+        names = [n for b, n in REASONS.items() if reasons & b and b != 0x1]
+        return {"sm_mhz": statistics.median(c for c, _ in busy), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(busy)}
+
+
+# ----------------------------------------------------------------------------- CUDA events usable inside graphs
+
+class ExtEvents:
+    """cudaEvent_t objects recorded with cudaEventRecordExternal, so that a
+    record placed in a captured stream becomes an event node of the graph."""
+
+    def __init__(self):
+        self.rt = ctypes.CDLL("libcudart.so.13")
+        self.rt.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
+        self.rt.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        self.rt.cudaEventDestroy.argtypes = [ctypes.c_void_p]
+        self.events = []
+
+    def new(self):
+        ev = ctypes.c_void_p()
+        if self.rt.cudaEventCreate(ctypes.byref(ev)) != 0:
+            raise RuntimeError("cudaEventCreate failed")
+        self.events.append(ev)
+        return ev
+
+    def record(self, ev, stream_handle: int):
+        if self.rt.cudaEventRecordWithFlags(ev, ctypes.c_void_p(stream_handle), 1) != 0:
+            raise RuntimeError("cudaEventRecordWithFlags failed")
+
+    def elapsed_ms(self, a, b) -> float:
+        ms = ctypes.c_float()
+        if self.rt.cudaEventElapsedTime(ctypes.byref(ms), a, b) != 0:
+            raise RuntimeError("cudaEventElapsedTime failed")
+        return float(ms.value)
+
+    def close(self):
+        for ev in self.events:
+            self.rt.cudaEventDestroy(ev)
+        self.events = []
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+def _oracle_decode_worker(args):
+    """Child process (spawned, BLAS pinned to one thread): compress one sampled
+    unit with the oracle (untimed), then time its decode for ~`seconds`."""
+    cfg_name, layer, replica, seconds, top_k = args
+    import numpy as np
+
+    from compressed_kv_cache_dkv_gb300 import synth
+    from oracle import dkv_oracle as O
+    w = synth.WORKLOADS[cfg_name]
+    K, V = synth.unit_kv(w, layer, 0, 0)
+    t0 = time.perf_counter()
+    unit = O.compress_unit(K, V, w.n_blocks, w.rank(layer), w.n_residual)
+    t_comp = time.perf_counter() - t0
+    q = synth.queries(w, layer)[0, :w.group].astype(np.float64)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        O.decode_unit(q, unit, top_k)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"decodes": n, "seconds": el, "queries": n * w.group, "compress_s": t_comp}
+
+
+def cpu_oracle(cfg_name: str, layer: int, seconds: float, top_k: int, n_proc: int = 1) -> dict:
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(n_proc) as pool:
+        res = pool.map(_oracle_decode_worker, [(cfg_name, layer, i, seconds, top_k) for i in range(n_proc)])
+    q = sum(r["queries"] for r in res)
+    t = max(r["seconds"] for r in res)
+    return {"queries": q, "seconds": t, "qps": q / t, "cores": n_proc, "compress_s": max(r["compress_s"] for r in res)}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["dkv", "reference"], default="dkv")
+    ap.add_argument("--config", default="64k")
+    ap.add_argument("--top-k", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=None, help="restrict to the first N layers (experiments only)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from compressed_kv_cache_dkv_gb300 import synth
+    w = synth.WORKLOADS[args.config]
+    top_k = w.top_k if args.top_k is None else args.top_k
+    n_layers = w.n_layers if args.layers is None else min(args.layers, w.n_layers)
+    wl_name = (f"{w.name}: batch {w.batch}, {n_layers} layer(s) of {w.n_q_heads}q/{w.n_kv_heads}kv heads x d{w.head_dim}, "
+               f"{w.n_blocks} blocks of 256 + {w.window}-token window, r {sorted(set(w.ranks[:n_layers]))}, "
+               f"R {w.n_residual}, top-K {top_k}")
+    queries_per_step = w.batch * w.n_q_heads * n_layers
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        K = args.steps
+        per = max(0.5, args.cpu_seconds / max(1, K + args.warmup))
+        r = cpu_oracle(w.name, 0, per * (K + args.warmup), top_k)
+        qps = r["qps"]
+        line = {"impl": "reference", "metric": METRIC, "value": qps, "unit": "queries/s", "n_gpus": args.gpus,
+                "steps": K, "warmup": args.warmup, "ms_per_step": 1e3 * queries_per_step / qps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": wl_name, "sample": "one unit (sequence 0, KV head 0) of layer 0"},
+                "cpu_baseline": {"value": qps, "unit": "queries/s", "cores": r["cores"], "kind": "oracle",
+                                 "sample": f"fp64 oracle decode of one unit of layer 0 ({w.group} queries), "
+                                           f"repeated for {r['seconds']:.1f} s; compression excluded"},
+                "e2e": {"value": qps, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import numpy as np
+    import torch
+
+    from compressed_kv_cache_dkv_gb300 import dkv
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    dkv.lib()
+
+    # ---------------- setup: compress every layer's K, V into its packed cache (untimed)
+    t_setup = time.perf_counter()
+    descs, caches, qs, outs, lses = [], [], [], [], []
+    ws_bytes = 0
+    for layer in range(n_layers):
+        d = dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window, w.rank(layer),
+                           w.n_residual)
+        ws_bytes = max(ws_bytes, dkv.dkv_decode_workspace_bytes(d, top_k))
+        descs.append(d)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    for layer in range(n_layers):
+        K, V = synth.layer_kv_torch(w, layer, dev, replica=rank)
+        caches.append(dkv.dkv_compress_layout(descs[layer], K, V, workspace=ws))
+        del K, V
+        qs.append(torch.from_numpy(synth.queries(w, layer)).to(dev))
+        outs.append(torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.float32, device=dev))
+        lses.append(torch.empty(w.batch, w.n_q_heads, dtype=torch.float32, device=dev))
+    torch.cuda.synchronize()
+    st, word = dkv.dkv_get_error(ws)
+    if st != dkv.DKV_OK:
+        raise RuntimeError(f"compression raised device error word {word:#x}")
+    t_setup = time.perf_counter() - t_setup
+    cache_gb = sum(c.numel() for c in caches) / 1e9
+    log(f"[bench] rank {rank}: setup {t_setup:.1f} s, packed caches {cache_gb:.2f} GB over {n_layers} layers")
+
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    ext = ExtEvents()
+
+    def step(events=None):
+        for layer in range(n_layers):
+            dkv.dkv_decode_route(descs[layer], qs[layer], caches[layer], top_k, ws, stream=sh)
+            if events is not None:
+                ext.record(events[layer][0], sh)
+            dkv.dkv_decode_blocks(descs[layer], qs[layer], caches[layer], top_k, ws, stream=sh)
+            if events is not None:
+                ext.record(events[layer][1], sh)
+            dkv.dkv_decode_combine(descs[layer], top_k, outs[layer], ws, lse=lses[layer], stream=sh)
+
+    # ---------------- warm-up (eager), then capture K steps into one graph
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    K_steps = args.steps
+    ev = [[(ext.new(), ext.new()) for _ in range(n_layers)] for _ in range(K_steps)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for k in range(K_steps):
+            step(ev[k])
+    graph.replay()  # one untimed replay of the captured steps (warm)
+    stream.synchronize()
+
+    # ---------------- timed region
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0.record(stream)
+        graph.replay()
+        t1.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1)
+    attend_ms = [ext.elapsed_ms(ev[k][l][0], ev[k][l][1]) for k in range(K_steps) for l in range(n_layers)]
+    st, word = dkv.dkv_get_error(ws, stream=sh)
+    if st != dkv.DKV_OK:
+        raise RuntimeError(f"decode raised device error word {word:#x}")
+
+    # ---------------- e2e through the C ABI with pinned host buffers
+    e2e_steps = args.e2e_steps or max(10, min(K_steps, 50))
+    q_host = [q.cpu().pin_memory() for q in qs]
+    q_dev = [torch.empty_like(q) for q in qs]
+    o_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    e_ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        for layer in range(n_layers):
+            q_dev[layer].copy_(q_host[layer], non_blocking=True)
+            dkv.dkv_decode_attend(descs[layer], q_dev[layer], caches[layer], top_k, out=outs[layer], lse=False,
+                                  routed=False, workspace=e_ws, stream=sh)
+            o_host[layer].copy_(outs[layer], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    # ---------------- reduce over ranks (max time)
+    if world > 1:
+        tt = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(tt[0]), float(tt[1])
+    ms_step = ms / K_steps
+    value = world * queries_per_step * K_steps / (ms / 1e3)
+    e2e_value = world * queries_per_step * e2e_steps / (e2e_ms / 1e3)
+
+    step_bytes = sum(call_bytes(w, l, top_k) for l in range(n_layers))
+    att_bytes_step = sum(attend_bytes(w, l, top_k) for l in range(n_layers))
+    att_ms_mean = statistics.fmean(attend_ms)
+    achieved_gbs = (att_bytes_step / n_layers) / (att_ms_mean / 1e3) / 1e9
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        peak = float(json.load(open(peaks_path))["hbm_gbs"])
+        peak_src = "measured"
+    else:
+        peak, peak_src = FALLBACK_HBM_GBS, "fallback"
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "attend_traffic.json")
+    if os.path.exists(tpath):
+        tinfo = json.load(open(tpath))
+        src = open(os.path.join(ROOT, "compressed_kv_cache_dkv_gb300", "csrc", "attend.cu"), "rb").read()
+        if tinfo.get("attend_cu_sha1") == hashlib.sha1(src).hexdigest() and tinfo.get("config") == w.name:
+            traffic = tinfo.get("bytes_per_launch")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": K_steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": wl_name, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: {cache_gb:.1f} GB of packed caches per step cycle, each layer "
+                         f"read once per step", "graph": "K steps captured in one CUDA graph"},
+        "hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
+        "hbm_frac_of_measured": step_bytes / (ms_step / 1e3) / 1e9 / peak,
+        "hbm_frac_of_nominal_8tbs": step_bytes / (ms_step / 1e3) / 1e9 / 8000.0,
+        "bytes_per_step": step_bytes,
+        "roofline": {"bound": "hbm", "kernel": "attend_kernel (block + window attention)", "achieved": achieved_gbs,
+                     "peak": peak, "unit": "GB/s", "frac": achieved_gbs / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
+                     "bytes_per_launch": att_bytes_step / n_layers, "mean_launch_us": att_ms_mean * 1e3},
+        "e2e": {"value": e2e_value, "unit": "queries/s", "steps": e2e_steps,
+                "h2d_bytes_per_step": sum(q.numel() * 2 for q in qs),
+                "d2h_bytes_per_step": sum(o.numel() * 4 for o in outs)},
+        "gpu_launches": K_steps * n_layers * 3,
+        "clocks": clocks.summary(),
+        "setup_s": t_setup,
+    }
+    ext.close()
+    if rank == 0 and not args.no_cpu_baseline:
+        cb = cpu_oracle(w.name, 0, args.cpu_seconds, top_k)
+        line["cpu_baseline"] = {"value": cb["qps"], "unit": "queries/s", "cores": cb["cores"], "kind": "oracle",
+                                "sample": f"fp64 oracle decode of one unit (sequence 0, KV head 0, {w.group} queries) "
+                                          f"of layer 0, repeated for {cb['seconds']:.1f} s on one host core; "
+                                          f"oracle compression ({cb['compress_s']:.1f} s) excluded"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

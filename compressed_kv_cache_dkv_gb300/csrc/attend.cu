@@ -568,11 +568,11 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
 
 template <int D, int RT>
 cudaError_t launch_one(const AttendArgs& a, size_t smem, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
+  static size_t configured = 0;  // largest dynamic shared memory size enabled so far
+  if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(attend_kernel<D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured = smem;
   }
   dim3 grid(a.n_items, a.L.units);
   attend_kernel<D, RT><<<grid, kThreads, smem, s>>>(a);

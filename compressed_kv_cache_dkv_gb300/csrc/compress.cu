@@ -31,7 +31,7 @@ namespace {
 
 constexpr int kCThreads = 544;   // 17 warps: 528 threads own the 8x8 Gram tiles when n = 256
 constexpr int kChunk = 16;       // tokens staged in shared memory at a time
-constexpr int kIters = 8;        // subspace iterations after the start block
+constexpr int kIters = 12;       // subspace iterations after the start block
 constexpr int kMaxSweeps = 16;
 
 struct CArgs {
@@ -388,6 +388,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
 
   // ---- top-r eigenpairs (eigenvalue desc, ties to the lower index)
   const int m = a.full ? n : p;
+  for (int k = tid; k < 256; k += nt) sel[k] = 0;  // in-range even if non-finite values break the ranking
+  __syncthreads();
   for (int c = tid; c < m; c += nt) {
     const float lc = H[c * ldh + c];
     int rank = 0;

@@ -35,7 +35,8 @@ BLOCK_SIZE = 256
 EXPORTED = (
     "dkv_version", "dkv_status_string", "dkv_layout", "dkv_layout_bytes",
     "dkv_compress_workspace_bytes", "dkv_compress_layout", "dkv_import_factors",
-    "dkv_decode_workspace_bytes", "dkv_decode_attend",
+    "dkv_decode_workspace_bytes", "dkv_decode_attend", "dkv_decode_route", "dkv_decode_blocks",
+    "dkv_decode_combine",
     "dkv_dense_workspace_bytes", "dkv_dense_decode", "dkv_get_error",
 )
 
@@ -89,6 +90,9 @@ def lib() -> ctypes.CDLL:
         L.dkv_decode_workspace_bytes.restype = sz
         L.dkv_decode_workspace_bytes.argtypes = [pdesc, i32]
         L.dkv_decode_attend.argtypes = [pdesc, vp, vp, i32, vp, vp, vp, vp, sz, vp]
+        L.dkv_decode_route.argtypes = [pdesc, vp, vp, i32, vp, vp, sz, vp]
+        L.dkv_decode_blocks.argtypes = [pdesc, vp, vp, i32, vp, sz, vp]
+        L.dkv_decode_combine.argtypes = [pdesc, i32, vp, vp, vp, sz, vp]
         L.dkv_dense_workspace_bytes.restype = sz
         L.dkv_dense_workspace_bytes.argtypes = [i32] * 5
         L.dkv_dense_decode.argtypes = [i32] * 5 + [vp] * 6 + [sz, vp]
@@ -192,6 +196,21 @@ def dkv_decode_attend(d: dkv_desc, q: torch.Tensor, cache: torch.Tensor, top_k: 
                                    _ptr(routed), _ptr(workspace), workspace.numel(), _stream(stream)),
            "dkv_decode_attend")
     return out, lse, routed
+
+
+def dkv_decode_route(d: dkv_desc, q, cache, top_k: int, workspace, routed=None, stream=None) -> None:
+    _check(lib().dkv_decode_route(ctypes.byref(d), _ptr(q), _ptr(cache), int(top_k), _ptr(routed), _ptr(workspace),
+                                  workspace.numel(), _stream(stream)), "dkv_decode_route")
+
+
+def dkv_decode_blocks(d: dkv_desc, q, cache, top_k: int, workspace, stream=None) -> None:
+    _check(lib().dkv_decode_blocks(ctypes.byref(d), _ptr(q), _ptr(cache), int(top_k), _ptr(workspace),
+                                   workspace.numel(), _stream(stream)), "dkv_decode_blocks")
+
+
+def dkv_decode_combine(d: dkv_desc, top_k: int, out, workspace, lse=None, stream=None) -> None:
+    _check(lib().dkv_decode_combine(ctypes.byref(d), int(top_k), _ptr(out), _ptr(lse), _ptr(workspace),
+                                    workspace.numel(), _stream(stream)), "dkv_decode_combine")
 
 
 def dkv_dense_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim, T) -> int:

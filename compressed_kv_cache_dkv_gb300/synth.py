@@ -177,3 +177,38 @@ def layer_kv(w: Workload, layer: int, units: Iterable[tuple[int, int]] | None = 
         with _cf.ThreadPoolExecutor(n) as ex:
             list(ex.map(one, todo))
     return K, V
+
+
+def layer_kv_torch(w: Workload, layer: int, device, replica: int = 0):
+    """Same recipe as ``layer_kv``, drawn with torch's generator on `device`
+    (a different random stream than the numpy one; used where throughput
+    inputs are needed fast and no host-side reference is computed).
+    Returns K, V fp16 [batch, n_kv_heads, T, d] on the device."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(int(np.random.SeedSequence([w.seed, layer, replica, 7]).generate_state(1)[0]))
+    B, H, d, lat = w.batch, w.n_kv_heads, w.head_dim, w.latent
+    NB, W = w.n_blocks, w.window
+    T = w.context
+    f32 = torch.float32
+    out = torch.empty(2, B, H, T, d, dtype=f32, device=device)
+    if NB:
+        lt = torch.randn(2, B, H, NB, BLOCK_SIZE, lat, generator=g, device=device, dtype=f32)
+        mix = torch.randn(2, B, H, NB, lat, d, generator=g, device=device, dtype=f32) / float(np.sqrt(lat))
+        mu = torch.randn(2, B, H, NB, 1, d, generator=g, device=device, dtype=f32)
+        out[:, :, :, :NB * BLOCK_SIZE] = (torch.matmul(lt, mix) + mu).reshape(2, B, H, NB * BLOCK_SIZE, d)
+        del lt, mix, mu
+    if W:
+        lt = torch.randn(2, B, H, W, lat, generator=g, device=device, dtype=f32)
+        mix = torch.randn(2, B, H, lat, d, generator=g, device=device, dtype=f32) / float(np.sqrt(lat))
+        mu = torch.randn(2, B, H, 1, d, generator=g, device=device, dtype=f32)
+        out[:, :, :, NB * BLOCK_SIZE:] = torch.matmul(lt, mix) + mu
+        del lt, mix, mu
+    out.add_(torch.randn(out.shape, generator=g, device=device, dtype=f32), alpha=NOISE_STD)
+    rows = np.stack([np.stack([_outlier_rows(_unit_rng(w.seed, layer, b, h, 1 + 2 * replica), T, w.outlier_runs)
+                               for h in range(H)]) for b in range(B)])
+    scale = torch.from_numpy(np.where(rows, OUTLIER_SCALE, 1.0).astype(np.float32)).to(device)
+    out.mul_(scale[None, :, :, :, None])
+    kv = out.to(torch.float16)
+    return kv[0].contiguous(), kv[1].contiguous()

@@ -190,6 +190,22 @@ DKV_API int dkv_decode_attend(const dkv_desc* d, const void* q, const void* cach
                       void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * The three stages of dkv_decode_attend as separate calls, for callers that
+ * schedule or time them individually.  Run in this order on one stream with
+ * one workspace (it carries the routed indices and the partial results from
+ * stage to stage); arguments mean the same as for dkv_decode_attend.
+ *   route:   top-K block selection per unit (skipped when n_blocks == 0)
+ *   blocks:  one partial (m, l, acc) per routed block and per window chunk
+ *   combine: fp32 log-sum-exp merge of the partials into out (and lse)
+ */
+DKV_API int dkv_decode_route(const dkv_desc* d, const void* q, const void* cache, int32_t top_k, int32_t* routed,
+                             void* workspace, size_t ws_bytes, void* stream);
+DKV_API int dkv_decode_blocks(const dkv_desc* d, const void* q, const void* cache, int32_t top_k,
+                              void* workspace, size_t ws_bytes, void* stream);
+DKV_API int dkv_decode_combine(const dkv_desc* d, int32_t top_k, float* out, float* lse,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Dense fp16 decode attention over uncompressed K, V: the bytes/throughput
  * reference the compressed path is compared with.
  *   K, V   device fp16 [B][Hkv][T][head_dim]; T >= 1

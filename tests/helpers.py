@@ -96,3 +96,18 @@ def check_routing(gpu_idx: np.ndarray, ref_idx: np.ndarray, bounds: np.ndarray) 
     kth = np.sort(bounds)[::-1][len(ref_idx) - 1]
     for b in g ^ r:
         assert abs(bounds[b] - kth) <= TIE_BAND, f"block {b} routed differently (bound {bounds[b]}, K-th {kth})"
+
+
+def _compress_blocks_job(args):
+    Kc, Vc, rank, R = args
+    n = Kc.shape[0] // O.BLOCK_SIZE
+    return [O.compress_block(Kc[i * 256:(i + 1) * 256], Vc[i * 256:(i + 1) * 256], rank, R) for i in range(n)]
+
+
+def oracle_unit_blockwise(K: np.ndarray, V: np.ndarray, n_blocks: int, rank: int, R: int, per_job: int = 8) -> O.Unit:
+    """compress_unit with the blocks spread over the process pool."""
+    jobs = [(K[b * 256:min(n_blocks, b + per_job) * 256], V[b * 256:min(n_blocks, b + per_job) * 256], rank, R)
+            for b in range(0, n_blocks, per_job)]
+    blocks = [blk for part in pool().map(_compress_blocks_job, jobs) for blk in part]
+    return O.Unit(blocks=blocks, win_K=np.asarray(K[n_blocks * 256:], np.float64),
+                  win_V=np.asarray(V[n_blocks * 256:], np.float64))

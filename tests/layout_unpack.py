@@ -1,0 +1,87 @@
+"""Host-side reader of the packed cache layout (test utility).
+
+Rebuilds the plain factors of a block, and the window, from the raw bytes of
+a cache produced by dkv_compress_layout or dkv_import_factors.  It follows
+the layout described in include/dkv.h and csrc/dkv_internal.cuh with its own
+index arithmetic (numpy), so a pack -> unpack round trip checks both.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def a_layout_index(rows: int, cols: int) -> np.ndarray:
+    """Half-element index (in the packed "A layout") of every (row, col): [rows, cols]."""
+    r = np.arange(rows)[:, None]
+    c = np.arange(cols)[None, :]
+    mt, kt = r // 16, c // 16
+    rows_in = np.minimum(16, rows - mt * 16)
+    cols_in = np.minimum(16, cols - kt * 16)
+    nr, nc = rows_in // 8, cols_in // 8
+    nsb = nr * nc
+    rr, cc = (r % 16) // 8, (c % 16) // 8
+    sbi = cc * nr + rr
+    lane = (r % 8) * 4 + (c % 8) // 2
+    base = mt * 16 * cols * 2 + kt * 16 * rows_in * 2
+    byte = base + lane * nsb * 4 + sbi * 4 + (c % 2) * 2
+    return byte // 2
+
+
+def bt_layout_index(rows: int, cols: int) -> np.ndarray:
+    r = np.arange(rows)[:, None]
+    c = np.arange(cols)[None, :]
+    nt, kp = r // 8, c // 32
+    lane = (r % 8) * 4 + (c % 8) // 2
+    sb = (c % 32) // 8
+    byte = nt * 8 * cols * 2 + kp * 512 + lane * 16 + sb * 4 + (c % 2) * 2
+    return byte // 2
+
+
+def exact_index(n_tok: int, d: int) -> tuple[np.ndarray, np.ndarray]:
+    """Half-element index of K[t][j] and V[t][j] in a run of 16-token exact groups."""
+    K = np.zeros((n_tok, d), np.int64)
+    V = np.zeros((n_tok, d), np.int64)
+    for g in range(0, n_tok, 16):
+        in_g = min(16, n_tok - g)
+        gbase = g * 4 * d // 2  # halves: g/16 groups * 64 d bytes
+        K[g:g + in_g] = gbase + a_layout_index(in_g, d)
+        V[g:g + in_g] = gbase + in_g * d + a_layout_index(d, in_g).T
+    return K, V
+
+
+def unpack_block(cache: np.ndarray, desc, u: int, b: int) -> dict:
+    d, r, r8, R, R8 = desc.head_dim, desc.rank, desc.rank_pad, desc.n_residual, desc.res_pad
+    unit = u * desc.unit_stride
+    blk = unit + desc.off_blocks + b * desc.block_stride
+    h = lambda off, n: cache[off:off + 2 * n].view(np.float16)
+    out = {}
+    out["a_k"] = h(blk, d).copy()
+    out["a_v"] = h(blk + 2 * d, d).copy()
+    words = cache[blk + desc.blk_off_mask: blk + desc.blk_off_mask + 32].view(np.uint32)
+    out["mask"] = np.array([(words[i >> 5] >> (i & 31)) & 1 for i in range(256)], dtype=bool)
+    vk = h(blk + desc.blk_off_vk, r8 * d)
+    out["V_K"] = vk[bt_layout_index(r8, d)][:r].copy()
+    uu = h(blk + desc.blk_off_u, 256 * r8)
+    Ufull = uu[a_layout_index(256, r8)]
+    out["U_row0"] = Ufull[0].copy()
+    out["U"] = Ufull[1:, :r].copy()
+    res = h(blk + desc.blk_off_res, 2 * R8 * d)
+    ki, vi = exact_index(R8, d)
+    out["K_res"] = res[ki][:R].copy()
+    out["V_res"] = res[vi][:R].copy()
+    out["res_pad_zero"] = bool((res[ki][R:] == 0).all() and (res[vi][R:] == 0).all())
+    vv = h(blk + desc.blk_off_vv, r8 * d)
+    out["V_V"] = vv[a_layout_index(d, r8)].T[:r].copy()
+    router = h(unit + desc.off_router + b * 4 * d, 2 * d)
+    out["kmin"], out["kmax"] = router[:d].copy(), router[d:].copy()
+    cold = cache[unit + desc.off_cold + b * R8 * 2: unit + desc.off_cold + (b + 1) * R8 * 2].view(np.uint16)
+    out["S"] = cold[:R].astype(np.int64)
+    return out
+
+
+def unpack_window(cache: np.ndarray, desc, u: int) -> tuple[np.ndarray, np.ndarray]:
+    d, W, W16 = desc.head_dim, desc.window, desc.window_pad
+    off = u * desc.unit_stride + desc.off_window
+    win = cache[off: off + W16 * 4 * d].view(np.float16)
+    ki, vi = exact_index(W16, d)
+    return win[ki][:W].copy(), win[vi][:W].copy()
