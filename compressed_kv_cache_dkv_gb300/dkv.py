@@ -37,7 +37,7 @@ EXPORTED = (
     "dkv_compress_workspace_bytes", "dkv_compress_layout", "dkv_import_factors",
     "dkv_decode_workspace_bytes", "dkv_decode_attend", "dkv_decode_route", "dkv_decode_blocks",
     "dkv_decode_combine",
-    "dkv_dense_workspace_bytes", "dkv_dense_decode", "dkv_get_error",
+    "dkv_dense_workspace_bytes", "dkv_dense_decode", "dkv_get_error", "dkv_decode_attend_noalloc",
 )
 
 
@@ -97,6 +97,7 @@ def lib() -> ctypes.CDLL:
         L.dkv_dense_workspace_bytes.argtypes = [i32] * 5
         L.dkv_dense_decode.argtypes = [i32] * 5 + [vp] * 6 + [sz, vp]
         L.dkv_get_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.dkv_decode_attend_noalloc.argtypes = [pdesc, vp, vp, i32, vp, vp, vp, vp]
         _lib = L
     return _lib
 

@@ -206,6 +206,33 @@ DKV_API int dkv_decode_combine(const dkv_desc* d, int32_t top_k, float* out, flo
                                void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * dkv_decode_attend without a workspace argument, for callers that cannot
+ * allocate device memory when they decode: runtimes that reserve a fixed
+ * memory pool at start-up and refuse later allocations, plugins that run
+ * inside another framework without access to its allocator, and serving
+ * loops that must not pay the device-wide synchronisation of cudaMalloc.
+ * The paper has no counterpart to this call; it only changes where the
+ * scratch memory comes from.
+ *
+ * The scratch (routed indices and partial results) lives in a fixed 8 MiB
+ * area compiled into the library; each GPU that loads the library keeps its
+ * own copy until the process exits.  A call whose scratch need
+ * (dkv_decode_workspace_bytes) is larger returns DKV_ERR_WORKSPACE and
+ * launches nothing.  The call itself allocates nothing.
+ *   - The first call on a device looks up that device's copy of the area;
+ *     make that first call before any stream capture on the device.
+ *   - Every call on a device shares the one area, which keeps the last
+ *     call's contents: calls that overlap on the GPU (on different streams,
+ *     or from different threads) race and corrupt each other's results.
+ *     Serialise them, for instance on one stream.
+ *   - The area's error word is cleared at the start of each call and cannot
+ *     be read back; use dkv_decode_attend with a workspace to diagnose.
+ * Other arguments, layouts and results are those of dkv_decode_attend.
+ */
+DKV_API int dkv_decode_attend_noalloc(const dkv_desc* d, const void* q, const void* cache, int32_t top_k,
+                                      float* out, float* lse, int32_t* routed, void* stream);
+
+/*
  * Dense fp16 decode attention over uncompressed K, V: the bytes/throughput
  * reference the compressed path is compared with.
  *   K, V   device fp16 [B][Hkv][T][head_dim]; T >= 1
