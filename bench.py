@@ -226,7 +226,8 @@ def main():
     ap.add_argument("--impl", choices=["dkv", "reference"], default="dkv")
     ap.add_argument("--config", default="64k")
     ap.add_argument("--top-k", type=int, default=None)
-    ap.add_argument("--layers", type=int, default=None, help="restrict to the first N layers (experiments only)")
+    ap.add_argument("--layers", type=int, default=None, help="restrict to N layers (experiments only)")
+    ap.add_argument("--layer-offset", type=int, default=0, help="first layer when --layers is given")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
@@ -241,9 +242,10 @@ def main():
     from compressed_kv_cache_dkv_gb300 import synth
     w = synth.WORKLOADS[args.config]
     top_k = w.top_k if args.top_k is None else args.top_k
-    n_layers = w.n_layers if args.layers is None else min(args.layers, w.n_layers)
+    n_layers = w.n_layers if args.layers is None else min(args.layers, w.n_layers - args.layer_offset)
+    layer_ids = [args.layer_offset + i for i in range(n_layers)] if args.layers is not None else list(range(n_layers))
     wl_name = (f"{w.name}: batch {w.batch}, {n_layers} layer(s) of {w.n_q_heads}q/{w.n_kv_heads}kv heads x d{w.head_dim}, "
-               f"{w.n_blocks} blocks of 256 + {w.window}-token window, r {sorted(set(w.ranks[:n_layers]))}, "
+               f"{w.n_blocks} blocks of 256 + {w.window}-token window, r {sorted(set(w.ranks[i] for i in layer_ids))}, "
                f"R {w.n_residual}, top-K {top_k}")
     queries_per_step = w.batch * w.n_q_heads * n_layers
 
@@ -281,15 +283,15 @@ def main():
     t_setup = time.perf_counter()
     descs, caches, qs, outs, lses = [], [], [], [], []
     ws_bytes = 0
-    for layer in range(n_layers):
+    for layer in layer_ids:
         d = dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window, w.rank(layer),
                            w.n_residual)
         ws_bytes = max(ws_bytes, dkv.dkv_decode_workspace_bytes(d, top_k))
         descs.append(d)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-    for layer in range(n_layers):
+    for i, layer in enumerate(layer_ids):
         K, V = synth.layer_kv_torch(w, layer, dev, replica=rank)
-        caches.append(dkv.dkv_compress_layout(descs[layer], K, V, workspace=ws))
+        caches.append(dkv.dkv_compress_layout(descs[i], K, V, workspace=ws))
         del K, V
         qs.append(torch.from_numpy(synth.queries(w, layer)).to(dev))
         outs.append(torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.float32, device=dev))
@@ -311,10 +313,10 @@ def main():
             dkv.dkv_decode_route(descs[layer], qs[layer], caches[layer], top_k, ws, stream=sh)
             if events is not None:
                 ext.record(events[layer][0], sh)
-            dkv.dkv_decode_blocks(descs[layer], qs[layer], caches[layer], top_k, ws, stream=sh)
+            dkv.dkv_decode_blocks(descs[layer], qs[layer], caches[layer], top_k, ws, out=outs[layer],
+                                  lse=lses[layer], stream=sh)
             if events is not None:
                 ext.record(events[layer][1], sh)
-            dkv.dkv_decode_combine(descs[layer], top_k, outs[layer], ws, lse=lses[layer], stream=sh)
 
     # ---------------- warm-up (eager), then capture K steps into one graph
     with torch.cuda.stream(stream):
@@ -386,8 +388,8 @@ def main():
     value = world * queries_per_step * K_steps / (ms / 1e3)
     e2e_value = world * queries_per_step * e2e_steps / (e2e_ms / 1e3)
 
-    step_bytes = sum(call_bytes(w, l, top_k) for l in range(n_layers))
-    att_bytes_step = sum(attend_bytes(w, l, top_k) for l in range(n_layers))
+    step_bytes = sum(call_bytes(w, l, top_k) for l in layer_ids)
+    att_bytes_step = sum(attend_bytes(w, l, top_k) for l in layer_ids)
     att_ms_mean = statistics.fmean(attend_ms)
     achieved_gbs = (att_bytes_step / n_layers) / (att_ms_mean / 1e3) / 1e9
     peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -415,14 +417,14 @@ def main():
         "hbm_frac_of_measured": step_bytes / (ms_step / 1e3) / 1e9 / peak,
         "hbm_frac_of_nominal_8tbs": step_bytes / (ms_step / 1e3) / 1e9 / 8000.0,
         "bytes_per_step": step_bytes,
-        "roofline": {"bound": "hbm", "kernel": "attend_kernel (block + window attention)", "achieved": achieved_gbs,
+        "roofline": {"bound": "hbm", "kernel": "attend_kernel (block + window attention, fused LSE merge)", "achieved": achieved_gbs,
                      "peak": peak, "unit": "GB/s", "frac": achieved_gbs / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
                      "bytes_per_launch": att_bytes_step / n_layers, "mean_launch_us": att_ms_mean * 1e3},
         "e2e": {"value": e2e_value, "unit": "queries/s", "steps": e2e_steps,
                 "h2d_bytes_per_step": sum(q.numel() * 2 for q in qs),
                 "d2h_bytes_per_step": sum(o.numel() * 4 for o in outs)},
-        "gpu_launches": K_steps * n_layers * 3,
+        "gpu_launches": K_steps * n_layers * (2 if w.n_blocks else 1),
         "clocks": clocks.summary(),
         "setup_s": t_setup,
     }

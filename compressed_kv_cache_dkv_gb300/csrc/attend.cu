@@ -44,6 +44,9 @@ struct AttendArgs {
   const int32_t* routed;
   float* partials;
   uint32_t* err;
+  uint32_t* counters;  // per-unit arrival counters (fused merge)
+  float* out;          // nullptr: partials only
+  float* lse;
 };
 
 struct Chunk {
@@ -564,6 +567,41 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
     int g = e / D, j = e % D;
     rec[16 + g * D + j] = ok ? obuf[j * 8 + g] : 0.f;
   }
+  if (a.out == nullptr) return;
+
+  // ---------------- fused split-LSE merge: the unit's last CTA to finish merges
+  // all of the unit's partials (arrival counter, no waiting on other CTAs)
+  __threadfence();
+  named_bar_sync(1, kConsumers * 32);
+  if (tid == 0) maskbuf[0] = atomicAdd(&a.counters[u], 1u) == (unsigned)(a.n_items - 1);
+  named_bar_sync(1, kConsumers * 32);
+  if (!maskbuf[0]) return;
+  __threadfence();
+  const size_t rs = 16 + 8 * (size_t)D;
+  const float* base = a.partials + (size_t)u * a.n_items * rs;
+  float* mstar = mbuf;          // [8] max of the unit's partials, per query of the group
+  float* linv = mbuf + 8;       // [8] 1 / merged normaliser
+  const size_t qrow0 = (size_t)bseq * a.Hq + (size_t)h * G;
+  if (tid < G) {
+    float m = -INFINITY;
+    for (int i = 0; i < a.n_items; ++i) m = fmaxf(m, __ldcg(base + i * rs + tid));
+    const float ms = m == -INFINITY ? 0.f : m;
+    float l = 0.f;
+    for (int i = 0; i < a.n_items; ++i) l += __ldcg(base + i * rs + 8 + tid) * exp2f(__ldcg(base + i * rs + tid) - ms);
+    mstar[tid] = ms;
+    linv[tid] = 1.f / l;
+    if (a.lse) a.lse[qrow0 + tid] = (ms + log2f(l)) * 0.6931471805599453f;
+  }
+  named_bar_sync(1, kConsumers * 32);
+  for (int e = tid; e < G * D; e += kConsumers * 32) {
+    const int g = e / D, j = e % D;
+    const float ms = mstar[g];
+    float acc = 0.f;
+    for (int i = 0; i < a.n_items; ++i)
+      acc = fmaf(exp2f(__ldcg(base + i * rs + g) - ms), __ldcg(base + i * rs + 16 + g * D + j), acc);
+    a.out[(qrow0 + g) * D + j] = acc * linv[g];
+  }
+  if (tid == 0) a.counters[u] = 0u;  // ready for the next call on this workspace
 }
 
 template <int D, int RT>
@@ -589,15 +627,17 @@ DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k
   P.wchunk_tokens = kWindowChunk;
   P.n_wchunks = (L.W16 + kWindowChunk - 1) / kWindowChunk;
   P.n_items = P.K_eff + P.n_wchunks;
-  P.off_routed = kWsHeader;
-  P.off_partials = round_up(kWsHeader + (size_t)L.units * P.K_eff * 4, 256);
+  P.route_splits = L.NB > 0 ? (L.NB + 63) / 64 : 0;
+  P.off_counters = kWsHeader;
+  P.off_bounds = round_up(P.off_counters + (size_t)L.units * 8, 256);
+  P.off_routed = round_up(P.off_bounds + (size_t)L.units * L.NB * 4, 256);
+  P.off_partials = round_up(P.off_routed + (size_t)L.units * P.K_eff * 4, 256);
   P.ws_bytes = P.off_partials + (size_t)L.units * P.n_items * (16 + 8 * L.d) * 4;
   return P;
 }
 
 cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
-                          const uint8_t* cache, const int32_t* routed, float* partials, uint32_t* err,
-                          cudaStream_t s) {
+                          const uint8_t* cache, uint8_t* ws, float* out, float* lse, cudaStream_t s) {
   AttendArgs a;
   a.L = L;
   a.G = n_q_heads / n_kv_heads;
@@ -624,9 +664,12 @@ cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, i
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)L.d);
   a.q = q;
   a.cache = cache;
-  a.routed = routed;
-  a.partials = partials;
-  a.err = err;
+  a.routed = reinterpret_cast<const int32_t*>(ws + P.off_routed);
+  a.partials = reinterpret_cast<float*>(ws + P.off_partials);
+  a.err = reinterpret_cast<uint32_t*>(ws);
+  a.counters = reinterpret_cast<uint32_t*>(ws + P.off_counters) + L.units;
+  a.out = out;
+  a.lse = lse;
   const size_t smem = (size_t)nslot * slot + extra;
   if (P.n_items == 0) return cudaSuccess;
   if (L.d == 128) {

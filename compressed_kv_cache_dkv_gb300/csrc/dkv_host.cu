@@ -161,8 +161,7 @@ struct DecodeCall {
   Layout L;
   DecodePlan P;
   cudaStream_t s;
-  uint32_t* err;
-  int32_t* ridx;
+  uint8_t* ws;
   float* parts;
 };
 
@@ -175,11 +174,9 @@ static int prep_decode(const dkv_desc* d, int32_t top_k, void* workspace, size_t
   if (!aligned16(workspace)) return DKV_ERR_ALIGN;
   c->P = plan_decode(c->L, d->n_q_heads, d->n_kv_heads, top_k);
   if (ws_bytes < c->P.ws_bytes) return DKV_ERR_WORKSPACE;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  c->ws = static_cast<uint8_t*>(workspace);
   c->s = static_cast<cudaStream_t>(stream);
-  c->err = reinterpret_cast<uint32_t*>(ws);
-  c->ridx = reinterpret_cast<int32_t*>(ws + c->P.off_routed);
-  c->parts = reinterpret_cast<float*>(ws + c->P.off_partials);
+  c->parts = reinterpret_cast<float*>(c->ws + c->P.off_partials);
   return DKV_OK;
 }
 
@@ -192,19 +189,20 @@ int dkv_decode_route(const dkv_desc* d, const void* q, const void* cache, int32_
   if (!aligned16(q) || !aligned16(cache) || (routed && !aligned16(routed))) return DKV_ERR_ALIGN;
   if (c.P.K_eff == 0) return DKV_OK;
   cudaError_t e = launch_route(c.L, c.P, d->n_q_heads, d->n_kv_heads, static_cast<const __half*>(q),
-                               static_cast<const uint8_t*>(cache), c.ridx, routed, c.s);
+                               static_cast<const uint8_t*>(cache), c.ws, routed, c.s);
   return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
 }
 
-int dkv_decode_blocks(const dkv_desc* d, const void* q, const void* cache, int32_t top_k, void* workspace,
-                      size_t ws_bytes, void* stream) {
+int dkv_decode_blocks(const dkv_desc* d, const void* q, const void* cache, int32_t top_k, float* out, float* lse,
+                      void* workspace, size_t ws_bytes, void* stream) {
   DecodeCall c;
   int st = prep_decode(d, top_k, workspace, ws_bytes, stream, &c);
   if (st != DKV_OK) return st;
-  if (!q || !cache) return DKV_ERR_ARG;
-  if (!aligned16(q) || !aligned16(cache)) return DKV_ERR_ALIGN;
+  if (!q || !cache || (!out && lse)) return DKV_ERR_ARG;
+  if (!aligned16(q) || !aligned16(cache) || (out && !aligned16(out)) || (lse && !aligned16(lse)))
+    return DKV_ERR_ALIGN;
   cudaError_t e = launch_attend(c.L, c.P, d->n_q_heads, d->n_kv_heads, static_cast<const __half*>(q),
-                                static_cast<const uint8_t*>(cache), c.ridx, c.parts, c.err, c.s);
+                                static_cast<const uint8_t*>(cache), c.ws, out, lse, c.s);
   return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
 }
 
@@ -231,9 +229,8 @@ int dkv_decode_attend(const dkv_desc* d, const void* q, const void* cache, int32
   const __half* qh = static_cast<const __half*>(q);
   const uint8_t* cc = static_cast<const uint8_t*>(cache);
   cudaError_t e = cudaSuccess;
-  if (c.P.K_eff > 0) e = launch_route(c.L, c.P, d->n_q_heads, d->n_kv_heads, qh, cc, c.ridx, routed, c.s);
-  if (e == cudaSuccess) e = launch_attend(c.L, c.P, d->n_q_heads, d->n_kv_heads, qh, cc, c.ridx, c.parts, c.err, c.s);
-  if (e == cudaSuccess) e = launch_combine(c.L, c.P, d->batch, d->n_q_heads, d->n_kv_heads, c.parts, out, lse, c.s);
+  if (c.P.K_eff > 0) e = launch_route(c.L, c.P, d->n_q_heads, d->n_kv_heads, qh, cc, c.ws, routed, c.s);
+  if (e == cudaSuccess) e = launch_attend(c.L, c.P, d->n_q_heads, d->n_kv_heads, qh, cc, c.ws, out, lse, c.s);
   return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
 }
 

@@ -225,16 +225,19 @@ cudaError_t launch_compress(const Layout& L, const __half* K, const __half* V, u
                             uint32_t* err, cudaStream_t s);
 size_t compress_ws_bytes(const Layout& L);
 
+// Decode workspace: [header 256 B][route counters, attend counters: u32 per unit]
+// [block scores: f32 per unit and block][routed: i32 per unit and slot][partials]
 struct DecodePlan {
-  int K_eff, n_wchunks, wchunk_tokens, n_items;
-  size_t off_routed, off_partials, ws_bytes;
+  int K_eff, n_wchunks, wchunk_tokens, n_items, route_splits;
+  size_t off_counters, off_bounds, off_routed, off_partials, ws_bytes;
 };
 DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k);
 cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
-                         const uint8_t* cache, int32_t* routed, int32_t* routed_out, cudaStream_t s);
+                         const uint8_t* cache, uint8_t* ws, int32_t* routed_out, cudaStream_t s);
+// out == nullptr: partials only (merge with launch_combine); otherwise the last
+// CTA of each unit merges the unit's partials into out (and lse)
 cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
-                          const uint8_t* cache, const int32_t* routed, float* partials, uint32_t* err,
-                          cudaStream_t s);
+                          const uint8_t* cache, uint8_t* ws, float* out, float* lse, cudaStream_t s);
 cudaError_t launch_combine(const Layout& L, const DecodePlan& P, int batch, int n_q_heads, int n_kv_heads,
                            const float* partials, float* out, float* lse, cudaStream_t s);
 

@@ -20,45 +20,89 @@ namespace dkv {
 
 namespace {
 
+constexpr int kRouteBlocks = 64;  // blocks scored per route CTA (8 warps x 8 blocks)
+
+// Scores the blocks [64*blockIdx.x, +64) of unit blockIdx.y into the workspace;
+// the last CTA of the unit to finish (arrival counter, no waiting) ranks all of
+// the unit's scores and writes the routed indices.
 __global__ void __launch_bounds__(256) route_kernel(Layout L, int G, int Hq, int Hkv, int K_eff, float cq,
                                                     const __half* __restrict__ q, const uint8_t* __restrict__ cache,
+                                                    float* __restrict__ bounds, uint32_t* __restrict__ counters,
                                                     int32_t* __restrict__ routed, int32_t* __restrict__ routed_out) {
-  extern __shared__ float sm[];
+  extern __shared__ float sm[];  // last CTA: scores [NB], selection flags [NB]
+  __shared__ float qbar[128];
+  __shared__ int s_last;
   const int d = L.d, NB = L.NB;
-  float* qbar = sm;               // [d]
-  float* bounds = sm + d;         // [NB]
-  int* sel = reinterpret_cast<int*>(bounds + NB);  // [NB]
-  const int u = blockIdx.x;
+  const int u = blockIdx.y, split = blockIdx.x, nsplit = gridDim.x;
   const int b = u / Hkv, h = u % Hkv;
   const int tid = threadIdx.x, nt = blockDim.x;
-  const int warp = tid >> 5, lane = tid & 31, nw = nt >> 5;
+  const int warp = tid >> 5, lane = tid & 31;
   for (int j = tid; j < d; j += nt) {
     float s = 0.f;
     for (int g = 0; g < G; ++g) s += __half2float(q[((size_t)b * Hq + (size_t)h * G + g) * d + j]);
     qbar[j] = s * cq;  // cq = c / G
   }
   __syncthreads();
-  const __half* router = reinterpret_cast<const __half*>(cache + (uint64_t)u * L.unit_stride + L.off_router);
-  for (int blk = warp; blk < NB; blk += nw) {
-    const __half* kmn = router + (size_t)blk * 2 * d;
-    const __half* kmx = kmn + d;
-    float acc = 0.f;
-    for (int j = lane; j < d; j += 32) {
-      float qj = qbar[j];
-      acc += fmaxf(qj * __half2float(kmx[j]), qj * __half2float(kmn[j]));
-    }
+  // A block's router record is [kmin | kmax], 4d bytes = d/4 pieces of 16 bytes.
+  // The warp's 8 blocks are contiguous: 2d pieces, 2d/32 per lane, all loaded first.
+  const uint8_t* router = cache + (uint64_t)u * L.unit_stride + L.off_router;
+  const int blk0 = split * kRouteBlocks + warp * 8;
+  const int per_blk = d / 4;                  // pieces per block (32 or 16)
+  const int npl = (2 * d) / 32;               // pieces per lane (8 or 4)
+  uint4 v[8];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) bounds[blk] = isnan(acc) ? -INFINITY : acc;
+  for (int i = 0; i < 8; ++i) {
+    v[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (i < npl) {
+      const int piece = i * 32 + lane;
+      const int blk = blk0 + piece / per_blk;
+      if (blk < NB) v[i] = *reinterpret_cast<const uint4*>(router + (size_t)blk0 * 4 * d + (size_t)piece * 16);
+    }
   }
+  const int half_pcs = d / 8;                 // kmin pieces per block; kmax partner at +d/8
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (i >= npl) break;
+    const int piece = i * 32 + lane;
+    const int q_in = piece % per_blk;
+    uint4 partner;
+    partner.x = __shfl_xor_sync(0xffffffffu, v[i].x, half_pcs);
+    partner.y = __shfl_xor_sync(0xffffffffu, v[i].y, half_pcs);
+    partner.z = __shfl_xor_sync(0xffffffffu, v[i].z, half_pcs);
+    partner.w = __shfl_xor_sync(0xffffffffu, v[i].w, half_pcs);
+    float acc = 0.f;
+    if (q_in < half_pcs) {
+      const __half* kmn = reinterpret_cast<const __half*>(&v[i]);
+      const __half* kmx = reinterpret_cast<const __half*>(&partner);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float qj = qbar[8 * q_in + e];
+        acc += fmaxf(qj * __half2float(kmx[e]), qj * __half2float(kmn[e]));
+      }
+    }
+    // sum over the per_blk lanes of this block (kmax lanes hold 0)
+    for (int o = per_blk >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    const int blk = blk0 + piece / per_blk;
+    if (q_in == 0 && blk < NB && blk < (split + 1) * kRouteBlocks)
+      bounds[(size_t)u * NB + blk] = isnan(acc) ? -INFINITY : acc;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&counters[u], 1u) == (unsigned)(nsplit - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  float* sc = sm;
+  int* sel = reinterpret_cast<int*>(sm + NB);
+  for (int i = tid; i < NB; i += nt) sc[i] = __ldcg(bounds + (size_t)u * NB + i);
   __syncthreads();
   for (int i = tid; i < NB; i += nt) {
     int s = 1;
     if (K_eff < NB) {
-      const float bi = bounds[i];
+      const float bi = sc[i];
       int rank = 0;
       for (int j = 0; j < NB; ++j) {
-        const float bj = bounds[j];
+        const float bj = sc[j];
         rank += (bj > bi) || (bj == bi && j < i);
       }
       s = rank < K_eff;
@@ -75,6 +119,7 @@ __global__ void __launch_bounds__(256) route_kernel(Layout L, int G, int Hq, int
       if (routed_out) routed_out[(size_t)u * K_eff + pos] = i;
     }
   }
+  if (tid == 0) counters[u] = 0u;  // ready for the next call on this workspace
 }
 
 __global__ void __launch_bounds__(128) combine_kernel(int n_items, int G, int Hq, int Hkv, int d,
@@ -101,17 +146,21 @@ __global__ void __launch_bounds__(128) combine_kernel(int n_items, int G, int Hq
 }  // namespace
 
 cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
-                         const uint8_t* cache, int32_t* routed, int32_t* routed_out, cudaStream_t s) {
+                         const uint8_t* cache, uint8_t* ws, int32_t* routed_out, cudaStream_t s) {
   const int G = n_q_heads / n_kv_heads;
   const float cq = 1.f / (sqrtf((float)L.d) * (float)G);
-  const size_t smem = (size_t)L.d * 4 + (size_t)L.NB * 8;
+  const size_t smem = (size_t)L.NB * 8;
   static size_t configured = 48 * 1024;
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  route_kernel<<<L.units, 256, smem, s>>>(L, G, n_q_heads, n_kv_heads, P.K_eff, cq, q, cache, routed, routed_out);
+  dim3 grid(P.route_splits, L.units);
+  route_kernel<<<grid, 256, smem, s>>>(L, G, n_q_heads, n_kv_heads, P.K_eff, cq, q, cache,
+                                       reinterpret_cast<float*>(ws + P.off_bounds),
+                                       reinterpret_cast<uint32_t*>(ws + P.off_counters),
+                                       reinterpret_cast<int32_t*>(ws + P.off_routed), routed_out);
   return cudaGetLastError();
 }
 

@@ -91,7 +91,7 @@ def lib() -> ctypes.CDLL:
         L.dkv_decode_workspace_bytes.argtypes = [pdesc, i32]
         L.dkv_decode_attend.argtypes = [pdesc, vp, vp, i32, vp, vp, vp, vp, sz, vp]
         L.dkv_decode_route.argtypes = [pdesc, vp, vp, i32, vp, vp, sz, vp]
-        L.dkv_decode_blocks.argtypes = [pdesc, vp, vp, i32, vp, sz, vp]
+        L.dkv_decode_blocks.argtypes = [pdesc, vp, vp, i32, vp, vp, vp, sz, vp]
         L.dkv_decode_combine.argtypes = [pdesc, i32, vp, vp, vp, sz, vp]
         L.dkv_dense_workspace_bytes.restype = sz
         L.dkv_dense_workspace_bytes.argtypes = [i32] * 5
@@ -204,9 +204,9 @@ def dkv_decode_route(d: dkv_desc, q, cache, top_k: int, workspace, routed=None, 
                                   workspace.numel(), _stream(stream)), "dkv_decode_route")
 
 
-def dkv_decode_blocks(d: dkv_desc, q, cache, top_k: int, workspace, stream=None) -> None:
-    _check(lib().dkv_decode_blocks(ctypes.byref(d), _ptr(q), _ptr(cache), int(top_k), _ptr(workspace),
-                                   workspace.numel(), _stream(stream)), "dkv_decode_blocks")
+def dkv_decode_blocks(d: dkv_desc, q, cache, top_k: int, workspace, out=None, lse=None, stream=None) -> None:
+    _check(lib().dkv_decode_blocks(ctypes.byref(d), _ptr(q), _ptr(cache), int(top_k), _ptr(out), _ptr(lse),
+                                   _ptr(workspace), workspace.numel(), _stream(stream)), "dkv_decode_blocks")
 
 
 def dkv_decode_combine(d: dkv_desc, top_k: int, out, workspace, lse=None, stream=None) -> None:

@@ -180,7 +180,9 @@ DKV_API int dkv_import_factors(const dkv_desc* d, const dkv_factors* f, void* ca
  *   lse     optional device fp32 [B][Hq]: natural-log log-sum-exp of the scores
  *   routed  optional device int32 [B][Hkv][K_eff]: routed block indices,
  *           ascending, K_eff = top_k clipped to n_blocks
- *   workspace / ws_bytes  device scratch of dkv_decode_workspace_bytes(d, top_k)
+ *   workspace / ws_bytes  device scratch of dkv_decode_workspace_bytes(d, top_k);
+ *           zero-fill it once before its first use: it holds per-unit arrival
+ *           counters that every call leaves at zero again
  * Routing: qbar = mean over the group of c*q; block score
  * sum_j max(qbar_j kmax_bj, qbar_j kmin_bj); top-K by (score desc, index asc).
  */
@@ -190,18 +192,22 @@ DKV_API int dkv_decode_attend(const dkv_desc* d, const void* q, const void* cach
                       void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * The three stages of dkv_decode_attend as separate calls, for callers that
- * schedule or time them individually.  Run in this order on one stream with
- * one workspace (it carries the routed indices and the partial results from
- * stage to stage); arguments mean the same as for dkv_decode_attend.
- *   route:   top-K block selection per unit (skipped when n_blocks == 0)
- *   blocks:  one partial (m, l, acc) per routed block and per window chunk
+ * The stages of dkv_decode_attend as separate calls, for callers that
+ * schedule or time them individually.  Run them in this order on one stream
+ * with one workspace (it carries the routed indices and the partial results
+ * from stage to stage); arguments mean the same as for dkv_decode_attend.
+ *   route:   top-K block selection per unit (does nothing when n_blocks == 0)
+ *   blocks:  one partial (m, l, acc) per routed block and per window chunk;
+ *            when `out` is given, the last CTA of each unit also merges the
+ *            unit's partials into out (and lse), which is what
+ *            dkv_decode_attend does; with out == NULL (and lse == NULL) the
+ *            partials stay in the workspace for dkv_decode_combine
  *   combine: fp32 log-sum-exp merge of the partials into out (and lse)
  */
 DKV_API int dkv_decode_route(const dkv_desc* d, const void* q, const void* cache, int32_t top_k, int32_t* routed,
                              void* workspace, size_t ws_bytes, void* stream);
 DKV_API int dkv_decode_blocks(const dkv_desc* d, const void* q, const void* cache, int32_t top_k,
-                              void* workspace, size_t ws_bytes, void* stream);
+                              float* out, float* lse, void* workspace, size_t ws_bytes, void* stream);
 DKV_API int dkv_decode_combine(const dkv_desc* d, int32_t top_k, float* out, float* lse,
                                void* workspace, size_t ws_bytes, void* stream);
 

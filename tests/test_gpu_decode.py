@@ -173,3 +173,30 @@ def test_decode_is_deterministic_and_stream_ordered():
     s.synchronize()
     for x in a[1:]:
         assert torch.equal(x, a[0])
+
+
+def test_stage_calls_equal_the_fused_call_and_reuse_the_workspace():
+    """route -> blocks (partials only) -> combine equals dkv_decode_attend (merge
+    fused into the attention kernel); one workspace serves many calls of
+    different top-K values, since every call leaves its arrival counters at zero."""
+    w = synth.WORKLOADS["8k"]
+    units = H.oracle_units(w, 0, [(0, 0), (0, 1)])
+    desc = dkv.dkv_layout(1, 12, 2, 128, w.n_blocks, w.window, 32, 40)
+    cache = dkv.dkv_import_factors(desc, H.to_device(H.factor_arrays(units, 128, 32, 40, w.window)))
+    q = torch.from_numpy(synth.queries(w, 0)).cuda()
+    ws = torch.zeros(dkv.dkv_decode_workspace_bytes(desc, 0), dtype=torch.uint8, device="cuda")
+    for top_k in (8, 3, 0, 8, 30, 1):
+        fused, fl, fr = dkv.dkv_decode_attend(desc, q, cache, top_k, workspace=ws)
+        k_eff = w.n_blocks if top_k in (0, w.n_blocks) else top_k
+        routed = torch.empty(1, 2, k_eff, dtype=torch.int32, device="cuda")
+        dkv.dkv_decode_route(desc, q, cache, top_k, ws, routed=routed)
+        dkv.dkv_decode_blocks(desc, q, cache, top_k, ws)
+        out = torch.empty_like(fused)
+        lse = torch.empty_like(fl)
+        dkv.dkv_decode_combine(desc, top_k, out, ws, lse=lse)
+        torch.cuda.synchronize()
+        assert torch.equal(routed, fr)
+        assert (out - fused).abs().max().item() <= 1e-5
+        assert (lse - fl).abs().max().item() <= 1e-5
+    st, word = dkv.dkv_get_error(ws)
+    assert st == dkv.DKV_OK and word == 0
