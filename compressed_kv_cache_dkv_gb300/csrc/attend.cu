@@ -1,12 +1,15 @@
-// Block + window attention of the DKV decode path.
+// Block + window attention of the DKV decode path (persistent kernel).
 //
-// One CTA per work item of a unit (a routed block, or a chunk of the exact
-// recency window).  Warp 4 is the producer: its lane 0 streams the item's
-// packed bytes, chunk by chunk, into a ring of shared-memory slots with 1-D
-// TMA bulk copies (cp.async.bulk + mbarrier complete_tx).  Warps 0-3 are the
+// Work items of one call: every (unit, routed block) and every (unit, chunk of
+// the exact recency window).  A fixed grid of about two CTAs per SM takes
+// items one after the other (the first statically, the rest from an atomic
+// counter).  Warp 4 is the producer: its lane 0 decodes items and streams their
+// packed bytes, chunk by chunk, into a ring of shared-memory slots with 1-D TMA
+// bulk copies (cp.async.bulk + mbarrier complete_tx), running ahead into the
+// next item while the consumers finish the current one.  Warps 0-3 are the
 // consumers; every matrix product runs on the tensor cores through
-// mma.sync m16n8k16 / m16n8k8 (fp16 operands, fp32 accumulate) with the
-// tokens (or the head dimension) in M and the GQA group in N = 8.
+// mma.sync m16n8k16 / m16n8k8 (fp16 operands, fp32 accumulate) with the tokens
+// (or the head dimension) in M and the GQA group in N = 8.
 //
 // Per routed block ("Low-Rank Space Query Scoring" / "Flash-Style LSE
 // Combine", Differential-KV README, section "Core Architecture & Paper
@@ -16,10 +19,11 @@
 //   s_i   = c q_g . a_k + U_i . z_g,  i not in S (K is never materialised)
 //   s_j   = c q_g . k_j,              j in S     (exact residual rows)
 //   acc_g = (sum_lowrank p) a_v + (sum_lowrank p_i U_i) V_V + sum_S p_j v_j
-// emitted as a partial (m, l, acc) in base-2 units; the combine kernel merges
-// partials with an fp32 log-sum-exp reduction.  Scores are kept in fp32; the
-// fp32 operands of a product (z, p, w) are split into an fp16 pair hi + lo so
-// the tensor-core products carry about 22 bits.
+// emitted as a partial (m, l, acc) in base-2 units.  The last CTA to finish an
+// item of a unit merges the unit's partials with an fp32 log-sum-exp
+// reduction.  Scores are kept in fp32; the fp32 operands of a product (z, p,
+// w) are split into an fp16 pair hi + lo so the tensor-core products carry
+// about 22 bits.
 #include <float.h>
 #include <math.h>
 
@@ -34,19 +38,30 @@ constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kUTok = 64;              // U rows per chunk
 constexpr int kWindowChunk = 256;      // window tokens per work item
 constexpr int kMaxSlots = 8;
+constexpr int kIQ = 2;                 // item descriptors in flight between producer and consumers
 
 struct AttendArgs {
   Layout L;
-  int G, Hq, Hkv, K_eff, n_items, nslot, slot_bytes, xtok;
+  int G, Hq, Hkv, K_eff, n_items, n_wchunks, total, nslot, slot_bytes, xtok;
   float scale_log2;  // log2(e) / sqrt(d)
   const __half* q;
   const uint8_t* cache;
   const int32_t* routed;
   float* partials;
   uint32_t* err;
-  uint32_t* counters;  // per-unit arrival counters (fused merge)
-  float* out;          // nullptr: partials only
-  float* lse;
+  uint32_t* sched;     // [0] next dynamic item, [1] CTAs done fetching
+};
+
+// One work item, as decoded by the producer and handed to the consumers.
+struct ItemDesc {
+  int stop;              // no more items for this CTA
+  int is_block;
+  int ok;                // routed index in range
+  int u, item;           // unit, item index inside the unit's partials
+  int n_chunks, n_u, n_x;
+  int tok0, ntok, nvalid;
+  uint32_t k0;           // global ring index of the item's first chunk
+  uint64_t base;         // block record or window offset (bytes from the cache base)
 };
 
 struct Chunk {
@@ -57,48 +72,82 @@ struct Chunk {
   int ntok;       // stored tokens in the chunk (multiple of 8)
 };
 
-struct ItemInfo {
-  bool is_block;
-  int n_chunks;
-  int n_u, n_x;          // U chunks and exact chunks
-  uint64_t base;         // block record or window offset
-  int tok0, ntok;        // window: first stored token and stored tokens of the item
-  int nvalid;            // exact tokens that are real (R for residuals, W for the window)
-};
-
-__device__ inline Chunk item_chunk(const AttendArgs& a, const ItemInfo& it, int k) {
+__device__ inline Chunk item_chunk(const AttendArgs& a, const ItemDesc& it, int k) {
   const Layout& L = a.L;
   Chunk c;
   if (it.is_block) {
     if (k == 0) {
       c.src = it.base; c.bytes = (uint32_t)L.off_u; c.kind = 0; c.tok0 = 0; c.ntok = 0;
     } else if (k <= it.n_u) {
-      int t0 = (k - 1) * kUTok;
+      const int t0 = (k - 1) * kUTok;
       c.src = it.base + L.off_u + (uint64_t)t0 * 2 * L.r8;
       c.bytes = (uint32_t)(kUTok * 2 * L.r8); c.kind = 1; c.tok0 = t0; c.ntok = kUTok;
     } else if (k <= it.n_u + it.n_x) {
-      int t0 = (k - 1 - it.n_u) * a.xtok;
-      int n = min(a.xtok, L.R8 - t0);
+      const int t0 = (k - 1 - it.n_u) * a.xtok;
+      const int n = min(a.xtok, L.R8 - t0);
       c.src = it.base + L.off_res + (uint64_t)t0 * 4 * L.d;
       c.bytes = (uint32_t)(n * 4 * L.d); c.kind = 2; c.tok0 = t0; c.ntok = n;
     } else {
       c.src = it.base + L.off_vv; c.bytes = (uint32_t)(2 * L.r8 * L.d); c.kind = 3; c.tok0 = 0; c.ntok = 0;
     }
   } else {
-    int t0 = it.tok0 + k * a.xtok;
-    int n = min(a.xtok, it.tok0 + it.ntok - t0);
+    const int t0 = it.tok0 + k * a.xtok;
+    const int n = min(a.xtok, it.tok0 + it.ntok - t0);
     c.src = it.base + (uint64_t)t0 * 4 * L.d;
     c.bytes = (uint32_t)(n * 4 * L.d); c.kind = 2; c.tok0 = t0; c.ntok = n;
   }
   return c;
 }
 
-__device__ inline int chunk_owner(const ItemInfo& it, int k) {
+__device__ inline int chunk_owner(const ItemDesc& it, int k) {
   if (it.is_block) {
     if (k == 0 || k == it.n_chunks - 1) return -1;  // all consumer warps
     return (k - 1) % kConsumers;
   }
   return k % kConsumers;
+}
+
+// Global item index -> item.  Window chunks come first (they need nothing from
+// the router, so they overlap its grid), then the routed blocks; consecutive
+// indices belong to different units.
+__device__ inline ItemDesc decode_item(const AttendArgs& a, int gi) {
+  const Layout& L = a.L;
+  ItemDesc it;
+  it.stop = 0;
+  it.ok = 1;
+  const int nwin = a.n_wchunks * L.units;
+  const uint64_t unit_stride = L.unit_stride;
+  if (gi < nwin) {
+    const int wc = gi / L.units;
+    it.u = gi % L.units;
+    it.item = a.K_eff + wc;
+    it.is_block = 0;
+    it.n_u = 0;
+    it.tok0 = wc * kWindowChunk;
+    it.ntok = min(kWindowChunk, L.W16 - it.tok0);
+    it.n_x = (it.ntok + a.xtok - 1) / a.xtok;
+    it.n_chunks = it.n_x;
+    it.base = (uint64_t)it.u * unit_stride + L.off_window;
+    it.nvalid = L.W;
+  } else {
+    const int bi = gi - nwin;
+    const int slot = bi / L.units;
+    it.u = bi % L.units;
+    it.item = slot;
+    int blk = a.routed[it.u * a.K_eff + slot];
+    if (blk < 0 || blk >= L.NB) {
+      it.ok = 0;
+      raise_error(a.err, DKV_DEVERR_INDEX);
+      blk = 0;
+    }
+    it.is_block = 1;
+    it.n_u = 256 / kUTok;
+    it.n_x = (L.R8 + a.xtok - 1) / a.xtok;
+    it.n_chunks = 1 + it.n_u + it.n_x + 1;
+    it.base = (uint64_t)it.u * unit_stride + L.off_blocks + (uint64_t)blk * L.block_stride;
+    it.tok0 = 0; it.ntok = 0; it.nvalid = L.R;
+  }
+  return it;
 }
 
 __device__ inline float warp_max_rows(float v) {  // max over lanes with the same lane%4
@@ -122,34 +171,48 @@ __device__ inline float pow2_down(float mx) {
   return ldexpf(1.f, 14 - e);
 }
 
-// Online-softmax state of one consumer warp, columns g = 2t, 2t+1 of the C fragment.
-template <int D, int RT>
-struct WarpState {
-  float m[2], l[2], pa[2];
-  float w[RT][4];
-  float o[D / 16][4];
+// Position in the ring of chunk slots.  Every consumer warp and the producer
+// walk the chunks of all items in the same order, so each keeps its own cursor.
+struct Ring {
+  int slot;
+  uint32_t use;  // how many times the slot ring has wrapped (parity = use & 1)
+  __device__ inline void next(int nslot) {
+    if (++slot == nslot) { slot = 0; ++use; }
+  }
 };
 
-template <int D, int RT>
-__device__ inline void rescale(WarpState<D, RT>& st, const float (&s)[4], float (&p)[4], bool gv0, bool gv1) {
-  float mx0 = warp_max_rows(fmaxf(s[0], s[2]));
-  float mx1 = warp_max_rows(fmaxf(s[1], s[3]));
-  float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
-  float ms0 = (mn0 == -INFINITY) ? 0.f : mn0;
-  float ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
-  float sc0 = exp2f(st.m[0] - ms0), sc1 = exp2f(st.m[1] - ms1);  // exp2(-inf) = 0
-  p[0] = gv0 ? exp2f(s[0] - ms0) : 0.f;
-  p[1] = gv1 ? exp2f(s[1] - ms1) : 0.f;
-  p[2] = gv0 ? exp2f(s[2] - ms0) : 0.f;
-  p[3] = gv1 ? exp2f(s[3] - ms1) : 0.f;
+// Online-softmax statistics of one consumer warp for the two C-fragment
+// columns it owns (g = 2t, 2t+1): running max m (base 2) and normaliser l.
+struct Stat {
+  float m[2], l[2];
+};
+
+__device__ inline void tile_max(const float (&s)[4], float& mx0, float& mx1) {
+  mx0 = fmaxf(mx0, fmaxf(s[0], s[2]));
+  mx1 = fmaxf(mx1, fmaxf(s[1], s[3]));
+}
+
+// Move the running maximum to include (mx0, mx1); returns the factors that
+// rescale everything accumulated so far, and the subtrahends for the new p.
+__device__ inline void stat_update(Stat& st, float mx0, float mx1, float& sc0, float& sc1, float& ms0, float& ms1) {
+  mx0 = warp_max_rows(mx0);
+  mx1 = warp_max_rows(mx1);
+  const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+  ms0 = (mn0 == -INFINITY) ? 0.f : mn0;
+  ms1 = (mn1 == -INFINITY) ? 0.f : mn1;
+  sc0 = fast_exp2(st.m[0] - ms0);  // 2^(-inf) = 0
+  sc1 = fast_exp2(st.m[1] - ms1);
   st.m[0] = mn0;
   st.m[1] = mn1;
-  st.l[0] *= sc0; st.l[1] *= sc1;
-  st.pa[0] *= sc0; st.pa[1] *= sc1;
-#pragma unroll
-  for (int i = 0; i < RT; ++i) { st.w[i][0] *= sc0; st.w[i][1] *= sc1; st.w[i][2] *= sc0; st.w[i][3] *= sc1; }
-#pragma unroll
-  for (int i = 0; i < D / 16; ++i) { st.o[i][0] *= sc0; st.o[i][1] *= sc1; st.o[i][2] *= sc0; st.o[i][3] *= sc1; }
+  st.l[0] *= sc0;
+  st.l[1] *= sc1;
+}
+
+__device__ inline void probs(const float (&s)[4], float ms0, float ms1, bool gv0, bool gv1, float (&p)[4], Stat& st) {
+  p[0] = gv0 ? fast_exp2(s[0] - ms0) : 0.f;
+  p[1] = gv1 ? fast_exp2(s[1] - ms1) : 0.f;
+  p[2] = gv0 ? fast_exp2(s[2] - ms0) : 0.f;
+  p[3] = gv1 ? fast_exp2(s[3] - ms1) : 0.f;
   st.l[0] += p[0] + p[2];
   st.l[1] += p[1] + p[3];
 }
@@ -163,165 +226,158 @@ __device__ inline void p_to_b(const float (&p)[4], uint32_t& bh0, uint32_t& bl0,
   bh1 = movtrans(h23); bl1 = movtrans(l23);
 }
 
+// shared-memory carve-up (the host computes the same sizes in launch_attend)
+struct Smem {
+  uint8_t* slots;
+  uint64_t *full, *empty, *iq_full, *iq_empty;
+  ItemDesc* iqd;
+  __half* qbuf;      // [kIQ][8][D + 8] the item's query rows (padded rows)
+  float2* zbuf;      // [RT*2][32] z^T C fragments, one n-tile per warp in turn
+  float* obw;        // [4][D][8]  per-warp exact-token accumulators, merged in place
+  float* wbw;        // [4][RT*16][8] per-warp low-rank w, merged in place
+  float* basebuf;    // [4][8]
+  float* stat;       // [4 warps][4][8]
+  float* fin;        // [12][8] merged statistics and per-warp scales
+  uint32_t* maskbuf; // [8]
+  int* flag;         // [4]
+  __half* av;        // [D]
+};
+
 template <int D, int RT>
-__global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__device__ inline Smem carve(uint8_t* smem, const AttendArgs& a) {
+  Smem s;
+  s.slots = smem;
+  uint8_t* p = smem + (size_t)a.nslot * a.slot_bytes;
+  s.full = reinterpret_cast<uint64_t*>(p);
+  s.empty = s.full + kMaxSlots;
+  s.iq_full = s.empty + kMaxSlots;
+  s.iq_empty = s.iq_full + kIQ;
+  s.iqd = reinterpret_cast<ItemDesc*>(s.iq_empty + kIQ);
+  s.qbuf = reinterpret_cast<__half*>((reinterpret_cast<uintptr_t>(s.iqd + kIQ) + 15) & ~uintptr_t(15));
+  s.zbuf = reinterpret_cast<float2*>(s.qbuf + kIQ * 8 * (D + 8));
+  s.obw = reinterpret_cast<float*>(s.zbuf + RT * 2 * 32);
+  s.wbw = s.obw + kConsumers * D * 8;
+  s.basebuf = s.wbw + kConsumers * RT * 16 * 8;
+  s.stat = s.basebuf + 32;
+  s.fin = s.stat + 128;
+  s.maskbuf = reinterpret_cast<uint32_t*>(s.fin + 96);
+  s.flag = reinterpret_cast<int*>(s.maskbuf + 8);
+  s.av = reinterpret_cast<__half*>(s.flag + 4);
+  return s;
+}
+
+template <int D, int RT>
+__host__ __device__ inline size_t smem_extra() {
+  return 4 * kMaxSlots * 8 + kIQ * sizeof(ItemDesc) + 16 + (size_t)kIQ * 8 * (D + 8) * 2 + (size_t)RT * 2 * 32 * 8 +
+         (size_t)kConsumers * D * 8 * 4 +
+         (size_t)kConsumers * RT * 16 * 8 * 4 + (32 + 128 + 96) * 4 + 32 + 16 + (size_t)D * 2 + 128;
+}
+
+// ---------------------------------------------------------------------------
+// consumers: one item
+// ---------------------------------------------------------------------------
+template <int D, int RT>
+__device__ inline void consume_item(const AttendArgs& a, const Smem& sm, const ItemDesc& it, Ring& rc,
+                                    const uint32_t (&qb)[D / 16][2]) {
   const Layout& L = a.L;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = lane & 3, gq = lane >> 2;
-  const int u = blockIdx.y, item = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int u = it.u;
   const int bseq = u / a.Hkv, h = u % a.Hkv;
   const int r8 = L.r8;
   const int nkk = r8 >> 4;                 // full 16-wide k tiles of r
   const bool rtail = (r8 & 15) != 0;       // one 8-wide tail
   const int nrt = nkk + (rtail ? 1 : 0);   // r tiles
-
-  // ---- shared memory carve-up
-  uint8_t* slots = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.nslot * a.slot_bytes);
-  uint64_t* empty = full + kMaxSlots;
-  float2* zbuf = reinterpret_cast<float2*>(empty + kMaxSlots);          // [r8/8][32]
-  float* wbuf = reinterpret_cast<float*>(zbuf + (RT * 2) * 32);         // [RT*16][8]
-  float* obuf = wbuf + RT * 16 * 8;                                     // [D][8]
-  float* mbuf = obuf + D * 8;                                           // [4][8]
-  float* lbuf = mbuf + 32;
-  float* pabuf = lbuf + 32;
-  uint32_t* maskbuf = reinterpret_cast<uint32_t*>(pabuf + 32);         // [8] residual mask bits
-  __half* av = reinterpret_cast<__half*>(maskbuf + 8);                  // [D]
-
-  // ---- work item
-  ItemInfo it;
-  uint64_t unit_base = (uint64_t)u * L.unit_stride;
-  bool item_ok = true;
-  if (item < a.K_eff) {
-    int blk = a.routed[u * a.K_eff + item];
-    if (blk < 0 || blk >= L.NB) {
-      item_ok = false;
-      if (threadIdx.x == 0) raise_error(a.err, DKV_DEVERR_INDEX);
-      blk = 0;
-    }
-    it.is_block = true;
-    it.n_u = L.r8 > 0 ? 256 / kUTok : 256 / kUTok;
-    it.n_x = (L.R8 + a.xtok - 1) / a.xtok;
-    it.n_chunks = 1 + it.n_u + it.n_x + 1;
-    it.base = unit_base + L.off_blocks + (uint64_t)blk * L.block_stride;
-    it.tok0 = 0; it.ntok = 0; it.nvalid = L.R;
-  } else {
-    int wc = item - a.K_eff;
-    it.is_block = false;
-    it.n_u = 0;
-    it.tok0 = wc * kWindowChunk;
-    it.ntok = min(kWindowChunk, L.W16 - it.tok0);
-    it.n_x = (it.ntok + a.xtok - 1) / a.xtok;
-    it.n_chunks = it.n_x;
-    it.base = unit_base + L.off_window;
-    it.nvalid = L.W;
-  }
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < a.nslot; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], 1); }
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  // =========================== producer warp
-  if (warp == kConsumers) {
-    if (lane == 0 && item_ok) {
-      const uint64_t pol = policy_evict_first();
-      for (int k = 0; k < it.n_chunks; ++k) {
-        int slot = k % a.nslot;
-        if (k >= a.nslot && !mbar_wait(&empty[slot], ((k / a.nslot) - 1) & 1, a.err)) break;
-        Chunk c = item_chunk(a, it, k);
-        if (c.bytes) {
-          mbar_arrive_expect_tx(&full[slot], c.bytes);
-          bulk_g2s(slots + (size_t)slot * a.slot_bytes, a.cache + c.src, c.bytes, &full[slot], pol);
-        } else {
-          mbar_arrive(&full[slot]);
-        }
-      }
-    }
-    return;
-  }
-
-  // =========================== consumer warps
+  constexpr int KT = D / 16;               // 16-wide k tiles of the head dimension
   const int G = a.G;
   const bool gv0 = (2 * t) < G, gv1 = (2 * t + 1) < G;
-  // q as B fragments (k = head dim, n = group): q[gq][16kt + 2t, +1] and [16kt + 8 + 2t, +1]
-  uint32_t qb[D / 16][2];
-  {
-    const __half* qrow = a.q + ((size_t)bseq * a.Hq + (size_t)h * G + (gq < G ? gq : 0)) * D;
+  const float slog2 = a.scale_log2;
+  const uint32_t slot0 = smem_u32(sm.slots);
+  (void)bseq;
+  (void)h;
+  // low-rank state (its normaliser is the sum of p over the low-rank tokens, anchor included)
+  Stat sL;
+  sL.m[0] = sL.m[1] = -INFINITY;
+  sL.l[0] = sL.l[1] = 0.f;
+  float w[RT][4];
 #pragma unroll
-    for (int kt = 0; kt < D / 16; ++kt) {
-      uint32_t x0 = *reinterpret_cast<const uint32_t*>(qrow + 16 * kt + 2 * t);
-      uint32_t x1 = *reinterpret_cast<const uint32_t*>(qrow + 16 * kt + 8 + 2 * t);
-      qb[kt][0] = gq < G ? x0 : 0u;
-      qb[kt][1] = gq < G ? x1 : 0u;
-    }
-  }
-  WarpState<D, RT> st;
-  st.m[0] = st.m[1] = -INFINITY;
-  st.l[0] = st.l[1] = st.pa[0] = st.pa[1] = 0.f;
+  for (int i = 0; i < RT; ++i) w[i][0] = w[i][1] = w[i][2] = w[i][3] = 0.f;
+  // exact-token state (residual rows or window tokens)
+  Stat sX;
+  sX.m[0] = sX.m[1] = -INFINITY;
+  sX.l[0] = sX.l[1] = 0.f;
+  float o[KT][4];
 #pragma unroll
-  for (int i = 0; i < RT; ++i) st.w[i][0] = st.w[i][1] = st.w[i][2] = st.w[i][3] = 0.f;
-#pragma unroll
-  for (int i = 0; i < D / 16; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+  for (int i = 0; i < KT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-  bool ok = item_ok;
+  bool ok = it.ok != 0;
   float base0 = 0.f, base1 = 0.f;       // c q_g . a_k in base-2 units, columns 2t, 2t+1
   float us0 = 1.f, us1 = 1.f;           // power-of-two unscale of z, columns 2t, 2t+1
   uint32_t zh[RT][2], zl[RT][2];        // z as B fragments (k = r, n = group), hi and lo
-  const uint32_t slot0 = smem_u32(slots);
 
   if (it.is_block) {
     // ---------------- head chunk: anchors, residual mask, V_K -> base and z
-    ok = ok && mbar_wait(&full[0], 0, a.err);
-    const __half* ak = reinterpret_cast<const __half*>(slots);
-    float part = 0.f;
+    const int hs = rc.slot;
+    ok = mbar_wait(&sm.full[hs], rc.use & 1u, a.err) && ok;
+    rc.next(a.nslot);
+    const uint8_t* head = sm.slots + (size_t)hs * a.slot_bytes;
+    {
+      // q . a_k: the warps split the head dimension, partial sums meet in shared memory
+      const __half* ak = reinterpret_cast<const __half*>(head);
+      constexpr int KPW = KT / kConsumers > 0 ? KT / kConsumers : 1;
+      float part = 0.f;
 #pragma unroll
-    for (int kt = 0; kt < D / 16; ++kt) {
-      __half2 q0 = *reinterpret_cast<__half2*>(&qb[kt][0]);
-      __half2 q1 = *reinterpret_cast<__half2*>(&qb[kt][1]);
-      float2 qf0 = __half22float2(q0), qf1 = __half22float2(q1);
-      int j0 = 16 * kt + 2 * t, j1 = j0 + 8;
-      part += qf0.x * __half2float(ak[j0]) + qf0.y * __half2float(ak[j0 + 1]);
-      part += qf1.x * __half2float(ak[j1]) + qf1.y * __half2float(ak[j1 + 1]);
+      for (int i = 0; i < KPW; ++i) {
+        const int kt = warp * KPW + i;
+        if (kt < KT) {
+          const float2 qf0 = __half22float2(*reinterpret_cast<const __half2*>(&qb[kt][0]));
+          const float2 qf1 = __half22float2(*reinterpret_cast<const __half2*>(&qb[kt][1]));
+          const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(ak + 16 * kt + 2 * t));
+          const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(ak + 16 * kt + 8 + 2 * t));
+          part += qf0.x * a0.x + qf0.y * a0.y + qf1.x * a1.x + qf1.y * a1.y;
+        }
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      if (t == 0) sm.basebuf[warp * 8 + gq] = part;
     }
-    part += __shfl_xor_sync(0xffffffffu, part, 1);
-    part += __shfl_xor_sync(0xffffffffu, part, 2);
-    part *= a.scale_log2;  // base for g = gq
-    base0 = __shfl_sync(0xffffffffu, part, 8 * t);
-    base1 = __shfl_sync(0xffffffffu, part, 8 * t + 4);
     if (warp == 0) {
-      for (int j = lane; j < D; j += 32) av[j] = reinterpret_cast<const __half*>(slots)[D + j];
-      if (lane < 8) maskbuf[lane] = reinterpret_cast<const uint32_t*>(slots + L.off_mask)[lane];
+      for (int j = lane; j < D; j += 32) sm.av[j] = reinterpret_cast<const __half*>(head)[D + j];
+      if (lane < 8) sm.maskbuf[lane] = reinterpret_cast<const uint32_t*>(head + L.off_mask)[lane];
     }
-    // z^T = q^T V_K^T : n-tiles of 8 r-rows split across warps
-    const uint32_t vk = slot0 + (uint32_t)L.off_vk;
+    // z^T = q^T V_K^T : n-tiles of 8 r-rows split across warps, shared through zbuf
+    const uint32_t vk = smem_u32(head) + (uint32_t)L.off_vk;
     for (int nt = warp; nt < (r8 >> 3); nt += kConsumers) {
       float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kp = 0; kp < D / 32; ++kp) {
-        uint4 b = lds128(vk + (uint32_t)(nt * 8 * D * 2 + kp * 512 + lane * 16));
+        const uint4 b = lds128(vk + (uint32_t)(nt * 8 * D * 2 + kp * 512 + lane * 16));
         mma16816(c, qb[2 * kp][0], 0u, qb[2 * kp][1], 0u, b.x, b.y);
         mma16816(c, qb[2 * kp + 1][0], 0u, qb[2 * kp + 1][1], 0u, b.z, b.w);
       }
-      zbuf[nt * 32 + lane] = make_float2(c[0] * a.scale_log2, c[1] * a.scale_log2);
+      sm.zbuf[nt * 32 + lane] = make_float2(c[0] * slog2, c[1] * slog2);
     }
-    named_bar_sync(1, kConsumers * 32);
-    if (warp == 0 && lane == 0) mbar_arrive(&empty[0]);
-    // z B fragments: b0 = z[16kk + 2t, +1][gq] = zbuf[2kk][lane], b1 = zbuf[2kk+1][lane]
+    named_bar_sync(1, kConsumers * 32);  // basebuf, zbuf, av, mask are written; the head slot is read
+    if (lane == 0) mbar_arrive(&sm.empty[hs]);
     float zf[RT][4];
-    float zmax = 0.f;
 #pragma unroll
     for (int kk = 0; kk < RT; ++kk) {
       float2 z0 = make_float2(0.f, 0.f), z1 = make_float2(0.f, 0.f);
       if (kk < nrt) {
-        z0 = zbuf[(2 * kk) * 32 + lane];
-        if (2 * kk + 1 < (r8 >> 3)) z1 = zbuf[(2 * kk + 1) * 32 + lane];
+        z0 = sm.zbuf[(2 * kk) * 32 + lane];
+        if (2 * kk + 1 < (r8 >> 3)) z1 = sm.zbuf[(2 * kk + 1) * 32 + lane];
       }
       zf[kk][0] = z0.x; zf[kk][1] = z0.y; zf[kk][2] = z1.x; zf[kk][3] = z1.y;
-      zmax = fmaxf(zmax, fmaxf(fmaxf(fabsf(z0.x), fabsf(z0.y)), fmaxf(fabsf(z1.x), fabsf(z1.y))));
     }
+    const float* bb = sm.basebuf;
+    base0 = (bb[2 * t] + bb[8 + 2 * t] + bb[16 + 2 * t] + bb[24 + 2 * t]) * slog2;
+    base1 = (bb[2 * t + 1] + bb[9 + 2 * t] + bb[17 + 2 * t] + bb[25 + 2 * t]) * slog2;
+    // z B fragments: b0 = z[16kk + 2t, +1][gq] (C fragment c0, c1 of n-tile 2kk), b1 from n-tile 2kk+1
+    float zmax = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < RT; ++kk)
+      zmax = fmaxf(zmax, fmaxf(fmaxf(fabsf(zf[kk][0]), fabsf(zf[kk][1])), fmaxf(fabsf(zf[kk][2]), fabsf(zf[kk][3]))));
     zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 1));
     zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 2));
     const float zsc = pow2_down(zmax);  // for g = gq
@@ -337,284 +393,454 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
   // ---------------- private chunks (U rows and exact rows), round-robin over warps
   const int k_first = it.is_block ? 1 : 0;
   const int k_last = it.is_block ? it.n_chunks - 2 : it.n_chunks - 1;
-  for (int k = k_first; k <= k_last && ok; ++k) {
-    if (chunk_owner(it, k) != warp) continue;
-    const int slot = k % a.nslot;
-    if (!mbar_wait(&full[slot], (k / a.nslot) & 1, a.err)) { ok = false; break; }
+  for (int k = k_first; k <= k_last; ++k) {
+    const int slot = rc.slot;
+    const bool have = mbar_wait(&sm.full[slot], rc.use & 1u, a.err);
+    rc.next(a.nslot);
+    if (chunk_owner(it, k) != warp) {  // observed only: release at once
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[slot]);
+      continue;
+    }
+    ok = ok && have;
     const Chunk c = item_chunk(a, it, k);
     const uint32_t sb = slot0 + (uint32_t)(slot * a.slot_bytes);
-    if (c.kind == 1) {
-      // ---- U rows: s = base + U z, online softmax, w += U^T p
-#pragma unroll 1
-      for (int mt = 0; mt < kUTok / 16; ++mt) {
+    if (!have) {
+      // no data: skip the arithmetic, still release the slot
+    } else if (c.kind == 1) {
+      // ---- U rows, pass 1: every score of the chunk, then one rescale
+      constexpr int MT = kUTok / 16;
+      float s[MT][4];
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
         const uint32_t tb = sb + (uint32_t)(mt * 16 * r8 * 2);
-        uint32_t ua[RT][4];
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < RT; ++kk) {
           if (kk < nkk) {
-            uint4 v = lds128(tb + (uint32_t)(kk * 512 + lane * 16));
-            ua[kk][0] = v.x; ua[kk][1] = v.y; ua[kk][2] = v.z; ua[kk][3] = v.w;
-            mma16816(s, v.x, v.y, v.z, v.w, zh[kk][0], zh[kk][1]);
-            mma16816(s, v.x, v.y, v.z, v.w, zl[kk][0], zl[kk][1]);
+            const uint4 v = lds128(tb + (uint32_t)(kk * 512 + lane * 16));
+            mma16816(acc, v.x, v.y, v.z, v.w, zh[kk][0], zh[kk][1]);
+            mma16816(acc, v.x, v.y, v.z, v.w, zl[kk][0], zl[kk][1]);
           } else if (kk == nkk && rtail) {
-            uint2 v = lds64(tb + (uint32_t)(kk * 512 + lane * 8));
-            ua[kk][0] = v.x; ua[kk][1] = v.y; ua[kk][2] = 0u; ua[kk][3] = 0u;
-            mma1688(s, v.x, v.y, zh[kk][0]);
-            mma1688(s, v.x, v.y, zl[kk][0]);
+            const uint2 v = lds64(tb + (uint32_t)(kk * 512 + lane * 8));
+            mma1688(acc, v.x, v.y, zh[kk][0]);
+            mma1688(acc, v.x, v.y, zl[kk][0]);
           }
         }
         const int tk0 = c.tok0 + mt * 16 + gq, tk1 = tk0 + 8;
-        const bool m0 = (maskbuf[tk0 >> 5] >> (tk0 & 31)) & 1u;
-        const bool m1 = (maskbuf[tk1 >> 5] >> (tk1 & 31)) & 1u;
-        s[0] = m0 ? -INFINITY : fmaf(s[0], us0, base0);
-        s[1] = m0 ? -INFINITY : fmaf(s[1], us1, base1);
-        s[2] = m1 ? -INFINITY : fmaf(s[2], us0, base0);
-        s[3] = m1 ? -INFINITY : fmaf(s[3], us1, base1);
+        const bool m0 = (sm.maskbuf[tk0 >> 5] >> (tk0 & 31)) & 1u;
+        const bool m1 = (sm.maskbuf[tk1 >> 5] >> (tk1 & 31)) & 1u;
+        s[mt][0] = m0 ? -INFINITY : fmaf(acc[0], us0, base0);
+        s[mt][1] = m0 ? -INFINITY : fmaf(acc[1], us1, base1);
+        s[mt][2] = m1 ? -INFINITY : fmaf(acc[2], us0, base0);
+        s[mt][3] = m1 ? -INFINITY : fmaf(acc[3], us1, base1);
+        tile_max(s[mt], mx0, mx1);
+      }
+      float sc0, sc1, ms0, ms1;
+      stat_update(sL, mx0, mx1, sc0, sc1, ms0, ms1);
+#pragma unroll
+      for (int i = 0; i < RT; ++i) { w[i][0] *= sc0; w[i][1] *= sc1; w[i][2] *= sc0; w[i][3] *= sc1; }
+      // ---- pass 2: p, and w += U^T p (U fragments reloaded, transposed in registers)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
         float p[4];
-        rescale(st, s, p, gv0, gv1);
-        st.pa[0] += p[0] + p[2];
-        st.pa[1] += p[1] + p[3];
+        probs(s[mt], ms0, ms1, gv0, gv1, p, sL);
         uint32_t bh0, bl0, bh1, bl1;
         p_to_b(p, bh0, bl0, bh1, bl1);
+        const uint32_t tb = sb + (uint32_t)(mt * 16 * r8 * 2);
 #pragma unroll
         for (int mr = 0; mr < RT; ++mr) {
-          if (mr < nrt) {
-            uint32_t A0 = movtrans(ua[mr][0]);
-            uint32_t A2 = movtrans(ua[mr][1]);
-            uint32_t A1 = (mr < nkk) ? movtrans(ua[mr][2]) : 0u;
-            uint32_t A3 = (mr < nkk) ? movtrans(ua[mr][3]) : 0u;
-            mma16816(st.w[mr], A0, A1, A2, A3, bh0, bh1);
-            mma16816(st.w[mr], A0, A1, A2, A3, bl0, bl1);
+          if (mr < nkk) {
+            const uint4 v = lds128(tb + (uint32_t)(mr * 512 + lane * 16));
+            const uint32_t A0 = movtrans(v.x), A2 = movtrans(v.y), A1 = movtrans(v.z), A3 = movtrans(v.w);
+            mma16816(w[mr], A0, A1, A2, A3, bh0, bh1);
+            mma16816(w[mr], A0, A1, A2, A3, bl0, bl1);
+          } else if (mr == nkk && rtail) {
+            const uint2 v = lds64(tb + (uint32_t)(mr * 512 + lane * 8));
+            const uint32_t A0 = movtrans(v.x), A2 = movtrans(v.y);
+            mma16816(w[mr], A0, 0u, A2, 0u, bh0, bh1);
+            mma16816(w[mr], A0, 0u, A2, 0u, bl0, bl1);
           }
         }
       }
     } else {
-      // ---- exact rows (residuals or window): s = c q . k, online softmax, o += V^T p
+      // ---- exact rows (residuals or window), pass 1: scores of the chunk's groups
+      constexpr int MG = 16384 / (64 * D);  // 16-token groups per chunk (2 at d = 128, 4 at d = 64)
       const int ng = (c.ntok + 15) >> 4;
-#pragma unroll 1
-      for (int gi = 0; gi < ng; ++gi) {
-        const int in_g = min(16, c.ntok - gi * 16);
-        const uint32_t gb = sb + (uint32_t)(gi * 64 * D);
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
-        if (in_g == 16) {
+      float s[MG][4];
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-          for (int kt = 0; kt < D / 16; ++kt) {
-            uint4 v = lds128(gb + (uint32_t)(kt * 512 + lane * 16));
-            mma16816(s, v.x, v.y, v.z, v.w, qb[kt][0], qb[kt][1]);
-          }
-        } else {
+      for (int gi = 0; gi < MG; ++gi) {
+        s[gi][0] = s[gi][1] = s[gi][2] = s[gi][3] = -INFINITY;
+        if (gi < ng) {
+          const int in_g = min(16, c.ntok - gi * 16);
+          const uint32_t gb = sb + (uint32_t)(gi * 64 * D);
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          if (in_g == 16) {
 #pragma unroll
-          for (int kt = 0; kt < D / 16; ++kt) {
-            uint2 v = lds64(gb + (uint32_t)(kt * 256 + lane * 8));
-            mma16816(s, v.x, 0u, v.y, 0u, qb[kt][0], qb[kt][1]);
+            for (int kt = 0; kt < KT; ++kt) {
+              const uint4 v = lds128(gb + (uint32_t)(kt * 512 + lane * 16));
+              mma16816(acc, v.x, v.y, v.z, v.w, qb[kt][0], qb[kt][1]);
+            }
+          } else {
+#pragma unroll
+            for (int kt = 0; kt < KT; ++kt) {
+              const uint2 v = lds64(gb + (uint32_t)(kt * 256 + lane * 8));
+              mma16816(acc, v.x, 0u, v.y, 0u, qb[kt][0], qb[kt][1]);
+            }
           }
+          const int tk0 = c.tok0 + gi * 16 + gq, tk1 = tk0 + 8;
+          const bool v0 = tk0 < it.nvalid && (gq < in_g);
+          const bool v1 = tk1 < it.nvalid && (gq + 8 < in_g);
+          s[gi][0] = v0 ? acc[0] * slog2 : -INFINITY;
+          s[gi][1] = v0 ? acc[1] * slog2 : -INFINITY;
+          s[gi][2] = v1 ? acc[2] * slog2 : -INFINITY;
+          s[gi][3] = v1 ? acc[3] * slog2 : -INFINITY;
+          tile_max(s[gi], mx0, mx1);
         }
-        const int tk0 = c.tok0 + gi * 16 + gq, tk1 = tk0 + 8;
-        const bool v0 = tk0 < it.nvalid && (gq < in_g);
-        const bool v1 = tk1 < it.nvalid && (gq + 8 < in_g);
-        s[0] = v0 ? s[0] * a.scale_log2 : -INFINITY;
-        s[1] = v0 ? s[1] * a.scale_log2 : -INFINITY;
-        s[2] = v1 ? s[2] * a.scale_log2 : -INFINITY;
-        s[3] = v1 ? s[3] * a.scale_log2 : -INFINITY;
-        float p[4];
-        rescale(st, s, p, gv0, gv1);
-        uint32_t bh0, bl0, bh1, bl1;
-        p_to_b(p, bh0, bl0, bh1, bl1);
-        const uint32_t vb = gb + (uint32_t)(in_g * D * 2);
-        if (in_g == 16) {
+      }
+      float sc0, sc1, ms0, ms1;
+      stat_update(sX, mx0, mx1, sc0, sc1, ms0, ms1);
 #pragma unroll
-          for (int md = 0; md < D / 16; ++md) {
-            uint4 v = lds128(vb + (uint32_t)(md * 512 + lane * 16));
-            mma16816(st.o[md], v.x, v.y, v.z, v.w, bh0, bh1);
-            mma16816(st.o[md], v.x, v.y, v.z, v.w, bl0, bl1);
-          }
-        } else {
+      for (int i = 0; i < KT; ++i) { o[i][0] *= sc0; o[i][1] *= sc1; o[i][2] *= sc0; o[i][3] *= sc1; }
+      // ---- pass 2: p, and o += V^T p
 #pragma unroll
-          for (int md = 0; md < D / 16; ++md) {
-            uint2 v = lds64(vb + (uint32_t)(md * 256 + lane * 8));
-            mma1688(st.o[md], v.x, v.y, bh0);
-            mma1688(st.o[md], v.x, v.y, bl0);
+      for (int gi = 0; gi < MG; ++gi) {
+        if (gi < ng) {
+          const int in_g = min(16, c.ntok - gi * 16);
+          const uint32_t gb = sb + (uint32_t)(gi * 64 * D);
+          float p[4];
+          probs(s[gi], ms0, ms1, gv0, gv1, p, sX);
+          uint32_t bh0, bl0, bh1, bl1;
+          p_to_b(p, bh0, bl0, bh1, bl1);
+          const uint32_t vb = gb + (uint32_t)(in_g * D * 2);
+          if (in_g == 16) {
+#pragma unroll
+            for (int md = 0; md < KT; ++md) {
+              const uint4 v = lds128(vb + (uint32_t)(md * 512 + lane * 16));
+              mma16816(o[md], v.x, v.y, v.z, v.w, bh0, bh1);
+              mma16816(o[md], v.x, v.y, v.z, v.w, bl0, bl1);
+            }
+          } else {
+#pragma unroll
+            for (int md = 0; md < KT; ++md) {
+              const uint2 v = lds64(vb + (uint32_t)(md * 256 + lane * 8));
+              mma1688(o[md], v.x, v.y, bh0);
+              mma1688(o[md], v.x, v.y, bl0);
+            }
           }
         }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (lane == 0) mbar_arrive(&sm.empty[slot]);
   }
 
   // ---------------- merge the four warps
-  st.l[0] = warp_sum_rows(st.l[0]);
-  st.l[1] = warp_sum_rows(st.l[1]);
-  st.pa[0] = warp_sum_rows(st.pa[0]);
-  st.pa[1] = warp_sum_rows(st.pa[1]);
-  if (lane < 4) { mbuf[warp * 8 + 2 * t] = st.m[0]; mbuf[warp * 8 + 2 * t + 1] = st.m[1]; }
-  named_bar_sync(1, kConsumers * 32);
-  float mf0 = -INFINITY, mf1 = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < kConsumers; ++w) { mf0 = fmaxf(mf0, mbuf[w * 8 + 2 * t]); mf1 = fmaxf(mf1, mbuf[w * 8 + 2 * t + 1]); }
-  const float sc0 = exp2f(st.m[0] - (mf0 == -INFINITY ? 0.f : mf0));
-  const float sc1 = exp2f(st.m[1] - (mf1 == -INFINITY ? 0.f : mf1));
+  sL.l[0] = warp_sum_rows(sL.l[0]);
+  sL.l[1] = warp_sum_rows(sL.l[1]);
+  sX.l[0] = warp_sum_rows(sX.l[0]);
+  sX.l[1] = warp_sum_rows(sX.l[1]);
+  float* obw = sm.obw;
+  float* wbw = sm.wbw;
+  float* stat = sm.stat;
+  float* fin = sm.fin;
+  // the previous item's readers of the merge buffers are done (barrier at its end)
   if (lane < 4) {
-    lbuf[warp * 8 + 2 * t] = st.l[0] * sc0; lbuf[warp * 8 + 2 * t + 1] = st.l[1] * sc1;
-    pabuf[warp * 8 + 2 * t] = st.pa[0] * sc0; pabuf[warp * 8 + 2 * t + 1] = st.pa[1] * sc1;
+    float* sw = stat + warp * 32;
+    sw[2 * t] = sL.m[0]; sw[2 * t + 1] = sL.m[1];
+    sw[8 + 2 * t] = sL.l[0]; sw[8 + 2 * t + 1] = sL.l[1];
+    sw[16 + 2 * t] = sX.m[0]; sw[16 + 2 * t + 1] = sX.m[1];
+    sw[24 + 2 * t] = sX.l[0]; sw[24 + 2 * t + 1] = sX.l[1];
   }
-  // sequential (deterministic) sum of w and o across warps
-  for (int w = 0; w < kConsumers; ++w) {
-    if (warp == w) {
 #pragma unroll
-      for (int mr = 0; mr < RT; ++mr) {
-        if (it.is_block && mr < nrt) {
-          const int r0 = mr * 16 + gq, r1 = r0 + 8;
-          float* w0 = wbuf + r0 * 8 + 2 * t;
-          float* w1 = wbuf + r1 * 8 + 2 * t;
-          if (w == 0) {
-            w0[0] = st.w[mr][0] * sc0; w0[1] = st.w[mr][1] * sc1;
-            if (r1 < r8) { w1[0] = st.w[mr][2] * sc0; w1[1] = st.w[mr][3] * sc1; }
-          } else {
-            w0[0] += st.w[mr][0] * sc0; w0[1] += st.w[mr][1] * sc1;
-            if (r1 < r8) { w1[0] += st.w[mr][2] * sc0; w1[1] += st.w[mr][3] * sc1; }
-          }
-        }
-      }
+  for (int md = 0; md < KT; ++md) {
+    float* o0 = obw + ((size_t)warp * D + md * 16 + gq) * 8 + 2 * t;
+    o0[0] = o[md][0]; o0[1] = o[md][1]; o0[64] = o[md][2]; o0[65] = o[md][3];
+  }
+  if (it.is_block) {
 #pragma unroll
-      for (int md = 0; md < D / 16; ++md) {
-        float* o0 = obuf + (md * 16 + gq) * 8 + 2 * t;
-        float* o1 = o0 + 64;
-        if (w == 0) {
-          o0[0] = st.o[md][0] * sc0; o0[1] = st.o[md][1] * sc1; o1[0] = st.o[md][2] * sc0; o1[1] = st.o[md][3] * sc1;
-        } else {
-          o0[0] += st.o[md][0] * sc0; o0[1] += st.o[md][1] * sc1; o1[0] += st.o[md][2] * sc0; o1[1] += st.o[md][3] * sc1;
-        }
+    for (int mr = 0; mr < RT; ++mr) {
+      if (mr < nrt) {
+        const int r0 = mr * 16 + gq;
+        float* w0 = wbw + ((size_t)warp * RT * 16 + r0) * 8 + 2 * t;
+        w0[0] = w[mr][0]; w0[1] = w[mr][1];
+        if (r0 + 8 < r8) { w0[64] = w[mr][2]; w0[65] = w[mr][3]; }
       }
     }
-    named_bar_sync(1, kConsumers * 32);
   }
-
-  // ---------------- low-rank value: o += V_V^T w + (sum p) a_v
+  named_bar_sync(1, kConsumers * 32);
+  // merged statistics per query column g (threads 0..7), and the per-warp scale
+  // factors 2^(m_warp - M) that bring each warp's accumulators to the merged maxima
+  float* scl = fin + 32;  // [4 warps][8]: low-rank scale factors
+  float* scx = fin + 64;  // [4 warps][8]: exact-token scale factors
+  if (tid < 8) {
+    const int g = tid;
+    float ML = -INFINITY, MX = -INFINITY;
+    for (int wi = 0; wi < kConsumers; ++wi) { ML = fmaxf(ML, stat[wi * 32 + g]); MX = fmaxf(MX, stat[wi * 32 + 16 + g]); }
+    const float mls = ML == -INFINITY ? 0.f : ML, mxs = MX == -INFINITY ? 0.f : MX;
+    float LL = 0.f, LX = 0.f;
+    for (int wi = 0; wi < kConsumers; ++wi) {
+      const float fl = fast_exp2(stat[wi * 32 + g] - mls), fx = fast_exp2(stat[wi * 32 + 16 + g] - mxs);
+      scl[wi * 8 + g] = fl;
+      scx[wi * 8 + g] = fx;
+      LL += stat[wi * 32 + 8 + g] * fl;
+      LX += stat[wi * 32 + 24 + g] * fx;
+    }
+    fin[g] = ML; fin[8 + g] = LL; fin[16 + g] = MX; fin[24 + g] = LX;
+  }
+  named_bar_sync(1, kConsumers * 32);
+  // merge the warps' accumulators in place (into warp 0's area), one element per thread
+  for (int e = tid; e < D * 8; e += kConsumers * 32) {
+    const int d = e >> 3, g = e & 7;
+    float v = 0.f;
+#pragma unroll
+    for (int wi = 0; wi < kConsumers; ++wi) v += scx[wi * 8 + g] * obw[((size_t)wi * D + d) * 8 + g];
+    obw[(size_t)d * 8 + g] = v;
+  }
   if (it.is_block) {
-    const int kv = it.n_chunks - 1;
-    const int slot = kv % a.nslot;
-    ok = ok && mbar_wait(&full[slot], (kv / a.nslot) & 1, a.err);
-    const uint32_t vv = slot0 + (uint32_t)(slot * a.slot_bytes);
-    // w as B fragments: b0 = w[16kk + 2t, +1][gq], b1 = w[16kk + 8 + 2t, +1][gq]
+    for (int e = tid; e < r8 * 8; e += kConsumers * 32) {
+      const int r = e >> 3, g = e & 7;
+      float v = 0.f;
+#pragma unroll
+      for (int wi = 0; wi < kConsumers; ++wi) v += scl[wi * 8 + g] * wbw[((size_t)wi * RT * 16 + r) * 8 + g];
+      wbw[(size_t)r * 8 + g] = v;
+    }
+  }
+  named_bar_sync(1, kConsumers * 32);
+
+  float* rec = a.partials + ((size_t)u * a.n_items + it.item) * (16 + 8 * D);
+  // final partial: M = max(M_L, M_X); o = 2^(M_L - M) (V_V^T w + L_L a_v) + 2^(M_X - M) o_X
+  auto final_stats = [&](int g, float& aL, float& aX, float& M) {
+    const float ML = fin[g], MX = fin[16 + g];
+    M = fmaxf(ML, MX);
+    const float ms = M == -INFINITY ? 0.f : M;
+    aL = fast_exp2(ML - ms);
+    aX = fast_exp2(MX - ms);
+  };
+  if (tid < 8) {
+    float aL, aX, M;
+    final_stats(tid, aL, aX, M);
+    rec[tid] = ok ? M : -INFINITY;
+    rec[8 + tid] = ok ? aL * fin[8 + tid] + aX * fin[24 + tid] : 0.f;
+  }
+  if (it.is_block) {
+    // ---------------- low-rank value: V_V^T w (+ L_L a_v), combined with the exact part
+    const int vs = rc.slot;
+    ok = mbar_wait(&sm.full[vs], rc.use & 1u, a.err) && ok;
+    rc.next(a.nslot);
+    const uint32_t vv = slot0 + (uint32_t)(vs * a.slot_bytes);
+    // merged w as B fragments: b0 = w[16kk + 2t, +1][gq], b1 = w[16kk + 8 + 2t, +1][gq]
     float wf[RT][4];
     float wmax = 0.f;
 #pragma unroll
     for (int kk = 0; kk < RT; ++kk) {
       wf[kk][0] = wf[kk][1] = wf[kk][2] = wf[kk][3] = 0.f;
       if (kk < nrt) {
-        int r0 = 16 * kk + 2 * t;
-        wf[kk][0] = wbuf[r0 * 8 + gq];
-        wf[kk][1] = wbuf[(r0 + 1) * 8 + gq];
-        if (r0 + 8 < r8) { wf[kk][2] = wbuf[(r0 + 8) * 8 + gq]; wf[kk][3] = wbuf[(r0 + 9) * 8 + gq]; }
+        const int r0 = 16 * kk + 2 * t;
+        wf[kk][0] = wbw[r0 * 8 + gq];
+        wf[kk][1] = wbw[(r0 + 1) * 8 + gq];
+        if (r0 + 8 < r8) { wf[kk][2] = wbw[(r0 + 8) * 8 + gq]; wf[kk][3] = wbw[(r0 + 9) * 8 + gq]; }
       }
       wmax = fmaxf(wmax, fmaxf(fmaxf(fabsf(wf[kk][0]), fabsf(wf[kk][1])), fmaxf(fabsf(wf[kk][2]), fabsf(wf[kk][3]))));
     }
     wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, 1));
     wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, 2));
-    const float wsc = pow2_down(wmax);
+    const float wsc2 = pow2_down(wmax);
     uint32_t wh[RT][2], wl[RT][2];
 #pragma unroll
     for (int kk = 0; kk < RT; ++kk) {
-      split_half2(wf[kk][0] * wsc, wf[kk][1] * wsc, wh[kk][0], wl[kk][0]);
-      split_half2(wf[kk][2] * wsc, wf[kk][3] * wsc, wh[kk][1], wl[kk][1]);
+      split_half2(wf[kk][0] * wsc2, wf[kk][1] * wsc2, wh[kk][0], wl[kk][0]);
+      split_half2(wf[kk][2] * wsc2, wf[kk][3] * wsc2, wh[kk][1], wl[kk][1]);
     }
-    const float wus0 = 1.f / __shfl_sync(0xffffffffu, wsc, 8 * t);
-    const float wus1 = 1.f / __shfl_sync(0xffffffffu, wsc, 8 * t + 4);
-    float pa0 = 0.f, pa1 = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumers; ++w) { pa0 += pabuf[w * 8 + 2 * t]; pa1 += pabuf[w * 8 + 2 * t + 1]; }
-    for (int md = warp; md < D / 16; md += kConsumers) {
+    const float wus0 = 1.f / __shfl_sync(0xffffffffu, wsc2, 8 * t);
+    const float wus1 = 1.f / __shfl_sync(0xffffffffu, wsc2, 8 * t + 4);
+    float aL0, aX0, M0, aL1, aX1, M1;
+    final_stats(2 * t, aL0, aX0, M0);
+    final_stats(2 * t + 1, aL1, aX1, M1);
+    const float LL0 = fin[8 + 2 * t], LL1 = fin[8 + 2 * t + 1];
+    for (int md = warp; md < KT; md += kConsumers) {
       float c[4] = {0.f, 0.f, 0.f, 0.f};
       const uint32_t mb = vv + (uint32_t)(md * 16 * r8 * 2);
 #pragma unroll
       for (int kk = 0; kk < RT; ++kk) {
         if (kk < nkk) {
-          uint4 v = lds128(mb + (uint32_t)(kk * 512 + lane * 16));
+          const uint4 v = lds128(mb + (uint32_t)(kk * 512 + lane * 16));
           mma16816(c, v.x, v.y, v.z, v.w, wh[kk][0], wh[kk][1]);
           mma16816(c, v.x, v.y, v.z, v.w, wl[kk][0], wl[kk][1]);
         } else if (kk == nkk && rtail) {
-          uint2 v = lds64(mb + (uint32_t)(kk * 512 + lane * 8));
+          const uint2 v = lds64(mb + (uint32_t)(kk * 512 + lane * 8));
           mma1688(c, v.x, v.y, wh[kk][0]);
           mma1688(c, v.x, v.y, wl[kk][0]);
         }
       }
       const int d0 = md * 16 + gq, d1 = d0 + 8;
-      const float av0 = __half2float(av[d0]), av1 = __half2float(av[d1]);
-      float* o0 = obuf + d0 * 8 + 2 * t;
-      float* o1 = obuf + d1 * 8 + 2 * t;
-      o0[0] += c[0] * wus0 + pa0 * av0;
-      o0[1] += c[1] * wus1 + pa1 * av0;
-      o1[0] += c[2] * wus0 + pa0 * av1;
-      o1[1] += c[3] * wus1 + pa1 * av1;
+      const float av0 = __half2float(sm.av[d0]), av1 = __half2float(sm.av[d1]);
+      const float2 x0 = *reinterpret_cast<const float2*>(obw + d0 * 8 + 2 * t);
+      const float2 x1 = *reinterpret_cast<const float2*>(obw + d1 * 8 + 2 * t);
+      const float r00 = aL0 * (c[0] * wus0 + LL0 * av0) + aX0 * x0.x;
+      const float r01 = aL1 * (c[1] * wus1 + LL1 * av0) + aX1 * x0.y;
+      const float r10 = aL0 * (c[2] * wus0 + LL0 * av1) + aX0 * x1.x;
+      const float r11 = aL1 * (c[3] * wus1 + LL1 * av1) + aX1 * x1.y;
+      if (gv0) { rec[16 + (2 * t) * D + d0] = ok ? r00 : 0.f; rec[16 + (2 * t) * D + d1] = ok ? r10 : 0.f; }
+      if (gv1) { rec[16 + (2 * t + 1) * D + d0] = ok ? r01 : 0.f; rec[16 + (2 * t + 1) * D + d1] = ok ? r11 : 0.f; }
     }
-    named_bar_sync(1, kConsumers * 32);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[vs]);  // this warp is done with the V_V slot
+  } else {
+    for (int e = tid; e < G * D; e += kConsumers * 32) {
+      const int g = e / D, d = e % D;
+      rec[16 + g * D + d] = ok ? obw[d * 8 + g] : 0.f;
+    }
+  }
+  named_bar_sync(1, kConsumers * 32);  // the merge buffers are reused by the next item
+}
+
+// ---------------------------------------------------------------------------
+// the persistent kernel
+// ---------------------------------------------------------------------------
+template <int D, int RT>
+__global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const Smem sm = carve<D, RT>(smem, a);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    // full: the producer's arrival + the bulk copy's bytes; empty: one arrival per
+    // consumer warp, so no slot is refilled before every warp has seen its data
+    // (a parity wait is unambiguous only while no barrier runs two phases ahead)
+    for (int i = 0; i < a.nslot; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], kConsumers); }
+    for (int i = 0; i < kIQ; ++i) { mbar_init(&sm.iq_full[i], 1); mbar_init(&sm.iq_empty[i], 1); }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  griddep_launch();  // the combine grid may be scheduled now; it waits for this grid's completion
+
+  // =========================== producer warp
+  if (warp == kConsumers) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      Ring rp = {0, 0};        // next chunk slot
+      uint32_t k = 0;          // global ring index of the next chunk
+      bool waited = false;     // the router's grid (and the previous launch) has completed
+      for (int j = 0;; ++j) {
+        int gi = blockIdx.x;
+        if (j > 0) {
+          if (!waited) { griddep_wait(); waited = true; }
+          gi = (int)gridDim.x + (int)atomicAdd(&a.sched[0], 1u);
+        }
+        const int iq = j % kIQ;
+        if (j >= kIQ && !mbar_wait(&sm.iq_empty[iq], ((j / kIQ) - 1) & 1, a.err)) break;
+        ItemDesc& dsc = sm.iqd[iq];
+        if (gi >= a.total) {
+          dsc.stop = 1;
+          mbar_arrive(&sm.iq_full[iq]);
+          // the last CTA out resets the dynamic scheduler for the next call
+          if (j > 0 && atomicAdd(&a.sched[1], 1u) == gridDim.x - 1) {
+            a.sched[0] = 0u;
+            a.sched[1] = 0u;
+          }
+          break;
+        }
+        if (gi >= a.n_wchunks * a.L.units && !waited) { griddep_wait(); waited = true; }
+        ItemDesc it = decode_item(a, gi);
+        it.k0 = k;
+        dsc = it;
+        if (it.ok) {
+          // the descriptor (generic stores, released by the arrive) and the unit's query
+          // rows (bulk copies into padded rows) complete the same barrier phase
+          const int G = a.G;
+          const uint32_t row = (uint32_t)(a.L.d * 2);
+          mbar_arrive_expect_tx(&sm.iq_full[iq], row * (uint32_t)G);
+          const __half* qsrc = a.q + ((size_t)(it.u / a.Hkv) * a.Hq + (size_t)(it.u % a.Hkv) * G) * a.L.d;
+          __half* qdst = sm.qbuf + (size_t)iq * 8 * (a.L.d + 8);
+          for (int g = 0; g < G; ++g)
+            bulk_g2s(qdst + (size_t)g * (a.L.d + 8), qsrc + (size_t)g * a.L.d, row, &sm.iq_full[iq], pol);
+        } else {
+          mbar_arrive(&sm.iq_full[iq]);  // nothing to stream for this item
+          continue;
+        }
+        for (int c = 0; c < it.n_chunks; ++c, ++k) {
+          const int slot = rp.slot;
+          if (rp.use > 0 && !mbar_wait(&sm.empty[slot], (rp.use - 1) & 1u, a.err)) return;
+          rp.next(a.nslot);
+          const Chunk ch = item_chunk(a, it, c);
+          if (ch.bytes) {
+            mbar_arrive_expect_tx(&sm.full[slot], ch.bytes);
+            bulk_g2s(sm.slots + (size_t)slot * a.slot_bytes, a.cache + ch.src, ch.bytes, &sm.full[slot], pol);
+          } else {
+            mbar_arrive(&sm.full[slot]);
+          }
+        }
+      }
+    }
+    return;
   }
 
-  // ---------------- write the partial: m[8], l[8], o[8][D] (base-2 units)
-  float* rec = a.partials + ((size_t)u * a.n_items + item) * (16 + 8 * D);
-  const int tid = threadIdx.x;
-  if (tid < 8) {
-    float m = -INFINITY, l = 0.f;
-    for (int w = 0; w < kConsumers; ++w) m = fmaxf(m, mbuf[w * 8 + tid]);
-    for (int w = 0; w < kConsumers; ++w) l += lbuf[w * 8 + tid];
-    if (!ok) { m = -INFINITY; l = 0.f; }
-    rec[tid] = m;
-    rec[8 + tid] = l;
+  // =========================== consumer warps
+  Ring rc = {0, 0};
+  const int t = lane & 3, gq = lane >> 2;
+  for (int j = 0;; ++j) {
+    const int iq = j % kIQ;
+    if (!mbar_wait(&sm.iq_full[iq], (j / kIQ) & 1, a.err)) break;
+    const ItemDesc it = sm.iqd[iq];
+    // q as B fragments (k = head dim, n = group): q[gq][16kt + 2t, +1] and [16kt + 8 + 2t, +1]
+    uint32_t qb[D / 16][2];
+    {
+      const uint32_t qrow = smem_u32(sm.qbuf + ((size_t)iq * 8 + gq) * (D + 8));
+      const bool gv = gq < a.G && !it.stop && it.ok;
+#pragma unroll
+      for (int kt = 0; kt < D / 16; ++kt) {
+        qb[kt][0] = gv ? lds32(qrow + (uint32_t)(16 * kt + 2 * t) * 2u) : 0u;
+        qb[kt][1] = gv ? lds32(qrow + (uint32_t)(16 * kt + 8 + 2 * t) * 2u) : 0u;
+      }
+    }
+    named_bar_sync(1, kConsumers * 32);  // every consumer has its copy of the descriptor and of q
+    if (warp == 0 && lane == 0) mbar_arrive(&sm.iq_empty[iq]);
+    if (it.stop) break;
+    if (it.ok) {
+      consume_item<D, RT>(a, sm, it, rc, qb);
+    } else {
+      // an out-of-range routed index (raised in the device error word): an empty
+      // partial keeps the unit's merge well defined
+      float* rec = a.partials + ((size_t)it.u * a.n_items + it.item) * (16 + 8 * D);
+      for (int e = threadIdx.x; e < 16 + 8 * D; e += kConsumers * 32) rec[e] = e < 8 ? -INFINITY : 0.f;
+    }
   }
-  for (int e = tid; e < G * D; e += kConsumers * 32) {
-    int g = e / D, j = e % D;
-    rec[16 + g * D + j] = ok ? obuf[j * 8 + g] : 0.f;
-  }
-  if (a.out == nullptr) return;
-
-  // ---------------- fused split-LSE merge: the unit's last CTA to finish merges
-  // all of the unit's partials (arrival counter, no waiting on other CTAs)
-  __threadfence();
-  named_bar_sync(1, kConsumers * 32);
-  if (tid == 0) maskbuf[0] = atomicAdd(&a.counters[u], 1u) == (unsigned)(a.n_items - 1);
-  named_bar_sync(1, kConsumers * 32);
-  if (!maskbuf[0]) return;
-  __threadfence();
-  const size_t rs = 16 + 8 * (size_t)D;
-  const float* base = a.partials + (size_t)u * a.n_items * rs;
-  float* mstar = mbuf;          // [8] max of the unit's partials, per query of the group
-  float* linv = mbuf + 8;       // [8] 1 / merged normaliser
-  const size_t qrow0 = (size_t)bseq * a.Hq + (size_t)h * G;
-  if (tid < G) {
-    float m = -INFINITY;
-    for (int i = 0; i < a.n_items; ++i) m = fmaxf(m, __ldcg(base + i * rs + tid));
-    const float ms = m == -INFINITY ? 0.f : m;
-    float l = 0.f;
-    for (int i = 0; i < a.n_items; ++i) l += __ldcg(base + i * rs + 8 + tid) * exp2f(__ldcg(base + i * rs + tid) - ms);
-    mstar[tid] = ms;
-    linv[tid] = 1.f / l;
-    if (a.lse) a.lse[qrow0 + tid] = (ms + log2f(l)) * 0.6931471805599453f;
-  }
-  named_bar_sync(1, kConsumers * 32);
-  for (int e = tid; e < G * D; e += kConsumers * 32) {
-    const int g = e / D, j = e % D;
-    const float ms = mstar[g];
-    float acc = 0.f;
-    for (int i = 0; i < a.n_items; ++i)
-      acc = fmaf(exp2f(__ldcg(base + i * rs + g) - ms), __ldcg(base + i * rs + 16 + g * D + j), acc);
-    a.out[(qrow0 + g) * D + j] = acc * linv[g];
-  }
-  if (tid == 0) a.counters[u] = 0u;  // ready for the next call on this workspace
 }
 
 template <int D, int RT>
-cudaError_t launch_one(const AttendArgs& a, size_t smem, cudaStream_t s) {
+cudaError_t launch_one(const AttendArgs& a, int grid, size_t smem, cudaStream_t s) {
   static size_t configured = 0;  // largest dynamic shared memory size enabled so far
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(attend_kernel<D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  dim3 grid(a.n_items, a.L.units);
-  attend_kernel<D, RT><<<grid, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap with the router's grid
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attend_kernel<D, RT>, a);
+}
+
+int sm_count() {
+  static int n[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!n[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    n[dev] = v;
+  }
+  return n[dev];
 }
 
 }  // namespace
@@ -629,7 +855,8 @@ DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k
   P.n_items = P.K_eff + P.n_wchunks;
   P.route_splits = L.NB > 0 ? (L.NB + 63) / 64 : 0;
   P.off_counters = kWsHeader;
-  P.off_bounds = round_up(P.off_counters + (size_t)L.units * 8, 256);
+  // route counters [units], attend counters [units], scheduler [2]
+  P.off_bounds = round_up(P.off_counters + (size_t)L.units * 8 + 8, 256);
   P.off_routed = round_up(P.off_bounds + (size_t)L.units * L.NB * 4, 256);
   P.off_partials = round_up(P.off_routed + (size_t)L.units * P.K_eff * 4, 256);
   P.ws_bytes = P.off_partials + (size_t)L.units * P.n_items * (16 + 8 * L.d) * 4;
@@ -645,6 +872,8 @@ cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, i
   a.Hkv = n_kv_heads;
   a.K_eff = P.K_eff;
   a.n_items = P.n_items;
+  a.n_wchunks = P.n_wchunks;
+  a.total = P.n_items * L.units;
   a.xtok = 16384 / (4 * L.d);
   const int head = (int)L.off_u;
   int slot = 16384;
@@ -653,9 +882,10 @@ cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, i
   slot = 2 * L.r8 * L.d > slot ? 2 * L.r8 * L.d : slot;
   slot = (int)round_up((uint64_t)slot, 128);
   const int RT = L.r8 <= 32 ? 2 : (L.r8 <= 64 ? 4 : 8);
-  const size_t extra = 2 * kMaxSlots * 8 + (size_t)(RT * 2) * 32 * 8 + (size_t)RT * 16 * 8 * 4 + (size_t)L.d * 8 * 4 +
-                       3 * 32 * 4 + 32 + (size_t)L.d * 2 + 128;
-  const size_t budget = 113 * 1024;
+  size_t extra;
+  if (L.d == 128) extra = RT == 2 ? smem_extra<128, 2>() : (RT == 4 ? smem_extra<128, 4>() : smem_extra<128, 8>());
+  else extra = RT == 2 ? smem_extra<64, 2>() : (RT == 4 ? smem_extra<64, 4>() : smem_extra<64, 8>());
+  const size_t budget = 113 * 1024;  // two CTAs per SM
   int nslot = (int)((budget - extra) / slot);
   nslot = nslot > kMaxSlots ? kMaxSlots : nslot;
   if (nslot < 2) nslot = 2;
@@ -667,19 +897,21 @@ cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, i
   a.routed = reinterpret_cast<const int32_t*>(ws + P.off_routed);
   a.partials = reinterpret_cast<float*>(ws + P.off_partials);
   a.err = reinterpret_cast<uint32_t*>(ws);
-  a.counters = reinterpret_cast<uint32_t*>(ws + P.off_counters) + L.units;
-  a.out = out;
-  a.lse = lse;
+  a.sched = reinterpret_cast<uint32_t*>(ws + P.off_counters) + 2 * L.units;
   const size_t smem = (size_t)nslot * slot + extra;
-  if (P.n_items == 0) return cudaSuccess;
+  if (a.total == 0) return cudaSuccess;
+  int grid = 2 * sm_count();
+  grid = grid < a.total ? grid : a.total;
+  cudaError_t e;
   if (L.d == 128) {
-    if (RT == 2) return launch_one<128, 2>(a, smem, s);
-    if (RT == 4) return launch_one<128, 4>(a, smem, s);
-    return launch_one<128, 8>(a, smem, s);
+    e = RT == 2 ? launch_one<128, 2>(a, grid, smem, s)
+                : (RT == 4 ? launch_one<128, 4>(a, grid, smem, s) : launch_one<128, 8>(a, grid, smem, s));
+  } else {
+    e = RT == 2 ? launch_one<64, 2>(a, grid, smem, s)
+                : (RT == 4 ? launch_one<64, 4>(a, grid, smem, s) : launch_one<64, 8>(a, grid, smem, s));
   }
-  if (RT == 2) return launch_one<64, 2>(a, smem, s);
-  if (RT == 4) return launch_one<64, 4>(a, smem, s);
-  return launch_one<64, 8>(a, smem, s);
+  if (e != cudaSuccess || out == nullptr) return e;
+  return launch_combine(L, P, L.units / n_kv_heads, n_q_heads, n_kv_heads, a.partials, out, lse, s);
 }
 
 }  // namespace dkv

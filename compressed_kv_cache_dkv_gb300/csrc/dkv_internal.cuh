@@ -123,20 +123,23 @@ __device__ inline void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
 __device__ inline void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// One bounded wait step: the thread may sleep in hardware until the phase
+// completes, for at most kWaitHintNs (suspend-time hint), instead of spinning.
+constexpr uint32_t kWaitHintNs = 20000;
 __device__ inline bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kWaitHintNs)
       : "memory");
   return ok != 0;
 }
-// Bounded wait: gives up after `limit` polls (each try_wait itself suspends for
-// a hardware-defined time slice), raises DKV_DEVERR_TIMEOUT and returns false.
-constexpr uint32_t kWaitLimit = 1u << 22;
+// Bounded wait: gives up after kWaitLimit steps (at most ~1.3 s), raises
+// DKV_DEVERR_TIMEOUT and returns false.
+constexpr uint32_t kWaitLimit = 1u << 16;
 __device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
   for (uint32_t i = 0; i < kWaitLimit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
@@ -156,6 +159,13 @@ __device__ inline uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// 2^x with the hardware approximation (2 ulp; ex2(-inf) = 0)
+__device__ inline float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ inline void named_bar_sync(int id, int nthreads) {
@@ -234,8 +244,8 @@ struct DecodePlan {
 DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k);
 cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
                          const uint8_t* cache, uint8_t* ws, int32_t* routed_out, cudaStream_t s);
-// out == nullptr: partials only (merge with launch_combine); otherwise the last
-// CTA of each unit merges the unit's partials into out (and lse)
+// out == nullptr: partials only (merge with launch_combine); otherwise the
+// combine grid is launched right after (programmatic dependent launch)
 cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
                           const uint8_t* cache, uint8_t* ws, float* out, float* lse, cudaStream_t s);
 cudaError_t launch_combine(const Layout& L, const DecodePlan& P, int batch, int n_q_heads, int n_kv_heads,

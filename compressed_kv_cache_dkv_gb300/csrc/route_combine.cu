@@ -11,7 +11,7 @@
 // combine: the flash-style log-sum-exp merge of every partial of a unit
 // ("Flash-Style LSE Combine", README section "Core Architecture & Paper
 // Overview"): m* = max m_j, l* = sum l_j 2^(m_j - m*),
-// o = sum acc_j 2^(m_j - m*) / l*, all in fp32.
+// o = sum acc_j 2^(m_j - m*) / l*, all in fp32, in a fixed order (deterministic).
 #include <math.h>
 
 #include "dkv_internal.cuh"
@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(256) route_kernel(Layout L, int G, int Hq, int
   const int b = u / Hkv, h = u % Hkv;
   const int tid = threadIdx.x, nt = blockDim.x;
   const int warp = tid >> 5, lane = tid & 31;
+  griddep_launch();  // the attention grid may start its window work now; its block work waits for this grid
   for (int j = tid; j < d; j += nt) {
     float s = 0.f;
     for (int g = 0; g < G; ++g) s += __half2float(q[((size_t)b * Hq + (size_t)h * G + g) * d + j]);
@@ -122,25 +123,62 @@ __global__ void __launch_bounds__(256) route_kernel(Layout L, int G, int Hq, int
   if (tid == 0) counters[u] = 0u;  // ready for the next call on this workspace
 }
 
-__global__ void __launch_bounds__(128) combine_kernel(int n_items, int G, int Hq, int Hkv, int d,
+// One CTA per unit: its G queries.  Launched as a programmatic dependent of the
+// attention grid, so its launch overlaps that grid's tail; griddepcontrol.wait
+// makes the partials visible before they are read.
+__global__ void __launch_bounds__(256) combine_kernel(int n_items, int G, int Hq, int Hkv, int d,
                                                       const float* __restrict__ partials, float* __restrict__ out,
                                                       float* __restrict__ lse) {
-  const int jq = blockIdx.x, b = blockIdx.y;
-  const int u = b * Hkv + jq / G, g = jq % G;
-  const size_t rec = 16 + 8 * (size_t)d;
-  const float* p = partials + (size_t)u * n_items * rec;
-  float mstar = -INFINITY;
-  for (int i = 0; i < n_items; ++i) mstar = fmaxf(mstar, p[i * rec + g]);
-  const float ms = mstar == -INFINITY ? 0.f : mstar;
-  float lstar = 0.f;
-  for (int i = 0; i < n_items; ++i) lstar += p[i * rec + 8 + g] * exp2f(p[i * rec + g] - ms);
-  const float inv = 1.f / lstar;
-  for (int j = threadIdx.x; j < d; j += blockDim.x) {
-    float acc = 0.f;
-    for (int i = 0; i < n_items; ++i) acc += p[i * rec + 16 + g * d + j] * exp2f(p[i * rec + g] - ms);
-    out[((size_t)b * Hq + jq) * d + j] = acc * inv;
+  griddep_wait();
+  __shared__ float mstar[8], linv[8];
+  const int u = blockIdx.x, b = u / Hkv, h = u % Hkv;
+  const int tid = threadIdx.x;
+  const size_t rs = 16 + 8 * (size_t)d;
+  const float* p = partials + (size_t)u * n_items * rs;
+  const size_t qrow0 = (size_t)b * Hq + (size_t)h * G;
+  if (tid < G) {
+    float m = -INFINITY;
+    for (int i = 0; i < n_items; ++i) m = fmaxf(m, __ldg(p + i * rs + tid));
+    const float ms = m == -INFINITY ? 0.f : m;
+    float l = 0.f;
+    for (int i = 0; i < n_items; ++i) l += __ldg(p + i * rs + 8 + tid) * fast_exp2(__ldg(p + i * rs + tid) - ms);
+    mstar[tid] = ms;
+    linv[tid] = 1.f / l;
+    if (lse) lse[qrow0 + tid] = (ms + log2f(l)) * 0.6931471805599453f;
   }
-  if (lse && threadIdx.x == 0) lse[(size_t)b * Hq + jq] = (ms + log2f(lstar)) * 0.6931471805599453f;
+  __syncthreads();
+  // float4 outputs, eight independent partial loads in flight per thread
+  for (int e = tid; e < G * d / 4; e += blockDim.x) {
+    const int g = (4 * e) / d, j = (4 * e) % d;
+    const float ms = mstar[g];
+    const float* src = p + 16 + g * d + j;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int i = 0;
+    for (; i + 8 <= n_items; i += 8) {
+      float4 v[8];
+      float wv[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        v[x] = __ldg(reinterpret_cast<const float4*>(src + (i + x) * rs));
+        wv[x] = __ldg(p + (i + x) * rs + g);
+      }
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const float wx = fast_exp2(wv[x] - ms);
+        acc.x = fmaf(wx, v[x].x, acc.x); acc.y = fmaf(wx, v[x].y, acc.y);
+        acc.z = fmaf(wx, v[x].z, acc.z); acc.w = fmaf(wx, v[x].w, acc.w);
+      }
+    }
+    for (; i < n_items; ++i) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(src + i * rs));
+      const float wx = fast_exp2(__ldg(p + i * rs + g) - ms);
+      acc.x = fmaf(wx, v.x, acc.x); acc.y = fmaf(wx, v.y, acc.y);
+      acc.z = fmaf(wx, v.z, acc.z); acc.w = fmaf(wx, v.w, acc.w);
+    }
+    const float li = linv[g];
+    acc.x *= li; acc.y *= li; acc.z *= li; acc.w *= li;
+    *reinterpret_cast<float4*>(out + (qrow0 + g) * d + j) = acc;
+  }
 }
 
 }  // namespace
@@ -166,10 +204,19 @@ cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, in
 
 cudaError_t launch_combine(const Layout& L, const DecodePlan& P, int batch, int n_q_heads, int n_kv_heads,
                            const float* partials, float* out, float* lse, cudaStream_t s) {
-  dim3 grid(n_q_heads, batch);
-  combine_kernel<<<grid, 128, 0, s>>>(P.n_items, n_q_heads / n_kv_heads, n_q_heads, n_kv_heads, L.d, partials, out,
-                                      lse);
-  return cudaGetLastError();
+  (void)batch;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.units);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, P.n_items, n_q_heads / n_kv_heads, n_q_heads, n_kv_heads, L.d,
+                            partials, out, lse);
 }
 
 }  // namespace dkv
