@@ -82,7 +82,8 @@ int dkv_layout(dkv_desc* d) {
   if (d->head_dim != 64 && d->head_dim != 128) return DKV_ERR_UNSUPPORTED;
   if (d->n_q_heads / d->n_kv_heads > 8) return DKV_ERR_UNSUPPORTED;
   if (d->rank > 128 || d->n_residual > 255) return DKV_ERR_UNSUPPORTED;
-  if (d->n_blocks > 16384) return DKV_ERR_UNSUPPORTED;  // router keeps all block scores in shared memory
+  // the router and the combine keep per-block / per-item values in shared memory
+  if (d->n_blocks > 2048 || d->window > 65536) return DKV_ERR_UNSUPPORTED;
   const uint64_t dd = (uint64_t)d->head_dim;
   const int r8 = (d->rank + 7) / 8 * 8;
   const int R8 = (d->n_residual + 7) / 8 * 8;

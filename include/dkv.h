@@ -79,8 +79,8 @@ extern "C" {
  * pass it by pointer, copy it freely.
  *
  * Supported: head_dim 64 or 128; 1 <= n_q_heads/n_kv_heads <= 8; block_size
- * 256; 0 <= rank <= 128; 0 <= n_residual <= 255; n_blocks >= 0; window >= 0;
- * n_blocks + window > 0.
+ * 256; 0 <= rank <= 128; 0 <= n_residual <= 255; 0 <= n_blocks <= 2048;
+ * 0 <= window <= 65536; n_blocks + window > 0.
  */
 typedef struct dkv_desc {
   int32_t batch;        /* sequences B */
