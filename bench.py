@@ -318,34 +318,45 @@ def main():
                 ext.record(events[layer][1], sh)
             dkv.dkv_decode_combine(descs[layer], top_k, outs[layer], ws, lse=lses[layer], stream=sh)
 
-    # ---------------- warm-up (eager), then capture K steps into one graph
+    # ---------------- warm-up (eager), then capture K steps into graphs: one plain (the
+    # timed step), one with events around every attention launch (the kernel's duration;
+    # the events split the programmatic launches apart, so that graph runs a little slower)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
     stream.synchronize()
     K_steps = args.steps
     ev = [[(ext.new(), ext.new()) for _ in range(n_layers)] for _ in range(K_steps)]
-    graph = torch.cuda.CUDAGraph()
+    graph, graph_ev = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for k in range(K_steps):
+            step()
+    with torch.cuda.graph(graph_ev, stream=stream):
+        for k in range(K_steps):
             step(ev[k])
-    graph.replay()  # one untimed replay of the captured steps (warm)
+    with torch.cuda.stream(stream):  # a graph replays on the current stream
+        graph.replay()  # untimed replays (warm)
+        graph_ev.replay()
     stream.synchronize()
 
-    # ---------------- timed region
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        t0.record(stream)
-        graph.replay()
-        t1.record(stream)
-        stream.synchronize()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    ms = t0.elapsed_time(t1)
+    # ---------------- timed regions
+    def timed(g):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk, torch.cuda.stream(stream):
+            t0.record(stream)
+            g.replay()
+            t1.record(stream)
+            stream.synchronize()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        return t0.elapsed_time(t1), clk
+
+    ms, clocks = timed(graph)
+    ms_ev, clocks_ev = timed(graph_ev)
     attend_ms = [ext.elapsed_ms(ev[k][l][0], ev[k][l][1]) for k in range(K_steps) for l in range(n_layers)]
     st, word = dkv.dkv_get_error(ws, stream=sh)
     if st != dkv.DKV_OK:
@@ -381,9 +392,9 @@ def main():
 
     # ---------------- reduce over ranks (max time)
     if world > 1:
-        tt = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+        tt = torch.tensor([ms, e2e_ms, ms_ev], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(tt[0]), float(tt[1])
+        ms, e2e_ms, ms_ev = float(tt[0]), float(tt[1]), float(tt[2])
     ms_step = ms / K_steps
     value = world * queries_per_step * K_steps / (ms / 1e3)
     e2e_value = world * queries_per_step * e2e_steps / (e2e_ms / 1e3)
@@ -420,7 +431,10 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "attend_kernel (block + window attention)", "achieved": achieved_gbs,
                      "peak": peak, "unit": "GB/s", "frac": achieved_gbs / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
-                     "bytes_per_launch": att_bytes_step / n_layers, "mean_launch_us": att_ms_mean * 1e3},
+                     "bytes_per_launch": att_bytes_step / n_layers, "mean_launch_us": att_ms_mean * 1e3,
+                     "timed_in": "a second replay of the same K steps with events around every attention "
+                                 "launch", "ms_per_step_with_events": ms_ev / K_steps,
+                     "clocks": clocks_ev.summary()},
         "e2e": {"value": e2e_value, "unit": "queries/s", "steps": e2e_steps,
                 "h2d_bytes_per_step": sum(q.numel() * 2 for q in qs),
                 "d2h_bytes_per_step": sum(o.numel() * 4 for o in outs)},

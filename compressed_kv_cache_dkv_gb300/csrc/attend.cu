@@ -853,11 +853,8 @@ DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k
   P.wchunk_tokens = kWindowChunk;
   P.n_wchunks = (L.W16 + kWindowChunk - 1) / kWindowChunk;
   P.n_items = P.K_eff + P.n_wchunks;
-  P.route_splits = L.NB > 0 ? (L.NB + 63) / 64 : 0;
-  P.off_counters = kWsHeader;
-  // route counters [units], attend counters [units], scheduler [2]
-  P.off_bounds = round_up(P.off_counters + (size_t)L.units * 8 + 8, 256);
-  P.off_routed = round_up(P.off_bounds + (size_t)L.units * L.NB * 4, 256);
+  P.off_sched = kWsHeader;  // attention scheduler: work counter, finished-CTA counter
+  P.off_routed = round_up(P.off_sched + 8, 256);
   P.off_partials = round_up(P.off_routed + (size_t)L.units * P.K_eff * 4, 256);
   P.ws_bytes = P.off_partials + (size_t)L.units * P.n_items * (16 + 8 * L.d) * 4;
   return P;
@@ -897,7 +894,7 @@ cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, i
   a.routed = reinterpret_cast<const int32_t*>(ws + P.off_routed);
   a.partials = reinterpret_cast<float*>(ws + P.off_partials);
   a.err = reinterpret_cast<uint32_t*>(ws);
-  a.sched = reinterpret_cast<uint32_t*>(ws + P.off_counters) + 2 * L.units;
+  a.sched = reinterpret_cast<uint32_t*>(ws + P.off_sched);
   const size_t smem = (size_t)nslot * slot + extra;
   if (a.total == 0) return cudaSuccess;
   int grid = 2 * sm_count();

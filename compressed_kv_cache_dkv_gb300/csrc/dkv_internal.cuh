@@ -235,11 +235,11 @@ cudaError_t launch_compress(const Layout& L, const __half* K, const __half* V, u
                             uint32_t* err, cudaStream_t s);
 size_t compress_ws_bytes(const Layout& L);
 
-// Decode workspace: [header 256 B][route counters, attend counters: u32 per unit]
-// [block scores: f32 per unit and block][routed: i32 per unit and slot][partials]
+// Decode workspace: [header 256 B][scheduler: 2 x u32][routed: i32 per unit and slot]
+// [partials: per unit and item, m[8] l[8] o[8][d] in f32]
 struct DecodePlan {
-  int K_eff, n_wchunks, wchunk_tokens, n_items, route_splits;
-  size_t off_counters, off_bounds, off_routed, off_partials, ws_bytes;
+  int K_eff, n_wchunks, wchunk_tokens, n_items;
+  size_t off_sched, off_routed, off_partials, ws_bytes;
 };
 DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k);
 cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,

@@ -20,164 +20,226 @@ namespace dkv {
 
 namespace {
 
-constexpr int kRouteBlocks = 64;  // blocks scored per route CTA (8 warps x 8 blocks)
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteInFlight = 6;  // router loads in flight per thread
 
-// Scores the blocks [64*blockIdx.x, +64) of unit blockIdx.y into the workspace;
-// the last CTA of the unit to finish (arrival counter, no waiting) ranks all of
-// the unit's scores and writes the routed indices.
-__global__ void __launch_bounds__(256) route_kernel(Layout L, int G, int Hq, int Hkv, int K_eff, float cq,
-                                                    const __half* __restrict__ q, const uint8_t* __restrict__ cache,
-                                                    float* __restrict__ bounds, uint32_t* __restrict__ counters,
-                                                    int32_t* __restrict__ routed, int32_t* __restrict__ routed_out) {
-  extern __shared__ float sm[];  // last CTA: scores [NB], selection flags [NB]
+// One CTA per unit.  The unit's router rows ([NB][kmin | kmax], 4d bytes per
+// block) are requested before the group-mean query is formed, so the two
+// memory round trips overlap; each block's bound is reduced over the lanes
+// that hold its row, and the top K are ranked in shared memory by several
+// threads per block.
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L, int G, int Hq, int Hkv, int K_eff, float cq,
+                                                               const __half* __restrict__ q,
+                                                               const uint8_t* __restrict__ cache,
+                                                               int32_t* __restrict__ routed,
+                                                               int32_t* __restrict__ routed_out) {
+  extern __shared__ float4 sc4[];  // bounds [NB rounded up to 4]
   __shared__ float qbar[128];
-  __shared__ int s_last;
+  __shared__ int wsum[kRouteThreads / 32 + 1];
   const int d = L.d, NB = L.NB;
-  const int u = blockIdx.y, split = blockIdx.x, nsplit = gridDim.x;
+  const int u = blockIdx.x;
   const int b = u / Hkv, h = u % Hkv;
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const int warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31, nw = kRouteThreads / 32;
   griddep_launch();  // the attention grid may start its window work now; its block work waits for this grid
-  for (int j = tid; j < d; j += nt) {
-    float s = 0.f;
-    for (int g = 0; g < G; ++g) s += __half2float(q[((size_t)b * Hq + (size_t)h * G + g) * d + j]);
-    qbar[j] = s * cq;  // cq = c / G
-  }
-  __syncthreads();
-  // A block's router record is [kmin | kmax], 4d bytes = d/4 pieces of 16 bytes.
-  // The warp's 8 blocks are contiguous: 2d pieces, 2d/32 per lane, all loaded first.
   const uint8_t* router = cache + (uint64_t)u * L.unit_stride + L.off_router;
-  const int blk0 = split * kRouteBlocks + warp * 8;
-  const int per_blk = d / 4;                  // pieces per block (32 or 16)
-  const int npl = (2 * d) / 32;               // pieces per lane (8 or 4)
-  uint4 v[8];
+  const int per_blk = d / 4;                  // 16-byte pieces per block (32 or 16): one warp covers 1 or 2 blocks
+  const int blk_per_pass = (32 / per_blk) * nw;
+  const int half_pcs = d / 8;                 // kmin pieces; the kmax partner is half_pcs lanes up
+  const int q_in = lane % per_blk;
+  const int blk_lane = warp * (32 / per_blk) + lane / per_blk;
+  const int n_pass = (NB + blk_per_pass - 1) / blk_per_pass;
+  uint4 v[kRouteInFlight];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (i < npl) {
-      const int piece = i * 32 + lane;
-      const int blk = blk0 + piece / per_blk;
-      if (blk < NB) v[i] = *reinterpret_cast<const uint4*>(router + (size_t)blk0 * 4 * d + (size_t)piece * 16);
-    }
+  for (int i = 0; i < kRouteInFlight; ++i) {
+    const int blk = i * blk_per_pass + blk_lane;
+    v[i] = blk < NB ? *reinterpret_cast<const uint4*>(router + (size_t)blk * 4 * d + (size_t)q_in * 16)
+                    : make_uint4(0u, 0u, 0u, 0u);
   }
-  const int half_pcs = d / 8;                 // kmin pieces per block; kmax partner at +d/8
+  for (int j = tid; j < d; j += kRouteThreads) {
+    float x[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (i >= npl) break;
-    const int piece = i * 32 + lane;
-    const int q_in = piece % per_blk;
-    uint4 partner;
-    partner.x = __shfl_xor_sync(0xffffffffu, v[i].x, half_pcs);
-    partner.y = __shfl_xor_sync(0xffffffffu, v[i].y, half_pcs);
-    partner.z = __shfl_xor_sync(0xffffffffu, v[i].z, half_pcs);
-    partner.w = __shfl_xor_sync(0xffffffffu, v[i].w, half_pcs);
-    float acc = 0.f;
-    if (q_in < half_pcs) {
-      const __half* kmn = reinterpret_cast<const __half*>(&v[i]);
-      const __half* kmx = reinterpret_cast<const __half*>(&partner);
+    for (int g = 0; g < 8; ++g)  // independent loads, summed in a fixed order below
+      x[g] = g < G ? __half2float(q[((size_t)b * Hq + (size_t)h * G + g) * d + j]) : 0.f;
+    float t = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float qj = qbar[8 * q_in + e];
-        acc += fmaxf(qj * __half2float(kmx[e]), qj * __half2float(kmn[e]));
+    for (int g = 0; g < 8; ++g) t += x[g];
+    qbar[j] = t * cq;  // cq = c / G
+  }
+  float* sc = reinterpret_cast<float*>(sc4);
+  const int NB4 = (NB + 3) / 4;
+  if (tid >= NB && tid < 4 * NB4) sc[tid] = -INFINITY;  // padding never outranks a block
+  __syncthreads();
+  for (int p0 = 0; p0 < n_pass; p0 += kRouteInFlight) {
+    if (p0 > 0) {
+#pragma unroll
+      for (int i = 0; i < kRouteInFlight; ++i) {
+        const int blk = (p0 + i) * blk_per_pass + blk_lane;
+        v[i] = blk < NB ? *reinterpret_cast<const uint4*>(router + (size_t)blk * 4 * d + (size_t)q_in * 16)
+                        : make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    // sum over the per_blk lanes of this block (kmax lanes hold 0)
-    for (int o = per_blk >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    const int blk = blk0 + piece / per_blk;
-    if (q_in == 0 && blk < NB && blk < (split + 1) * kRouteBlocks)
-      bounds[(size_t)u * NB + blk] = isnan(acc) ? -INFINITY : acc;
+#pragma unroll
+    for (int i = 0; i < kRouteInFlight; ++i) {
+      const int blk = (p0 + i) * blk_per_pass + blk_lane;
+      uint4 partner;
+      partner.x = __shfl_xor_sync(0xffffffffu, v[i].x, half_pcs);
+      partner.y = __shfl_xor_sync(0xffffffffu, v[i].y, half_pcs);
+      partner.z = __shfl_xor_sync(0xffffffffu, v[i].z, half_pcs);
+      partner.w = __shfl_xor_sync(0xffffffffu, v[i].w, half_pcs);
+      float acc = 0.f;
+      if (q_in < half_pcs) {
+        const __half* kmn = reinterpret_cast<const __half*>(&v[i]);
+        const __half* kmx = reinterpret_cast<const __half*>(&partner);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float qj = qbar[8 * q_in + e];
+          acc += fmaxf(qj * __half2float(kmx[e]), qj * __half2float(kmn[e]));
+        }
+      }
+      for (int o = per_blk >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (q_in == 0 && blk < NB) sc[blk] = isnan(acc) ? -INFINITY : acc;
+    }
   }
-  __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&counters[u], 1u) == (unsigned)(nsplit - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  float* sc = sm;
-  int* sel = reinterpret_cast<int*>(sm + NB);
-  for (int i = tid; i < NB; i += nt) sc[i] = __ldcg(bounds + (size_t)u * NB + i);
-  __syncthreads();
-  for (int i = tid; i < NB; i += nt) {
-    int s = 1;
-    if (K_eff < NB) {
+  // rank of block i = number of blocks ahead of it (score desc, index asc);
+  // tpb threads share one block's comparisons
+  int tpb = 32;
+  while (tpb > 1 && tpb * NB > kRouteThreads) tpb >>= 1;
+  const int per_round = kRouteThreads / tpb;
+  const int sub = tid % tpb;
+  for (int base = 0; base < NB; base += per_round) {
+    const int i = base + tid / tpb;
+    int rank = 0;
+    if (i < NB && K_eff < NB) {
       const float bi = sc[i];
-      int rank = 0;
-      for (int j = 0; j < NB; ++j) {
-        const float bj = sc[j];
-        rank += (bj > bi) || (bj == bi && j < i);
+      for (int j4 = sub; j4 < NB4; j4 += tpb) {
+        const float4 bj = sc4[j4];
+        const int j = 4 * j4;
+        rank += (bj.x > bi) || (bj.x == bi && j < i);
+        rank += (bj.y > bi) || (bj.y == bi && j + 1 < i);
+        rank += (bj.z > bi) || (bj.z == bi && j + 2 < i);
+        rank += (bj.w > bi) || (bj.w == bi && j + 3 < i);
       }
-      s = rank < K_eff;
     }
-    sel[i] = s;
-  }
-  __syncthreads();
-  for (int i = tid; i < NB; i += nt) {
-    if (!sel[i]) continue;
-    int pos = 0;
-    for (int j = 0; j < i; ++j) pos += sel[j];
-    if (pos < K_eff) {
+    for (int o = tpb >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    const bool sel = sub == 0 && i < NB && rank < K_eff;
+    // ascending output position = number of routed blocks with a lower index
+    const unsigned bal = __ballot_sync(0xffffffffu, sel);
+    if (lane == 0) wsum[warp] = __popc(bal);
+    __syncthreads();
+    if (warp == 0) {
+      const int c = lane < nw ? wsum[lane] : 0;
+      int incl = c;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int run = base == 0 ? 0 : wsum[nw];
+      __syncwarp();
+      if (lane < nw) wsum[lane] = run + incl - c;
+      if (lane == 31) wsum[nw] = run + incl;
+    }
+    __syncthreads();
+    if (sel) {
+      const int pos = wsum[warp] + __popc(bal & ((1u << lane) - 1u));
       routed[(size_t)u * K_eff + pos] = i;
       if (routed_out) routed_out[(size_t)u * K_eff + pos] = i;
     }
+    __syncthreads();
   }
-  if (tid == 0) counters[u] = 0u;  // ready for the next call on this workspace
 }
 
-// One CTA per unit: its G queries.  Launched as a programmatic dependent of the
-// attention grid, so its launch overlaps that grid's tail; griddepcontrol.wait
-// makes the partials visible before they are read.
-__global__ void __launch_bounds__(256) combine_kernel(int n_items, int G, int Hq, int Hkv, int d,
-                                                      const float* __restrict__ partials, float* __restrict__ out,
-                                                      float* __restrict__ lse) {
+constexpr int kCombineThreads = 256;
+constexpr int kCombinePrefetch = 4;
+
+// One CTA per (unit, query head).  Partial records of all items are merged with
+// weights exp2(m_i - m*) / l* (m*, l* the merged maximum and normaliser);
+// the first kCombinePrefetch records of every thread are loaded before the
+// statistics are reduced, so both round trips to memory overlap.
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(int n_items, int G, int Hq, int Hkv, int d,
+                                                                  const float* __restrict__ partials,
+                                                                  float* __restrict__ out, float* __restrict__ lse) {
   griddep_wait();
-  __shared__ float mstar[8], linv[8];
-  const int u = blockIdx.x, b = u / Hkv, h = u % Hkv;
-  const int tid = threadIdx.x;
+  extern __shared__ float csm[];  // [n_items] maxima, [n_items] normalisers
+  __shared__ float4 red[kCombineThreads];
+  __shared__ float wred[kCombineThreads / 32];
+  const int u = blockIdx.x, g = blockIdx.y, b = u / Hkv, h = u % Hkv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t rs = 16 + 8 * (size_t)d;
   const float* p = partials + (size_t)u * n_items * rs;
-  const size_t qrow0 = (size_t)b * Hq + (size_t)h * G;
-  if (tid < G) {
-    float m = -INFINITY;
-    for (int i = 0; i < n_items; ++i) m = fmaxf(m, __ldg(p + i * rs + tid));
-    const float ms = m == -INFINITY ? 0.f : m;
-    float l = 0.f;
-    for (int i = 0; i < n_items; ++i) l += __ldg(p + i * rs + 8 + tid) * fast_exp2(__ldg(p + i * rs + tid) - ms);
-    mstar[tid] = ms;
-    linv[tid] = 1.f / l;
-    if (lse) lse[qrow0 + tid] = (ms + log2f(l)) * 0.6931471805599453f;
+  const size_t qrow = (size_t)b * Hq + (size_t)h * G + g;
+  const int n4 = d / 4, n_sub = kCombineThreads / n4;
+  const int e = tid % n4, sub = tid / n4;
+  const float* src = p + 16 + (size_t)g * d + 4 * e;
+  float4 pre[kCombinePrefetch];
+#pragma unroll
+  for (int x = 0; x < kCombinePrefetch; ++x) {
+    const int i = sub + x * n_sub;
+    pre[x] = i < n_items ? __ldg(reinterpret_cast<const float4*>(src + i * rs)) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  float* mi = csm;
+  float* li = csm + n_items;
+  float m = -INFINITY;
+  for (int i = tid; i < n_items; i += kCombineThreads) {
+    const float mv = __ldg(p + i * rs + g);
+    mi[i] = mv;
+    li[i] = __ldg(p + i * rs + 8 + g);
+    m = fmaxf(m, mv);
+  }
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) wred[warp] = m;
   __syncthreads();
-  // float4 outputs, eight independent partial loads in flight per thread
-  for (int e = tid; e < G * d / 4; e += blockDim.x) {
-    const int g = (4 * e) / d, j = (4 * e) % d;
-    const float ms = mstar[g];
-    const float* src = p + 16 + g * d + j;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int i = 0;
-    for (; i + 8 <= n_items; i += 8) {
-      float4 v[8];
-      float wv[8];
+  m = wred[0];
 #pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        v[x] = __ldg(reinterpret_cast<const float4*>(src + (i + x) * rs));
-        wv[x] = __ldg(p + (i + x) * rs + g);
-      }
+  for (int w = 1; w < kCombineThreads / 32; ++w) m = fmaxf(m, wred[w]);
+  const float ms = m == -INFINITY ? 0.f : m;
+  float l = 0.f;
+  for (int i = tid; i < n_items; i += kCombineThreads) l += li[i] * fast_exp2(mi[i] - ms);
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  __syncthreads();  // every thread has read wred
+  if (lane == 0) wred[warp] = l;
+  __syncthreads();
+  l = 0.f;
 #pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const float wx = fast_exp2(wv[x] - ms);
-        acc.x = fmaf(wx, v[x].x, acc.x); acc.y = fmaf(wx, v[x].y, acc.y);
-        acc.z = fmaf(wx, v[x].z, acc.z); acc.w = fmaf(wx, v[x].w, acc.w);
+  for (int w = 0; w < kCombineThreads / 32; ++w) l += wred[w];
+  const float linv = 1.f / l;
+  if (lse && tid == 0) lse[qrow] = (ms + log2f(l)) * 0.6931471805599453f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int x = 0; x < kCombinePrefetch; ++x) {
+    const int i = sub + x * n_sub;
+    if (i < n_items) {
+      const float wx = fast_exp2(mi[i] - ms) * linv;
+      acc.x = fmaf(wx, pre[x].x, acc.x); acc.y = fmaf(wx, pre[x].y, acc.y);
+      acc.z = fmaf(wx, pre[x].z, acc.z); acc.w = fmaf(wx, pre[x].w, acc.w);
+    }
+  }
+  for (int i0 = sub + kCombinePrefetch * n_sub; i0 < n_items; i0 += kCombinePrefetch * n_sub) {
+#pragma unroll
+    for (int x = 0; x < kCombinePrefetch; ++x) {
+      const int i = i0 + x * n_sub;
+      pre[x] = i < n_items ? __ldg(reinterpret_cast<const float4*>(src + i * rs)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int x = 0; x < kCombinePrefetch; ++x) {
+      const int i = i0 + x * n_sub;
+      if (i < n_items) {
+        const float wx = fast_exp2(mi[i] - ms) * linv;
+        acc.x = fmaf(wx, pre[x].x, acc.x); acc.y = fmaf(wx, pre[x].y, acc.y);
+        acc.z = fmaf(wx, pre[x].z, acc.z); acc.w = fmaf(wx, pre[x].w, acc.w);
       }
     }
-    for (; i < n_items; ++i) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(src + i * rs));
-      const float wx = fast_exp2(__ldg(p + i * rs + g) - ms);
-      acc.x = fmaf(wx, v.x, acc.x); acc.y = fmaf(wx, v.y, acc.y);
-      acc.z = fmaf(wx, v.z, acc.z); acc.w = fmaf(wx, v.w, acc.w);
+  }
+  red[tid] = acc;
+  __syncthreads();
+  if (tid < n4) {
+    float4 t = red[tid];
+    for (int s2 = 1; s2 < n_sub; ++s2) {
+      const float4 v = red[s2 * n4 + tid];
+      t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
     }
-    const float li = linv[g];
-    acc.x *= li; acc.y *= li; acc.z *= li; acc.w *= li;
-    *reinterpret_cast<float4*>(out + (qrow0 + g) * d + j) = acc;
+    *reinterpret_cast<float4*>(out + qrow * d + 4 * tid) = t;
   }
 }
 
@@ -187,18 +249,9 @@ cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, in
                          const uint8_t* cache, uint8_t* ws, int32_t* routed_out, cudaStream_t s) {
   const int G = n_q_heads / n_kv_heads;
   const float cq = 1.f / (sqrtf((float)L.d) * (float)G);
-  const size_t smem = (size_t)L.NB * 8;
-  static size_t configured = 48 * 1024;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
-  dim3 grid(P.route_splits, L.units);
-  route_kernel<<<grid, 256, smem, s>>>(L, G, n_q_heads, n_kv_heads, P.K_eff, cq, q, cache,
-                                       reinterpret_cast<float*>(ws + P.off_bounds),
-                                       reinterpret_cast<uint32_t*>(ws + P.off_counters),
-                                       reinterpret_cast<int32_t*>(ws + P.off_routed), routed_out);
+  const size_t smem = ((size_t)L.NB + 3) / 4 * 16;  // at most 2048 blocks: 8 KB
+  route_kernel<<<L.units, kRouteThreads, smem, s>>>(L, G, n_q_heads, n_kv_heads, P.K_eff, cq, q, cache,
+                                                    reinterpret_cast<int32_t*>(ws + P.off_routed), routed_out);
   return cudaGetLastError();
 }
 
@@ -206,9 +259,10 @@ cudaError_t launch_combine(const Layout& L, const DecodePlan& P, int batch, int 
                            const float* partials, float* out, float* lse, cudaStream_t s) {
   (void)batch;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(L.units);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
+  const size_t smem = (size_t)P.n_items * 8;  // at most (2048 + 256) items: 18 KB
+  cfg.gridDim = dim3(L.units, n_q_heads / n_kv_heads);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
