@@ -20,41 +20,54 @@ namespace dkv {
 
 namespace {
 
-constexpr int kRouteThreads = 1024;
-constexpr int kRouteInFlight = 6;  // router loads in flight per thread
+constexpr int kRouteCluster = 8;    // CTAs per unit (one thread-block cluster)
+constexpr int kRouteThreads = 256;
+constexpr int kRouteInFlight = 2;   // router rows in flight per lane (kmin and kmax pieces each)
 
-// One CTA per unit.  The unit's router rows ([NB][kmin | kmax], 4d bytes per
-// block) are requested before the group-mean query is formed, so the two
-// memory round trips overlap; each block's bound is reduced over the lanes
-// that hold its row, and the top K are ranked in shared memory by several
-// threads per block.
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L, int G, int Hq, int Hkv, int K_eff, float cq,
-                                                               const __half* __restrict__ q,
-                                                               const uint8_t* __restrict__ cache,
-                                                               int32_t* __restrict__ routed,
-                                                               int32_t* __restrict__ routed_out) {
-  extern __shared__ float4 sc4[];  // bounds [NB rounded up to 4]
+// One cluster of kRouteCluster CTAs per unit; CTA c of the cluster owns blocks
+// [c*per, (c+1)*per).  Each CTA loads its blocks' router rows ([kmin | kmax],
+// 4d bytes per block), bounds them, and stores every bound into all CTAs of the
+// cluster (distributed shared memory).  After a cluster barrier each CTA ranks
+// its own blocks against all NB bounds (score desc, index asc), and the
+// selected counts are exchanged once more so each CTA knows where its blocks
+// go in the ascending output.
+//
+// max(q kmax, q kmin) equals q kmax for q >= 0 and q kmin for q < 0 (rounding
+// is monotone), so every channel costs one select and one FMA.
+__global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteThreads)
+    route_kernel(Layout L, int G, int Hq, int Hkv, int K_eff, float cq, const __half* __restrict__ q,
+                 const uint8_t* __restrict__ cache, int32_t* __restrict__ routed, int32_t* __restrict__ routed_out) {
+  extern __shared__ float4 sc4[];  // bounds of all NB blocks of the unit, padded to 4 with -inf
   __shared__ float qbar[128];
-  __shared__ int wsum[kRouteThreads / 32 + 1];
+  __shared__ int cnt[kRouteCluster];
+  __shared__ int wsum[kRouteThreads / 32];
   const int d = L.d, NB = L.NB;
-  const int u = blockIdx.x;
+  const uint32_t crank = cluster_ctarank();
+  const int u = blockIdx.x / kRouteCluster;
   const int b = u / Hkv, h = u % Hkv;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31, nw = kRouteThreads / 32;
-  griddep_launch();  // the attention grid may start its window work now; its block work waits for this grid
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int nw = kRouteThreads / 32;
+  cluster_arrive_relaxed();  // this CTA has started (matched by the wait before the first peer store)
+  griddep_launch();          // the attention grid may start its window work now; its block work waits for this grid
   const uint8_t* router = cache + (uint64_t)u * L.unit_stride + L.off_router;
-  const int per_blk = d / 4;                  // 16-byte pieces per block (32 or 16): one warp covers 1 or 2 blocks
-  const int blk_per_pass = (32 / per_blk) * nw;
-  const int half_pcs = d / 8;                 // kmin pieces; the kmax partner is half_pcs lanes up
-  const int q_in = lane % per_blk;
-  const int blk_lane = warp * (32 / per_blk) + lane / per_blk;
-  const int n_pass = (NB + blk_per_pass - 1) / blk_per_pass;
-  uint4 v[kRouteInFlight];
+  const int per = (NB + kRouteCluster - 1) / kRouteCluster;
+  const int b0 = min(NB, (int)crank * per), b1 = min(NB, b0 + per);
+  const int hp = d / 8;                  // 16-byte pieces per half row (kmin or kmax)
+  const int bpw = 32 / hp;               // blocks per warp and pass
+  const int bpp = bpw * nw;              // blocks per pass
+  const int piece = lane % hp;
+  const int lb = warp * bpw + lane / hp;
+  const int n_pass = (b1 - b0 + bpp - 1) / bpp;
+  uint4 mn[kRouteInFlight], mx[kRouteInFlight];
 #pragma unroll
   for (int i = 0; i < kRouteInFlight; ++i) {
-    const int blk = i * blk_per_pass + blk_lane;
-    v[i] = blk < NB ? *reinterpret_cast<const uint4*>(router + (size_t)blk * 4 * d + (size_t)q_in * 16)
-                    : make_uint4(0u, 0u, 0u, 0u);
+    const int blk = b0 + i * bpp + lb;
+    mn[i] = mx[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (blk < b1) {
+      const uint8_t* row = router + (size_t)blk * 4 * d + (size_t)piece * 16;
+      mn[i] = *reinterpret_cast<const uint4*>(row);
+      mx[i] = *reinterpret_cast<const uint4*>(row + 2 * d);
+    }
   }
   for (int j = tid; j < d; j += kRouteThreads) {
     float x[8];
@@ -68,85 +81,85 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(Layout L, int G, i
   }
   float* sc = reinterpret_cast<float*>(sc4);
   const int NB4 = (NB + 3) / 4;
-  if (tid >= NB && tid < 4 * NB4) sc[tid] = -INFINITY;  // padding never outranks a block
+  if (tid < 4 * NB4 - NB) sc[NB + tid] = -INFINITY;  // padding never outranks a block
   __syncthreads();
+  float qv[8];
+  uint32_t selm[4];  // per half: all ones where q_j >= 0 (take kmax), zero where q_j < 0 (take kmin)
+#pragma unroll
+  for (int e = 0; e < 8; ++e) qv[e] = qbar[8 * piece + e];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) selm[w] = (qv[2 * w] >= 0.f ? 0x0000ffffu : 0u) | (qv[2 * w + 1] >= 0.f ? 0xffff0000u : 0u);
+  cluster_wait();  // every CTA of the cluster has started: peer shared memory may be written
   for (int p0 = 0; p0 < n_pass; p0 += kRouteInFlight) {
     if (p0 > 0) {
 #pragma unroll
       for (int i = 0; i < kRouteInFlight; ++i) {
-        const int blk = (p0 + i) * blk_per_pass + blk_lane;
-        v[i] = blk < NB ? *reinterpret_cast<const uint4*>(router + (size_t)blk * 4 * d + (size_t)q_in * 16)
-                        : make_uint4(0u, 0u, 0u, 0u);
+        const int blk = b0 + (p0 + i) * bpp + lb;
+        mn[i] = mx[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (blk < b1) {
+          const uint8_t* row = router + (size_t)blk * 4 * d + (size_t)piece * 16;
+          mn[i] = *reinterpret_cast<const uint4*>(row);
+          mx[i] = *reinterpret_cast<const uint4*>(row + 2 * d);
+        }
       }
     }
 #pragma unroll
     for (int i = 0; i < kRouteInFlight; ++i) {
-      const int blk = (p0 + i) * blk_per_pass + blk_lane;
-      uint4 partner;
-      partner.x = __shfl_xor_sync(0xffffffffu, v[i].x, half_pcs);
-      partner.y = __shfl_xor_sync(0xffffffffu, v[i].y, half_pcs);
-      partner.z = __shfl_xor_sync(0xffffffffu, v[i].z, half_pcs);
-      partner.w = __shfl_xor_sync(0xffffffffu, v[i].w, half_pcs);
+      const int blk = b0 + (p0 + i) * bpp + lb;
+      const uint32_t wn[4] = {mn[i].x, mn[i].y, mn[i].z, mn[i].w};
+      const uint32_t wx[4] = {mx[i].x, mx[i].y, mx[i].z, mx[i].w};
       float acc = 0.f;
-      if (q_in < half_pcs) {
-        const __half* kmn = reinterpret_cast<const __half*>(&v[i]);
-        const __half* kmx = reinterpret_cast<const __half*>(&partner);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float qj = qbar[8 * q_in + e];
-          acc += fmaxf(qj * __half2float(kmx[e]), qj * __half2float(kmn[e]));
-        }
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t v = (wx[w] & selm[w]) | (wn[w] & ~selm[w]);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+        acc = fmaf(qv[2 * w], f.x, acc);
+        acc = fmaf(qv[2 * w + 1], f.y, acc);
       }
-      for (int o = per_blk >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (q_in == 0 && blk < NB) sc[blk] = isnan(acc) ? -INFINITY : acc;
+      for (int o = hp >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (blk < b1 && piece < kRouteCluster) st_cluster_f32(sc + blk, (uint32_t)piece, isnan(acc) ? -INFINITY : acc);
     }
   }
-  __syncthreads();
-  // rank of block i = number of blocks ahead of it (score desc, index asc);
-  // tpb threads share one block's comparisons
+  cluster_sync();  // all NB bounds are in every CTA
+  // rank own blocks: tpb threads share one block's comparisons
+  const int n_own = b1 - b0;
   int tpb = 32;
-  while (tpb > 1 && tpb * NB > kRouteThreads) tpb >>= 1;
-  const int per_round = kRouteThreads / tpb;
+  while (tpb > 1 && tpb * n_own > kRouteThreads) tpb >>= 1;
   const int sub = tid % tpb;
-  for (int base = 0; base < NB; base += per_round) {
-    const int i = base + tid / tpb;
-    int rank = 0;
-    if (i < NB && K_eff < NB) {
-      const float bi = sc[i];
-      for (int j4 = sub; j4 < NB4; j4 += tpb) {
-        const float4 bj = sc4[j4];
-        const int j = 4 * j4;
-        rank += (bj.x > bi) || (bj.x == bi && j < i);
-        rank += (bj.y > bi) || (bj.y == bi && j + 1 < i);
-        rank += (bj.z > bi) || (bj.z == bi && j + 2 < i);
-        rank += (bj.w > bi) || (bj.w == bi && j + 3 < i);
-      }
+  const int i = b0 + tid / tpb;
+  const bool mine = tid / tpb < n_own;
+  int rank = 0;
+  if (mine && K_eff < NB) {
+    const float bi = sc[i];
+    for (int j4 = sub; j4 < NB4; j4 += tpb) {
+      const float4 bj = sc4[j4];
+      const int j = 4 * j4;
+      rank += (bj.x > bi) || (bj.x == bi && j < i);
+      rank += (bj.y > bi) || (bj.y == bi && j + 1 < i);
+      rank += (bj.z > bi) || (bj.z == bi && j + 2 < i);
+      rank += (bj.w > bi) || (bj.w == bi && j + 3 < i);
     }
-    for (int o = tpb >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-    const bool sel = sub == 0 && i < NB && rank < K_eff;
-    // ascending output position = number of routed blocks with a lower index
-    const unsigned bal = __ballot_sync(0xffffffffu, sel);
-    if (lane == 0) wsum[warp] = __popc(bal);
-    __syncthreads();
-    if (warp == 0) {
-      const int c = lane < nw ? wsum[lane] : 0;
-      int incl = c;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const int run = base == 0 ? 0 : wsum[nw];
-      __syncwarp();
-      if (lane < nw) wsum[lane] = run + incl - c;
-      if (lane == 31) wsum[nw] = run + incl;
-    }
-    __syncthreads();
-    if (sel) {
-      const int pos = wsum[warp] + __popc(bal & ((1u << lane) - 1u));
-      routed[(size_t)u * K_eff + pos] = i;
-      if (routed_out) routed_out[(size_t)u * K_eff + pos] = i;
-    }
-    __syncthreads();
+  }
+  for (int o = tpb >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+  const bool sel = mine && sub == 0 && rank < K_eff;
+  const unsigned bal = __ballot_sync(0xffffffffu, sel);
+  if (lane == 0) wsum[warp] = __popc(bal);
+  __syncthreads();
+  int before = 0, total = 0;  // selected blocks of this CTA in lower warps, and in the whole CTA
+#pragma unroll
+  for (int w = 0; w < nw; ++w) {
+    const int c = wsum[w];
+    before += w < warp ? c : 0;
+    total += c;
+  }
+  if (tid < kRouteCluster) st_cluster_s32(&cnt[crank], (uint32_t)tid, total);
+  cluster_sync();  // every CTA's count is everywhere; no peer access follows
+  int offset = 0;
+  for (int c = 0; c < (int)crank; ++c) offset += cnt[c];
+  if (sel) {
+    const int pos = offset + before + __popc(bal & ((1u << lane) - 1u));
+    routed[(size_t)u * K_eff + pos] = i;
+    if (routed_out) routed_out[(size_t)u * K_eff + pos] = i;
   }
 }
 
@@ -250,7 +263,7 @@ cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, in
   const int G = n_q_heads / n_kv_heads;
   const float cq = 1.f / (sqrtf((float)L.d) * (float)G);
   const size_t smem = ((size_t)L.NB + 3) / 4 * 16;  // at most 2048 blocks: 8 KB
-  route_kernel<<<L.units, kRouteThreads, smem, s>>>(L, G, n_q_heads, n_kv_heads, P.K_eff, cq, q, cache,
+  route_kernel<<<L.units * kRouteCluster, kRouteThreads, smem, s>>>(L, G, n_q_heads, n_kv_heads, P.K_eff, cq, q, cache,
                                                     reinterpret_cast<int32_t*>(ws + P.off_routed), routed_out);
   return cudaGetLastError();
 }
