@@ -38,7 +38,7 @@ constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kUTok = 64;              // U rows per chunk
 constexpr int kWindowChunk = 256;      // window tokens per work item
 constexpr int kMaxSlots = 8;
-constexpr int kIQ = 2;                 // item descriptors in flight between producer and consumers
+constexpr int kIQ = 3;                 // item descriptors in flight between producer and consumers
 
 struct AttendArgs {
   Layout L;
@@ -171,6 +171,17 @@ __device__ inline float pow2_down(float mx) {
   return ldexpf(1.f, 14 - e);
 }
 
+// Operand registers of one 16x16 fp16 tile stored in fragment order: a full
+// tile holds 16 bytes per lane (at lane * 16); a half tile (8 rows or 8 columns)
+// 8 bytes per lane (at lane * 8).  Both are read with one aligned 16-byte load;
+// for a half tile each lane keeps its own 8 bytes in .x, .y (.z, .w are not
+// meaningful and the caller zeroes what it does not use).
+__device__ inline uint4 ld_tile(uint32_t base, int lane, bool full) {
+  const uint4 v = lds128(base + (uint32_t)(full ? lane * 16 : (lane >> 1) * 16));
+  const bool odd = (lane & 1) != 0;
+  return make_uint4(full ? v.x : (odd ? v.z : v.x), full ? v.y : (odd ? v.w : v.y), v.z, v.w);
+}
+
 // Position in the ring of chunk slots.  Every consumer warp and the producer
 // walk the chunks of all items in the same order, so each keeps its own cursor.
 struct Ring {
@@ -276,15 +287,29 @@ __host__ __device__ inline size_t smem_extra() {
 // ---------------------------------------------------------------------------
 // consumers: one item
 // ---------------------------------------------------------------------------
+template <int D>
+__device__ inline void load_qb(uint32_t qrow, bool valid, int t, uint32_t (&qb)[D / 16][2]) {
+#pragma unroll
+  for (int kt = 0; kt < D / 16; ++kt) {
+    qb[kt][0] = valid ? lds32(qrow + (uint32_t)(16 * kt + 2 * t) * 2u) : 0u;
+    qb[kt][1] = valid ? lds32(qrow + (uint32_t)(16 * kt + 8 + 2 * t) * 2u) : 0u;
+  }
+}
+
+// One work item, processed by the four consumer warps.  A routed block runs in
+// two phases whose register state never coexists: the low-rank phase (head:
+// base score and z; U chunks; merge of the four warps' low-rank state into
+// shared memory) and the exact phase (residual rows, merged the same way),
+// followed by the low-rank value product V_V^T w and the item's partial record.
+// A window item has the exact phase only.  The item's query slot is released
+// once every warp holds the query fragments of its exact phase.
 template <int D, int RT>
-__device__ inline void consume_item(const AttendArgs& a, const Smem& sm, const ItemDesc& it, Ring& rc,
-                                    const uint32_t (&qb)[D / 16][2]) {
+__device__ __forceinline__ void consume_item(const AttendArgs& a, const Smem& sm, const ItemDesc& it, Ring& rc,
+                                             int iq) {
   const Layout& L = a.L;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = lane & 3, gq = lane >> 2;
   const int tid = threadIdx.x;
-  const int u = it.u;
-  const int bseq = u / a.Hkv, h = u % a.Hkv;
   const int r8 = L.r8;
   const int nkk = r8 >> 4;                 // full 16-wide k tiles of r
   const bool rtail = (r8 & 15) != 0;       // one 8-wide tail
@@ -294,272 +319,188 @@ __device__ inline void consume_item(const AttendArgs& a, const Smem& sm, const I
   const bool gv0 = (2 * t) < G, gv1 = (2 * t + 1) < G;
   const float slog2 = a.scale_log2;
   const uint32_t slot0 = smem_u32(sm.slots);
-  (void)bseq;
-  (void)h;
-  // low-rank state (its normaliser is the sum of p over the low-rank tokens, anchor included)
-  Stat sL;
-  sL.m[0] = sL.m[1] = -INFINITY;
-  sL.l[0] = sL.l[1] = 0.f;
-  float w[RT][4];
-#pragma unroll
-  for (int i = 0; i < RT; ++i) w[i][0] = w[i][1] = w[i][2] = w[i][3] = 0.f;
-  // exact-token state (residual rows or window tokens)
-  Stat sX;
-  sX.m[0] = sX.m[1] = -INFINITY;
-  sX.l[0] = sX.l[1] = 0.f;
-  float o[KT][4];
-#pragma unroll
-  for (int i = 0; i < KT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-
-  bool ok = it.ok != 0;
-  float base0 = 0.f, base1 = 0.f;       // c q_g . a_k in base-2 units, columns 2t, 2t+1
-  float us0 = 1.f, us1 = 1.f;           // power-of-two unscale of z, columns 2t, 2t+1
-  uint32_t zh[RT][2], zl[RT][2];        // z as B fragments (k = r, n = group), hi and lo
-
-  if (it.is_block) {
-    // ---------------- head chunk: anchors, residual mask, V_K -> base and z
-    const int hs = rc.slot;
-    ok = mbar_wait(&sm.full[hs], rc.use & 1u, a.err) && ok;
-    rc.next(a.nslot);
-    const uint8_t* head = sm.slots + (size_t)hs * a.slot_bytes;
-    {
-      // q . a_k: the warps split the head dimension, partial sums meet in shared memory
-      const __half* ak = reinterpret_cast<const __half*>(head);
-      constexpr int KPW = KT / kConsumers > 0 ? KT / kConsumers : 1;
-      float part = 0.f;
-#pragma unroll
-      for (int i = 0; i < KPW; ++i) {
-        const int kt = warp * KPW + i;
-        if (kt < KT) {
-          const float2 qf0 = __half22float2(*reinterpret_cast<const __half2*>(&qb[kt][0]));
-          const float2 qf1 = __half22float2(*reinterpret_cast<const __half2*>(&qb[kt][1]));
-          const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(ak + 16 * kt + 2 * t));
-          const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(ak + 16 * kt + 8 + 2 * t));
-          part += qf0.x * a0.x + qf0.y * a0.y + qf1.x * a1.x + qf1.y * a1.y;
-        }
-      }
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);
-      if (t == 0) sm.basebuf[warp * 8 + gq] = part;
-    }
-    if (warp == 0) {
-      for (int j = lane; j < D; j += 32) sm.av[j] = reinterpret_cast<const __half*>(head)[D + j];
-      if (lane < 8) sm.maskbuf[lane] = reinterpret_cast<const uint32_t*>(head + L.off_mask)[lane];
-    }
-    // z^T = q^T V_K^T : n-tiles of 8 r-rows split across warps, shared through zbuf
-    const uint32_t vk = smem_u32(head) + (uint32_t)L.off_vk;
-    for (int nt = warp; nt < (r8 >> 3); nt += kConsumers) {
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int kp = 0; kp < D / 32; ++kp) {
-        const uint4 b = lds128(vk + (uint32_t)(nt * 8 * D * 2 + kp * 512 + lane * 16));
-        mma16816(c, qb[2 * kp][0], 0u, qb[2 * kp][1], 0u, b.x, b.y);
-        mma16816(c, qb[2 * kp + 1][0], 0u, qb[2 * kp + 1][1], 0u, b.z, b.w);
-      }
-      sm.zbuf[nt * 32 + lane] = make_float2(c[0] * slog2, c[1] * slog2);
-    }
-    named_bar_sync(1, kConsumers * 32);  // basebuf, zbuf, av, mask are written; the head slot is read
-    if (lane == 0) mbar_arrive(&sm.empty[hs]);
-    float zf[RT][4];
-#pragma unroll
-    for (int kk = 0; kk < RT; ++kk) {
-      float2 z0 = make_float2(0.f, 0.f), z1 = make_float2(0.f, 0.f);
-      if (kk < nrt) {
-        z0 = sm.zbuf[(2 * kk) * 32 + lane];
-        if (2 * kk + 1 < (r8 >> 3)) z1 = sm.zbuf[(2 * kk + 1) * 32 + lane];
-      }
-      zf[kk][0] = z0.x; zf[kk][1] = z0.y; zf[kk][2] = z1.x; zf[kk][3] = z1.y;
-    }
-    const float* bb = sm.basebuf;
-    base0 = (bb[2 * t] + bb[8 + 2 * t] + bb[16 + 2 * t] + bb[24 + 2 * t]) * slog2;
-    base1 = (bb[2 * t + 1] + bb[9 + 2 * t] + bb[17 + 2 * t] + bb[25 + 2 * t]) * slog2;
-    // z B fragments: b0 = z[16kk + 2t, +1][gq] (C fragment c0, c1 of n-tile 2kk), b1 from n-tile 2kk+1
-    float zmax = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < RT; ++kk)
-      zmax = fmaxf(zmax, fmaxf(fmaxf(fabsf(zf[kk][0]), fabsf(zf[kk][1])), fmaxf(fabsf(zf[kk][2]), fabsf(zf[kk][3]))));
-    zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 1));
-    zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 2));
-    const float zsc = pow2_down(zmax);  // for g = gq
-#pragma unroll
-    for (int kk = 0; kk < RT; ++kk) {
-      split_half2(zf[kk][0] * zsc, zf[kk][1] * zsc, zh[kk][0], zl[kk][0]);
-      split_half2(zf[kk][2] * zsc, zf[kk][3] * zsc, zh[kk][1], zl[kk][1]);
-    }
-    us0 = 1.f / __shfl_sync(0xffffffffu, zsc, 8 * t);
-    us1 = 1.f / __shfl_sync(0xffffffffu, zsc, 8 * t + 4);
-  }
-
-  // ---------------- private chunks (U rows and exact rows), round-robin over warps
-  const int k_first = it.is_block ? 1 : 0;
-  const int k_last = it.is_block ? it.n_chunks - 2 : it.n_chunks - 1;
-  for (int k = k_first; k <= k_last; ++k) {
-    const int slot = rc.slot;
-    const bool have = mbar_wait(&sm.full[slot], rc.use & 1u, a.err);
-    rc.next(a.nslot);
-    if (chunk_owner(it, k) != warp) {  // observed only: release at once
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[slot]);
-      continue;
-    }
-    ok = ok && have;
-    const Chunk c = item_chunk(a, it, k);
-    const uint32_t sb = slot0 + (uint32_t)(slot * a.slot_bytes);
-    if (!have) {
-      // no data: skip the arithmetic, still release the slot
-    } else if (c.kind == 1) {
-      // ---- U rows, pass 1: every score of the chunk, then one rescale
-      constexpr int MT = kUTok / 16;
-      float s[MT][4];
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        const uint32_t tb = sb + (uint32_t)(mt * 16 * r8 * 2);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < RT; ++kk) {
-          if (kk < nkk) {
-            const uint4 v = lds128(tb + (uint32_t)(kk * 512 + lane * 16));
-            mma16816(acc, v.x, v.y, v.z, v.w, zh[kk][0], zh[kk][1]);
-            mma16816(acc, v.x, v.y, v.z, v.w, zl[kk][0], zl[kk][1]);
-          } else if (kk == nkk && rtail) {
-            const uint2 v = lds64(tb + (uint32_t)(kk * 512 + lane * 8));
-            mma1688(acc, v.x, v.y, zh[kk][0]);
-            mma1688(acc, v.x, v.y, zl[kk][0]);
-          }
-        }
-        const int tk0 = c.tok0 + mt * 16 + gq, tk1 = tk0 + 8;
-        const bool m0 = (sm.maskbuf[tk0 >> 5] >> (tk0 & 31)) & 1u;
-        const bool m1 = (sm.maskbuf[tk1 >> 5] >> (tk1 & 31)) & 1u;
-        s[mt][0] = m0 ? -INFINITY : fmaf(acc[0], us0, base0);
-        s[mt][1] = m0 ? -INFINITY : fmaf(acc[1], us1, base1);
-        s[mt][2] = m1 ? -INFINITY : fmaf(acc[2], us0, base0);
-        s[mt][3] = m1 ? -INFINITY : fmaf(acc[3], us1, base1);
-        tile_max(s[mt], mx0, mx1);
-      }
-      float sc0, sc1, ms0, ms1;
-      stat_update(sL, mx0, mx1, sc0, sc1, ms0, ms1);
-#pragma unroll
-      for (int i = 0; i < RT; ++i) { w[i][0] *= sc0; w[i][1] *= sc1; w[i][2] *= sc0; w[i][3] *= sc1; }
-      // ---- pass 2: p, and w += U^T p (U fragments reloaded, transposed in registers)
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        float p[4];
-        probs(s[mt], ms0, ms1, gv0, gv1, p, sL);
-        uint32_t bh0, bl0, bh1, bl1;
-        p_to_b(p, bh0, bl0, bh1, bl1);
-        const uint32_t tb = sb + (uint32_t)(mt * 16 * r8 * 2);
-#pragma unroll
-        for (int mr = 0; mr < RT; ++mr) {
-          if (mr < nkk) {
-            const uint4 v = lds128(tb + (uint32_t)(mr * 512 + lane * 16));
-            const uint32_t A0 = movtrans(v.x), A2 = movtrans(v.y), A1 = movtrans(v.z), A3 = movtrans(v.w);
-            mma16816(w[mr], A0, A1, A2, A3, bh0, bh1);
-            mma16816(w[mr], A0, A1, A2, A3, bl0, bl1);
-          } else if (mr == nkk && rtail) {
-            const uint2 v = lds64(tb + (uint32_t)(mr * 512 + lane * 8));
-            const uint32_t A0 = movtrans(v.x), A2 = movtrans(v.y);
-            mma16816(w[mr], A0, 0u, A2, 0u, bh0, bh1);
-            mma16816(w[mr], A0, 0u, A2, 0u, bl0, bl1);
-          }
-        }
-      }
-    } else {
-      // ---- exact rows (residuals or window), pass 1: scores of the chunk's groups
-      constexpr int MG = 16384 / (64 * D);  // 16-token groups per chunk (2 at d = 128, 4 at d = 64)
-      const int ng = (c.ntok + 15) >> 4;
-      float s[MG][4];
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int gi = 0; gi < MG; ++gi) {
-        s[gi][0] = s[gi][1] = s[gi][2] = s[gi][3] = -INFINITY;
-        if (gi < ng) {
-          const int in_g = min(16, c.ntok - gi * 16);
-          const uint32_t gb = sb + (uint32_t)(gi * 64 * D);
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          if (in_g == 16) {
-#pragma unroll
-            for (int kt = 0; kt < KT; ++kt) {
-              const uint4 v = lds128(gb + (uint32_t)(kt * 512 + lane * 16));
-              mma16816(acc, v.x, v.y, v.z, v.w, qb[kt][0], qb[kt][1]);
-            }
-          } else {
-#pragma unroll
-            for (int kt = 0; kt < KT; ++kt) {
-              const uint2 v = lds64(gb + (uint32_t)(kt * 256 + lane * 8));
-              mma16816(acc, v.x, 0u, v.y, 0u, qb[kt][0], qb[kt][1]);
-            }
-          }
-          const int tk0 = c.tok0 + gi * 16 + gq, tk1 = tk0 + 8;
-          const bool v0 = tk0 < it.nvalid && (gq < in_g);
-          const bool v1 = tk1 < it.nvalid && (gq + 8 < in_g);
-          s[gi][0] = v0 ? acc[0] * slog2 : -INFINITY;
-          s[gi][1] = v0 ? acc[1] * slog2 : -INFINITY;
-          s[gi][2] = v1 ? acc[2] * slog2 : -INFINITY;
-          s[gi][3] = v1 ? acc[3] * slog2 : -INFINITY;
-          tile_max(s[gi], mx0, mx1);
-        }
-      }
-      float sc0, sc1, ms0, ms1;
-      stat_update(sX, mx0, mx1, sc0, sc1, ms0, ms1);
-#pragma unroll
-      for (int i = 0; i < KT; ++i) { o[i][0] *= sc0; o[i][1] *= sc1; o[i][2] *= sc0; o[i][3] *= sc1; }
-      // ---- pass 2: p, and o += V^T p
-#pragma unroll
-      for (int gi = 0; gi < MG; ++gi) {
-        if (gi < ng) {
-          const int in_g = min(16, c.ntok - gi * 16);
-          const uint32_t gb = sb + (uint32_t)(gi * 64 * D);
-          float p[4];
-          probs(s[gi], ms0, ms1, gv0, gv1, p, sX);
-          uint32_t bh0, bl0, bh1, bl1;
-          p_to_b(p, bh0, bl0, bh1, bl1);
-          const uint32_t vb = gb + (uint32_t)(in_g * D * 2);
-          if (in_g == 16) {
-#pragma unroll
-            for (int md = 0; md < KT; ++md) {
-              const uint4 v = lds128(vb + (uint32_t)(md * 512 + lane * 16));
-              mma16816(o[md], v.x, v.y, v.z, v.w, bh0, bh1);
-              mma16816(o[md], v.x, v.y, v.z, v.w, bl0, bl1);
-            }
-          } else {
-#pragma unroll
-            for (int md = 0; md < KT; ++md) {
-              const uint2 v = lds64(vb + (uint32_t)(md * 256 + lane * 8));
-              mma1688(o[md], v.x, v.y, bh0);
-              mma1688(o[md], v.x, v.y, bl0);
-            }
-          }
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[slot]);
-  }
-
-  // ---------------- merge the four warps
-  sL.l[0] = warp_sum_rows(sL.l[0]);
-  sL.l[1] = warp_sum_rows(sL.l[1]);
-  sX.l[0] = warp_sum_rows(sX.l[0]);
-  sX.l[1] = warp_sum_rows(sX.l[1]);
+  const uint32_t qrow = smem_u32(sm.qbuf + ((size_t)iq * 8 + gq) * (D + 8));
+  const bool qvalid = gq < G;
   float* obw = sm.obw;
   float* wbw = sm.wbw;
-  float* stat = sm.stat;
-  float* fin = sm.fin;
-  // the previous item's readers of the merge buffers are done (barrier at its end)
-  if (lane < 4) {
-    float* sw = stat + warp * 32;
-    sw[2 * t] = sL.m[0]; sw[2 * t + 1] = sL.m[1];
-    sw[8 + 2 * t] = sL.l[0]; sw[8 + 2 * t + 1] = sL.l[1];
-    sw[16 + 2 * t] = sX.m[0]; sw[16 + 2 * t + 1] = sX.m[1];
-    sw[24 + 2 * t] = sX.l[0]; sw[24 + 2 * t + 1] = sX.l[1];
-  }
-#pragma unroll
-  for (int md = 0; md < KT; ++md) {
-    float* o0 = obw + ((size_t)warp * D + md * 16 + gq) * 8 + 2 * t;
-    o0[0] = o[md][0]; o0[1] = o[md][1]; o0[64] = o[md][2]; o0[65] = o[md][3];
-  }
+  float* stat = sm.stat;  // [4 warps][mL 8 | lL 8 | mX 8 | lX 8]
+  float* fin = sm.fin;    // [ML 8 | LL 8 | MX 8 | LX 8]
+  float* scl = fin + 32;  // [4 warps][8]: low-rank scale factors
+  float* scx = fin + 64;  // [4 warps][8]: exact-token scale factors
+  bool ok = it.ok != 0;
+  int k = 0;              // chunk index inside the item
+
   if (it.is_block) {
+    // ======================= low-rank phase
+    float base0, base1;        // c q_g . a_k in base-2 units, columns 2t, 2t+1
+    float us0, us1;            // power-of-two unscale of z, columns 2t, 2t+1
+    uint32_t zh[RT][2], zl[RT][2];  // z as B fragments (k = r, n = group), hi and lo
+    {
+      // ---------------- head chunk: anchors, residual mask, V_K -> base and z
+      uint32_t qb[KT][2];
+      load_qb<D>(qrow, qvalid, t, qb);
+      const int hs = rc.slot;
+      ok = mbar_wait(&sm.full[hs], rc.use & 1u, a.err) && ok;
+      rc.next(a.nslot);
+      const uint8_t* head = sm.slots + (size_t)hs * a.slot_bytes;
+      {
+        // q . a_k: the warps split the head dimension, partial sums meet in shared memory
+        const __half* ak = reinterpret_cast<const __half*>(head);
+        constexpr int KPW = KT / kConsumers > 0 ? KT / kConsumers : 1;
+        float part = 0.f;
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt) {
+          if (kt / KPW == warp) {  // compile-time index: q fragments stay in registers
+            const float2 qf0 = __half22float2(*reinterpret_cast<const __half2*>(&qb[kt][0]));
+            const float2 qf1 = __half22float2(*reinterpret_cast<const __half2*>(&qb[kt][1]));
+            const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(ak + 16 * kt + 2 * t));
+            const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(ak + 16 * kt + 8 + 2 * t));
+            part += qf0.x * a0.x + qf0.y * a0.y + qf1.x * a1.x + qf1.y * a1.y;
+          }
+        }
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        if (t == 0) sm.basebuf[warp * 8 + gq] = part;
+      }
+      if (warp == 0) {
+        for (int j = lane; j < D; j += 32) sm.av[j] = reinterpret_cast<const __half*>(head)[D + j];
+        if (lane < 8) sm.maskbuf[lane] = reinterpret_cast<const uint32_t*>(head + L.off_mask)[lane];
+      }
+      // z^T = q^T V_K^T : n-tiles of 8 r-rows split across warps, shared through zbuf
+      const uint32_t vk = smem_u32(head) + (uint32_t)L.off_vk;
+      for (int nt = warp; nt < (r8 >> 3); nt += kConsumers) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        uint4 bv[D / 32];
+#pragma unroll
+        for (int kp = 0; kp < D / 32; ++kp) bv[kp] = lds128(vk + (uint32_t)(nt * 8 * D * 2 + kp * 512 + lane * 16));
+#pragma unroll
+        for (int kp = 0; kp < D / 32; ++kp) {
+          mma16816(c, qb[2 * kp][0], 0u, qb[2 * kp][1], 0u, bv[kp].x, bv[kp].y);
+          mma16816(c, qb[2 * kp + 1][0], 0u, qb[2 * kp + 1][1], 0u, bv[kp].z, bv[kp].w);
+        }
+        sm.zbuf[nt * 32 + lane] = make_float2(c[0] * slog2, c[1] * slog2);
+      }
+      named_bar_sync(1, kConsumers * 32);  // basebuf, zbuf, av, mask are written; the head slot is read
+      if (lane == 0) mbar_arrive(&sm.empty[hs]);
+      float zf[RT][4];
+#pragma unroll
+      for (int kk = 0; kk < RT; ++kk) {
+        float2 z0 = make_float2(0.f, 0.f), z1 = make_float2(0.f, 0.f);
+        if (kk < nrt) {
+          z0 = sm.zbuf[(2 * kk) * 32 + lane];
+          if (2 * kk + 1 < (r8 >> 3)) z1 = sm.zbuf[(2 * kk + 1) * 32 + lane];
+        }
+        zf[kk][0] = z0.x; zf[kk][1] = z0.y; zf[kk][2] = z1.x; zf[kk][3] = z1.y;
+      }
+      const float* bb = sm.basebuf;
+      base0 = (bb[2 * t] + bb[8 + 2 * t] + bb[16 + 2 * t] + bb[24 + 2 * t]) * slog2;
+      base1 = (bb[2 * t + 1] + bb[9 + 2 * t] + bb[17 + 2 * t] + bb[25 + 2 * t]) * slog2;
+      // z B fragments: b0 = z[16kk + 2t, +1][gq] (C fragment c0, c1 of n-tile 2kk), b1 from n-tile 2kk+1
+      float zmax = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < RT; ++kk)
+        zmax = fmaxf(zmax, fmaxf(fmaxf(fabsf(zf[kk][0]), fabsf(zf[kk][1])), fmaxf(fabsf(zf[kk][2]), fabsf(zf[kk][3]))));
+      zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 1));
+      zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 2));
+      const float zsc = pow2_down(zmax);  // for g = gq
+#pragma unroll
+      for (int kk = 0; kk < RT; ++kk) {
+        split_half2(zf[kk][0] * zsc, zf[kk][1] * zsc, zh[kk][0], zl[kk][0]);
+        split_half2(zf[kk][2] * zsc, zf[kk][3] * zsc, zh[kk][1], zl[kk][1]);
+      }
+      us0 = 1.f / __shfl_sync(0xffffffffu, zsc, 8 * t);
+      us1 = 1.f / __shfl_sync(0xffffffffu, zsc, 8 * t + 4);
+    }
+    // ---------------- U chunks, round-robin over warps (every warp observes every chunk in order)
+    Stat sL;  // its normaliser sums p over the low-rank tokens, anchor included
+    sL.m[0] = sL.m[1] = -INFINITY;
+    sL.l[0] = sL.l[1] = 0.f;
+    float w[RT][4];
+#pragma unroll
+    for (int i = 0; i < RT; ++i) w[i][0] = w[i][1] = w[i][2] = w[i][3] = 0.f;
+    for (k = 1; k <= it.n_u; ++k) {
+      const int slot = rc.slot;
+      const bool have = mbar_wait(&sm.full[slot], rc.use & 1u, a.err);
+      rc.next(a.nslot);
+      if (chunk_owner(it, k) == warp) {
+        ok = ok && have;
+        const int tok0 = (k - 1) * kUTok;
+        const uint32_t sb = slot0 + (uint32_t)(slot * a.slot_bytes);
+        if (have) {
+          // ---- pass 1: every score of the chunk, then one rescale.  A half-width last
+          // k tile (r8 % 16 == 8) has its missing half zeroed.
+          constexpr int MT = kUTok / 16;
+          const uint32_t mbase = smem_u32(sm.maskbuf) + (uint32_t)(tok0 >> 5) * 4u;
+          const uint32_t mw0 = lds32(mbase), mw1 = lds32(mbase + 4u);  // residual rows among the chunk's 64
+          float s[MT][4];
+          float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t tb = sb + (uint32_t)(mt * 16 * r8 * 2);
+            uint4 uv[RT];
+#pragma unroll
+            for (int kk = 0; kk < RT; ++kk) uv[kk] = ld_tile(tb + (uint32_t)(kk * 512), lane, kk < nkk);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < RT; ++kk) {
+              if (kk < nrt) {
+                const bool full = kk < nkk;
+                // a half tile holds (x, y) = rows gq and gq + 8 of k 2t..2t+1 only
+                const uint32_t a2 = full ? uv[kk].z : 0u, a3 = full ? uv[kk].w : 0u;
+                mma16816(acc, uv[kk].x, uv[kk].y, a2, a3, zh[kk][0], zh[kk][1]);
+                mma16816(acc, uv[kk].x, uv[kk].y, a2, a3, zl[kk][0], zl[kk][1]);
+              }
+            }
+            const uint32_t wsel = mt < 2 ? mw0 : mw1;
+            const bool m0 = (wsel >> ((mt & 1) * 16 + gq)) & 1u;
+            const bool m1 = (wsel >> ((mt & 1) * 16 + gq + 8)) & 1u;
+            s[mt][0] = m0 ? -INFINITY : fmaf(acc[0], us0, base0);
+            s[mt][1] = m0 ? -INFINITY : fmaf(acc[1], us1, base1);
+            s[mt][2] = m1 ? -INFINITY : fmaf(acc[2], us0, base0);
+            s[mt][3] = m1 ? -INFINITY : fmaf(acc[3], us1, base1);
+            tile_max(s[mt], mx0, mx1);
+          }
+          float sc0, sc1, ms0, ms1;
+          stat_update(sL, mx0, mx1, sc0, sc1, ms0, ms1);
+#pragma unroll
+          for (int i = 0; i < RT; ++i) { w[i][0] *= sc0; w[i][1] *= sc1; w[i][2] *= sc0; w[i][3] *= sc1; }
+          // ---- pass 2: p, and w += U^T p (U fragments reloaded, transposed in registers)
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t tb = sb + (uint32_t)(mt * 16 * r8 * 2);
+            uint4 uv[RT];
+#pragma unroll
+            for (int mr = 0; mr < RT; ++mr) uv[mr] = ld_tile(tb + (uint32_t)(mr * 512), lane, mr < nkk);
+            float p[4];
+            probs(s[mt], ms0, ms1, gv0, gv1, p, sL);
+            uint32_t bh0, bl0, bh1, bl1;
+            p_to_b(p, bh0, bl0, bh1, bl1);
+#pragma unroll
+            for (int mr = 0; mr < RT; ++mr) {
+              if (mr < nrt) {
+                const bool full = mr < nkk;
+                // U^T tile (m = r, k = tokens): a half tile only has the first r half
+                const uint32_t A0 = movtrans(uv[mr].x), A2 = movtrans(uv[mr].y);
+                const uint32_t T2 = movtrans(uv[mr].z), T3 = movtrans(uv[mr].w);
+                const uint32_t A1 = full ? T2 : 0u, A3 = full ? T3 : 0u;
+                mma16816(w[mr], A0, A1, A2, A3, bh0, bh1);
+                mma16816(w[mr], A0, A1, A2, A3, bl0, bl1);
+              }
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    }
+    // ---------------- merge the low-rank state of the four warps (w and its statistics)
+    sL.l[0] = warp_sum_rows(sL.l[0]);
+    sL.l[1] = warp_sum_rows(sL.l[1]);
+    if (lane < 4) {
+      float* sw = stat + warp * 32;
+      sw[2 * t] = sL.m[0]; sw[2 * t + 1] = sL.m[1];
+      sw[8 + 2 * t] = sL.l[0]; sw[8 + 2 * t + 1] = sL.l[1];
+    }
 #pragma unroll
     for (int mr = 0; mr < RT; ++mr) {
       if (mr < nrt) {
@@ -569,38 +510,22 @@ __device__ inline void consume_item(const AttendArgs& a, const Smem& sm, const I
         if (r0 + 8 < r8) { w0[64] = w[mr][2]; w0[65] = w[mr][3]; }
       }
     }
-  }
-  named_bar_sync(1, kConsumers * 32);
-  // merged statistics per query column g (threads 0..7), and the per-warp scale
-  // factors 2^(m_warp - M) that bring each warp's accumulators to the merged maxima
-  float* scl = fin + 32;  // [4 warps][8]: low-rank scale factors
-  float* scx = fin + 64;  // [4 warps][8]: exact-token scale factors
-  if (tid < 8) {
-    const int g = tid;
-    float ML = -INFINITY, MX = -INFINITY;
-    for (int wi = 0; wi < kConsumers; ++wi) { ML = fmaxf(ML, stat[wi * 32 + g]); MX = fmaxf(MX, stat[wi * 32 + 16 + g]); }
-    const float mls = ML == -INFINITY ? 0.f : ML, mxs = MX == -INFINITY ? 0.f : MX;
-    float LL = 0.f, LX = 0.f;
-    for (int wi = 0; wi < kConsumers; ++wi) {
-      const float fl = fast_exp2(stat[wi * 32 + g] - mls), fx = fast_exp2(stat[wi * 32 + 16 + g] - mxs);
-      scl[wi * 8 + g] = fl;
-      scx[wi * 8 + g] = fx;
-      LL += stat[wi * 32 + 8 + g] * fl;
-      LX += stat[wi * 32 + 24 + g] * fx;
+    named_bar_sync(1, kConsumers * 32);
+    if (tid < 8) {
+      const int g = tid;
+      float ML = -INFINITY;
+      for (int wi = 0; wi < kConsumers; ++wi) ML = fmaxf(ML, stat[wi * 32 + g]);
+      const float mls = ML == -INFINITY ? 0.f : ML;
+      float LL = 0.f;
+      for (int wi = 0; wi < kConsumers; ++wi) {
+        const float fl = fast_exp2(stat[wi * 32 + g] - mls);
+        scl[wi * 8 + g] = fl;
+        LL += stat[wi * 32 + 8 + g] * fl;
+      }
+      fin[g] = ML; fin[8 + g] = LL;
     }
-    fin[g] = ML; fin[8 + g] = LL; fin[16 + g] = MX; fin[24 + g] = LX;
-  }
-  named_bar_sync(1, kConsumers * 32);
-  // merge the warps' accumulators in place (into warp 0's area), one element per thread
-  for (int e = tid; e < D * 8; e += kConsumers * 32) {
-    const int d = e >> 3, g = e & 7;
-    float v = 0.f;
-#pragma unroll
-    for (int wi = 0; wi < kConsumers; ++wi) v += scx[wi * 8 + g] * obw[((size_t)wi * D + d) * 8 + g];
-    obw[(size_t)d * 8 + g] = v;
-  }
-  if (it.is_block) {
-    for (int e = tid; e < r8 * 8; e += kConsumers * 32) {
+    named_bar_sync(1, kConsumers * 32);
+    for (int e = tid; e < r8 * 8; e += kConsumers * 32) {  // in place, into warp 0's area
       const int r = e >> 3, g = e & 7;
       float v = 0.f;
 #pragma unroll
@@ -608,9 +533,137 @@ __device__ inline void consume_item(const AttendArgs& a, const Smem& sm, const I
       wbw[(size_t)r * 8 + g] = v;
     }
   }
+
+  // ======================= exact phase (residual rows, or a window item)
+  {
+    uint32_t qb[KT][2];
+    load_qb<D>(qrow, qvalid, t, qb);
+    Stat sX;
+    sX.m[0] = sX.m[1] = -INFINITY;
+    sX.l[0] = sX.l[1] = 0.f;
+    float o[KT][4];
+#pragma unroll
+    for (int i = 0; i < KT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    const int k_last = it.is_block ? it.n_chunks - 2 : it.n_chunks - 1;
+    for (; k <= k_last; ++k) {
+      const int slot = rc.slot;
+      const bool have = mbar_wait(&sm.full[slot], rc.use & 1u, a.err);
+      rc.next(a.nslot);
+      if (chunk_owner(it, k) == warp) {
+        ok = ok && have;
+        const Chunk c = item_chunk(a, it, k);
+        const uint32_t sb = slot0 + (uint32_t)(slot * a.slot_bytes);
+        if (have) {
+          // ---- pass 1: scores of the chunk's 16-token groups.  A group holds 16, 8 (the
+          // last residual group when R8 % 16 == 8) or 0 tokens; all three share one code
+          // path (operands of missing rows are zeroed).
+          constexpr int MG = 16384 / (64 * D);  // 16-token groups per chunk (2 at d = 128, 4 at d = 64)
+          float s[MG][4];
+          float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+          for (int gi = 0; gi < MG; ++gi) {
+            const int in_g = max(0, min(16, c.ntok - gi * 16));
+            const bool full = in_g == 16, any = in_g > 0;
+            const uint32_t gb = sb + (uint32_t)(gi * 64 * D);
+            const uint32_t kst = full ? 512u : 256u;
+            uint4 kv[KT];
+#pragma unroll
+            for (int kt = 0; kt < KT; ++kt) kv[kt] = ld_tile(gb + (uint32_t)kt * kst, lane, full);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kt = 0; kt < KT; ++kt) {
+              // K tile (m = tokens, k = d): a half group has only rows gq: (x, y) = k 2t.., 2t + 8..
+              const uint4 v = kv[kt];
+              const uint32_t a0 = any ? v.x : 0u, a1 = full ? v.y : 0u, a2 = full ? v.z : (any ? v.y : 0u),
+                             a3 = full ? v.w : 0u;
+              mma16816(acc, a0, a1, a2, a3, qb[kt][0], qb[kt][1]);
+            }
+            const int tk0 = c.tok0 + gi * 16 + gq, tk1 = tk0 + 8;
+            const bool v0 = tk0 < it.nvalid && (gq < in_g);
+            const bool v1 = tk1 < it.nvalid && (gq + 8 < in_g);
+            s[gi][0] = v0 ? acc[0] * slog2 : -INFINITY;
+            s[gi][1] = v0 ? acc[1] * slog2 : -INFINITY;
+            s[gi][2] = v1 ? acc[2] * slog2 : -INFINITY;
+            s[gi][3] = v1 ? acc[3] * slog2 : -INFINITY;
+            tile_max(s[gi], mx0, mx1);
+          }
+          float sc0, sc1, ms0, ms1;
+          stat_update(sX, mx0, mx1, sc0, sc1, ms0, ms1);
+#pragma unroll
+          for (int i = 0; i < KT; ++i) { o[i][0] *= sc0; o[i][1] *= sc1; o[i][2] *= sc0; o[i][3] *= sc1; }
+          // ---- pass 2: p, and o += V^T p
+#pragma unroll
+          for (int gi = 0; gi < MG; ++gi) {
+            const int in_g = max(0, min(16, c.ntok - gi * 16));
+            const bool full = in_g == 16, any = in_g > 0;
+            const uint32_t gb = sb + (uint32_t)(gi * 64 * D);
+            const uint32_t kst = full ? 512u : 256u;
+            const uint32_t vb = gb + (uint32_t)(in_g * D * 2);
+            uint4 vv4[KT];
+#pragma unroll
+            for (int md = 0; md < KT; ++md) vv4[md] = ld_tile(vb + (uint32_t)md * kst, lane, full);
+            float p[4];
+            probs(s[gi], ms0, ms1, gv0, gv1, p, sX);
+            uint32_t bh0, bl0, bh1, bl1;
+            p_to_b(p, bh0, bl0, bh1, bl1);
+#pragma unroll
+            for (int md = 0; md < KT; ++md) {
+              // V^T tile (m = d, k = tokens): a half group holds k 0..7 only
+              const uint4 v = vv4[md];
+              const uint32_t a0 = any ? v.x : 0u, a1 = any ? v.y : 0u, a2 = full ? v.z : 0u,
+                             a3 = full ? v.w : 0u;
+              mma16816(o[md], a0, a1, a2, a3, bh0, bh1);
+              mma16816(o[md], a0, a1, a2, a3, bl0, bl1);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    }
+    // ---------------- merge the exact state of the four warps
+    sX.l[0] = warp_sum_rows(sX.l[0]);
+    sX.l[1] = warp_sum_rows(sX.l[1]);
+    if (lane < 4) {
+      float* sw = stat + warp * 32;
+      sw[16 + 2 * t] = sX.m[0]; sw[16 + 2 * t + 1] = sX.m[1];
+      sw[24 + 2 * t] = sX.l[0]; sw[24 + 2 * t + 1] = sX.l[1];
+    }
+#pragma unroll
+    for (int md = 0; md < KT; ++md) {
+      float* o0 = obw + ((size_t)warp * D + md * 16 + gq) * 8 + 2 * t;
+      o0[0] = o[md][0]; o0[1] = o[md][1]; o0[64] = o[md][2]; o0[65] = o[md][3];
+    }
+  }
+  named_bar_sync(1, kConsumers * 32);
+  // every warp holds its query fragments: the producer may reuse this item's query slot
+  if (warp == 0 && lane == 0) mbar_arrive(&sm.iq_empty[iq]);
+  if (tid < 8) {
+    const int g = tid;
+    float MX = -INFINITY;
+    for (int wi = 0; wi < kConsumers; ++wi) MX = fmaxf(MX, stat[wi * 32 + 16 + g]);
+    const float mxs = MX == -INFINITY ? 0.f : MX;
+    float LX = 0.f;
+    for (int wi = 0; wi < kConsumers; ++wi) {
+      const float fx = fast_exp2(stat[wi * 32 + 16 + g] - mxs);
+      scx[wi * 8 + g] = fx;
+      LX += stat[wi * 32 + 24 + g] * fx;
+    }
+    fin[16 + g] = MX; fin[24 + g] = LX;
+    if (!it.is_block) { fin[g] = -INFINITY; fin[8 + g] = 0.f; }  // no low-rank part
+  }
+  named_bar_sync(1, kConsumers * 32);
+  // merge the warps' exact accumulators in place (into warp 0's area), one element per thread
+  for (int e = tid; e < D * 8; e += kConsumers * 32) {
+    const int d = e >> 3, g = e & 7;
+    float v = 0.f;
+#pragma unroll
+    for (int wi = 0; wi < kConsumers; ++wi) v += scx[wi * 8 + g] * obw[((size_t)wi * D + d) * 8 + g];
+    obw[(size_t)d * 8 + g] = v;
+  }
   named_bar_sync(1, kConsumers * 32);
 
-  float* rec = a.partials + ((size_t)u * a.n_items + it.item) * (16 + 8 * D);
+  float* rec = a.partials + ((size_t)it.u * a.n_items + it.item) * (16 + 8 * D);
   // final partial: M = max(M_L, M_X); o = 2^(M_L - M) (V_V^T w + L_L a_v) + 2^(M_X - M) o_X
   auto final_stats = [&](int g, float& aL, float& aX, float& M) {
     const float ML = fin[g], MX = fin[16 + g];
@@ -780,30 +833,18 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
 
   // =========================== consumer warps
   Ring rc = {0, 0};
-  const int t = lane & 3, gq = lane >> 2;
   for (int j = 0;; ++j) {
     const int iq = j % kIQ;
     if (!mbar_wait(&sm.iq_full[iq], (j / kIQ) & 1, a.err)) break;
     const ItemDesc it = sm.iqd[iq];
-    // q as B fragments (k = head dim, n = group): q[gq][16kt + 2t, +1] and [16kt + 8 + 2t, +1]
-    uint32_t qb[D / 16][2];
-    {
-      const uint32_t qrow = smem_u32(sm.qbuf + ((size_t)iq * 8 + gq) * (D + 8));
-      const bool gv = gq < a.G && !it.stop && it.ok;
-#pragma unroll
-      for (int kt = 0; kt < D / 16; ++kt) {
-        qb[kt][0] = gv ? lds32(qrow + (uint32_t)(16 * kt + 2 * t) * 2u) : 0u;
-        qb[kt][1] = gv ? lds32(qrow + (uint32_t)(16 * kt + 8 + 2 * t) * 2u) : 0u;
-      }
-    }
-    named_bar_sync(1, kConsumers * 32);  // every consumer has its copy of the descriptor and of q
-    if (warp == 0 && lane == 0) mbar_arrive(&sm.iq_empty[iq]);
+    named_bar_sync(1, kConsumers * 32);  // every consumer has its copy of the descriptor
     if (it.stop) break;
     if (it.ok) {
-      consume_item<D, RT>(a, sm, it, rc, qb);
+      consume_item<D, RT>(a, sm, it, rc, iq);  // releases the query slot itself
     } else {
       // an out-of-range routed index (raised in the device error word): an empty
       // partial keeps the unit's merge well defined
+      if (warp == 0 && lane == 0) mbar_arrive(&sm.iq_empty[iq]);
       float* rec = a.partials + ((size_t)it.u * a.n_items + it.item) * (16 + 8 * D);
       for (int e = threadIdx.x; e < 16 + 8 * D; e += kConsumers * 32) rec[e] = e < 8 ? -INFINITY : 0.f;
     }
