@@ -872,6 +872,8 @@ cudaError_t launch_one(const AttendArgs& a, int grid, size_t smem, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, attend_kernel<D, RT>, a);
 }
 
+}  // namespace
+
 int sm_count() {
   static int n[64] = {0};
   int dev = 0;
@@ -883,8 +885,6 @@ int sm_count() {
   }
   return n[dev];
 }
-
-}  // namespace
 
 DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k) {
   (void)n_q_heads;

@@ -270,6 +270,10 @@ cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, in
 // combine grid is launched right after (programmatic dependent launch)
 cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
                           const uint8_t* cache, uint8_t* ws, float* out, float* lse, cudaStream_t s);
+// merge n_items partial records [m 8][l 8][o 8 x d] per unit into out (and lse)
+cudaError_t launch_combine_records(int units, int n_items, int n_q_heads, int n_kv_heads, int d,
+                                   const float* partials, float* out, float* lse, cudaStream_t s);
+int sm_count();  // multiprocessors of the current device
 cudaError_t launch_combine(const Layout& L, const DecodePlan& P, int batch, int n_q_heads, int n_kv_heads,
                            const float* partials, float* out, float* lse, cudaStream_t s);
 

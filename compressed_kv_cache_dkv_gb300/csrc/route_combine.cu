@@ -268,12 +268,11 @@ cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const Layout& L, const DecodePlan& P, int batch, int n_q_heads, int n_kv_heads,
-                           const float* partials, float* out, float* lse, cudaStream_t s) {
-  (void)batch;
+cudaError_t launch_combine_records(int units, int n_items, int n_q_heads, int n_kv_heads, int d,
+                                   const float* partials, float* out, float* lse, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
-  const size_t smem = (size_t)P.n_items * 8;  // at most (2048 + 256) items: 18 KB
-  cfg.gridDim = dim3(L.units, n_q_heads / n_kv_heads);
+  const size_t smem = (size_t)n_items * 8;  // at most (2048 + 256) items: 18 KB
+  cfg.gridDim = dim3(units, n_q_heads / n_kv_heads);
   cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -282,8 +281,14 @@ cudaError_t launch_combine(const Layout& L, const DecodePlan& P, int batch, int 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, P.n_items, n_q_heads / n_kv_heads, n_q_heads, n_kv_heads, L.d,
+  return cudaLaunchKernelEx(&cfg, combine_kernel, n_items, n_q_heads / n_kv_heads, n_q_heads, n_kv_heads, d,
                             partials, out, lse);
+}
+
+cudaError_t launch_combine(const Layout& L, const DecodePlan& P, int batch, int n_q_heads, int n_kv_heads,
+                           const float* partials, float* out, float* lse, cudaStream_t s) {
+  (void)batch;
+  return launch_combine_records(L.units, P.n_items, n_q_heads, n_kv_heads, L.d, partials, out, lse, s);
 }
 
 }  // namespace dkv
