@@ -231,6 +231,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-dense-reference", action="store_true",
+                    help="skip timing the dense fp16 decode kernel over one layer of uncompressed K, V")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -362,6 +364,35 @@ def main():
     if st != dkv.DKV_OK:
         raise RuntimeError(f"decode raised device error word {word:#x}")
 
+    # ---------------- dense fp16 reference: one layer of uncompressed K, V (same recipe, on the device)
+    dense = None
+    if not args.no_dense_reference:
+        Kd, Vd = synth.layer_kv_torch(w, layer_ids[0], dev, replica=rank)
+        od = torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.float32, device=dev)
+        ld = torch.empty(w.batch, w.n_q_heads, dtype=torch.float32, device=dev)
+        wsd = torch.zeros(max(256, dkv.dkv_dense_workspace_bytes(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                                                                  w.context)), dtype=torch.uint8, device=dev)
+        n_dense = max(10, min(K_steps, 50))
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                dkv.dkv_dense_decode(qs[0], Kd, Vd, out=od, lse=ld, workspace=wsd, stream=sh)
+            d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            d0.record(stream)
+            for _ in range(n_dense):  # each call reads K and V once (far larger than L2)
+                dkv.dkv_dense_decode(qs[0], Kd, Vd, out=od, lse=ld, workspace=wsd, stream=sh)
+            d1.record(stream)
+            stream.synchronize()
+        dense_ms = d0.elapsed_time(d1) / n_dense
+        dense_bytes = (2 * Kd.numel() * 2 + w.batch * w.n_q_heads * w.head_dim * (2 + 4))
+        st, word = dkv.dkv_get_error(wsd, stream=sh)
+        if st != dkv.DKV_OK:
+            raise RuntimeError(f"dense decode raised device error word {word:#x}")
+        dense = {"kernel": "dense_kernel + combine (dkv_dense_decode)", "calls": n_dense,
+                 "ms_per_layer": dense_ms, "queries_per_s": w.batch * w.n_q_heads / (dense_ms / 1e3),
+                 "bytes_per_layer": dense_bytes, "gbs": dense_bytes / (dense_ms / 1e3) / 1e9,
+                 "context_tokens": w.context}
+        del Kd, Vd
+
     # ---------------- e2e through the C ABI with pinned host buffers
     e2e_steps = args.e2e_steps or max(10, min(K_steps, 50))
     q_host = [q.cpu().pin_memory() for q in qs]
@@ -441,6 +472,9 @@ def main():
         "gpu_launches": K_steps * n_layers * (3 if w.n_blocks else 2),
         "clocks": clocks.summary(),
         "setup_s": t_setup,
+        "dense_reference": None if dense is None else dict(
+            dense, frac=dense["gbs"] / peak,
+            compressed_speedup=dense["ms_per_layer"] / (ms_step / n_layers)),
     }
     ext.close()
     if rank == 0 and not args.no_cpu_baseline:
