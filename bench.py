@@ -44,6 +44,23 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+# ----------------------------------------------------------------------------- multi-rank arithmetic
+
+def max_over_ranks(values, device):
+    """Elementwise maximum of per-rank timings over the process group (every rank gets it)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(world: int, queries_per_step: int, steps: int, ms: float) -> float:
+    """Queries per second of the whole job: every rank runs its own replica of the
+    workload (weak scaling), so all ranks' queries count over the slowest rank's time."""
+    return world * queries_per_step * steps / (ms / 1e3)
+
+
 # ----------------------------------------------------------------------------- byte accounting
 
 def attend_bytes(w, layer: int, top_k: int) -> int:
@@ -423,12 +440,10 @@ def main():
 
     # ---------------- reduce over ranks (max time)
     if world > 1:
-        tt = torch.tensor([ms, e2e_ms, ms_ev], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms, ms_ev = float(tt[0]), float(tt[1]), float(tt[2])
+        ms, e2e_ms, ms_ev = max_over_ranks([ms, e2e_ms, ms_ev], dev)
     ms_step = ms / K_steps
-    value = world * queries_per_step * K_steps / (ms / 1e3)
-    e2e_value = world * queries_per_step * e2e_steps / (e2e_ms / 1e3)
+    value = whole_job_rate(world, queries_per_step, K_steps, ms)
+    e2e_value = whole_job_rate(world, queries_per_step, e2e_steps, e2e_ms)
 
     step_bytes = sum(call_bytes(w, l, top_k) for l in layer_ids)
     att_bytes_step = sum(attend_bytes(w, l, top_k) for l in layer_ids)

@@ -1,0 +1,50 @@
+"""Host logic of the multi-rank bench (weak scaling, one replica per rank) on
+CPU: two gloo ranks reduce their timings to the maximum, and the whole-job rate
+counts every rank's queries over the slowest rank's time.  The decode path
+itself has no collective (units are independent), so nothing else crosses ranks."""
+import multiprocessing as mp
+import os
+import socket
+
+import pytest
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r timed (ms, e2e_ms, ms_with_events) = (10 + r, 20 - r, 30 + 2r)
+        got = bench.max_over_ranks([10.0 + rank, 20.0 - rank, 30.0 + 2 * rank], "cpu")
+        q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_reduce_to_the_slowest_rank():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    out = dict(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in range(world):
+        assert out[r] == [11.0, 20.0, 32.0]
+
+
+def test_whole_job_rate_counts_every_replica():
+    import bench
+    # 192 queries per step, 100 steps in 250 ms on each of 4 ranks -> 4 * 19200 / 0.25 s
+    assert bench.whole_job_rate(4, 192, 100, 250.0) == pytest.approx(4 * 192 * 100 / 0.25)
+    assert bench.whole_job_rate(1, 192, 100, 250.0) * 4 == pytest.approx(bench.whole_job_rate(4, 192, 100, 250.0))
