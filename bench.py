@@ -248,6 +248,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--layout", choices=["fragment", "tc"], default="fragment",
+                    help="cache layout and with it the decode kernel of the timed path: fragment = mma.sync "
+                         "kernel, tc = tcgen05 kernel")
+    ap.add_argument("--no-alt-layout", action="store_true",
+                    help="skip timing the other cache layout's decode kernel over the same step")
     ap.add_argument("--no-dense-reference", action="store_true",
                     help="skip timing the dense fp16 decode kernel over one layer of uncompressed K, V")
     args = ap.parse_args()
@@ -299,26 +304,39 @@ def main():
     dkv.lib()
 
     # ---------------- setup: compress every layer's K, V into its packed cache (untimed)
+    layout_ids = {"fragment": dkv.DKV_LAYOUT_FRAGMENT, "tc": dkv.DKV_LAYOUT_TC}
+    kernel_names = {"fragment": "attend_kernel (mma.sync, block + window attention)",
+                    "tc": "attend_tc_kernel (tcgen05 + TMEM, block + window attention)"}
+
+    def build_caches(layout: str):
+        descs_, caches_ = [], []
+        for layer in layer_ids:
+            descs_.append(dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window,
+                                         w.rank(layer), w.n_residual, layout=layout_ids[layout]))
+        for i, layer in enumerate(layer_ids):
+            K, V = synth.layer_kv_torch(w, layer, dev, replica=rank)
+            caches_.append(dkv.dkv_compress_layout(descs_[i], K, V, workspace=ws))
+            del K, V
+        torch.cuda.synchronize()
+        st_, word_ = dkv.dkv_get_error(ws)
+        if st_ != dkv.DKV_OK:
+            raise RuntimeError(f"compression raised device error word {word_:#x}")
+        return descs_, caches_
+
     t_setup = time.perf_counter()
-    descs, caches, qs, outs, lses = [], [], [], [], []
     ws_bytes = 0
     for layer in layer_ids:
-        d = dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window, w.rank(layer),
-                           w.n_residual)
-        ws_bytes = max(ws_bytes, dkv.dkv_decode_workspace_bytes(d, top_k))
-        descs.append(d)
+        for lay in layout_ids.values():
+            d = dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window, w.rank(layer),
+                               w.n_residual, layout=lay)
+            ws_bytes = max(ws_bytes, dkv.dkv_decode_workspace_bytes(d, top_k))
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-    for i, layer in enumerate(layer_ids):
-        K, V = synth.layer_kv_torch(w, layer, dev, replica=rank)
-        caches.append(dkv.dkv_compress_layout(descs[i], K, V, workspace=ws))
-        del K, V
+    descs, caches = build_caches(args.layout)
+    qs, outs, lses = [], [], []
+    for layer in layer_ids:
         qs.append(torch.from_numpy(synth.queries(w, layer)).to(dev))
         outs.append(torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.float32, device=dev))
         lses.append(torch.empty(w.batch, w.n_q_heads, dtype=torch.float32, device=dev))
-    torch.cuda.synchronize()
-    st, word = dkv.dkv_get_error(ws)
-    if st != dkv.DKV_OK:
-        raise RuntimeError(f"compression raised device error word {word:#x}")
     t_setup = time.perf_counter() - t_setup
     cache_gb = sum(c.numel() for c in caches) / 1e9
     log(f"[bench] rank {rank}: setup {t_setup:.1f} s, packed caches {cache_gb:.2f} GB over {n_layers} layers")
@@ -327,36 +345,44 @@ def main():
     sh = stream.cuda_stream
     ext = ExtEvents()
 
-    def step(events=None):
-        for layer in range(n_layers):
-            dkv.dkv_decode_route(descs[layer], qs[layer], caches[layer], top_k, ws, stream=sh)
-            if events is not None:
-                ext.record(events[layer][0], sh)
-            dkv.dkv_decode_blocks(descs[layer], qs[layer], caches[layer], top_k, ws, stream=sh)
-            if events is not None:
-                ext.record(events[layer][1], sh)
-            dkv.dkv_decode_combine(descs[layer], top_k, outs[layer], ws, lse=lses[layer], stream=sh)
+    def measure(descs_, caches_):
+        """Warm up, capture K steps into two CUDA graphs (one plain: the timed step; one
+        with events around every attention launch: the kernel's duration -- the events
+        split the programmatic launches apart, so that graph runs a little slower),
+        replay each once untimed, then time one replay of each."""
+        def step(events=None):
+            for layer in range(n_layers):
+                dkv.dkv_decode_route(descs_[layer], qs[layer], caches_[layer], top_k, ws, stream=sh)
+                if events is not None:
+                    ext.record(events[layer][0], sh)
+                dkv.dkv_decode_blocks(descs_[layer], qs[layer], caches_[layer], top_k, ws, stream=sh)
+                if events is not None:
+                    ext.record(events[layer][1], sh)
+                dkv.dkv_decode_combine(descs_[layer], top_k, outs[layer], ws, lse=lses[layer], stream=sh)
 
-    # ---------------- warm-up (eager), then capture K steps into graphs: one plain (the
-    # timed step), one with events around every attention launch (the kernel's duration;
-    # the events split the programmatic launches apart, so that graph runs a little slower)
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    stream.synchronize()
-    K_steps = args.steps
-    ev = [[(ext.new(), ext.new()) for _ in range(n_layers)] for _ in range(K_steps)]
-    graph, graph_ev = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for k in range(K_steps):
-            step()
-    with torch.cuda.graph(graph_ev, stream=stream):
-        for k in range(K_steps):
-            step(ev[k])
-    with torch.cuda.stream(stream):  # a graph replays on the current stream
-        graph.replay()  # untimed replays (warm)
-        graph_ev.replay()
-    stream.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                step()
+        stream.synchronize()
+        ev = [[(ext.new(), ext.new()) for _ in range(n_layers)] for _ in range(K_steps)]
+        graph, graph_ev = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for k in range(K_steps):
+                step()
+        with torch.cuda.graph(graph_ev, stream=stream):
+            for k in range(K_steps):
+                step(ev[k])
+        with torch.cuda.stream(stream):  # a graph replays on the current stream
+            graph.replay()  # untimed replays (warm)
+            graph_ev.replay()
+        stream.synchronize()
+        ms_, clocks_ = timed(graph)
+        ms_ev_, clocks_ev_ = timed(graph_ev)
+        attend_ms_ = [ext.elapsed_ms(ev[k][l][0], ev[k][l][1]) for k in range(K_steps) for l in range(n_layers)]
+        st_, word_ = dkv.dkv_get_error(ws, stream=sh)
+        if st_ != dkv.DKV_OK:
+            raise RuntimeError(f"decode raised device error word {word_:#x}")
+        return ms_, clocks_, ms_ev_, clocks_ev_, attend_ms_
 
     # ---------------- timed regions
     def timed(g):
@@ -374,12 +400,8 @@ def main():
             torch.distributed.barrier()
         return t0.elapsed_time(t1), clk
 
-    ms, clocks = timed(graph)
-    ms_ev, clocks_ev = timed(graph_ev)
-    attend_ms = [ext.elapsed_ms(ev[k][l][0], ev[k][l][1]) for k in range(K_steps) for l in range(n_layers)]
-    st, word = dkv.dkv_get_error(ws, stream=sh)
-    if st != dkv.DKV_OK:
-        raise RuntimeError(f"decode raised device error word {word:#x}")
+    K_steps = args.steps
+    ms, clocks, ms_ev, clocks_ev, attend_ms = measure(descs, caches)
 
     # ---------------- dense fp16 reference: one layer of uncompressed K, V (same recipe, on the device)
     dense = None
@@ -438,9 +460,26 @@ def main():
         stream.synchronize()
     e2e_ms = e0.elapsed_time(e1)
 
+    # ---------------- the other cache layout's decode kernel over the same step (same inputs)
+    alt = None
+    if not args.no_alt_layout:
+        alt_layout = "tc" if args.layout == "fragment" else "fragment"
+        if all(dkv.dkv_layout_supported(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window,
+                                        w.rank(l), w.n_residual, layout_ids[alt_layout]) for l in layer_ids):
+            del caches
+            torch.cuda.empty_cache()
+            a_descs, a_caches = build_caches(alt_layout)
+            a_ms, a_clocks, a_ms_ev, _, a_attend_ms = measure(a_descs, a_caches)
+            del a_caches
+            alt = {"layout": alt_layout, "kernel": kernel_names[alt_layout], "ms": a_ms, "ms_ev": a_ms_ev,
+                   "attend_ms_mean": statistics.fmean(a_attend_ms), "clocks": a_clocks.summary()}
+
     # ---------------- reduce over ranks (max time)
     if world > 1:
         ms, e2e_ms, ms_ev = max_over_ranks([ms, e2e_ms, ms_ev], dev)
+        if alt is not None:
+            alt["ms"], alt["ms_ev"], alt["attend_ms_mean"] = max_over_ranks(
+                [alt["ms"], alt["ms_ev"], alt["attend_ms_mean"]], dev)
     ms_step = ms / K_steps
     value = whole_job_rate(world, queries_per_step, K_steps, ms)
     e2e_value = whole_job_rate(world, queries_per_step, e2e_steps, e2e_ms)
@@ -458,23 +497,26 @@ def main():
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "attend_traffic.json")
     if os.path.exists(tpath):
+        # ncu's DRAM bytes per launch, valid while the kernel's source is the one measured
         tinfo = json.load(open(tpath))
-        src = open(os.path.join(ROOT, "compressed_kv_cache_dkv_gb300", "csrc", "attend.cu"), "rb").read()
-        if tinfo.get("attend_cu_sha1") == hashlib.sha1(src).hexdigest() and tinfo.get("config") == w.name:
+        src_name = "attend.cu" if args.layout == "fragment" else "attend_tc.cu"
+        src = open(os.path.join(ROOT, "compressed_kv_cache_dkv_gb300", "csrc", src_name), "rb").read()
+        if (tinfo.get("layout", "fragment") == args.layout and tinfo.get("config") == w.name
+                and tinfo.get("attend_cu_sha1") == hashlib.sha1(src).hexdigest()):
             traffic = tinfo.get("bytes_per_launch")
 
     line = {
         "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": K_steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": wl_name, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "config": {"workload": wl_name, "cache_layout": args.layout, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {cache_gb:.1f} GB of packed caches per step cycle, each layer "
                          f"read once per step", "graph": "K steps captured in one CUDA graph"},
         "hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
         "hbm_frac_of_measured": step_bytes / (ms_step / 1e3) / 1e9 / peak,
         "hbm_frac_of_nominal_8tbs": step_bytes / (ms_step / 1e3) / 1e9 / 8000.0,
         "bytes_per_step": step_bytes,
-        "roofline": {"bound": "hbm", "kernel": "attend_kernel (block + window attention)", "achieved": achieved_gbs,
+        "roofline": {"bound": "hbm", "kernel": kernel_names[args.layout], "achieved": achieved_gbs,
                      "peak": peak, "unit": "GB/s", "frac": achieved_gbs / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
                      "bytes_per_launch": att_bytes_step / n_layers, "mean_launch_us": att_ms_mean * 1e3,
@@ -490,6 +532,13 @@ def main():
         "dense_reference": None if dense is None else dict(
             dense, frac=dense["gbs"] / peak,
             compressed_speedup=dense["ms_per_layer"] / (ms_step / n_layers)),
+        "other_layout": None if alt is None else {
+            "layout": alt["layout"], "kernel": alt["kernel"], "ms_per_step": alt["ms"] / K_steps,
+            "value": whole_job_rate(world, queries_per_step, K_steps, alt["ms"]),
+            "mean_launch_us": alt["attend_ms_mean"] * 1e3,
+            "achieved_gbs": (att_bytes_step / n_layers) / (alt["attend_ms_mean"] / 1e3) / 1e9,
+            "frac": (att_bytes_step / n_layers) / (alt["attend_ms_mean"] / 1e3) / 1e9 / peak,
+            "ms_per_step_with_events": alt["ms_ev"] / K_steps, "clocks": alt["clocks"]},
     }
     ext.close()
     if rank == 0 and not args.no_cpu_baseline:

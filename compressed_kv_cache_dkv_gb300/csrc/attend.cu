@@ -887,12 +887,10 @@ int sm_count() {
 }
 
 DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k) {
-  (void)n_q_heads;
-  (void)n_kv_heads;
   DecodePlan P;
   P.K_eff = (top_k == 0 || top_k >= L.NB) ? L.NB : top_k;
-  P.wchunk_tokens = kWindowChunk;
-  P.n_wchunks = (L.W16 + kWindowChunk - 1) / kWindowChunk;
+  P.wchunk_tokens = tc_eligible(L, n_q_heads, n_kv_heads) ? tc_window_tokens() : kWindowChunk;
+  P.n_wchunks = (L.W16 + P.wchunk_tokens - 1) / P.wchunk_tokens;
   P.n_items = P.K_eff + P.n_wchunks;
   P.off_sched = kWsHeader;  // attention scheduler: work counter, finished-CTA counter
   P.off_routed = round_up(P.off_sched + 8, 256);
@@ -903,6 +901,7 @@ DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k
 
 cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
                           const uint8_t* cache, uint8_t* ws, float* out, float* lse, cudaStream_t s) {
+  if (tc_eligible(L, n_q_heads, n_kv_heads)) return launch_attend_tc(L, P, n_q_heads, n_kv_heads, q, cache, ws, out, lse, s);
   AttendArgs a;
   a.L = L;
   a.G = n_q_heads / n_kv_heads;

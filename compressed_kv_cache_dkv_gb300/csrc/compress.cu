@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
       int t = e / D, j = e % D;
       __half kv = __float2half(0.f), vv = kv;
       if (t < L.W) { kv = Kw[(size_t)t * D + j]; vv = Vw[(size_t)t * D + j]; }
-      *reinterpret_cast<__half*>(win + exact_k_off(L.W16, D, t, j)) = kv;
-      *reinterpret_cast<__half*>(win + exact_v_off(L.W16, D, t, j)) = vv;
+      *reinterpret_cast<__half*>(win + win_k_off(L, t, j)) = kv;
+      *reinterpret_cast<__half*>(win + win_v_off(L, t, j)) = vv;
     }
     return;
   }
@@ -191,8 +191,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
     __half* router = reinterpret_cast<__half*>(unit + L.off_router + (uint64_t)blk * 4 * D);
     router[j] = mn;
     router[D + j] = mx;
-    reinterpret_cast<__half*>(bp)[j] = Kb[j];
-    reinterpret_cast<__half*>(bp)[D + j] = Vb[j];
+    reinterpret_cast<__half*>(bp + L.off_head)[j] = Kb[j];
+    reinterpret_cast<__half*>(bp + L.off_head)[D + j] = Vb[j];
   }
   __syncthreads();
 
@@ -422,7 +422,6 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
   __syncthreads();
 
   // ---- U = X W per token, key error, U rows into the packed layout
-  uint8_t* ubase = bp + L.off_u;
   for (int t0 = 1; t0 < 256; t0 += kChunk) {
     const int nv = min(kChunk, 256 - t0);
     __syncthreads();
@@ -455,14 +454,14 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
       if (lane == 0) errv[tok - 1] = sqrtf(e2);
       for (int kk = lane; kk < r8; kk += 32) {
         const __half v = kk < r ? to_h(ub[kk], a.err) : __float2half(0.f);
-        *reinterpret_cast<__half*>(ubase + a_layout_off(256, r8, tok, kk)) = v;
+        *reinterpret_cast<__half*>(bp + blk_u_off(L, tok, kk)) = v;
       }
       __syncwarp();
     }
   }
   // U row 0 (the anchor) is zero
   for (int kk = tid; kk < r8; kk += nt)
-    *reinterpret_cast<__half*>(ubase + a_layout_off(256, r8, 0, kk)) = __float2half(0.f);
+    *reinterpret_cast<__half*>(bp + blk_u_off(L, 0, kk)) = __float2half(0.f);
   __syncthreads();
 
   // ---- residual selection: R largest errors, ties to the lower token
@@ -494,21 +493,20 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
   const int nres = min(R, 255);
   uint16_t* cold = reinterpret_cast<uint16_t*>(unit + L.off_cold) + (size_t)blk * R8;
   for (int i = tid; i < R8; i += nt) cold[i] = i < nres ? (uint16_t)sel[i] : 0;
-  uint8_t* rb = bp + L.off_res;
   for (int e = tid; e < R8 * D; e += nt) {
     const int i = e / D, j = e % D;
     __half kv = __float2half(0.f), vv = kv;
     if (i < nres) { kv = Kb[(size_t)sel[i] * D + j]; vv = Vb[(size_t)sel[i] * D + j]; }
-    *reinterpret_cast<__half*>(rb + exact_k_off(R8, D, i, j)) = kv;
-    *reinterpret_cast<__half*>(rb + exact_v_off(R8, D, i, j)) = vv;
+    *reinterpret_cast<__half*>(bp + blk_resk_off(L, i, j)) = kv;
+    *reinterpret_cast<__half*>(bp + blk_resv_off(L, i, j)) = vv;
   }
-  // ---- V_K (B^T layout) and V_V^T (A layout) from W
+  // ---- V_K (B^T layout) and V_V from W
   for (int e = tid; e < r8 * D; e += nt) {
     const int k = e / D, j = e % D;
     __half vk = __float2half(0.f), vv = vk;
     if (k < r) { vk = to_h(Wm[j * r + k], a.err); vv = to_h(Wm[(D + j) * r + k], a.err); }
     *reinterpret_cast<__half*>(bp + L.off_vk + bt_layout_off(r8, D, k, j)) = vk;
-    *reinterpret_cast<__half*>(bp + L.off_vv + a_layout_off(D, r8, j, k)) = vv;
+    *reinterpret_cast<__half*>(bp + blk_vv_off(L, k, j)) = vv;
   }
 }
 

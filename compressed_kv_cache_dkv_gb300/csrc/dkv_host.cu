@@ -19,6 +19,8 @@ bool make_layout(const dkv_desc* d, Layout* L) {
   L->W16 = d->window_pad;
   L->NB = d->n_blocks;
   L->units = d->n_units;
+  L->tc = d->layout == DKV_LAYOUT_TC ? 1 : 0;
+  L->off_head = L->tc ? d->blk_off_vk - 4ull * d->head_dim : 0;
   L->off_mask = d->blk_off_mask;
   L->off_vk = d->blk_off_vk;
   L->off_u = d->blk_off_u;
@@ -76,6 +78,7 @@ int dkv_layout(dkv_desc* d) {
   if (d->batch < 1 || d->n_q_heads < 1 || d->n_kv_heads < 1 || d->head_dim < 1 || d->n_blocks < 0 ||
       d->window < 0 || d->rank < 0 || d->n_residual < 0 || d->block_size < 1)
     return DKV_ERR_ARG;
+  if (d->layout != DKV_LAYOUT_FRAGMENT && d->layout != DKV_LAYOUT_TC) return DKV_ERR_ARG;
   if (d->n_q_heads % d->n_kv_heads != 0) return DKV_ERR_SHAPE;
   if (d->n_blocks == 0 && d->window == 0) return DKV_ERR_SHAPE;  // nothing to attend
   if (d->block_size != DKV_BLOCK_SIZE) return DKV_ERR_UNSUPPORTED;
@@ -92,12 +95,23 @@ int dkv_layout(dkv_desc* d) {
   d->res_pad = R8;
   d->window_pad = W16;
   d->n_units = d->batch * d->n_kv_heads;
-  d->blk_off_mask = 4 * dd;
-  d->blk_off_vk = 4 * dd + 32;
-  d->blk_off_u = d->blk_off_vk + 2ull * r8 * dd;
-  d->blk_off_res = d->blk_off_u + 2ull * 256 * r8;
-  d->blk_off_vv = d->blk_off_res + 4ull * R8 * dd;
-  d->block_bytes = d->blk_off_vv + 2ull * r8 * dd;
+  if (d->layout == DKV_LAYOUT_TC) {
+    if (!tc_layout(d->head_dim, r8, d->n_residual)) return DKV_ERR_UNSUPPORTED;
+    // tensor-core layout: [U][V_V][a_k a_v][V_K][mask][K_res][V_res] (same bytes, other order)
+    d->blk_off_u = 0;
+    d->blk_off_vv = 2ull * 256 * r8;
+    d->blk_off_vk = d->blk_off_vv + 2ull * r8 * dd + 4 * dd;
+    d->blk_off_mask = d->blk_off_vk + 2ull * r8 * dd;
+    d->blk_off_res = d->blk_off_mask + 32;
+    d->block_bytes = d->blk_off_res + 4ull * R8 * dd;
+  } else {
+    d->blk_off_mask = 4 * dd;
+    d->blk_off_vk = 4 * dd + 32;
+    d->blk_off_u = d->blk_off_vk + 2ull * r8 * dd;
+    d->blk_off_res = d->blk_off_u + 2ull * 256 * r8;
+    d->blk_off_vv = d->blk_off_res + 4ull * R8 * dd;
+    d->block_bytes = d->blk_off_vv + 2ull * r8 * dd;
+  }
   d->block_stride = round_up(d->block_bytes, 128);
   const uint64_t nb = (uint64_t)d->n_blocks;
   d->off_router = 0;

@@ -39,11 +39,47 @@ namespace dkv {
 
 struct Layout {
   int d, r, r8, R, R8, W, W16, NB, units;
+  int tc;              // 1: tensor-core (core-matrix) layout, 0: mma.sync fragment layout
+  uint64_t off_head;   // anchors a_k, a_v (0 in the fragment layout)
   uint64_t off_mask, off_vk, off_u, off_res, off_vv, block_bytes;
   uint64_t off_router, off_blocks, off_cold, off_window, block_stride, unit_stride, total;
 };
 
 __host__ __device__ inline uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------
+// Tensor-core layout (head_dim 128, 8 <= r8 <= 48, 1 <= R <= 128).  Operand
+// matrices are stored as 8 x 8 "core matrices" (8 rows of 16 bytes, 128 B
+// contiguous), the no-swizzle form tcgen05.mma reads through shared-memory
+// descriptors in either K-major or MN-major role.  Block record:
+//   [U: 256 tokens x r8]   plane per 8 r-columns (4096 B: 32 token groups)
+//   [V_V: r8 x d]          plane per 8 r-rows (2048 B: 16 d groups)
+//   [a_k | a_v]            fp16 d each
+//   [V_K: r8 x d]          mma.sync B^T fragment layout (z is computed with mma.sync)
+//   [mask 32 B]            residual rows
+//   [K_res: R8 x d][V_res: R8 x d]  plane per 8 token rows (2048 B: 16 d groups)
+// Window: groups of 128 tokens, each [K: n x d][V: n x d] in the same planes.
+// ---------------------------------------------------------------------------
+__host__ __device__ inline bool tc_layout(int d, int r8, int R) {
+  return d == 128 && r8 >= 8 && r8 <= 48 && R >= 1 && R <= 128;
+}
+// U element (token t, r-column k)
+__host__ __device__ inline uint32_t tc_u_off(int t, int k) {
+  return (uint32_t)(k >> 3) * 4096u + (uint32_t)(t >> 3) * 128u + (uint32_t)(t & 7) * 16u + (uint32_t)(k & 7) * 2u;
+}
+// element (row, j) of a [rows][d] matrix with d contiguous per row
+__host__ __device__ inline uint32_t tc_rd_off(int d, int row, int j) {
+  return (uint32_t)(row >> 3) * (uint32_t)(d >> 3) * 128u + (uint32_t)(j >> 3) * 128u + (uint32_t)(row & 7) * 16u +
+         (uint32_t)(j & 7) * 2u;
+}
+
+// Section element offsets inside a block record (both layouts)
+__host__ __device__ inline uint64_t blk_u_off(const Layout& L, int t, int k);
+__host__ __device__ inline uint64_t blk_vv_off(const Layout& L, int k, int j);
+__host__ __device__ inline uint64_t blk_resk_off(const Layout& L, int i, int j);
+__host__ __device__ inline uint64_t blk_resv_off(const Layout& L, int i, int j);
+__host__ __device__ inline uint64_t win_k_off(const Layout& L, int t, int j);
+__host__ __device__ inline uint64_t win_v_off(const Layout& L, int t, int j);
 
 // byte offset of element (row, col) inside an "A layout" matrix of rows x cols
 __host__ __device__ inline uint32_t a_layout_off(int rows, int cols, int row, int col) {
@@ -82,6 +118,29 @@ __host__ __device__ inline uint32_t exact_v_off(int n_tok, int d, int t, int j) 
   int in_g = n_tok - (g << 4); in_g = in_g > 16 ? 16 : in_g;
   uint32_t gbase = (uint32_t)g * 64u * (uint32_t)d + (uint32_t)in_g * (uint32_t)d * 2u;
   return gbase + a_layout_off(d, in_g, j, t & 15);
+}
+
+__host__ __device__ inline uint64_t blk_u_off(const Layout& L, int t, int k) {
+  return L.off_u + (L.tc ? tc_u_off(t, k) : a_layout_off(256, L.r8, t, k));
+}
+__host__ __device__ inline uint64_t blk_vv_off(const Layout& L, int k, int j) {
+  return L.off_vv + (L.tc ? tc_rd_off(L.d, k, j) : a_layout_off(L.d, L.r8, j, k));
+}
+__host__ __device__ inline uint64_t blk_resk_off(const Layout& L, int i, int j) {
+  return L.off_res + (L.tc ? tc_rd_off(L.d, i, j) : exact_k_off(L.R8, L.d, i, j));
+}
+__host__ __device__ inline uint64_t blk_resv_off(const Layout& L, int i, int j) {
+  return L.off_res + (L.tc ? (uint64_t)L.R8 * 2 * L.d + tc_rd_off(L.d, i, j) : exact_v_off(L.R8, L.d, i, j));
+}
+// window token t of W16 (relative to the unit's window section)
+__host__ __device__ inline uint64_t win_k_off(const Layout& L, int t, int j) {
+  if (!L.tc) return exact_k_off(L.W16, L.d, t, j);
+  return (uint64_t)(t >> 7) * 128 * 4 * L.d + tc_rd_off(L.d, t & 127, j);
+}
+__host__ __device__ inline uint64_t win_v_off(const Layout& L, int t, int j) {
+  if (!L.tc) return exact_v_off(L.W16, L.d, t, j);
+  const int g = t >> 7, n = L.W16 - 128 * g < 128 ? L.W16 - 128 * g : 128;
+  return (uint64_t)g * 128 * 4 * L.d + (uint64_t)n * 2 * L.d + tc_rd_off(L.d, t & 127, j);
 }
 
 bool make_layout(const dkv_desc* d, Layout* L);  // from a desc filled by dkv_layout()
@@ -270,6 +329,11 @@ cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, in
 // combine grid is launched right after (programmatic dependent launch)
 cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
                           const uint8_t* cache, uint8_t* ws, float* out, float* lse, cudaStream_t s);
+// tcgen05 attention kernel (tensor-core cache layout)
+bool tc_eligible(const Layout& L, int n_q_heads, int n_kv_heads);
+int tc_window_tokens();
+cudaError_t launch_attend_tc(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
+                             const uint8_t* cache, uint8_t* ws, float* out, float* lse, cudaStream_t s);
 // merge n_items partial records [m 8][l 8][o 8 x d] per unit into out (and lse)
 cudaError_t launch_combine_records(int units, int n_items, int n_q_heads, int n_kv_heads, int d,
                                    const float* partials, float* out, float* lse, cudaStream_t s);

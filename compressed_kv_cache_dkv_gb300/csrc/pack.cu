@@ -27,8 +27,8 @@ __global__ void __launch_bounds__(256) pack_kernel(Layout L, dkv_factors f, uint
         kv = ld_h(f.win_K, idx);
         vv = ld_h(f.win_V, idx);
       }
-      *reinterpret_cast<__half*>(win + exact_k_off(L.W16, d, t, j)) = kv;
-      *reinterpret_cast<__half*>(win + exact_v_off(L.W16, d, t, j)) = vv;
+      *reinterpret_cast<__half*>(win + win_k_off(L, t, j)) = kv;
+      *reinterpret_cast<__half*>(win + win_v_off(L, t, j)) = vv;
     }
     return;
   }
@@ -37,8 +37,8 @@ __global__ void __launch_bounds__(256) pack_kernel(Layout L, dkv_factors f, uint
   uint8_t* blk = unit + L.off_blocks + (uint64_t)b * L.block_stride;
   __half* router = reinterpret_cast<__half*>(unit + L.off_router + (uint64_t)b * 4 * d);
   for (int j = tid; j < d; j += nt) {
-    reinterpret_cast<__half*>(blk)[j] = ld_h(f.a_k, base * d + j);
-    reinterpret_cast<__half*>(blk)[d + j] = ld_h(f.a_v, base * d + j);
+    reinterpret_cast<__half*>(blk + L.off_head)[j] = ld_h(f.a_k, base * d + j);
+    reinterpret_cast<__half*>(blk + L.off_head)[d + j] = ld_h(f.a_v, base * d + j);
     router[j] = ld_h(f.kmin, base * d + j);
     router[d + j] = ld_h(f.kmax, base * d + j);
   }
@@ -72,13 +72,13 @@ __global__ void __launch_bounds__(256) pack_kernel(Layout L, dkv_factors f, uint
     __half v = k < r ? ld_h(f.V_K, (base * r + k) * d + j) : zero;
     *reinterpret_cast<__half*>(blk + L.off_vk + bt_layout_off(r8, d, k, j)) = v;
   }
-  // U [256][r8] in A layout, row 0 (the anchor) all zero
+  // U [256][r8], row 0 (the anchor) all zero
   for (int e = tid; e < 256 * r8; e += nt) {
     int t = e / r8, k = e % r8;
     __half v = (t >= 1 && k < r) ? ld_h(f.U, (base * 255 + (t - 1)) * r + k) : zero;
-    *reinterpret_cast<__half*>(blk + L.off_u + a_layout_off(256, r8, t, k)) = v;
+    *reinterpret_cast<__half*>(blk + blk_u_off(L, t, k)) = v;
   }
-  // residual K and V^T groups
+  // residual K and V
   for (int e = tid; e < R8 * d; e += nt) {
     int i = e / d, j = e % d;
     __half kv = zero, vv = zero;
@@ -86,14 +86,14 @@ __global__ void __launch_bounds__(256) pack_kernel(Layout L, dkv_factors f, uint
       kv = ld_h(f.K_res, (base * R + i) * d + j);
       vv = ld_h(f.V_res, (base * R + i) * d + j);
     }
-    *reinterpret_cast<__half*>(blk + L.off_res + exact_k_off(R8, d, i, j)) = kv;
-    *reinterpret_cast<__half*>(blk + L.off_res + exact_v_off(R8, d, i, j)) = vv;
+    *reinterpret_cast<__half*>(blk + blk_resk_off(L, i, j)) = kv;
+    *reinterpret_cast<__half*>(blk + blk_resv_off(L, i, j)) = vv;
   }
-  // V_V^T [d][r8] in A layout
+  // V_V [r8][d]
   for (int e = tid; e < r8 * d; e += nt) {
     int k = e / d, j = e % d;
     __half v = k < r ? ld_h(f.V_V, (base * r + k) * d + j) : zero;
-    *reinterpret_cast<__half*>(blk + L.off_vv + a_layout_off(d, r8, j, k)) = v;
+    *reinterpret_cast<__half*>(blk + blk_vv_off(L, k, j)) = v;
   }
 }
 

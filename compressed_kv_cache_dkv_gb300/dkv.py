@@ -31,6 +31,8 @@ DKV_DEVERR_TIMEOUT = 0x1
 DKV_DEVERR_INDEX = 0x2
 DKV_DEVERR_RANGE = 0x4
 BLOCK_SIZE = 256
+DKV_LAYOUT_FRAGMENT = 0
+DKV_LAYOUT_TC = 1
 
 EXPORTED = (
     "dkv_version", "dkv_status_string", "dkv_layout", "dkv_layout_bytes",
@@ -50,7 +52,7 @@ class DkvError(RuntimeError):
 class dkv_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "n_q_heads", "n_kv_heads", "head_dim", "block_size", "n_blocks", "window", "rank",
-        "n_residual", "rank_pad", "res_pad", "window_pad", "n_units")] + [
+        "n_residual", "layout", "rank_pad", "res_pad", "window_pad", "n_units")] + [
         (n, ctypes.c_uint64) for n in (
             "blk_off_mask", "blk_off_vk", "blk_off_u", "blk_off_res", "blk_off_vv", "block_bytes",
             "off_router", "off_blocks", "off_cold", "off_window", "block_stride", "unit_stride", "total_bytes")]
@@ -128,11 +130,25 @@ def _stream(stream) -> int | None:
 
 
 def dkv_layout(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int, n_blocks: int, window: int,
-               rank: int, n_residual: int, block_size: int = BLOCK_SIZE) -> dkv_desc:
+               rank: int, n_residual: int, block_size: int = BLOCK_SIZE,
+               layout: int | None = None) -> dkv_desc:
+    """Fill a descriptor.  `layout` is DKV_LAYOUT_FRAGMENT (mma.sync decode kernel, the
+    default) or DKV_LAYOUT_TC (tcgen05 decode kernel; head_dim 128, rank <= 48, 1 <= R <= 128)."""
     d = dkv_desc(batch=batch, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim=head_dim,
-                 block_size=block_size, n_blocks=n_blocks, window=window, rank=rank, n_residual=n_residual)
+                 block_size=block_size, n_blocks=n_blocks, window=window, rank=rank, n_residual=n_residual,
+                 layout=DKV_LAYOUT_FRAGMENT if layout is None else layout)
     _check(lib().dkv_layout(ctypes.byref(d)), "dkv_layout")
     return d
+
+
+def dkv_layout_supported(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int, n_blocks: int, window: int,
+                         rank: int, n_residual: int, layout: int) -> bool:
+    """True when dkv_layout accepts these sizes under `layout`."""
+    try:
+        dkv_layout(batch, n_q_heads, n_kv_heads, head_dim, n_blocks, window, rank, n_residual, layout=layout)
+    except DkvError:
+        return False
+    return True
 
 
 def dkv_layout_bytes(d: dkv_desc) -> int:

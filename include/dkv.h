@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define DKV_VERSION 1
+#define DKV_VERSION 2
 
 #if defined(__GNUC__)
 #define DKV_API __attribute__((visibility("default")))
@@ -73,14 +73,23 @@ extern "C" {
 
 #define DKV_BLOCK_SIZE 256      /* [README Core]: fixed micro-blocks of B_s = 256 tokens */
 
+/* byte order of the packed cache (dkv_desc.layout); both hold the same bytes */
+#define DKV_LAYOUT_FRAGMENT 0   /* operand tiles in mma.sync fragment order (default) */
+#define DKV_LAYOUT_TC       1   /* operand tiles as 8x8 core matrices read by tcgen05.mma:
+                                   head_dim 128, 1 <= rank <= 48, 1 <= n_residual <= 128 */
+
 /*
- * Descriptor of one layer's compressed cache.  The caller sets the first nine
+ * Descriptor of one layer's compressed cache.  The caller sets the first ten
  * fields; dkv_layout() validates them and fills the rest.  Plain old data:
  * pass it by pointer, copy it freely.
  *
  * Supported: head_dim 64 or 128; 1 <= n_q_heads/n_kv_heads <= 8; block_size
  * 256; 0 <= rank <= 128; 0 <= n_residual <= 255; 0 <= n_blocks <= 2048;
- * 0 <= window <= 65536; n_blocks + window > 0.
+ * 0 <= window <= 65536; n_blocks + window > 0.  layout DKV_LAYOUT_TC narrows
+ * this to head_dim 128, 1 <= rank <= 48 and 1 <= n_residual <= 128.  The layout
+ * picks the decode kernel: DKV_LAYOUT_FRAGMENT the mma.sync kernel,
+ * DKV_LAYOUT_TC the tcgen05 kernel (TMEM accumulators).  A cache is only
+ * readable under the layout it was written with.
  */
 typedef struct dkv_desc {
   int32_t batch;        /* sequences B */
@@ -92,6 +101,7 @@ typedef struct dkv_desc {
   int32_t window;       /* exact recency-window tokens W per unit */
   int32_t rank;         /* r: rank of the joint K|V delta ([README Core] item 2) */
   int32_t n_residual;   /* R: exact residual rows per block ([README Core] item 3) */
+  int32_t layout;       /* DKV_LAYOUT_FRAGMENT (0) or DKV_LAYOUT_TC (1) */
   /* ---- filled by dkv_layout() ---- */
   int32_t rank_pad;     /* r rounded up to a multiple of 8 (zero-padded) */
   int32_t res_pad;      /* R rounded up to a multiple of 8 (zero-padded) */
@@ -133,8 +143,9 @@ DKV_API const char* dkv_status_string(int status);
 
 /*
  * Validate the caller-set fields of *d and fill the layout fields.
- * Returns DKV_OK, DKV_ERR_ARG (null / negative), DKV_ERR_SHAPE (Hq % Hkv != 0,
- * nothing to attend) or DKV_ERR_UNSUPPORTED.  Host only; needs no GPU.
+ * Returns DKV_OK, DKV_ERR_ARG (null / negative / unknown layout), DKV_ERR_SHAPE
+ * (Hq % Hkv != 0, nothing to attend) or DKV_ERR_UNSUPPORTED.  Host only; needs
+ * no GPU.
  */
 DKV_API int dkv_layout(dkv_desc* d);
 

@@ -49,29 +49,57 @@ def exact_index(n_tok: int, d: int) -> tuple[np.ndarray, np.ndarray]:
     return K, V
 
 
+def is_tc(desc) -> bool:
+    """The tensor-core (core-matrix) layout, chosen by the descriptor's `layout` field."""
+    return desc.layout == 1
+
+
+def rd_index(rows: int, d: int) -> np.ndarray:
+    """Half-element index of (row, j) of a [rows][d] matrix stored as 8 x 8 core matrices
+    (8 rows of 16 bytes each), one plane of d/8 core matrices per 8 rows."""
+    r = np.arange(rows)[:, None]
+    j = np.arange(d)[None, :]
+    byte = (r // 8) * (d // 8) * 128 + (j // 8) * 128 + (r % 8) * 16 + (j % 8) * 2
+    return byte // 2
+
+
+def u_index(r8: int) -> np.ndarray:
+    """Half-element index of (token t, r-column k) of U in core matrices, one plane per 8 columns."""
+    t = np.arange(256)[:, None]
+    k = np.arange(r8)[None, :]
+    byte = (k // 8) * 4096 + (t // 8) * 128 + (t % 8) * 16 + (k % 8) * 2
+    return byte // 2
+
+
 def unpack_block(cache: np.ndarray, desc, u: int, b: int) -> dict:
     d, r, r8, R, R8 = desc.head_dim, desc.rank, desc.rank_pad, desc.n_residual, desc.res_pad
     unit = u * desc.unit_stride
     blk = unit + desc.off_blocks + b * desc.block_stride
     h = lambda off, n: cache[off:off + 2 * n].view(np.float16)
+    tc = is_tc(desc)
+    head = desc.blk_off_vk - 4 * d if tc else 0
     out = {}
-    out["a_k"] = h(blk, d).copy()
-    out["a_v"] = h(blk + 2 * d, d).copy()
+    out["a_k"] = h(blk + head, d).copy()
+    out["a_v"] = h(blk + head + 2 * d, d).copy()
     words = cache[blk + desc.blk_off_mask: blk + desc.blk_off_mask + 32].view(np.uint32)
     out["mask"] = np.array([(words[i >> 5] >> (i & 31)) & 1 for i in range(256)], dtype=bool)
     vk = h(blk + desc.blk_off_vk, r8 * d)
     out["V_K"] = vk[bt_layout_index(r8, d)][:r].copy()
     uu = h(blk + desc.blk_off_u, 256 * r8)
-    Ufull = uu[a_layout_index(256, r8)]
+    Ufull = uu[u_index(r8)] if tc else uu[a_layout_index(256, r8)]
     out["U_row0"] = Ufull[0].copy()
     out["U"] = Ufull[1:, :r].copy()
     res = h(blk + desc.blk_off_res, 2 * R8 * d)
-    ki, vi = exact_index(R8, d)
+    if tc:
+        ki = rd_index(R8, d)
+        vi = R8 * d + ki
+    else:
+        ki, vi = exact_index(R8, d)
     out["K_res"] = res[ki][:R].copy()
     out["V_res"] = res[vi][:R].copy()
     out["res_pad_zero"] = bool((res[ki][R:] == 0).all() and (res[vi][R:] == 0).all())
     vv = h(blk + desc.blk_off_vv, r8 * d)
-    out["V_V"] = vv[a_layout_index(d, r8)].T[:r].copy()
+    out["V_V"] = (vv[rd_index(r8, d)] if tc else vv[a_layout_index(d, r8)].T)[:r].copy()
     router = h(unit + desc.off_router + b * 4 * d, 2 * d)
     out["kmin"], out["kmax"] = router[:d].copy(), router[d:].copy()
     cold = cache[unit + desc.off_cold + b * R8 * 2: unit + desc.off_cold + (b + 1) * R8 * 2].view(np.uint16)
@@ -83,5 +111,14 @@ def unpack_window(cache: np.ndarray, desc, u: int) -> tuple[np.ndarray, np.ndarr
     d, W, W16 = desc.head_dim, desc.window, desc.window_pad
     off = u * desc.unit_stride + desc.off_window
     win = cache[off: off + W16 * 4 * d].view(np.float16)
-    ki, vi = exact_index(W16, d)
+    if is_tc(desc):
+        ki = np.zeros((W16, d), np.int64)
+        vi = np.zeros((W16, d), np.int64)
+        for g in range(0, W16, 128):
+            n = min(128, W16 - g)
+            base = g * 4 * d // 2          # halves: 128-token groups of K then V
+            ki[g:g + n] = base + rd_index(n, d)
+            vi[g:g + n] = base + n * d + rd_index(n, d)
+    else:
+        ki, vi = exact_index(W16, d)
     return win[ki][:W].copy(), win[vi][:W].copy()

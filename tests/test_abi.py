@@ -24,7 +24,7 @@ def test_library_exports_every_declared_symbol():
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(dkv.EXPORTED)
-    assert lib.dkv_version() == 1
+    assert lib.dkv_version() == 2
 
 
 def test_status_strings():
@@ -41,7 +41,12 @@ def test_layout_validation():
         (dict(n_q_heads=13), dkv.DKV_ERR_SHAPE), (dict(n_blocks=0, window=0), dkv.DKV_ERR_SHAPE),
         (dict(head_dim=96), dkv.DKV_ERR_UNSUPPORTED), (dict(rank=129), dkv.DKV_ERR_UNSUPPORTED),
         (dict(n_residual=256), dkv.DKV_ERR_UNSUPPORTED), (dict(n_q_heads=18), dkv.DKV_ERR_UNSUPPORTED),
-        (dict(block_size=128), dkv.DKV_ERR_UNSUPPORTED),
+        (dict(block_size=128), dkv.DKV_ERR_UNSUPPORTED), (dict(layout=2), dkv.DKV_ERR_ARG),
+        (dict(layout=-1), dkv.DKV_ERR_ARG),
+        # the tensor-core layout: head_dim 128, 1 <= rank <= 48, 1 <= R <= 128
+        (dict(layout=1, head_dim=64), dkv.DKV_ERR_UNSUPPORTED), (dict(layout=1, rank=49), dkv.DKV_ERR_UNSUPPORTED),
+        (dict(layout=1, rank=0), dkv.DKV_ERR_UNSUPPORTED), (dict(layout=1, n_residual=0), dkv.DKV_ERR_UNSUPPORTED),
+        (dict(layout=1, n_residual=129), dkv.DKV_ERR_UNSUPPORTED),
     ]
     for change, status in bad:
         kw = dict(ok, **change)
@@ -50,10 +55,14 @@ def test_layout_validation():
         assert e.value.status == status, change
 
 
-@pytest.mark.parametrize("d,nb,W,r,R", [(128, 30, 512, 32, 40), (128, 252, 1024, 48, 128), (64, 3, 256, 8, 16),
-                                        (128, 5, 17, 24, 5), (64, 0, 100, 0, 0)])
-def test_layout_bytes(d, nb, W, r, R):
-    desc = dkv.dkv_layout(2, 6, 2, d, nb, W, r, R)
+@pytest.mark.parametrize("d,nb,W,r,R,layout", [
+    (128, 30, 512, 32, 40, 0), (128, 252, 1024, 48, 128, 0), (64, 3, 256, 8, 16, 0), (128, 5, 17, 24, 5, 0),
+    (64, 0, 100, 0, 0, 0), (128, 30, 512, 32, 40, 1), (128, 252, 1024, 48, 128, 1), (128, 5, 17, 24, 5, 1),
+    (128, 2, 300, 1, 1, 1)])
+def test_layout_bytes(d, nb, W, r, R, layout):
+    """Both layouts hold the same sections in the same number of bytes, 16-byte aligned."""
+    desc = dkv.dkv_layout(2, 6, 2, d, nb, W, r, R, layout=layout)
+    assert desc.layout == layout
     r8, R8, W16 = -(-r // 8) * 8, -(-R // 8) * 8, -(-W // 16) * 16
     hot = 4 * d + 32 + 2 * r8 * d + 512 * r8 + 4 * R8 * d + 2 * r8 * d
     assert desc.block_bytes == hot
@@ -64,6 +73,12 @@ def test_layout_bytes(d, nb, W, r, R):
     assert desc.unit_stride >= nb * (4 * d + desc.block_stride) + W16 * 4 * d
     assert desc.total_bytes == desc.unit_stride * 2 * 2
     assert dkv.dkv_layout_bytes(desc) == desc.total_bytes
+    # sections do not overlap: [start, end) of each inside the block record
+    sec = sorted([(desc.blk_off_mask, 32), (desc.blk_off_vk, 2 * r8 * d), (desc.blk_off_u, 512 * r8),
+                  (desc.blk_off_res, 4 * R8 * d), (desc.blk_off_vv, 2 * r8 * d)])
+    for (a, na), (b, _) in zip(sec, sec[1:]):
+        assert a + na <= b
+    assert sec[-1][0] + sec[-1][1] <= desc.block_bytes
 
 
 def test_calls_validate_before_touching_the_device():

@@ -32,9 +32,10 @@ RES_LOSS = 0.02
 GAP = 1.1
 
 
-def _gpu_cache(w, layer, K, V):
+def _gpu_cache(w, layer, K, V, layout=dkv.DKV_LAYOUT_FRAGMENT):
     r = w.rank(layer)
-    desc = dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window, r, w.n_residual)
+    desc = dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window, r, w.n_residual,
+                          layout=layout)
     ws = torch.zeros(max(256, dkv.dkv_decode_workspace_bytes(desc, w.top_k)), dtype=torch.uint8, device="cuda")
     cache = dkv.dkv_compress_layout(desc, torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda(), workspace=ws)
     st, word = dkv.dkv_get_error(ws)
@@ -102,9 +103,9 @@ def _check_block(g, ob, Kb, Vb, r, R, stats):
                 assert rel <= RES_BAND, f"row {t}: oracle error {ob.err[t - 1]} vs R-th {thr}"
 
 
-def _run(w, layer, bh_check, decode=True):
+def _run(w, layer, bh_check, decode=True, layout=dkv.DKV_LAYOUT_FRAGMENT):
     K, V = synth.layer_kv(w, layer)
-    desc, cache = _gpu_cache(w, layer, K, V)
+    desc, cache = _gpu_cache(w, layer, K, V, layout)
     host = cache.cpu().numpy()
     r, R = w.rank(layer), w.n_residual
     stats = {"ey": [], "res_diff": [], "res_rel": [], "res_loss": []}
@@ -138,11 +139,15 @@ def _run(w, layer, bh_check, decode=True):
     return stats
 
 
-def test_layout_roundtrip_is_bit_exact():
+LAYOUTS = [dkv.DKV_LAYOUT_FRAGMENT, dkv.DKV_LAYOUT_TC]
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_layout_roundtrip_is_bit_exact(layout):
     w = synth.WORKLOADS["8k"]
     units = H.oracle_units(w, 0, [(0, 0), (0, 1)])
     arrs = H.factor_arrays(units, 128, 32, 40, w.window)
-    desc = dkv.dkv_layout(1, 12, 2, 128, w.n_blocks, w.window, 32, 40)
+    desc = dkv.dkv_layout(1, 12, 2, 128, w.n_blocks, w.window, 32, 40, layout=layout)
     host = dkv.dkv_import_factors(desc, H.to_device(arrs)).cpu().numpy()
     for u in range(2):
         for b in range(w.n_blocks):
@@ -161,9 +166,10 @@ def test_compress_tiny():
     print("tiny", {k: (np.max(v) if len(v) else None) for k, v in s.items() if k != "e2e"}, s.get("e2e"))
 
 
-def test_compress_8k():
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_compress_8k(layout):
     w = synth.WORKLOADS["8k"]
-    s = _run(w, 0, [(0, 0), (0, 1)])
+    s = _run(w, 0, [(0, 0), (0, 1)], layout=layout)
     print("8k", {k: (np.max(v) if len(v) else None) for k, v in s.items() if k != "e2e"}, s.get("e2e"))
 
 
@@ -173,10 +179,11 @@ def test_compress_32k_sampled():
     print("32k", {k: (np.max(v) if len(v) else None) for k, v in s.items() if k != "e2e"}, s.get("e2e"))
 
 
+@pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("layer", [0, 10, 27])
-def test_compress_64k_sampled(layer):
+def test_compress_64k_sampled(layer, layout):
     w = synth.WORKLOADS["64k"]
-    s = _run(w, layer, [(5, 1)])
+    s = _run(w, layer, [(5, 1)], layout=layout)
     print("64k", layer, {k: (np.max(v) if len(v) else None) for k, v in s.items() if k != "e2e"}, s.get("e2e"))
 
 
@@ -188,3 +195,12 @@ def test_compress_edge(kw):
     w = synth.Workload("edge", 1, base["G"], 1, base["d"], base["nb"], base["W"], (base["r"],), base["R"], 2, 4,
                        False, 11)
     _run(w, 0, [(0, 0)])
+
+
+@pytest.mark.parametrize("kw", [dict(r=1, R=1, W=17), dict(r=48, R=128, W=300), dict(nb=0, W=129)])
+def test_compress_edge_tensor_core_layout(kw):
+    base = dict(G=6, nb=3, W=100, r=16, R=24)
+    base.update(kw)
+    w = synth.Workload("edge", 1, base["G"], 1, 128, base["nb"], base["W"], (base["r"],), base["R"], 2, 4,
+                       False, 11)
+    _run(w, 0, [(0, 0)], layout=dkv.DKV_LAYOUT_TC)

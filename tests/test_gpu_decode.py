@@ -20,9 +20,11 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 
-def _run_case(w: synth.Workload, layer: int, top_ks, distinct: int | None = None, units_override=None):
+def _run_case(w: synth.Workload, layer: int, top_ks, distinct: int | None = None, units_override=None,
+              layout: int = dkv.DKV_LAYOUT_FRAGMENT):
     """Import oracle factors for every unit of `w` (optionally replicating `distinct`
-    oracle-compressed units across the batch), decode on the GPU, compare all units."""
+    oracle-compressed units across the batch), decode on the GPU, compare all units.
+    `layout` picks the cache byte order and with it the decode kernel (mma.sync or tcgen05)."""
     r = w.rank(layer)
     bh = [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)]
     n_units = len(bh)
@@ -33,7 +35,8 @@ def _run_case(w: synth.Workload, layer: int, top_ks, distinct: int | None = None
         base_units = H.oracle_units(w, layer, todo)
     units = [base_units[i % len(base_units)] for i in range(n_units)]
     rounded = [H.round_unit(u) for u in base_units]
-    desc = dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window, r, w.n_residual)
+    desc = dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window, r, w.n_residual,
+                          layout=layout)
     arrs = H.factor_arrays(units, w.head_dim, r, w.n_residual, w.window)
     cache = dkv.dkv_import_factors(desc, H.to_device(arrs))
     q = synth.queries(w, layer)
@@ -68,23 +71,30 @@ def test_tiny():
     _run_case(w, 0, [w.top_k, 0, 1, 3])
 
 
-def test_8k():
+TC = dkv.DKV_LAYOUT_TC
+LAYOUTS = [dkv.DKV_LAYOUT_FRAGMENT, TC]
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_8k(layout):
     w = synth.WORKLOADS["8k"]
-    _run_case(w, 0, [w.top_k, 0])
+    _run_case(w, 0, [w.top_k, 0], layout=layout)
 
 
-def test_32k():
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_32k(layout):
     w = synth.WORKLOADS["32k"]
-    _run_case(w, 0, [w.top_k])
+    _run_case(w, 0, [w.top_k], layout=layout)
 
 
+@pytest.mark.parametrize("layout", LAYOUTS)
 @pytest.mark.parametrize("layer", [0, 10, 27])
-def test_64k_full_launch_sampled_units(layer):
+def test_64k_full_launch_sampled_units(layer, layout):
     """Full 64k launch (batch 16, 32 units, R=128, W=1024) with the layer's rank;
     two oracle-compressed units are replicated over the batch (queries differ per
     unit), and every unit is checked against the oracle."""
     w = synth.WORKLOADS["64k"]
-    _run_case(w, layer, [w.top_k], distinct=2)
+    _run_case(w, layer, [w.top_k], distinct=2, layout=layout)
 
 
 def test_sweep16k_full_launch_sampled_units():
@@ -107,6 +117,19 @@ def test_edge_shapes(kw):
     w = _small(**kw)
     tks = [0, 1, 2, w.n_blocks + 3] if w.n_blocks else [0, 4]
     _run_case(w, 0, tks)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(), dict(r=8, R=8), dict(r=1, R=1), dict(r=48, R=128, W=1024), dict(W=0), dict(nb=0, W=300),
+    dict(W=17), dict(W=1), dict(W=129), dict(G=1), dict(G=8), dict(G=3), dict(B=2, Hkv=2, nb=5),
+    dict(r=40, R=100, W=700, nb=9),
+])
+def test_edge_shapes_tensor_core_layout(kw):
+    """The tcgen05 decode kernel: head_dim 128; ragged windows across its 128-token
+    groups, every group size, one-row residual sets, a rank that fills one plane."""
+    w = _small(**dict(dict(d=128), **kw))
+    tks = [0, 1, 2, w.n_blocks + 3] if w.n_blocks else [0, 4]
+    _run_case(w, 0, tks, layout=TC)
 
 
 def test_full_rank_matches_dense_attention():
@@ -175,13 +198,14 @@ def test_decode_is_deterministic_and_stream_ordered():
         assert torch.equal(x, a[0])
 
 
-def test_stage_calls_equal_the_fused_call_and_reuse_the_workspace():
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_stage_calls_equal_the_fused_call_and_reuse_the_workspace(layout):
     """route -> blocks (partials only) -> combine equals dkv_decode_attend (merge
     fused into the attention kernel); one workspace serves many calls of
     different top-K values, since every call leaves its arrival counters at zero."""
     w = synth.WORKLOADS["8k"]
     units = H.oracle_units(w, 0, [(0, 0), (0, 1)])
-    desc = dkv.dkv_layout(1, 12, 2, 128, w.n_blocks, w.window, 32, 40)
+    desc = dkv.dkv_layout(1, 12, 2, 128, w.n_blocks, w.window, 32, 40, layout=layout)
     cache = dkv.dkv_import_factors(desc, H.to_device(H.factor_arrays(units, 128, 32, 40, w.window)))
     q = torch.from_numpy(synth.queries(w, 0)).cuda()
     ws = torch.zeros(dkv.dkv_decode_workspace_bytes(desc, 0), dtype=torch.uint8, device="cuda")
