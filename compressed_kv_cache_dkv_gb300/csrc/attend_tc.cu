@@ -5,11 +5,11 @@
 // Per routed block ("Low-Rank Space Query Scoring" / "Flash-Style LSE Combine",
 // Differential-KV README, section "Core Architecture & Paper Overview"; DKV
 // Zenodo abstract), with M = 128 rows and N = 16 columns per product:
+//   S_X    = K_res [q | 0]              tcgen05, A = K_res (K-major)
 //   z      = V_K (c q)                  mma.sync (r x 8, small)
 //   S_L    = U [z_hi | z_lo]            tcgen05, A = U (K-major), two 128-token tiles
 //   p      = 2^(s - max) over the 255 low-rank tokens and the anchor (s = c q.a_k + U z)
 //   W      = U^T [p_hi | p_lo]          tcgen05, A = U viewed MN-major (no transpose)
-//   S_X    = K_res [q | 0]              tcgen05, A = K_res (K-major)
 //   O_X    = V_res^T [p_hi | p_lo]      tcgen05, A = V_res viewed MN-major
 //   O_L    = V_V^T [w_hi | w_lo]        tcgen05, A = V_V viewed MN-major
 // and the partial (m, l, o) with o = 2^(m_L - m) (O_L + L_L a_v) + 2^(m_X - m) O_X.
@@ -17,11 +17,15 @@
 // two 8-column halves of N, so one MMA carries about 22 bits.  A window item
 // (128 tokens) is the exact half alone.
 //
-// CTA: four consumer warps (warp w owns tensor-memory lanes 32w..32w+31, i.e.
-// one token / r / d row per thread) and one producer warp that streams each
-// item's chunks (the low-rank chunk: U, V_V, head; the exact chunk: K, V) into
-// a ring of 64 KB shared-memory slots with 1-D TMA bulk copies.  Thread 0 issues
-// the tcgen05.mma groups; each group completes its own mbarrier.
+// Two CTAs share an SM.  Each has four consumer warps (warp w owns tensor-memory
+// lanes 32w..32w+31, i.e. one token / r / d row per thread) and one producer
+// warp that streams each item's chunks into a ring of 16 KB shared-memory units
+// with 1-D TMA bulk copies.  A chunk takes one unit (anchors + V_K, one U tile,
+// V_V) or two adjacent units (the exact rows' K or V, when more than 64 rows);
+// a two-unit chunk never wraps around the ring.  Thread 0 issues the
+// tcgen05.mma groups; tcgen05.commit completes both the group's own mbarrier
+// and the "empty" mbarriers of the units the group was the last to read, so a
+// unit returns to the producer as soon as its tensor-core reads are done.
 #include <math.h>
 
 #include "dkv_internal.cuh"
@@ -32,8 +36,9 @@ namespace {
 
 constexpr int kTcConsumers = 4;
 constexpr int kTcThreads = (kTcConsumers + 1) * 32;
-constexpr uint32_t kTcSlot = 64 * 1024;
-constexpr int kTcSlots = 3;
+constexpr int kTcCtasPerSm = 2;
+constexpr uint32_t kUnit = 16 * 1024;
+constexpr int kUnits = 5;
 constexpr int kTcIQ = 2;
 constexpr int kTcWin = 128;          // window tokens per item
 constexpr uint32_t kTmemCols = 128;  // S_L (2 x 16), S_X, W, O_X, O_L (16 each)
@@ -56,16 +61,20 @@ struct TcItem {
   uint64_t base;  // block record or window group (bytes from the cache base)
 };
 
-// shared memory after the ring (byte offsets from the dynamic base)
-constexpr uint32_t kOffBq = kTcSlots * kTcSlot;          // [16 x 128] K-major, 4 KB
-constexpr uint32_t kOffBz = kOffBq + 4096;               // [16 x r16] K-major, <= 1.5 KB
-constexpr uint32_t kOffBPL = kOffBz + 2048;              // [256 x 16] MN-major, 8 KB
+// Shared memory: the ring, then the operand buffers.  A one-unit exact chunk
+// is read as 128 rows by S_X (rows past its end are masked), so at least one
+// unit's worth of allocated memory follows the ring.
+constexpr uint32_t kOffBq = kUnits * kUnit;              // [16 x 128] K-major, 4 KB
+constexpr uint32_t kOffBPL = kOffBq + 4096;              // [256 x 16] MN-major, 8 KB
 constexpr uint32_t kOffBPX = kOffBPL + 8192;             // [128 x 16] MN-major, 4 KB
-constexpr uint32_t kOffBW = kOffBPX + 4096;              // [r16 x 16] MN-major, <= 1.5 KB
+constexpr uint32_t kOffBz = kOffBPX + 4096;              // [16 x r16] K-major, <= 1.5 KB
+constexpr uint32_t kOffBW = kOffBz + 2048;               // [r16 x 16] MN-major, <= 1.5 KB
 constexpr uint32_t kOffQ = kOffBW + 2048;                // [kTcIQ][8][136] fp16 query rows
 constexpr uint32_t kOffZ = kOffQ + kTcIQ * 8 * 136 * 2;  // [r8][8] fp32 z
-constexpr uint32_t kOffMisc = kOffZ + 48 * 8 * 4;        // small arrays below
+constexpr uint32_t kOffMisc = kOffZ + 48 * 8 * 4;        // barriers and small arrays
 constexpr uint32_t kTcSmem = kOffMisc + 2048;
+static_assert(kTcSmem - kOffBq >= kUnit, "guard after the ring");
+static_assert(kTcCtasPerSm * (kTcSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 
 struct TcSmem {
   uint8_t* base;
@@ -73,7 +82,7 @@ struct TcSmem {
   TcItem* iqd;
   float* basebuf;  // [4][8] partial q . a_k
   float* red;      // [2][4][8] per-warp maxima / sums (low-rank half, exact half)
-  float* st;       // [8] base, [8] M_L, [8] L_L, [8] M_X, [8] L_X, [8] w scale
+  float* st;       // [8] base, [8] (unused), [8] L_L
   __half* av;      // [128]
   uint32_t* mask;  // [8]
   uint32_t* tmem;  // allocated tensor-memory address
@@ -85,8 +94,8 @@ __device__ inline TcSmem tc_carve(uint8_t* smem) {
   s.base = smem;
   uint8_t* p = smem + kOffMisc;
   s.full = reinterpret_cast<uint64_t*>(p);
-  s.empty = s.full + kTcSlots;
-  s.iq_full = s.empty + kTcSlots;
+  s.empty = s.full + kUnits;
+  s.iq_full = s.empty + kUnits;
   s.iq_empty = s.iq_full + kTcIQ;
   s.mma = s.iq_empty + kTcIQ;
   s.iqd = reinterpret_cast<TcItem*>(s.mma + 4);
@@ -99,6 +108,21 @@ __device__ inline TcSmem tc_carve(uint8_t* smem) {
   s.flag = reinterpret_cast<int*>(s.tmem + 1);
   return s;
 }
+
+// ---------------------------------------------------------------- ring of units
+// First unit of an s-unit chunk; a chunk that would run past the last unit
+// starts again at unit 0 (the skipped units are left alone this time round).
+// Producer and consumers call it in the same order and so agree on every
+// chunk's place.
+__device__ inline int ring_take(int& pos, int s) {
+  if (pos + s > kUnits) pos = 0;
+  const int u = pos;
+  pos += s;
+  if (pos == kUnits) pos = 0;
+  return u;
+}
+// units of an exact chunk (K or V) of n rows
+__device__ inline int exact_units(int n) { return n * 256 > (int)kUnit ? 2 : 1; }
 
 // ---------------------------------------------------------------- tcgen05 helpers
 // Shared-memory matrix descriptor, no swizzle: start address, LBO = byte stride
@@ -118,6 +142,7 @@ __device__ inline void umma(uint32_t dt, uint64_t ad, uint64_t bd, uint32_t id, 
       "l"(ad), "l"(bd), "r"(id), "r"(acc)
       : "memory");
 }
+// arrive on `bar` once every tcgen05.mma issued so far by this thread has completed
 __device__ inline void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -147,6 +172,10 @@ __device__ inline void split8(const float (&x)[8], uint4& hi, uint4& lo) {
   for (int i = 0; i < 4; ++i) split_half2(x[2 * i], x[2 * i + 1], h[i], l[i]);
   hi = make_uint4(h[0], h[1], h[2], h[3]);
   lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+// zero `bytes` (a multiple of 16 * 128) at shared address addr with the 128 consumer threads
+__device__ inline void zero_smem(uint32_t addr, uint32_t bytes, int tid) {
+  for (uint32_t o = (uint32_t)tid * 16u; o < bytes; o += kTcConsumers * 32 * 16u) sts128(addr + o, make_uint4(0u, 0u, 0u, 0u));
 }
 
 // per-column max / sum over the 128 consumer threads: warp butterfly, then the
@@ -224,8 +253,28 @@ __device__ inline TcItem tc_decode(const TcArgs& a, int gi) {
   return it;
 }
 
+// Ring places of one item's chunks, in streaming order: K, head (anchors, mask,
+// V_K), U tile 0, U tile 1, V, V_V for a block; K, V for a window group.
+struct Places {
+  int k, head, u0, u1, v, vv, sx;  // first units; sx = units of K and of V
+};
+__device__ inline Places take_places(int& pos, const TcItem& it) {
+  Places p;
+  p.sx = exact_units(it.n);
+  p.k = ring_take(pos, p.sx);
+  p.head = p.u0 = p.u1 = p.vv = -1;
+  if (it.is_block) {
+    p.head = ring_take(pos, 1);
+    p.u0 = ring_take(pos, 1);
+    p.u1 = ring_take(pos, 1);
+  }
+  p.v = ring_take(pos, p.sx);
+  if (it.is_block) p.vv = ring_take(pos, 1);
+  return p;
+}
+
 // ---------------------------------------------------------------- the kernel
-__global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
+__global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm) attend_tc_kernel(TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const TcSmem sm = tc_carve(smem);
   const Layout& L = a.L;
@@ -234,7 +283,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
   constexpr int D = 128;
 
   if (tid == 0) {
-    for (int i = 0; i < kTcSlots; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], kTcConsumers); }
+    for (int i = 0; i < kUnits; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], 1); }
     for (int i = 0; i < kTcIQ; ++i) { mbar_init(&sm.iq_full[i], 1); mbar_init(&sm.iq_empty[i], 1); }
     for (int i = 0; i < 4; ++i) mbar_init(&sm.mma[i], 1);
     sm.flag[0] = 0;
@@ -257,10 +306,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
   if (warp == kTcConsumers) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int slot = 0;
-      uint32_t use = 0;
+      int pos = 0;
+      uint32_t eph = 0u, used = 0u;  // per unit: parity of its next release, filled at least once
       bool waited = false;
-      const uint32_t r8 = (uint32_t)L.r8, R8 = (uint32_t)L.R8;
+      const uint32_t r8 = (uint32_t)L.r8;
+      // claim s units starting at u (waiting for their previous contents to be released) and fill them
+      auto put = [&](int u, int s, const uint8_t* src, uint32_t bytes) -> bool {
+        for (int v = u; v < u + s; ++v) {
+          if ((used >> v) & 1u) {
+            if (!mbar_wait(&sm.empty[v], (eph >> v) & 1u, a.err)) return false;
+            eph ^= 1u << v;
+          }
+          used |= 1u << v;
+        }
+        mbar_arrive_expect_tx(&sm.full[u], bytes);
+        bulk_g2s(smem + (size_t)u * kUnit, src, bytes, &sm.full[u], pol);
+        return true;
+      };
       for (int j = 0;; ++j) {
         int gi = blockIdx.x;
         if (j > 0) {
@@ -293,34 +355,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
           __half* qdst = reinterpret_cast<__half*>(smem + kOffQ) + (size_t)iq * 8 * 136;
           for (int g = 0; g < a.G; ++g) bulk_g2s(qdst + (size_t)g * 136, qsrc + (size_t)g * D, row, &sm.iq_full[iq], pol);
         }
-        for (int c = it.is_block ? 0 : 1; c < 2; ++c) {  // block: low-rank chunk, then exact chunk
-          if (use > 0 && !mbar_wait(&sm.empty[slot], (use - 1) & 1u, a.err)) return;
-          uint8_t* dst = smem + (size_t)slot * kTcSlot;
-          const uint8_t* src = a.cache + it.base;
-          if (c == 0) {
-            const uint32_t bu = 512u * r8, bv = 2u * r8 * D, bh = 4u * D + 2u * r8 * D + 32u;
-            mbar_arrive_expect_tx(&sm.full[slot], bu + bv + bh);
-            bulk_g2s(dst, src + L.off_u, bu, &sm.full[slot], pol);
-            bulk_g2s(dst + 32768, src + L.off_vv, bv, &sm.full[slot], pol);
-            bulk_g2s(dst + 49152, src + L.off_head, bh, &sm.full[slot], pol);
-          } else {
-            const uint32_t bk = (uint32_t)it.n * 2u * D;
-            const uint8_t* k0 = it.is_block ? src + L.off_res : src;
-            mbar_arrive_expect_tx(&sm.full[slot], 2u * bk);
-            bulk_g2s(dst, k0, bk, &sm.full[slot], pol);
-            bulk_g2s(dst + 32768, k0 + bk, bk, &sm.full[slot], pol);
-          }
-          if (++slot == kTcSlots) { slot = 0; ++use; }
+        const Places p = take_places(pos, it);
+        const uint8_t* src = a.cache + it.base;
+        const uint32_t bx = (uint32_t)it.n * 2u * D;  // K (or V) bytes of the item
+        const uint8_t* k0 = it.is_block ? src + L.off_res : src;
+        bool ok = put(p.k, p.sx, k0, bx);
+        if (ok && it.is_block) {
+          ok = put(p.head, 1, src, (uint32_t)L.off_u) &&
+               put(p.u0, 1, src + L.off_u, 256u * r8) &&
+               put(p.u1, 1, src + L.off_u + 256u * r8, 256u * r8);
         }
-        (void)R8;
+        ok = ok && put(p.v, p.sx, k0 + bx, bx);
+        if (ok && it.is_block) ok = put(p.vv, 1, src + L.off_vv, 256u * r8);
+        if (!ok) break;
       }
     }
     return;
   }
 
   // =========================== consumer warps
-  int slot = 0;
-  uint32_t use = 0;          // ring position
+  int pos = 0;
+  uint32_t fph = 0u;              // per unit: parity of its next fill
   uint32_t mu[4] = {0, 0, 0, 0};  // uses of the four MMA-group barriers
   const int G = a.G;
   const float slog2 = a.scale_log2;
@@ -328,6 +383,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
   const int t = lane & 3, gq = lane >> 2;
   const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lane quarter
   float* st = sm.st;
+  auto unit_addr = [&](int u) -> uint32_t { return sbase + (uint32_t)u * kUnit; };
+  // wait for the fill of unit u taken with parity `par`
+  auto wait_fill = [&](int u, uint32_t par) -> bool { return mbar_wait(&sm.full[u], par, a.err); };
   int j = 0;
   for (;; ++j) {
     const int iq = j % kTcIQ;
@@ -343,6 +401,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
       continue;
     }
     bool ok = true;
+    // ring places and fill parities of this item's chunks (a unit may serve two chunks of one item)
+    const Places p = take_places(pos, it);
+    uint32_t par_k, par_h = 0, par_u0 = 0, par_u1 = 0, par_v, par_vv = 0;
+    par_k = (fph >> p.k) & 1u; fph ^= 1u << p.k;
+    if (it.is_block) {
+      par_h = (fph >> p.head) & 1u; fph ^= 1u << p.head;
+      par_u0 = (fph >> p.u0) & 1u; fph ^= 1u << p.u0;
+      par_u1 = (fph >> p.u1) & 1u; fph ^= 1u << p.u1;
+    }
+    par_v = (fph >> p.v) & 1u; fph ^= 1u << p.v;
+    if (it.is_block) { par_vv = (fph >> p.vv) & 1u; fph ^= 1u << p.vv; }
+
     const __half* qrows = reinterpret_cast<const __half*>(smem + kOffQ) + (size_t)iq * 8 * 136;
     // ---- B_q [16 x 128] K-major: rows 0..G-1 the queries, the rest zero
     for (int e = tid; e < 256; e += kTcConsumers * 32) {
@@ -351,43 +421,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
       if (n < G) v = *reinterpret_cast<const uint4*>(qrows + n * 136 + kg * 8);
       sts128(sbase + kOffBq + (uint32_t)(n >> 3) * 2048u + (uint32_t)kg * 128u + (uint32_t)(n & 7) * 16u, v);
     }
-    // ring positions of the item's chunks: block = low-rank chunk then exact chunk
-    int sL = -1;
-    uint32_t pL = 0;
-    if (it.is_block) {
-      sL = slot;
-      pL = use & 1u;
-      if (++slot == kTcSlots) { slot = 0; ++use; }
-    }
-    const int sX = slot;
-    const uint32_t pX = use & 1u;
-    if (++slot == kTcSlots) { slot = 0; ++use; }
-
-    // ======================= exact chunk first: its scores need only B_q
-    ok = mbar_wait(&sm.full[sX], pX, a.err) && ok;
-    const uint32_t xb = sbase + (uint32_t)sX * kTcSlot;  // K at +0, V at +32 KB
-    const int n16 = (it.n + 15) & ~15;
-    if (n16 > it.n) {  // zero the V rows n .. n16-1 read by the 16-token k steps (one 8-row plane)
-      const uint32_t zv = xb + 32768u + (uint32_t)(it.n >> 3) * 2048u;
-      for (int e = tid; e < 128; e += kTcConsumers * 32) sts128(zv + (uint32_t)e * 16u, make_uint4(0u, 0u, 0u, 0u));
-    }
     fence_async_smem();
     tc_fence_before();
-    named_bar_sync(1, kTcConsumers * 32);  // B_q and the padding plane are visible to the tensor cores
+    named_bar_sync(1, kTcConsumers * 32);  // B_q is visible to the tensor cores
     tc_fence_after();
+    const int n16 = (it.n + 15) & ~15;
     if (tid == 0) {
-      // S_X = K [q | 0]: K = head dim (8 k steps)
-      const uint64_t a0 = sdesc(xb, 128u, 2048u), b0 = sdesc(sbase + kOffBq, 128u, 2048u);
+      // S_X = K [q | 0]: K = head dim (8 k steps); then K's units go back to the producer
+      ok = wait_fill(p.k, par_k) && ok;
+      tc_fence_after();
+      const uint64_t a0 = sdesc(unit_addr(p.k), 128u, 2048u), b0 = sdesc(sbase + kOffBq, 128u, 2048u);
       for (int ks = 0; ks < 8; ++ks)
         umma(tmem + kColSX, a0 + (uint64_t)(ks * 16), b0 + (uint64_t)(ks * 16), idesc(false, false), ks > 0 ? 1u : 0u);
       umma_commit(&sm.mma[1]);
+      for (int v = p.k; v < p.k + p.sx; ++v) umma_commit(&sm.empty[v]);
       if (!it.is_block) mbar_arrive(&sm.iq_empty[iq]);  // the queries are in B_q
     }
     if (it.is_block) {
-      // ======================= low-rank chunk: head -> base, z; U and V_V pads
-      ok = mbar_wait(&sm.full[sL], pL, a.err) && ok;
-      const uint32_t ub = sbase + (uint32_t)sL * kTcSlot;  // U at +0, V_V at +32 KB, head at +48 KB
-      const uint8_t* head = smem + (size_t)sL * kTcSlot + 49152;
+      // ======================= head chunk -> base, z; U tiles -> S_L
+      ok = wait_fill(p.head, par_h) && ok;
+      const uint8_t* head = smem + (size_t)p.head * kUnit;
       {
         // q fragments (B operand: k = head dim, n = group)
         uint32_t qb[8][2];
@@ -414,9 +467,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
         part += __shfl_xor_sync(0xffffffffu, part, 2);
         if (t == 0) sm.basebuf[warp * 8 + gq] = part;
         if (tid < D) sm.av[tid] = reinterpret_cast<const __half*>(head)[D + tid];
-        if (tid < 8) sm.mask[tid] = reinterpret_cast<const uint32_t*>(head + 4 * D + 2 * r8 * D)[tid];
+        if (tid < 8) sm.mask[tid] = reinterpret_cast<const uint32_t*>(head + L.off_mask)[tid];
         // z^T = q^T V_K^T (V_K in the mma.sync B^T layout): n-tiles of 8 r-rows over the warps
-        const uint32_t vk = smem_u32(head) + 4u * D;
+        const uint32_t vk = smem_u32(head) + (uint32_t)L.off_vk;
         float* zb = reinterpret_cast<float*>(smem + kOffZ);
         for (int nt = warp; nt < (r8 >> 3); nt += kTcConsumers) {
           float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -433,13 +486,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
           zb[(nt * 8 + 2 * t + 1) * 8 + gq] = c[1] * slog2;
         }
       }
-      // zero the padding planes the 16-wide k steps read (U, V_V rows r8 .. r16-1)
-      if (r16 > r8) {
-        const uint32_t zu = ub + (uint32_t)(r8 >> 3) * 4096u, zv = ub + 32768u + (uint32_t)(r8 >> 3) * 2048u;
-        for (int e = tid; e < 256 + 128; e += kTcConsumers * 32)
-          sts128(e < 256 ? zu + (uint32_t)e * 16u : zv + (uint32_t)(e - 256) * 16u, make_uint4(0u, 0u, 0u, 0u));
+      named_bar_sync(1, kTcConsumers * 32);  // base, z, a_v, mask written; the head unit and the query rows are read
+      if (tid == 0) {
+        mbar_arrive(&sm.empty[p.head]);
+        mbar_arrive(&sm.iq_empty[iq]);
       }
-      named_bar_sync(1, kTcConsumers * 32);
       // base score per query (base-2 units) and B_z [16 x r16] K-major: rows 0-7 z_hi, 8-15 z_lo
       if (tid < 8) st[tid] = (sm.basebuf[tid] + sm.basebuf[8 + tid] + sm.basebuf[16 + tid] + sm.basebuf[24 + tid]) * slog2;
       {
@@ -460,19 +511,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
           sts128(row_hi + (uint32_t)nkg * 128u, lo);                                        // N group 1 (rows 8-15)
         }
       }
+      // U tiles: with r8 % 16 == 8 the last 16-wide k step of the last token group reads one
+      // core matrix past the tile; it multiplies zero rows of B_z but must hold finite values
+      ok = wait_fill(p.u0, par_u0) && ok;
+      ok = wait_fill(p.u1, par_u1) && ok;
+      if (r16 > r8 && tid < 16) {
+        const uint32_t tail = 256u * (uint32_t)r8 + (uint32_t)(tid & 7) * 16u;
+        sts128(unit_addr(tid < 8 ? p.u0 : p.u1) + tail, make_uint4(0u, 0u, 0u, 0u));
+      }
       fence_async_smem();
       tc_fence_before();
       named_bar_sync(1, kTcConsumers * 32);
       tc_fence_after();
       if (tid == 0) {
-        mbar_arrive(&sm.iq_empty[iq]);  // queries are in B_q and in the z product
-        // S_L = U [z_hi | z_lo]: two 128-token tiles, K = r16
+        // S_L = U [z_hi | z_lo] per 128-token tile: K = r16; A K-major (LBO = core matrices along r,
+        // SBO = 8-token groups, r8 * 16 B apart)
         const uint32_t nkg = (uint32_t)(r16 >> 3);
-        const uint64_t a0 = sdesc(ub, 4096u, 128u), b0 = sdesc(sbase + kOffBz, 128u, nkg * 128u);
-        for (int tile = 0; tile < 2; ++tile)
+        const uint64_t b0 = sdesc(sbase + kOffBz, 128u, nkg * 128u);
+        for (int tile = 0; tile < 2; ++tile) {
+          const uint64_t a0 = sdesc(unit_addr(tile == 0 ? p.u0 : p.u1), 128u, 16u * (uint32_t)r8);
           for (int ks = 0; ks < (r16 >> 4); ++ks)
-            umma(tmem + kColSL + (uint32_t)tile * 16u, a0 + (uint64_t)(tile * 128 + ks * 512), b0 + (uint64_t)(ks * 16),
+            umma(tmem + kColSL + (uint32_t)tile * 16u, a0 + (uint64_t)(ks * 16), b0 + (uint64_t)(ks * 16),
                  idesc(false, false), ks > 0 ? 1u : 0u);
+        }
         umma_commit(&sm.mma[0]);
       }
     }
@@ -522,12 +583,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
       tc_fence_after();
       if (lane < 8) sm.red[warp * 8 + lane] = pick8(ps, lane);
       if (tid == 0) {
-        // W = U^T [p_hi | p_lo]: A = U viewed MN-major (M = r, K = 256 tokens)
-        const uint32_t ub = sbase + (uint32_t)sL * kTcSlot;
-        const uint64_t a0 = sdesc(ub, 128u, 4096u), b0 = sdesc(sbase + kOffBPL, 256u, 128u);
-        for (int ks = 0; ks < 16; ++ks)
-          umma(tmem + kColW, a0 + (uint64_t)(ks * 16), b0 + (uint64_t)(ks * 32), idesc(true, true), ks > 0 ? 1u : 0u);
+        // W = U^T [p_hi | p_lo]: A = U viewed MN-major (M = r, K = tokens; LBO = 8-token groups,
+        // SBO = core matrices along r); 8 k steps of 16 tokens per tile.  Then the U units are free.
+        const uint64_t b0 = sdesc(sbase + kOffBPL, 256u, 128u);
+        for (int ks = 0; ks < 16; ++ks) {
+          const uint32_t ua = unit_addr(ks < 8 ? p.u0 : p.u1) + (uint32_t)(ks & 7) * 32u * (uint32_t)r8;
+          umma(tmem + kColW, sdesc(ua, 16u * (uint32_t)r8, 128u), b0 + (uint64_t)(ks * 32), idesc(true, true),
+               ks > 0 ? 1u : 0u);
+        }
         umma_commit(&sm.mma[2]);
+        umma_commit(&sm.empty[p.u0]);
+        umma_commit(&sm.empty[p.u1]);
       }
     }
 
@@ -547,7 +613,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
       }
       warp_allmax8(mx);
       named_bar_sync(1, kTcConsumers * 32);  // the previous contents of red are read
-      if (lane < 8) sm.red[32 + warp * 8 + lane] = pick8(mx, lane);  // second half of the scratch (st follows red)
+      if (lane < 8) sm.red[32 + warp * 8 + lane] = pick8(mx, lane);  // second half of the scratch
       if (it.is_block) {
         // low-rank normaliser, from the per-warp sums stored before the barrier
         if (tid < 8) st[16 + tid] = sm.red[tid] + sm.red[8 + tid] + sm.red[16 + tid] + sm.red[24 + tid];
@@ -572,6 +638,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
       }
       if (lane < 8) sm.basebuf[warp * 8 + lane] = pick8(mx, lane);  // per-warp exact sums
     }
+    // V: zero the rows n .. n16-1 read by the 16-token k steps (one 8-row plane)
+    ok = wait_fill(p.v, par_v) && ok;
+    if (n16 > it.n) zero_smem(unit_addr(p.v) + (uint32_t)(it.n >> 3) * 2048u, 2048u, tid);
     if (it.is_block) {
       // ---- W (lane = r) -> B_W [r16 x 16] MN-major, scaled per query by 1 / w_unscale(L_L)
       ok = mma_wait(&sm.mma[2], mu[2], a.err) && ok;
@@ -581,18 +650,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
       if (r < r16) {
         float x[8];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          x[g] = r < r8 ? (wv[g] + wv[8 + g]) * w_scale(LL[g]) : 0.f;
-        }
+        for (int g = 0; g < 8; ++g) x[g] = r < r8 ? (wv[g] + wv[8 + g]) * w_scale(LL[g]) : 0.f;
         uint4 hi, lo;
         split8(x, hi, lo);
         sts128(sbase + kOffBW + (uint32_t)(r >> 3) * 256u + (uint32_t)(r & 7) * 16u, hi);
         sts128(sbase + kOffBW + (uint32_t)(r >> 3) * 256u + 128u + (uint32_t)(r & 7) * 16u, lo);
       }
+      // V_V: zero the r rows r8 .. r16-1 read by the last 16-wide k step (one 8-row plane)
+      ok = wait_fill(p.vv, par_vv) && ok;
+      if (r16 > r8) zero_smem(unit_addr(p.vv) + (uint32_t)(r8 >> 3) * 2048u, 2048u, tid);
     }
     fence_async_smem();
     tc_fence_before();
-    named_bar_sync(1, kTcConsumers * 32);  // B_PX, B_W, the padding plane and the exact sums are written
+    named_bar_sync(1, kTcConsumers * 32);  // B_PX, B_W, the padding planes and the exact sums are written
     tc_fence_after();
 #pragma unroll
     for (int g = 0; g < 8; ++g)
@@ -600,18 +670,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
     if (tid == 0) {
       // O_X = V^T [p_hi | p_lo]: A = V viewed MN-major (M = d, K = n16 tokens)
       {
-        const uint64_t a0 = sdesc(xb + 32768u, 2048u, 128u), b0 = sdesc(sbase + kOffBPX, 256u, 128u);
+        const uint64_t a0 = sdesc(unit_addr(p.v), 2048u, 128u), b0 = sdesc(sbase + kOffBPX, 256u, 128u);
         for (int ks = 0; ks < (n16 >> 4); ++ks)
           umma(tmem + kColOX, a0 + (uint64_t)(ks * 256), b0 + (uint64_t)(ks * 32), idesc(true, true), ks > 0 ? 1u : 0u);
       }
       if (it.is_block) {
         // O_L = V_V^T [w_hi | w_lo]: A = V_V viewed MN-major (M = d, K = r16)
-        const uint32_t vb = sbase + (uint32_t)sL * kTcSlot + 32768u;
-        const uint64_t a0 = sdesc(vb, 2048u, 128u), b0 = sdesc(sbase + kOffBW, 256u, 128u);
+        const uint64_t a0 = sdesc(unit_addr(p.vv), 2048u, 128u), b0 = sdesc(sbase + kOffBW, 256u, 128u);
         for (int ks = 0; ks < (r16 >> 4); ++ks)
           umma(tmem + kColOL, a0 + (uint64_t)(ks * 256), b0 + (uint64_t)(ks * 32), idesc(true, true), ks > 0 ? 1u : 0u);
       }
       umma_commit(&sm.mma[3]);
+      for (int v = p.v; v < p.v + p.sx; ++v) umma_commit(&sm.empty[v]);
+      if (it.is_block) umma_commit(&sm.empty[p.vv]);
     }
 
     // ======================= epilogue: thread = head-dim row d
@@ -628,9 +699,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
         const float ms = M == -INFINITY ? 0.f : M;
         const float aL = fast_exp2(ML[g] - ms), aX = fast_exp2(MX[g] - ms);
         float oL = 0.f;
-        if (it.is_block) {
-          oL = (ol[g] + ol[8 + g]) * w_unscale(LL[g]) + LL[g] * av;
-        }
+        if (it.is_block) oL = (ol[g] + ol[8 + g]) * w_unscale(LL[g]) + LL[g] * av;
         const float o = aL * oL + aX * (ox[g] + ox[8 + g]);
         if (g < G) rec[16 + g * D + dd] = ok ? o : 0.f;
         if (dd == g) {
@@ -639,12 +708,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attend_tc_kernel(TcArgs a) {
         }
       }
     }
-    // release the slots (every MMA that read them has completed) and the tensor memory
+    if (!ok && lane == 0) sm.flag[0] = 1;
+    // the tensor memory and the operand buffers are reused by the next item
     tc_fence_before();
-    if (lane == 0) {
-      if (sL >= 0) mbar_arrive(&sm.empty[sL]);
-      mbar_arrive(&sm.empty[sX]);
-    }
     named_bar_sync(1, kTcConsumers * 32);
     tc_fence_after();
   }
@@ -686,7 +752,7 @@ cudaError_t launch_attend_tc(const Layout& L, const DecodePlan& P, int n_q_heads
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  int grid = sm_count();
+  int grid = kTcCtasPerSm * sm_count();
   grid = grid < a.total ? grid : a.total;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -191,8 +191,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
     __half* router = reinterpret_cast<__half*>(unit + L.off_router + (uint64_t)blk * 4 * D);
     router[j] = mn;
     router[D + j] = mx;
-    reinterpret_cast<__half*>(bp + L.off_head)[j] = Kb[j];
-    reinterpret_cast<__half*>(bp + L.off_head)[D + j] = Vb[j];
+    reinterpret_cast<__half*>(bp)[j] = Kb[j];
+    reinterpret_cast<__half*>(bp)[D + j] = Vb[j];
   }
   __syncthreads();
 

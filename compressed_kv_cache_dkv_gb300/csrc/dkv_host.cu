@@ -20,7 +20,6 @@ bool make_layout(const dkv_desc* d, Layout* L) {
   L->NB = d->n_blocks;
   L->units = d->n_units;
   L->tc = d->layout == DKV_LAYOUT_TC ? 1 : 0;
-  L->off_head = L->tc ? d->blk_off_vk - 4ull * d->head_dim : 0;
   L->off_mask = d->blk_off_mask;
   L->off_vk = d->blk_off_vk;
   L->off_u = d->blk_off_u;
@@ -97,12 +96,12 @@ int dkv_layout(dkv_desc* d) {
   d->n_units = d->batch * d->n_kv_heads;
   if (d->layout == DKV_LAYOUT_TC) {
     if (!tc_layout(d->head_dim, r8, d->n_residual)) return DKV_ERR_UNSUPPORTED;
-    // tensor-core layout: [U][V_V][a_k a_v][V_K][mask][K_res][V_res] (same bytes, other order)
-    d->blk_off_u = 0;
-    d->blk_off_vv = 2ull * 256 * r8;
-    d->blk_off_vk = d->blk_off_vv + 2ull * r8 * dd + 4 * dd;
-    d->blk_off_mask = d->blk_off_vk + 2ull * r8 * dd;
-    d->blk_off_res = d->blk_off_mask + 32;
+    // tensor-core layout: [a_k a_v][mask][V_K][U][V_V][K_res V_res] (same bytes, other order)
+    d->blk_off_mask = 4 * dd;
+    d->blk_off_vk = 4 * dd + 32;
+    d->blk_off_u = d->blk_off_vk + 2ull * r8 * dd;
+    d->blk_off_vv = d->blk_off_u + 2ull * 256 * r8;
+    d->blk_off_res = d->blk_off_vv + 2ull * r8 * dd;
     d->block_bytes = d->blk_off_res + 4ull * R8 * dd;
   } else {
     d->blk_off_mask = 4 * dd;

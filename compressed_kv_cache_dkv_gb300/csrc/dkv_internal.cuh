@@ -40,7 +40,6 @@ namespace dkv {
 struct Layout {
   int d, r, r8, R, R8, W, W16, NB, units;
   int tc;              // 1: tensor-core (core-matrix) layout, 0: mma.sync fragment layout
-  uint64_t off_head;   // anchors a_k, a_v (0 in the fragment layout)
   uint64_t off_mask, off_vk, off_u, off_res, off_vv, block_bytes;
   uint64_t off_router, off_blocks, off_cold, off_window, block_stride, unit_stride, total;
 };
@@ -51,12 +50,14 @@ __host__ __device__ inline uint64_t round_up(uint64_t x, uint64_t a) { return (x
 // Tensor-core layout (head_dim 128, 8 <= r8 <= 48, 1 <= R <= 128).  Operand
 // matrices are stored as 8 x 8 "core matrices" (8 rows of 16 bytes, 128 B
 // contiguous), the no-swizzle form tcgen05.mma reads through shared-memory
-// descriptors in either K-major or MN-major role.  Block record:
-//   [U: 256 tokens x r8]   plane per 8 r-columns (4096 B: 32 token groups)
-//   [V_V: r8 x d]          plane per 8 r-rows (2048 B: 16 d groups)
+// descriptors in either K-major or MN-major role.  Block record (the same
+// sections as the fragment layout; only V_V and the residual rows swap places):
 //   [a_k | a_v]            fp16 d each
-//   [V_K: r8 x d]          mma.sync B^T fragment layout (z is computed with mma.sync)
 //   [mask 32 B]            residual rows
+//   [V_K: r8 x d]          mma.sync B^T fragment layout (z is computed with mma.sync)
+//   [U: 256 tokens x r8]   two 128-token tiles; inside a tile, per 8-token group
+//                          the r8/8 core matrices side by side (r8 * 16 B a group)
+//   [V_V: r8 x d]          plane per 8 r-rows (2048 B: 16 d groups)
 //   [K_res: R8 x d][V_res: R8 x d]  plane per 8 token rows (2048 B: 16 d groups)
 // Window: groups of 128 tokens, each [K: n x d][V: n x d] in the same planes.
 // ---------------------------------------------------------------------------
@@ -64,8 +65,9 @@ __host__ __device__ inline bool tc_layout(int d, int r8, int R) {
   return d == 128 && r8 >= 8 && r8 <= 48 && R >= 1 && R <= 128;
 }
 // U element (token t, r-column k)
-__host__ __device__ inline uint32_t tc_u_off(int t, int k) {
-  return (uint32_t)(k >> 3) * 4096u + (uint32_t)(t >> 3) * 128u + (uint32_t)(t & 7) * 16u + (uint32_t)(k & 7) * 2u;
+__host__ __device__ inline uint32_t tc_u_off(int r8, int t, int k) {
+  return (uint32_t)(t >> 7) * 256u * (uint32_t)r8 + (uint32_t)((t & 127) >> 3) * 16u * (uint32_t)r8 +
+         (uint32_t)(k >> 3) * 128u + (uint32_t)(t & 7) * 16u + (uint32_t)(k & 7) * 2u;
 }
 // element (row, j) of a [rows][d] matrix with d contiguous per row
 __host__ __device__ inline uint32_t tc_rd_off(int d, int row, int j) {
@@ -121,7 +123,7 @@ __host__ __device__ inline uint32_t exact_v_off(int n_tok, int d, int t, int j) 
 }
 
 __host__ __device__ inline uint64_t blk_u_off(const Layout& L, int t, int k) {
-  return L.off_u + (L.tc ? tc_u_off(t, k) : a_layout_off(256, L.r8, t, k));
+  return L.off_u + (L.tc ? tc_u_off(L.r8, t, k) : a_layout_off(256, L.r8, t, k));
 }
 __host__ __device__ inline uint64_t blk_vv_off(const Layout& L, int k, int j) {
   return L.off_vv + (L.tc ? tc_rd_off(L.d, k, j) : a_layout_off(L.d, L.r8, j, k));

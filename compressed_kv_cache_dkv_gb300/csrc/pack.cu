@@ -37,8 +37,8 @@ __global__ void __launch_bounds__(256) pack_kernel(Layout L, dkv_factors f, uint
   uint8_t* blk = unit + L.off_blocks + (uint64_t)b * L.block_stride;
   __half* router = reinterpret_cast<__half*>(unit + L.off_router + (uint64_t)b * 4 * d);
   for (int j = tid; j < d; j += nt) {
-    reinterpret_cast<__half*>(blk + L.off_head)[j] = ld_h(f.a_k, base * d + j);
-    reinterpret_cast<__half*>(blk + L.off_head)[d + j] = ld_h(f.a_v, base * d + j);
+    reinterpret_cast<__half*>(blk)[j] = ld_h(f.a_k, base * d + j);
+    reinterpret_cast<__half*>(blk)[d + j] = ld_h(f.a_v, base * d + j);
     router[j] = ld_h(f.kmin, base * d + j);
     router[d + j] = ld_h(f.kmax, base * d + j);
   }

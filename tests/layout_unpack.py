@@ -64,10 +64,11 @@ def rd_index(rows: int, d: int) -> np.ndarray:
 
 
 def u_index(r8: int) -> np.ndarray:
-    """Half-element index of (token t, r-column k) of U in core matrices, one plane per 8 columns."""
+    """Half-element index of (token t, r-column k) of U in core matrices: two 128-token
+    tiles; inside a tile each 8-token group holds its r8/8 core matrices side by side."""
     t = np.arange(256)[:, None]
     k = np.arange(r8)[None, :]
-    byte = (k // 8) * 4096 + (t // 8) * 128 + (t % 8) * 16 + (k % 8) * 2
+    byte = (t // 128) * 256 * r8 + ((t % 128) // 8) * 16 * r8 + (k // 8) * 128 + (t % 8) * 16 + (k % 8) * 2
     return byte // 2
 
 
@@ -77,10 +78,9 @@ def unpack_block(cache: np.ndarray, desc, u: int, b: int) -> dict:
     blk = unit + desc.off_blocks + b * desc.block_stride
     h = lambda off, n: cache[off:off + 2 * n].view(np.float16)
     tc = is_tc(desc)
-    head = desc.blk_off_vk - 4 * d if tc else 0
     out = {}
-    out["a_k"] = h(blk + head, d).copy()
-    out["a_v"] = h(blk + head + 2 * d, d).copy()
+    out["a_k"] = h(blk, d).copy()
+    out["a_v"] = h(blk + 2 * d, d).copy()
     words = cache[blk + desc.blk_off_mask: blk + desc.blk_off_mask + 32].view(np.uint32)
     out["mask"] = np.array([(words[i >> 5] >> (i & 31)) & 1 for i in range(256)], dtype=bool)
     vk = h(blk + desc.blk_off_vk, r8 * d)
