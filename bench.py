@@ -497,14 +497,13 @@ def main():
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "attend_traffic.json")
     if os.path.exists(tpath):
-        # ncu's DRAM bytes per launch, valid while the kernel's source is the one measured
-        tinfo = json.load(open(tpath))
+        # ncu's DRAM bytes per launch, valid while the kernel's source file is the one measured
         src_name = "attend.cu" if args.layout == "fragment" else "attend_tc.cu"
         src = open(os.path.join(ROOT, "compressed_kv_cache_dkv_gb300", "csrc", src_name), "rb").read()
-        if (tinfo.get("layout", "fragment") == args.layout and tinfo.get("config") == w.name
-                and tinfo.get("attend_cu_sha1") == hashlib.sha1(src).hexdigest()):
-            traffic = tinfo.get("bytes_per_launch")
-
+        sha = hashlib.sha1(src).hexdigest()
+        for entry in json.load(open(tpath)).get("captures", []):
+            if entry.get("source") == src_name and entry.get("source_sha1") == sha and entry.get("config") == w.name:
+                traffic = entry.get("bytes_per_launch")
     line = {
         "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": K_steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
