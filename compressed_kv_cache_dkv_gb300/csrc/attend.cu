@@ -3,7 +3,9 @@
 // Work items of one call: every (unit, routed block) and every (unit, chunk of
 // the exact recency window).  A fixed grid of about two CTAs per SM takes
 // items one after the other (the first statically, the rest from an atomic
-// counter).  Warp 4 is the producer: its lane 0 decodes items and streams their
+// counter).  Half of the window chunks come first (they need nothing from the
+// router, so they overlap its grid), then the routed blocks, then the other
+// half, which fills the tail left by the larger block items.  Warp 4 is the producer: its lane 0 decodes items and streams their
 // packed bytes, chunk by chunk, into a ring of shared-memory slots with 1-D TMA
 // bulk copies (cp.async.bulk + mbarrier complete_tx), running ahead into the
 // next item while the consumers finish the current one.  Warps 0-3 are the
@@ -19,9 +21,8 @@
 //   s_i   = c q_g . a_k + U_i . z_g,  i not in S (K is never materialised)
 //   s_j   = c q_g . k_j,              j in S     (exact residual rows)
 //   acc_g = (sum_lowrank p) a_v + (sum_lowrank p_i U_i) V_V + sum_S p_j v_j
-// emitted as a partial (m, l, acc) in base-2 units.  The last CTA to finish an
-// item of a unit merges the unit's partials with an fp32 log-sum-exp
-// reduction.  Scores are kept in fp32; the fp32 operands of a product (z, p,
+// emitted as a partial (m, l, acc) in base-2 units; the combine kernel merges
+// a unit's partials with an fp32 log-sum-exp reduction.  Scores are kept in fp32; the fp32 operands of a product (z, p,
 // w) are split into an fp16 pair hi + lo so the tensor-core products carry
 // about 22 bits.
 #include <float.h>
@@ -42,7 +43,7 @@ constexpr int kIQ = 3;                 // item descriptors in flight between pro
 
 struct AttendArgs {
   Layout L;
-  int G, Hq, Hkv, K_eff, n_items, n_wchunks, total, nslot, slot_bytes, xtok;
+  int G, Hq, Hkv, K_eff, n_items, n_wchunks, n_wfront, total, nslot, slot_bytes, xtok;
   float scale_log2;  // log2(e) / sqrt(d)
   const __half* q;
   const uint8_t* cache;
@@ -107,18 +108,22 @@ __device__ inline int chunk_owner(const ItemDesc& it, int k) {
   return k % kConsumers;
 }
 
-// Global item index -> item.  Window chunks come first (they need nothing from
-// the router, so they overlap its grid), then the routed blocks; consecutive
-// indices belong to different units.
+// Global item index -> item: n_wfront window chunks of every unit, the routed
+// blocks, then the remaining window chunks; consecutive indices belong to
+// different units.
+__device__ inline bool needs_route(const AttendArgs& a, int gi) {
+  const int nfront = a.n_wfront * a.L.units;
+  return gi >= nfront && gi < nfront + a.K_eff * a.L.units;
+}
 __device__ inline ItemDesc decode_item(const AttendArgs& a, int gi) {
   const Layout& L = a.L;
   ItemDesc it;
   it.stop = 0;
   it.ok = 1;
-  const int nwin = a.n_wchunks * L.units;
+  const int nfront = a.n_wfront * L.units, nblk = a.K_eff * L.units;
   const uint64_t unit_stride = L.unit_stride;
-  if (gi < nwin) {
-    const int wc = gi / L.units;
+  if (gi < nfront || gi >= nfront + nblk) {
+    const int wc = gi < nfront ? gi / L.units : a.n_wfront + (gi - nfront - nblk) / L.units;
     it.u = gi % L.units;
     it.item = a.K_eff + wc;
     it.is_block = 0;
@@ -130,7 +135,7 @@ __device__ inline ItemDesc decode_item(const AttendArgs& a, int gi) {
     it.base = (uint64_t)it.u * unit_stride + L.off_window;
     it.nvalid = L.W;
   } else {
-    const int bi = gi - nwin;
+    const int bi = gi - nfront;
     const int slot = bi / L.units;
     it.u = bi % L.units;
     it.item = slot;
@@ -796,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
           }
           break;
         }
-        if (gi >= a.n_wchunks * a.L.units && !waited) { griddep_wait(); waited = true; }
+        if (needs_route(a, gi) && !waited) { griddep_wait(); waited = true; }
         ItemDesc it = decode_item(a, gi);
         it.k0 = k;
         dsc = it;
@@ -910,6 +915,7 @@ cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, i
   a.K_eff = P.K_eff;
   a.n_items = P.n_items;
   a.n_wchunks = P.n_wchunks;
+  a.n_wfront = (P.n_wchunks + 1) / 2;
   a.total = P.n_items * L.units;
   a.xtok = 16384 / (4 * L.d);
   const int head = (int)L.off_u;

@@ -46,7 +46,7 @@ constexpr uint32_t kColSL = 0, kColSX = 32, kColW = 48, kColOX = 64, kColOL = 80
 
 struct TcArgs {
   Layout L;
-  int G, Hq, Hkv, K_eff, n_items, n_wgroups, total;
+  int G, Hq, Hkv, K_eff, n_items, n_wgroups, n_wfront, total;
   float scale_log2;  // log2(e) / sqrt(d)
   const __half* q;
   const uint8_t* cache;
@@ -225,9 +225,10 @@ __device__ inline TcItem tc_decode(const TcArgs& a, int gi) {
   TcItem it;
   it.stop = 0;
   it.ok = 1;
-  const int nwin = a.n_wgroups * L.units;
-  if (gi < nwin) {
-    const int wg = gi / L.units;
+  // n_wfront window groups of every unit, the routed blocks, the other window groups
+  const int nfront = a.n_wfront * L.units, nblk = a.K_eff * L.units;
+  if (gi < nfront || gi >= nfront + nblk) {
+    const int wg = gi < nfront ? gi / L.units : a.n_wfront + (gi - nfront - nblk) / L.units;
     it.u = gi % L.units;
     it.item = a.K_eff + wg;
     it.is_block = 0;
@@ -235,7 +236,7 @@ __device__ inline TcItem tc_decode(const TcArgs& a, int gi) {
     it.nvalid = min(it.n, L.W - wg * kTcWin);
     it.base = (uint64_t)it.u * L.unit_stride + L.off_window + (uint64_t)wg * kTcWin * 4 * L.d;
   } else {
-    const int bi = gi - nwin;
+    const int bi = gi - nfront;
     const int slot = bi / L.units;
     it.u = bi % L.units;
     it.item = slot;
@@ -341,7 +342,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm) attend_tc_kernel(TcA
           }
           break;
         }
-        if (gi >= a.n_wgroups * L.units && !waited) { griddep_wait(); waited = true; }
+        if (gi >= a.n_wfront * L.units && gi < (a.n_wfront + a.K_eff) * L.units && !waited) {
+          griddep_wait();
+          waited = true;
+        }
         const TcItem it = tc_decode(a, gi);
         dsc = it;
         if (!it.ok) {
@@ -737,6 +741,7 @@ cudaError_t launch_attend_tc(const Layout& L, const DecodePlan& P, int n_q_heads
   a.K_eff = P.K_eff;
   a.n_items = P.n_items;
   a.n_wgroups = P.n_wchunks;
+  a.n_wfront = (P.n_wchunks + 1) / 2;
   a.total = L.units * P.n_items;
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)L.d);
   a.q = q;
