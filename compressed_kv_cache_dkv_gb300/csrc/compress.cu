@@ -40,7 +40,10 @@ struct CArgs {
   const __half* V;
   uint8_t* cache;
   uint32_t* err;
-  int T, n, p, full;
+  int T;             // source tokens per unit (K, V are [units][T][D])
+  int blk0, nblk;    // CTA x = i < nblk compresses source tokens [256 i, 256 i + 256) into block blk0 + i
+  int with_window;   // CTA x = nblk copies the source tokens from 256 nblk on as the exact window
+  int n, p, full;
   uint32_t off_q, off_xc, off_misc;  // byte offsets of the shared-memory regions (R1 at 0)
 };
 
@@ -145,12 +148,12 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
   const int p = a.p;
   const int r = L.r, r8 = L.r8, R = L.R, R8 = L.R8;
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-  const int u = blockIdx.y, blk = blockIdx.x;
+  const int u = blockIdx.y, sb = blockIdx.x, blk = a.blk0 + sb;
   uint8_t* unit = a.cache + (uint64_t)u * L.unit_stride;
 
-  if (blk == L.NB) {  // ---------------- exact recency window
-    const __half* Kw = a.K + ((size_t)u * a.T + (size_t)L.NB * 256) * D;
-    const __half* Vw = a.V + ((size_t)u * a.T + (size_t)L.NB * 256) * D;
+  if (sb == a.nblk) {  // ---------------- exact recency window
+    const __half* Kw = a.K + ((size_t)u * a.T + (size_t)a.nblk * 256) * D;
+    const __half* Vw = a.V + ((size_t)u * a.T + (size_t)a.nblk * 256) * D;
     uint8_t* win = unit + L.off_window;
     for (int e = tid; e < L.W16 * D; e += nt) {
       int t = e / D, j = e % D;
@@ -175,8 +178,8 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
   int* sel = reinterpret_cast<int*>(pr + 64);              // [256]
   int* flag = sel + 256;                                   // [256]
 
-  const __half* Kb = a.K + ((size_t)u * a.T + (size_t)blk * 256) * D;
-  const __half* Vb = a.V + ((size_t)u * a.T + (size_t)blk * 256) * D;
+  const __half* Kb = a.K + ((size_t)u * a.T + (size_t)sb * 256) * D;
+  const __half* Vb = a.V + ((size_t)u * a.T + (size_t)sb * 256) * D;
   uint8_t* bp = unit + L.off_blocks + (uint64_t)blk * L.block_stride;
 
   // ---- anchor, router min / max, anchors in the block record
@@ -543,7 +546,8 @@ template <int D>
 cudaError_t launch_t(const CArgs& a, uint32_t smem, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(compress_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.L.NB + 1, a.L.units);
+  dim3 grid(a.nblk + (a.with_window ? 1 : 0), a.L.units);
+  if (grid.x == 0) return cudaSuccess;
   compress_kernel<D><<<grid, kCThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
@@ -553,6 +557,29 @@ cudaError_t launch_t(const CArgs& a, uint32_t smem, cudaStream_t s) {
 size_t compress_ws_bytes(const Layout& L) {
   (void)L;
   return kWsHeader;
+}
+
+cudaError_t launch_compress_blocks(const Layout& L, const __half* K, const __half* V, int T, int blk0, int nblk,
+                                   uint8_t* cache, uint32_t* err, cudaStream_t s) {
+  CPlan c = plan(L);
+  CArgs a;
+  a.L = L;
+  a.K = K;
+  a.V = V;
+  a.cache = cache;
+  a.err = err;
+  a.T = T;
+  a.blk0 = blk0;
+  a.nblk = nblk;
+  a.with_window = 0;
+  a.n = c.n;
+  a.p = c.p;
+  a.full = c.full;
+  a.off_q = c.off_q;
+  a.off_xc = c.off_xc;
+  a.off_misc = c.off_misc;
+  if (L.d == 128) return launch_t<128>(a, c.smem, s);
+  return launch_t<64>(a, c.smem, s);
 }
 
 cudaError_t launch_compress(const Layout& L, const __half* K, const __half* V, uint8_t* cache, uint8_t* ws,
@@ -568,6 +595,9 @@ cudaError_t launch_compress(const Layout& L, const __half* K, const __half* V, u
   a.cache = cache;
   a.err = err;
   a.T = L.NB * 256 + L.W;
+  a.blk0 = 0;
+  a.nblk = L.NB;
+  a.with_window = 1;
   a.n = c.n;
   a.p = c.p;
   a.full = c.full;

@@ -75,17 +75,22 @@ const char* dkv_status_string(int status) {
 int dkv_layout(dkv_desc* d) {
   if (!d) return DKV_ERR_ARG;
   if (d->batch < 1 || d->n_q_heads < 1 || d->n_kv_heads < 1 || d->head_dim < 1 || d->n_blocks < 0 ||
-      d->window < 0 || d->rank < 0 || d->n_residual < 0 || d->block_size < 1)
+      d->window < 0 || d->rank < 0 || d->n_residual < 0 || d->block_size < 1 || d->block_capacity < 0 ||
+      d->window_capacity < 0)
     return DKV_ERR_ARG;
   if (d->layout != DKV_LAYOUT_FRAGMENT && d->layout != DKV_LAYOUT_TC) return DKV_ERR_ARG;
   if (d->n_q_heads % d->n_kv_heads != 0) return DKV_ERR_SHAPE;
-  if (d->n_blocks == 0 && d->window == 0) return DKV_ERR_SHAPE;  // nothing to attend
+  const int cap_b = d->block_capacity ? d->block_capacity : d->n_blocks;
+  const int cap_w = d->window_capacity ? d->window_capacity : d->window;
+  if (d->n_blocks > cap_b || d->window > cap_w) return DKV_ERR_SHAPE;
+  // nothing to attend, and no room for tokens to come
+  if (d->n_blocks == 0 && d->window == 0 && cap_w == 0) return DKV_ERR_SHAPE;
   if (d->block_size != DKV_BLOCK_SIZE) return DKV_ERR_UNSUPPORTED;
   if (d->head_dim != 64 && d->head_dim != 128) return DKV_ERR_UNSUPPORTED;
   if (d->n_q_heads / d->n_kv_heads > 8) return DKV_ERR_UNSUPPORTED;
   if (d->rank > 128 || d->n_residual > 255) return DKV_ERR_UNSUPPORTED;
   // the router and the combine keep per-block / per-item values in shared memory
-  if (d->n_blocks > 2048 || d->window > 65536) return DKV_ERR_UNSUPPORTED;
+  if (cap_b > 2048 || cap_w > 65536) return DKV_ERR_UNSUPPORTED;
   const uint64_t dd = (uint64_t)d->head_dim;
   const int r8 = (d->rank + 7) / 8 * 8;
   const int R8 = (d->n_residual + 7) / 8 * 8;
@@ -112,12 +117,14 @@ int dkv_layout(dkv_desc* d) {
     d->block_bytes = d->blk_off_vv + 2ull * r8 * dd;
   }
   d->block_stride = round_up(d->block_bytes, 128);
-  const uint64_t nb = (uint64_t)d->n_blocks;
+  // offsets follow the capacities, so they stay put while the live counts change
+  const uint64_t nb = (uint64_t)cap_b;
+  const uint64_t W16cap = (uint64_t)(cap_w + 15) / 16 * 16;
   d->off_router = 0;
   d->off_blocks = round_up(nb * 4 * dd, 128);
   d->off_cold = d->off_blocks + nb * d->block_stride;
   d->off_window = d->off_cold + round_up(nb * (uint64_t)R8 * 2, 128);
-  d->unit_stride = round_up(d->off_window + (uint64_t)W16 * 4 * dd, 128);
+  d->unit_stride = round_up(d->off_window + W16cap * 4 * dd, 128);
   d->total_bytes = d->unit_stride * (uint64_t)d->n_units;
   return DKV_OK;
 }
@@ -164,6 +171,70 @@ int dkv_import_factors(const dkv_desc* d, const dkv_factors* f, void* cache, voi
   return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
 }
 
+size_t dkv_append_workspace_bytes(const dkv_desc* d) {
+  Layout L;
+  if (check_desc(d, &L) != DKV_OK) return 0;
+  return append_ws_bytes(L);
+}
+
+int dkv_append(dkv_desc* d, const void* K_new, const void* V_new, int32_t n_new, void* cache, void* workspace,
+               size_t ws_bytes, void* stream) {
+  Layout L;
+  int st = check_desc(d, &L);
+  if (st != DKV_OK) return st;
+  if (n_new < 0) return DKV_ERR_ARG;
+  if (n_new == 0) return DKV_OK;
+  if (!K_new || !V_new || !cache || !workspace) return DKV_ERR_ARG;
+  if (!aligned16(K_new) || !aligned16(V_new) || !aligned16(cache) || !aligned16(workspace)) return DKV_ERR_ALIGN;
+  if (L.tc) return DKV_ERR_UNSUPPORTED;  // the tensor-core window's byte image depends on its length
+  if (ws_bytes < append_ws_bytes(L)) return DKV_ERR_WORKSPACE;
+  const int p_cap = L.d == 128 ? 64 : 128;  // the GPU compressor's rank limit
+  const int cap_b = d->block_capacity ? d->block_capacity : d->n_blocks;
+  const int cap_w = d->window_capacity ? d->window_capacity : d->window;
+  // plan every step on the host first: nothing is launched unless the whole append fits
+  {
+    int nb = d->n_blocks, w = d->window, rem = n_new;
+    while (rem > 0) {
+      if (w == cap_w) {
+        if (w < 256 || nb == cap_b || L.r > p_cap) return DKV_ERR_UNSUPPORTED;
+        ++nb;
+        w -= 256;
+      }
+      const int take = rem < cap_w - w ? rem : cap_w - w;
+      w += take;
+      rem -= take;
+    }
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* cb = static_cast<uint8_t*>(cache);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int nb = d->n_blocks, w = d->window, i0 = 0;
+  cudaError_t e = cudaSuccess;
+  while (i0 < n_new && e == cudaSuccess) {
+    Layout S = L;  // the live state this step starts from
+    S.NB = nb;
+    S.W = w;
+    S.W16 = (w + 15) / 16 * 16;
+    if (w == cap_w) {
+      e = launch_append_compress(S, cb, ws, err, s);
+      ++nb;
+      w -= 256;
+      continue;
+    }
+    const int take = n_new - i0 < cap_w - w ? n_new - i0 : cap_w - w;
+    S.W16 = (w + take + 15) / 16 * 16;
+    e = launch_append_write(S, static_cast<const __half*>(K_new), static_cast<const __half*>(V_new), n_new, i0,
+                            take, w, cb, s);
+    w += take;
+    i0 += take;
+  }
+  if (e != cudaSuccess) return DKV_ERR_CUDA;
+  d->n_blocks = nb;
+  d->window = w;
+  return dkv_layout(d);
+}
+
 size_t dkv_decode_workspace_bytes(const dkv_desc* d, int32_t top_k) {
   Layout L;
   if (top_k < 0 || check_desc(d, &L) != DKV_OK) return 0;
@@ -184,6 +255,7 @@ static int prep_decode(const dkv_desc* d, int32_t top_k, void* workspace, size_t
   int st = check_desc(d, &c->L);
   if (st != DKV_OK) return st;
   if (top_k < 0) return DKV_ERR_ARG;
+  if (c->L.NB == 0 && c->L.W == 0) return DKV_ERR_SHAPE;  // an empty stream: nothing to attend yet
   if (!workspace) return DKV_ERR_ARG;
   if (!aligned16(workspace)) return DKV_ERR_ALIGN;
   c->P = plan_decode(c->L, d->n_q_heads, d->n_kv_heads, top_k);

@@ -317,6 +317,16 @@ cudaError_t launch_pack(const Layout& L, const dkv_factors& f, uint8_t* cache, u
 cudaError_t launch_compress(const Layout& L, const __half* K, const __half* V, uint8_t* cache, uint8_t* ws,
                             uint32_t* err, cudaStream_t s);
 size_t compress_ws_bytes(const Layout& L);
+// compress source tokens [256 i, 256 i + 256) of K, V [units][T][d] into block blk0 + i, i < nblk
+// (block record, router row, residual positions; nothing else of the cache is touched)
+cudaError_t launch_compress_blocks(const Layout& L, const __half* K, const __half* V, int T, int blk0, int nblk,
+                                   uint8_t* cache, uint32_t* err, cudaStream_t s);
+// streaming append: the window's oldest 256 tokens -> block L.NB, then the window slides down by
+// 256 tokens (L: the state before); new tokens into window slots [w0, w0 + take)
+size_t append_ws_bytes(const Layout& L);
+cudaError_t launch_append_compress(const Layout& L, uint8_t* cache, uint8_t* ws, uint32_t* err, cudaStream_t s);
+cudaError_t launch_append_write(const Layout& L, const __half* Kn, const __half* Vn, int n_new, int i0, int take,
+                                int w0, uint8_t* cache, cudaStream_t s);
 
 // Decode workspace: [header 256 B][scheduler: 2 x u32][routed: i32 per unit and slot]
 // [partials: per unit and item, m[8] l[8] o[8][d] in f32]

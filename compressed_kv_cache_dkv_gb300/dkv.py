@@ -40,6 +40,7 @@ EXPORTED = (
     "dkv_decode_workspace_bytes", "dkv_decode_attend", "dkv_decode_route", "dkv_decode_blocks",
     "dkv_decode_combine",
     "dkv_dense_workspace_bytes", "dkv_dense_decode", "dkv_get_error", "dkv_decode_attend_noalloc",
+    "dkv_append_workspace_bytes", "dkv_append",
 )
 
 
@@ -52,7 +53,7 @@ class DkvError(RuntimeError):
 class dkv_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "n_q_heads", "n_kv_heads", "head_dim", "block_size", "n_blocks", "window", "rank",
-        "n_residual", "layout", "rank_pad", "res_pad", "window_pad", "n_units")] + [
+        "n_residual", "layout", "block_capacity", "window_capacity", "rank_pad", "res_pad", "window_pad", "n_units")] + [
         (n, ctypes.c_uint64) for n in (
             "blk_off_mask", "blk_off_vk", "blk_off_u", "blk_off_res", "blk_off_vv", "block_bytes",
             "off_router", "off_blocks", "off_cold", "off_window", "block_stride", "unit_stride", "total_bytes")]
@@ -100,6 +101,9 @@ def lib() -> ctypes.CDLL:
         L.dkv_dense_decode.argtypes = [i32] * 5 + [vp] * 6 + [sz, vp]
         L.dkv_get_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
         L.dkv_decode_attend_noalloc.argtypes = [pdesc, vp, vp, i32, vp, vp, vp, vp]
+        L.dkv_append_workspace_bytes.restype = sz
+        L.dkv_append_workspace_bytes.argtypes = [pdesc]
+        L.dkv_append.argtypes = [pdesc, vp, vp, i32, vp, vp, sz, vp]
         _lib = L
     return _lib
 
@@ -131,12 +135,14 @@ def _stream(stream) -> int | None:
 
 def dkv_layout(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int, n_blocks: int, window: int,
                rank: int, n_residual: int, block_size: int = BLOCK_SIZE,
-               layout: int | None = None) -> dkv_desc:
+               layout: int | None = None, block_capacity: int = 0, window_capacity: int = 0) -> dkv_desc:
     """Fill a descriptor.  `layout` is DKV_LAYOUT_FRAGMENT (mma.sync decode kernel, the
-    default) or DKV_LAYOUT_TC (tcgen05 decode kernel; head_dim 128, rank <= 48, 1 <= R <= 128)."""
+    default) or DKV_LAYOUT_TC (tcgen05 decode kernel; head_dim 128, rank <= 48, 1 <= R <= 128).
+    `block_capacity` / `window_capacity` reserve room for dkv_append (0: the live counts)."""
     d = dkv_desc(batch=batch, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim=head_dim,
                  block_size=block_size, n_blocks=n_blocks, window=window, rank=rank, n_residual=n_residual,
-                 layout=DKV_LAYOUT_FRAGMENT if layout is None else layout)
+                 layout=DKV_LAYOUT_FRAGMENT if layout is None else layout,
+                 block_capacity=block_capacity, window_capacity=window_capacity)
     _check(lib().dkv_layout(ctypes.byref(d)), "dkv_layout")
     return d
 
@@ -161,6 +167,10 @@ def _ws(nbytes: int, device, workspace):
     return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
+def dkv_compress_workspace_bytes(d: dkv_desc) -> int:
+    return int(lib().dkv_compress_workspace_bytes(ctypes.byref(d)))
+
+
 def dkv_compress_layout(d: dkv_desc, K: torch.Tensor, V: torch.Tensor, cache: torch.Tensor | None = None,
                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """K, V: fp16 [B, Hkv, T, d] on the GPU -> packed cache (uint8 [total_bytes])."""
@@ -171,6 +181,22 @@ def dkv_compress_layout(d: dkv_desc, K: torch.Tensor, V: torch.Tensor, cache: to
     _check(lib().dkv_compress_layout(ctypes.byref(d), _ptr(K), _ptr(V), _ptr(cache), _ptr(workspace),
                                      workspace.numel(), _stream(stream)), "dkv_compress_layout")
     return cache
+
+
+def dkv_append_workspace_bytes(d: dkv_desc) -> int:
+    return int(lib().dkv_append_workspace_bytes(ctypes.byref(d)))
+
+
+def dkv_append(d: dkv_desc, K_new: torch.Tensor, V_new: torch.Tensor, cache: torch.Tensor,
+               workspace: torch.Tensor | None = None, stream=None) -> dkv_desc:
+    """Append K_new, V_new (fp16 [B, Hkv, n_new, d] on the GPU) to the cache; advances d in place."""
+    if K_new.shape != V_new.shape or K_new.dim() != 4:
+        raise DkvError(DKV_ERR_SHAPE, "dkv_append")
+    K_new, V_new = K_new.contiguous(), V_new.contiguous()
+    workspace = _ws(dkv_append_workspace_bytes(d), K_new.device, workspace)
+    _check(lib().dkv_append(ctypes.byref(d), _ptr(K_new), _ptr(V_new), int(K_new.shape[2]), _ptr(cache),
+                            _ptr(workspace), workspace.numel(), _stream(stream)), "dkv_append")
+    return d
 
 
 def dkv_import_factors(d: dkv_desc, f: dict, cache: torch.Tensor | None = None,

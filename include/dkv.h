@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define DKV_VERSION 2
+#define DKV_VERSION 3
 
 #if defined(__GNUC__)
 #define DKV_API __attribute__((visibility("default")))
@@ -79,7 +79,7 @@ extern "C" {
                                    head_dim 128, 1 <= rank <= 48, 1 <= n_residual <= 128 */
 
 /*
- * Descriptor of one layer's compressed cache.  The caller sets the first ten
+ * Descriptor of one layer's compressed cache.  The caller sets the first twelve
  * fields; dkv_layout() validates them and fills the rest.  Plain old data:
  * pass it by pointer, copy it freely.
  *
@@ -90,6 +90,11 @@ extern "C" {
  * picks the decode kernel: DKV_LAYOUT_FRAGMENT the mma.sync kernel,
  * DKV_LAYOUT_TC the tcgen05 kernel (TMEM accumulators).  A cache is only
  * readable under the layout it was written with.
+ *
+ * n_blocks and window are the live counts; the byte layout follows
+ * block_capacity and window_capacity, so a cache keeps its offsets while
+ * dkv_append() grows n_blocks and moves the window (0 means "no spare room").
+ * Capacities obey the same limits as the counts (2048 blocks, 65536 tokens).
  */
 typedef struct dkv_desc {
   int32_t batch;        /* sequences B */
@@ -102,6 +107,8 @@ typedef struct dkv_desc {
   int32_t rank;         /* r: rank of the joint K|V delta ([README Core] item 2) */
   int32_t n_residual;   /* R: exact residual rows per block ([README Core] item 3) */
   int32_t layout;       /* DKV_LAYOUT_FRAGMENT (0) or DKV_LAYOUT_TC (1) */
+  int32_t block_capacity;   /* blocks the cache has room for (0: n_blocks); >= n_blocks */
+  int32_t window_capacity;  /* window token slots (0: window); >= window */
   /* ---- filled by dkv_layout() ---- */
   int32_t rank_pad;     /* r rounded up to a multiple of 8 (zero-padded) */
   int32_t res_pad;      /* R rounded up to a multiple of 8 (zero-padded) */
@@ -178,6 +185,31 @@ DKV_API int dkv_compress_layout(const dkv_desc* d, const void* K, const void* V,
  * block keeps no residual row (its mask is left empty).
  */
 DKV_API int dkv_import_factors(const dkv_desc* d, const dkv_factors* f, void* cache, void* workspace, void* stream);
+
+/*
+ * Streaming append ([DKV-Z]; [README Core] items 1-4 applied as tokens
+ * arrive): add n_new tokens per unit to the exact recency window.  Whenever
+ * the window has no free slot left, its oldest 256 tokens are first
+ * compressed into block n_blocks (anchor, joint K|V truncated SVD, residual
+ * rows, router min/max: the same computation as dkv_compress_layout) and the
+ * window slides down by 256 tokens.  After any sequence of appends the cache
+ * holds exactly what dkv_compress_layout writes for the whole token sequence
+ * with the final (n_blocks, window).
+ *   d          descriptor filled by dkv_layout(); on DKV_OK its n_blocks and
+ *              window are advanced and its layout fields refreshed (the byte
+ *              offsets do not change)
+ *   K_new, V_new  device fp16 [B][Hkv][n_new][head_dim]
+ *   cache      device buffer written by dkv_compress_layout / dkv_import_factors
+ *              / dkv_append with the same capacities
+ *   workspace / ws_bytes  device scratch of dkv_append_workspace_bytes(d); its
+ *              header receives the device error word
+ * Returns DKV_ERR_UNSUPPORTED, with nothing launched, when the appends would
+ * need a block beyond block_capacity, when a compression step finds fewer than
+ * 256 window tokens (window_capacity < 256), or for the tensor-core layout.
+ */
+DKV_API size_t dkv_append_workspace_bytes(const dkv_desc* d);
+DKV_API int dkv_append(dkv_desc* d, const void* K_new, const void* V_new, int32_t n_new, void* cache,
+                       void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Decode-time attention for one layer ([DKV-Z]; [README Core]; [README

@@ -150,6 +150,36 @@ def compress_unit(K: np.ndarray, V: np.ndarray, n_blocks: int, rank: int, n_resi
     return Unit(blocks=blocks, win_K=K[nb * BLOCK_SIZE:].copy(), win_V=V[nb * BLOCK_SIZE:].copy())
 
 
+def append_tokens(unit: Unit, K_new: np.ndarray, V_new: np.ndarray, window_capacity: int, rank: int,
+                  n_residual: int) -> Unit:
+    """Streaming append: new tokens join the exact recency window; whenever the
+    window has no free slot left, its oldest 256 tokens are compressed into a
+    new block and leave the window ([DKV-Z]: recent tokens exact, older ones
+    compressed; [README Core] items 1-4 applied as tokens arrive).  Raises
+    ValueError when a compression step finds fewer than 256 window tokens."""
+    blocks = list(unit.blocks)
+    win_K = [row for row in np.asarray(unit.win_K, dtype=np.float64)]
+    win_V = [row for row in np.asarray(unit.win_V, dtype=np.float64)]
+    K_new = np.asarray(K_new, dtype=np.float64)
+    V_new = np.asarray(V_new, dtype=np.float64)
+    i = 0
+    while i < len(K_new):
+        if len(win_K) == window_capacity:
+            if len(win_K) < BLOCK_SIZE:
+                raise ValueError("window capacity below one block")
+            blocks.append(compress_block(np.array(win_K[:BLOCK_SIZE]), np.array(win_V[:BLOCK_SIZE]), rank,
+                                         n_residual))
+            win_K = win_K[BLOCK_SIZE:]
+            win_V = win_V[BLOCK_SIZE:]
+            continue
+        win_K.append(K_new[i])
+        win_V.append(V_new[i])
+        i += 1
+    d = K_new.shape[1] if K_new.ndim == 2 else np.asarray(unit.win_K).shape[-1]
+    as_arr = lambda rows: np.array(rows).reshape(len(rows), d)
+    return Unit(blocks=blocks, win_K=as_arr(win_K), win_V=as_arr(win_V))
+
+
 def reconstruct_block(blk: Block) -> tuple[np.ndarray, np.ndarray]:
     """K_hat, V_hat [256, d] of a compressed block: row 0 the anchor, rows in S
     the stored exact rows, every other row a + U_i [V_K | V_V] ([README Core])."""

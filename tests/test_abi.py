@@ -24,7 +24,7 @@ def test_library_exports_every_declared_symbol():
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(dkv.EXPORTED)
-    assert lib.dkv_version() == 2
+    assert lib.dkv_version() == 3
 
 
 def test_status_strings():
@@ -99,3 +99,59 @@ def test_calls_validate_before_touching_the_device():
     assert L.dkv_dense_decode(1, 6, 1, 80, 10, fake, fake, fake, fake, None, fake, 1 << 20, None) == dkv.DKV_ERR_UNSUPPORTED
     assert dkv.dkv_decode_workspace_bytes(desc, -1) == 0
     assert dkv.dkv_decode_workspace_bytes(desc, 2) > 0
+
+
+def test_capacity_fields_fix_the_offsets():
+    """With capacities set, the byte layout stays the same whatever the live counts."""
+    base = dict(batch=2, n_q_heads=12, n_kv_heads=2, head_dim=128, rank=32, n_residual=40,
+                block_capacity=40, window_capacity=700)
+    ref = dkv.dkv_layout(n_blocks=40, window=700, **base)
+    for nb, w in ((0, 1), (3, 0), (17, 699), (40, 700), (0, 0)):
+        desc = dkv.dkv_layout(n_blocks=nb, window=w, **base)
+        for f in ("off_router", "off_blocks", "off_cold", "off_window", "block_stride", "unit_stride", "total_bytes"):
+            assert getattr(desc, f) == getattr(ref, f), f
+        assert desc.window_pad == -(-w // 16) * 16
+    # no capacity: the live counts are the capacity
+    plain = dkv.dkv_layout(2, 12, 2, 128, 40, 700, 32, 40)
+    assert plain.total_bytes == ref.total_bytes
+    bad = [(dict(n_blocks=41, window=1), dkv.DKV_ERR_SHAPE), (dict(n_blocks=1, window=701), dkv.DKV_ERR_SHAPE),
+           (dict(n_blocks=1, window=1, block_capacity=-1), dkv.DKV_ERR_ARG),
+           (dict(n_blocks=1, window=1, block_capacity=2049), dkv.DKV_ERR_UNSUPPORTED),
+           (dict(n_blocks=1, window=1, window_capacity=65537), dkv.DKV_ERR_UNSUPPORTED),
+           (dict(n_blocks=0, window=0, window_capacity=0, block_capacity=0), dkv.DKV_ERR_SHAPE)]
+    for change, status in bad:
+        with pytest.raises(dkv.DkvError) as e:
+            dkv.dkv_layout(**dict(base, **change))
+        assert e.value.status == status, change
+
+
+def test_append_validates_before_touching_the_device():
+    """dkv_append plans the whole append on the host: too little room, a bad
+    count, misaligned pointers, a small workspace or the tensor-core layout are
+    reported with nothing launched (the fake pointers are never dereferenced)."""
+    L = dkv.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    big = 1 << 30
+
+    def call(desc, n_new, k=fake, ws=big):
+        before = bytes(desc)
+        st = L.dkv_append(ctypes.byref(desc), k, fake, n_new, fake, fake, ws, None)
+        assert bytes(desc) == before  # the descriptor only advances on success
+        return st
+
+    d = dkv.dkv_layout(1, 6, 1, 64, 1, 300, 8, 4, block_capacity=2, window_capacity=300)
+    assert call(d, -1) == dkv.DKV_ERR_ARG
+    assert call(d, 1, k=odd) == dkv.DKV_ERR_ALIGN
+    assert call(d, 1, ws=16) == dkv.DKV_ERR_WORKSPACE
+    # 300 + 256 + 1 tokens would need a third block
+    assert call(d, 2 * 256 + 1) == dkv.DKV_ERR_UNSUPPORTED
+    st0 = bytes(d)
+    assert L.dkv_append(ctypes.byref(d), fake, fake, 0, fake, fake, big, None) == dkv.DKV_OK  # nothing to do
+    assert bytes(d) == st0
+    # a window capacity below one block cannot slide
+    small = dkv.dkv_layout(1, 6, 1, 64, 0, 200, 8, 4, block_capacity=4, window_capacity=200)
+    assert call(small, 1) == dkv.DKV_ERR_UNSUPPORTED
+    tc = dkv.dkv_layout(1, 6, 1, 128, 1, 300, 8, 4, layout=dkv.DKV_LAYOUT_TC, block_capacity=4, window_capacity=512)
+    assert call(tc, 1) == dkv.DKV_ERR_UNSUPPORTED
+    assert dkv.dkv_append_workspace_bytes(d) >= 256 + 2 * 256 * 64 * 2

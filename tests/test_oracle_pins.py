@@ -388,3 +388,41 @@ def test_window_only_and_empty_inputs():
         O.decode_unit(q, O.compress_unit(K[:0], V[:0], 0, 4, 4), 1)
     with pytest.raises(ValueError):
         O.route(np.zeros(3), -1)
+
+
+@pytest.mark.parametrize("cap,T0,chunks", [(300, 0, [1, 2, 297, 1, 255, 1, 400, 3]), (256, 100, [156, 1, 600]),
+                                           (512, 700, [5, 1, 1, 300, 200])])
+def test_streaming_append_equals_batch_compression(cap, T0, chunks):
+    """Appending tokens in arbitrary pieces leaves the same state as compressing
+    the whole sequence at once: the block count follows from the window rule
+    (no block until the window is full; then one per 256 tokens past the
+    capacity) and every block is the batch compression of the same 256 tokens."""
+    rng = np.random.default_rng(cap + T0)
+    d, rank, R = 16, 3, 5
+    T = T0 + sum(chunks)
+    K = rng.standard_normal((T, d))
+    V = rng.standard_normal((T, d))
+    nb0 = 0 if T0 <= cap else -(-(T0 - cap) // 256)
+    unit = O.compress_unit(K[:T0], V[:T0], nb0, rank, R)
+    t = T0
+    for n in chunks:
+        unit = O.append_tokens(unit, K[t:t + n], V[t:t + n], cap, rank, R)
+        t += n
+        nb = 0 if t <= cap else -(-(t - cap) // 256)
+        assert len(unit.blocks) == nb and len(unit.win_K) == t - 256 * nb
+        assert cap - 256 < len(unit.win_K) <= cap or nb == 0
+    ref = O.compress_unit(K, V, len(unit.blocks), rank, R)
+    np.testing.assert_array_equal(unit.win_K, ref.win_K)
+    np.testing.assert_array_equal(unit.win_V, ref.win_V)
+    for a, b in zip(unit.blocks, ref.blocks):
+        np.testing.assert_array_equal(a.a_k, b.a_k)
+        np.testing.assert_array_equal(a.U, b.U)
+        np.testing.assert_array_equal(a.V_K, b.V_K)
+        np.testing.assert_array_equal(a.S, b.S)
+        np.testing.assert_array_equal(a.kmax, b.kmax)
+
+
+def test_streaming_append_needs_a_full_block_of_window():
+    unit = O.compress_unit(np.zeros((100, 8)), np.zeros((100, 8)), 0, 2, 1)
+    with pytest.raises(ValueError):
+        O.append_tokens(unit, np.ones((1, 8)), np.ones((1, 8)), 100, 2, 1)
