@@ -48,8 +48,8 @@ def test_noalloc_matches_decode_attend_on_consecutive_calls():
 
 
 def test_noalloc_rejects_a_scratch_need_beyond_its_area():
-    w = synth.WORKLOADS["sweep16k"]  # 128 units x 64 items of partials: ~34 MB of scratch at top-K = all
-    desc = dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window, 32, 40)
+    w = synth.WORKLOADS["sweep16k"]  # at batch 2048: 4096 units of partial records, ~17 MB of scratch
+    desc = dkv.dkv_layout(2048, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window, 32, 40)
     assert dkv.dkv_decode_workspace_bytes(desc, 0) > (8 << 20)
     t = torch.zeros(16, dtype=torch.float32, device="cuda")
     st = dkv.lib().dkv_decode_attend_noalloc(ctypes.byref(desc), t.data_ptr(), t.data_ptr(), 0, t.data_ptr(), None,
