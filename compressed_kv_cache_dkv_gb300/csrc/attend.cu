@@ -51,15 +51,17 @@ constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kNBar = 16;                     // chunk barrier pairs: chunks in the ring at most
 constexpr int kStageTok = 16 * kConsumers;    // exact tokens per stage (one 16-token group per warp)
 constexpr int kMaxRanges = 128;               // ranges per unit
-constexpr int kTargetCtas = 2 * 152;          // two CTAs on each of GB300's 152 SMs: one wave
-constexpr size_t kSmemPerCta = 113 * 1024;    // two CTAs per SM
+constexpr int kCtasPerSm = 2;                 // resident CTAs per SM (registers and shared memory)
+constexpr int kTargetCtas = kCtasPerSm * 152; // one wave on GB300's 152 SMs
+// 2 x (108 + 1 reserved) KB leaves an SM room for one router CTA of the same
+// call (programmatic launch lets the two grids overlap)
+constexpr size_t kSmemPerCta = 108 * 1024;
 
-enum ChunkKind { kQ = 0, kWin = 1, kRes = 2, kHead = 3, kU = 4, kVV = 5, kMerge = 6 };
+enum ChunkKind { kWin = 0, kRes = 1, kHead = 2, kU = 3, kVV = 4 };
 
 struct AttendArgs {
   Layout L;
   int G, Hq, Hkv, K_eff, n_r, nres, n_wst, ring;
-  uint32_t merge_bytes;
   float scale_log2;  // log2(e) / sqrt(d)
   const __half* q;
   const uint8_t* cache;
@@ -78,7 +80,7 @@ struct Chunk {
   uint64_t off;   // source offset inside the block record / the unit's window
 };
 
-// Walks the chunks of one range in order: Q, window stages, block items, merge.
+// Walks the chunks of one range in order: window stages, then block items.
 struct Cursor {
   int phase, ws, ws1, it, it1, sub;
   __device__ inline void init(const AttendArgs& a, int range) {
@@ -92,12 +94,7 @@ struct Cursor {
   __device__ inline bool next(const AttendArgs& a, Chunk& c) {
     const Layout& L = a.L;
     c.j = 0; c.tok0 = 0; c.ntok = 0; c.off = 0;
-    if (phase == 0) {
-      phase = 1;
-      c.kind = kQ;
-      c.bytes = (uint32_t)(a.G * L.d * 2);
-      return true;
-    }
+    if (phase == 0) phase = 1;
     if (phase == 1) {
       if (ws < ws1) {
         c.kind = kWin;
@@ -135,12 +132,6 @@ struct Cursor {
         return true;
       }
       phase = 3;
-    }
-    if (phase == 3) {
-      phase = 4;
-      c.kind = kMerge;
-      c.bytes = a.merge_bytes;
-      return true;
     }
     return false;
   }
@@ -275,11 +266,7 @@ __device__ __forceinline__ void exact_group(WarpState<D>& st, uint32_t qrow, uin
   s[1] = v0 ? (acc[0][1] + acc[1][1]) * slog2 : -INFINITY;
   s[2] = v1 ? (acc[0][2] + acc[1][2]) * slog2 : -INFINITY;
   s[3] = v1 ? (acc[0][3] + acc[1][3]) * slog2 : -INFINITY;
-  // V^T tiles are read before the softmax so the loads overlap it
   const uint32_t vb = gb + (uint32_t)(in_g * D * 2);
-  uint4 vv[KT];
-#pragma unroll
-  for (int md = 0; md < KT; ++md) vv[md] = ld_tile(vb + (uint32_t)md * kst, lane, full);
   float sc0, sc1, ms0, ms1;
   raise_max<D>(st, fmaxf(s[0], s[2]), fmaxf(s[1], s[3]), sc0, sc1, ms0, ms1);
   float p[4];
@@ -294,7 +281,7 @@ __device__ __forceinline__ void exact_group(WarpState<D>& st, uint32_t qrow, uin
 #pragma unroll
   for (int md = 0; md < KT; ++md) {
     // V^T tile (m = d, k = tokens): a half group holds k 0..7 only
-    const uint4 v = vv[md];
+    const uint4 v = ld_tile(vb + (uint32_t)md * kst, lane, full);
     const uint32_t a2 = full ? v.z : 0u, a3 = full ? v.w : 0u;
     mma16816(st.o[md], v.x, v.y, a2, a3, bh0, bh1);
     mma16816(st.o[md], v.x, v.y, a2, a3, bl0, bl1);
@@ -319,16 +306,14 @@ struct BlockState {
   float pa0, pa1;                 // per-lane partial sum of the low-rank p
 };
 
-// shared memory: [ring][full kNBar][empty kNBar][ends kNBar][z exchange 2 x RT x 2 x 32 float2]
-// [a_v 2 x 128 fp16][query rows 8 x (D + 8) fp16]; the z and a_v areas alternate between
-// consecutive blocks
-template <int RT>
+// shared memory: [ring][full kNBar][empty kNBar][query barrier][ends kNBar]
+// [query rows 8 x (D + 8) fp16][a_v, one copy per consumer warp: 4 x D fp16]
 __host__ __device__ inline size_t smem_extra() {
-  return (size_t)kNBar * 8 * 2 + (size_t)kNBar * 4 + 2 * (size_t)RT * 2 * 32 * 8 + 2 * 128 * 2 + 8 * 136 * 2 + 64;
+  return (size_t)kNBar * 8 * 2 + 16 + (size_t)kNBar * 4 + 8 * 136 * 2 + kConsumers * 128 * 2 + 64;
 }
 
 template <int D, int R8S>
-__global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int KT = D / 16;
   constexpr int RT = RankTiles<R8S>::RT;
@@ -336,16 +321,19 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
   const uint32_t ring = (uint32_t)a.ring;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + ring);
   uint64_t* empty = full + kNBar;
-  uint32_t* ends = reinterpret_cast<uint32_t*>(empty + kNBar);
-  float2* zbuf = reinterpret_cast<float2*>(ends + kNBar);  // [2][RT * 2][32]
-  __half* avbuf = reinterpret_cast<__half*>(zbuf + 2 * RT * 2 * 32);  // [2][128]
-  __half* qsm = avbuf + 2 * 128;                                      // [8][D + 8]
+  uint64_t* qbar = empty + kNBar;
+  uint32_t* ends = reinterpret_cast<uint32_t*>(qbar + 2);
+  __half* qsm = reinterpret_cast<__half*>(ends + kNBar);  // [8][D + 8]: 16-byte aligned rows
+  __half* avw = qsm + 8 * (D + 8);                        // [4][D]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x / a.n_r, range = blockIdx.x % a.n_r;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNBar; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kConsumers); }
+    mbar_init(qbar, 1);
     fence_mbar_init();
   }
+  // query rows past the group stay zero (the bulk copies fill rows 0 .. G-1)
+  for (int e = threadIdx.x; e < (8 - a.G) * (D + 8); e += kThreads) qsm[a.G * (D + 8) + e] = __float2half(0.f);
   __syncthreads();
   griddep_launch();  // the combine grid may be scheduled now; it waits for this grid's completion
 
@@ -355,6 +343,9 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
     const uint64_t pol = policy_evict_first();
     const uint8_t* unit = a.cache + (uint64_t)u * L.unit_stride;
     const __half* qsrc = a.q + ((size_t)(u / a.Hkv) * a.Hq + (size_t)(u % a.Hkv) * a.G) * L.d;
+    // the unit's G query rows, into padded shared-memory rows
+    mbar_arrive_expect_tx(qbar, (uint32_t)(a.G * L.d * 2));
+    for (int g = 0; g < a.G; ++g) bulk_g2s(qsm + g * (D + 8), qsrc + (size_t)g * L.d, (uint32_t)(L.d * 2), qbar, pol);
     Cursor cur;
     cur.init(a, range);
     Chunk ch;
@@ -375,14 +366,11 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
       ends[c % kNBar] = pos;
       uint64_t* fb = &full[c % kNBar];
       uint8_t* dst = smem + off;
-      if (ch.kind == kQ) {
-        mbar_arrive_expect_tx(fb, ch.bytes);
-        bulk_g2s(dst, qsrc, ch.bytes, fb, pol);
-      } else if (ch.kind == kWin) {
+      if (ch.kind == kWin) {
         mbar_arrive_expect_tx(fb, ch.bytes);
         bulk_g2s(dst, unit + L.off_window + ch.off, ch.bytes, fb, pol);
-      } else if (ch.kind == kMerge || ch.bytes == 0) {
-        mbar_arrive(fb);  // space only (merge buffer), or an empty section (rank 0)
+      } else if (ch.bytes == 0) {
+        mbar_arrive(fb);  // an empty section (rank 0)
       } else {
         if (ch.j != jb) {
           if (!routed_ready) { griddep_wait(); routed_ready = true; }  // the router's grid has completed
@@ -404,7 +392,6 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
 
   // =========================== consumer warps
   const int t = lane & 3, gq = lane >> 2;
-  const int tid = threadIdx.x;
   const int G = a.G;
   const bool gv0 = (2 * t) < G, gv1 = (2 * t + 1) < G;
   const float slog2 = a.scale_log2;
@@ -416,12 +403,18 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
   bool alive = true;                       // false after a bounded wait gave up
   WarpState<D> st;
   BlockState<D, RT> bs;
-  const uint32_t qrow = smem_u32(qsm + gq * (D + 8));  // this lane's query row (B / A fragments of q)
+  const uint32_t qrow = smem_u32(qsm + gq * (D + 8));  // this lane's query row (B fragments of q)
+  __half* av = avw + warp * D;                         // this warp's copy of the block's a_v
+  alive = mbar_wait(qbar, 0u, a.err);
+  st.m0 = st.m1 = -INFINITY;
+  st.l0 = st.l1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < KT; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
   Cursor cur;
   cur.init(a, range);
   Chunk ch;
   uint32_t pos = 0;
-  int c = 0, nhead = 0;
+  int c = 0;
   while (cur.next(a, ch)) {
     const uint32_t off = ring_place(pos, ch.bytes, ring);
     const int bi = c % kNBar;
@@ -429,20 +422,6 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
     const uint32_t sb = sbase + off;
     const uint8_t* sp = smem + off;
     switch (ch.kind) {
-      case kQ: {
-        // the range's query rows, kept for its whole length (padded rows: conflict-free fragment loads)
-        const __half* qs = reinterpret_cast<const __half*>(sp);
-        for (int e = tid; e < 8 * D; e += kConsumers * 32) {
-          const int g = e / D, dd = e % D;
-          qsm[g * (D + 8) + dd] = (alive && g < G) ? qs[g * D + dd] : __float2half(0.f);
-        }
-        named_bar_sync(1, kConsumers * 32);
-        st.m0 = st.m1 = -INFINITY;
-        st.l0 = st.l1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < KT; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
-        break;
-      }
       case kWin:
       case kRes: {
         const int in_g = max(0, min(16, ch.ntok - 16 * warp));
@@ -461,66 +440,64 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
           qb[kt][0] = lds32(qrow + (uint32_t)(16 * kt + 2 * t) * 2u);
           qb[kt][1] = lds32(qrow + (uint32_t)(16 * kt + 8 + 2 * t) * 2u);
         }
-        // base = c q . a_k for this lane's query row gq, then columns 2t, 2t + 1
+        // base = c q . a_k for this lane's query row gq (four partial sums), then columns 2t, 2t + 1
         const __half* ak = reinterpret_cast<const __half*>(sp);
-        float part = 0.f;
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kt = 0; kt < KT; ++kt) {
           const float2 q0 = __half22float2(*reinterpret_cast<const __half2*>(&qb[kt][0]));
           const float2 q1 = __half22float2(*reinterpret_cast<const __half2*>(&qb[kt][1]));
           const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(ak + 16 * kt + 2 * t));
           const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(ak + 16 * kt + 8 + 2 * t));
-          part = fmaf(q0.x, a0.x, part); part = fmaf(q0.y, a0.y, part);
-          part = fmaf(q1.x, a1.x, part); part = fmaf(q1.y, a1.y, part);
+          part[kt & 3] = fmaf(q0.x, a0.x, fmaf(q0.y, a0.y, fmaf(q1.x, a1.x, fmaf(q1.y, a1.y, part[kt & 3]))));
         }
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        bs.base0 = __shfl_sync(0xffffffffu, part, 8 * t) * slog2;
-        bs.base1 = __shfl_sync(0xffffffffu, part, 8 * t + 4) * slog2;
+        float pb = (part[0] + part[1]) + (part[2] + part[3]);
+        pb += __shfl_xor_sync(0xffffffffu, pb, 1);
+        pb += __shfl_xor_sync(0xffffffffu, pb, 2);
+        bs.base0 = __shfl_sync(0xffffffffu, pb, 8 * t) * slog2;
+        bs.base1 = __shfl_sync(0xffffffffu, pb, 8 * t + 4) * slog2;
         const uint32_t* mask = reinterpret_cast<const uint32_t*>(sp + L.off_mask);
         bs.mk0 = alive ? mask[2 * warp] : 0u;
         bs.mk1 = alive ? mask[2 * warp + 1] : 0u;
-        if (tid < D) avbuf[(nhead & 1) * 128 + tid] = ak[D + tid];  // a_v, read back at the V_V chunk
-        // z^T = q^T V_K^T: n-tiles of 8 r-rows split across warps, exchanged through zbuf
-        float2* zb = zbuf + (size_t)(nhead & 1) * RT * 2 * 32;
+        for (int j = lane; j < D; j += 32) av[j] = ak[D + j];  // read back at the V_V chunk
+        // z = V_K (c q): V_K (stored as 8-row B^T tiles) read as the A operand, two tiles per
+        // 16-row m-tile; q as B.  The C fragments (rows = r, columns = group) become the B
+        // fragments of U z through movmatrix, with a per-column power-of-two scale.
         const uint32_t vk = sb + (uint32_t)L.off_vk;
-        for (int nt = warp; nt < (r8 >> 3); nt += kConsumers) {
-          float cz[4] = {0.f, 0.f, 0.f, 0.f};
-          uint4 bv[D / 32];
+        const int nt8 = r8 >> 3;
+        float zc[RT][4];
 #pragma unroll
-          for (int kp = 0; kp < D / 32; ++kp) bv[kp] = lds128(vk + (uint32_t)(nt * 8 * D * 2 + kp * 512 + lane * 16));
+        for (int mt = 0; mt < RT; ++mt) {
+          zc[mt][0] = zc[mt][1] = zc[mt][2] = zc[mt][3] = 0.f;
+          if (mt < nrt) {
+            const bool lo_rows = 2 * mt + 1 < nt8;  // the m-tile's rows 8..15 exist
 #pragma unroll
-          for (int kp = 0; kp < D / 32; ++kp) {
-            mma16816(cz, qb[2 * kp][0], 0u, qb[2 * kp][1], 0u, bv[kp].x, bv[kp].y);
-            mma16816(cz, qb[2 * kp + 1][0], 0u, qb[2 * kp + 1][1], 0u, bv[kp].z, bv[kp].w);
+            for (int kp = 0; kp < D / 32; ++kp) {
+              const uint4 b0 = lds128(vk + (uint32_t)((2 * mt) * 8 * D * 2 + kp * 512 + lane * 16));
+              const uint4 b1 = lo_rows ? lds128(vk + (uint32_t)((2 * mt + 1) * 8 * D * 2 + kp * 512 + lane * 16))
+                                       : make_uint4(0u, 0u, 0u, 0u);
+              mma16816(zc[mt], b0.x, b1.x, b0.y, b1.y, qb[2 * kp][0], qb[2 * kp][1]);
+              mma16816(zc[mt], b0.z, b1.z, b0.w, b1.w, qb[2 * kp + 1][0], qb[2 * kp + 1][1]);
+            }
           }
-          zb[nt * 32 + lane] = make_float2(cz[0] * slog2, cz[1] * slog2);
         }
-        named_bar_sync(1, kConsumers * 32);  // every n-tile of z is in zbuf
-        ++nhead;
-        // z B fragments: b0 = z[16kk + 2t, +1][gq] (C fragment c0, c1 of n-tile 2kk), b1 from n-tile 2kk + 1
-        float zf[RT][4];
-        float zmax = 0.f;
+        float zm0 = 0.f, zm1 = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < RT; ++kk) {
-          float2 z0 = make_float2(0.f, 0.f), z1 = make_float2(0.f, 0.f);
-          if (kk < nrt) {
-            z0 = zb[(2 * kk) * 32 + lane];
-            if (2 * kk + 1 < (r8 >> 3)) z1 = zb[(2 * kk + 1) * 32 + lane];
-          }
-          zf[kk][0] = z0.x; zf[kk][1] = z0.y; zf[kk][2] = z1.x; zf[kk][3] = z1.y;
-          zmax = fmaxf(zmax, fmaxf(fmaxf(fabsf(z0.x), fabsf(z0.y)), fmaxf(fabsf(z1.x), fabsf(z1.y))));
-        }
-        zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 1));
-        zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, 2));
-        const float zsc = pow2_down(zmax);  // for query gq
+        for (int mt = 0; mt < RT; ++mt) {
 #pragma unroll
-        for (int kk = 0; kk < RT; ++kk) {
-          split_half2(zf[kk][0] * zsc, zf[kk][1] * zsc, bs.zh[kk][0], bs.zl[kk][0]);
-          split_half2(zf[kk][2] * zsc, zf[kk][3] * zsc, bs.zh[kk][1], bs.zl[kk][1]);
+          for (int e = 0; e < 4; ++e) zc[mt][e] *= slog2;
+          zm0 = fmaxf(zm0, fmaxf(fabsf(zc[mt][0]), fabsf(zc[mt][2])));
+          zm1 = fmaxf(zm1, fmaxf(fabsf(zc[mt][1]), fabsf(zc[mt][3])));
         }
-        bs.us0 = 1.f / __shfl_sync(0xffffffffu, zsc, 8 * t);
-        bs.us1 = 1.f / __shfl_sync(0xffffffffu, zsc, 8 * t + 4);
+        zm0 = warp_max_rows(zm0);
+        zm1 = warp_max_rows(zm1);
+        const float zs0 = pow2_down(zm0), zs1 = pow2_down(zm1);  // per column 2t, 2t + 1
+#pragma unroll
+        for (int mt = 0; mt < RT; ++mt)
+          c_to_b(zc[mt][0] * zs0, zc[mt][1] * zs1, zc[mt][2] * zs0, zc[mt][3] * zs1, bs.zh[mt][0], bs.zl[mt][0],
+                 bs.zh[mt][1], bs.zl[mt][1]);
+        bs.us0 = 1.f / zs0;
+        bs.us1 = 1.f / zs1;
 #pragma unroll
         for (int i = 0; i < RT; ++i) bs.w[i][0] = bs.w[i][1] = bs.w[i][2] = bs.w[i][3] = 0.f;
         bs.pa0 = bs.pa1 = 0.f;
@@ -618,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
           c_to_b(bs.w[kk][0] * ws0, bs.w[kk][1] * ws1, bs.w[kk][2] * ws0, bs.w[kk][3] * ws1, wh[kk][0], wl[kk][0],
                  wh[kk][1], wl[kk][1]);
         const float wu0 = 1.f / ws0, wu1 = 1.f / ws1;
-        const __half* avp = avbuf + ((nhead - 1) & 1) * 128;  // this block's a_v (written at its head)
+        const __half* avp = av;  // this block's a_v (this warp's copy, written at its head)
 #pragma unroll
         for (int md = 0; md < KT; ++md) {
           float cv[4] = {0.f, 0.f, 0.f, 0.f};
@@ -643,56 +620,33 @@ __global__ void __launch_bounds__(kThreads, 2) attend_kernel(AttendArgs a) {
         }
         break;
       }
-      case kMerge: {
-        // merge the four warps' states into the range's partial record
-        float* obw = reinterpret_cast<float*>(smem + off);  // [4][D][8]
-        float* sst = obw + kConsumers * D * 8;               // [4][m 8 | l 8]
-        float* fin = sst + kConsumers * 16;                  // [M 8][L 8][factor 4 x 8]
-        const float l0 = warp_sum_rows(st.l0), l1 = warp_sum_rows(st.l1);
-        if (lane < 4) {
-          sst[warp * 16 + 2 * t] = st.m0; sst[warp * 16 + 2 * t + 1] = st.m1;
-          sst[warp * 16 + 8 + 2 * t] = l0; sst[warp * 16 + 8 + 2 * t + 1] = l1;
-        }
-#pragma unroll
-        for (int md = 0; md < KT; ++md) {
-          float* o0 = obw + ((size_t)warp * D + md * 16 + gq) * 8 + 2 * t;
-          *reinterpret_cast<float2*>(o0) = make_float2(st.o[md][0], st.o[md][1]);
-          *reinterpret_cast<float2*>(o0 + 64) = make_float2(st.o[md][2], st.o[md][3]);
-        }
-        named_bar_sync(1, kConsumers * 32);
-        if (tid < 8) {
-          const int g = tid;
-          float M = -INFINITY;
-          for (int wi = 0; wi < kConsumers; ++wi) M = fmaxf(M, sst[wi * 16 + g]);
-          const float Ms = M == -INFINITY ? 0.f : M;
-          float Lsum = 0.f;
-          for (int wi = 0; wi < kConsumers; ++wi) {
-            const float f = fast_exp2(sst[wi * 16 + g] - Ms);
-            fin[16 + wi * 8 + g] = f;
-            Lsum += f * sst[wi * 16 + 8 + g];
-          }
-          fin[g] = M;
-          fin[8 + g] = Lsum;
-        }
-        named_bar_sync(1, kConsumers * 32);
-        float* rec = a.partials + ((size_t)u * a.n_r + range) * (16 + 8 * D);
-        if (tid < 16) rec[tid] = alive ? fin[tid] : (tid < 8 ? -INFINITY : 0.f);
-        for (int e = tid; e < G * D; e += kConsumers * 32) {
-          const int g = e / D, dd = e % D;
-          float v = 0.f;
-#pragma unroll
-          for (int wi = 0; wi < kConsumers; ++wi) v = fmaf(fin[16 + wi * 8 + g], obw[((size_t)wi * D + dd) * 8 + g], v);
-          rec[16 + e] = alive ? v : 0.f;
-        }
-        fence_proxy_async();  // generic accesses to this ring area precede later bulk copies into it
-        break;
-      }
       default:
         break;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[bi]);
     ++c;
+  }
+  // this warp's partial record (m, l, o) over every token it scored; the combine merges them
+  const float l0 = warp_sum_rows(st.l0), l1 = warp_sum_rows(st.l1);
+  float* rec = a.partials + (((size_t)u * a.n_r + range) * kConsumers + warp) * (16 + 8 * D);
+  if (lane < 4) {
+    rec[2 * t] = alive ? st.m0 : -INFINITY;
+    rec[2 * t + 1] = alive ? st.m1 : -INFINITY;
+    rec[8 + 2 * t] = alive ? l0 : 0.f;
+    rec[8 + 2 * t + 1] = alive ? l1 : 0.f;
+  }
+#pragma unroll
+  for (int md = 0; md < KT; ++md) {
+    const int d0 = 16 * md + gq;
+    if (gv0) {
+      rec[16 + (2 * t) * D + d0] = alive ? st.o[md][0] : 0.f;
+      rec[16 + (2 * t) * D + d0 + 8] = alive ? st.o[md][2] : 0.f;
+    }
+    if (gv1) {
+      rec[16 + (2 * t + 1) * D + d0] = alive ? st.o[md][1] : 0.f;
+      rec[16 + (2 * t + 1) * D + d0 + 8] = alive ? st.o[md][3] : 0.f;
+    }
   }
 }
 
@@ -714,8 +668,12 @@ uint64_t win_stage_bytes(const Layout& L, int s) {
   const int n = L.W16 - s * kStageTok < kStageTok ? L.W16 - s * kStageTok : kStageTok;
   return (uint64_t)n * 4 * L.d;
 }
+// Balancing weight of a block item: its bytes, the low-rank part's times
+// kLowRankWeight (its z, U and V_V products cost the consumer warps about
+// three times as long per byte as an exact stage; measured on GB300).
+constexpr uint64_t kLowRankWeight = 3;
 uint64_t block_item_bytes(const Layout& L, int k) {  // k = 0: low-rank part; k >= 1: residual stage k - 1
-  if (k == 0) return L.off_u + (L.off_res - L.off_u) + (L.block_bytes - L.off_vv);
+  if (k == 0) return kLowRankWeight * (L.off_u + (L.off_res - L.off_u) + (L.block_bytes - L.off_vv));
   const int t0 = (k - 1) * kStageTok;
   const int n = L.R8 - t0 < kStageTok ? L.R8 - t0 : kStageTok;
   return (uint64_t)n * 4 * L.d;
@@ -724,7 +682,7 @@ uint64_t block_item_bytes(const Layout& L, int k) {  // k = 0: low-rank part; k 
 // Cut one unit's work list into n_r ranges.  Every range starts with one
 // window stage where there are enough (so it has work while the router runs);
 // the block items are cut into contiguous runs and the other window stages are
-// spread over the ranges, for the smallest capacity (largest range, in bytes)
+// spread over the ranges, for the smallest capacity (largest range, in weight)
 // that holds everything: binary search on the capacity, with the block runs
 // filled in order up to it (exact for contiguous runs) and the spare window
 // stages placed in whatever room is left.  Range i reads window stages
@@ -851,7 +809,7 @@ DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k
     const int n_list = P.n_wchunks + P.K_eff * (1 + nres);
     int n_r = ranges_per_unit(L.units);
     n_r = n_r < n_list ? n_r : n_list;
-    P.n_items = n_r < 1 ? 1 : n_r;
+    P.n_items = (n_r < 1 ? 1 : n_r) * kConsumers;  // one record per consumer warp
   }
   P.off_sched = kWsHeader;  // scheduler counters of the tensor-core kernel
   P.off_routed = round_up(P.off_sched + 8, 256);
@@ -869,16 +827,16 @@ cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, i
   a.Hq = n_q_heads;
   a.Hkv = n_kv_heads;
   a.K_eff = P.K_eff;
-  a.n_r = P.n_items;
+  a.n_r = P.n_items / kConsumers;
   a.nres = (L.R8 + kStageTok - 1) / kStageTok;
   a.n_wst = P.n_wchunks;
   if (a.n_r > kMaxRanges) return cudaErrorInvalidValue;
   fill_ranges(L, a.K_eff, a.nres, a.n_wst, a.n_r, a.tab);
   const int r8s = instance_r8s(L.d, L.r8);
   const int RT = instance_rt(r8s);
-  const size_t extra = RT <= 2 ? smem_extra<2>() : (RT <= 4 ? smem_extra<4>() : smem_extra<8>());
+  (void)RT;
+  const size_t extra = smem_extra();
   a.ring = (int)((kSmemPerCta - extra) / 128 * 128);
-  a.merge_bytes = (uint32_t)(kConsumers * L.d * 8 * 4 + kConsumers * 16 * 4 + 48 * 4);
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)L.d);
   a.q = q;
   a.cache = cache;

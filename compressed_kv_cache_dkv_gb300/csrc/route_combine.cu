@@ -21,8 +21,11 @@ namespace dkv {
 namespace {
 
 constexpr int kRouteCluster = 8;    // CTAs per unit (one thread-block cluster)
-constexpr int kRouteThreads = 256;
-constexpr int kRouteInFlight = 2;   // router rows in flight per lane (kmin and kmax pieces each)
+// 128 threads (8 K registers): a router CTA fits on an SM beside two attention
+// CTAs of the same call, which start while routing runs
+constexpr int kRouteThreads = 128;
+constexpr int kRouteInFlight = 4;   // router rows in flight per lane (kmin and kmax pieces each)
+constexpr int kRouteRounds = 2;     // ranking rounds: 2048 blocks over 8 CTAs of 128 threads
 
 // One cluster of kRouteCluster CTAs per unit; CTA c of the cluster owns blocks
 // [c*per, (c+1)*per).  Each CTA loads its blocks' router rows ([kmin | kmax],
@@ -40,7 +43,7 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
   extern __shared__ float4 sc4[];  // bounds of all NB blocks of the unit, padded to 4 with -inf
   __shared__ float qbar[128];
   __shared__ int cnt[kRouteCluster];
-  __shared__ int wsum[kRouteThreads / 32];
+  __shared__ int wsum[kRouteRounds * (kRouteThreads / 32)];
   const int d = L.d, NB = L.NB;
   const uint32_t crank = cluster_ctarank();
   const int u = blockIdx.x / kRouteCluster;
@@ -121,45 +124,56 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
     }
   }
   cluster_sync();  // all NB bounds are in every CTA
-  // rank own blocks: tpb threads share one block's comparisons
+  // rank own blocks: tpb threads share one block's comparisons; with more blocks
+  // than threads (NB > 8 x 128) a CTA ranks its blocks in two rounds
   const int n_own = b1 - b0;
   int tpb = 32;
   while (tpb > 1 && tpb * n_own > kRouteThreads) tpb >>= 1;
+  const int per_round = kRouteThreads / tpb;
+  const int rounds = (n_own + per_round - 1) / per_round;  // at most kRouteRounds (NB <= 2048)
   const int sub = tid % tpb;
-  const int i = b0 + tid / tpb;
-  const bool mine = tid / tpb < n_own;
-  int rank = 0;
-  if (mine && K_eff < NB) {
-    const float bi = sc[i];
-    for (int j4 = sub; j4 < NB4; j4 += tpb) {
-      const float4 bj = sc4[j4];
-      const int j = 4 * j4;
-      rank += (bj.x > bi) || (bj.x == bi && j < i);
-      rank += (bj.y > bi) || (bj.y == bi && j + 1 < i);
-      rank += (bj.z > bi) || (bj.z == bi && j + 2 < i);
-      rank += (bj.w > bi) || (bj.w == bi && j + 3 < i);
-    }
-  }
-  for (int o = tpb >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-  const bool sel = mine && sub == 0 && rank < K_eff;
-  const unsigned bal = __ballot_sync(0xffffffffu, sel);
-  if (lane == 0) wsum[warp] = __popc(bal);
-  __syncthreads();
-  int before = 0, total = 0;  // selected blocks of this CTA in lower warps, and in the whole CTA
+  bool sel[kRouteRounds];
+  unsigned bal[kRouteRounds];
 #pragma unroll
-  for (int w = 0; w < nw; ++w) {
-    const int c = wsum[w];
-    before += w < warp ? c : 0;
-    total += c;
+  for (int r = 0; r < kRouteRounds; ++r) {
+    const int own = r * per_round + tid / tpb;
+    const int i = b0 + own;
+    const bool mine = r < rounds && own < n_own;
+    int rank = 0;
+    if (mine && K_eff < NB) {
+      const float bi = sc[i];
+      for (int j4 = sub; j4 < NB4; j4 += tpb) {
+        const float4 bj = sc4[j4];
+        const int j = 4 * j4;
+        rank += (bj.x > bi) || (bj.x == bi && j < i);
+        rank += (bj.y > bi) || (bj.y == bi && j + 1 < i);
+        rank += (bj.z > bi) || (bj.z == bi && j + 2 < i);
+        rank += (bj.w > bi) || (bj.w == bi && j + 3 < i);
+      }
+    }
+    for (int o = tpb >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    sel[r] = mine && sub == 0 && rank < K_eff;
+    bal[r] = __ballot_sync(0xffffffffu, sel[r]);
+    if (lane == 0) wsum[r * nw + warp] = __popc(bal[r]);
   }
+  __syncthreads();
+  int total = 0;  // selected blocks of this CTA
+#pragma unroll
+  for (int w = 0; w < kRouteRounds * nw; ++w) total += wsum[w];
   if (tid < kRouteCluster) st_cluster_s32(&cnt[crank], (uint32_t)tid, total);
   cluster_sync();  // every CTA's count is everywhere; no peer access follows
   int offset = 0;
   for (int c = 0; c < (int)crank; ++c) offset += cnt[c];
-  if (sel) {
-    const int pos = offset + before + __popc(bal & ((1u << lane) - 1u));
-    routed[(size_t)u * K_eff + pos] = i;
-    if (routed_out) routed_out[(size_t)u * K_eff + pos] = i;
+#pragma unroll
+  for (int r = 0; r < kRouteRounds; ++r) {
+    if (sel[r]) {
+      int before = 0;  // selected blocks of this CTA below this one: earlier rounds, lower warps
+      for (int w = 0; w < r * nw + warp; ++w) before += wsum[w];
+      const int i = b0 + r * per_round + tid / tpb;
+      const int pos = offset + before + __popc(bal[r] & ((1u << lane) - 1u));
+      routed[(size_t)u * K_eff + pos] = i;
+      if (routed_out) routed_out[(size_t)u * K_eff + pos] = i;
+    }
   }
 }
 
