@@ -59,14 +59,18 @@ constexpr size_t kSmemPerCta = 108 * 1024;
 
 enum ChunkKind { kWin = 0, kRes = 1, kHead = 2, kU = 3, kVV = 4 };
 
+// Every block is routed (top-K >= NB): slot j is block j, and no router grid runs.
+constexpr int kModeAll = 2;
+
 struct AttendArgs {
   Layout L;
-  int G, Hq, Hkv, K_eff, n_r, nres, n_wst, ring;
+  int G, Hq, Hkv, K_eff, n_r, nres, n_wst, ring, mode;
   float scale_log2;  // log2(e) / sqrt(d)
   const __half* q;
   const uint8_t* cache;
-  const int32_t* routed;
-  float* partials;
+  const int32_t* routed;  // [units][K_eff], written by the router grid
+  int32_t* routed_out;    // kModeAll, optional: the caller's copy of the routed indices (0 .. NB-1)
+  float* partials;        // [units][n_r][4 consumer warps] records [m 8][l 8][o 8][d]
   uint32_t* err;
   int tab[kMaxRanges][4];  // per range: window stages [0, 1), block items [2, 3)
 };
@@ -306,6 +310,7 @@ struct BlockState {
   float pa0, pa1;                 // per-lane partial sum of the low-rank p
 };
 
+
 // shared memory: [ring][full kNBar][empty kNBar][query barrier][ends kNBar]
 // [query rows 8 x (D + 8) fp16][a_v, one copy per consumer warp: 4 x D fp16]
 __host__ __device__ inline size_t smem_extra() {
@@ -373,8 +378,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
         mbar_arrive(fb);  // an empty section (rank 0)
       } else {
         if (ch.j != jb) {
-          if (!routed_ready) { griddep_wait(); routed_ready = true; }  // the router's grid has completed
-          int b = a.routed[u * a.K_eff + ch.j];
+          int b = ch.j;  // kModeAll: slot j is block j
+          if (!(a.mode & kModeAll)) {
+            if (!routed_ready) { griddep_wait(); routed_ready = true; }  // the router's grid has completed
+            b = a.routed[(size_t)u * a.K_eff + ch.j];
+          }
           if (b < 0 || b >= L.NB) {
             raise_error(a.err, DKV_DEVERR_INDEX);
             b = 0;
@@ -406,6 +414,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
   const uint32_t qrow = smem_u32(qsm + gq * (D + 8));  // this lane's query row (B fragments of q)
   __half* av = avw + warp * D;                         // this warp's copy of the block's a_v
   alive = mbar_wait(qbar, 0u, a.err);
+  const int tid = threadIdx.x;
+  if ((a.mode & kModeAll) && a.routed_out && range == 0)
+    for (int j = tid; j < a.K_eff; j += kConsumers * 32) a.routed_out[(size_t)u * a.K_eff + j] = j;
   st.m0 = st.m1 = -INFINITY;
   st.l0 = st.l1 = 0.f;
 #pragma unroll
@@ -760,25 +771,42 @@ int instance_r8s(int d, int r8) {
   if (d == 128 && (r8 == 16 || r8 == 24 || r8 == 32 || r8 == 48)) return r8;
   return r8 <= 32 ? -2 : (r8 <= 64 ? -4 : -8);
 }
-int instance_rt(int r8s) { return r8s > 0 ? (r8s + 15) / 16 : -r8s; }
+
+#define DKV_INSTANCES(X)                                                                                  \
+  X(128, 16) X(128, 24) X(128, 32) X(128, 48) X(128, -2) X(128, -4) X(128, -8) X(64, -2) X(64, -4) X(64, -8)
 
 cudaError_t launch_instance(int d, int r8s, const AttendArgs& a, int grid, size_t smem, cudaStream_t s) {
-  if (d == 128) {
-    switch (r8s) {
-      case 16: return launch_one<128, 16>(a, grid, smem, s);
-      case 24: return launch_one<128, 24>(a, grid, smem, s);
-      case 32: return launch_one<128, 32>(a, grid, smem, s);
-      case 48: return launch_one<128, 48>(a, grid, smem, s);
-      case -2: return launch_one<128, -2>(a, grid, smem, s);
-      case -4: return launch_one<128, -4>(a, grid, smem, s);
-      default: return launch_one<128, -8>(a, grid, smem, s);
-    }
-  }
-  switch (r8s) {
-    case -2: return launch_one<64, -2>(a, grid, smem, s);
-    case -4: return launch_one<64, -4>(a, grid, smem, s);
-    default: return launch_one<64, -8>(a, grid, smem, s);
-  }
+#define DKV_LAUNCH(D_, R_) \
+  if (d == D_ && r8s == R_) return launch_one<D_, R_>(a, grid, smem, s);
+  DKV_INSTANCES(DKV_LAUNCH)
+#undef DKV_LAUNCH
+  return cudaErrorInvalidValue;
+}
+// Arguments shared by every attention launch of a call (mode and outputs set by the caller).
+AttendArgs make_args(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
+                     const uint8_t* cache, uint8_t* ws, size_t* smem) {
+  AttendArgs a;
+  a.L = L;
+  a.G = n_q_heads / n_kv_heads;
+  a.Hq = n_q_heads;
+  a.Hkv = n_kv_heads;
+  a.K_eff = P.K_eff;
+  a.n_r = P.n_items / kConsumers;
+  a.nres = (L.R8 + kStageTok - 1) / kStageTok;
+  a.n_wst = P.n_wchunks;
+  a.mode = 0;
+  if (a.n_r <= kMaxRanges) fill_ranges(L, a.K_eff, a.nres, a.n_wst, a.n_r, a.tab);
+  const size_t extra = smem_extra();
+  a.ring = (int)((kSmemPerCta - extra) / 128 * 128);
+  a.scale_log2 = 1.4426950408889634f / sqrtf((float)L.d);
+  a.q = q;
+  a.cache = cache;
+  a.routed = reinterpret_cast<const int32_t*>(ws + P.off_routed);
+  a.routed_out = nullptr;
+  a.partials = reinterpret_cast<float*>(ws + P.off_partials);
+  a.err = reinterpret_cast<uint32_t*>(ws);
+  *smem = (size_t)a.ring + extra;
+  return a;
 }
 
 }  // namespace
@@ -804,12 +832,12 @@ DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k
   if (tc) {
     P.n_items = P.K_eff + P.n_wchunks;
   } else {
-    // one partial record per (unit, range)
+    // one partial record per (unit, range, consumer warp)
     const int nres = (L.R8 + kStageTok - 1) / kStageTok;
     const int n_list = P.n_wchunks + P.K_eff * (1 + nres);
     int n_r = ranges_per_unit(L.units);
     n_r = n_r < n_list ? n_r : n_list;
-    P.n_items = (n_r < 1 ? 1 : n_r) * kConsumers;  // one record per consumer warp
+    P.n_items = (n_r < 1 ? 1 : n_r) * kConsumers;
   }
   P.off_sched = kWsHeader;  // scheduler counters of the tensor-core kernel
   P.off_routed = round_up(P.off_sched + 8, 256);
@@ -818,36 +846,42 @@ DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k
   return P;
 }
 
+cudaError_t launch_attend_mode(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
+                               const uint8_t* cache, uint8_t* ws, float* out, float* lse, int mode,
+                               int32_t* routed_out, cudaStream_t s) {
+  size_t smem;
+  AttendArgs a = make_args(L, P, n_q_heads, n_kv_heads, q, cache, ws, &smem);
+  if (a.n_r > kMaxRanges) return cudaErrorInvalidValue;
+  a.mode = mode;
+  a.routed_out = routed_out;
+  const cudaError_t e = launch_instance(L.d, instance_r8s(L.d, L.r8), a, L.units * a.n_r, smem, s);
+  if (e != cudaSuccess || out == nullptr) return e;
+  return launch_combine(L, P, L.units / n_kv_heads, n_q_heads, n_kv_heads, a.partials, out, lse, s);
+}
+
 cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
                           const uint8_t* cache, uint8_t* ws, float* out, float* lse, cudaStream_t s) {
   if (tc_eligible(L, n_q_heads, n_kv_heads)) return launch_attend_tc(L, P, n_q_heads, n_kv_heads, q, cache, ws, out, lse, s);
-  AttendArgs a;
-  a.L = L;
-  a.G = n_q_heads / n_kv_heads;
-  a.Hq = n_q_heads;
-  a.Hkv = n_kv_heads;
-  a.K_eff = P.K_eff;
-  a.n_r = P.n_items / kConsumers;
-  a.nres = (L.R8 + kStageTok - 1) / kStageTok;
-  a.n_wst = P.n_wchunks;
-  if (a.n_r > kMaxRanges) return cudaErrorInvalidValue;
-  fill_ranges(L, a.K_eff, a.nres, a.n_wst, a.n_r, a.tab);
-  const int r8s = instance_r8s(L.d, L.r8);
-  const int RT = instance_rt(r8s);
-  (void)RT;
-  const size_t extra = smem_extra();
-  a.ring = (int)((kSmemPerCta - extra) / 128 * 128);
-  a.scale_log2 = 1.4426950408889634f / sqrtf((float)L.d);
-  a.q = q;
-  a.cache = cache;
-  a.routed = reinterpret_cast<const int32_t*>(ws + P.off_routed);
-  a.partials = reinterpret_cast<float*>(ws + P.off_partials);
-  a.err = reinterpret_cast<uint32_t*>(ws);
-  const size_t smem = (size_t)a.ring + extra;
-  const int grid = L.units * a.n_r;
-  const cudaError_t e = launch_instance(L.d, r8s, a, grid, smem, s);
-  if (e != cudaSuccess || out == nullptr) return e;
-  return launch_combine(L, P, L.units / n_kv_heads, n_q_heads, n_kv_heads, a.partials, out, lse, s);
+  return launch_attend_mode(L, P, n_q_heads, n_kv_heads, q, cache, ws, out, lse, 0, nullptr, s);
+}
+
+int decode_launches(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads) {
+  const bool all = P.K_eff == L.NB && !tc_eligible(L, n_q_heads, n_kv_heads);  // no router grid
+  return (P.K_eff > 0 && !all) ? 3 : 2;  // router, attention, combine
+}
+
+cudaError_t launch_decode(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
+                          const uint8_t* cache, uint8_t* ws, float* out, float* lse, int32_t* routed_out,
+                          cudaStream_t s) {
+  if (tc_eligible(L, n_q_heads, n_kv_heads)) {
+    cudaError_t e = cudaSuccess;
+    if (P.K_eff > 0) e = launch_route(L, P, n_q_heads, n_kv_heads, q, cache, ws, routed_out, s);
+    return e == cudaSuccess ? launch_attend_tc(L, P, n_q_heads, n_kv_heads, q, cache, ws, out, lse, s) : e;
+  }
+  if (P.K_eff == L.NB)  // every block (or none) is routed: no router grid
+    return launch_attend_mode(L, P, n_q_heads, n_kv_heads, q, cache, ws, out, lse, kModeAll, routed_out, s);
+  const cudaError_t e = launch_route(L, P, n_q_heads, n_kv_heads, q, cache, ws, routed_out, s);
+  return e == cudaSuccess ? launch_attend_mode(L, P, n_q_heads, n_kv_heads, q, cache, ws, out, lse, 0, nullptr, s) : e;
 }
 
 }  // namespace dkv

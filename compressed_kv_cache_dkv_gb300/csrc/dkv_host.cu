@@ -235,6 +235,12 @@ int dkv_append(dkv_desc* d, const void* K_new, const void* V_new, int32_t n_new,
   return dkv_layout(d);
 }
 
+int dkv_decode_launches(const dkv_desc* d, int32_t top_k) {
+  Layout L;
+  if (top_k < 0 || check_desc(d, &L) != DKV_OK) return 0;
+  return decode_launches(L, plan_decode(L, d->n_q_heads, d->n_kv_heads, top_k), d->n_q_heads, d->n_kv_heads);
+}
+
 size_t dkv_decode_workspace_bytes(const dkv_desc* d, int32_t top_k) {
   Layout L;
   if (top_k < 0 || check_desc(d, &L) != DKV_OK) return 0;
@@ -312,11 +318,8 @@ int dkv_decode_attend(const dkv_desc* d, const void* q, const void* cache, int32
   if (!aligned16(q) || !aligned16(cache) || !aligned16(out) || (lse && !aligned16(lse)) ||
       (routed && !aligned16(routed)))
     return DKV_ERR_ALIGN;
-  const __half* qh = static_cast<const __half*>(q);
-  const uint8_t* cc = static_cast<const uint8_t*>(cache);
-  cudaError_t e = cudaSuccess;
-  if (c.P.K_eff > 0) e = launch_route(c.L, c.P, d->n_q_heads, d->n_kv_heads, qh, cc, c.ws, routed, c.s);
-  if (e == cudaSuccess) e = launch_attend(c.L, c.P, d->n_q_heads, d->n_kv_heads, qh, cc, c.ws, out, lse, c.s);
+  const cudaError_t e = launch_decode(c.L, c.P, d->n_q_heads, d->n_kv_heads, static_cast<const __half*>(q),
+                                      static_cast<const uint8_t*>(cache), c.ws, out, lse, routed, c.s);
   return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
 }
 

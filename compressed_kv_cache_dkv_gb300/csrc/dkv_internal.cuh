@@ -341,6 +341,13 @@ cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, in
 // combine grid is launched right after (programmatic dependent launch)
 cudaError_t launch_attend(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
                           const uint8_t* cache, uint8_t* ws, float* out, float* lse, cudaStream_t s);
+// kernel launches launch_decode makes for this plan
+int decode_launches(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads);
+// the whole decode call: the router grid (not for the fragment layout when every
+// block is routed), the attention grid and the combine grid
+cudaError_t launch_decode(const Layout& L, const DecodePlan& P, int n_q_heads, int n_kv_heads, const __half* q,
+                          const uint8_t* cache, uint8_t* ws, float* out, float* lse, int32_t* routed_out,
+                          cudaStream_t s);
 // tcgen05 attention kernel (tensor-core cache layout)
 bool tc_eligible(const Layout& L, int n_q_heads, int n_kv_heads);
 int tc_window_tokens();

@@ -37,7 +37,7 @@ DKV_LAYOUT_TC = 1
 EXPORTED = (
     "dkv_version", "dkv_status_string", "dkv_layout", "dkv_layout_bytes",
     "dkv_compress_workspace_bytes", "dkv_compress_layout", "dkv_import_factors",
-    "dkv_decode_workspace_bytes", "dkv_decode_attend", "dkv_decode_route", "dkv_decode_blocks",
+    "dkv_decode_workspace_bytes", "dkv_decode_launches", "dkv_decode_attend", "dkv_decode_route", "dkv_decode_blocks",
     "dkv_decode_combine",
     "dkv_dense_workspace_bytes", "dkv_dense_decode", "dkv_get_error", "dkv_decode_attend_noalloc",
     "dkv_append_workspace_bytes", "dkv_append",
@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.dkv_import_factors.argtypes = [pdesc, ctypes.POINTER(dkv_factors), vp, vp, vp]
         L.dkv_decode_workspace_bytes.restype = sz
         L.dkv_decode_workspace_bytes.argtypes = [pdesc, i32]
+        L.dkv_decode_launches.restype = i32
+        L.dkv_decode_launches.argtypes = [pdesc, i32]
         L.dkv_decode_attend.argtypes = [pdesc, vp, vp, i32, vp, vp, vp, vp, sz, vp]
         L.dkv_decode_route.argtypes = [pdesc, vp, vp, i32, vp, vp, sz, vp]
         L.dkv_decode_blocks.argtypes = [pdesc, vp, vp, i32, vp, vp, vp, sz, vp]
@@ -214,6 +216,11 @@ def dkv_import_factors(d: dkv_desc, f: dict, cache: torch.Tensor | None = None,
 
 def dkv_decode_workspace_bytes(d: dkv_desc, top_k: int) -> int:
     return int(lib().dkv_decode_workspace_bytes(ctypes.byref(d), int(top_k)))
+
+
+def dkv_decode_launches(d: dkv_desc, top_k: int) -> int:
+    """Kernel launches one dkv_decode_attend call makes on the current device (1: one grid)."""
+    return int(lib().dkv_decode_launches(ctypes.byref(d), int(top_k)))
 
 
 def dkv_decode_attend(d: dkv_desc, q: torch.Tensor, cache: torch.Tensor, top_k: int,

@@ -235,15 +235,25 @@ DKV_API int dkv_decode_attend(const dkv_desc* d, const void* q, const void* cach
                       void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Kernel launches one dkv_decode_attend(d, ..., top_k, ...) makes: the router,
+ * the block/window attention and the log-sum-exp combine, 3; 2 when there is
+ * nothing to route (n_blocks == 0, or, for the fragment layout, every block
+ * routed: top_k 0 or >= n_blocks).  Returns 0 for an invalid descriptor or
+ * top_k.
+ */
+DKV_API int dkv_decode_launches(const dkv_desc* d, int32_t top_k);
+
+/*
  * The stages of dkv_decode_attend as separate calls, for callers that
  * schedule or time them individually.  Run them in this order on one stream
  * with one workspace (it carries the routed indices and the partial results
  * from stage to stage); arguments mean the same as for dkv_decode_attend.
  *   route:   top-K block selection per unit (does nothing when n_blocks == 0)
- *   blocks:  one partial (m, l, acc) per routed block and per window chunk;
- *            when `out` is given, the last CTA of each unit also merges the
- *            unit's partials into out (and lse), which is what
- *            dkv_decode_attend does; with out == NULL (and lse == NULL) the
+ *   blocks:  partial results (m, l, acc): for the fragment layout one per
+ *            unit, balanced slice of its work and consumer warp, for the
+ *            tensor-core layout one per routed block and window chunk; when
+ *            `out` is given the combine follows at once (what
+ *            dkv_decode_attend does); with out == NULL (and lse == NULL) the
  *            partials stay in the workspace for dkv_decode_combine
  *   combine: fp32 log-sum-exp merge of the partials into out (and lse)
  */

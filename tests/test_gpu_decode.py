@@ -200,8 +200,8 @@ def test_decode_is_deterministic_and_stream_ordered():
 
 @pytest.mark.parametrize("layout", LAYOUTS)
 def test_stage_calls_equal_the_fused_call_and_reuse_the_workspace(layout):
-    """route -> blocks (partials only) -> combine equals dkv_decode_attend (merge
-    fused into the attention kernel); one workspace serves many calls of
+    """route -> blocks (partials only) -> combine equals dkv_decode_attend (routing
+    and merge in the attention grid); one workspace serves many calls of
     different top-K values, since every call leaves its arrival counters at zero."""
     w = synth.WORKLOADS["8k"]
     units = H.oracle_units(w, 0, [(0, 0), (0, 1)])
@@ -220,7 +220,10 @@ def test_stage_calls_equal_the_fused_call_and_reuse_the_workspace(layout):
         dkv.dkv_decode_combine(desc, top_k, out, ws, lse=lse)
         torch.cuda.synchronize()
         assert torch.equal(routed, fr)
-        assert (out - fused).abs().max().item() <= 1e-5
-        assert (lse - fl).abs().max().item() <= 1e-5
+        # the one-grid call merges the partial records in another order than the combine
+        # kernel: fp32 reassociation over n records moves a result by at most about
+        # n * 2^-24 of its magnitude (n = 96 here)
+        assert torch.allclose(out, fused, rtol=1e-5, atol=1e-5)
+        assert torch.allclose(lse, fl, rtol=1e-5, atol=1e-5)
     st, word = dkv.dkv_get_error(ws)
     assert st == dkv.DKV_OK and word == 0
