@@ -84,73 +84,88 @@ struct Chunk {
   uint64_t off;   // source offset inside the block record / the unit's window
 };
 
-// Walks the chunks of one range in order: window stages, then block items.
+// What the consumer warps need of a chunk, written by the producer into the
+// chunk's slot of a small shared-memory queue before it arrives on the chunk's
+// full barrier (whose completion releases the descriptor with the data).
+struct ChunkDesc {
+  int kind;
+  uint32_t off;   // byte offset in the ring
+  int tok0, ntok; // exact stages
+};
+
+// Walks the chunks of one range in order: window stages, then block items
+// (item x: block slot x / (1 + nres), part x % (1 + nres); counters kept
+// incrementally, so a step costs no division).
 struct Cursor {
-  int phase, ws, ws1, it, it1, sub;
+  int ws, ws1, it, it1, j, k, sub;
   __device__ inline void init(const AttendArgs& a, int range) {
-    phase = 0;
     ws = a.tab[range][0];
     ws1 = a.tab[range][1];
     it = a.tab[range][2];
     it1 = a.tab[range][3];
+    j = it / (1 + a.nres);
+    k = it % (1 + a.nres);
     sub = 0;
   }
   __device__ inline bool next(const AttendArgs& a, Chunk& c) {
     const Layout& L = a.L;
     c.j = 0; c.tok0 = 0; c.ntok = 0; c.off = 0;
-    if (phase == 0) phase = 1;
-    if (phase == 1) {
-      if (ws < ws1) {
-        c.kind = kWin;
-        c.tok0 = ws * kStageTok;
-        c.ntok = min(kStageTok, L.W16 - c.tok0);
-        c.bytes = (uint32_t)(c.ntok * 4 * L.d);
-        c.off = (uint64_t)c.tok0 * 4 * L.d;
-        ++ws;
-        return true;
-      }
-      phase = 2;
+    if (ws < ws1) {
+      c.kind = kWin;
+      c.tok0 = ws * kStageTok;
+      c.ntok = min(kStageTok, L.W16 - c.tok0);
+      c.bytes = (uint32_t)(c.ntok * 4 * L.d);
+      c.off = (uint64_t)c.tok0 * 4 * L.d;
+      ++ws;
+      return true;
     }
-    if (phase == 2) {
-      if (it < it1) {
-        const int per = 1 + a.nres;
-        c.j = it / per;
-        const int k = it % per;
-        if (k == 0) {
-          if (sub == 0) {
-            c.kind = kHead; c.bytes = (uint32_t)L.off_u; c.off = 0;
-          } else if (sub == 1) {
-            c.kind = kU; c.bytes = (uint32_t)(L.off_res - L.off_u); c.off = L.off_u;
-          } else {
-            c.kind = kVV; c.bytes = (uint32_t)(L.block_bytes - L.off_vv); c.off = L.off_vv;
-          }
-          if (++sub == 3) { sub = 0; ++it; }
-        } else {
-          c.kind = kRes;
-          c.tok0 = (k - 1) * kStageTok;
-          c.ntok = min(kStageTok, L.R8 - c.tok0);
-          c.bytes = (uint32_t)(c.ntok * 4 * L.d);
-          c.off = L.off_res + (uint64_t)c.tok0 * 4 * L.d;
-          ++it;
-        }
-        return true;
+    if (it >= it1) return false;
+    c.j = j;
+    if (k == 0) {
+      if (sub == 0) {
+        c.kind = kHead; c.bytes = (uint32_t)L.off_u; c.off = 0;
+      } else if (sub == 1) {
+        c.kind = kU; c.bytes = (uint32_t)(L.off_res - L.off_u); c.off = L.off_u;
+      } else {
+        c.kind = kVV; c.bytes = (uint32_t)(L.block_bytes - L.off_vv); c.off = L.off_vv;
       }
-      phase = 3;
+      if (++sub < 3) return true;
+      sub = 0;
+    } else {
+      c.kind = kRes;
+      c.tok0 = (k - 1) * kStageTok;
+      c.ntok = min(kStageTok, L.R8 - c.tok0);
+      c.bytes = (uint32_t)(c.ntok * 4 * L.d);
+      c.off = L.off_res + (uint64_t)c.tok0 * 4 * L.d;
     }
-    return false;
+    ++it;
+    if (++k > a.nres) { k = 0; ++j; }
+    return true;
   }
 };
 
+// Chunks of one range (window stages, block items, and two more chunks per low-rank part)
+__device__ inline int range_chunks(const AttendArgs& a, int range) {
+  const int per = 1 + a.nres, it0 = a.tab[range][2], it1 = a.tab[range][3];
+  const int n_lr = (it1 + per - 1) / per - (it0 + per - 1) / per;  // multiples of per in [it0, it1)
+  return (a.tab[range][1] - a.tab[range][0]) + (it1 - it0) + 2 * n_lr;
+}
+
 // Place a chunk of `bytes` in the ring: chunks are contiguous, 128-byte aligned,
 // and never wrap (a chunk that would wrap starts at the ring's beginning; the
-// skipped tail counts as part of it).  `pos` is a running byte count.
-__device__ inline uint32_t ring_place(uint32_t& pos, uint32_t bytes, uint32_t ring) {
-  const uint32_t b = (bytes + 127u) & ~127u;
-  uint32_t off = pos % ring;
-  if (off + b > ring) { pos += ring - off; off = 0; }
-  pos += b;
-  return off;
-}
+// skipped tail counts as part of it).  pos: running byte count; off: pos in the ring.
+struct RingPos {
+  uint32_t pos, off;
+  __device__ inline uint32_t place(uint32_t bytes, uint32_t ring) {
+    const uint32_t b = (bytes + 127u) & ~127u;
+    if (off + b > ring) { pos += ring - off; off = 0; }
+    const uint32_t at = off;
+    pos += b;
+    off += b;
+    if (off >= ring) off = 0;
+    return at;
+  }
+};
 
 __device__ inline float warp_max_rows(float v) {  // over lanes with the same lane % 4
   v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
@@ -314,7 +329,7 @@ struct BlockState {
 // shared memory: [ring][full kNBar][empty kNBar][query barrier][ends kNBar]
 // [query rows 8 x (D + 8) fp16][a_v, one copy per consumer warp: 4 x D fp16]
 __host__ __device__ inline size_t smem_extra() {
-  return (size_t)kNBar * 8 * 2 + 16 + (size_t)kNBar * 4 + 8 * 136 * 2 + kConsumers * 128 * 2 + 64;
+  return (size_t)kNBar * 8 * 2 + 16 + (size_t)kNBar * 4 + 8 * 136 * 2 + kConsumers * 128 * 2 + kNBar * 16 + 64;
 }
 
 template <int D, int R8S>
@@ -330,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
   uint32_t* ends = reinterpret_cast<uint32_t*>(qbar + 2);
   __half* qsm = reinterpret_cast<__half*>(ends + kNBar);  // [8][D + 8]: 16-byte aligned rows
   __half* avw = qsm + 8 * (D + 8);                        // [4][D]
+  ChunkDesc* cdq = reinterpret_cast<ChunkDesc*>(avw + kConsumers * 128);  // [kNBar] chunk descriptors
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x / a.n_r, range = blockIdx.x % a.n_r;
   if (threadIdx.x == 0) {
@@ -354,22 +370,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
     Cursor cur;
     cur.init(a, range);
     Chunk ch;
-    uint32_t pos = 0, rel_end = 0;
+    RingPos rp = {0u, 0u};
+    uint32_t rel_end = 0;
     int c = 0, rel = 0;      // chunks issued; chunks whose release has been seen
     bool routed_ready = false;
     int jb = -1;
     const uint8_t* blk = unit;
     while (cur.next(a, ch)) {
-      const uint32_t off = ring_place(pos, ch.bytes, ring);
+      const uint32_t off = rp.place(ch.bytes, ring);
       // wait until the chunk's bytes and barrier pair are free: the chunks not yet
       // released occupy [rel_end, start) of the running byte count (releases come in order)
-      while (c - rel >= kNBar || (rel < c && pos - rel_end > ring)) {
-        if (!mbar_wait(&empty[rel % kNBar], (uint32_t)(rel / kNBar) & 1u, a.err)) return;
-        rel_end = ends[rel % kNBar];
+      while (c - rel >= kNBar || (rel < c && rp.pos - rel_end > ring)) {
+        const int rb = rel & (kNBar - 1);
+        if (!mbar_wait(&empty[rb], (uint32_t)(rel / kNBar) & 1u, a.err)) return;
+        rel_end = ends[rb];
         ++rel;
       }
-      ends[c % kNBar] = pos;
-      uint64_t* fb = &full[c % kNBar];
+      const int cb = c & (kNBar - 1);
+      ends[cb] = rp.pos;
+      ChunkDesc dsc;
+      dsc.kind = ch.kind;
+      dsc.off = off;
+      dsc.tok0 = ch.tok0;
+      dsc.ntok = ch.ntok;
+      cdq[cb] = dsc;  // released to the consumers by this chunk's barrier phase
+      uint64_t* fb = &full[cb];
       uint8_t* dst = smem + off;
       if (ch.kind == kWin) {
         mbar_arrive_expect_tx(fb, ch.bytes);
@@ -421,18 +446,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
   st.l0 = st.l1 = 0.f;
 #pragma unroll
   for (int i = 0; i < KT; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
-  Cursor cur;
-  cur.init(a, range);
-  Chunk ch;
-  uint32_t pos = 0;
-  int c = 0;
-  while (cur.next(a, ch)) {
-    const uint32_t off = ring_place(pos, ch.bytes, ring);
-    const int bi = c % kNBar;
+  const int n_chunks = range_chunks(a, range);
+  for (int c = 0; c < n_chunks; ++c) {
+    const int bi = c & (kNBar - 1);
     if (alive) alive = mbar_wait(&full[bi], (uint32_t)(c / kNBar) & 1u, a.err);
-    const uint32_t sb = sbase + off;
-    const uint8_t* sp = smem + off;
-    switch (ch.kind) {
+    const ChunkDesc ch = cdq[bi];  // kind, ring offset and tokens, from the producer
+    const uint32_t sb = sbase + ch.off;
+    const uint8_t* sp = smem + ch.off;
+    switch (alive ? ch.kind : -1) {
       case kWin:
       case kRes: {
         const int in_g = max(0, min(16, ch.ntok - 16 * warp));
@@ -636,7 +657,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[bi]);
-    ++c;
   }
   // this warp's partial record (m, l, o) over every token it scored; the combine merges them
   const float l0 = warp_sum_rows(st.l0), l1 = warp_sum_rows(st.l1);
