@@ -65,6 +65,7 @@ constexpr int kModeAll = 2;
 struct AttendArgs {
   Layout L;
   int G, Hq, Hkv, K_eff, n_r, nres, n_wst, ring, mode;
+  uint32_t inflight;  // bytes a CTA keeps in flight (issued, not yet landed) at most
   float scale_log2;  // log2(e) / sqrt(d)
   const __half* q;
   const uint8_t* cache;
@@ -371,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
     cur.init(a, range);
     Chunk ch;
     RingPos rp = {0u, 0u};
-    uint32_t rel_end = 0;
-    int c = 0, rel = 0;      // chunks issued; chunks whose release has been seen
+    uint32_t rel_end = 0, land_end = 0;
+    int c = 0, rel = 0, land = 0;  // chunks issued; released (seen); landed (seen)
     bool routed_ready = false;
     int jb = -1;
     const uint8_t* blk = unit;
@@ -385,6 +386,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
         if (!mbar_wait(&empty[rb], (uint32_t)(rel / kNBar) & 1u, a.err)) return;
         rel_end = ends[rb];
         ++rel;
+      }
+      // keep at most a.inflight bytes in flight: more only lengthens the queues of the
+      // memory system (every CTA's first chunks land later) without adding bandwidth
+      if (land < rel) { land = rel; land_end = rel_end; }
+      while (land < c && rp.pos - land_end > a.inflight) {
+        const int lb = land & (kNBar - 1);
+        if (!mbar_wait(&full[lb], (uint32_t)(land / kNBar) & 1u, a.err)) return;
+        land_end = ends[lb];
+        ++land;
       }
       const int cb = c & (kNBar - 1);
       ends[cb] = rp.pos;
@@ -818,6 +828,9 @@ AttendArgs make_args(const Layout& L, const DecodePlan& P, int n_q_heads, int n_
   if (a.n_r <= kMaxRanges) fill_ranges(L, a.K_eff, a.nres, a.n_wst, a.n_r, a.tab);
   const size_t extra = smem_extra();
   a.ring = (int)((kSmemPerCta - extra) / 128 * 128);
+  // 64 KB in flight per CTA (about 19 MB over the grid) covers the memory latency at full
+  // bandwidth; measured on GB300 against 16, 24, 40 KB and the whole ring (about 103 KB)
+  a.inflight = a.ring < 65536 ? (uint32_t)a.ring : 65536u;
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)L.d);
   a.q = q;
   a.cache = cache;
