@@ -223,16 +223,18 @@ struct WarpState {
 // rescale of o.  The record's (m, l, o) stays consistent whatever m is.
 constexpr float kSlack = 8.f;
 
-// Include the tile maxima (mx0, mx1) (reduced over the warp here).  Returns
+// Include this lane's tile maxima (mx0, mx1) of its two columns.  Returns
 // whether the accumulated state was rescaled (a warp-uniform answer), the
 // rescale factors (1 if not) and the subtrahends of the new p.
 template <int D>
 __device__ inline bool raise_max(WarpState<D>& st, float mx0, float mx1, float& sc0, float& sc1, float& ms0,
                                  float& ms1) {
-  mx0 = warp_max_rows(mx0);
-  mx1 = warp_max_rows(mx1);
+  // st.m is the same on every lane of a column, so the vote can take each lane's own
+  // tile maximum: the reduction over the column's lanes runs only when the maximum moves
   const bool up = __any_sync(0xffffffffu, mx0 > st.m0 + kSlack || mx1 > st.m1 + kSlack);
   if (up) {
+    mx0 = warp_max_rows(mx0);
+    mx1 = warp_max_rows(mx1);
     const float n0 = fmaxf(st.m0, mx0), n1 = fmaxf(st.m1, mx1);
     ms0 = n0 == -INFINITY ? 0.f : n0;
     ms1 = n1 == -INFINITY ? 0.f : n1;
