@@ -21,11 +21,9 @@ namespace dkv {
 namespace {
 
 constexpr int kRouteCluster = 8;    // CTAs per unit (one thread-block cluster)
-// 128 threads (8 K registers): a router CTA fits on an SM beside two attention
-// CTAs of the same call, which start while routing runs
-constexpr int kRouteThreads = 128;
-constexpr int kRouteInFlight = 4;   // router rows in flight per lane (kmin and kmax pieces each)
-constexpr int kRouteRounds = 2;     // ranking rounds: 2048 blocks over 8 CTAs of 128 threads
+constexpr int kRouteThreads = 256;
+constexpr int kRouteInFlight = 2;   // router rows in flight per lane (kmin and kmax pieces each)
+constexpr int kRouteRounds = 2;     // ranking rounds (one at up to 2048 blocks over 8 CTAs of 256 threads)
 
 // One cluster of kRouteCluster CTAs per unit; CTA c of the cluster owns blocks
 // [c*per, (c+1)*per).  Each CTA loads its blocks' router rows ([kmin | kmax],
@@ -178,7 +176,7 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
 }
 
 constexpr int kCombineThreads = 256;
-constexpr int kCombinePrefetch = 4;
+constexpr int kCombinePrefetch = 8;  // records a thread loads before the reduction: 64 per pass at d = 128
 
 // One CTA per (unit, query head).  Partial records of all items are merged with
 // weights exp2(m_i - m*) / l* (m*, l* the merged maximum and normaliser);

@@ -1,9 +1,8 @@
 """Routing on the GPU against the oracle's router ("Decode router bounds" of
 the Differential-KV README's per-block memory table; DKV_TOPK_BLOCKS and
 DKV_CB_GQA_ROUTE, README "Key Environment Knobs"), at block counts the other
-parity tests do not reach: 1000 blocks, and 1100, where each CTA of the
-router's 8-CTA cluster owns more blocks than it has threads and ranks them in
-two rounds.
+parity tests do not reach (1000 and 1100 blocks: 125 and 138 blocks for each
+CTA of the router's 8-CTA cluster).
 
 The cache comes from the GPU compressor (the router rows are the exact fp16
 key minima and maxima, so both sides bound the same keys).  Routed indices
