@@ -198,6 +198,31 @@ __device__ inline uint4 ld_tile(uint32_t base, int lane, bool full) {
   return make_uint4(full ? v.x : (odd ? v.z : v.x), full ? v.y : (odd ? v.w : v.y), v.z, v.w);
 }
 
+// ldmatrix: four (x4) or two (x2) 8x8 b16 matrices, row addresses from lanes 8i..8i+7
+// for matrix i; .trans gives the transposed matrices' fragments
+__device__ inline uint4 ldsm4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ inline uint4 ldsm4t(uint32_t addr) {
+  uint4 v;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ inline uint2 ldsm2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ inline uint2 ldsm2t(uint32_t addr) {
+  uint2 v;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
 // C fragment (rows = k, two columns per lane) -> B fragments (k, n = group), hi and lo
 __device__ inline void c_to_b(float c0, float c1, float c2, float c3, uint32_t& bh0, uint32_t& bl0, uint32_t& bh1,
                               uint32_t& bl1) {
@@ -549,27 +574,38 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
       }
       case kU: {
         if (!alive) break;
-        // this warp's 64 U rows: m-tiles 4 warp .. 4 warp + 3
+        // this warp's 64 U rows: m-tiles 4 warp .. 4 warp + 3.  U is stored as 8x8 core
+        // matrices (8 tokens x 8 r, 128 contiguous bytes; tc_u_off): ldmatrix gives the A
+        // fragments of U (m = tokens, k = r) and, transposed, those of U^T (m = r, k = tokens).
         constexpr int MT = 4;
-        const uint32_t ub = sb + (uint32_t)(warp * MT * 16 * r8 * 2);
+        const int mi = lane >> 3, mrow = lane & 7;  // this lane's matrix and row of an ldmatrix
+        // byte offset of core matrix (8-token group starting at token tk, r group rg)
+        auto core = [&](int tk, int rg) -> uint32_t {
+          return (uint32_t)((tk >> 7) * 256 * r8 + ((tk & 127) >> 3) * 16 * r8 + rg * 128 + mrow * 16);
+        };
         float s[MT][4];
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          const uint32_t tb = ub + (uint32_t)(mt * 16 * r8 * 2);
+          const int t0 = 64 * warp + 16 * mt;
           uint4 uv[RT];
 #pragma unroll
-          for (int kk = 0; kk < RT; ++kk)
-            uv[kk] = kk < nrt ? ld_tile(tb + (uint32_t)(kk * 512), lane, kk < nkk) : make_uint4(0u, 0u, 0u, 0u);
+          for (int kk = 0; kk < RT; ++kk) {
+            uv[kk] = make_uint4(0u, 0u, 0u, 0u);
+            if (kk < nkk) {  // a0..a3: (tokens 0-7 | 8-15) x (r 0-7 | 8-15) of the tile
+              uv[kk] = ldsm4(sb + core(t0 + 8 * (mi & 1), 2 * kk + (mi >> 1)));
+            } else if (kk < nrt) {  // a half-width tile: a0, a1 (r 0-7)
+              const uint2 h = ldsm2(sb + core(t0 + 8 * (mi & 1), 2 * kk));
+              uv[kk].x = h.x;
+              uv[kk].y = h.y;
+            }
+          }
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int kk = 0; kk < RT; ++kk) {
             if (kk < nrt) {
-              const bool fullk = kk < nkk;
-              // a half tile holds (x, y) = rows gq and gq + 8 of k 2t..2t+1 only
-              const uint32_t a2 = fullk ? uv[kk].z : 0u, a3 = fullk ? uv[kk].w : 0u;
-              mma16816(acc, uv[kk].x, uv[kk].y, a2, a3, bs.zh[kk][0], bs.zh[kk][1]);
-              mma16816(acc, uv[kk].x, uv[kk].y, a2, a3, bs.zl[kk][0], bs.zl[kk][1]);
+              mma16816(acc, uv[kk].x, uv[kk].y, uv[kk].z, uv[kk].w, bs.zh[kk][0], bs.zh[kk][1]);
+              mma16816(acc, uv[kk].x, uv[kk].y, uv[kk].z, uv[kk].w, bs.zl[kk][0], bs.zl[kk][1]);
             }
           }
           const uint32_t wsel = mt < 2 ? bs.mk0 : bs.mk1;
@@ -588,14 +624,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
         bs.pa1 *= sc1;
 #pragma unroll
         for (int i = 0; i < RT; ++i) { bs.w[i][0] *= sc0; bs.w[i][1] *= sc1; bs.w[i][2] *= sc0; bs.w[i][3] *= sc1; }
-        // p, and w += U^T p (U fragments reloaded, transposed in registers)
+        // p, and w += U^T p (U^T fragments straight from shared memory)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          const uint32_t tb = ub + (uint32_t)(mt * 16 * r8 * 2);
+          const int t0 = 64 * warp + 16 * mt;
           uint4 uv[RT];
 #pragma unroll
-          for (int mr = 0; mr < RT; ++mr)
-            uv[mr] = mr < nrt ? ld_tile(tb + (uint32_t)(mr * 512), lane, mr < nkk) : make_uint4(0u, 0u, 0u, 0u);
+          for (int mr = 0; mr < RT; ++mr) {
+            uv[mr] = make_uint4(0u, 0u, 0u, 0u);
+            if (mr < nkk) {  // a0..a3: (r 0-7 | 8-15) x (tokens 0-7 | 8-15), transposed core matrices
+              uv[mr] = ldsm4t(sb + core(t0 + 8 * (mi >> 1), 2 * mr + (mi & 1)));
+            } else if (mr < nrt) {  // a half-width tile: a0, a2 (r 0-7)
+              const uint2 h = ldsm2t(sb + core(t0 + 8 * (mi & 1), 2 * mr));
+              uv[mr].x = h.x;
+              uv[mr].z = h.y;
+            }
+          }
           float p[4];
           p[0] = gv0 ? fast_exp2(s[mt][0] - ms0) : 0.f;
           p[1] = gv1 ? fast_exp2(s[mt][1] - ms1) : 0.f;
@@ -610,12 +654,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
 #pragma unroll
           for (int mr = 0; mr < RT; ++mr) {
             if (mr < nrt) {
-              const bool fullk = mr < nkk;
-              // U^T tile (m = r, k = tokens): a half tile only has the first r half
-              const uint32_t A0 = movtrans(uv[mr].x), A2 = movtrans(uv[mr].y);
-              const uint32_t A1 = fullk ? movtrans(uv[mr].z) : 0u, A3 = fullk ? movtrans(uv[mr].w) : 0u;
-              mma16816(bs.w[mr], A0, A1, A2, A3, bh0, bh1);
-              mma16816(bs.w[mr], A0, A1, A2, A3, bl0, bl1);
+              mma16816(bs.w[mr], uv[mr].x, uv[mr].y, uv[mr].z, uv[mr].w, bh0, bh1);
+              mma16816(bs.w[mr], uv[mr].x, uv[mr].y, uv[mr].z, uv[mr].w, bl0, bl1);
             }
           }
         }

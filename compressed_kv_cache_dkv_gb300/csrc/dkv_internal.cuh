@@ -16,7 +16,7 @@ namespace dkv {
 //   [0, 4d)            a_k[d], a_v[d]                       fp16, plain
 //   [4d, 4d+32)        residual mask, 256 bits (bit i = token i kept exact)
 //   [off_vk, off_u)    V_K  [r8][d]   "B^T layout"  (B operand of z^T = q^T V_K^T)
-//   [off_u, off_res)   U    [256][r8] "A layout"    (row 0 = anchor, all zero)
+//   [off_u, off_res)   U    [256][r8] as 8x8 core matrices (tc_u_off; row 0 = anchor, all zero)
 //   [off_res, off_vv)  residual groups of 16 tokens (last group may hold 8):
 //                      K_res tile in "A layout" then V_res^T tile in "A layout"
 //   [off_vv, bytes)    V_V^T [d][r8]  "A layout"    (A operand of o = V_V^T w)
@@ -123,7 +123,7 @@ __host__ __device__ inline uint32_t exact_v_off(int n_tok, int d, int t, int j) 
 }
 
 __host__ __device__ inline uint64_t blk_u_off(const Layout& L, int t, int k) {
-  return L.off_u + (L.tc ? tc_u_off(L.r8, t, k) : a_layout_off(256, L.r8, t, k));
+  return L.off_u + tc_u_off(L.r8, t, k);  // both layouts: 8 x 8 core matrices
 }
 __host__ __device__ inline uint64_t blk_vv_off(const Layout& L, int k, int j) {
   return L.off_vv + (L.tc ? tc_rd_off(L.d, k, j) : a_layout_off(L.d, L.r8, j, k));

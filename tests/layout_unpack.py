@@ -86,7 +86,7 @@ def unpack_block(cache: np.ndarray, desc, u: int, b: int) -> dict:
     vk = h(blk + desc.blk_off_vk, r8 * d)
     out["V_K"] = vk[bt_layout_index(r8, d)][:r].copy()
     uu = h(blk + desc.blk_off_u, 256 * r8)
-    Ufull = uu[u_index(r8)] if tc else uu[a_layout_index(256, r8)]
+    Ufull = uu[u_index(r8)]  # both layouts store U as 8 x 8 core matrices
     out["U_row0"] = Ufull[0].copy()
     out["U"] = Ufull[1:, :r].copy()
     res = h(blk + desc.blk_off_res, 2 * R8 * d)
