@@ -5,8 +5,10 @@
 // Environment Knobs") scores every block by the upper bound of qbar . k over
 // the block's key box, sum_j max(qbar_j kmax_bj, qbar_j kmin_bj) (the per-block
 // "Key Min/Max ... Decode router bounds" of the README's per-block memory
-// table), and keeps the top K (DKV_TOPK_BLOCKS) by (score desc, index asc);
-// indices are written in ascending order.
+// table), and keeps the top K (DKV_TOPK_BLOCKS) by (score desc, index asc).
+// The selected indices are written in ascending order when the caller asks for
+// them; otherwise slot k of the attention grid's list holds the block of rank k
+// (the attention result does not depend on the order of its blocks).
 //
 // combine: the flash-style log-sum-exp merge of every partial of a unit
 // ("Flash-Style LSE Combine", README section "Core Architecture & Paper
@@ -31,7 +33,8 @@ constexpr int kRouteRounds = 2;     // ranking rounds (one at up to 2048 blocks 
 // cluster (distributed shared memory).  After a cluster barrier each CTA ranks
 // its own blocks against all NB bounds (score desc, index asc), and the
 // selected counts are exchanged once more so each CTA knows where its blocks
-// go in the ascending output.
+// go in the ascending output.  Without a caller's copy the rank itself is the
+// slot: no second exchange, and every CTA is done after its own ranking.
 //
 // max(q kmax, q kmin) equals q kmax for q >= 0 and q kmin for q < 0 (rounding
 // is monotone), so every channel costs one select and one FMA.
@@ -131,6 +134,7 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
   const int rounds = (n_own + per_round - 1) / per_round;  // at most kRouteRounds (NB <= 2048)
   const int sub = tid % tpb;
   bool sel[kRouteRounds];
+  int rk[kRouteRounds];
   unsigned bal[kRouteRounds];
 #pragma unroll
   for (int r = 0; r < kRouteRounds; ++r) {
@@ -150,9 +154,16 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
       }
     }
     for (int o = tpb >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    rk[r] = K_eff < NB ? rank : i;  // every block routed: block i in slot i
     sel[r] = mine && sub == 0 && rank < K_eff;
     bal[r] = __ballot_sync(0xffffffffu, sel[r]);
     if (lane == 0) wsum[r * nw + warp] = __popc(bal[r]);
+  }
+  if (routed_out == nullptr) {  // slot = rank; no peer access follows the first cluster barrier
+#pragma unroll
+    for (int r = 0; r < kRouteRounds; ++r)
+      if (sel[r]) routed[(size_t)u * K_eff + rk[r]] = b0 + r * per_round + tid / tpb;
+    return;
   }
   __syncthreads();
   int total = 0;  // selected blocks of this CTA
