@@ -27,6 +27,16 @@ constexpr int kRouteThreads = 256;
 constexpr int kRouteInFlight = 2;   // router rows in flight per lane (kmin and kmax pieces each)
 constexpr int kRouteRounds = 2;     // ranking rounds (one at up to 2048 blocks over 8 CTAs of 256 threads)
 
+// Order-preserving integer image of a bound: a < b as floats iff key(a) < key(b)
+// as int32, equal floats give equal keys (-0 is taken as +0; NaN is ranked as
+// -inf).  key - 1 never overflows (key(-inf) is far above INT_MIN).
+__device__ inline int bound_key(float v) {
+  if (isnan(v)) v = -INFINITY;
+  if (v == 0.f) v = 0.f;
+  const int u = __float_as_int(v);
+  return u >= 0 ? u : u ^ 0x7fffffff;
+}
+
 // One cluster of kRouteCluster CTAs per unit; CTA c of the cluster owns blocks
 // [c*per, (c+1)*per).  Each CTA loads its blocks' router rows ([kmin | kmax],
 // 4d bytes per block), bounds them, and stores every bound into all CTAs of the
@@ -41,7 +51,7 @@ constexpr int kRouteRounds = 2;     // ranking rounds (one at up to 2048 blocks 
 __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteThreads)
     route_kernel(Layout L, int G, int Hq, int Hkv, int K_eff, float cq, const __half* __restrict__ q,
                  const uint8_t* __restrict__ cache, int32_t* __restrict__ routed, int32_t* __restrict__ routed_out) {
-  extern __shared__ float4 sc4[];  // bounds of all NB blocks of the unit, padded to 4 with -inf
+  extern __shared__ int4 key4[];  // bound keys of all NB blocks of the unit, padded to 4 with key(-inf)
   __shared__ float qbar[128];
   __shared__ int cnt[kRouteCluster];
   __shared__ int wsum[kRouteRounds * (kRouteThreads / 32)];
@@ -83,9 +93,9 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
     for (int g = 0; g < 8; ++g) t += x[g];
     qbar[j] = t * cq;  // cq = c / G
   }
-  float* sc = reinterpret_cast<float*>(sc4);
+  int* key = reinterpret_cast<int*>(key4);
   const int NB4 = (NB + 3) / 4;
-  if (tid < 4 * NB4 - NB) sc[NB + tid] = -INFINITY;  // padding never outranks a block
+  if (tid < 4 * NB4 - NB) key[NB + tid] = bound_key(-INFINITY);  // padding never outranks a block
   __syncthreads();
   float qv[8];
   uint32_t selm[4];  // per half: all ones where q_j >= 0 (take kmax), zero where q_j < 0 (take kmin)
@@ -121,7 +131,7 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
         acc = fmaf(qv[2 * w + 1], f.y, acc);
       }
       for (int o = hp >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (blk < b1 && piece < kRouteCluster) st_cluster_f32(sc + blk, (uint32_t)piece, isnan(acc) ? -INFINITY : acc);
+      if (blk < b1 && piece < kRouteCluster) st_cluster_s32(key + blk, (uint32_t)piece, bound_key(acc));
     }
   }
   cluster_sync();  // all NB bounds are in every CTA
@@ -138,25 +148,36 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
   unsigned bal[kRouteRounds];
 #pragma unroll
   for (int r = 0; r < kRouteRounds; ++r) {
-    const int own = r * per_round + tid / tpb;
-    const int i = b0 + own;
-    const bool mine = r < rounds && own < n_own;
-    int rank = 0;
-    if (mine && K_eff < NB) {
-      const float bi = sc[i];
-      for (int j4 = sub; j4 < NB4; j4 += tpb) {
-        const float4 bj = sc4[j4];
-        const int j = 4 * j4;
-        rank += (bj.x > bi) || (bj.x == bi && j < i);
-        rank += (bj.y > bi) || (bj.y == bi && j + 1 < i);
-        rank += (bj.z > bi) || (bj.z == bi && j + 2 < i);
-        rank += (bj.w > bi) || (bj.w == bi && j + 3 < i);
+    sel[r] = false;
+    rk[r] = 0;
+    bal[r] = 0u;
+    if (r < rounds) {  // uniform over the CTA
+      const int own = r * per_round + tid / tpb;
+      const int i = b0 + own;
+      const bool mine = own < n_own;
+      int rank = 0;
+      if (mine && K_eff < NB) {
+        // rank of i = #{j < i: key_j >= key_i} + #{j > i: key_j > key_i}: one threshold per
+        // group of four (key_i - 1 below i's group, key_i from it on), and the ties
+        // inside i's own group below i added once
+        const int ki = key[i], i4 = i >> 2;
+        int ra = 0, rb = 0;
+#pragma unroll 2
+        for (int j4 = sub; j4 < NB4; j4 += tpb) {
+          const int4 kj = key4[j4];
+          const int th = j4 < i4 ? ki - 1 : ki;
+          ra += (kj.x > th) + (kj.y > th);
+          rb += (kj.z > th) + (kj.w > th);
+        }
+        rank = ra + rb;
+        if (sub == 0)
+          for (int e = i & ~3; e < i; ++e) rank += key[e] == ki;
       }
+      for (int o = tpb >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+      rk[r] = K_eff < NB ? rank : i;  // every block routed: block i in slot i
+      sel[r] = mine && sub == 0 && rank < K_eff;
+      bal[r] = __ballot_sync(0xffffffffu, sel[r]);
     }
-    for (int o = tpb >> 1; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-    rk[r] = K_eff < NB ? rank : i;  // every block routed: block i in slot i
-    sel[r] = mine && sub == 0 && rank < K_eff;
-    bal[r] = __ballot_sync(0xffffffffu, sel[r]);
     if (lane == 0) wsum[r * nw + warp] = __popc(bal[r]);
   }
   if (routed_out == nullptr) {  // slot = rank; no peer access follows the first cluster barrier
