@@ -222,7 +222,9 @@ DKV_API int dkv_append(dkv_desc* d, const void* K_new, const void* V_new, int32_
  *           routed blocks and the window, c = 1/sqrt(head_dim)
  *   lse     optional device fp32 [B][Hq]: natural-log log-sum-exp of the scores
  *   routed  optional device int32 [B][Hkv][K_eff]: routed block indices,
- *           ascending, K_eff = top_k clipped to n_blocks
+ *           ascending, K_eff = top_k clipped to n_blocks.  Asking for them
+ *           costs the router a second cluster exchange (about 1 us); without
+ *           them the router writes each block to its rank's slot.
  *   workspace / ws_bytes  device scratch of dkv_decode_workspace_bytes(d, top_k);
  *           zero-fill it once before its first use: it holds per-unit arrival
  *           counters that every call leaves at zero again
@@ -248,7 +250,12 @@ DKV_API int dkv_decode_launches(const dkv_desc* d, int32_t top_k);
  * schedule or time them individually.  Run them in this order on one stream
  * with one workspace (it carries the routed indices and the partial results
  * from stage to stage); arguments mean the same as for dkv_decode_attend.
- *   route:   top-K block selection per unit (does nothing when n_blocks == 0)
+ *   route:   top-K block selection per unit (does nothing when n_blocks == 0).
+ *            With `routed` given, the workspace list and the caller's copy
+ *            hold the indices in ascending order; with routed == NULL the
+ *            workspace list holds block of rank k (by score desc, index asc)
+ *            in slot k.  The attention result is the same set of blocks
+ *            either way; only the fp32 summation order differs.
  *   blocks:  partial results (m, l, acc): for the fragment layout one per
  *            unit, balanced slice of its work and consumer warp, for the
  *            tensor-core layout one per routed block and window chunk; when
