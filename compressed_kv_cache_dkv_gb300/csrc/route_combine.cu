@@ -135,8 +135,9 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
     }
   }
   cluster_sync();  // all NB bounds are in every CTA
-  // rank own blocks: tpb threads share one block's comparisons; with more blocks
-  // than threads (NB > 8 x 128) a CTA ranks its blocks in two rounds
+  // rank own blocks: tpb threads share one block's comparisons (tpb = 1 at the
+  // 2048-block limit: 256 blocks per CTA); a CTA with more blocks than threads
+  // would rank them in rounds, which the block limit never needs
   const int n_own = b1 - b0;
   int tpb = 32;
   while (tpb > 1 && tpb * n_own > kRouteThreads) tpb >>= 1;

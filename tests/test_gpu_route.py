@@ -1,8 +1,8 @@
 """Routing on the GPU against the oracle's router ("Decode router bounds" of
 the Differential-KV README's per-block memory table; DKV_TOPK_BLOCKS and
 DKV_CB_GQA_ROUTE, README "Key Environment Knobs"), at block counts the other
-parity tests do not reach (1000 and 1100 blocks: 125 and 138 blocks for each
-CTA of the router's 8-CTA cluster).
+parity tests do not reach (1000, 1100 and the 2048-block limit: 125, 138 and
+256 blocks for each CTA of the router's 8-CTA cluster).
 
 The cache comes from the GPU compressor (the router rows are the exact fp16
 key minima and maxima, so both sides bound the same keys).  Routed indices
@@ -22,7 +22,7 @@ from tests import helpers as H
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("n_blocks, top_ks", [(1000, [1, 7, 300, 999]), (1100, [5, 600])])
+@pytest.mark.parametrize("n_blocks, top_ks", [(1000, [1, 7, 300, 999]), (1100, [5, 600]), (2048, [1, 16, 2047])])
 def test_routing_at_large_block_counts(n_blocks, top_ks):
     d, G, B, Hkv = 64, 6, 1, 2
     w = synth.Workload("route", B, G * Hkv, Hkv, d, n_blocks, 16, (8,), 8, 2, 4, False, 11)
