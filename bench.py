@@ -81,6 +81,12 @@ def call_bytes(w, layer: int, top_k: int) -> int:
             + w.batch * w.n_q_heads * w.head_dim * 4)
 
 
+def cache_replicas(bytes_per_pass: int, l2_bytes: int) -> int:
+    """Cache replicas a step's calls rotate over, so that the bytes one step reads
+    (bytes_per_pass per replica) span at least 4x the L2: 1 when one pass already does."""
+    return max(1, -(-4 * l2_bytes // max(1, bytes_per_pass)))
+
+
 # ----------------------------------------------------------------------------- clocks (NVML, read only)
 
 REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
@@ -310,8 +316,7 @@ def main():
     # span at least 4x the L2 and every call reads its cache from HBM.  Each replica is a
     # separate copy of the cache at its own address.
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    one_pass = sum(call_bytes(w, l, top_k) for l in layer_ids)
-    n_rep = max(1, -(-4 * l2_bytes // max(1, one_pass)))
+    n_rep = cache_replicas(sum(call_bytes(w, l, top_k) for l in layer_ids), l2_bytes)
     if n_rep > 1:
         layer_ids = layer_ids * n_rep
         n_layers = len(layer_ids)

@@ -48,3 +48,19 @@ def test_whole_job_rate_counts_every_replica():
     # 192 queries per step, 100 steps in 250 ms on each of 4 ranks -> 4 * 19200 / 0.25 s
     assert bench.whole_job_rate(4, 192, 100, 250.0) == pytest.approx(4 * 192 * 100 / 0.25)
     assert bench.whole_job_rate(1, 192, 100, 250.0) * 4 == pytest.approx(bench.whole_job_rate(4, 192, 100, 250.0))
+
+
+def test_small_workloads_rotate_over_enough_cache_replicas():
+    import bench
+    from compressed_kv_cache_dkv_gb300 import synth
+    l2 = 126 << 20
+    # the 64k step reads 2 GB: no replicas
+    w = synth.WORKLOADS["64k"]
+    assert bench.cache_replicas(sum(bench.call_bytes(w, l, w.top_k) for l in range(w.n_layers)), l2) == 1
+    # 32k and 8k read 9.0 and 1.4 MB per call: a step's reads reach 4x the L2, and one replica
+    # fewer would not
+    for name in ("32k", "8k"):
+        w = synth.WORKLOADS[name]
+        per = bench.call_bytes(w, 0, w.top_k)
+        n = bench.cache_replicas(per, l2)
+        assert n * per >= 4 * l2 > (n - 1) * per
