@@ -1,0 +1,235 @@
+"""Planted mistakes in the oracle (CPU only).
+
+Each case swaps one function of the fp64 oracle for a copy with one plausible
+slip (a dropped term, a wrong sign, index or tie order, a transposed or swapped
+operand, a missing rescale) and runs the pins of tests/test_oracle_pins.py
+against it: at least one pin must fail.  A slip that no pin catches would mean
+the pins leave that part of the oracle unchecked.  The mistakes are planted in
+the oracle only, on the CPU; nothing here touches the GPU path.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import dkv_oracle as O
+from tests import test_oracle_pins as P
+
+BS = O.BLOCK_SIZE
+
+
+def _pin_calls():
+    """Every pin of test_oracle_pins with each of its parameter sets."""
+    calls = []
+    for name in sorted(n for n in dir(P) if n.startswith("test_")):
+        f = getattr(P, name)
+        params = [m for m in getattr(f, "pytestmark", []) if m.name == "parametrize"]
+        if not params:
+            calls.append((name, f, {}))
+            continue
+        assert len(params) == 1, name
+        argnames, values = params[0].args[0], params[0].args[1]
+        argnames = [a.strip() for a in argnames.split(",")] if isinstance(argnames, str) else list(argnames)
+        for v in values:
+            v = tuple(v) if len(argnames) > 1 else (v,)
+            calls.append((name, f, dict(zip(argnames, v))))
+    return calls
+
+
+def _first_failing_pin(monkeypatch, fn_name, mutant):
+    """The first pin whose assertion fails with the mutant in place, and the
+    other errors met on the way (an error is not a catch: it may be the
+    mutant's own fault)."""
+    monkeypatch.setattr(O, fn_name, mutant)
+    errors = []
+    for name, f, kw in _pin_calls():
+        try:
+            f(**kw)
+        except (AssertionError, pytest.fail.Exception):
+            return name, errors
+        except Exception as e:
+            errors.append(f"{name}{kw}: {type(e).__name__}: {e}")
+    return None, errors
+
+
+# ----------------------------------------------------------------------------- mutants
+
+_orig = {n: getattr(O, n) for n in ("router_bounds", "route", "select_residuals", "compress_block",
+                                    "reconstruct_block", "softmax_attention", "lse_merge", "block_partial",
+                                    "decode_unit", "append_tokens", "effective_top_k")}
+
+
+def _bounds_without_kmin(q, kmin, kmax):
+    q = np.asarray(q, dtype=np.float64)
+    qbar = (q / math.sqrt(q.shape[1])).mean(axis=0)
+    return (qbar[None, :] * np.asarray(kmax, dtype=np.float64)).sum(axis=1)
+
+
+def _bounds_first_head_only(q, kmin, kmax):
+    return _orig["router_bounds"](np.asarray(q)[:1], kmin, kmax)
+
+
+def _bounds_unscaled(q, kmin, kmax):
+    q = np.asarray(q, dtype=np.float64)
+    return _orig["router_bounds"](q * math.sqrt(q.shape[1]), kmin, kmax)
+
+
+def _route_ties_to_higher(bounds, top_k):
+    k = O.effective_top_k(top_k, bounds.shape[0])
+    order = sorted(range(bounds.shape[0]), key=lambda b: (-float(bounds[b]), -b))[:k]
+    return np.array(sorted(order), dtype=np.int64)
+
+
+def _route_in_rank_order(bounds, top_k):
+    k = O.effective_top_k(top_k, bounds.shape[0])
+    return np.array(sorted(range(bounds.shape[0]), key=lambda b: (-float(bounds[b]), b))[:k], dtype=np.int64)
+
+
+def _residuals_best_rows(err, n_residual):
+    R = max(0, min(int(n_residual), err.shape[0]))
+    return np.array(sorted(i + 1 for i in sorted(range(err.shape[0]), key=lambda i: (float(err[i]), i))[:R]),
+                    dtype=np.int64)
+
+
+def _residuals_ties_to_higher(err, n_residual):
+    R = max(0, min(int(n_residual), err.shape[0]))
+    return np.array(sorted(i + 1 for i in sorted(range(err.shape[0]), key=lambda i: (-float(err[i]), -i))[:R]),
+                    dtype=np.int64)
+
+
+def _compress(Kb, Vb, rank, n_residual, *, fold_sigma=True, delta_to_mean=False, swap_halves=False,
+              minmax_over_deltas=False, error_on_values=False):
+    """compress_block with one switchable slip."""
+    Kb = np.asarray(Kb, dtype=np.float64)
+    Vb = np.asarray(Vb, dtype=np.float64)
+    d = Kb.shape[1]
+    a_k, a_v = Kb[0].copy(), Vb[0].copy()
+    ref_k, ref_v = (Kb[1:].mean(0), Vb[1:].mean(0)) if delta_to_mean else (a_k, a_v)
+    dK, dV = Kb[1:] - ref_k, Vb[1:] - ref_v
+    U_hat, sigma, Wt = np.linalg.svd(np.concatenate([dK, dV], axis=1), full_matrices=False)
+    r = max(0, min(int(rank), sigma.shape[0]))
+    U = U_hat[:, :r] * sigma[:r] if fold_sigma else U_hat[:, :r].copy()
+    V_K, V_V = Wt[:r, :d].copy(), Wt[:r, d:].copy()
+    if swap_halves:
+        V_K, V_V = V_V, V_K
+    err = np.sqrt((((dV - U @ V_V) if error_on_values else (dK - U @ V_K)) ** 2).sum(axis=1))
+    S = O.select_residuals(err, n_residual)
+    keys = Kb[1:] - a_k if minmax_over_deltas else Kb
+    return O.Block(a_k=a_k, a_v=a_v, U=U, V_K=V_K, V_V=V_V, S=S, K_res=Kb[S].copy(), V_res=Vb[S].copy(),
+                   kmin=keys.min(axis=0), kmax=keys.max(axis=0), sigma=sigma, err=err)
+
+
+def _reconstruct(blk, *, substitute=True, shift=0):
+    d = blk.a_k.shape[0]
+    Kh, Vh = np.empty((BS, d)), np.empty((BS, d))
+    Kh[0], Vh[0] = blk.a_k, blk.a_v
+    Kh[1:] = blk.a_k + blk.U @ blk.V_K
+    Vh[1:] = blk.a_v + blk.U @ blk.V_V
+    if substitute and blk.S.size:
+        Kh[blk.S - shift] = blk.K_res
+        Vh[blk.S - shift] = blk.V_res
+    return Kh, Vh
+
+
+def _softmax_unscaled(q, K, V):
+    q = np.asarray(q, dtype=np.float64)
+    return _orig["softmax_attention"](q * math.sqrt(q.shape[1]), K, V)
+
+
+def _merge_without_rescale(parts):
+    ms = np.stack([p[0] for p in parts])
+    mstar = ms.max(axis=0)
+    w = np.exp(ms - mstar[None, :])
+    lstar = sum(p[1] for p in parts)
+    acc = sum(wj[:, None] * p[2] for wj, p in zip(w, parts))
+    return acc / lstar[:, None], mstar + np.log(lstar)
+
+
+def _merge_lse_without_max(parts):
+    o, lse = _orig["lse_merge"](parts)
+    return o, lse - np.stack([p[0] for p in parts]).max(axis=0)
+
+
+def _partial(q, blk, *, anchor=True, anchor_value=True, z_sign=1.0):
+    """block_partial with one switchable slip."""
+    q = np.asarray(q, dtype=np.float64)
+    qt = q / math.sqrt(q.shape[1])
+    z = qt @ blk.V_K.T
+    base = qt @ blk.a_k
+    lowrank = np.ones(BS, dtype=bool)
+    lowrank[blk.S] = False
+    lr = np.nonzero(lowrank[1:])[0]
+    s_lr = base[:, None] + z_sign * (z @ blk.U[lr].T)
+    s_res = qt @ blk.K_res.T
+    s_anchor = base[:, None] if anchor else np.full_like(base[:, None], -np.inf)
+    m = np.concatenate([s_anchor, s_lr, s_res], axis=1).max(axis=1)
+    p_a, p_lr, p_res = (np.exp(x - m[:, None]) for x in (s_anchor, s_lr, s_res))
+    pa = p_a[:, 0] + p_lr.sum(axis=1)
+    acc = (pa if anchor_value else p_lr.sum(axis=1))[:, None] * blk.a_v[None, :] + (p_lr @ blk.U[lr]) @ blk.V_V \
+        + p_res @ blk.V_res
+    return m, pa + p_res.sum(axis=1), acc
+
+
+def _decode_without_window(q, unit, top_k):
+    return _orig["decode_unit"](q, O.Unit(blocks=unit.blocks, win_K=unit.win_K[:0], win_V=unit.win_V[:0]), top_k)
+
+
+def _append_newest_first(unit, K_new, V_new, window_capacity, rank, n_residual):
+    blocks = list(unit.blocks)
+    win_K = [row for row in np.asarray(unit.win_K, dtype=np.float64)]
+    win_V = [row for row in np.asarray(unit.win_V, dtype=np.float64)]
+    for k, v in zip(np.asarray(K_new, dtype=np.float64), np.asarray(V_new, dtype=np.float64)):
+        if len(win_K) == window_capacity:
+            if len(win_K) < BS:
+                raise ValueError("window capacity below one block")
+            blocks.append(O.compress_block(np.array(win_K[-BS:]), np.array(win_V[-BS:]), rank, n_residual))
+            win_K, win_V = win_K[:-BS], win_V[:-BS]
+        win_K.append(k)
+        win_V.append(v)
+    d = np.asarray(unit.win_K).shape[-1]
+    return O.Unit(blocks=blocks, win_K=np.array(win_K).reshape(-1, d), win_V=np.array(win_V).reshape(-1, d))
+
+
+def _top_k_zero_is_none(top_k, n_blocks):
+    if top_k < 0:
+        raise ValueError("top_k must be >= 0")
+    return min(int(top_k), n_blocks)
+
+
+MUTANTS = {
+    "router bound drops the kmin branch": ("router_bounds", _bounds_without_kmin),
+    "router bound uses one head, not the group mean": ("router_bounds", _bounds_first_head_only),
+    "router bound misses the 1/sqrt(d) scale": ("router_bounds", _bounds_unscaled),
+    "routing ties go to the higher block": ("route", _route_ties_to_higher),
+    "routed indices left in rank order": ("route", _route_in_rank_order),
+    "residuals keep the best rows": ("select_residuals", _residuals_best_rows),
+    "residual ties go to the higher token": ("select_residuals", _residuals_ties_to_higher),
+    "singular values not folded into U": ("compress_block", lambda *a, **k: _compress(*a, **k, fold_sigma=False)),
+    "deltas taken to the block mean": ("compress_block", lambda *a, **k: _compress(*a, **k, delta_to_mean=True)),
+    "V_K and V_V swapped": ("compress_block", lambda *a, **k: _compress(*a, **k, swap_halves=True)),
+    "key box over the deltas": ("compress_block", lambda *a, **k: _compress(*a, **k, minmax_over_deltas=True)),
+    "residual error measured on values": ("compress_block", lambda *a, **k: _compress(*a, **k, error_on_values=True)),
+    "residual rows not substituted": ("reconstruct_block", lambda b: _reconstruct(b, substitute=False)),
+    "residual rows substituted one row early": ("reconstruct_block", lambda b: _reconstruct(b, shift=1)),
+    "softmax misses the 1/sqrt(d) scale": ("softmax_attention", _softmax_unscaled),
+    "merge sums l without rescaling": ("lse_merge", _merge_without_rescale),
+    "merged lse drops the maximum": ("lse_merge", _merge_lse_without_max),
+    "factored scores drop the anchor": ("block_partial", lambda q, b: _partial(q, b, anchor=False)),
+    "factored value drops the anchor's weight": ("block_partial", lambda q, b: _partial(q, b, anchor_value=False)),
+    "factored scores subtract U z": ("block_partial", lambda q, b: _partial(q, b, z_sign=-1.0)),
+    "decode skips the window": ("decode_unit", _decode_without_window),
+    "append compresses the newest tokens": ("append_tokens", _append_newest_first),
+    "top-K 0 routes no block": ("effective_top_k", _top_k_zero_is_none),
+}
+
+
+@pytest.mark.parametrize("slip", sorted(MUTANTS))
+def test_pins_catch_a_planted_slip(slip, monkeypatch):
+    fn_name, mutant = MUTANTS[slip]
+    caught_by, errors = _first_failing_pin(monkeypatch, fn_name, mutant)
+    assert caught_by is not None, f"no pin fails when the oracle's {fn_name} has the slip: {slip}; errors: {errors[:3]}"
+
+
+def test_the_unmutated_oracle_passes_every_pin(monkeypatch):
+    """The harness itself: with the oracle as it is, no pin fails."""
+    assert _first_failing_pin(monkeypatch, "route", _orig["route"]) == (None, [])
