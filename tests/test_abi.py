@@ -155,3 +155,18 @@ def test_append_validates_before_touching_the_device():
     tc = dkv.dkv_layout(1, 6, 1, 128, 1, 300, 8, 4, layout=dkv.DKV_LAYOUT_TC, block_capacity=4, window_capacity=512)
     assert call(tc, 1) == dkv.DKV_ERR_UNSUPPORTED
     assert dkv.dkv_append_workspace_bytes(d) >= 256 + 2 * 256 * 64 * 2
+
+
+def test_decode_launch_counts():
+    """dkv_decode_launches (host only): router, attention and combine; no router grid
+    when nothing is routed or, for the fragment layout, when every block is."""
+    frag = dkv.dkv_layout(2, 12, 2, 128, 30, 512, 32, 40)
+    assert [dkv.dkv_decode_launches(frag, k) for k in (8, 1, 29)] == [3, 3, 3]
+    assert [dkv.dkv_decode_launches(frag, k) for k in (30, 31, 0)] == [2, 2, 2]  # every block routed
+    assert dkv.dkv_decode_launches(frag, -1) == 0                                # invalid top_k
+    empty = dkv.dkv_layout(2, 12, 2, 128, 0, 512, 32, 40)
+    assert [dkv.dkv_decode_launches(empty, k) for k in (0, 4)] == [2, 2]
+    tc = dkv.dkv_layout(2, 12, 2, 128, 30, 512, 32, 40, layout=dkv.DKV_LAYOUT_TC)
+    assert [dkv.dkv_decode_launches(tc, k) for k in (8, 0, 30)] == [3, 3, 3]  # the tc path always routes
+    tc_empty = dkv.dkv_layout(2, 12, 2, 128, 0, 512, 32, 40, layout=dkv.DKV_LAYOUT_TC)
+    assert [dkv.dkv_decode_launches(tc_empty, k) for k in (0, 4)] == [2, 2]
