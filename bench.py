@@ -454,18 +454,22 @@ def main():
         del Kd, Vd
 
     # ---------------- e2e through the C ABI with pinned host buffers
+    # every step copies all its layers' queries in (one pinned copy) and reads all its
+    # layers' outputs back (one copy): the same bytes as one copy per layer, without
+    # putting 2 x n_layers small copies between the decode kernels
     e2e_steps = args.e2e_steps or max(10, min(K_steps, 50))
-    q_host = [q.cpu().pin_memory() for q in qs]
-    q_dev = [torch.empty_like(q) for q in qs]
-    o_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    q_host = torch.stack([q.cpu() for q in qs]).pin_memory()
+    q_dev = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev)
+    o_dev = torch.empty((n_layers,) + tuple(outs[0].shape), dtype=outs[0].dtype, device=dev)
+    o_host = torch.empty(o_dev.shape, dtype=o_dev.dtype, pin_memory=True)
     e_ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
 
     def e2e_step():
+        q_dev.copy_(q_host, non_blocking=True)
         for layer in range(n_layers):
-            q_dev[layer].copy_(q_host[layer], non_blocking=True)
-            dkv.dkv_decode_attend(descs[layer], q_dev[layer], caches[layer], top_k, out=outs[layer], lse=False,
+            dkv.dkv_decode_attend(descs[layer], q_dev[layer], caches[layer], top_k, out=o_dev[layer], lse=False,
                                   routed=False, workspace=e_ws, stream=sh)
-            o_host[layer].copy_(outs[layer], non_blocking=True)
+        o_host.copy_(o_dev, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -546,8 +550,8 @@ def main():
                      "ms_per_step_with_events": ms_ev / K_steps,
                      "clocks": clocks_ev.summary()},
         "e2e": {"value": e2e_value, "unit": "queries/s", "steps": e2e_steps,
-                "h2d_bytes_per_step": sum(q.numel() * 2 for q in qs),
-                "d2h_bytes_per_step": sum(o.numel() * 4 for o in outs)},
+                "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
+                "d2h_bytes_per_step": o_host.numel() * o_host.element_size()},
         "gpu_launches": K_steps * sum(launches_per_call),
         "clocks": clocks.summary(),
         "setup_s": t_setup,
