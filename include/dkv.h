@@ -226,8 +226,10 @@ DKV_API int dkv_append(dkv_desc* d, const void* K_new, const void* V_new, int32_
  *           costs the router a second cluster exchange (about 0.7 us at 64k); without
  *           them the router writes each block to its rank's slot.
  *   workspace / ws_bytes  device scratch of dkv_decode_workspace_bytes(d, top_k);
- *           zero-fill it once before its first use: it holds per-unit arrival
- *           counters that every call leaves at zero again
+ *           zero-fill it once before its first use: its header holds the
+ *           device error word (read by dkv_get_error) and the work-queue
+ *           counters of the tensor-core layout's kernel, which every call
+ *           leaves at zero again
  * Routing: qbar = mean over the group of c*q; block score
  * sum_j max(qbar_j kmax_bj, qbar_j kmin_bj); top-K by (score desc, index asc).
  */
