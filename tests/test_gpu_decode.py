@@ -117,6 +117,7 @@ def _small(d=64, G=6, nb=3, W=100, r=16, R=24, B=1, Hkv=1, seed=7, latent=4):
     dict(), dict(r=0), dict(R=0), dict(R=255), dict(r=8, R=8), dict(r=24, R=40), dict(W=0), dict(nb=0, W=300),
     dict(W=17), dict(W=1), dict(G=1), dict(G=8), dict(G=3), dict(d=128), dict(d=128, r=48, R=128, W=1024),
     dict(d=128, r=104, R=5), dict(d=64, r=128, R=0), dict(B=2, Hkv=2, nb=5),
+    dict(nb=1, W=65536),  # the largest window the layout accepts
 ])
 def test_edge_shapes(kw):
     w = _small(**kw)
