@@ -56,7 +56,9 @@ def _first_failing_pin(monkeypatch, fn_name, mutant):
 
 _orig = {n: getattr(O, n) for n in ("router_bounds", "route", "select_residuals", "compress_block",
                                     "reconstruct_block", "softmax_attention", "lse_merge", "block_partial",
-                                    "decode_unit", "append_tokens", "effective_top_k")}
+                                    "decode_unit", "append_tokens", "effective_top_k", "compress_unit",
+                                    "decode_unit_factored", "_part", "pages_block_bytes", "residual_row_bytes",
+                                    "dense_kv_bytes")}
 
 
 def _bounds_without_kmin(q, kmin, kmax):
@@ -190,6 +192,70 @@ def _append_newest_first(unit, K_new, V_new, window_capacity, rank, n_residual):
     return O.Unit(blocks=blocks, win_K=np.array(win_K).reshape(-1, d), win_V=np.array(win_V).reshape(-1, d))
 
 
+def _window_one_token_late(K, V, n_blocks, rank, n_residual):
+    unit = _orig["compress_unit"](K, V, n_blocks, rank, n_residual)
+    return O.Unit(blocks=unit.blocks, win_K=unit.win_K[1:], win_V=unit.win_V[1:])
+
+
+def _factored_window_chunks_overlap(q, unit, top_k, window_chunk=256):
+    W = unit.win_K.shape[0]
+    if W <= 1:
+        return _orig["decode_unit_factored"](q, unit, top_k, window_chunk)
+    step = max(1, window_chunk - 1)  # consecutive chunks share a token
+    q = np.asarray(q, dtype=np.float64)
+    qt = q / math.sqrt(q.shape[1])
+    nb = len(unit.blocks)
+    bounds = O.router_bounds(q, np.stack([b.kmin for b in unit.blocks]), np.stack([b.kmax for b in unit.blocks])) \
+        if nb else np.zeros(0)
+    idx = O.route(bounds, top_k) if nb else np.zeros(0, dtype=np.int64)
+    parts = [O.block_partial(q, unit.blocks[b]) for b in idx]
+    for t0 in range(0, W, step):
+        parts.append(O._part(qt @ unit.win_K[t0:t0 + window_chunk].T, unit.win_V[t0:t0 + window_chunk]))
+    o, lse = O.lse_merge(parts)
+    return {"o": o, "lse": lse, "idx": idx, "bounds": bounds}
+
+
+def _part_with_mean_shift(s, V):
+    m = s.mean(axis=1)  # any shift cancels in o, but l and m must describe the same exponentials
+    e = np.exp(s - s.max(axis=1)[:, None])
+    return m, e.sum(axis=1), e @ V
+
+
+def _residual_positions_zero_based(err, n_residual):
+    return _orig["select_residuals"](err, n_residual) - 1
+
+
+def _bytes_u_with_256_rows(d, u_rank, R, elem_bytes=4, basis_bytes=None, meta_bytes=8):
+    acc = _orig["pages_block_bytes"](d, u_rank, R, elem_bytes, basis_bytes, meta_bytes)
+    extra = u_rank * elem_bytes
+    return dict(acc, U=acc["U"] + extra, core=acc["core"] + extra, block=acc["block"] + extra,
+                ratio=acc["dense"] / (acc["block"] + extra))
+
+
+def _residual_row_key_only(d, elem_bytes=2):
+    return d * elem_bytes
+
+
+def _dense_bytes_one_layer(context, d, n_layers, n_kv_heads, elem_bytes=2):
+    return _orig["dense_kv_bytes"](context, d, 1, n_kv_heads, elem_bytes)
+
+
+def _top_k_all_but_one(top_k, n_blocks):
+    k = _orig["effective_top_k"](top_k, n_blocks)
+    return max(0, n_blocks - 1) if k == n_blocks else k
+
+
+def _partial_residuals_offset_by_anchor(q, blk):
+    m, l, acc = _orig["block_partial"](q, blk)
+    if blk.S.size == 0:
+        return m, l, acc
+    q = np.asarray(q, dtype=np.float64)
+    qt = q / math.sqrt(q.shape[1])
+    # score the exact rows as if they were deltas: q.(a_k + k_j)
+    shifted = O.Block(**{**blk.__dict__, "K_res": blk.K_res + blk.a_k[None, :]})
+    return _orig["block_partial"](q, shifted)
+
+
 def _top_k_zero_is_none(top_k, n_blocks):
     if top_k < 0:
         raise ValueError("top_k must be >= 0")
@@ -220,6 +286,15 @@ MUTANTS = {
     "decode skips the window": ("decode_unit", _decode_without_window),
     "append compresses the newest tokens": ("append_tokens", _append_newest_first),
     "top-K 0 routes no block": ("effective_top_k", _top_k_zero_is_none),
+    "top-K >= NB routes all but one block": ("effective_top_k", _top_k_all_but_one),
+    "window starts one token late": ("compress_unit", _window_one_token_late),
+    "factored window chunks overlap by a token": ("decode_unit_factored", _factored_window_chunks_overlap),
+    "partial's maximum is not its shift": ("_part", _part_with_mean_shift),
+    "residual positions zero-based": ("select_residuals", _residual_positions_zero_based),
+    "factored residual scores offset by the anchor": ("block_partial", _partial_residuals_offset_by_anchor),
+    "page table: U with 256 rows": ("pages_block_bytes", _bytes_u_with_256_rows),
+    "residual row counts the key only": ("residual_row_bytes", _residual_row_key_only),
+    "dense bytes of one layer": ("dense_kv_bytes", _dense_bytes_one_layer),
 }
 
 

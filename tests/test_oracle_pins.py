@@ -6,7 +6,7 @@ closed form, an invariant, brute force on tiny inputs, or the numbers the
 pages print (tests/golden).  A plausible slip in the oracle (dropped anchor,
 wrong sign of a delta, transposed basis, residual rows not substituted,
 wrong tie order, a missing LSE rescale) fails at least one of them;
-tests/test_oracle_mutants.py plants 23 such slips and checks exactly that.
+tests/test_oracle_mutants.py plants 32 such slips and checks exactly that.
 """
 import itertools
 import json
