@@ -64,3 +64,27 @@ def test_small_workloads_rotate_over_enough_cache_replicas():
         per = bench.call_bytes(w, 0, w.top_k)
         n = bench.cache_replicas(per, l2)
         assert n * per >= 4 * l2 > (n - 1) * per
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the fp64 oracle on the host cores, no GPU) prints one
+    JSON line with the keys of the benchmark contract."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--config", "8k",
+           "--steps", "2", "--warmup", "3", "--cpu-seconds", "1"]
+    res = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["unit"] == "queries/s" and d["value"] > 0
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["higher_is_better"] is True
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
