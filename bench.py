@@ -273,7 +273,12 @@ def main():
     ap.add_argument("--no-alt-layout", action="store_true",
                     help="skip timing the other cache layout's decode kernel over the same step")
     ap.add_argument("--no-dense-reference", action="store_true",
-                    help="skip timing the dense fp16 decode kernel over one layer of uncompressed K, V")
+                    help="skip timing the dense fp16 decode kernel over the 16k sweep's uncompressed K, V")
+    ap.add_argument("--reps", type=int, default=10, help="graph replays timed (the median is reported; >= 10)")
+    ap.add_argument("--configs", default="32k,8k,sweep16k",
+                    help="further workloads reported under `configs` (one layer each, several cache replicas)")
+    ap.add_argument("--config-steps", type=int, default=20, help="steps per graph for the further workloads")
+    ap.add_argument("--no-configs", action="store_true", help="skip the further workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -312,7 +317,7 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
-    import numpy as np
+    import numpy as np  # noqa: F401
     import torch
 
     from compressed_kv_cache_dkv_gb300 import dkv
@@ -323,166 +328,181 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     dkv.lib()
+    reps = max(10, args.reps)
 
-    # ---------------- setup: compress every layer's K, V into its packed cache (untimed)
     layout_ids = {"fragment": dkv.DKV_LAYOUT_FRAGMENT, "tc": dkv.DKV_LAYOUT_TC}
-    # A workload whose calls read less than a few L2s (8k, 32k: one layer, 1.4 and 9.0 MB read
-    # per call) rotates a step's calls over cache replicas, so that the bytes one step reads
-    # span at least 4x the L2 and every call reads its cache from HBM.  Each replica is a
-    # separate copy of the cache at its own address.
-    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    n_rep = cache_replicas(sum(call_bytes(w, l, top_k) for l in layer_ids), l2_bytes)
-    if n_rep > 1:
-        layer_ids = layer_ids * n_rep
-        n_layers = len(layer_ids)
-        queries_per_step = w.batch * w.n_q_heads * n_layers
-        wl_name += f"; each step {n_rep} calls over {n_rep} cache replicas"
     kernel_names = {"fragment": "attend_kernel (mma.sync, block + window attention)",
                     "tc": "attend_tc_kernel (tcgen05 + TMEM, block + window attention) + combine_kernel"}
-
-    def build_caches(layout: str):
-        descs_, caches_ = [], []
-        for layer in layer_ids:
-            descs_.append(dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window,
-                                         w.rank(layer), w.n_residual, layout=layout_ids[layout]))
-        for i, layer in enumerate(layer_ids):
-            K, V = synth.layer_kv_torch(w, layer, dev, replica=rank)
-            caches_.append(dkv.dkv_compress_layout(descs_[i], K, V, workspace=ws))
-            del K, V
-        torch.cuda.synchronize()
-        st_, word_ = dkv.dkv_get_error(ws)
-        if st_ != dkv.DKV_OK:
-            raise RuntimeError(f"compression raised device error word {word_:#x}")
-        return descs_, caches_
-
-    t_setup = time.perf_counter()
-    ws_bytes = 0
-    for layer in layer_ids:
-        for lay in layout_ids.values():
-            d = dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window, w.rank(layer),
-                               w.n_residual, layout=lay)
-            ws_bytes = max(ws_bytes, dkv.dkv_decode_workspace_bytes(d, top_k))
-    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-    descs, caches = build_caches(args.layout)
-    qs, outs, lses = [], [], []
-    for layer in layer_ids:
-        qs.append(torch.from_numpy(synth.queries(w, layer)).to(dev))
-        outs.append(torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.float32, device=dev))
-        lses.append(torch.empty(w.batch, w.n_q_heads, dtype=torch.float32, device=dev))
-    t_setup = time.perf_counter() - t_setup
-    cache_gb = sum(c.numel() for c in caches) / 1e9
-    log(f"[bench] rank {rank}: setup {t_setup:.1f} s, packed caches {cache_gb:.2f} GB over {n_layers} layers")
-
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
     ext = ExtEvents()
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        peak = float(json.load(open(peaks_path))["hbm_gbs"])
+        peak_src = "measured"
+    else:
+        peak, peak_src = FALLBACK_HBM_GBS, "fallback"
 
-    def measure(descs_, caches_):
-        """Warm up, capture K steps into two CUDA graphs, replay each once untimed, then time
-        one replay of each.  The plain graph is the timed step: one dkv_decode_attend per
-        layer.  The other runs the same work as its stage calls, with events around the
-        attention grid alone, which gives that kernel's duration; its events split the
-        programmatic launches apart, so that graph runs a little slower."""
-        def step(events=None):
-            for layer in range(n_layers):
-                if events is None:
-                    dkv.dkv_decode_attend(descs_[layer], qs[layer], caches_[layer], top_k, out=outs[layer],
-                                          lse=lses[layer], routed=False, workspace=ws, stream=sh)
-                    continue
-                dkv.dkv_decode_route(descs_[layer], qs[layer], caches_[layer], top_k, ws, stream=sh)
-                ext.record(events[layer][0], sh)
-                dkv.dkv_decode_blocks(descs_[layer], qs[layer], caches_[layer], top_k, ws, stream=sh)
-                ext.record(events[layer][1], sh)
-                dkv.dkv_decode_combine(descs_[layer], top_k, outs[layer], ws, lse=lses[layer], stream=sh)
-
-        with torch.cuda.stream(stream):
-            for _ in range(args.warmup):
-                step()
-        stream.synchronize()
-        ev = [[(ext.new(), ext.new()) for _ in range(n_layers)] for _ in range(K_steps)]
-        graph, graph_ev = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            for k in range(K_steps):
-                step()
-        with torch.cuda.graph(graph_ev, stream=stream):
-            for k in range(K_steps):
-                step(ev[k])
-        with torch.cuda.stream(stream):  # a graph replays on the current stream
-            graph.replay()  # untimed replays (warm)
-            graph_ev.replay()
-        stream.synchronize()
-        ms_, clocks_ = timed(graph)
-        ms_ev_, clocks_ev_ = timed(graph_ev)
-        attend_ms_ = [ext.elapsed_ms(ev[k][l][0], ev[k][l][1]) for k in range(K_steps) for l in range(n_layers)]
-        st_, word_ = dkv.dkv_get_error(ws, stream=sh)
-        if st_ != dkv.DKV_OK:
-            raise RuntimeError(f"decode raised device error word {word_:#x}")
-        return ms_, clocks_, ms_ev_, clocks_ev_, attend_ms_
-
-    # ---------------- timed regions
-    def timed(g):
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    def timed(g, n_rep):
+        """Replay graph `g` n_rep times, each bracketed by events on its stream (after a
+        barrier and a device synchronisation on both sides); returns the per-replay
+        times (ms) and the clocks sampled during them."""
+        times = []
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
         with ClockSampler(local) as clk, torch.cuda.stream(stream):
-            t0.record(stream)
-            g.replay()
-            t1.record(stream)
-            stream.synchronize()
+            for _ in range(n_rep):
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record(stream)
+                g.replay()
+                t1.record(stream)
+                stream.synchronize()
+                times.append(t0.elapsed_time(t1))
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-        return t0.elapsed_time(t1), clk
+        return times, clk
 
-    K_steps = args.steps
-    launches_per_call = [dkv.dkv_decode_launches(d_, top_k) for d_ in descs]
-    ms, clocks, ms_ev, clocks_ev, attend_ms = measure(descs, caches)
+    class Setup:
+        """Packed caches, queries and outputs of one workload at one top-K; small
+        workloads rotate a step's calls over cache replicas so that the bytes one step
+        reads span at least 4x the L2 and every call reads its cache from HBM."""
 
-    # ---------------- dense fp16 reference: one layer of uncompressed K, V (same recipe, on the device)
-    dense = None
-    if not args.no_dense_reference:
-        Kd, Vd = synth.layer_kv_torch(w, layer_ids[0], dev, replica=rank)
-        od = torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.float32, device=dev)
-        ld = torch.empty(w.batch, w.n_q_heads, dtype=torch.float32, device=dev)
-        wsd = torch.zeros(max(256, dkv.dkv_dense_workspace_bytes(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim,
-                                                                  w.context)), dtype=torch.uint8, device=dev)
-        n_dense = max(10, min(K_steps, 50))
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                dkv.dkv_dense_decode(qs[0], Kd, Vd, out=od, lse=ld, workspace=wsd, stream=sh)
-            d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            d0.record(stream)
-            for _ in range(n_dense):  # each call reads K and V once (far larger than L2)
-                dkv.dkv_dense_decode(qs[0], Kd, Vd, out=od, lse=ld, workspace=wsd, stream=sh)
-            d1.record(stream)
+        def __init__(self, w, layer_ids, top_k, layout, ws_bytes=None, min_call_bytes=None):
+            self.w, self.top_k, self.layout = w, top_k, layout
+            base = sum(call_bytes(w, l, top_k) for l in layer_ids)
+            self.n_rep = cache_replicas(min_call_bytes or base, l2_bytes)
+            self.layer_ids = layer_ids * self.n_rep
+            self.n_layers = len(self.layer_ids)
+            self.descs = [dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window,
+                                         w.rank(l), w.n_residual, layout=layout_ids[layout]) for l in self.layer_ids]
+            need = max(dkv.dkv_decode_workspace_bytes(d, k) for d in self.descs for k in {top_k, 0})
+            self.ws = torch.zeros(max(need, ws_bytes or 0), dtype=torch.uint8, device=dev)
+            self.caches = []
+            for i, layer in enumerate(self.layer_ids):
+                K, V = synth.layer_kv_torch(w, layer, dev, replica=rank)
+                self.caches.append(dkv.dkv_compress_layout(self.descs[i], K, V, workspace=self.ws))
+                del K, V
+            torch.cuda.synchronize()
+            st_, word_ = dkv.dkv_get_error(self.ws)
+            if st_ != dkv.DKV_OK:
+                raise RuntimeError(f"compression raised device error word {word_:#x}")
+            self.qs = [torch.from_numpy(synth.queries(w, l)).to(dev) for l in self.layer_ids]
+            self.outs = [torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.float32, device=dev)
+                         for _ in self.layer_ids]
+            self.lses = [torch.empty(w.batch, w.n_q_heads, dtype=torch.float32, device=dev) for _ in self.layer_ids]
+            self.cache_gb = sum(c.numel() for c in self.caches) / 1e9
+
+        def measure(self, top_k, steps, warmup, n_rep, stage_timing=True, latency=True):
+            """Warm up, capture `steps` steps (one call per cache of the set) into a CUDA graph,
+            time n_rep replays of it (median taken); with stage_timing also a second graph of
+            the same steps run as the stage calls with events around every attention launch
+            (its events split the programmatic launches, so that graph runs a little slower);
+            with latency one call alone, captured in its own graph and replayed n_rep times."""
+            n = self.n_layers
+
+            def call(i, events=None):
+                if events is None:
+                    dkv.dkv_decode_attend(self.descs[i], self.qs[i], self.caches[i], top_k, out=self.outs[i],
+                                          lse=self.lses[i], routed=False, workspace=self.ws, stream=sh)
+                    return
+                dkv.dkv_decode_route(self.descs[i], self.qs[i], self.caches[i], top_k, self.ws, stream=sh)
+                ext.record(events[0], sh)
+                dkv.dkv_decode_blocks(self.descs[i], self.qs[i], self.caches[i], top_k, self.ws, stream=sh)
+                ext.record(events[1], sh)
+                dkv.dkv_decode_combine(self.descs[i], top_k, self.outs[i], self.ws, lse=self.lses[i], stream=sh)
+
+            with torch.cuda.stream(stream):
+                for _ in range(warmup):
+                    for i in range(n):
+                        call(i)
             stream.synchronize()
-        dense_ms = d0.elapsed_time(d1) / n_dense
-        dense_bytes = (2 * Kd.numel() * 2 + w.batch * w.n_q_heads * w.head_dim * (2 + 4))
-        st, word = dkv.dkv_get_error(wsd, stream=sh)
-        if st != dkv.DKV_OK:
-            raise RuntimeError(f"dense decode raised device error word {word:#x}")
-        dense = {"kernel": "dense_kernel + combine (dkv_dense_decode)", "calls": n_dense,
-                 "ms_per_layer": dense_ms, "queries_per_s": w.batch * w.n_q_heads / (dense_ms / 1e3),
-                 "bytes_per_layer": dense_bytes, "gbs": dense_bytes / (dense_ms / 1e3) / 1e9,
-                 "context_tokens": w.context}
-        del Kd, Vd
+            res = {}
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(steps):
+                    for i in range(n):
+                        call(i)
+            with torch.cuda.stream(stream):
+                g.replay()
+            stream.synchronize()
+            times, clk = timed(g, n_rep)
+            res["ms_replays"] = times
+            res["ms"] = statistics.median(times)
+            res["clocks"] = clk.summary()
+            if stage_timing:
+                ev = [[(ext.new(), ext.new()) for _ in range(n)] for _ in range(steps)]
+                g2 = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g2, stream=stream):
+                    for k in range(steps):
+                        for i in range(n):
+                            call(i, ev[k][i])
+                with torch.cuda.stream(stream):
+                    g2.replay()
+                stream.synchronize()
+                t2, clk2 = timed(g2, 1)
+                res["ms_ev"] = t2[0]
+                res["attend_ms"] = [ext.elapsed_ms(ev[k][i][0], ev[k][i][1]) for k in range(steps) for i in range(n)]
+                res["clocks_ev"] = clk2.summary()
+                del g2
+            if latency:
+                g1 = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g1, stream=stream):
+                    call(0)
+                with torch.cuda.stream(stream):
+                    g1.replay()
+                stream.synchronize()
+                t1, _ = timed(g1, max(20, n_rep))
+                res["latency_us"] = 1e3 * statistics.median(t1)
+                del g1
+            del g
+            st_, word_ = dkv.dkv_get_error(self.ws, stream=sh)
+            if st_ != dkv.DKV_OK:
+                raise RuntimeError(f"decode raised device error word {word_:#x}")
+            return res
+
+        def free(self):
+            del self.caches, self.ws, self.qs, self.outs, self.lses
+            torch.cuda.empty_cache()
+
+    # ---------------- headline workload (untimed setup: compress every layer's K, V)
+    w = synth.WORKLOADS[args.config]
+    top_k = w.top_k if args.top_k is None else args.top_k
+    n_layers0 = w.n_layers if args.layers is None else min(args.layers, w.n_layers - args.layer_offset)
+    base_ids = [args.layer_offset + i for i in range(n_layers0)] if args.layers is not None else list(range(n_layers0))
+    wl_name = (f"{w.name}: batch {w.batch}, {n_layers0} layer(s) of {w.n_q_heads}q/{w.n_kv_heads}kv heads x d{w.head_dim}, "
+               f"{w.n_blocks} blocks of 256 + {w.window}-token window, r {sorted(set(w.ranks[i] for i in base_ids))}, "
+               f"R {w.n_residual}, top-K {top_k}")
+    t_setup = time.perf_counter()
+    S = Setup(w, base_ids, top_k, args.layout)
+    t_setup = time.perf_counter() - t_setup
+    if S.n_rep > 1:
+        wl_name += f"; each step {S.n_rep} calls over {S.n_rep} cache replicas"
+    n_layers = S.n_layers
+    queries_per_step = w.batch * w.n_q_heads * n_layers
+    log(f"[bench] rank {rank}: setup {t_setup:.1f} s, packed caches {S.cache_gb:.2f} GB over {n_layers} layers")
+    K_steps = args.steps
+    launches_per_call = [dkv.dkv_decode_launches(d_, top_k) for d_ in S.descs]
+    R = S.measure(top_k, K_steps, args.warmup, reps)
+    ms, ms_ev, attend_ms = R["ms"], R["ms_ev"], R["attend_ms"]
 
     # ---------------- e2e through the C ABI with pinned host buffers
     # every step copies all its layers' queries in (one pinned copy) and reads all its
     # layers' outputs back (one copy): the same bytes as one copy per layer, without
     # putting 2 x n_layers small copies between the decode kernels
     e2e_steps = args.e2e_steps or max(10, min(K_steps, 50))
-    q_host = torch.stack([q.cpu() for q in qs]).pin_memory()
+    q_host = torch.stack([q.cpu() for q in S.qs]).pin_memory()
     q_dev = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev)
-    o_dev = torch.empty((n_layers,) + tuple(outs[0].shape), dtype=outs[0].dtype, device=dev)
+    o_dev = torch.empty((n_layers,) + tuple(S.outs[0].shape), dtype=S.outs[0].dtype, device=dev)
     o_host = torch.empty(o_dev.shape, dtype=o_dev.dtype, pin_memory=True)
-    e_ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    e_ws = torch.zeros(S.ws.numel(), dtype=torch.uint8, device=dev)
 
     def e2e_step():
         q_dev.copy_(q_host, non_blocking=True)
         for layer in range(n_layers):
-            dkv.dkv_decode_attend(descs[layer], q_dev[layer], caches[layer], top_k, out=o_dev[layer], lse=False,
+            dkv.dkv_decode_attend(S.descs[layer], q_dev[layer], S.caches[layer], top_k, out=o_dev[layer], lse=False,
                                   routed=False, workspace=e_ws, stream=sh)
         o_host.copy_(o_dev, non_blocking=True)
 
@@ -499,20 +519,87 @@ def main():
         e1.record(stream)
         stream.synchronize()
     e2e_ms = e0.elapsed_time(e1)
+    step_bytes = sum(call_bytes(w, l, top_k) for l in S.layer_ids)
+    att_bytes_step = sum(attend_bytes(w, l, top_k) for l in S.layer_ids)
+    S.free()
+    del q_dev, o_dev, e_ws
 
     # ---------------- the other cache layout's decode kernel over the same step (same inputs)
     alt = None
     if not args.no_alt_layout:
         alt_layout = "tc" if args.layout == "fragment" else "fragment"
         if all(dkv.dkv_layout_supported(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window,
-                                        w.rank(l), w.n_residual, layout_ids[alt_layout]) for l in layer_ids):
-            del caches
-            torch.cuda.empty_cache()
-            a_descs, a_caches = build_caches(alt_layout)
-            a_ms, a_clocks, a_ms_ev, _, a_attend_ms = measure(a_descs, a_caches)
-            del a_caches
-            alt = {"layout": alt_layout, "kernel": kernel_names[alt_layout], "ms": a_ms, "ms_ev": a_ms_ev,
-                   "attend_ms_mean": statistics.fmean(a_attend_ms), "clocks": a_clocks.summary()}
+                                        w.rank(l), w.n_residual, layout_ids[alt_layout]) for l in base_ids):
+            A = Setup(w, base_ids, top_k, alt_layout)
+            AR = A.measure(top_k, K_steps, args.warmup, reps, latency=False)
+            A.free()
+            alt = {"layout": alt_layout, "kernel": kernel_names[alt_layout], "ms": AR["ms"], "ms_ev": AR["ms_ev"],
+                   "attend_ms_mean": statistics.fmean(AR["attend_ms"]), "clocks": AR["clocks"]}
+
+    # ---------------- the other workloads: 32k, 8k and the 16k top-K sweep beside the dense fp16 kernel
+    configs = {}
+    if not args.no_configs and args.layers is None:
+        def config_entry(wc, k, R_, S_, steps_c):
+            cb = sum(call_bytes(wc, l, k) for l in S_.layer_ids)
+            ab = sum(attend_bytes(wc, l, k) for l in S_.layer_ids)
+            ms_call = R_["ms"] / (steps_c * S_.n_layers)
+            att_us = 1e3 * statistics.fmean(R_["attend_ms"])
+            return {"workload": (f"{wc.name}: batch {wc.batch}, {wc.n_q_heads}q/{wc.n_kv_heads}kv x d{wc.head_dim}, "
+                                 f"{wc.n_blocks} blocks + {wc.window}-token window, r {wc.rank(0)}, R {wc.n_residual}, "
+                                 f"top-K {k}; {S_.n_rep} cache replicas"),
+                    "queries_per_s": wc.batch * wc.n_q_heads / (ms_call / 1e3),
+                    "us_per_call": 1e3 * ms_call, "bytes_per_call": cb / S_.n_layers,
+                    "gbs": cb / (R_["ms"] / steps_c / 1e3) / 1e9,
+                    "frac_call": cb / (R_["ms"] / steps_c / 1e3) / 1e9 / peak,
+                    "steps_per_replay": steps_c,
+                    "attend_us_mean": att_us, "attend_bytes_per_launch": ab / S_.n_layers,
+                    "attend_frac": (ab / S_.n_layers) / (att_us / 1e6) / 1e9 / peak,
+                    "latency_us": R_["latency_us"],
+                    "replays": len(R_["ms_replays"]), "clocks": R_["clocks"]}
+        for name in args.configs.split(","):
+            wc = synth.WORKLOADS[name]
+            ks = [wc.top_k] if name != "sweep16k" else [4, 16, wc.n_blocks]
+            min_b = min(call_bytes(wc, 0, k) for k in ks)
+            Sc = Setup(wc, [0], ks[0], "fragment", min_call_bytes=min_b)
+            steps_c = max(1, min(args.config_steps, 1200 // Sc.n_layers))  # about 1200 calls per graph at most
+            for k in ks:
+                Rc = Sc.measure(k, steps_c, args.warmup, reps)
+                configs[f"{name}_top{k}" if len(ks) > 1 else name] = config_entry(wc, k, Rc, Sc, steps_c)
+            Sc.free()
+            if name == "sweep16k" and not args.no_dense_reference:
+                # dense fp16 decode over the uncompressed K, V of the same seed (config 5's reference)
+                Kd, Vd = synth.layer_kv_torch(wc, 0, dev, replica=rank)
+                od = torch.empty(wc.batch, wc.n_q_heads, wc.head_dim, dtype=torch.float32, device=dev)
+                ld = torch.empty(wc.batch, wc.n_q_heads, dtype=torch.float32, device=dev)
+                wsd = torch.zeros(max(256, dkv.dkv_dense_workspace_bytes(wc.batch, wc.n_q_heads, wc.n_kv_heads,
+                                                                          wc.head_dim, wc.context)),
+                                  dtype=torch.uint8, device=dev)
+                qd = torch.from_numpy(synth.queries(wc, 0)).to(dev)
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        dkv.dkv_dense_decode(qd, Kd, Vd, out=od, lse=ld, workspace=wsd, stream=sh)
+                gd = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gd, stream=stream):  # each call reads K and V once (far larger than L2)
+                    dkv.dkv_dense_decode(qd, Kd, Vd, out=od, lse=ld, workspace=wsd, stream=sh)
+                with torch.cuda.stream(stream):
+                    gd.replay()
+                stream.synchronize()
+                td, clkd = timed(gd, reps)
+                dense_ms = statistics.median(td)
+                dense_bytes = 2 * Kd.numel() * 2 + wc.batch * wc.n_q_heads * wc.head_dim * (2 + 4)
+                st, word = dkv.dkv_get_error(wsd, stream=sh)
+                if st != dkv.DKV_OK:
+                    raise RuntimeError(f"dense decode raised device error word {word:#x}")
+                configs["sweep16k_dense_fp16"] = {
+                    "workload": f"dense fp16 decode over the uncompressed K, V of {wc.name} (same seed), "
+                                f"{wc.context} tokens per unit",
+                    "kernel": "dense_kernel + combine (dkv_dense_decode)",
+                    "queries_per_s": wc.batch * wc.n_q_heads / (dense_ms / 1e3), "us_per_call": 1e3 * dense_ms,
+                    "bytes_per_call": dense_bytes, "gbs": dense_bytes / (dense_ms / 1e3) / 1e9,
+                    "frac_call": dense_bytes / (dense_ms / 1e3) / 1e9 / peak, "replays": len(td),
+                    "clocks": clkd.summary()}
+                del Kd, Vd, gd
+                torch.cuda.empty_cache()
 
     # ---------------- reduce over ranks (max time)
     if world > 1:
@@ -524,17 +611,8 @@ def main():
     value = whole_job_rate(world, queries_per_step, K_steps, ms)
     e2e_value = whole_job_rate(world, queries_per_step, e2e_steps, e2e_ms)
 
-    step_bytes = sum(call_bytes(w, l, top_k) for l in layer_ids)
-    # the attention grid reads the routed blocks, the window and the queries
-    att_bytes_step = sum(attend_bytes(w, l, top_k) for l in layer_ids)
     att_ms_mean = statistics.fmean(attend_ms)
     achieved_gbs = (att_bytes_step / n_layers) / (att_ms_mean / 1e3) / 1e9
-    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(peaks_path):
-        peak = float(json.load(open(peaks_path))["hbm_gbs"])
-        peak_src = "measured"
-    else:
-        peak, peak_src = FALLBACK_HBM_GBS, "fallback"
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "attend_traffic.json")
     if os.path.exists(tpath):
@@ -549,13 +627,16 @@ def main():
         "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": K_steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": wl_name, "cache_layout": args.layout, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"inputs larger than L2: {cache_gb:.1f} GB of packed caches per step cycle, each "
-                         f"{'cache replica' if n_rep > 1 else 'layer'} read once per step", "graph": "K steps captured in one CUDA graph"},
+        "config": {"workload": wl_name, "cache_layout": args.layout,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: {S.cache_gb:.1f} GB of packed caches per step cycle, each "
+                         f"{'cache replica' if S.n_rep > 1 else 'layer'} read once per step",
+                   "graph": f"K steps captured in one CUDA graph; value from the median of {reps} replays"},
         "hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
         "hbm_frac_of_measured": step_bytes / (ms_step / 1e3) / 1e9 / peak,
         "hbm_frac_of_nominal_8tbs": step_bytes / (ms_step / 1e3) / 1e9 / 8000.0,
         "bytes_per_step": step_bytes,
+        "single_call_latency_us": R["latency_us"],
         "roofline": {"bound": "hbm", "kernel": kernel_names[args.layout], "achieved": achieved_gbs,
                      "peak": peak, "unit": "GB/s", "frac": achieved_gbs / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
@@ -563,16 +644,15 @@ def main():
                      "timed_in": "a second replay of the same K steps as stage calls, with events around "
                                  "every attention launch", "launches_per_call": max(launches_per_call),
                      "ms_per_step_with_events": ms_ev / K_steps,
-                     "clocks": clocks_ev.summary()},
+                     "clocks": R["clocks_ev"]},
         "e2e": {"value": e2e_value, "unit": "queries/s", "steps": e2e_steps,
                 "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
                 "d2h_bytes_per_step": o_host.numel() * o_host.element_size()},
         "gpu_launches": K_steps * sum(launches_per_call),
-        "clocks": clocks.summary(),
+        "clocks": R["clocks"],
         "setup_s": t_setup,
-        "dense_reference": None if dense is None else dict(
-            dense, frac=dense["gbs"] / peak,
-            compressed_speedup=dense["ms_per_layer"] / (ms_step / n_layers)),
+        "replays_ms": [round(x, 4) for x in R["ms_replays"]],
+        "configs": configs or None,
         "other_layout": None if alt is None else {
             "layout": alt["layout"], "kernel": alt["kernel"], "ms_per_step": alt["ms"] / K_steps,
             "value": whole_job_rate(world, queries_per_step, K_steps, alt["ms"]),

@@ -38,6 +38,7 @@
 #include <float.h>
 #include <math.h>
 
+#include <atomic>
 #include <vector>
 
 #include "dkv_internal.cuh"
@@ -52,7 +53,6 @@ constexpr int kNBar = 16;                     // chunk barrier pairs: chunks in 
 constexpr int kStageTok = 16 * kConsumers;    // exact tokens per stage (one 16-token group per warp)
 constexpr int kMaxRanges = 128;               // ranges per unit
 constexpr int kCtasPerSm = 2;                 // resident CTAs per SM (registers and shared memory)
-constexpr int kTargetCtas = kCtasPerSm * 152; // one wave on GB300's 152 SMs
 // 2 x (108 + 1 reserved) KB leaves an SM room for one router CTA of the same
 // call (programmatic launch lets the two grids overlap)
 constexpr size_t kSmemPerCta = 108 * 1024;
@@ -733,14 +733,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
   }
 }
 
-// ranges per unit: fill whole waves of kTargetCtas CTAs, preferring one wave
+// ranges per unit: fill whole waves of kCtasPerSm CTAs per SM, preferring one wave
 int ranges_per_unit(int units) {
+  const long target = (long)kCtasPerSm * sm_count();
   int best = 1;
   double best_score = -1.0;
   for (int n = 1; n <= kMaxRanges; ++n) {
     const long ctas = (long)units * n;
-    const long waves = (ctas + kTargetCtas - 1) / kTargetCtas;
-    const double score = (double)ctas / (double)(waves * kTargetCtas) - 0.06 * (double)(waves - 1);
+    const long waves = (ctas + target - 1) / target;
+    const double score = (double)ctas / (double)(waves * target) - 0.06 * (double)(waves - 1);
     if (score > best_score + 1e-9) { best_score = score; best = n; }
   }
   return best;
@@ -817,12 +818,8 @@ void fill_ranges(const Layout& L, int K_eff, int nres, int n_wst, int n_r, int (
 
 template <int D, int R8S>
 cudaError_t launch_one(const AttendArgs& a, int grid, size_t smem, cudaStream_t s) {
-  static size_t configured = 0;  // largest dynamic shared memory size enabled so far
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(attend_kernel<D, R8S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attend_kernel<D, R8S>), smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -886,16 +883,18 @@ AttendArgs make_args(const Layout& L, const DecodePlan& P, int n_q_heads, int n_
 
 }  // namespace
 
+// Multiprocessors of the current device (cached per device; a host without a
+// usable device plans for 148).
 int sm_count() {
-  static int n[64] = {0};
+  static std::atomic<int> n[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!n[dev]) {
-    int v = 0;
+  int v = n[dev].load(std::memory_order_relaxed);
+  if (v <= 0) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
-    n[dev] = v;
+    n[dev].store(v, std::memory_order_relaxed);
   }
-  return n[dev];
+  return v;
 }
 
 DecodePlan plan_decode(const Layout& L, int n_q_heads, int n_kv_heads, int top_k) {

@@ -751,11 +751,9 @@ cudaError_t launch_attend_tc(const Layout& L, const DecodePlan& P, int n_q_heads
   a.err = reinterpret_cast<uint32_t*>(ws);
   a.sched = reinterpret_cast<uint32_t*>(ws + P.off_sched);
   if (a.total == 0) return cudaSuccess;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+  {
+    const cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attend_tc_kernel), kTcSmem);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   int grid = kTcCtasPerSm * sm_count();
   grid = grid < a.total ? grid : a.total;

@@ -544,7 +544,7 @@ CPlan plan(const Layout& L) {
 
 template <int D>
 cudaError_t launch_t(const CArgs& a, uint32_t smem, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(compress_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(compress_kernel<D>), smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.nblk + (a.with_window ? 1 : 0), a.L.units);
   if (grid.x == 0) return cudaSuccess;

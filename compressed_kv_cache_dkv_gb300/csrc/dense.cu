@@ -24,7 +24,7 @@ namespace {
 constexpr int kDenseThreads = 128;
 constexpr int kDenseTile = 64;     // tokens per pipeline stage (16 per warp)
 constexpr int kDenseStages = 3;
-constexpr int kDenseItems = 8 * 152;  // work items aimed at: about four resident waves of two CTAs per SM
+constexpr int kDenseWaves = 4;  // work items aimed at: about four resident waves of two CTAs per SM
 
 struct DenseArgs {
   int Hq, Hkv, G, T, chunk, nchunk;
@@ -233,7 +233,8 @@ DensePlan plan_dense(int batch, int n_kv_heads, int d, int T) {
   DensePlan P;
   const int units = batch * n_kv_heads;
   const int max_chunks = (T + kDenseTile - 1) / kDenseTile;
-  int n = (kDenseItems + units - 1) / units;
+  const int items = kDenseWaves * 2 * sm_count();
+  int n = (items + units - 1) / units;
   n = n < 1 ? 1 : (n > max_chunks ? max_chunks : n);
   P.chunk = ((T + n - 1) / n + kDenseTile - 1) / kDenseTile * kDenseTile;
   P.nchunk = (T + P.chunk - 1) / P.chunk;
@@ -245,12 +246,8 @@ DensePlan plan_dense(int batch, int n_kv_heads, int d, int T) {
 template <int D>
 cudaError_t launch_dense_d(const DenseArgs& a, int units, cudaStream_t s) {
   const size_t smem = (size_t)kDenseStages * 2 * kDenseTile * D * 2;
-  static size_t configured = 0;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(dense_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(dense_kernel<D>), smem);
+  if (e != cudaSuccess) return e;
   dense_kernel<D><<<units * a.nchunk, kDenseThreads, smem, s>>>(a);
   return cudaGetLastError();
 }

@@ -1,10 +1,45 @@
 // Host side of libdkv: descriptor validation, layout, argument checks and the
 // extern "C" entry points declared in include/dkv.h.  No kernel code here.
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "dkv_internal.cuh"
 
 namespace dkv {
+
+// Kernel attributes are per device: one record per (kernel, device) of what was
+// set on it, behind one lock (attribute calls happen at launch time only).
+namespace {
+std::mutex g_attr_mutex;
+std::map<std::pair<const void*, int>, size_t> g_smem_limit;
+std::map<std::pair<const void*, int>, bool> g_carveout;
+}  // namespace
+
+cudaError_t ensure_smem_limit(const void* func, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  size_t& have = g_smem_limit[{func, dev}];
+  if (bytes <= have) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
+cudaError_t ensure_max_carveout(const void* func) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  bool& done = g_carveout[{func, dev}];
+  if (done) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -357,6 +357,13 @@ cudaError_t launch_attend_tc(const Layout& L, const DecodePlan& P, int n_q_heads
 cudaError_t launch_combine_records(int units, int n_items, int n_q_heads, int n_kv_heads, int d,
                                    const float* partials, float* out, float* lse, cudaStream_t s);
 int sm_count();  // multiprocessors of the current device
+// Raise `func`'s dynamic shared-memory limit to at least `bytes` on the current
+// device: once per (kernel, device), again only when a larger size is asked for.
+// Thread-safe.
+cudaError_t ensure_smem_limit(const void* func, size_t bytes);
+// Ask for the largest shared-memory carveout for `func` on the current device,
+// once per (kernel, device).  Thread-safe.
+cudaError_t ensure_max_carveout(const void* func);
 cudaError_t launch_combine(const Layout& L, const DecodePlan& P, int batch, int n_q_heads, int n_kv_heads,
                            const float* partials, float* out, float* lse, cudaStream_t s);
 

@@ -64,7 +64,12 @@ extern "C" int dkv_decode_attend_noalloc(const dkv_desc* d, const void* q, const
   void* scratch = nullptr;
   if (dkv::scratch_address(&scratch) != cudaSuccess) return DKV_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the header (device error word) starts every call at zero
-  if (cudaMemsetAsync(scratch, 0, dkv::kWsHeader, s) != cudaSuccess) return DKV_ERR_CUDA;
+  // the header (device error word) and the tensor-core kernel's work-queue counters
+  // right after it start every call at zero: a call that gave up on a bounded wait
+  // can leave the counters set, and no caller can reach this area to clear them
+  dkv::Layout L;
+  dkv::make_layout(&c, &L);
+  const size_t clear = dkv::plan_decode(L, c.n_q_heads, c.n_kv_heads, top_k).off_routed;
+  if (cudaMemsetAsync(scratch, 0, clear, s) != cudaSuccess) return DKV_ERR_CUDA;
   return dkv_decode_attend(d, q, cache, top_k, out, lse, routed, scratch, dkv::kNoAllocScratchBytes, stream);
 }

@@ -308,13 +308,9 @@ cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, in
   const int G = n_q_heads / n_kv_heads;
   const float cq = 1.f / (sqrtf((float)L.d) * (float)G);
   const size_t smem = ((size_t)L.NB + 3) / 4 * 16;  // at most 2048 blocks: 8 KB
-  static bool carveout = false;  // an SM running a router CTA keeps room for attention CTAs of 108 KB
-  if (!carveout) {
-    const cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                               (int)cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    carveout = true;
-  }
+  // an SM running a router CTA keeps room for attention CTAs of 108 KB
+  const cudaError_t e = ensure_max_carveout(reinterpret_cast<const void*>(route_kernel));
+  if (e != cudaSuccess) return e;
   route_kernel<<<L.units * kRouteCluster, kRouteThreads, smem, s>>>(L, G, n_q_heads, n_kv_heads, P.K_eff, cq, q, cache,
                                                     reinterpret_cast<int32_t*>(ws + P.off_routed), routed_out);
   return cudaGetLastError();

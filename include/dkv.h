@@ -225,11 +225,15 @@ DKV_API int dkv_append(dkv_desc* d, const void* K_new, const void* V_new, int32_
  *           ascending, K_eff = top_k clipped to n_blocks.  Asking for them
  *           costs the router a second cluster exchange (about 0.7 us at 64k); without
  *           them the router writes each block to its rank's slot.
- *   workspace / ws_bytes  device scratch of dkv_decode_workspace_bytes(d, top_k);
- *           zero-fill it once before its first use: its header holds the
- *           device error word (read by dkv_get_error) and the work-queue
- *           counters of the tensor-core layout's kernel, which every call
- *           leaves at zero again
+ *   workspace / ws_bytes  device scratch of dkv_decode_workspace_bytes(d, top_k)
+ *           (its size depends on the current device's multiprocessor count);
+ *           zero-fill it once before its first use: its 256-byte header holds
+ *           the device error word (read by dkv_get_error), and the 8 bytes
+ *           right after the header hold the work-queue counters of the
+ *           tensor-core layout's kernel, which every call that completes
+ *           leaves at zero again.  After DKV_ERR_TIMEOUT zero-fill the
+ *           workspace again before reusing it: a kernel that gave up on a
+ *           wait can leave those counters set
  * Routing: qbar = mean over the group of c*q; block score
  * sum_j max(qbar_j kmax_bj, qbar_j kmin_bj); top-K by (score desc, index asc).
  */
@@ -293,7 +297,9 @@ DKV_API int dkv_decode_combine(const dkv_desc* d, int32_t top_k, float* out, flo
  *     call's contents: calls that overlap on the GPU (on different streams,
  *     or from different threads) race and corrupt each other's results.
  *     Serialise them, for instance on one stream.
- *   - The area's error word is cleared at the start of each call and cannot
+ *   - Each call first clears the area's header (the error word) and the
+ *     work-queue counters after it, so a call that gave up on a wait does
+ *     not leave later calls with a stale work queue; the error word cannot
  *     be read back; use dkv_decode_attend with a workspace to diagnose.
  * Other arguments, layouts and results are those of dkv_decode_attend.
  */
