@@ -370,6 +370,81 @@ def decode_unit_factored(q: np.ndarray, unit: Unit, top_k: int, window_chunk: in
 
 
 # ---------------------------------------------------------------------------
+# group-quantised residual rows
+# ---------------------------------------------------------------------------
+
+RESIDUAL_QUANT_GROUP = 64  # [README Innov] "asymmetric group quantization (group_size=64, ...)"
+
+
+def quantize_groups(X: np.ndarray, bits: int, group: int = RESIDUAL_QUANT_GROUP):
+    """Asymmetric group quantisation of the rows of X ([README Innov] "Physical
+    4-Bit Group-Quantized Residual Buffers"; [README Knobs] DKV_RESIDUAL_QUANT,
+    DKV_RESIDUAL_QUANT_GROUP_SIZE, DKV_RESIDUAL_QUANT_BITS).
+
+    Every row is cut into groups of ``group`` consecutive channels.  Per group:
+    bias = the group's minimum and scale = (maximum - minimum) / (2^bits - 1),
+    both kept in fp16 (the pages' "half-precision scale and bias"); each value's
+    code is the nearest integer to (x - bias) / scale, clamped to
+    [0, 2^bits - 1]; a group whose fp16 scale is 0 has every code 0.  The code
+    is an integer decision, taken in fp32 (the difference, the division and the
+    range of the group are fp32 operations on the fp16 values; the rounding goes
+    to the nearest integer, ties to even).
+
+    X holds fp16 values (any float dtype).  Returns codes uint8 [n, d] and the
+    fp16 scale and bias [n, d / group].
+    """
+    X = np.asarray(X, dtype=np.float32)  # exact for fp16 values
+    n, d = X.shape
+    if d % group:
+        raise ValueError("head_dim must be a multiple of the group size")
+    Xg = X.reshape(n, d // group, group)
+    lo = Xg.min(axis=2)
+    hi = Xg.max(axis=2)
+    levels = np.float32(2 ** bits - 1)
+    scale = ((hi - lo) / levels).astype(np.float16)
+    bias = lo.astype(np.float16)  # exact: the minimum is one of the fp16 values
+    s = scale.astype(np.float32)[:, :, None]
+    b = bias.astype(np.float32)[:, :, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint((Xg - b) / s)
+    q = np.where(s == 0, 0.0, q)
+    q = np.clip(q, 0, 2 ** bits - 1)
+    return q.reshape(n, d).astype(np.uint8), scale, bias
+
+
+def dequantize_groups(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray,
+                      group: int = RESIDUAL_QUANT_GROUP) -> np.ndarray:
+    """x_hat = scale * code + bias, per group of ``group`` channels, in fp64 from
+    the stored fp16 scale and bias (the dequantisation of ``quantize_groups``)."""
+    codes = np.asarray(codes, dtype=np.float64)
+    n, d = codes.shape
+    s = np.asarray(scale, dtype=np.float64)
+    b = np.asarray(bias, dtype=np.float64)
+    return (codes.reshape(n, d // group, group) * s[:, :, None] + b[:, :, None]).reshape(n, d)
+
+
+def quantize_block_residuals(blk: Block, bits: int) -> Block:
+    """The block as the decode reads it when its exact residual rows are stored
+    group-quantised ([README Innov]: "only the gathered top-K routed blocks are
+    dequantized ... during decode attention"): K_res and V_res are replaced by
+    the dequantised images of their own quantisation, each row on its own
+    (keys and values separately); positions and every other part stay as they are."""
+    if blk.S.size == 0:
+        return dataclasses.replace(blk)
+    Kq = dequantize_groups(*quantize_groups(blk.K_res, bits))
+    Vq = dequantize_groups(*quantize_groups(blk.V_res, bits))
+    return dataclasses.replace(blk, K_res=Kq, V_res=Vq)
+
+
+def quant_residual_row_bytes(d: int, bits: int, group: int = RESIDUAL_QUANT_GROUP) -> int:
+    """Bytes of one group-quantised residual row (a key or a value): d codes of
+    ``bits`` bits packed in 32-bit words, plus an fp16 scale and an fp16 bias
+    per group of ``group`` channels ([README Innov]: "head_dim * bits // 32 = 16
+    words for D=128 alongside half-precision scale and bias vectors (8 bytes)")."""
+    return d * bits // 32 * 4 + (d // group) * 4
+
+
+# ---------------------------------------------------------------------------
 # byte accounting
 # ---------------------------------------------------------------------------
 

@@ -58,7 +58,8 @@ _orig = {n: getattr(O, n) for n in ("router_bounds", "route", "select_residuals"
                                     "reconstruct_block", "softmax_attention", "lse_merge", "block_partial",
                                     "decode_unit", "append_tokens", "effective_top_k", "compress_unit",
                                     "decode_unit_factored", "_part", "pages_block_bytes", "residual_row_bytes",
-                                    "dense_kv_bytes")}
+                                    "dense_kv_bytes", "quantize_groups", "dequantize_groups",
+                                    "quantize_block_residuals", "quant_residual_row_bytes")}
 
 
 def _bounds_without_kmin(q, kmin, kmax):
@@ -262,7 +263,57 @@ def _top_k_zero_is_none(top_k, n_blocks):
     return min(int(top_k), n_blocks)
 
 
+def _quantize(X, bits, group=64, rounding=np.rint, levels=None, bias_fn=None, interleave=False):
+    """quantize_groups with one slip (rounding, step count, bias or group shape)."""
+    X = np.asarray(X, dtype=np.float32)
+    n, d = X.shape
+    Xg = X.reshape(n, group, d // group).transpose(0, 2, 1) if interleave else X.reshape(n, d // group, group)
+    lo, hi = Xg.min(axis=2), Xg.max(axis=2)
+    lv = np.float32(levels if levels is not None else 2 ** bits - 1)
+    scale = ((hi - lo) / lv).astype(np.float16)
+    bias = (bias_fn(Xg) if bias_fn else lo).astype(np.float16)
+    sv = scale.astype(np.float32)[:, :, None]
+    bv = bias.astype(np.float32)[:, :, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = rounding((Xg - bv) / sv)
+    q = np.clip(np.where(sv == 0, 0.0, q), 0, 2 ** bits - 1)
+    if interleave:
+        q = q.transpose(0, 2, 1)
+    return q.reshape(n, d).astype(np.uint8), scale, bias
+
+
+def _dequantize_scale_bias_swapped(codes, scale, bias, group=64):
+    return _orig["dequantize_groups"](codes, bias, scale, group)
+
+
+def _quant_block_kv_swapped(blk, bits):
+    import dataclasses
+    if blk.S.size == 0:
+        return dataclasses.replace(blk)
+    return dataclasses.replace(blk, K_res=O.dequantize_groups(*O.quantize_groups(blk.V_res, bits)),
+                               V_res=O.dequantize_groups(*O.quantize_groups(blk.K_res, bits)))
+
+
+def _quant_block_keys_only(blk, bits):
+    import dataclasses
+    if blk.S.size == 0:
+        return dataclasses.replace(blk)
+    return dataclasses.replace(blk, K_res=O.dequantize_groups(*O.quantize_groups(blk.K_res, bits)))
+
+
 MUTANTS = {
+    "quantisation rounds down": ("quantize_groups", lambda X, bits, group=64: _quantize(X, bits, group, rounding=np.floor)),
+    "quantisation step over 2^bits levels": ("quantize_groups",
+                                             lambda X, bits, group=64: _quantize(X, bits, group, levels=2 ** bits)),
+    "quantisation bias at the group mean": ("quantize_groups", lambda X, bits, group=64: _quantize(
+        X, bits, group, bias_fn=lambda Xg: Xg.mean(axis=2))),
+    "quantisation groups strided across the row": ("quantize_groups",
+                                                   lambda X, bits, group=64: _quantize(X, bits, group, interleave=True)),
+    "dequantisation swaps scale and bias": ("dequantize_groups", _dequantize_scale_bias_swapped),
+    "quantised residual keys and values swapped": ("quantize_block_residuals", _quant_block_kv_swapped),
+    "quantised residuals leave the values exact": ("quantize_block_residuals", _quant_block_keys_only),
+    "quantised row bytes without scale and bias": ("quant_residual_row_bytes", lambda d, bits, group=64: d * bits // 8),
+
     "router bound drops the kmin branch": ("router_bounds", _bounds_without_kmin),
     "router bound uses one head, not the group mean": ("router_bounds", _bounds_first_head_only),
     "router bound misses the 1/sqrt(d) scale": ("router_bounds", _bounds_unscaled),

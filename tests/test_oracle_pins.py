@@ -6,7 +6,7 @@ closed form, an invariant, brute force on tiny inputs, or the numbers the
 pages print (tests/golden).  A plausible slip in the oracle (dropped anchor,
 wrong sign of a delta, transposed basis, residual rows not substituted,
 wrong tie order, a missing LSE rescale) fails at least one of them;
-tests/test_oracle_mutants.py plants 32 such slips and checks exactly that.
+tests/test_oracle_mutants.py plants 40 such slips and checks exactly that.
 """
 import itertools
 import json
@@ -427,3 +427,139 @@ def test_streaming_append_needs_a_full_block_of_window():
     unit = O.compress_unit(np.zeros((100, 8)), np.zeros((100, 8)), 0, 2, 1)
     with pytest.raises(ValueError):
         O.append_tokens(unit, np.ones((1, 8)), np.ones((1, 8)), 100, 2, 1)
+
+
+# ----------------------------------------------------------------- group-quantised residuals
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantization_recovers_values_on_its_own_grid(bits):
+    """Values that sit exactly on a group's grid (bias + scale * code, with the
+    lowest and highest codes present) quantise to exactly that scale, bias and
+    codes, and dequantise back without error."""
+    rng = np.random.default_rng(70 + bits)
+    top = 2 ** bits - 1
+    n, d, g = 6, 128, O.RESIDUAL_QUANT_GROUP
+    scale = 2.0 ** rng.integers(-8, -2, size=(n, d // g))
+    bias = rng.integers(-64, 64, size=(n, d // g)) * scale
+    codes = rng.integers(0, top + 1, size=(n, d))
+    codes[:, 0::g] = 0
+    codes[:, 1::g] = top
+    X = (codes.reshape(n, d // g, g) * scale[:, :, None] + bias[:, :, None]).reshape(n, d)
+    assert np.array_equal(X.astype(np.float16).astype(np.float64), X)  # exact fp16 values
+    q, s, b = O.quantize_groups(X, bits)
+    assert np.array_equal(q, codes)
+    assert np.array_equal(s.astype(np.float64), scale) and np.array_equal(b.astype(np.float64), bias)
+    assert np.array_equal(O.dequantize_groups(q, s, b), X)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantization_picks_the_nearest_code(bits):
+    """Brute force over every code: the chosen code's reconstruction is the
+    nearest to the value on the group's stored fp16 grid (within the fp32
+    rounding of the division at exact midpoints)."""
+    rng = np.random.default_rng(80 + bits)
+    X = (rng.standard_normal((8, 128)) * rng.uniform(0.1, 20, size=(8, 1))).astype(np.float16).astype(np.float64)
+    q, s, b = O.quantize_groups(X, bits)
+    g = O.RESIDUAL_QUANT_GROUP
+    grid = np.arange(2 ** bits, dtype=np.float64)
+    for i in range(X.shape[0]):
+        for j in range(X.shape[1]):
+            sv, bv = float(s[i, j // g]), float(b[i, j // g])
+            err = np.abs(X[i, j] - (sv * grid + bv))
+            assert err[q[i, j]] <= err.min() + 1e-6 * max(sv, 1e-30), (i, j, q[i, j], int(err.argmin()))
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantization_error_is_within_half_a_step(bits):
+    """|x - x_hat| <= scale / 2, up to the fp16 rounding of the stored scale at the
+    top of the group's range ((2^bits - 1) steps of at most 2^-11 scale each)."""
+    rng = np.random.default_rng(90 + bits)
+    X = (rng.standard_normal((64, 128)) * 4).astype(np.float16).astype(np.float64)
+    X[3] *= 8.0  # an outlier row
+    q, s, b = O.quantize_groups(X, bits)
+    xr = O.dequantize_groups(q, s, b)
+    g = O.RESIDUAL_QUANT_GROUP
+    step = np.repeat(s.astype(np.float64), g, axis=1)
+    rng_ = np.repeat((X.reshape(64, -1, g).max(2) - X.reshape(64, -1, g).min(2)), g, axis=1)
+    assert (np.abs(X - xr) <= step / 2 + rng_ * 2.0 ** -10 + 1e-12).all()
+    assert q.max() <= 2 ** bits - 1
+
+
+def test_quantization_of_a_constant_group_is_exact():
+    """A group whose values are all equal has scale 0, every code 0 and
+    reconstructs exactly; the other group of the row is unaffected."""
+    X = np.zeros((2, 128))
+    X[0, :64] = 1.5
+    X[0, 64:] = np.linspace(-2, 2, 64).astype(np.float16)
+    X[1, :] = -3.25
+    for bits in (8, 4):
+        q, s, b = O.quantize_groups(X, bits)
+        assert float(s[0, 0]) == 0.0 and (q[0, :64] == 0).all() and float(b[0, 0]) == 1.5
+        assert (q[1] == 0).all()
+        xr = O.dequantize_groups(q, s, b)
+        assert np.array_equal(xr[0, :64], X[0, :64]) and np.array_equal(xr[1], X[1])
+        assert float(s[0, 1]) > 0
+
+
+def test_quantized_row_bytes_match_the_pages():
+    """[README Innov] item 2: 16 words of codes plus 8 bytes of scale and bias per
+    d128 int4 row; 3.56x (int4) and 1.9x (int8) against an fp16 row; R = 256 int4
+    residuals in 44 % less memory than R = 128 fp16 ones (112.9 / 200.7 MB at 16k)."""
+    gold = json.load(open(os.path.join(GOLDEN, "residual_quant.json")))
+    d = gold["head_dim"]
+    assert gold["group_size"] == O.RESIDUAL_QUANT_GROUP
+    int4 = O.quant_residual_row_bytes(d, 4)
+    int8 = O.quant_residual_row_bytes(d, 8)
+    assert int4 == gold["int4_words_per_row"] * 4 + gold["scale_bias_bytes_per_row"]
+    fp16 = O.residual_row_bytes(d) // 2  # one row (key or value) of fp16
+    assert round(fp16 / int4, 2) == gold["compression_vs_fp16"]["int4"]
+    assert round(fp16 / int8, 1) == gold["compression_vs_fp16"]["int8"]
+    ratio = (256 * int4) / (128 * fp16)
+    mb = gold["store_16k_mb"]
+    assert abs(ratio - mb["int4_R256"] / mb["fp16_R128"]) < 5e-4
+    assert round(100 * (1 - ratio)) == gold["less_memory_pct"]
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantized_residual_decode_brute_force(bits):
+    """Decode over blocks whose residual rows are stored quantised equals a
+    scalar-loop reconstruction: rows in S rebuilt element by element from their
+    own codes, scale and bias (keys and values each from their own); every
+    other row from the anchor and the low-rank factors."""
+    rng = np.random.default_rng(100 + bits)
+    d, nb, W, r, R = 64, 2, 20, 5, 9
+    K, V = _kv(rng, nb * BS + W, d)
+    K = K.astype(np.float16).astype(np.float64)
+    V = V.astype(np.float16).astype(np.float64)
+    q = rng.standard_normal((2, d))
+    unit = O.compress_unit(K, V, nb, r, R)
+    qunit = O.Unit(blocks=[O.quantize_block_residuals(b, bits) for b in unit.blocks], win_K=unit.win_K,
+                   win_V=unit.win_V)
+    got = O.decode_unit(q, qunit, 0)
+    g = O.RESIDUAL_QUANT_GROUP
+    Ks, Vs = [], []
+    for blk in unit.blocks:
+        kq, ks, kb = O.quantize_groups(blk.K_res, bits)
+        vq, vs, vb = O.quantize_groups(blk.V_res, bits)
+        for t in range(BS):
+            krow, vrow = [], []
+            for j in range(d):
+                if t == 0:
+                    kx, vx = blk.a_k[j], blk.a_v[j]
+                elif t in list(blk.S):
+                    i = list(blk.S).index(t)
+                    kx = float(ks[i, j // g]) * int(kq[i, j]) + float(kb[i, j // g])
+                    vx = float(vs[i, j // g]) * int(vq[i, j]) + float(vb[i, j // g])
+                else:
+                    kx = blk.a_k[j] + sum(blk.U[t - 1, k] * blk.V_K[k, j] for k in range(r))
+                    vx = blk.a_v[j] + sum(blk.U[t - 1, k] * blk.V_V[k, j] for k in range(r))
+                krow.append(kx)
+                vrow.append(vx)
+            Ks.append(krow)
+            Vs.append(vrow)
+    Ks = np.array(Ks + list(unit.win_K))
+    Vs = np.array(Vs + list(unit.win_V))
+    o, lse = _dense(q, Ks, Vs)
+    np.testing.assert_allclose(got["o"], o, atol=1e-10, rtol=0)
+    np.testing.assert_allclose(got["lse"], lse, atol=1e-10, rtol=0)
+    assert np.abs(got["o"] - O.decode_unit(q, unit, 0)["o"]).max() > 0  # the quantisation is visible
