@@ -414,20 +414,24 @@ def quantize_groups(X: np.ndarray, bits: int, group: int = RESIDUAL_QUANT_GROUP)
 
 def dequantize_groups(codes: np.ndarray, scale: np.ndarray, bias: np.ndarray,
                       group: int = RESIDUAL_QUANT_GROUP) -> np.ndarray:
-    """x_hat = scale * code + bias, per group of ``group`` channels, in fp64 from
-    the stored fp16 scale and bias (the dequantisation of ``quantize_groups``)."""
+    """x_hat = scale * code + bias per group of ``group`` channels, from the stored
+    fp16 scale and bias, rounded once to fp16: [README Innov] dequantises the
+    routed blocks "into transient scratchpads" for the attention, whose operands
+    are fp16.  (scale * code + bias is exact in fp64, so the one rounding is the
+    fp16 one.)  Returned as float64."""
     codes = np.asarray(codes, dtype=np.float64)
     n, d = codes.shape
     s = np.asarray(scale, dtype=np.float64)
     b = np.asarray(bias, dtype=np.float64)
-    return (codes.reshape(n, d // group, group) * s[:, :, None] + b[:, :, None]).reshape(n, d)
+    x = (codes.reshape(n, d // group, group) * s[:, :, None] + b[:, :, None]).reshape(n, d)
+    return x.astype(np.float16).astype(np.float64)
 
 
 def quantize_block_residuals(blk: Block, bits: int) -> Block:
     """The block as the decode reads it when its exact residual rows are stored
     group-quantised ([README Innov]: "only the gathered top-K routed blocks are
     dequantized ... during decode attention"): K_res and V_res are replaced by
-    the dequantised images of their own quantisation, each row on its own
+    the dequantised (fp16) images of their own quantisation, each row on its own
     (keys and values separately); positions and every other part stay as they are."""
     if blk.S.size == 0:
         return dataclasses.replace(blk)
