@@ -63,21 +63,28 @@ def whole_job_rate(world: int, queries_per_step: int, steps: int, ms: float) -> 
 
 # ----------------------------------------------------------------------------- byte accounting
 
-def attend_bytes(w, layer: int, top_k: int) -> int:
+def residual_token_bytes(d: int, bits: int) -> int:
+    """Bytes of one residual token (its key row and value row): fp16 rows, or
+    group-quantised rows (codes plus an fp16 scale and bias per 64 channels)."""
+    return 4 * d if bits == 0 else 2 * (d * bits // 8 + 4 * (d // 64))
+
+
+def attend_bytes(w, layer: int, top_k: int, bits: int = 0) -> int:
     """Algorithmic bytes the block/window attention kernel must read per launch:
     per unit K routed blocks (anchors 4d + V_K,V_V 4rd + U 2*255*r + residual
-    rows 4Rd + mask 32) plus the window 4Wd; per launch the queries."""
+    rows R * (4d, or their quantised size) + mask 32) plus the window 4Wd; per
+    launch the queries."""
     d, r, R, W, NB = w.head_dim, w.rank(layer), w.n_residual, w.window, w.n_blocks
     k = NB if (top_k == 0 or top_k >= NB) else top_k
-    per_block = 4 * d + 4 * r * d + 2 * 255 * r + 4 * R * d + 32
+    per_block = 4 * d + 4 * r * d + 2 * 255 * r + R * residual_token_bytes(d, bits) + 32
     per_unit = k * per_block + W * 4 * d
     return w.units_per_layer * per_unit + w.batch * w.n_q_heads * d * 2
 
 
-def call_bytes(w, layer: int, top_k: int) -> int:
+def call_bytes(w, layer: int, top_k: int, bits: int = 0) -> int:
     """Algorithmic bytes of one dkv_decode_attend: the attention kernel's bytes,
     the router rows NB*4d per unit, and the fp32 output."""
-    return (attend_bytes(w, layer, top_k) + w.units_per_layer * w.n_blocks * 4 * w.head_dim
+    return (attend_bytes(w, layer, top_k, bits) + w.units_per_layer * w.n_blocks * 4 * w.head_dim
             + w.batch * w.n_q_heads * w.head_dim * 4)
 
 
@@ -279,6 +286,8 @@ def main():
                     help="further workloads reported under `configs` (one layer each, several cache replicas)")
     ap.add_argument("--config-steps", type=int, default=20, help="steps per graph for the further workloads")
     ap.add_argument("--no-configs", action="store_true", help="skip the further workloads")
+    ap.add_argument("--quant-bits", default="8,4",
+                    help="also time the headline workload with residual rows group-quantised to these widths")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -370,14 +379,15 @@ def main():
         workloads rotate a step's calls over cache replicas so that the bytes one step
         reads span at least 4x the L2 and every call reads its cache from HBM."""
 
-        def __init__(self, w, layer_ids, top_k, layout, ws_bytes=None, min_call_bytes=None):
-            self.w, self.top_k, self.layout = w, top_k, layout
-            base = sum(call_bytes(w, l, top_k) for l in layer_ids)
+        def __init__(self, w, layer_ids, top_k, layout, ws_bytes=None, min_call_bytes=None, bits=0):
+            self.w, self.top_k, self.layout, self.bits = w, top_k, layout, bits
+            base = sum(call_bytes(w, l, top_k, bits) for l in layer_ids)
             self.n_rep = cache_replicas(min_call_bytes or base, l2_bytes)
             self.layer_ids = layer_ids * self.n_rep
             self.n_layers = len(self.layer_ids)
             self.descs = [dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window,
-                                         w.rank(l), w.n_residual, layout=layout_ids[layout]) for l in self.layer_ids]
+                                         w.rank(l), w.n_residual, layout=layout_ids[layout], residual_bits=bits)
+                          for l in self.layer_ids]
             need = max(dkv.dkv_decode_workspace_bytes(d, k) for d in self.descs for k in {top_k, 0})
             self.ws = torch.zeros(max(need, ws_bytes or 0), dtype=torch.uint8, device=dev)
             self.caches = []
@@ -540,8 +550,8 @@ def main():
     configs = {}
     if not args.no_configs and args.layers is None:
         def config_entry(wc, k, R_, S_, steps_c):
-            cb = sum(call_bytes(wc, l, k) for l in S_.layer_ids)
-            ab = sum(attend_bytes(wc, l, k) for l in S_.layer_ids)
+            cb = sum(call_bytes(wc, l, k, S_.bits) for l in S_.layer_ids)
+            ab = sum(attend_bytes(wc, l, k, S_.bits) for l in S_.layer_ids)
             ms_call = R_["ms"] / (steps_c * S_.n_layers)
             att_us = 1e3 * statistics.fmean(R_["attend_ms"])
             return {"workload": (f"{wc.name}: batch {wc.batch}, {wc.n_q_heads}q/{wc.n_kv_heads}kv x d{wc.head_dim}, "
@@ -556,6 +566,16 @@ def main():
                     "attend_frac": (ab / S_.n_layers) / (att_us / 1e6) / 1e9 / peak,
                     "latency_us": R_["latency_us"],
                     "replays": len(R_["ms_replays"]), "clocks": R_["clocks"]}
+        # the headline workload with group-quantised residual rows (README "Core Innovations" item 2)
+        for bits in ([int(x) for x in args.quant_bits.split(",")] if args.quant_bits else []):
+            Sq = Setup(w, base_ids, top_k, "fragment", bits=bits)
+            Rq = Sq.measure(top_k, K_steps, args.warmup, reps)
+            ent = config_entry(w, top_k, Rq, Sq, K_steps)
+            ent["workload"] = f"{wl_name}; residual rows group-quantised to int{bits} (64-channel groups)"
+            ent["queries_per_s"] = queries_per_step * K_steps / (Rq["ms"] / 1e3)
+            ent["ms_per_step"] = Rq["ms"] / K_steps
+            configs[f"{w.name}_int{bits}_residuals"] = ent
+            Sq.free()
         for name in args.configs.split(","):
             wc = synth.WORKLOADS[name]
             ks = [wc.top_k] if name != "sweep16k" else [4, 16, wc.n_blocks]

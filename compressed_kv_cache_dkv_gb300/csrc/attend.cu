@@ -66,6 +66,8 @@ struct AttendArgs {
   Layout L;
   int G, Hq, Hkv, K_eff, n_r, nres, n_wst, ring, mode;
   uint32_t inflight;  // bytes a CTA keeps in flight (issued, not yet landed) at most
+  uint32_t wait_limit;  // polls of a bounded wait (kWaitLimit unless a diagnostic limit is set)
+  int stop_after;       // diagnostic: chunks a producer issues at most (negative: all)
   float scale_log2;  // log2(e) / sqrt(d)
   const __half* q;
   const uint8_t* cache;
@@ -136,8 +138,9 @@ struct Cursor {
       c.kind = kRes;
       c.tok0 = (k - 1) * kStageTok;
       c.ntok = min(kStageTok, L.R8 - c.tok0);
-      c.bytes = (uint32_t)(c.ntok * 4 * L.d);
-      c.off = L.off_res + (uint64_t)c.tok0 * 4 * L.d;
+      // fp16 rows: 4d bytes a token; quantised rows: whole 16-token groups of L.qgb bytes
+      c.bytes = L.qbits ? (uint32_t)(c.ntok / 16 * L.qgb) : (uint32_t)(c.ntok * 4 * L.d);
+      c.off = L.off_res + (L.qbits ? (uint64_t)(c.tok0 / 16) * L.qgb : (uint64_t)c.tok0 * 4 * L.d);
     }
     ++it;
     if (++k > a.nres) { k = 0; ++j; }
@@ -335,6 +338,128 @@ __device__ __forceinline__ void exact_group(WarpState<D>& st, uint32_t qrow, uin
   }
 }
 
+// One 16-token group of group-quantised residual rows (Layout.qbits = BITS) of
+// one warp: the same products as exact_group, with each operand register
+// rebuilt from its codes in registers: (code | 0x6400) is the half 1024 + code,
+// so h - 1024 is the code exactly and fma(scale, code, bias) rounds the
+// dequantised value to fp16 once.  Key rows take their row's scale (rows gq,
+// gq + 8 of the tile); value columns (tokens 2t, 2t + 1 and 2t + 8, 2t + 9)
+// their tokens' scales, per 64-channel group.
+__device__ inline __half2 lds_h2(uint32_t addr) {  // one fp16 from shared memory, in both halves
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return __half2half2(__ushort_as_half(v));
+}
+__device__ inline uint32_t deq2(uint32_t codes, __half2 s, __half2 b) {
+  const __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&codes), __float2half2_rn(1024.f));
+  const __half2 x = __hfma2(s, c, b);
+  return *reinterpret_cast<const uint32_t*>(&x);
+}
+template <int BITS>
+__device__ inline uint32_t qfield(uint32_t w, int sh) {  // the half2 1024 + codes of one register
+  return ((w >> sh) & (BITS == 8 ? 0x00FF00FFu : 0x000F000Fu)) | 0x64006400u;
+}
+template <int D, int BITS>
+__device__ __forceinline__ void exact_group_q(WarpState<D>& st, uint32_t qrow, uint32_t gb, int tok, int nvalid,
+                                              float slog2, bool gv0, bool gv1, int lane) {
+  constexpr int KT = D / 16;
+  constexpr int G = D / kQuantGroup;
+  constexpr uint32_t CB = 16u * D * BITS / 8u;
+  constexpr int TPC = BITS == 8 ? 2 : 4;  // k tiles per 512-byte chunk
+  const int gq = lane >> 2, t = lane & 3;
+  uint32_t qb[KT][2];
+#pragma unroll
+  for (int kt = 0; kt < KT; ++kt) {
+    qb[kt][0] = lds32(qrow + (uint32_t)(16 * kt + 2 * t) * 2u);
+    qb[kt][1] = lds32(qrow + (uint32_t)(16 * kt + 8 + 2 * t) * 2u);
+  }
+  const uint32_t ksc = gb + 2 * CB, vsc = ksc + 64u * G;  // [scale G x 16][bias G x 16] of K, then of V
+  uint4 kw[KT / TPC];
+#pragma unroll
+  for (int c = 0; c < KT / TPC; ++c) kw[c] = lds128(gb + (uint32_t)c * 512u + (uint32_t)lane * 16u);
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    // this lane's key rows gq and gq + 8: one scale and one bias each, for both halves
+    const __half2 s0 = lds_h2(ksc + (uint32_t)(g * 16 + gq) * 2u), s1 = lds_h2(ksc + (uint32_t)(g * 16 + gq + 8) * 2u);
+    const __half2 b0 = lds_h2(ksc + 32u * G + (uint32_t)(g * 16 + gq) * 2u);
+    const __half2 b1 = lds_h2(ksc + 32u * G + (uint32_t)(g * 16 + gq + 8) * 2u);
+#pragma unroll
+    for (int kq = 0; kq < 4; ++kq) {  // the four k tiles of this 64-channel group
+      const int kt = 4 * g + kq;
+      const uint4 v = kw[kt / TPC];
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t a0, a1, a2, a3;
+      if (BITS == 8) {
+        const uint32_t wa = wv[2 * (kt % 2)], wb = wv[2 * (kt % 2) + 1];
+        a0 = deq2(qfield<8>(wa, 0), s0, b0);
+        a1 = deq2(qfield<8>(wa, 8), s1, b1);
+        a2 = deq2(qfield<8>(wb, 0), s0, b0);
+        a3 = deq2(qfield<8>(wb, 8), s1, b1);
+      } else {
+        const uint32_t w = wv[kt % 4];
+        a0 = deq2(qfield<4>(w, 0), s0, b0);
+        a1 = deq2(qfield<4>(w, 4), s1, b1);
+        a2 = deq2(qfield<4>(w, 8), s0, b0);
+        a3 = deq2(qfield<4>(w, 12), s1, b1);
+      }
+      mma16816(acc[kt & 1], a0, a1, a2, a3, qb[kt][0], qb[kt][1]);
+    }
+  }
+  const int tk0 = tok + gq, tk1 = tk0 + 8;
+  const bool v0 = tk0 < nvalid, v1 = tk1 < nvalid;
+  float s[4];
+  s[0] = v0 ? (acc[0][0] + acc[1][0]) * slog2 : -INFINITY;
+  s[1] = v0 ? (acc[0][1] + acc[1][1]) * slog2 : -INFINITY;
+  s[2] = v1 ? (acc[0][2] + acc[1][2]) * slog2 : -INFINITY;
+  s[3] = v1 ? (acc[0][3] + acc[1][3]) * slog2 : -INFINITY;
+  float sc0, sc1, ms0, ms1;
+  raise_max<D>(st, fmaxf(s[0], s[2]), fmaxf(s[1], s[3]), sc0, sc1, ms0, ms1);
+  float p[4];
+  p[0] = gv0 ? fast_exp2(s[0] - ms0) : 0.f;
+  p[1] = gv1 ? fast_exp2(s[1] - ms1) : 0.f;
+  p[2] = gv0 ? fast_exp2(s[2] - ms0) : 0.f;
+  p[3] = gv1 ? fast_exp2(s[3] - ms1) : 0.f;
+  st.l0 += p[0] + p[2];
+  st.l1 += p[1] + p[3];
+  uint32_t bh0, bl0, bh1, bl1;
+  c_to_b(p[0], p[1], p[2], p[3], bh0, bl0, bh1, bl1);
+  uint4 vw[KT / TPC];
+#pragma unroll
+  for (int c = 0; c < KT / TPC; ++c) vw[c] = lds128(gb + CB + (uint32_t)c * 512u + (uint32_t)lane * 16u);
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    // value columns: tokens (2t, 2t + 1) and (2t + 8, 2t + 9), their own scales and biases
+    const uint32_t sl = lds32(vsc + (uint32_t)(g * 16 + 2 * t) * 2u), sh = lds32(vsc + (uint32_t)(g * 16 + 2 * t + 8) * 2u);
+    const uint32_t bl = lds32(vsc + 32u * G + (uint32_t)(g * 16 + 2 * t) * 2u);
+    const uint32_t bhh = lds32(vsc + 32u * G + (uint32_t)(g * 16 + 2 * t + 8) * 2u);
+    const __half2 s01 = *reinterpret_cast<const __half2*>(&sl), s89 = *reinterpret_cast<const __half2*>(&sh);
+    const __half2 b01 = *reinterpret_cast<const __half2*>(&bl), b89 = *reinterpret_cast<const __half2*>(&bhh);
+#pragma unroll
+    for (int mq = 0; mq < 4; ++mq) {
+      const int md = 4 * g + mq;
+      const uint4 v = vw[md / TPC];
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t a0, a1, a2, a3;
+      if (BITS == 8) {
+        const uint32_t wa = wv[2 * (md % 2)], wb = wv[2 * (md % 2) + 1];
+        a0 = deq2(qfield<8>(wa, 0), s01, b01);
+        a1 = deq2(qfield<8>(wa, 8), s01, b01);
+        a2 = deq2(qfield<8>(wb, 0), s89, b89);
+        a3 = deq2(qfield<8>(wb, 8), s89, b89);
+      } else {
+        const uint32_t w = wv[md % 4];
+        a0 = deq2(qfield<4>(w, 0), s01, b01);
+        a1 = deq2(qfield<4>(w, 4), s01, b01);
+        a2 = deq2(qfield<4>(w, 8), s89, b89);
+        a3 = deq2(qfield<4>(w, 12), s89, b89);
+      }
+      mma16816(st.o[md], a0, a1, a2, a3, bh0, bh1);
+      mma16816(st.o[md], a0, a1, a2, a3, bl0, bl1);
+    }
+  }
+}
+
 // Low-rank state of one routed block, live from its head chunk to its V_V chunk.
 // Padded rank of a kernel instance: R8S > 0 fixes it at compile time (every
 // tile test then folds away); R8S < 0 reads it at run time, up to 16 * (-R8S).
@@ -401,28 +526,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
     RingPos rp = {0u, 0u};
     uint32_t rel_end = 0, land_end = 0;
     int c = 0, rel = 0, land = 0;  // chunks issued; released (seen); landed (seen)
-    bool routed_ready = false;
+    bool routed_ready = false, ok = true;
     int jb = -1;
     const uint8_t* blk = unit;
-    while (cur.next(a, ch)) {
+    while (ok && cur.next(a, ch)) {
+      if (a.stop_after >= 0 && c >= a.stop_after) break;  // diagnostic: nothing further is issued
       const uint32_t off = rp.place(ch.bytes, ring);
       // wait until the chunk's bytes and barrier pair are free: the chunks not yet
       // released occupy [rel_end, start) of the running byte count (releases come in order)
-      while (c - rel >= kNBar || (rel < c && rp.pos - rel_end > ring)) {
+      while (ok && (c - rel >= kNBar || (rel < c && rp.pos - rel_end > ring))) {
         const int rb = rel & (kNBar - 1);
-        if (!mbar_wait(&empty[rb], (uint32_t)(rel / kNBar) & 1u, a.err)) return;
-        rel_end = ends[rb];
-        ++rel;
+        ok = mbar_wait(&empty[rb], (uint32_t)(rel / kNBar) & 1u, a.err, a.wait_limit);
+        if (ok) { rel_end = ends[rb]; ++rel; }
       }
       // keep at most a.inflight bytes in flight: more only lengthens the queues of the
       // memory system (every CTA's first chunks land later) without adding bandwidth
       if (land < rel) { land = rel; land_end = rel_end; }
-      while (land < c && rp.pos - land_end > a.inflight) {
+      while (ok && land < c && rp.pos - land_end > a.inflight) {
         const int lb = land & (kNBar - 1);
-        if (!mbar_wait(&full[lb], (uint32_t)(land / kNBar) & 1u, a.err)) return;
-        land_end = ends[lb];
-        ++land;
+        ok = mbar_wait(&full[lb], (uint32_t)(land / kNBar) & 1u, a.err, a.wait_limit);
+        if (ok) { land_end = ends[lb]; ++land; }
       }
+      if (!ok) break;  // a wait gave up: nothing further is issued
       const int cb = c & (kNBar - 1);
       ends[cb] = rp.pos;
       ChunkDesc dsc;
@@ -457,6 +582,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
       }
       ++c;
     }
+    // every copy this CTA issued lands before the producer (and with it the CTA) may
+    // finish, whether or not a wait gave up: the chunks not seen released, fewer than
+    // kNBar of them, each on its own barrier
+    for (int x = rel; x < c; ++x)
+      if (!mbar_wait(&full[x & (kNBar - 1)], (uint32_t)(x / kNBar) & 1u, a.err, a.wait_limit)) break;
     return;
   }
 
@@ -475,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
   BlockState<D, RT> bs;
   const uint32_t qrow = smem_u32(qsm + gq * (D + 8));  // this lane's query row (B fragments of q)
   __half* av = avw + warp * D;                         // this warp's copy of the block's a_v
-  alive = mbar_wait(qbar, 0u, a.err);
+  alive = __all_sync(0xffffffffu, mbar_wait(qbar, 0u, a.err, a.wait_limit));
   const int tid = threadIdx.x;
   if ((a.mode & kModeAll) && a.routed_out && range == 0)
     for (int j = tid; j < a.K_eff; j += kConsumers * 32) a.routed_out[(size_t)u * a.K_eff + j] = j;
@@ -486,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
   const int n_chunks = range_chunks(a, range);
   for (int c = 0; c < n_chunks; ++c) {
     const int bi = c & (kNBar - 1);
-    if (alive) alive = mbar_wait(&full[bi], (uint32_t)(c / kNBar) & 1u, a.err);
+    if (alive) alive = __all_sync(0xffffffffu, mbar_wait(&full[bi], (uint32_t)(c / kNBar) & 1u, a.err, a.wait_limit));
     const ChunkDesc ch = cdq[bi];  // kind, ring offset and tokens, from the producer
     const uint32_t sb = sbase + ch.off;
     const uint8_t* sp = smem + ch.off;
@@ -494,8 +624,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
       case kWin:
       case kRes: {
         const int in_g = max(0, min(16, ch.ntok - 16 * warp));
-        const uint32_t gb = sb + (uint32_t)(warp * 64 * D);
         const int nvalid = ch.kind == kWin ? L.W : L.R;
+        if (ch.kind == kRes && L.qbits) {  // quantised residual rows: whole 16-token groups
+          const uint32_t qg = sb + (uint32_t)(warp * L.qgb);
+          if (alive && in_g == 16 && L.qbits == 8)
+            exact_group_q<D, 8>(st, qrow, qg, ch.tok0 + 16 * warp, nvalid, slog2, gv0, gv1, lane);
+          else if (alive && in_g == 16)
+            exact_group_q<D, 4>(st, qrow, qg, ch.tok0 + 16 * warp, nvalid, slog2, gv0, gv1, lane);
+          break;
+        }
+        const uint32_t gb = sb + (uint32_t)(warp * 64 * D);
         if (alive && in_g == 16)
           exact_group<D, true>(st, qrow, gb, ch.tok0 + 16 * warp, nvalid, slog2, gv0, gv1, lane);
         else if (alive && in_g == 8)
@@ -760,7 +898,8 @@ uint64_t block_item_bytes(const Layout& L, int k) {  // k = 0: low-rank part; k 
   if (k == 0) return kLowRankWeight * (L.off_u + (L.off_res - L.off_u) + (L.block_bytes - L.off_vv));
   const int t0 = (k - 1) * kStageTok;
   const int n = L.R8 - t0 < kStageTok ? L.R8 - t0 : kStageTok;
-  return (uint64_t)n * 4 * L.d;
+  // quantised rows: their bytes, weighted 2x for the dequantisation in registers
+  return L.qbits ? (uint64_t)(n / 16) * L.qgb * 2 : (uint64_t)n * 4 * L.d;
 }
 
 // Cut one unit's work list into n_r ranges.  Every range starts with one
@@ -870,6 +1009,7 @@ AttendArgs make_args(const Layout& L, const DecodePlan& P, int n_q_heads, int n_
   // 64 KB in flight per CTA (about 19 MB over the grid) covers the memory latency at full
   // bandwidth; measured on GB300 against 16, 24, 40 KB and the whole ring (about 103 KB)
   a.inflight = a.ring < 65536 ? (uint32_t)a.ring : 65536u;
+  debug_limits(&a.stop_after, &a.wait_limit);
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)L.d);
   a.q = q;
   a.cache = cache;
@@ -882,6 +1022,19 @@ AttendArgs make_args(const Layout& L, const DecodePlan& P, int n_q_heads, int n_
 }
 
 }  // namespace
+
+namespace {
+std::atomic<int> g_stop_after{-1};
+std::atomic<uint32_t> g_wait_polls{kWaitLimit};
+}  // namespace
+void debug_limits(int* stop_after, uint32_t* wait_polls) {
+  *stop_after = g_stop_after.load(std::memory_order_relaxed);
+  *wait_polls = g_wait_polls.load(std::memory_order_relaxed);
+}
+void set_debug_limits(int stop_after, uint32_t wait_polls) {
+  g_stop_after.store(stop_after < 0 ? -1 : stop_after, std::memory_order_relaxed);
+  g_wait_polls.store(wait_polls ? wait_polls : kWaitLimit, std::memory_order_relaxed);
+}
 
 // Multiprocessors of the current device (cached per device; a host without a
 // usable device plans for 148).

@@ -309,6 +309,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm) attend_tc_kernel(TcA
       const uint64_t pol = policy_evict_first();
       int pos = 0;
       uint32_t eph = 0u, used = 0u;  // per unit: parity of its next release, filled at least once
+      // per unit whose full barrier a fill armed (the first unit of the fill's span): the parity
+      // of its next fill's phase and of its last one
+      uint32_t armed = 0u, fpar = 0u, lastf = 0u;
+      uint32_t qpar = 0u, qused = 0u;  // per query slot: parity of its last copy's phase, copied at least once
       bool waited = false;
       const uint32_t r8 = (uint32_t)L.r8;
       // claim s units starting at u (waiting for their previous contents to be released) and fill them
@@ -322,6 +326,9 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm) attend_tc_kernel(TcA
         }
         mbar_arrive_expect_tx(&sm.full[u], bytes);
         bulk_g2s(smem + (size_t)u * kUnit, src, bytes, &sm.full[u], pol);
+        lastf = (lastf & ~(1u << u)) | (fpar & (1u << u));
+        fpar ^= 1u << u;
+        armed |= 1u << u;
         return true;
       };
       for (int j = 0;; ++j) {
@@ -358,6 +365,8 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm) attend_tc_kernel(TcA
           const __half* qsrc = a.q + ((size_t)(it.u / a.Hkv) * a.Hq + (size_t)(it.u % a.Hkv) * a.G) * D;
           __half* qdst = reinterpret_cast<__half*>(smem + kOffQ) + (size_t)iq * 8 * 136;
           for (int g = 0; g < a.G; ++g) bulk_g2s(qdst + (size_t)g * 136, qsrc + (size_t)g * D, row, &sm.iq_full[iq], pol);
+          qpar = (qpar & ~(1u << iq)) | ((uint32_t)((j / kTcIQ) & 1) << iq);
+          qused |= 1u << iq;
         }
         const Places p = take_places(pos, it);
         const uint8_t* src = a.cache + it.base;
@@ -373,6 +382,12 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm) attend_tc_kernel(TcA
         if (ok && it.is_block) ok = put(p.vv, 1, src + L.off_vv, 256u * r8);
         if (!ok) break;
       }
+      // every copy this CTA issued lands before it may finish, whether or not a wait gave
+      // up: the last fill of every ring unit and the last query copy of every slot
+      for (int v = 0; v < kUnits; ++v)
+        if ((armed >> v) & 1u) mbar_wait(&sm.full[v], (lastf >> v) & 1u, a.err);
+      for (int q = 0; q < kTcIQ; ++q)
+        if ((qused >> q) & 1u) mbar_wait(&sm.iq_full[q], (qpar >> q) & 1u, a.err);
     }
     return;
   }

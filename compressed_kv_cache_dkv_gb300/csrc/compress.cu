@@ -496,12 +496,18 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
   const int nres = min(R, 255);
   uint16_t* cold = reinterpret_cast<uint16_t*>(unit + L.off_cold) + (size_t)blk * R8;
   for (int i = tid; i < R8; i += nt) cold[i] = i < nres ? (uint16_t)sel[i] : 0;
-  for (int e = tid; e < R8 * D; e += nt) {
-    const int i = e / D, j = e % D;
-    __half kv = __float2half(0.f), vv = kv;
-    if (i < nres) { kv = Kb[(size_t)sel[i] * D + j]; vv = Vb[(size_t)sel[i] * D + j]; }
-    *reinterpret_cast<__half*>(bp + blk_resk_off(L, i, j)) = kv;
-    *reinterpret_cast<__half*>(bp + blk_resv_off(L, i, j)) = vv;
+  if (L.qbits) {  // group-quantised residual rows (every thread of the CTA takes part)
+    write_quant_residuals(
+        L, bp + L.off_res, nres, [&](int i, int j) { return Kb[(size_t)sel[i] * D + j]; },
+        [&](int i, int j) { return Vb[(size_t)sel[i] * D + j]; });
+  } else {
+    for (int e = tid; e < R8 * D; e += nt) {
+      const int i = e / D, j = e % D;
+      __half kv = __float2half(0.f), vv = kv;
+      if (i < nres) { kv = Kb[(size_t)sel[i] * D + j]; vv = Vb[(size_t)sel[i] * D + j]; }
+      *reinterpret_cast<__half*>(bp + blk_resk_off(L, i, j)) = kv;
+      *reinterpret_cast<__half*>(bp + blk_resv_off(L, i, j)) = vv;
+    }
   }
   // ---- V_K (B^T layout) and V_V from W
   for (int e = tid; e < r8 * D; e += nt) {

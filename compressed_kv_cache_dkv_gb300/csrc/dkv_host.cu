@@ -55,6 +55,8 @@ bool make_layout(const dkv_desc* d, Layout* L) {
   L->NB = d->n_blocks;
   L->units = d->n_units;
   L->tc = d->layout == DKV_LAYOUT_TC ? 1 : 0;
+  L->qbits = d->residual_bits;
+  L->qgb = d->residual_bits ? (int)qgroup_bytes(d->head_dim, d->residual_bits) : 0;
   L->off_mask = d->blk_off_mask;
   L->off_vk = d->blk_off_vk;
   L->off_u = d->blk_off_u;
@@ -114,6 +116,7 @@ int dkv_layout(dkv_desc* d) {
       d->window_capacity < 0)
     return DKV_ERR_ARG;
   if (d->layout != DKV_LAYOUT_FRAGMENT && d->layout != DKV_LAYOUT_TC) return DKV_ERR_ARG;
+  if (d->residual_bits != 0 && d->residual_bits != 8 && d->residual_bits != 4) return DKV_ERR_ARG;
   if (d->n_q_heads % d->n_kv_heads != 0) return DKV_ERR_SHAPE;
   const int cap_b = d->block_capacity ? d->block_capacity : d->n_blocks;
   const int cap_w = d->window_capacity ? d->window_capacity : d->window;
@@ -128,7 +131,10 @@ int dkv_layout(dkv_desc* d) {
   if (cap_b > 2048 || cap_w > 65536) return DKV_ERR_UNSUPPORTED;
   const uint64_t dd = (uint64_t)d->head_dim;
   const int r8 = (d->rank + 7) / 8 * 8;
-  const int R8 = (d->n_residual + 7) / 8 * 8;
+  const int rq = d->residual_bits;
+  if (rq && d->layout == DKV_LAYOUT_TC) return DKV_ERR_UNSUPPORTED;
+  const int R8 = rq ? (d->n_residual + 15) / 16 * 16 : (d->n_residual + 7) / 8 * 8;
+  const uint64_t res_bytes = rq ? (uint64_t)(R8 / 16) * qgroup_bytes(d->head_dim, rq) : 4ull * R8 * dd;
   const int W16 = (d->window + 15) / 16 * 16;
   d->rank_pad = r8;
   d->res_pad = R8;
@@ -148,7 +154,7 @@ int dkv_layout(dkv_desc* d) {
     d->blk_off_vk = 4 * dd + 32;
     d->blk_off_u = d->blk_off_vk + 2ull * r8 * dd;
     d->blk_off_res = d->blk_off_u + 2ull * 256 * r8;
-    d->blk_off_vv = d->blk_off_res + 4ull * R8 * dd;
+    d->blk_off_vv = d->blk_off_res + res_bytes;
     d->block_bytes = d->blk_off_vv + 2ull * r8 * dd;
   }
   d->block_stride = round_up(d->block_bytes, 128);
@@ -380,6 +386,11 @@ int dkv_dense_decode(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32
                                static_cast<const __half*>(K), static_cast<const __half*>(V), out, lse, ws,
                                reinterpret_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
+}
+
+int dkv_debug_set_limits(int32_t stop_after_chunks, uint32_t wait_polls) {
+  set_debug_limits(stop_after_chunks, wait_polls);
+  return DKV_OK;
 }
 
 int dkv_get_error(void* workspace, void* stream, uint32_t* word) {

@@ -40,11 +40,91 @@ namespace dkv {
 struct Layout {
   int d, r, r8, R, R8, W, W16, NB, units;
   int tc;              // 1: tensor-core (core-matrix) layout, 0: mma.sync fragment layout
+  int qbits;           // residual rows: 0 fp16, 8 or 4 group-quantised (fragment layout)
+  int qgb;             // bytes of one 16-token group of quantised residual rows (0 for fp16)
   uint64_t off_mask, off_vk, off_u, off_res, off_vv, block_bytes;
   uint64_t off_router, off_blocks, off_cold, off_window, block_stride, unit_stride, total;
 };
 
 __host__ __device__ inline uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------
+// Group-quantised residual rows (Layout.qbits = 8 or 4; fragment layout).  The
+// residual rows are stored in 16-token groups (R padded to 16); one group is
+//   [K codes: 16 tokens x d][V^T codes: d x 16 tokens]
+//   [K scale: G x 16][K bias: G x 16][V scale: G x 16][V bias: G x 16]   fp16, G = d / 64
+// Each code section is in the A-fragment order of mma.sync m16n8k16 per 16-wide
+// k tile (K: rows = tokens, k = channels; V^T: rows = channels, k = tokens): per
+// 512-byte chunk and lane 16 bytes, a chunk holding two k tiles (int8) or four
+// (int4).  For the fragment registers a0..a3 of one k tile (two halves x, y each):
+//   int8: two words, (a0.x, a1.x, a0.y, a1.y) and (a2.x, a3.x, a2.y, a3.y) as bytes
+//   int4: one word, bits 4i..4i+3 = a_i.x and bits 16+4i..16+4i+3 = a_i.y
+// so ((word >> s) & 0x00FF00FF) | 0x64006400 (int8; 0x000F000F for int4) is the
+// half2 (1024 + code x, 1024 + code y) of one register, exactly.
+// ---------------------------------------------------------------------------
+constexpr int kQuantGroup = 64;  // channels per scale and bias
+__host__ __device__ inline uint32_t qcode_bytes(int d, int bits) { return 16u * (uint32_t)d * (uint32_t)bits / 8u; }
+__host__ __device__ inline uint32_t qgroup_bytes(int d, int bits) {
+  return 2u * qcode_bytes(d, bits) + 128u * (uint32_t)(d / kQuantGroup);
+}
+
+// Write residual rows 0 .. n-1 of one block into its quantised residual store
+// `res` (the rows n .. R8-1 of the padding get scale and bias 0 and code 0).
+// src_k(i, j) / src_v(i, j) return channel j of residual row i as fp16.  Called by
+// every thread of the CTA (it synchronises the CTA once): first the scale and bias
+// of every (row, key or value, channel group), then every 32-bit code word, each
+// written by one thread.
+template <class FK, class FV>
+__device__ void write_quant_residuals(const Layout& L, uint8_t* res, int n, FK src_k, FV src_v) {
+  const int d = L.d, bits = L.qbits, G = d / kQuantGroup, levels = (1 << bits) - 1;
+  const uint32_t cb = qcode_bytes(d, bits), gb = (uint32_t)L.qgb;
+  for (int e = threadIdx.x; e < L.R8 * 2 * G; e += blockDim.x) {
+    const int i = e / (2 * G), kv = (e / G) & 1, g = e % G;
+    __half sh = __float2half(0.f), bh = __float2half(0.f);
+    if (i < n) {
+      float lo = INFINITY, hi = -INFINITY;
+      for (int c = 0; c < kQuantGroup; ++c) {
+        const float x = __half2float(kv ? src_v(i, g * kQuantGroup + c) : src_k(i, g * kQuantGroup + c));
+        lo = fminf(lo, x);
+        hi = fmaxf(hi, x);
+      }
+      sh = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), (float)levels));
+      bh = __float2half_rn(lo);  // exact: the minimum is one of the fp16 values
+    }
+    __half* sc = reinterpret_cast<__half*>(res + (uint64_t)(i / 16) * gb + 2 * cb + (uint32_t)kv * 64u * G);
+    sc[g * 16 + (i & 15)] = sh;
+    sc[16 * G + g * 16 + (i & 15)] = bh;
+  }
+  __syncthreads();
+  const uint32_t words = cb / 4, ngrp = (uint32_t)L.R8 / 16;
+  for (uint32_t e = threadIdx.x; e < ngrp * 2 * words; e += blockDim.x) {
+    const uint32_t grp = e / (2 * words), kv = (e / words) & 1u, w = e % words;
+    const int chunk = (int)(w / 128), lane = (int)((w % 128) / 4), wi = (int)(w % 4);
+    const int gq = lane >> 2, t = lane & 3;
+    const __half* sc = reinterpret_cast<const __half*>(res + (uint64_t)grp * gb + 2 * cb + kv * 64u * G);
+    uint32_t word = 0;
+    const int ne = bits == 8 ? 4 : 8;
+    for (int x = 0; x < ne; ++x) {
+      int tile, ai, ex, shift;
+      if (bits == 8) { tile = 2 * chunk + (wi >> 1); ai = 2 * (wi & 1) + (x & 1); ex = x >> 1; shift = 8 * x; }
+      else { tile = 4 * chunk + wi; ai = x & 3; ex = x >> 2; shift = 4 * x; }
+      const int r = gq + 8 * (ai & 1), c = 2 * t + ex + 8 * (ai >> 1);  // row and column inside the tile
+      const int tok = 16 * (int)grp + (kv ? c : r), ch = 16 * tile + (kv ? r : c);
+      uint32_t code = 0;
+      if (tok < n) {
+        const int g = ch / kQuantGroup;
+        const float s = __half2float(sc[g * 16 + (tok & 15)]), b = __half2float(sc[16 * G + g * 16 + (tok & 15)]);
+        if (s != 0.f) {
+          const float xv = __half2float(kv ? src_v(tok, ch) : src_k(tok, ch));
+          const float qv = rintf(__fdiv_rn(__fsub_rn(xv, b), s));
+          code = (uint32_t)fminf(fmaxf(qv, 0.f), (float)levels);
+        }
+      }
+      word |= code << shift;
+    }
+    *reinterpret_cast<uint32_t*>(res + (uint64_t)grp * gb + kv * cb + w * 4) = word;
+  }
+}
 
 // ---------------------------------------------------------------------------
 // Tensor-core layout (head_dim 128, 8 <= r8 <= 48, 1 <= R <= 128).  Operand
@@ -201,8 +281,8 @@ __device__ inline bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait: gives up after kWaitLimit steps (at most ~1.3 s), raises
 // DKV_DEVERR_TIMEOUT and returns false.
 constexpr uint32_t kWaitLimit = 1u << 16;
-__device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+__device__ inline bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   raise_error(err, DKV_DEVERR_TIMEOUT);
   return false;
@@ -357,6 +437,10 @@ cudaError_t launch_attend_tc(const Layout& L, const DecodePlan& P, int n_q_heads
 cudaError_t launch_combine_records(int units, int n_items, int n_q_heads, int n_kv_heads, int d,
                                    const float* partials, float* out, float* lse, cudaStream_t s);
 int sm_count();  // multiprocessors of the current device
+// Diagnostic limits of the fragment-layout attention kernel (dkv_debug_set_limits):
+// chunks a CTA's producer issues at most (negative: all) and polls of a bounded wait.
+void debug_limits(int* stop_after, uint32_t* wait_polls);
+void set_debug_limits(int stop_after, uint32_t wait_polls);
 // Raise `func`'s dynamic shared-memory limit to at least `bytes` on the current
 // device: once per (kernel, device), again only when a larger size is asked for.
 // Thread-safe.

@@ -78,16 +78,22 @@ __global__ void __launch_bounds__(256) pack_kernel(Layout L, dkv_factors f, uint
     __half v = (t >= 1 && k < r) ? ld_h(f.U, (base * 255 + (t - 1)) * r + k) : zero;
     *reinterpret_cast<__half*>(blk + blk_u_off(L, t, k)) = v;
   }
-  // residual K and V
-  for (int e = tid; e < R8 * d; e += nt) {
-    int i = e / d, j = e % d;
-    __half kv = zero, vv = zero;
-    if (i < R) {
-      kv = ld_h(f.K_res, (base * R + i) * d + j);
-      vv = ld_h(f.V_res, (base * R + i) * d + j);
+  // residual K and V (group-quantised when the layout asks for it; every thread takes part)
+  if (L.qbits) {
+    write_quant_residuals(
+        L, blk + L.off_res, R, [&](int i, int j) { return ld_h(f.K_res, (base * R + i) * d + j); },
+        [&](int i, int j) { return ld_h(f.V_res, (base * R + i) * d + j); });
+  } else {
+    for (int e = tid; e < R8 * d; e += nt) {
+      int i = e / d, j = e % d;
+      __half kv = zero, vv = zero;
+      if (i < R) {
+        kv = ld_h(f.K_res, (base * R + i) * d + j);
+        vv = ld_h(f.V_res, (base * R + i) * d + j);
+      }
+      *reinterpret_cast<__half*>(blk + blk_resk_off(L, i, j)) = kv;
+      *reinterpret_cast<__half*>(blk + blk_resv_off(L, i, j)) = vv;
     }
-    *reinterpret_cast<__half*>(blk + blk_resk_off(L, i, j)) = kv;
-    *reinterpret_cast<__half*>(blk + blk_resv_off(L, i, j)) = vv;
   }
   // V_V [r8][d]
   for (int e = tid; e < r8 * d; e += nt) {

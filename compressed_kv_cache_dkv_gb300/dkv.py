@@ -40,7 +40,7 @@ EXPORTED = (
     "dkv_decode_workspace_bytes", "dkv_decode_launches", "dkv_decode_attend", "dkv_decode_route", "dkv_decode_blocks",
     "dkv_decode_combine",
     "dkv_dense_workspace_bytes", "dkv_dense_decode", "dkv_get_error", "dkv_decode_attend_noalloc",
-    "dkv_append_workspace_bytes", "dkv_append",
+    "dkv_append_workspace_bytes", "dkv_append", "dkv_debug_set_limits",
 )
 
 
@@ -53,7 +53,8 @@ class DkvError(RuntimeError):
 class dkv_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "n_q_heads", "n_kv_heads", "head_dim", "block_size", "n_blocks", "window", "rank",
-        "n_residual", "layout", "block_capacity", "window_capacity", "rank_pad", "res_pad", "window_pad", "n_units")] + [
+        "n_residual", "layout", "block_capacity", "window_capacity", "residual_bits", "rank_pad", "res_pad",
+        "window_pad", "n_units")] + [
         (n, ctypes.c_uint64) for n in (
             "blk_off_mask", "blk_off_vk", "blk_off_u", "blk_off_res", "blk_off_vv", "block_bytes",
             "off_router", "off_blocks", "off_cold", "off_window", "block_stride", "unit_stride", "total_bytes")]
@@ -106,6 +107,7 @@ def lib() -> ctypes.CDLL:
         L.dkv_append_workspace_bytes.restype = sz
         L.dkv_append_workspace_bytes.argtypes = [pdesc]
         L.dkv_append.argtypes = [pdesc, vp, vp, i32, vp, vp, sz, vp]
+        L.dkv_debug_set_limits.argtypes = [i32, ctypes.c_uint32]
         _lib = L
     return _lib
 
@@ -137,14 +139,16 @@ def _stream(stream) -> int | None:
 
 def dkv_layout(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int, n_blocks: int, window: int,
                rank: int, n_residual: int, block_size: int = BLOCK_SIZE,
-               layout: int | None = None, block_capacity: int = 0, window_capacity: int = 0) -> dkv_desc:
+               layout: int | None = None, block_capacity: int = 0, window_capacity: int = 0,
+               residual_bits: int = 0) -> dkv_desc:
     """Fill a descriptor.  `layout` is DKV_LAYOUT_FRAGMENT (mma.sync decode kernel, the
     default) or DKV_LAYOUT_TC (tcgen05 decode kernel; head_dim 128, rank <= 48, 1 <= R <= 128).
-    `block_capacity` / `window_capacity` reserve room for dkv_append (0: the live counts)."""
+    `block_capacity` / `window_capacity` reserve room for dkv_append (0: the live counts).
+    `residual_bits` 0 keeps residual rows fp16; 8 or 4 stores them group-quantised."""
     d = dkv_desc(batch=batch, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim=head_dim,
                  block_size=block_size, n_blocks=n_blocks, window=window, rank=rank, n_residual=n_residual,
                  layout=DKV_LAYOUT_FRAGMENT if layout is None else layout,
-                 block_capacity=block_capacity, window_capacity=window_capacity)
+                 block_capacity=block_capacity, window_capacity=window_capacity, residual_bits=residual_bits)
     _check(lib().dkv_layout(ctypes.byref(d)), "dkv_layout")
     return d
 
@@ -284,6 +288,13 @@ def dkv_dense_decode(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, out: tor
     _check(lib().dkv_dense_decode(B, Hq, Hkv, dh, T, _ptr(q), _ptr(K), _ptr(V), _ptr(out), _ptr(lse),
                                   _ptr(workspace), workspace.numel(), _stream(stream)), "dkv_dense_decode")
     return out, lse
+
+
+def dkv_debug_set_limits(stop_after_chunks: int = -1, wait_polls: int = 0) -> None:
+    """Failure-path diagnostics: producers of the fragment layout's attention CTAs stop
+    after `stop_after_chunks` chunks, bounded waits give up after `wait_polls` polls;
+    (-1, 0) restores the defaults."""
+    _check(lib().dkv_debug_set_limits(int(stop_after_chunks), int(wait_polls)), "dkv_debug_set_limits")
 
 
 def dkv_get_error(workspace: torch.Tensor, stream=None) -> tuple[int, int]:

@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define DKV_VERSION 3
+#define DKV_VERSION 4
 
 #if defined(__GNUC__)
 #define DKV_API __attribute__((visibility("default")))
@@ -79,9 +79,9 @@ extern "C" {
                                    head_dim 128, 1 <= rank <= 48, 1 <= n_residual <= 128 */
 
 /*
- * Descriptor of one layer's compressed cache.  The caller sets the first twelve
- * fields; dkv_layout() validates them and fills the rest.  Plain old data:
- * pass it by pointer, copy it freely.
+ * Descriptor of one layer's compressed cache.  The caller sets the first
+ * thirteen fields; dkv_layout() validates them and fills the rest.  Plain old
+ * data: pass it by pointer, copy it freely.
  *
  * Supported: head_dim 64 or 128; 1 <= n_q_heads/n_kv_heads <= 8; block_size
  * 256; 0 <= rank <= 128; 0 <= n_residual <= 255; 0 <= n_blocks <= 2048;
@@ -95,6 +95,18 @@ extern "C" {
  * block_capacity and window_capacity, so a cache keeps its offsets while
  * dkv_append() grows n_blocks and moves the window (0 means "no spare room").
  * Capacities obey the same limits as the counts (2048 blocks, 65536 tokens).
+ *
+ * residual_bits picks how the R exact residual rows are stored ([README Innov]
+ * "Physical 4-Bit Group-Quantized Residual Buffers"; [README Knobs]
+ * DKV_RESIDUAL_QUANT, DKV_RESIDUAL_QUANT_GROUP_SIZE): 0 keeps them as fp16; 8
+ * or 4 stores each key row and each value row group-quantised: per 64
+ * channels an fp16 bias (the group's minimum) and an fp16 scale ((maximum -
+ * minimum) / (2^bits - 1)), and per channel the code round((x - bias) /
+ * scale) clamped to [0, 2^bits - 1] (taken in fp32, ties to even; a group of
+ * equal values has scale 0 and codes 0).  The decode attends the dequantised
+ * rows scale * code + bias, rounded to fp16 (the operand precision).  Only the
+ * fragment layout, and head_dim 64 or 128, take quantised residuals; R is then
+ * padded to a multiple of 16.
  */
 typedef struct dkv_desc {
   int32_t batch;        /* sequences B */
@@ -109,9 +121,10 @@ typedef struct dkv_desc {
   int32_t layout;       /* DKV_LAYOUT_FRAGMENT (0) or DKV_LAYOUT_TC (1) */
   int32_t block_capacity;   /* blocks the cache has room for (0: n_blocks); >= n_blocks */
   int32_t window_capacity;  /* window token slots (0: window); >= window */
+  int32_t residual_bits;    /* 0: fp16 residual rows; 8 or 4: group-quantised (see above) */
   /* ---- filled by dkv_layout() ---- */
   int32_t rank_pad;     /* r rounded up to a multiple of 8 (zero-padded) */
-  int32_t res_pad;      /* R rounded up to a multiple of 8 (zero-padded) */
+  int32_t res_pad;      /* R rounded up to a multiple of 8 (16 when quantised; zero-padded) */
   int32_t window_pad;   /* W rounded up to a multiple of 16 (zero-padded) */
   int32_t n_units;      /* B * Hkv */
   /* byte offsets inside one block record */
@@ -317,6 +330,21 @@ DKV_API size_t dkv_dense_workspace_bytes(int32_t batch, int32_t n_q_heads, int32
 DKV_API int dkv_dense_decode(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t T,
                      const void* q, const void* K, const void* V, float* out, float* lse,
                      void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Diagnostics for the failure path (no counterpart in the pages): from the
+ * next launch on, the producer of every attention CTA of the fragment layout
+ * issues at most `stop_after_chunks` chunks (negative: all of them) and every
+ * bounded device wait of that kernel gives up after `wait_polls` polls of at
+ * most about 20 us each (0: the default limit, about 1.3 s).  A stopped
+ * producer leaves its consumer warps waiting for data that never comes: their
+ * waits give up, DKV_DEVERR_TIMEOUT is raised in the error word and the
+ * outputs of the call are meaningless; every copy that was issued has landed
+ * before the kernel ends, so the context stays usable.  The setting is
+ * process-wide; dkv_debug_set_limits(-1, 0) restores the defaults.  Returns
+ * DKV_OK.
+ */
+DKV_API int dkv_debug_set_limits(int32_t stop_after_chunks, uint32_t wait_polls);
 
 /*
  * Synchronise `stream`, read the device error word kept in the header of

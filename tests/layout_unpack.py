@@ -72,6 +72,39 @@ def u_index(r8: int) -> np.ndarray:
     return byte // 2
 
 
+def quant_residuals(raw: np.ndarray, n_rows: int, R16: int, d: int, bits: int) -> dict:
+    """Codes, fp16 scale and bias of the K and V rows of a block's group-quantised
+    residual store (16-token groups: K codes, V^T codes in mma A-fragment order,
+    then K scale, K bias, V scale, V bias [d/64][16] fp16), from its raw bytes."""
+    G = d // 64
+    cb = 16 * d * bits // 8
+    gb = 2 * cb + 128 * G
+    out = {k: np.zeros((R16, d), np.uint8) for k in ("K_codes", "V_codes")}
+    for k in ("K_scale", "K_bias", "V_scale", "V_bias"):
+        out[k] = np.zeros((R16, G), np.float16)
+    for grp in range(R16 // 16):
+        base = grp * gb
+        for kv, name in ((0, "K"), (1, "V")):
+            words = raw[base + kv * cb: base + (kv + 1) * cb].view(np.uint32)
+            for w, word in enumerate(words):
+                chunk, lane, wi = w // 128, (w % 128) // 4, w % 4
+                gq, t = lane // 4, lane % 4
+                for x in range(4 if bits == 8 else 8):
+                    if bits == 8:
+                        tile, ai, ex, sh, mask = 2 * chunk + wi // 2, 2 * (wi % 2) + x % 2, x // 2, 8 * x, 0xFF
+                    else:
+                        tile, ai, ex, sh, mask = 4 * chunk + wi, x % 4, x // 4, 4 * x, 0xF
+                    r, c = gq + 8 * (ai % 2), 2 * t + ex + 8 * (ai // 2)
+                    tok, ch = (16 * grp + r, 16 * tile + c) if kv == 0 else (16 * grp + c, 16 * tile + r)
+                    out[name + "_codes"][tok, ch] = (int(word) >> sh) & mask
+            sc = raw[base + 2 * cb + kv * 64 * G: base + 2 * cb + (kv + 1) * 64 * G].view(np.float16)
+            out[name + "_scale"][16 * grp:16 * grp + 16] = sc[:16 * G].reshape(G, 16).T
+            out[name + "_bias"][16 * grp:16 * grp + 16] = sc[16 * G:].reshape(G, 16).T
+    for k in list(out):
+        out[k] = out[k][:n_rows] if k.endswith(("codes", "scale", "bias")) else out[k]
+    return out
+
+
 def unpack_block(cache: np.ndarray, desc, u: int, b: int) -> dict:
     d, r, r8, R, R8 = desc.head_dim, desc.rank, desc.rank_pad, desc.n_residual, desc.res_pad
     unit = u * desc.unit_stride
@@ -89,15 +122,27 @@ def unpack_block(cache: np.ndarray, desc, u: int, b: int) -> dict:
     Ufull = uu[u_index(r8)]  # both layouts store U as 8 x 8 core matrices
     out["U_row0"] = Ufull[0].copy()
     out["U"] = Ufull[1:, :r].copy()
-    res = h(blk + desc.blk_off_res, 2 * R8 * d)
-    if tc:
+    if desc.residual_bits:
+        q = quant_residuals(cache[blk + desc.blk_off_res: blk + desc.blk_off_vv], R, R8, d, desc.residual_bits)
+        out.update(q)
+        deq = lambda c, s, bb: (c.astype(np.float64).reshape(R, d // 64, 64) * s.astype(np.float64)[:, :, None]
+                                + bb.astype(np.float64)[:, :, None]).reshape(R, d)
+        out["K_res"] = deq(q["K_codes"], q["K_scale"], q["K_bias"])
+        out["V_res"] = deq(q["V_codes"], q["V_scale"], q["V_bias"])
+        res = None
+    else:
+        res = h(blk + desc.blk_off_res, 2 * R8 * d)
+    if res is None:
+        pass
+    elif tc:
         ki = rd_index(R8, d)
         vi = R8 * d + ki
     else:
         ki, vi = exact_index(R8, d)
-    out["K_res"] = res[ki][:R].copy()
-    out["V_res"] = res[vi][:R].copy()
-    out["res_pad_zero"] = bool((res[ki][R:] == 0).all() and (res[vi][R:] == 0).all())
+    if res is not None:
+        out["K_res"] = res[ki][:R].copy()
+        out["V_res"] = res[vi][:R].copy()
+        out["res_pad_zero"] = bool((res[ki][R:] == 0).all() and (res[vi][R:] == 0).all())
     vv = h(blk + desc.blk_off_vv, r8 * d)
     out["V_V"] = (vv[rd_index(r8, d)] if tc else vv[a_layout_index(d, r8)].T)[:r].copy()
     router = h(unit + desc.off_router + b * 4 * d, 2 * d)

@@ -24,7 +24,7 @@ def test_library_exports_every_declared_symbol():
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(dkv.EXPORTED)
-    assert lib.dkv_version() == 3
+    assert lib.dkv_version() == 4
 
 
 def test_status_strings():
@@ -47,6 +47,9 @@ def test_layout_validation():
         (dict(layout=1, head_dim=64), dkv.DKV_ERR_UNSUPPORTED), (dict(layout=1, rank=49), dkv.DKV_ERR_UNSUPPORTED),
         (dict(layout=1, rank=0), dkv.DKV_ERR_UNSUPPORTED), (dict(layout=1, n_residual=0), dkv.DKV_ERR_UNSUPPORTED),
         (dict(layout=1, n_residual=129), dkv.DKV_ERR_UNSUPPORTED),
+        # group-quantised residual rows: 8 or 4 bits, fragment layout only
+        (dict(residual_bits=2), dkv.DKV_ERR_ARG), (dict(residual_bits=16), dkv.DKV_ERR_ARG),
+        (dict(residual_bits=-8), dkv.DKV_ERR_ARG), (dict(layout=1, residual_bits=8), dkv.DKV_ERR_UNSUPPORTED),
     ]
     for change, status in bad:
         kw = dict(ok, **change)
@@ -170,3 +173,21 @@ def test_decode_launch_counts():
     assert [dkv.dkv_decode_launches(tc, k) for k in (8, 0, 30)] == [3, 3, 3]  # the tc path always routes
     tc_empty = dkv.dkv_layout(2, 12, 2, 128, 0, 512, 32, 40, layout=dkv.DKV_LAYOUT_TC)
     assert [dkv.dkv_decode_launches(tc_empty, k) for k in (0, 4)] == [2, 2]
+
+
+@pytest.mark.parametrize("d,R,bits", [(128, 40, 8), (128, 128, 4), (64, 16, 8), (64, 5, 4), (128, 255, 8), (128, 0, 4)])
+def test_quantised_residual_layout_bytes(d, R, bits):
+    """A group-quantised residual store holds R rounded up to 16 rows in 16-token groups
+    of K and V codes plus one fp16 scale and bias per 64 channels of every row; the
+    other sections are those of the fp16 layout."""
+    desc = dkv.dkv_layout(2, 6, 2, d, 7, 100, 24, R, residual_bits=bits)
+    plain = dkv.dkv_layout(2, 6, 2, d, 7, 100, 24, R)
+    R16 = -(-R // 16) * 16
+    assert desc.res_pad == R16 and desc.residual_bits == bits
+    group = 2 * 16 * d * bits // 8 + 4 * 16 * 2 * (d // 64)
+    assert desc.blk_off_vv - desc.blk_off_res == R16 // 16 * group
+    assert desc.block_bytes - desc.blk_off_vv == plain.block_bytes - plain.blk_off_vv
+    assert desc.blk_off_res == plain.blk_off_res
+    for off in (desc.blk_off_vv, desc.block_stride, desc.off_window, desc.unit_stride):
+        assert off % 16 == 0
+    assert desc.block_bytes < plain.block_bytes or R == 0

@@ -37,12 +37,24 @@ def _expected_counts(T, cap_w):
     (128, 48, 5, 3, 256, 100, [156, 1, 255, 3]),                # capacity of exactly one block
 ])
 def test_append_equals_batch_compression(d, r, R, cap_b, cap_w, T0, chunks):
+    _append_vs_batch(d, r, R, cap_b, cap_w, T0, chunks, 0)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_append_with_quantised_residuals_equals_batch_compression(bits):
+    """The same byte identity when the residual rows are stored group-quantised."""
+    _append_vs_batch(128, 24, 40, 6, 600, 856, [1, 7, 36, 1, 300, 256, 5], bits)
+    _append_vs_batch(64, 8, 16, 4, 300, 300, [1, 1, 254, 300], bits)
+
+
+def _append_vs_batch(d, r, R, cap_b, cap_w, T0, chunks, bits):
     B, Hq, Hkv = 2, 6, 2
     T = T0 + sum(chunks)
     K, V, _ = _tokens(B, Hq, Hkv, d, T, r, R, 321 + T)
     Kd, Vd = torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda()
     nb0, w0 = _expected_counts(T0, cap_w)
-    desc = dkv.dkv_layout(B, Hq, Hkv, d, nb0, w0, r, R, block_capacity=cap_b, window_capacity=cap_w)
+    desc = dkv.dkv_layout(B, Hq, Hkv, d, nb0, w0, r, R, block_capacity=cap_b, window_capacity=cap_w,
+                          residual_bits=bits)
     ws = torch.zeros(max(dkv.dkv_append_workspace_bytes(desc), dkv.dkv_compress_workspace_bytes(desc), 256),
                      dtype=torch.uint8, device="cuda")
     cache = torch.empty(desc.total_bytes, dtype=torch.uint8, device="cuda")
@@ -60,7 +72,7 @@ def test_append_equals_batch_compression(d, r, R, cap_b, cap_w, T0, chunks):
     st, word = dkv.dkv_get_error(ws)
     assert st == dkv.DKV_OK, f"device error word {word:#x}"
     ref_desc = dkv.dkv_layout(B, Hq, Hkv, d, desc.n_blocks, desc.window, r, R, block_capacity=cap_b,
-                              window_capacity=cap_w)
+                              window_capacity=cap_w, residual_bits=bits)
     assert bytes(ref_desc) == bytes(desc)
     ref = dkv.dkv_compress_layout(ref_desc, Kd, Vd, workspace=ws)
     torch.cuda.synchronize()
