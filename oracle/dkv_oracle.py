@@ -449,6 +449,83 @@ def quant_residual_row_bytes(d: int, bits: int, group: int = RESIDUAL_QUANT_GROU
 
 
 # ---------------------------------------------------------------------------
+# block-sparse prefill
+# ---------------------------------------------------------------------------
+
+def prefill_routes(Q: np.ndarray, K: np.ndarray, top_k: int) -> list:
+    """Blocks each query block attends beside its own, for one unit ([DKV-Z]:
+    "Prefill uses training-free block-sparse attention, so its cost grows
+    sub-quadratically"; [README Core] "Sub-Quadratic Prefill": O(L^2) down to
+    O(L * K)).  Q [G, T, d] are the GQA group's queries, K [T, d] the exact keys.
+
+    Query block i (tokens 256 i .. 256 i + 255, the last one possibly shorter)
+    scores every earlier key block j < i with the key-box bound of the decode
+    router, taken with the block's mean query: qbar_i = mean over the block's
+    tokens and the group's heads of c q, c = 1/sqrt(d), and
+        bound_ij = sum_d max(qbar_id kmax_jd, qbar_id kmin_jd)
+    over the channel extremes of block j's 256 keys; it keeps the top_k blocks
+    by (bound desc, j asc), every earlier block when top_k is 0 or >= i.
+    Returns, per query block, (routed blocks ascending, bounds [i]).
+    """
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    G, T, d = Q.shape
+    nb = -(-T // BLOCK_SIZE)
+    out = []
+    for i in range(nb):
+        t0, t1 = i * BLOCK_SIZE, min(T, (i + 1) * BLOCK_SIZE)
+        qbar = (Q[:, t0:t1, :] / math.sqrt(d)).mean(axis=(0, 1))
+        bounds = np.array([np.maximum(qbar * K[j * BLOCK_SIZE:(j + 1) * BLOCK_SIZE].max(axis=0),
+                                      qbar * K[j * BLOCK_SIZE:(j + 1) * BLOCK_SIZE].min(axis=0)).sum()
+                           for j in range(i)])
+        k = i if (top_k == 0 or top_k >= i) else int(top_k)
+        order = sorted(range(i), key=lambda j: (-float(bounds[j]), j))[:k]
+        out.append((np.array(sorted(order), dtype=np.int64), bounds))
+    return out
+
+
+def prefill_unit(Q: np.ndarray, K: np.ndarray, V: np.ndarray, top_k: int) -> dict:
+    """Block-sparse prefill attention of one unit, by definition: the query at
+    token t of query block i attends the keys of its own block up to t (causal)
+    and every key of the blocks ``prefill_routes`` gives block i; one softmax of
+    c q . k over that set.  Returns o [G, T, d], lse [G, T] and the routes."""
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    G, T, d = Q.shape
+    routes = prefill_routes(Q, K, top_k)
+    o = np.zeros((G, T, d))
+    lse = np.zeros((G, T))
+    for i, (idx, _) in enumerate(routes):
+        t0, t1 = i * BLOCK_SIZE, min(T, (i + 1) * BLOCK_SIZE)
+        keys = np.concatenate([np.arange(j * BLOCK_SIZE, (j + 1) * BLOCK_SIZE) for j in idx] +
+                              [np.arange(t0, t1)]).astype(np.int64)
+        s = np.einsum("gtd,kd->gtk", Q[:, t0:t1, :], K[keys]) / math.sqrt(d)
+        own = keys >= t0
+        causal = keys[None, :] > np.arange(t0, t1)[:, None]  # a key after the query
+        s = np.where((own[None, :] & causal)[None, :, :], -np.inf, s)
+        m = s.max(axis=2, keepdims=True)
+        e = np.exp(s - m)
+        l = e.sum(axis=2, keepdims=True)
+        o[:, t0:t1, :] = np.einsum("gtk,kd->gtd", e, V[keys]) / l
+        lse[:, t0:t1] = (m + np.log(l))[:, :, 0]
+    return {"o": o, "lse": lse, "routes": [r for r, _ in routes], "bounds": [b for _, b in routes]}
+
+
+def prefill_pairs(T: int, top_k: int) -> int:
+    """(query, key) pairs block-sparse prefill scores for one query head: per query
+    block its own causal triangle plus 256 keys of each routed earlier block; the
+    cost the pages call O(L * K)."""
+    nb = -(-T // BLOCK_SIZE)
+    pairs = 0
+    for i in range(nb):
+        n = min(T, (i + 1) * BLOCK_SIZE) - i * BLOCK_SIZE
+        k = i if (top_k == 0 or top_k >= i) else top_k
+        pairs += n * (n + 1) // 2 + n * k * BLOCK_SIZE
+    return pairs
+
+
+# ---------------------------------------------------------------------------
 # byte accounting
 # ---------------------------------------------------------------------------
 

@@ -59,7 +59,8 @@ _orig = {n: getattr(O, n) for n in ("router_bounds", "route", "select_residuals"
                                     "decode_unit", "append_tokens", "effective_top_k", "compress_unit",
                                     "decode_unit_factored", "_part", "pages_block_bytes", "residual_row_bytes",
                                     "dense_kv_bytes", "quantize_groups", "dequantize_groups",
-                                    "quantize_block_residuals", "quant_residual_row_bytes")}
+                                    "quantize_block_residuals", "quant_residual_row_bytes", "prefill_routes",
+                                    "prefill_unit", "prefill_pairs")}
 
 
 def _bounds_without_kmin(q, kmin, kmax):
@@ -301,7 +302,68 @@ def _quant_block_keys_only(blk, bits):
     return dataclasses.replace(blk, K_res=O.dequantize_groups(*O.quantize_groups(blk.K_res, bits)))
 
 
+def _prefill_routes(Q, K, top_k, mean=True, use_min=True, later=False, zero_is_none=False):
+    """prefill_routes with one slip."""
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    G, T, d = Q.shape
+    nb = -(-T // BS)
+    out = []
+    for i in range(nb):
+        t0, t1 = i * BS, min(T, (i + 1) * BS)
+        qbar = (Q[:, t0:t1, :] / math.sqrt(d)).mean(axis=(0, 1)) if mean else Q[0, t0] / math.sqrt(d)
+        cand = [j for j in range(nb) if j != i] if later else list(range(i))
+        b = {}
+        for j in cand:
+            blk = K[j * BS:min(T, (j + 1) * BS)]
+            b[j] = (np.maximum(qbar * blk.max(axis=0), qbar * blk.min(axis=0)) if use_min else qbar * blk.max(axis=0)).sum()
+        k = len(cand) if (top_k >= len(cand) or (top_k == 0 and not zero_is_none)) else int(top_k)
+        order = sorted(cand, key=lambda j: (-float(b[j]), j))[:k]
+        out.append((np.array(sorted(order), dtype=np.int64), np.array([b.get(j, 0.0) for j in range(i)])))
+    return out
+
+
+def _prefill_unit(Q, K, V, top_k, causal_shift=0, own=True):
+    """prefill_unit with one slip (the causal mask one token off, or the own block left out)."""
+    Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    G, T, d = Q.shape
+    routes = O.prefill_routes(Q, K, top_k)
+    o = np.zeros((G, T, d))
+    lse = np.zeros((G, T))
+    for i, (idx, _) in enumerate(routes):
+        t0, t1 = i * BS, min(T, (i + 1) * BS)
+        parts = [np.arange(j * BS, (j + 1) * BS) for j in idx]
+        if own or not parts:
+            parts.append(np.arange(t0, t1))
+        keys = np.concatenate(parts).astype(np.int64)
+        s = np.einsum("gtd,kd->gtk", Q[:, t0:t1, :], K[keys]) / math.sqrt(d)
+        mask = (keys[None, :] >= t0) & (keys[None, :] > np.arange(t0, t1)[:, None] + causal_shift)
+        s = np.where(mask[None], -np.inf, s)
+        m = s.max(axis=2, keepdims=True)
+        e = np.exp(s - m)
+        l = e.sum(axis=2, keepdims=True)
+        o[:, t0:t1, :] = np.einsum("gtk,kd->gtd", e, V[keys]) / l
+        lse[:, t0:t1] = (m + np.log(l))[:, :, 0]
+    return {"o": o, "lse": lse, "routes": [r for r, _ in routes], "bounds": [b for _, b in routes]}
+
+
+def _prefill_pairs_full_own_block(T, top_k):
+    nb = -(-T // BS)
+    return sum((min(T, (i + 1) * BS) - i * BS) ** 2 + (min(T, (i + 1) * BS) - i * BS) *
+               (i if (top_k == 0 or top_k >= i) else top_k) * BS for i in range(nb))
+
+
 MUTANTS = {
+    "prefill routes by the block's first query": ("prefill_routes", lambda Q, K, k: _prefill_routes(Q, K, k, mean=False)),
+    "prefill bound drops the kmin branch": ("prefill_routes", lambda Q, K, k: _prefill_routes(Q, K, k, use_min=False)),
+    "prefill routes later blocks too": ("prefill_routes", lambda Q, K, k: _prefill_routes(Q, K, k, later=True)),
+    "prefill top-K 0 routes no block": ("prefill_routes", lambda Q, K, k: _prefill_routes(Q, K, k, zero_is_none=True)),
+    "prefill causal mask one token late": ("prefill_unit", lambda Q, K, V, k: _prefill_unit(Q, K, V, k, causal_shift=1)),
+    "prefill leaves out the own block": ("prefill_unit", lambda Q, K, V, k: _prefill_unit(Q, K, V, k, own=False)),
+    "prefill cost counts the whole own block": ("prefill_pairs", _prefill_pairs_full_own_block),
+
     "quantisation rounds down": ("quantize_groups", lambda X, bits, group=64: _quantize(X, bits, group, rounding=np.floor)),
     "quantisation step over 2^bits levels": ("quantize_groups",
                                              lambda X, bits, group=64: _quantize(X, bits, group, levels=2 ** bits)),

@@ -6,7 +6,7 @@ closed form, an invariant, brute force on tiny inputs, or the numbers the
 pages print (tests/golden).  A plausible slip in the oracle (dropped anchor,
 wrong sign of a delta, transposed basis, residual rows not substituted,
 wrong tie order, a missing LSE rescale) fails at least one of them;
-tests/test_oracle_mutants.py plants 40 such slips and checks exactly that.
+tests/test_oracle_mutants.py plants 47 such slips and checks exactly that.
 """
 import itertools
 import json
@@ -564,3 +564,126 @@ def test_quantized_residual_decode_brute_force(bits):
     np.testing.assert_allclose(got["o"], o, atol=1e-10, rtol=0)
     np.testing.assert_allclose(got["lse"], lse, atol=1e-10, rtol=0)
     assert np.abs(got["o"] - O.decode_unit(q, unit, 0)["o"]).max() > 0  # the quantisation is visible
+
+
+# ----------------------------------------------------------------- block-sparse prefill
+
+def _causal_dense(Q, K, V):
+    """Textbook causal softmax attention via scipy: token t attends keys 0..t."""
+    G, T, d = Q.shape
+    s = np.einsum("gtd,kd->gtk", Q, K) / math.sqrt(d)
+    s = np.where(np.triu(np.ones((T, T), bool), 1)[None], -np.inf, s)
+    return scipy.special.softmax(s, axis=2) @ V, scipy.special.logsumexp(s, axis=2)
+
+
+@pytest.mark.parametrize("T,top_k", [(700, 0), (700, 3), (512, 2), (256, 0), (37, 1), (1100, 50)])
+def test_prefill_routing_every_block_is_dense_causal_attention(T, top_k):
+    """top_k 0 or >= the number of earlier blocks: every query attends every key at
+    or before it, i.e. dense causal softmax attention."""
+    rng = np.random.default_rng(T + top_k)
+    d = 16
+    K, V = _kv(rng, T, d)
+    Q = rng.standard_normal((3, T, d))
+    got = O.prefill_unit(Q, K, V, top_k)
+    o, lse = _causal_dense(Q, K, V)
+    nb = -(-T // BS)
+    if top_k == 0 or top_k >= nb - 1:
+        np.testing.assert_allclose(got["o"], o, atol=1e-11, rtol=0)
+        np.testing.assert_allclose(got["lse"], lse, atol=1e-11, rtol=0)
+    else:  # the first top_k + 1 query blocks still see every earlier block
+        t1 = (top_k + 1) * BS
+        np.testing.assert_allclose(got["o"][:, :t1], o[:, :t1], atol=1e-11, rtol=0)
+
+
+def test_prefill_brute_force_loops():
+    """Scalar loops: the block-mean query, the bounds (max of the two products per
+    channel over the block's own min and max), the ranking with ties to the lower
+    block, each token's key set (own block causally, routed blocks whole) and its
+    softmax.  Each block's first query is made atypical, so that routing on one
+    token instead of the block mean would pick other blocks."""
+    rng = np.random.default_rng(5)
+    T, d, G, top_k = 6 * BS + 40, 8, 2, 2
+    K, V = _kv(rng, T, d)
+    Q = 0.3 * rng.standard_normal((G, T, d))
+    for i in range(7):  # each block's queries lean one way, its first query the other way
+        lean = 2.0 * rng.standard_normal(d)
+        Q[:, i * BS:(i + 1) * BS, :] += lean
+        Q[:, i * BS, :] = -3.0 * lean
+    K[BS:2 * BS] = K[:BS]  # blocks 0 and 1 have the same box: a tie, to the lower block
+    got = O.prefill_unit(Q, K, V, top_k)
+    differs = False
+    for i in range(7):
+        t0, t1 = i * BS, min(T, (i + 1) * BS)
+        qbar = [sum(Q[g, t, c] / math.sqrt(d) for g in range(G) for t in range(t0, t1)) / (G * (t1 - t0))
+                for c in range(d)]
+        bounds, first = [], []
+        for j in range(i):
+            lo = [min(K[t, c] for t in range(j * BS, (j + 1) * BS)) for c in range(d)]
+            hi = [max(K[t, c] for t in range(j * BS, (j + 1) * BS)) for c in range(d)]
+            bounds.append(sum(max(qbar[c] * lo[c], qbar[c] * hi[c]) for c in range(d)))
+            q0 = [Q[0, t0, c] / math.sqrt(d) for c in range(d)]
+            first.append(sum(max(q0[c] * lo[c], q0[c] * hi[c]) for c in range(d)))
+        routed = sorted(sorted(range(i), key=lambda j: (-bounds[j], j))[:top_k]) if i > top_k else list(range(i))
+        by_first = sorted(sorted(range(i), key=lambda j: (-first[j], j))[:top_k]) if i > top_k else list(range(i))
+        differs |= routed != by_first
+        assert list(got["routes"][i]) == routed
+        for t in range(t0, t1, 61):
+            keys = [k for j in routed for k in range(j * BS, (j + 1) * BS)] + list(range(t0, t + 1))
+            for g in range(G):
+                sc = [sum(Q[g, t, c] * K[k, c] for c in range(d)) / math.sqrt(d) for k in keys]
+                m = max(sc)
+                e = [math.exp(x - m) for x in sc]
+                o = [sum(e[n] * V[k, c] for n, k in enumerate(keys)) / sum(e) for c in range(d)]
+                np.testing.assert_allclose(got["o"][g, t], o, atol=1e-10, rtol=0)
+                assert abs(got["lse"][g, t] - (m + math.log(sum(e)))) < 1e-10
+    assert differs, "the case does not tell the block mean from the first query"
+
+
+def test_prefill_bound_is_an_upper_bound_on_every_key():
+    rng = np.random.default_rng(6)
+    T, d = 5 * BS, 32
+    K, _ = _kv(rng, T, d)
+    Q = rng.standard_normal((6, T, d))
+    routes = O.prefill_routes(Q, K, 2)
+    for i, (_, bounds) in enumerate(routes):
+        qbar = (Q[:, i * BS:(i + 1) * BS] / math.sqrt(d)).mean(axis=(0, 1))
+        for j in range(i):
+            assert bounds[j] >= (K[j * BS:(j + 1) * BS] @ qbar).max() - 1e-12
+
+
+def test_prefill_blockwise_merge_equals_the_single_softmax():
+    """Per query block, a partial per attended key block (routed blocks whole, the own
+    block causally) merged by the split log-sum-exp gives the one-softmax result."""
+    rng = np.random.default_rng(7)
+    T, d, top_k = 4 * BS + 100, 16, 2
+    K, V = _kv(rng, T, d)
+    Q = rng.standard_normal((2, T, d))
+    got = O.prefill_unit(Q, K, V, top_k)
+    for i, idx in enumerate(got["routes"]):
+        t0, t1 = i * BS, min(T, (i + 1) * BS)
+        for t in range(t0, t1, 29):
+            parts = []
+            for j in list(idx) + [i]:
+                k1 = (j + 1) * BS if j != i else t + 1
+                s = (Q[:, t, :] / math.sqrt(d)) @ K[j * BS:k1].T
+                m = s.max(axis=1)
+                e = np.exp(s - m[:, None])
+                parts.append((m, e.sum(axis=1), e @ V[j * BS:k1]))
+            o, lse = O.lse_merge(parts)
+            np.testing.assert_allclose(got["o"][:, t], o, atol=1e-12, rtol=0)
+            np.testing.assert_allclose(got["lse"][:, t], lse, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("n,top_k", [(1, 4), (8, 4), (64, 16), (256, 16), (5, 0)])
+def test_prefill_cost_is_linear_in_length(n, top_k):
+    """[README Core] "Sub-Quadratic Prefill": O(L^2) down to O(L * K).  For T = 256 n the
+    scored pairs are n causal triangles plus 256^2 per routed block, sum_i min(i, K)."""
+    T = n * BS
+    k_of = lambda i: i if (top_k == 0 or top_k >= i) else top_k
+    closed = n * BS * (BS + 1) // 2 + BS * BS * sum(k_of(i) for i in range(n))
+    assert O.prefill_pairs(T, top_k) == closed
+    if top_k and n >= 256:  # doubling the length doubles the cost once n >> K
+        ratio = O.prefill_pairs(2 * T, top_k) / O.prefill_pairs(T, top_k)
+        assert 1.95 < ratio < 2.05
+    if top_k == 0:
+        assert O.prefill_pairs(T, 0) == T * (T + 1) // 2  # dense causal
