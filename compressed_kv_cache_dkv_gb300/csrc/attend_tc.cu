@@ -312,7 +312,10 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm) attend_tc_kernel(TcA
       // per unit whose full barrier a fill armed (the first unit of the fill's span): the parity
       // of its next fill's phase and of its last one
       uint32_t armed = 0u, fpar = 0u, lastf = 0u;
-      uint32_t qpar = 0u, qused = 0u;  // per query slot: parity of its last copy's phase, copied at least once
+      // per query slot: parity of its last phase (iteration j is phase j / kTcIQ of slot j % kTcIQ,
+      // a copy or a plain arrival) and whether it had one; waiting on an older phase's parity
+      // after a later one completed would sit out the whole bounded wait
+      uint32_t qpar = 0u, qused = 0u;
       bool waited = false;
       const uint32_t r8 = (uint32_t)L.r8;
       // claim s units starting at u (waiting for their previous contents to be released) and fill them
@@ -339,6 +342,8 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm) attend_tc_kernel(TcA
         }
         const int iq = j % kTcIQ;
         if (j >= kTcIQ && !mbar_wait(&sm.iq_empty[iq], ((j / kTcIQ) - 1) & 1, a.err)) break;
+        qpar = (qpar & ~(1u << iq)) | ((uint32_t)((j / kTcIQ) & 1) << iq);  // every path below arrives once
+        qused |= 1u << iq;
         TcItem& dsc = sm.iqd[iq];
         if (gi >= a.total) {
           dsc.stop = 1;
@@ -365,8 +370,6 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm) attend_tc_kernel(TcA
           const __half* qsrc = a.q + ((size_t)(it.u / a.Hkv) * a.Hq + (size_t)(it.u % a.Hkv) * a.G) * D;
           __half* qdst = reinterpret_cast<__half*>(smem + kOffQ) + (size_t)iq * 8 * 136;
           for (int g = 0; g < a.G; ++g) bulk_g2s(qdst + (size_t)g * 136, qsrc + (size_t)g * D, row, &sm.iq_full[iq], pol);
-          qpar = (qpar & ~(1u << iq)) | ((uint32_t)((j / kTcIQ) & 1) << iq);
-          qused |= 1u << iq;
         }
         const Places p = take_places(pos, it);
         const uint8_t* src = a.cache + it.base;
@@ -383,7 +386,8 @@ __global__ void __launch_bounds__(kTcThreads, kTcCtasPerSm) attend_tc_kernel(TcA
         if (!ok) break;
       }
       // every copy this CTA issued lands before it may finish, whether or not a wait gave
-      // up: the last fill of every ring unit and the last query copy of every slot
+      // up: the last fill of every ring unit and the last phase of every query slot (fills of
+      // a unit and phases of a slot complete in order: each waits for the release of the last)
       for (int v = 0; v < kUnits; ++v)
         if ((armed >> v) & 1u) mbar_wait(&sm.full[v], (lastf >> v) & 1u, a.err);
       for (int q = 0; q < kTcIQ; ++q)

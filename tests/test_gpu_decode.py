@@ -44,12 +44,16 @@ def _run_case(w: synth.Workload, layer: int, top_ks, distinct: int | None = None
     G = w.group
     worst = 0.0
     n_tie = 0
+    ws = torch.zeros(max(dkv.dkv_decode_workspace_bytes(desc, k) for k in top_ks), dtype=torch.uint8, device="cuda")
     for top_k in top_ks:
-        out, lse, routed = dkv.dkv_decode_attend(desc, qd, cache, top_k)
+        out, lse, routed = dkv.dkv_decode_attend(desc, qd, cache, top_k, workspace=ws)
         # without a copy of the indices the router puts each block in its rank's slot
         # (another block order, the same blocks): the path the benchmark times
-        out_ns, lse_ns, _ = dkv.dkv_decode_attend(desc, qd, cache, top_k, routed=False)
+        out_ns, lse_ns, _ = dkv.dkv_decode_attend(desc, qd, cache, top_k, routed=False, workspace=ws)
         torch.cuda.synchronize()
+        # no bounded wait gave up, not even one that only delays the exit (outputs stay right then)
+        st, word = dkv.dkv_get_error(ws)
+        assert st == dkv.DKV_OK and word == 0, f"top_k {top_k}: device error word {word:#x}"
         out, lse = out.cpu().numpy(), lse.cpu().numpy()
         out_ns, lse_ns = out_ns.cpu().numpy(), lse_ns.cpu().numpy()
         routed = routed.cpu().numpy() if routed is not None else None
