@@ -40,8 +40,11 @@ METRIC = "decode attention queries/s and HBM GB/s (% of roofline) over DKV cache
 FALLBACK_HBM_GBS = 6800.0
 
 
+_T0 = time.perf_counter()
+
+
 def log(*a):
-    print(*a, file=sys.stderr, flush=True)
+    print(f"[{time.perf_counter() - _T0:7.1f} s]", *a, file=sys.stderr, flush=True)
 
 
 # ----------------------------------------------------------------------------- multi-rank arithmetic
@@ -286,6 +289,8 @@ def main():
                     help="further workloads reported under `configs` (one layer each, several cache replicas)")
     ap.add_argument("--config-steps", type=int, default=20, help="steps per graph for the further workloads")
     ap.add_argument("--no-configs", action="store_true", help="skip the further workloads")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the block-sparse prefill measurement")
+    ap.add_argument("--prefill-tokens", type=int, default=32768, help="prompt length of the prefill measurement")
     ap.add_argument("--quant-bits", default="8,4",
                     help="also time the headline workload with residual rows group-quantised to these widths")
     args = ap.parse_args()
@@ -496,6 +501,7 @@ def main():
     K_steps = args.steps
     launches_per_call = [dkv.dkv_decode_launches(d_, top_k) for d_ in S.descs]
     R = S.measure(top_k, K_steps, args.warmup, reps)
+    log(f"[bench] headline step timed: {R['ms'] / K_steps:.3f} ms/step")
     ms, ms_ev, attend_ms = R["ms"], R["ms_ev"], R["attend_ms"]
 
     # ---------------- e2e through the C ABI with pinned host buffers
@@ -533,6 +539,7 @@ def main():
     att_bytes_step = sum(attend_bytes(w, l, top_k) for l in S.layer_ids)
     S.free()
     del q_dev, o_dev, e_ws
+    log(f"[bench] e2e timed: {e2e_ms / e2e_steps:.3f} ms/step")
 
     # ---------------- the other cache layout's decode kernel over the same step (same inputs)
     alt = None
@@ -543,6 +550,7 @@ def main():
             A = Setup(w, base_ids, top_k, alt_layout)
             AR = A.measure(top_k, K_steps, args.warmup, reps, latency=False)
             A.free()
+            log(f"[bench] {alt_layout} layout timed: {AR['ms'] / K_steps:.3f} ms/step")
             alt = {"layout": alt_layout, "kernel": kernel_names[alt_layout], "ms": AR["ms"], "ms_ev": AR["ms_ev"],
                    "attend_ms_mean": statistics.fmean(AR["attend_ms"]), "clocks": AR["clocks"]}
 
@@ -575,6 +583,7 @@ def main():
             ent["queries_per_s"] = queries_per_step * K_steps / (Rq["ms"] / 1e3)
             ent["ms_per_step"] = Rq["ms"] / K_steps
             configs[f"{w.name}_int{bits}_residuals"] = ent
+            log(f"[bench] int{bits} residuals timed: {ent['ms_per_step']:.3f} ms/step")
             Sq.free()
         for name in args.configs.split(","):
             wc = synth.WORKLOADS[name]
@@ -585,6 +594,7 @@ def main():
             for k in ks:
                 Rc = Sc.measure(k, steps_c, args.warmup, reps)
                 configs[f"{name}_top{k}" if len(ks) > 1 else name] = config_entry(wc, k, Rc, Sc, steps_c)
+                log(f"[bench] {name} top-K {k} timed")
             Sc.free()
             if name == "sweep16k" and not args.no_dense_reference:
                 # dense fp16 decode over the uncompressed K, V of the same seed (config 5's reference)
@@ -606,6 +616,7 @@ def main():
                 stream.synchronize()
                 td, clkd = timed(gd, reps)
                 dense_ms = statistics.median(td)
+                log(f"[bench] dense fp16 decode timed: {1e3 * dense_ms:.1f} us")
                 dense_bytes = 2 * Kd.numel() * 2 + wc.batch * wc.n_q_heads * wc.head_dim * (2 + 4)
                 st, word = dkv.dkv_get_error(wsd, stream=sh)
                 if st != dkv.DKV_OK:
@@ -620,6 +631,60 @@ def main():
                     "clocks": clkd.summary()}
                 del Kd, Vd, gd
                 torch.cuda.empty_cache()
+
+    # ---------------- block-sparse prefill (README "Sub-Quadratic Prefill") beside dense causal prefill
+    if not args.no_prefill and args.layers is None:
+        pw = synth.WORKLOADS["32k"]
+        T, ktop = args.prefill_tokens, pw.top_k
+        Bp, Hq, Hkv, d = 1, pw.n_q_heads, pw.n_kv_heads, pw.head_dim
+        gen = torch.Generator(device=dev).manual_seed(4242 + rank)
+        qp = torch.randn(Bp, Hq, T, d, generator=gen, device=dev).half()
+        Kp = torch.randn(Bp, Hkv, T, d, generator=gen, device=dev).half()
+        Vp = torch.randn(Bp, Hkv, T, d, generator=gen, device=dev).half()
+        op = torch.empty(Bp, Hq, T, d, dtype=torch.float32, device=dev)
+        lp = torch.empty(Bp, Hq, T, dtype=torch.float32, device=dev)
+        res = {}
+        for tk in (ktop, 0):
+            wsp = torch.zeros(max(256, dkv.dkv_prefill_workspace_bytes(Bp, Hq, Hkv, d, T, tk)), dtype=torch.uint8,
+                              device=dev)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    dkv.dkv_prefill_attend(qp, Kp, Vp, tk, out=op, lse=lp, routed=False, workspace=wsp, stream=sh)
+            stream.synchronize()
+            gp = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gp, stream=stream):
+                dkv.dkv_prefill_attend(qp, Kp, Vp, tk, out=op, lse=lp, routed=False, workspace=wsp, stream=sh)
+            with torch.cuda.stream(stream):
+                gp.replay()
+            stream.synchronize()
+            tp, clkp = timed(gp, reps)
+            res[tk] = (statistics.median(tp), clkp.summary())
+            log(f"[bench] prefill {T} tokens top-K {tk}: {res[tk][0]:.3f} ms")
+            del gp, wsp
+        nb = -(-T // 256)
+        pairs = lambda k: sum((min(T, (i + 1) * 256) - i * 256) * (min(T, (i + 1) * 256) - i * 256 + 1) // 2 +
+                              (min(T, (i + 1) * 256) - i * 256) * (i if (k == 0 or k >= i) else k) * 256
+                              for i in range(nb))
+        flops = lambda k: 4.0 * d * pairs(k) * Bp * Hq  # q.k and p.v, 2d flops each per scored pair
+        tf_peak = float(json.load(open(peaks_path))["bf16_tflops"]) if os.path.exists(peaks_path) else 1900.0
+        ms_s, ms_d = res[ktop][0], res[0][0]
+        configs["prefill32k"] = {
+            "workload": f"block-sparse prefill, batch {Bp}, {Hq}q/{Hkv}kv x d{d}, {T} tokens, top-K {ktop} earlier "
+                        f"256-token blocks per query block (random fp16 q, K, V)",
+            "kernel": "prefill_stats + prefill_route + prefill_attend (mma.sync, fp16 operands, fp32 accumulation)",
+            "ms_per_call": ms_s, "tokens_per_s": Bp * T / (ms_s / 1e3),
+            "tflops": flops(ktop) / (ms_s / 1e3) / 1e12,
+            "roofline": {"bound": "tensor", "achieved": flops(ktop) / (ms_s / 1e3) / 1e12, "peak": tf_peak,
+                         "unit": "TFLOP/s", "frac": flops(ktop) / (ms_s / 1e3) / 1e12 / tf_peak,
+                         "peak_source": "measured bf16 dense (MEASURED_PEAKS.json; fp16 has the same nominal rate)",
+                         "flops_per_call": flops(ktop)},
+            "dense_causal_ms_per_call": ms_d,
+            "dense_causal_tflops": flops(0) / (ms_d / 1e3) / 1e12,
+            "speedup_vs_dense_causal": ms_d / ms_s,
+            "scored_pairs_fraction": pairs(ktop) / pairs(0),
+            "replays": reps, "clocks": res[ktop][1]}
+        del qp, Kp, Vp, op, lp
+        torch.cuda.empty_cache()
 
     # ---------------- reduce over ranks (max time)
     if world > 1:
@@ -686,7 +751,9 @@ def main():
         # all host cores (one spawned process per core, one unit each), then one core
         n_cores = host_cores()
         cb = cpu_oracle(w.name, 0, args.cpu_seconds, top_k, n_proc=n_cores)
+        log(f"[bench] oracle on {n_cores} host cores timed")
         cb1 = cpu_oracle(w.name, 0, args.cpu_seconds, top_k) if n_cores > 1 else cb
+        log("[bench] oracle on one host core timed")
         line["cpu_baseline"] = {"value": cb["qps"], "unit": "queries/s", "cores": cb["cores"], "kind": "oracle",
                                 "sample": f"fp64 oracle decode of {cb['cores']} units of layer 0 ({w.group} queries "
                                           f"each), one spawned process per host core, each repeated for "

@@ -388,6 +388,43 @@ int dkv_dense_decode(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32
   return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
 }
 
+static int check_prefill(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t T,
+                         int32_t top_k) {
+  if (batch < 1 || n_q_heads < 1 || n_kv_heads < 1 || T < 1 || top_k < 0) return DKV_ERR_ARG;
+  if (n_q_heads % n_kv_heads) return DKV_ERR_SHAPE;
+  if ((head_dim != 64 && head_dim != 128) || n_q_heads / n_kv_heads > 8) return DKV_ERR_UNSUPPORTED;
+  if (T > 1025 * DKV_BLOCK_SIZE) return DKV_ERR_UNSUPPORTED;  // routed lists kept in shared memory
+  return DKV_OK;
+}
+
+int32_t dkv_prefill_routed_slots(int32_t T, int32_t top_k) {
+  if (T < 1 || top_k < 0) return 0;
+  return plan_prefill(1, 1, 64, T, top_k).K_eff;
+}
+
+size_t dkv_prefill_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t T,
+                                   int32_t top_k) {
+  if (check_prefill(batch, n_q_heads, n_kv_heads, head_dim, T, top_k) != DKV_OK) return 0;
+  return plan_prefill(batch, n_kv_heads, head_dim, T, top_k).ws_bytes;
+}
+
+int dkv_prefill_attend(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t T,
+                       int32_t top_k, const void* q, const void* K, const void* V, float* out, float* lse,
+                       int32_t* routed, void* workspace, size_t ws_bytes, void* stream) {
+  const int st = check_prefill(batch, n_q_heads, n_kv_heads, head_dim, T, top_k);
+  if (st != DKV_OK) return st;
+  if (!q || !K || !V || !out || !workspace) return DKV_ERR_ARG;
+  if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(out) || !aligned16(workspace) ||
+      (lse && !aligned16(lse)) || (routed && !aligned16(routed)))
+    return DKV_ERR_ALIGN;
+  if (ws_bytes < plan_prefill(batch, n_kv_heads, head_dim, T, top_k).ws_bytes) return DKV_ERR_WORKSPACE;
+  const cudaError_t e = launch_prefill(batch, n_q_heads, n_kv_heads, head_dim, T, top_k,
+                                       static_cast<const __half*>(q), static_cast<const __half*>(K),
+                                       static_cast<const __half*>(V), out, lse, routed,
+                                       static_cast<uint8_t*>(workspace), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DKV_OK : DKV_ERR_CUDA;
+}
+
 int dkv_debug_set_limits(int32_t stop_after_chunks, uint32_t wait_polls) {
   set_debug_limits(stop_after_chunks, wait_polls);
   return DKV_OK;

@@ -452,6 +452,17 @@ cudaError_t launch_combine(const Layout& L, const DecodePlan& P, int batch, int 
                            const float* partials, float* out, float* lse, cudaStream_t s);
 
 size_t dense_ws_bytes(int batch, int n_q_heads, int n_kv_heads, int d, int T);
+
+// Block-sparse prefill: workspace [header][kbox: units x nb x 2d f32][qbar: units x nb x d f32]
+// [routed: units x nb x K_eff i32]
+struct PrefillPlan {
+  int nb, K_eff;
+  size_t off_kbox, off_qbar, off_routed, ws_bytes;
+};
+PrefillPlan plan_prefill(int batch, int n_kv_heads, int d, int T, int top_k);
+cudaError_t launch_prefill(int batch, int n_q_heads, int n_kv_heads, int d, int T, int top_k, const __half* q,
+                           const __half* K, const __half* V, float* out, float* lse, int32_t* routed_out, uint8_t* ws,
+                           cudaStream_t s);
 cudaError_t launch_dense(int batch, int n_q_heads, int n_kv_heads, int d, int T, const __half* q, const __half* K,
                          const __half* V, float* out, float* lse, uint8_t* ws, uint32_t* err, cudaStream_t s);
 

@@ -40,7 +40,8 @@ EXPORTED = (
     "dkv_decode_workspace_bytes", "dkv_decode_launches", "dkv_decode_attend", "dkv_decode_route", "dkv_decode_blocks",
     "dkv_decode_combine",
     "dkv_dense_workspace_bytes", "dkv_dense_decode", "dkv_get_error", "dkv_decode_attend_noalloc",
-    "dkv_append_workspace_bytes", "dkv_append", "dkv_debug_set_limits",
+    "dkv_append_workspace_bytes", "dkv_append", "dkv_debug_set_limits", "dkv_prefill_routed_slots",
+    "dkv_prefill_workspace_bytes", "dkv_prefill_attend",
 )
 
 
@@ -108,6 +109,11 @@ def lib() -> ctypes.CDLL:
         L.dkv_append_workspace_bytes.argtypes = [pdesc]
         L.dkv_append.argtypes = [pdesc, vp, vp, i32, vp, vp, sz, vp]
         L.dkv_debug_set_limits.argtypes = [i32, ctypes.c_uint32]
+        L.dkv_prefill_routed_slots.restype = i32
+        L.dkv_prefill_routed_slots.argtypes = [i32, i32]
+        L.dkv_prefill_workspace_bytes.restype = sz
+        L.dkv_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+        L.dkv_prefill_attend.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         _lib = L
     return _lib
 
@@ -288,6 +294,44 @@ def dkv_dense_decode(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, out: tor
     _check(lib().dkv_dense_decode(B, Hq, Hkv, dh, T, _ptr(q), _ptr(K), _ptr(V), _ptr(out), _ptr(lse),
                                   _ptr(workspace), workspace.numel(), _stream(stream)), "dkv_dense_decode")
     return out, lse
+
+
+def dkv_prefill_routed_slots(T: int, top_k: int) -> int:
+    """Slots per query block of dkv_prefill_attend's routed-index output (0 on bad arguments)."""
+    return int(lib().dkv_prefill_routed_slots(int(T), int(top_k)))
+
+
+def dkv_prefill_workspace_bytes(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int, T: int,
+                                top_k: int) -> int:
+    """Workspace bytes dkv_prefill_attend needs for these sizes (0 on bad arguments)."""
+    return int(lib().dkv_prefill_workspace_bytes(int(batch), int(n_q_heads), int(n_kv_heads), int(head_dim), int(T),
+                                                 int(top_k)))
+
+
+def dkv_prefill_attend(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, top_k: int, out: torch.Tensor | None = None,
+                       lse: torch.Tensor | bool = True, routed: torch.Tensor | bool = True,
+                       workspace: torch.Tensor | None = None, stream=None):
+    """Block-sparse prefill: q fp16 [B, Hq, T, d], K, V fp16 [B, Hkv, T, d] on the GPU ->
+    (out fp32 [B, Hq, T, d], lse fp32 [B, Hq, T] or None, routed int32 [B, Hkv, nb, slots] or None)."""
+    B, Hq, T, d = q.shape
+    Hkv = K.shape[1]
+    dev = q.device
+    if out is None:
+        out = torch.empty(B, Hq, T, d, dtype=torch.float32, device=dev)
+    if lse is True:
+        lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
+    nb = -(-T // BLOCK_SIZE)
+    if routed is True:
+        routed = torch.empty(B, Hkv, nb, dkv_prefill_routed_slots(T, top_k), dtype=torch.int32, device=dev)
+    need = dkv_prefill_workspace_bytes(B, Hq, Hkv, d, T, top_k)
+    workspace = _ws(need, dev, workspace)
+    lse_t = lse if isinstance(lse, torch.Tensor) else None
+    routed_t = routed if isinstance(routed, torch.Tensor) else None
+    _check(lib().dkv_prefill_attend(B, Hq, Hkv, d, T, int(top_k), _ptr(q), _ptr(K), _ptr(V), _ptr(out),
+                                    _ptr(lse_t) if lse_t is not None else None,
+                                    _ptr(routed_t) if routed_t is not None else None, _ptr(workspace),
+                                    workspace.numel(), _stream(stream)), "dkv_prefill_attend")
+    return out, lse_t, routed_t
 
 
 def dkv_debug_set_limits(stop_after_chunks: int = -1, wait_polls: int = 0) -> None:

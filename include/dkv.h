@@ -332,6 +332,36 @@ DKV_API int dkv_dense_decode(int32_t batch, int32_t n_q_heads, int32_t n_kv_head
                      void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Block-sparse prefill attention ([DKV-Z]: "Prefill uses training-free
+ * block-sparse attention, so its cost grows sub-quadratically"; [README Core]
+ * "Sub-Quadratic Prefill": O(L^2) down to O(L * K)).  Exact K and V are in hand
+ * at prefill; each 256-token query block i attends the keys of its own block
+ * causally (token t sees keys up to t) and every key of the top_k earlier
+ * blocks j < i, ranked by the decode router's key-box bound taken with the
+ * block's mean query: qbar_i = mean over the block's tokens and the GQA
+ * group's heads of c*q, bound_ij = sum_d max(qbar_id kmax_jd, qbar_id kmin_jd)
+ * over the channel extremes of block j's keys, top_k by (bound desc, j asc);
+ * top_k 0 or >= i attends every earlier block (top_k 0 is dense causal
+ * attention).  The last block may be partial (T need not be a multiple of 256).
+ *   q       device fp16 [B][Hq][T][head_dim]
+ *   K, V    device fp16 [B][Hkv][T][head_dim]
+ *   out     device fp32 [B][Hq][T][head_dim]: softmax(c q k^T) v over each token's key set
+ *   lse     optional device fp32 [B][Hq][T]: natural-log log-sum-exp of the scores
+ *   routed  optional device int32 [B][Hkv][nb][slots] with nb = ceil(T / 256) and
+ *           slots = dkv_prefill_routed_slots(T, top_k): each query block's routed
+ *           blocks ascending, -1 in the unused slots
+ *   workspace / ws_bytes  device scratch of dkv_prefill_workspace_bytes(...)
+ * Supported: head_dim 64 or 128, n_q_heads / n_kv_heads <= 8, 1 <= T <= 262400.
+ * The products run on the tensor cores (mma.sync, fp16 operands, fp32 accumulation).
+ */
+DKV_API int32_t dkv_prefill_routed_slots(int32_t T, int32_t top_k);
+DKV_API size_t dkv_prefill_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                           int32_t T, int32_t top_k);
+DKV_API int dkv_prefill_attend(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t T,
+                               int32_t top_k, const void* q, const void* K, const void* V, float* out, float* lse,
+                               int32_t* routed, void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Diagnostics for the failure path (no counterpart in the pages): from the
  * next launch on, the producer of every attention CTA of the fragment layout
  * issues at most `stop_after_chunks` chunks (negative: all of them) and every
