@@ -130,24 +130,89 @@ def compress_block(Kb: np.ndarray, Vb: np.ndarray, rank: int, n_residual: int) -
                  kmin=Kb.min(axis=0), kmax=Kb.max(axis=0), sigma=sigma, err=err)
 
 
+@dataclasses.dataclass(frozen=True)
+class Rope:
+    """Rotary position embedding of an un-rotated pool ([README Knobs]
+    DKV_ROTATED_POOL=0: the pool stores keys before RoPE and rotates them to
+    their absolute positions at read).  The pages name RoPE without restating
+    it; the reading taken is the rotate-half form of the models they measure
+    (Qwen2.5 / Qwen3.5 under Hugging Face): the first ``dims`` channels are
+    rotated in pairs (j, j + dims/2) by the angle pos * base^(-2j/dims); the
+    channels from ``dims`` on are left alone (partial RoPE, "64 of 256 dims" on
+    Qwen3.5 in the README's verification list)."""
+
+    dims: int
+    base: float
+
+
+def rope_angles(pos: np.ndarray, rope: Rope) -> np.ndarray:
+    """[n, dims/2] angles pos_t * base^(-2j/dims), j = 0 .. dims/2 - 1."""
+    h = rope.dims // 2
+    theta = float(rope.base) ** (-2.0 * np.arange(h, dtype=np.float64) / rope.dims)
+    return np.asarray(pos, dtype=np.float64)[:, None] * theta[None, :]
+
+
+def apply_rope(X: np.ndarray, pos: np.ndarray, rope: Rope) -> np.ndarray:
+    """Rows of X [n, d] rotated to positions pos [n]: for j < h = dims/2
+        x'_j     = x_j cos(a_tj) - x_{j+h} sin(a_tj)
+        x'_{j+h} = x_{j+h} cos(a_tj) + x_j sin(a_tj)
+    and x'_c = x_c for c >= dims."""
+    X = np.asarray(X, dtype=np.float64)
+    out = X.copy()
+    if rope.dims == 0 or X.shape[0] == 0:
+        return out
+    h = rope.dims // 2
+    a = rope_angles(pos, rope)
+    c, s = np.cos(a), np.sin(a)
+    x1, x2 = X[:, :h], X[:, h:2 * h]
+    out[:, :h] = x1 * c - x2 * s
+    out[:, h:2 * h] = x2 * c + x1 * s
+    return out
+
+
+def rope_key_box(Kb: np.ndarray, block_index: int, rope: Rope) -> tuple[np.ndarray, np.ndarray]:
+    """Router box of a block in an un-rotated pool: the channel-wise min / max
+    of its 256 exact keys rotated to their absolute positions 256 b .. 256 b +
+    255 (the keys the decode scores; reading of [README Bench] "Decode router
+    bounds" for a pool that rotates at read)."""
+    pos = np.arange(block_index * BLOCK_SIZE, (block_index + 1) * BLOCK_SIZE)
+    Kr = apply_rope(Kb, pos, rope)
+    return Kr.min(axis=0), Kr.max(axis=0)
+
+
 @dataclasses.dataclass
 class Unit:
-    """Compressed cache of one (layer, sequence, KV head): blocks + window."""
+    """Compressed cache of one (layer, sequence, KV head): blocks + window.
+    With ``rope`` set the pool is un-rotated: every stored key (anchors,
+    low-rank factors, residual rows, window) is the key before RoPE; block b's
+    token i sits at absolute position 256 b + i and window token w at
+    256 NB + w."""
 
     blocks: list
     win_K: np.ndarray  # [W, d] exact recency window ([README Core] item 4)
     win_V: np.ndarray
+    rope: Rope | None = None
 
 
-def compress_unit(K: np.ndarray, V: np.ndarray, n_blocks: int, rank: int, n_residual: int) -> Unit:
+def compress_unit(K: np.ndarray, V: np.ndarray, n_blocks: int, rank: int, n_residual: int,
+                  rope: Rope | None = None) -> Unit:
     """Split a unit's T = n_blocks*256 + W tokens into compressed blocks and the
-    exact recency window ([DKV-Z]: recent tokens exact, older ones compressed)."""
+    exact recency window ([DKV-Z]: recent tokens exact, older ones compressed).
+    With ``rope`` K holds keys before RoPE (an un-rotated pool): the blocks
+    compress them as they are and only the router box is taken over the
+    rotated keys (``rope_key_box``)."""
     K = np.asarray(K, dtype=np.float64)
     V = np.asarray(V, dtype=np.float64)
     nb = int(n_blocks)
-    blocks = [compress_block(K[b * BLOCK_SIZE:(b + 1) * BLOCK_SIZE], V[b * BLOCK_SIZE:(b + 1) * BLOCK_SIZE],
-                             rank, n_residual) for b in range(nb)]
-    return Unit(blocks=blocks, win_K=K[nb * BLOCK_SIZE:].copy(), win_V=V[nb * BLOCK_SIZE:].copy())
+    blocks = []
+    for b in range(nb):
+        Kb, Vb = K[b * BLOCK_SIZE:(b + 1) * BLOCK_SIZE], V[b * BLOCK_SIZE:(b + 1) * BLOCK_SIZE]
+        blk = compress_block(Kb, Vb, rank, n_residual)
+        if rope is not None:
+            kmin, kmax = rope_key_box(Kb, b, rope)
+            blk = dataclasses.replace(blk, kmin=kmin, kmax=kmax)
+        blocks.append(blk)
+    return Unit(blocks=blocks, win_K=K[nb * BLOCK_SIZE:].copy(), win_V=V[nb * BLOCK_SIZE:].copy(), rope=rope)
 
 
 def append_tokens(unit: Unit, K_new: np.ndarray, V_new: np.ndarray, window_capacity: int, rank: int,
@@ -167,8 +232,12 @@ def append_tokens(unit: Unit, K_new: np.ndarray, V_new: np.ndarray, window_capac
         if len(win_K) == window_capacity:
             if len(win_K) < BLOCK_SIZE:
                 raise ValueError("window capacity below one block")
-            blocks.append(compress_block(np.array(win_K[:BLOCK_SIZE]), np.array(win_V[:BLOCK_SIZE]), rank,
-                                         n_residual))
+            Kb = np.array(win_K[:BLOCK_SIZE])
+            blk = compress_block(Kb, np.array(win_V[:BLOCK_SIZE]), rank, n_residual)
+            if unit.rope is not None:  # the window's oldest tokens become block len(blocks), same positions
+                kmin, kmax = rope_key_box(Kb, len(blocks), unit.rope)
+                blk = dataclasses.replace(blk, kmin=kmin, kmax=kmax)
+            blocks.append(blk)
             win_K = win_K[BLOCK_SIZE:]
             win_V = win_V[BLOCK_SIZE:]
             continue
@@ -177,7 +246,7 @@ def append_tokens(unit: Unit, K_new: np.ndarray, V_new: np.ndarray, window_capac
         i += 1
     d = K_new.shape[1] if K_new.ndim == 2 else np.asarray(unit.win_K).shape[-1]
     as_arr = lambda rows: np.array(rows).reshape(len(rows), d)
-    return Unit(blocks=blocks, win_K=as_arr(win_K), win_V=as_arr(win_V))
+    return Unit(blocks=blocks, win_K=as_arr(win_K), win_V=as_arr(win_V), rope=unit.rope)
 
 
 def reconstruct_block(blk: Block) -> tuple[np.ndarray, np.ndarray]:
@@ -259,7 +328,10 @@ def decode_unit(q: np.ndarray, unit: Unit, top_k: int) -> dict:
     recency window.  Token set = for each routed block its anchor, its
     reconstructed low-rank rows and its exact residual rows; then the W window
     tokens.  One softmax over that set (the split log-sum-exp merge the pages
-    describe reaches the same value; see ``decode_unit_factored``).
+    describe reaches the same value; see ``decode_unit_factored``).  In an
+    un-rotated pool (``unit.rope``) every key of the set is rotated to its
+    absolute position before it is scored; q is the query as the model gives
+    it (already rotated to its own position); values are not rotated.
     Returns o [G, d], lse [G], idx (routed blocks, ascending), bounds [NB].
     """
     q = np.asarray(q, dtype=np.float64)
@@ -276,9 +348,14 @@ def decode_unit(q: np.ndarray, unit: Unit, top_k: int) -> dict:
     Ks, Vs = [], []
     for b in idx:
         Kh, Vh = reconstruct_block(unit.blocks[b])
+        if unit.rope is not None:
+            Kh = apply_rope(Kh, np.arange(b * BLOCK_SIZE, (b + 1) * BLOCK_SIZE), unit.rope)
         Ks.append(Kh)
         Vs.append(Vh)
-    Ks.append(np.asarray(unit.win_K, dtype=np.float64).reshape(-1, d))
+    Kw = np.asarray(unit.win_K, dtype=np.float64).reshape(-1, d)
+    if unit.rope is not None:
+        Kw = apply_rope(Kw, nb * BLOCK_SIZE + np.arange(Kw.shape[0]), unit.rope)
+    Ks.append(Kw)
     Vs.append(np.asarray(unit.win_V, dtype=np.float64).reshape(-1, d))
     Kall = np.concatenate(Ks)
     Vall = np.concatenate(Vs)
@@ -350,6 +427,10 @@ def decode_unit_factored(q: np.ndarray, unit: Unit, top_k: int, window_chunk: in
     """Same result as ``decode_unit`` through the factored steps: route, one
     partial per routed block (``block_partial``), exact window partials in
     chunks, then the split log-sum-exp merge."""
+    if unit.rope is not None:
+        # the scorer shares z = V_K q over a block's tokens, which needs one frame for all
+        # of them ([README Knobs] DKV_ROTATED_POOL: the low-rank scorer refuses un-rotated keys)
+        raise ValueError("the factored low-rank scorer needs a rotated pool")
     q = np.asarray(q, dtype=np.float64)
     d = q.shape[1]
     qt = q / math.sqrt(d)

@@ -60,7 +60,7 @@ _orig = {n: getattr(O, n) for n in ("router_bounds", "route", "select_residuals"
                                     "decode_unit_factored", "_part", "pages_block_bytes", "residual_row_bytes",
                                     "dense_kv_bytes", "quantize_groups", "dequantize_groups",
                                     "quantize_block_residuals", "quant_residual_row_bytes", "prefill_routes",
-                                    "prefill_unit", "prefill_pairs")}
+                                    "prefill_unit", "prefill_pairs", "apply_rope", "rope_angles", "rope_key_box")}
 
 
 def _bounds_without_kmin(q, kmin, kmax):
@@ -355,7 +355,77 @@ def _prefill_pairs_full_own_block(T, top_k):
                (i if (top_k == 0 or top_k >= i) else top_k) * BS for i in range(nb))
 
 
+def _rope(X, pos, rope, pairs="half", sin_sign=1.0, exponent=2.0, all_channels=False):
+    X = np.asarray(X, dtype=np.float64)
+    out = X.copy()
+    dims = X.shape[1] if all_channels else rope.dims
+    if dims == 0 or X.shape[0] == 0:
+        return out
+    h = dims // 2
+    theta = float(rope.base) ** (-exponent * np.arange(h) / dims)
+    a = np.asarray(pos, dtype=np.float64)[:, None] * theta[None, :]
+    c, sn = np.cos(a), sin_sign * np.sin(a)
+    if pairs == "half":
+        i, j = np.arange(h), np.arange(h) + h
+    else:  # adjacent channels (2j, 2j + 1)
+        i, j = 2 * np.arange(h), 2 * np.arange(h) + 1
+    out[:, i] = X[:, i] * c - X[:, j] * sn
+    out[:, j] = X[:, j] * c + X[:, i] * sn
+    return out
+
+
+def _decode_rope_positions(q, unit, top_k, block_pos=True, window_base=True, rotate_values=False):
+    """decode_unit with a slip in where the keys sit (or in what is rotated)."""
+    if unit.rope is None:
+        return _orig["decode_unit"](q, unit, top_k)
+    q = np.asarray(q, dtype=np.float64)
+    d = q.shape[1]
+    nb = len(unit.blocks)
+    bounds = O.router_bounds(q, np.stack([b.kmin for b in unit.blocks]), np.stack([b.kmax for b in unit.blocks])) \
+        if nb else np.zeros(0)
+    idx = O.route(bounds, top_k) if nb else np.zeros(0, dtype=np.int64)
+    Ks, Vs = [], []
+    for b in idx:
+        Kh, Vh = O.reconstruct_block(unit.blocks[b])
+        pos = np.arange(BS) + (b * BS if block_pos else 0)
+        Ks.append(O.apply_rope(Kh, pos, unit.rope))
+        Vs.append(O.apply_rope(Vh, pos, unit.rope) if rotate_values else Vh)
+    W = unit.win_K.shape[0]
+    Ks.append(O.apply_rope(unit.win_K, np.arange(W) + (nb * BS if window_base else 0), unit.rope))
+    Vs.append(unit.win_V)
+    o, lse = O.softmax_attention(q, np.concatenate(Ks), np.concatenate(Vs))
+    return {"o": o, "lse": lse, "idx": idx, "bounds": bounds}
+
+
+def _append_rope_box_at_block_zero(unit, K_new, V_new, window_capacity, rank, n_residual):
+    out = _orig["append_tokens"](unit, K_new, V_new, window_capacity, rank, n_residual)
+    if unit.rope is None:
+        return out
+    # recompute the boxes of the blocks this call cut as if each sat at block 0
+    blocks = list(out.blocks)
+    for b in range(len(unit.blocks), len(blocks)):
+        Kh, _ = O.reconstruct_block(blocks[b])
+        Kr = O.apply_rope(Kh, np.arange(BS), unit.rope)
+        blocks[b] = O.Block(**{**blocks[b].__dict__, "kmin": Kr.min(axis=0), "kmax": Kr.max(axis=0)})
+    return O.Unit(blocks=blocks, win_K=out.win_K, win_V=out.win_V, rope=out.rope)
+
+
 MUTANTS = {
+    "RoPE pairs adjacent channels": ("apply_rope", lambda X, pos, rope: _rope(X, pos, rope, pairs="adjacent")),
+    "RoPE turns the wrong way": ("apply_rope", lambda X, pos, rope: _rope(X, pos, rope, sin_sign=-1.0)),
+    "RoPE frequencies base^(-j/dims)": ("apply_rope", lambda X, pos, rope: _rope(X, pos, rope, exponent=1.0)),
+    "partial RoPE rotates every channel": ("apply_rope", lambda X, pos, rope: _rope(X, pos, rope, all_channels=True)),
+    "RoPE angles one position late": ("rope_angles", lambda pos, rope: _orig["rope_angles"](np.asarray(pos) + 1, rope)),
+    "un-rotated box over the keys before RoPE": ("rope_key_box",
+                                                 lambda Kb, b, rope: (np.asarray(Kb).min(axis=0), np.asarray(Kb).max(axis=0))),
+    "un-rotated box at block 0's positions": ("rope_key_box", lambda Kb, b, rope: _orig["rope_key_box"](Kb, 0, rope)),
+    "un-rotated blocks all at positions 0..255": ("decode_unit",
+                                                  lambda q, u, k: _decode_rope_positions(q, u, k, block_pos=False)),
+    "un-rotated window positions from 0": ("decode_unit",
+                                           lambda q, u, k: _decode_rope_positions(q, u, k, window_base=False)),
+    "un-rotated pool rotates the values too": ("decode_unit",
+                                               lambda q, u, k: _decode_rope_positions(q, u, k, rotate_values=True)),
+    "un-rotated append boxes at block 0": ("append_tokens", _append_rope_box_at_block_zero),
     "prefill routes by the block's first query": ("prefill_routes", lambda Q, K, k: _prefill_routes(Q, K, k, mean=False)),
     "prefill bound drops the kmin branch": ("prefill_routes", lambda Q, K, k: _prefill_routes(Q, K, k, use_min=False)),
     "prefill routes later blocks too": ("prefill_routes", lambda Q, K, k: _prefill_routes(Q, K, k, later=True)),

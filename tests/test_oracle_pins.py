@@ -6,7 +6,7 @@ closed form, an invariant, brute force on tiny inputs, or the numbers the
 pages print (tests/golden).  A plausible slip in the oracle (dropped anchor,
 wrong sign of a delta, transposed basis, residual rows not substituted,
 wrong tie order, a missing LSE rescale) fails at least one of them;
-tests/test_oracle_mutants.py plants 47 such slips and checks exactly that.
+tests/test_oracle_mutants.py plants 58 such slips and checks exactly that.
 """
 import itertools
 import json
@@ -687,3 +687,190 @@ def test_prefill_cost_is_linear_in_length(n, top_k):
         assert 1.95 < ratio < 2.05
     if top_k == 0:
         assert O.prefill_pairs(T, 0) == T * (T + 1) // 2  # dense causal
+
+
+# ----------------------------------------------------------------- un-rotated pool (RoPE at read)
+# [README Knobs] DKV_ROTATED_POOL=0 stores keys before RoPE and rotates them to their
+# absolute positions at read.  The pins below rotate with complex arithmetic of their
+# own (pair j as the complex number x_j + i x_{j + dims/2}, multiplied by
+# exp(i pos base^(-2j/dims))), not with the oracle's rotation.
+
+def _rope_complex(X, pos, dims, base):
+    X = np.asarray(X, dtype=np.float64)
+    out = X.copy()
+    if dims == 0:
+        return out
+    h = dims // 2
+    inv_freq = 1.0 / np.power(float(base), np.arange(0, dims, 2, dtype=np.float64) / dims)
+    z = (X[:, :h] + 1j * X[:, h:dims]) * np.exp(1j * np.outer(np.asarray(pos, dtype=np.float64), inv_freq))
+    out[:, :h], out[:, h:dims] = z.real, z.imag
+    return out
+
+
+@pytest.mark.parametrize("d,dims,base", [(16, 16, 10000.0), (32, 8, 500.0), (64, 64, 1e6), (32, 0, 1e4)])
+def test_rope_is_a_complex_rotation_of_channel_pairs(d, dims, base):
+    """Each pair (j, j + dims/2) turns by pos * base^(-2j/dims); channels >= dims stay."""
+    rng = np.random.default_rng(dims + d)
+    X = rng.standard_normal((40, d))
+    pos = rng.integers(0, 70000, 40)
+    got = O.apply_rope(X, pos, O.Rope(dims, base))
+    # angles up to 7e4 rad carry fp64 rounding of ~1e-11 rad whichever way the frequency is written
+    np.testing.assert_allclose(got, _rope_complex(X, pos, dims, base), atol=2e-10, rtol=0)
+    np.testing.assert_array_equal(got[:, dims:], X[:, dims:])
+    np.testing.assert_allclose(O.apply_rope(X, np.zeros(40, dtype=np.int64), O.Rope(dims, base)), X, atol=0)
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    """(R_m q) . (R_n k) = (R_{m+s} q) . (R_{n+s} k) = q . (R_{n-m} k): RoPE's defining property."""
+    rng = np.random.default_rng(77)
+    rope = O.Rope(32, 10000.0)
+    q, k = rng.standard_normal((1, 32)), rng.standard_normal((1, 32))
+    for m, n, s in ((5, 900, 1000), (0, 3, 65000), (700, 2, 12345)):
+        a = (O.apply_rope(q, [m], rope) * O.apply_rope(k, [n], rope)).sum()
+        b = (O.apply_rope(q, [m + s], rope) * O.apply_rope(k, [n + s], rope)).sum()
+        c = (q * O.apply_rope(k, [n - m], rope)).sum()
+        assert abs(a - b) < 1e-9 and abs(a - c) < 1e-9
+
+
+def _rope_unit_case(rng, d, nb, W, rank, R, dims, base=10000.0, exact_rank=None):
+    K, V = _kv(rng, nb * BS + W, d)
+    if exact_rank is not None:  # every block's K|V deltas to its anchor of rank exact_rank
+        for b in range(nb):
+            L = rng.standard_normal((BS - 1, exact_rank))
+            Wk, Wv = rng.standard_normal((2, exact_rank, d))
+            K[b * BS + 1:(b + 1) * BS] = K[b * BS] + L @ Wk
+            V[b * BS + 1:(b + 1) * BS] = V[b * BS] + L @ Wv
+    rope = O.Rope(dims, base)
+    return K, V, rope, O.compress_unit(K, V, nb, rank, R, rope=rope)
+
+
+@pytest.mark.parametrize("d,nb,W,dims", [(16, 3, 40, 16), (8, 2, 0, 8), (32, 2, 7, 16)])
+def test_unrotated_pool_full_rank_equals_dense_rope_attention(d, nb, W, dims):
+    """r = min(255, 2d), R = 0, every block routed: softmax of q against every key
+    rotated to its own position (block b token i at 256 b + i, window token w at
+    256 NB + w), values unrotated."""
+    rng = np.random.default_rng(90 + d)
+    K, V, rope, unit = _rope_unit_case(rng, d, nb, W, min(255, 2 * d), 0, dims)
+    q = rng.standard_normal((3, d))
+    Kr = _rope_complex(K, np.arange(K.shape[0]), dims, rope.base)
+    o, lse = _dense(q, Kr, V)
+    got = O.decode_unit(q, unit, 0)
+    np.testing.assert_allclose(got["o"], o, atol=1e-10, rtol=0)
+    np.testing.assert_allclose(got["lse"], lse, atol=1e-10, rtol=0)
+
+
+def test_unrotated_pool_is_exact_on_low_rank_keys_before_rope():
+    """Blocks whose K|V deltas before RoPE have rank r: the un-rotated pool at rank r
+    is lossless, while compressing the rotated keys at the same rank is not (RoPE
+    turns every token by its own angle, which raises the rank of the deltas)."""
+    rng = np.random.default_rng(5)
+    d, nb, W, r = 16, 2, 10, 3
+    K, V, rope, unit = _rope_unit_case(rng, d, nb, W, r, 0, d, base=100.0, exact_rank=r)
+    q = rng.standard_normal((2, d))
+    Kr = _rope_complex(K, np.arange(K.shape[0]), d, rope.base)
+    o, _ = _dense(q, Kr, V)
+    np.testing.assert_allclose(O.decode_unit(q, unit, 0)["o"], o, atol=1e-9, rtol=0)
+    rotated = O.compress_unit(Kr, V, nb, r, 0)
+    assert np.abs(O.decode_unit(q, rotated, 0)["o"] - o).max() > 1e-4
+
+
+def test_unrotated_residual_key_round_trip():
+    """A residual key read back from the pool and rotated to its absolute position
+    reproduces the rotated key that lived there (the README's un-rotated pool
+    round trip); with partial RoPE a position off by one moves only the rotated
+    channels."""
+    rng = np.random.default_rng(6)
+    d, nb, dims = 32, 3, 8
+    K, V, rope, unit = _rope_unit_case(rng, d, nb, 5, 2, 12, dims)
+    Kr = _rope_complex(K, np.arange(K.shape[0]), dims, rope.base)
+    for b, blk in enumerate(unit.blocks):
+        pos = b * BS + blk.S
+        np.testing.assert_allclose(O.apply_rope(blk.K_res, pos, rope), Kr[pos], atol=1e-12, rtol=0)
+        off = O.apply_rope(blk.K_res, pos + 1, rope) - Kr[pos]
+        assert np.abs(off[:, :dims]).max() > 1e-3
+        np.testing.assert_array_equal(off[:, dims:], 0.0)
+
+
+def test_unrotated_router_box_bounds_every_rotated_key():
+    """The box is the channel extremes of the block's exact keys at their positions,
+    so bound_b >= qbar . k for each of them."""
+    rng = np.random.default_rng(8)
+    d, nb = 16, 4
+    K, V, rope, unit = _rope_unit_case(rng, d, nb, 0, 2, 3, d)
+    Kr = _rope_complex(K, np.arange(K.shape[0]), d, rope.base)
+    q = rng.standard_normal((4, d))
+    qbar = (q / math.sqrt(d)).mean(axis=0)
+    bounds = O.router_bounds(q, np.stack([b.kmin for b in unit.blocks]), np.stack([b.kmax for b in unit.blocks]))
+    for b, blk in enumerate(unit.blocks):
+        np.testing.assert_allclose(blk.kmin, Kr[b * BS:(b + 1) * BS].min(axis=0), atol=1e-12, rtol=0)
+        np.testing.assert_allclose(blk.kmax, Kr[b * BS:(b + 1) * BS].max(axis=0), atol=1e-12, rtol=0)
+        assert bounds[b] >= (Kr[b * BS:(b + 1) * BS] @ qbar).max() - 1e-12
+
+
+def test_unrotated_streaming_append_equals_batch_compression():
+    """Appending into an un-rotated pool: the window's oldest tokens keep their
+    positions when they become a block, so the result equals compressing the whole
+    sequence at once."""
+    rng = np.random.default_rng(9)
+    d, cap = 16, 300
+    K, V = _kv(rng, 1100, d)
+    rope = O.Rope(16, 10000.0)
+    unit = O.compress_unit(K[:0], V[:0], 0, 3, 5, rope=rope)
+    t = 0
+    for n in (1, 299, 1, 256, 300, 243):
+        unit = O.append_tokens(unit, K[t:t + n], V[t:t + n], cap, 3, 5)
+        t += n
+    nb = len(unit.blocks)
+    ref = O.compress_unit(K[:t], V[:t], nb, 3, 5, rope=rope)
+    for a, b in zip(unit.blocks, ref.blocks):
+        np.testing.assert_allclose(a.kmin, b.kmin, atol=1e-12, rtol=0)
+        np.testing.assert_allclose(a.kmax, b.kmax, atol=1e-12, rtol=0)
+    q = rng.standard_normal((2, d))
+    np.testing.assert_allclose(O.decode_unit(q, unit, 2)["o"], O.decode_unit(q, ref, 2)["o"], atol=1e-12, rtol=0)
+
+
+def test_unrotated_pool_brute_force_loops():
+    """Tiny case in scalar Python: rotate every routed key with math.cos / math.sin at
+    its position, one softmax, against decode_unit."""
+    rng = np.random.default_rng(11)
+    d, nb, W, dims, base = 8, 3, 5, 4, 50.0
+    K, V, rope, unit = _rope_unit_case(rng, d, nb, W, 2, 4, dims, base=base)
+    q = rng.standard_normal((2, d))
+    got = O.decode_unit(q, unit, 2)
+    keys, vals = [], []
+    for b in got["idx"]:
+        Kh, Vh = O.reconstruct_block(unit.blocks[b])
+        for i in range(BS):
+            keys.append((b * BS + i, list(Kh[i])))
+            vals.append(list(Vh[i]))
+    for w in range(W):
+        keys.append((nb * BS + w, list(K[nb * BS + w])))
+        vals.append(list(V[nb * BS + w]))
+    h = dims // 2
+    for g in range(2):
+        scores = []
+        for pos, k in keys:
+            kr = list(k)
+            for j in range(h):
+                a = pos * base ** (-2.0 * j / dims)
+                kr[j] = k[j] * math.cos(a) - k[j + h] * math.sin(a)
+                kr[j + h] = k[j + h] * math.cos(a) + k[j] * math.sin(a)
+            scores.append(sum(q[g][c] * kr[c] for c in range(d)) / math.sqrt(d))
+        m = max(scores)
+        e = [math.exp(s - m) for s in scores]
+        l = sum(e)
+        o = [sum(e[t] * vals[t][c] for t in range(len(e))) / l for c in range(d)]
+        np.testing.assert_allclose(got["o"][g], o, atol=1e-11, rtol=0)
+        assert abs(got["lse"][g] - (m + math.log(l))) < 1e-11
+
+
+def test_unrotated_pool_refuses_the_factored_scorer_and_zero_dims_is_the_rotated_pool():
+    rng = np.random.default_rng(12)
+    d = 16
+    K, V = _kv(rng, 2 * BS + 9, d)
+    q = rng.standard_normal((2, d))
+    with pytest.raises(ValueError):
+        O.decode_unit_factored(q, O.compress_unit(K, V, 2, 3, 4, rope=O.Rope(16, 1e4)), 1)
+    plain = O.decode_unit(q, O.compress_unit(K, V, 2, 3, 4), 1)
+    zero = O.decode_unit(q, O.compress_unit(K, V, 2, 3, 4, rope=O.Rope(0, 1e4)), 1)
+    np.testing.assert_allclose(zero["o"], plain["o"], atol=1e-13, rtol=0)
