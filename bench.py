@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 import hashlib
 import json
 import math
@@ -84,10 +85,11 @@ def attend_bytes(w, layer: int, top_k: int, bits: int = 0) -> int:
     return w.units_per_layer * per_unit + w.batch * w.n_q_heads * d * 2
 
 
-def call_bytes(w, layer: int, top_k: int, bits: int = 0) -> int:
+def call_bytes(w, layer: int, top_k: int, bits: int = 0, rope: bool = False) -> int:
     """Algorithmic bytes of one dkv_decode_attend: the attention kernel's bytes,
-    the router rows NB*4d per unit, and the fp32 output."""
-    return (attend_bytes(w, layer, top_k, bits) + w.units_per_layer * w.n_blocks * 4 * w.head_dim
+    the router rows NB*4d per unit (NB*8d: an un-rotated pool's fp32 boxes), and
+    the fp32 output."""
+    return (attend_bytes(w, layer, top_k, bits) + w.units_per_layer * w.n_blocks * (8 if rope else 4) * w.head_dim
             + w.batch * w.n_q_heads * w.head_dim * 4)
 
 
@@ -290,6 +292,8 @@ def main():
     ap.add_argument("--config-steps", type=int, default=20, help="steps per graph for the further workloads")
     ap.add_argument("--no-configs", action="store_true", help="skip the further workloads")
     ap.add_argument("--no-prefill", action="store_true", help="skip the block-sparse prefill measurement")
+    ap.add_argument("--no-append", action="store_true", help="skip the streaming-append measurement")
+    ap.add_argument("--no-unrotated", action="store_true", help="skip the un-rotated pool (RoPE at read) step")
     ap.add_argument("--prefill-tokens", type=int, default=32768, help="prompt length of the prefill measurement")
     ap.add_argument("--quant-bits", default="8,4",
                     help="also time the headline workload with residual rows group-quantised to these widths")
@@ -384,14 +388,15 @@ def main():
         workloads rotate a step's calls over cache replicas so that the bytes one step
         reads span at least 4x the L2 and every call reads its cache from HBM."""
 
-        def __init__(self, w, layer_ids, top_k, layout, ws_bytes=None, min_call_bytes=None, bits=0):
-            self.w, self.top_k, self.layout, self.bits = w, top_k, layout, bits
-            base = sum(call_bytes(w, l, top_k, bits) for l in layer_ids)
+        def __init__(self, w, layer_ids, top_k, layout, ws_bytes=None, min_call_bytes=None, bits=0, rope=(0, 0.0)):
+            self.w, self.top_k, self.layout, self.bits, self.rope = w, top_k, layout, bits, rope
+            base = sum(call_bytes(w, l, top_k, bits, rope[0] > 0) for l in layer_ids)
             self.n_rep = cache_replicas(min_call_bytes or base, l2_bytes)
             self.layer_ids = layer_ids * self.n_rep
             self.n_layers = len(self.layer_ids)
             self.descs = [dkv.dkv_layout(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.n_blocks, w.window,
-                                         w.rank(l), w.n_residual, layout=layout_ids[layout], residual_bits=bits)
+                                         w.rank(l), w.n_residual, layout=layout_ids[layout], residual_bits=bits,
+                                         rope_dims=rope[0], rope_base=rope[1])
                           for l in self.layer_ids]
             need = max(dkv.dkv_decode_workspace_bytes(d, k) for d in self.descs for k in {top_k, 0})
             self.ws = torch.zeros(max(need, ws_bytes or 0), dtype=torch.uint8, device=dev)
@@ -558,7 +563,7 @@ def main():
     configs = {}
     if not args.no_configs and args.layers is None:
         def config_entry(wc, k, R_, S_, steps_c):
-            cb = sum(call_bytes(wc, l, k, S_.bits) for l in S_.layer_ids)
+            cb = sum(call_bytes(wc, l, k, S_.bits, S_.rope[0] > 0) for l in S_.layer_ids)
             ab = sum(attend_bytes(wc, l, k, S_.bits) for l in S_.layer_ids)
             ms_call = R_["ms"] / (steps_c * S_.n_layers)
             att_us = 1e3 * statistics.fmean(R_["attend_ms"])
@@ -585,6 +590,20 @@ def main():
             configs[f"{w.name}_int{bits}_residuals"] = ent
             log(f"[bench] int{bits} residuals timed: {ent['ms_per_step']:.3f} ms/step")
             Sq.free()
+        # the headline workload as an un-rotated pool (README knob DKV_ROTATED_POOL=0: keys stored
+        # before RoPE, every attended key rotated to its absolute position at read)
+        if not args.no_unrotated:
+            Sr = Setup(w, base_ids, top_k, "fragment", rope=(w.head_dim, 1e6))
+            Rr = Sr.measure(top_k, K_steps, args.warmup, reps)
+            ent = config_entry(w, top_k, Rr, Sr, K_steps)
+            ent["workload"] = (f"{wl_name}; un-rotated pool: keys stored before RoPE and rotated at read "
+                               f"(all {w.head_dim} channels, RoPE base 1e6), fp32 router boxes")
+            ent["queries_per_s"] = queries_per_step * K_steps / (Rr["ms"] / 1e3)
+            ent["ms_per_step"] = Rr["ms"] / K_steps
+            ent["step_time_vs_rotated_pool"] = Rr["ms"] / R["ms"]
+            configs[f"{w.name}_unrotated_pool"] = ent
+            log(f"[bench] un-rotated pool timed: {ent['ms_per_step']:.3f} ms/step")
+            Sr.free()
         for name in args.configs.split(","):
             wc = synth.WORKLOADS[name]
             ks = [wc.top_k] if name != "sweep16k" else [4, 16, wc.n_blocks]
@@ -684,6 +703,71 @@ def main():
             "scored_pairs_fraction": pairs(ktop) / pairs(0),
             "replays": reps, "clocks": res[ktop][1]}
         del qp, Kp, Vp, op, lp
+        torch.cuda.empty_cache()
+
+    # ---------------- streaming append (README "Core Architecture": the window's oldest 256 tokens
+    # become a new block when it overflows): one token per (sequence, KV head) per call
+    if not args.no_append and args.layers is None:
+        n_cyc = 2
+        wa = dataclasses.replace(synth.WORKLOADS["64k"], name="append64k", n_blocks=synth.WORKLOADS["64k"].n_blocks + n_cyc)
+        nb0, W0, ra = wa.n_blocks - n_cyc, wa.window, wa.rank(0)
+        T0 = nb0 * 256 + W0
+        Ka, Va = synth.layer_kv_torch(wa, 0, dev, replica=rank)
+        desc_a = dkv.dkv_layout(wa.batch, wa.n_q_heads, wa.n_kv_heads, wa.head_dim, nb0, W0, ra, wa.n_residual,
+                                block_capacity=wa.n_blocks, window_capacity=W0)
+        ws_a = torch.zeros(max(dkv.dkv_append_workspace_bytes(desc_a), dkv.dkv_compress_workspace_bytes(desc_a), 256),
+                           dtype=torch.uint8, device=dev)
+        cache_a = torch.empty(desc_a.total_bytes, dtype=torch.uint8, device=dev)
+        dkv.dkv_compress_layout(desc_a, Ka[:, :, :T0].contiguous(), Va[:, :, :T0].contiguous(), cache=cache_a,
+                                workspace=ws_a)
+        # the appended tokens, one contiguous [B, Hkv, 1, d] slab per call
+        Kn = Ka[:, :, T0:].permute(2, 0, 1, 3).contiguous().unsqueeze(3)
+        Vn = Va[:, :, T0:].permute(2, 0, 1, 3).contiguous().unsqueeze(3)
+        del Ka, Va
+        n_new = Kn.shape[0]
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_new)]
+        cut = []
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clka, torch.cuda.stream(stream):
+            for i in range(n_new):
+                if i % 64 == 0:
+                    # keep the stream busy while the host queues the next calls, so that each event
+                    # pair spans device time only
+                    stream.synchronize()
+                    torch.cuda._sleep(20_000_000)
+                cut.append(desc_a.window == W0)
+                ev[i][0].record(stream)
+                dkv.dkv_append(desc_a, Kn[i], Vn[i], cache_a, workspace=ws_a, stream=sh)
+                ev[i][1].record(stream)
+            stream.synchronize()
+        st_a, word_a = dkv.dkv_get_error(ws_a)
+        if st_a != dkv.DKV_OK:
+            raise RuntimeError(f"append raised device error word {word_a:#x}")
+        if (desc_a.n_blocks, desc_a.window) != (wa.n_blocks, W0):
+            raise RuntimeError("append left an unexpected (n_blocks, window)")
+        ta = [e0.elapsed_time(e1) * 1e3 for e0, e1 in ev]
+        t_cut = [t for t, c in zip(ta, cut) if c]
+        t_tok = [t for t, c in zip(ta, cut) if not c]
+        units_a = wa.batch * wa.n_kv_heads
+        amort = sum(ta) / n_new
+        # a cut reads the 256 oldest window tokens (K and V) and writes the block and its router box
+        blk_bytes = 256 * 4 * wa.head_dim + int(desc_a.block_stride) + 4 * wa.head_dim
+        configs["append64k"] = {
+            "workload": (f"streaming append into the 64k layer-0 cache: batch {wa.batch}, {wa.n_kv_heads} KV heads x "
+                         f"d{wa.head_dim}, r {ra}, R {wa.n_residual}, window {W0}; {n_new} calls of one token per "
+                         f"(sequence, KV head), every 256th compressing the window's oldest 256 tokens into a new "
+                         f"block"),
+            "kernel": "append_write (window row store) / append_compress (GPU block compression + window slide)",
+            "token_us_median": statistics.median(t_tok), "cut_us_median": statistics.median(t_cut),
+            "amortised_us_per_token": amort, "sequence_tokens_per_s": wa.batch / (amort / 1e6),
+            "calls": n_new, "cuts": len(t_cut),
+            "cut_bytes_min": units_a * blk_bytes,
+            "cut_gbs": units_a * blk_bytes / (statistics.median(t_cut) / 1e6) / 1e9,
+            "timing": "events around each call on its stream, queued behind a sleep kernel (device time only)",
+            "clocks": clka.summary()}
+        log(f"[bench] append: token {configs['append64k']['token_us_median']:.1f} us, "
+            f"cut {configs['append64k']['cut_us_median']:.1f} us")
+        del Kn, Vn, cache_a, ws_a
         torch.cuda.empty_cache()
 
     # ---------------- reduce over ranks (max time)

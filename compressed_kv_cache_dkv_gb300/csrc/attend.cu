@@ -94,6 +94,7 @@ struct ChunkDesc {
   int kind;
   uint32_t off;   // byte offset in the ring
   int tok0, ntok; // exact stages
+  int blk;        // block index (block chunks; an un-rotated pool rotates by position)
 };
 
 // Walks the chunks of one range in order: window stages, then block items
@@ -282,32 +283,100 @@ __device__ inline bool raise_max(WarpState<D>& st, float mx0, float mx1, float& 
   return up;
 }
 
+// RoPE at read of an un-rotated pool, for one lane: the positions of its two
+// key rows (gq, gq + 8 of the 16-token tile) and the cache's RoPE tables.
+struct RopeRows {
+  const float2* tab;
+  int pages, h;  // h = rope channels / 2: channel j < h pairs with j + h
+  int P0, P1;
+};
+// turn the pair (x, y) = (channel j, channel j + h) by the angle whose (cos, sin) is cs
+__device__ inline void rot_pair(float& x, float& y, float2 cs) {
+  const float xr = fmaf(x, cs.x, -y * cs.y);
+  y = fmaf(y, cs.x, x * cs.y);
+  x = xr;
+}
+// rotate one register pair of key fragments: ra holds channels (j, j + 1) of a row, rb
+// the same row's channels (j + h, j + h + 1); returns them rotated as fp32
+__device__ inline void rot_regs(uint32_t ra, uint32_t rb, const RopeRows& rr, int P, int j, float2& xa, float2& xb) {
+  xa = __half22float2(*reinterpret_cast<const __half2*>(&ra));
+  xb = __half22float2(*reinterpret_cast<const __half2*>(&rb));
+  rot_pair(xa.x, xb.x, rope_cs(rr.tab, rr.pages, rr.h, P, j));
+  rot_pair(xa.y, xb.y, rope_cs(rr.tab, rr.pages, rr.h, P, j + 1));
+}
+
 // One 16-token exact group (residual rows or window tokens) of one warp:
-// K tile [in_g x D] then V^T tile [D x in_g] at gb, in_g = 16 or 8.
-template <int D, bool FULL>
+// K tile [in_g x D] then V^T tile [D x in_g] at gb, in_g = 16 or 8.  With ROPE
+// the key rows are rotated to their positions (rr) first: k tiles kt < h/16 pair
+// with kt + h/16, and each rotated tile enters the product as fp16 hi + lo.
+template <int D, bool FULL, bool ROPE = false>
 __device__ __forceinline__ void exact_group(WarpState<D>& st, uint32_t qrow, uint32_t gb, int tok, int nvalid,
-                                            float slog2, bool gv0, bool gv1, int lane) {
+                                            float slog2, bool gv0, bool gv1, int lane, const RopeRows* rr = nullptr) {
   constexpr int KT = D / 16;
   constexpr int in_g = FULL ? 16 : 8;
   constexpr bool full = FULL;
   const int gq = lane >> 2, t = lane & 3;
-  uint32_t qb[KT][2];
-#pragma unroll
-  for (int kt = 0; kt < KT; ++kt) {
-    qb[kt][0] = lds32(qrow + (uint32_t)(16 * kt + 2 * t) * 2u);
-    qb[kt][1] = lds32(qrow + (uint32_t)(16 * kt + 8 + 2 * t) * 2u);
-  }
   constexpr uint32_t kst = full ? 512u : 256u;
-  uint4 kv[KT];
-#pragma unroll
-  for (int kt = 0; kt < KT; ++kt) kv[kt] = ld_tile(gb + (uint32_t)kt * kst, lane, full);
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  if constexpr (ROPE) {
+    const int hk = rr->h / 16;  // rotated k-tile pairs
+    auto qfrag = [&](int kt, uint32_t& b0, uint32_t& b1) {
+      b0 = lds32(qrow + (uint32_t)(16 * kt + 2 * t) * 2u);
+      b1 = lds32(qrow + (uint32_t)(16 * kt + 8 + 2 * t) * 2u);
+    };
+#pragma unroll 1
+    for (int kt = 0; kt < hk; ++kt) {
+      const uint4 va = ld_tile(gb + (uint32_t)kt * kst, lane, full);
+      const uint4 vb = ld_tile(gb + (uint32_t)(kt + hk) * kst, lane, full);
+      // a0 / a2: row gq, channels 16 kt + 2t.. / 16 kt + 8 + 2t..; a1 / a3: row gq + 8
+      const int j0 = 16 * kt + 2 * t;
+      float2 xa0, xb0, xa2, xb2, xa1 = make_float2(0.f, 0.f), xb1 = xa1, xa3 = xa1, xb3 = xa1;
+      rot_regs(va.x, vb.x, *rr, rr->P0, j0, xa0, xb0);
+      rot_regs(full ? va.z : va.y, full ? vb.z : vb.y, *rr, rr->P0, j0 + 8, xa2, xb2);
+      if (full) {
+        rot_regs(va.y, vb.y, *rr, rr->P1, j0, xa1, xb1);
+        rot_regs(va.w, vb.w, *rr, rr->P1, j0 + 8, xa3, xb3);
+      }
+      uint32_t h0, l0, h1, l1, h2, l2, h3, l3, b0, b1;
+      split_half2(xa0.x, xa0.y, h0, l0);
+      split_half2(xa1.x, xa1.y, h1, l1);
+      split_half2(xa2.x, xa2.y, h2, l2);
+      split_half2(xa3.x, xa3.y, h3, l3);
+      qfrag(kt, b0, b1);
+      mma16816(acc[0], h0, h1, h2, h3, b0, b1);
+      mma16816(acc[0], l0, l1, l2, l3, b0, b1);
+      split_half2(xb0.x, xb0.y, h0, l0);
+      split_half2(xb1.x, xb1.y, h1, l1);
+      split_half2(xb2.x, xb2.y, h2, l2);
+      split_half2(xb3.x, xb3.y, h3, l3);
+      qfrag(kt + hk, b0, b1);
+      mma16816(acc[1], h0, h1, h2, h3, b0, b1);
+      mma16816(acc[1], l0, l1, l2, l3, b0, b1);
+    }
+#pragma unroll 1
+    for (int kt = 2 * hk; kt < KT; ++kt) {  // channels past the rotated ones, exact fp16
+      const uint4 v = ld_tile(gb + (uint32_t)kt * kst, lane, full);
+      uint32_t b0, b1;
+      qfrag(kt, b0, b1);
+      mma16816(acc[kt & 1], v.x, full ? v.y : 0u, full ? v.z : v.y, full ? v.w : 0u, b0, b1);
+    }
+  } else {
+    uint32_t qb[KT][2];
 #pragma unroll
-  for (int kt = 0; kt < KT; ++kt) {
-    // K tile (m = tokens, k = d): a half group holds rows gq only: (x, y) = k 2t.., 2t + 8..
-    const uint4 v = kv[kt];
-    const uint32_t a0 = v.x, a1 = full ? v.y : 0u, a2 = full ? v.z : v.y, a3 = full ? v.w : 0u;
-    mma16816(acc[kt & 1], a0, a1, a2, a3, qb[kt][0], qb[kt][1]);
+    for (int kt = 0; kt < KT; ++kt) {
+      qb[kt][0] = lds32(qrow + (uint32_t)(16 * kt + 2 * t) * 2u);
+      qb[kt][1] = lds32(qrow + (uint32_t)(16 * kt + 8 + 2 * t) * 2u);
+    }
+    uint4 kv[KT];
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) kv[kt] = ld_tile(gb + (uint32_t)kt * kst, lane, full);
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) {
+      // K tile (m = tokens, k = d): a half group holds rows gq only: (x, y) = k 2t.., 2t + 8..
+      const uint4 v = kv[kt];
+      const uint32_t a0 = v.x, a1 = full ? v.y : 0u, a2 = full ? v.z : v.y, a3 = full ? v.w : 0u;
+      mma16816(acc[kt & 1], a0, a1, a2, a3, qb[kt][0], qb[kt][1]);
+    }
   }
   const int tk0 = tok + gq, tk1 = tk0 + 8;
   const bool v0 = tk0 < nvalid, v1 = tk1 < nvalid && (gq + 8 < in_g);
@@ -476,6 +545,7 @@ struct BlockState {
   uint32_t mk0, mk1;              // residual-row mask of this warp's 64 U rows
   float w[RT][4];                 // sum p_i U_i (C fragment: rows = r, columns = group)
   float pa0, pa1;                 // per-lane partial sum of the low-rank p
+  uint32_t hsb;                   // un-rotated pool: the block's head chunk (a_k, V_K), held until U is scored
 };
 
 
@@ -485,7 +555,7 @@ __host__ __device__ inline size_t smem_extra() {
   return (size_t)kNBar * 8 * 2 + 16 + (size_t)kNBar * 4 + 8 * 136 * 2 + kConsumers * 128 * 2 + kNBar * 16 + 64;
 }
 
-template <int D, int R8S>
+template <int D, int R8S, bool ROPE>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int KT = D / 16;
@@ -527,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
     uint32_t rel_end = 0, land_end = 0;
     int c = 0, rel = 0, land = 0;  // chunks issued; released (seen); landed (seen)
     bool routed_ready = false, ok = true;
-    int jb = -1;
+    int jb = -1, bcur = 0;
     const uint8_t* blk = unit;
     while (ok && cur.next(a, ch)) {
       if (a.stop_after >= 0 && c >= a.stop_after) break;  // diagnostic: nothing further is issued
@@ -550,11 +620,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
       if (!ok) break;  // a wait gave up: nothing further is issued
       const int cb = c & (kNBar - 1);
       ends[cb] = rp.pos;
+      if (ch.kind != kWin && ch.j != jb) {
+        int b = ch.j;  // kModeAll: slot j is block j
+        if (!(a.mode & kModeAll)) {
+          if (!routed_ready) { griddep_wait(); routed_ready = true; }  // the router's grid has completed
+          b = a.routed[(size_t)u * a.K_eff + ch.j];
+        }
+        if (b < 0 || b >= L.NB) {
+          raise_error(a.err, DKV_DEVERR_INDEX);
+          b = 0;
+        }
+        jb = ch.j;
+        bcur = b;
+        blk = unit + L.off_blocks + (uint64_t)b * L.block_stride;
+      }
       ChunkDesc dsc;
       dsc.kind = ch.kind;
       dsc.off = off;
       dsc.tok0 = ch.tok0;
       dsc.ntok = ch.ntok;
+      dsc.blk = ch.kind == kWin ? -1 : bcur;
       cdq[cb] = dsc;  // released to the consumers by this chunk's barrier phase
       uint64_t* fb = &full[cb];
       uint8_t* dst = smem + off;
@@ -564,19 +649,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
       } else if (ch.bytes == 0) {
         mbar_arrive(fb);  // an empty section (rank 0)
       } else {
-        if (ch.j != jb) {
-          int b = ch.j;  // kModeAll: slot j is block j
-          if (!(a.mode & kModeAll)) {
-            if (!routed_ready) { griddep_wait(); routed_ready = true; }  // the router's grid has completed
-            b = a.routed[(size_t)u * a.K_eff + ch.j];
-          }
-          if (b < 0 || b >= L.NB) {
-            raise_error(a.err, DKV_DEVERR_INDEX);
-            b = 0;
-          }
-          jb = ch.j;
-          blk = unit + L.off_blocks + (uint64_t)b * L.block_stride;
-        }
         mbar_arrive_expect_tx(fb, ch.bytes);
         bulk_g2s(dst, blk + ch.off, ch.bytes, fb, pol);
       }
@@ -613,6 +685,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
   st.l0 = st.l1 = 0.f;
 #pragma unroll
   for (int i = 0; i < KT; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+  RopeRows rr;
+  const uint8_t* unit_g = a.cache + (uint64_t)u * L.unit_stride;
+  if constexpr (ROPE) {
+    rr.tab = reinterpret_cast<const float2*>(a.cache + L.off_rope);
+    rr.pages = L.rope_pages;
+    rr.h = L.rope / 2;
+  }
+  int held = -1;  // ROPE: ring slot of the block head this warp still holds
   const int n_chunks = range_chunks(a, range);
   for (int c = 0; c < n_chunks; ++c) {
     const int bi = c & (kNBar - 1);
@@ -634,13 +714,41 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
           break;
         }
         const uint32_t gb = sb + (uint32_t)(warp * 64 * D);
-        if (alive && in_g == 16)
-          exact_group<D, true>(st, qrow, gb, ch.tok0 + 16 * warp, nvalid, slog2, gv0, gv1, lane);
-        else if (alive && in_g == 8)
-          exact_group<D, false>(st, qrow, gb, ch.tok0 + 16 * warp, nvalid, slog2, gv0, gv1, lane);
+        if constexpr (ROPE) {
+          // positions: window token w at 256 NB + w; residual row i of block b at 256 b + its token
+          const int tk = ch.tok0 + 16 * warp + gq;
+          if (ch.kind == kWin) {
+            rr.P0 = 256 * L.NB + tk;
+            rr.P1 = rr.P0 + 8;
+          } else {
+            const uint16_t* cold = reinterpret_cast<const uint16_t*>(unit_g + L.off_cold) + (size_t)ch.blk * L.R8;
+            rr.P0 = 256 * ch.blk + (tk < L.R8 ? (int)cold[tk] : 0);
+            rr.P1 = 256 * ch.blk + (tk + 8 < L.R8 ? (int)cold[tk + 8] : 0);
+          }
+          if (alive && in_g == 16)
+            exact_group<D, true, true>(st, qrow, gb, ch.tok0 + 16 * warp, nvalid, slog2, gv0, gv1, lane, &rr);
+          else if (alive && in_g == 8)
+            exact_group<D, false, true>(st, qrow, gb, ch.tok0 + 16 * warp, nvalid, slog2, gv0, gv1, lane, &rr);
+        } else {
+          if (alive && in_g == 16)
+            exact_group<D, true>(st, qrow, gb, ch.tok0 + 16 * warp, nvalid, slog2, gv0, gv1, lane);
+          else if (alive && in_g == 8)
+            exact_group<D, false>(st, qrow, gb, ch.tok0 + 16 * warp, nvalid, slog2, gv0, gv1, lane);
+        }
         break;
       }
       case kHead: {
+        if constexpr (ROPE) {
+          const uint32_t* mask = reinterpret_cast<const uint32_t*>(sp + L.off_mask);
+          bs.mk0 = alive ? mask[2 * warp] : 0u;
+          bs.mk1 = alive ? mask[2 * warp + 1] : 0u;
+          const __half* ak = reinterpret_cast<const __half*>(sp);
+          for (int j = lane; j < D; j += 32) av[j] = ak[D + j];  // read back at the V_V chunk
+          bs.hsb = sb;
+#pragma unroll
+          for (int i = 0; i < RT; ++i) bs.w[i][0] = bs.w[i][1] = bs.w[i][2] = bs.w[i][3] = 0.f;
+          bs.pa0 = bs.pa1 = 0.f;
+        } else {
         uint32_t qb[KT][2];
 #pragma unroll
         for (int kt = 0; kt < KT; ++kt) {
@@ -708,6 +816,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
 #pragma unroll
         for (int i = 0; i < RT; ++i) bs.w[i][0] = bs.w[i][1] = bs.w[i][2] = bs.w[i][3] = 0.f;
         bs.pa0 = bs.pa1 = 0.f;
+        }
         break;
       }
       case kU: {
@@ -723,10 +832,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
         };
         float s[MT][4];
         float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
+        // A fragments of U for m-tile mt (m = tokens, k = r)
+        auto load_u = [&](int mt, uint4 (&uv)[RT]) {
           const int t0 = 64 * warp + 16 * mt;
-          uint4 uv[RT];
 #pragma unroll
           for (int kk = 0; kk < RT; ++kk) {
             uv[kk] = make_uint4(0u, 0u, 0u, 0u);
@@ -738,6 +846,116 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
               uv[kk].y = h.y;
             }
           }
+        };
+        if constexpr (ROPE) {
+          // Un-rotated pool: score against the rebuilt keys K_hat = a_k + U V_K (m = tokens,
+          // n = channels, fp32 accumulators), each pair (j, j + h) turned to its token's
+          // position 256 b + i, then S = K_hat q with K_hat as fp16 hi + lo (its accumulators
+          // are the A fragments).  Channels go in chunks of two k tiles: a rotated pair
+          // (kt, kt + h/16) or two unrotated ones, so that V_K's operand registers serve
+          // all four m-tiles of the warp.
+          const uint32_t vk = bs.hsb + (uint32_t)L.off_vk;
+          const __half* akp = reinterpret_cast<const __half*>(smem + (bs.hsb - sbase));
+          const int hk = rr.h / 16, nro = r8 >> 3;
+          const int P00 = 256 * ch.blk + 64 * warp + gq;  // position of row gq of m-tile 0
+          float sacc[MT][4];
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            const bool rot = c < hk;
+            const int ka = rot ? c : 2 * c, kb = rot ? c + hk : 2 * c + 1;
+            const int nts[4] = {2 * ka, 2 * ka + 1, 2 * kb, 2 * kb + 1};
+            // V_K as B fragments (k = r, n = channel): its stored 8x8 blocks (r octet x
+            // channel octet, lane L holding r 8o + L/4, channels 2(L%4)..) transposed in registers
+            uint32_t bf[4][RT][2];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t col = (uint32_t)((nts[i] >> 2) * 512 + lane * 16 + (nts[i] & 3) * 4);
+#pragma unroll
+              for (int kk = 0; kk < RT; ++kk) {
+                bf[i][kk][0] = bf[i][kk][1] = 0u;
+                if (kk < nrt) {
+                  bf[i][kk][0] = movtrans(lds32(vk + (uint32_t)(2 * kk) * 16u * D + col));
+                  if (2 * kk + 1 < nro) bf[i][kk][1] = movtrans(lds32(vk + (uint32_t)(2 * kk + 1) * 16u * D + col));
+                }
+              }
+            }
+            float2 akv[4], pg[2][2];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) akv[i] = __half22float2(*reinterpret_cast<const __half2*>(akp + 8 * nts[i] + 2 * t));
+            if (rot) {  // page entries of block b for this lane's pairs j = 8 n + 2t + e, n = nts[0], nts[1]
+#pragma unroll
+              for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) pg[i][e] = __ldg(rr.tab + (size_t)ch.blk * rr.h + 8 * nts[i] + 2 * t + e);
+            }
+            const uint32_t qa0 = lds32(qrow + (uint32_t)(16 * ka + 2 * t) * 2u);
+            const uint32_t qa1 = lds32(qrow + (uint32_t)(16 * ka + 8 + 2 * t) * 2u);
+            const uint32_t qb0 = lds32(qrow + (uint32_t)(16 * kb + 2 * t) * 2u);
+            const uint32_t qb1 = lds32(qrow + (uint32_t)(16 * kb + 8 + 2 * t) * 2u);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              uint4 uv[RT];
+              load_u(mt, uv);
+              float kh[4][4];  // [n-tile][row gq: channels 2t, 2t+1 | row gq + 8: the same]
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                kh[i][0] = akv[i].x;
+                kh[i][1] = akv[i].y;
+                kh[i][2] = akv[i].x;
+                kh[i][3] = akv[i].y;
+#pragma unroll
+                for (int kk = 0; kk < RT; ++kk)
+                  if (kk < nrt) mma16816(kh[i], uv[kk].x, uv[kk].y, uv[kk].z, uv[kk].w, bf[i][kk][0], bf[i][kk][1]);
+              }
+              if (rot) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                  const int ip = (P00 + 16 * mt + 8 * r) & 255;  // in-page index (the page is block b)
+#pragma unroll
+                  for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                      const float2 bb = __ldg(rr.tab + (size_t)(rr.pages + ip) * rr.h + 8 * nts[i] + 2 * t + e);
+                      const float2 aa = pg[i][e];
+                      const float2 cs = make_float2(fmaf(aa.x, bb.x, -aa.y * bb.y), fmaf(aa.x, bb.y, aa.y * bb.x));
+                      rot_pair(kh[i][2 * r + e], kh[i + 2][2 * r + e], cs);
+                    }
+                }
+              }
+              uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+              split_half2(kh[0][0], kh[0][1], h0, l0);  // a0: row gq, channels 16 ka + 2t..
+              split_half2(kh[0][2], kh[0][3], h1, l1);  // a1: row gq + 8
+              split_half2(kh[1][0], kh[1][1], h2, l2);  // a2: row gq, channels 16 ka + 8 + 2t..
+              split_half2(kh[1][2], kh[1][3], h3, l3);  // a3: row gq + 8
+              mma16816(sacc[mt], h0, h1, h2, h3, qa0, qa1);
+              mma16816(sacc[mt], l0, l1, l2, l3, qa0, qa1);
+              split_half2(kh[2][0], kh[2][1], h0, l0);
+              split_half2(kh[2][2], kh[2][3], h1, l1);
+              split_half2(kh[3][0], kh[3][1], h2, l2);
+              split_half2(kh[3][2], kh[3][3], h3, l3);
+              mma16816(sacc[mt], h0, h1, h2, h3, qb0, qb1);
+              mma16816(sacc[mt], l0, l1, l2, l3, qb0, qb1);
+            }
+          }
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t wsel = mt < 2 ? bs.mk0 : bs.mk1;
+            const bool m0 = (wsel >> ((mt & 1) * 16 + gq)) & 1u;
+            const bool m1 = (wsel >> ((mt & 1) * 16 + gq + 8)) & 1u;
+            s[mt][0] = m0 ? -INFINITY : sacc[mt][0] * slog2;
+            s[mt][1] = m0 ? -INFINITY : sacc[mt][1] * slog2;
+            s[mt][2] = m1 ? -INFINITY : sacc[mt][2] * slog2;
+            s[mt][3] = m1 ? -INFINITY : sacc[mt][3] * slog2;
+            mx0 = fmaxf(mx0, fmaxf(s[mt][0], s[mt][2]));
+            mx1 = fmaxf(mx1, fmaxf(s[mt][1], s[mt][3]));
+          }
+        } else {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint4 uv[RT];
+          load_u(mt, uv);
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int kk = 0; kk < RT; ++kk) {
@@ -755,6 +973,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
           s[mt][3] = m1 ? -INFINITY : fmaf(acc[3], bs.us1, bs.base1);
           mx0 = fmaxf(mx0, fmaxf(s[mt][0], s[mt][2]));
           mx1 = fmaxf(mx1, fmaxf(s[mt][1], s[mt][3]));
+        }
         }
         float sc0, sc1, ms0, ms1;
         raise_max<D>(st, mx0, mx1, sc0, sc1, ms0, ms1);
@@ -846,8 +1065,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
         break;
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[bi]);
+    if constexpr (ROPE) {
+      if (alive && ch.kind == kHead) {
+        held = bi;  // its a_k and V_K are read at the U chunk
+      } else {
+        if (lane == 0) mbar_arrive(&empty[bi]);
+        if (held >= 0 && (ch.kind == kU || !alive)) {
+          if (lane == 0) mbar_arrive(&empty[held]);
+          held = -1;
+        }
+      }
+    } else {
+      if (lane == 0) mbar_arrive(&empty[bi]);
+    }
   }
+  if (ROPE && held >= 0 && lane == 0) mbar_arrive(&empty[held]);
   // this warp's partial record (m, l, o) over every token it scored; the combine merges them
   const float l0 = warp_sum_rows(st.l0), l1 = warp_sum_rows(st.l1);
   float* rec = a.partials + (((size_t)u * a.n_r + range) * kConsumers + warp) * (16 + 8 * D);
@@ -955,9 +1187,9 @@ void fill_ranges(const Layout& L, int K_eff, int nres, int n_wst, int n_r, int (
   }
 }
 
-template <int D, int R8S>
+template <int D, int R8S, bool ROPE>
 cudaError_t launch_one(const AttendArgs& a, int grid, size_t smem, cudaStream_t s) {
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attend_kernel<D, R8S>), smem);
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attend_kernel<D, R8S, ROPE>), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -969,7 +1201,7 @@ cudaError_t launch_one(const AttendArgs& a, int grid, size_t smem, cudaStream_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attend_kernel<D, R8S>, a);
+  return cudaLaunchKernelEx(&cfg, attend_kernel<D, R8S, ROPE>, a);
 }
 
 // Kernel instance for a layout: compile-time ranks for the padded ranks of the
@@ -982,12 +1214,19 @@ int instance_r8s(int d, int r8) {
 
 #define DKV_INSTANCES(X)                                                                                  \
   X(128, 16) X(128, 24) X(128, 32) X(128, 48) X(128, -2) X(128, -4) X(128, -8) X(64, -2) X(64, -4) X(64, -8)
+// the un-rotated pool's instances (ranks up to 64)
+#define DKV_ROPE_INSTANCES(X) \
+  X(128, 16) X(128, 24) X(128, 32) X(128, 48) X(128, -2) X(128, -4) X(64, -2) X(64, -4)
 
-cudaError_t launch_instance(int d, int r8s, const AttendArgs& a, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_instance(int d, int r8s, bool rope, const AttendArgs& a, int grid, size_t smem, cudaStream_t s) {
 #define DKV_LAUNCH(D_, R_) \
-  if (d == D_ && r8s == R_) return launch_one<D_, R_>(a, grid, smem, s);
+  if (!rope && d == D_ && r8s == R_) return launch_one<D_, R_, false>(a, grid, smem, s);
   DKV_INSTANCES(DKV_LAUNCH)
 #undef DKV_LAUNCH
+#define DKV_LAUNCH_ROPE(D_, R_) \
+  if (rope && d == D_ && r8s == R_) return launch_one<D_, R_, true>(a, grid, smem, s);
+  DKV_ROPE_INSTANCES(DKV_LAUNCH_ROPE)
+#undef DKV_LAUNCH_ROPE
   return cudaErrorInvalidValue;
 }
 // Arguments shared by every attention launch of a call (mode and outputs set by the caller).
@@ -1081,7 +1320,7 @@ cudaError_t launch_attend_mode(const Layout& L, const DecodePlan& P, int n_q_hea
   if (a.n_r > kMaxRanges) return cudaErrorInvalidValue;
   a.mode = mode;
   a.routed_out = routed_out;
-  const cudaError_t e = launch_instance(L.d, instance_r8s(L.d, L.r8), a, L.units * a.n_r, smem, s);
+  const cudaError_t e = launch_instance(L.d, instance_r8s(L.d, L.r8), L.rope != 0, a, L.units * a.n_r, smem, s);
   if (e != cudaSuccess || out == nullptr) return e;
   return launch_combine(L, P, L.units / n_kv_heads, n_q_heads, n_kv_heads, a.partials, out, lse, s);
 }

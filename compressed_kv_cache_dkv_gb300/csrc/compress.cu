@@ -185,15 +185,35 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
   // ---- anchor, router min / max, anchors in the block record
   for (int i = tid; i < n; i += nt) anc[i] = i < D ? h2f(Kb[i]) : h2f(Vb[i - D]);
   for (int j = tid; j < D; j += nt) {
-    __half mn = Kb[j], mx = Kb[j];
-    for (int t = 1; t < 256; ++t) {
-      __half v = Kb[(size_t)t * D + j];
-      if (__hlt(v, mn)) mn = v;
-      if (__hgt(v, mx)) mx = v;
+    if (L.rope) {
+      // un-rotated pool: the box of the keys rotated to positions 256 blk + t, in fp32
+      const int h = L.rope / 2, jj = j < h ? j : j - h, jp = j < h ? j + h : j - h;
+      const float2* tab = reinterpret_cast<const float2*>(a.cache + L.off_rope);
+      float mn = INFINITY, mx = -INFINITY;
+      for (int t = 0; t < 256; ++t) {
+        float x = h2f(Kb[(size_t)t * D + j]);
+        if (j < L.rope) {
+          const float y = h2f(Kb[(size_t)t * D + jp]);
+          const float2 c = rope_cs(tab, L.rope_pages, h, 256 * blk + t, jj);
+          x = j < h ? fmaf(x, c.x, -y * c.y) : fmaf(x, c.x, y * c.y);
+        }
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
+      }
+      float* router = reinterpret_cast<float*>(unit + L.off_router + (uint64_t)blk * 8 * D);
+      router[j] = mn;
+      router[D + j] = mx;
+    } else {
+      __half mn = Kb[j], mx = Kb[j];
+      for (int t = 1; t < 256; ++t) {
+        __half v = Kb[(size_t)t * D + j];
+        if (__hlt(v, mn)) mn = v;
+        if (__hgt(v, mx)) mx = v;
+      }
+      __half* router = reinterpret_cast<__half*>(unit + L.off_router + (uint64_t)blk * 4 * D);
+      router[j] = mn;
+      router[D + j] = mx;
     }
-    __half* router = reinterpret_cast<__half*>(unit + L.off_router + (uint64_t)blk * 4 * D);
-    router[j] = mn;
-    router[D + j] = mx;
     reinterpret_cast<__half*>(bp)[j] = Kb[j];
     reinterpret_cast<__half*>(bp)[D + j] = Vb[j];
   }
@@ -592,6 +612,8 @@ cudaError_t launch_compress(const Layout& L, const __half* K, const __half* V, u
                             uint32_t* err, cudaStream_t s) {
   (void)ws;
   cudaError_t e = cudaMemsetAsync(cache, 0, L.total, s);
+  if (e != cudaSuccess) return e;
+  e = launch_rope_tables(L, cache, s);  // the boxes of an un-rotated pool read them
   if (e != cudaSuccess) return e;
   CPlan c = plan(L);
   CArgs a;

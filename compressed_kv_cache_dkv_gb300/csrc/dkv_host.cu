@@ -1,5 +1,6 @@
 // Host side of libdkv: descriptor validation, layout, argument checks and the
 // extern "C" entry points declared in include/dkv.h.  No kernel code here.
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -43,6 +44,16 @@ cudaError_t ensure_max_carveout(const void* func) {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// 256-token pages of absolute positions an un-rotated pool can hold: every block
+// and window slot of the capacities (block b's tokens on page b, the window after
+// them)
+static int rope_pages(const dkv_desc* d) {
+  const int cap_b = d->block_capacity ? d->block_capacity : d->n_blocks;
+  const int cap_w = d->window_capacity ? d->window_capacity : d->window;
+  const int n = (cap_b * 256 + cap_w + 255) / 256;
+  return n > 0 ? n : 1;
+}
+
 bool make_layout(const dkv_desc* d, Layout* L) {
   if (!d || !L || d->total_bytes == 0) return false;
   L->d = d->head_dim;
@@ -57,6 +68,10 @@ bool make_layout(const dkv_desc* d, Layout* L) {
   L->tc = d->layout == DKV_LAYOUT_TC ? 1 : 0;
   L->qbits = d->residual_bits;
   L->qgb = d->residual_bits ? (int)qgroup_bytes(d->head_dim, d->residual_bits) : 0;
+  L->rope = d->rope_dims;
+  L->rope_base = d->rope_base;
+  L->rope_pages = d->rope_dims ? rope_pages(d) : 0;
+  L->off_rope = d->off_rope;
   L->off_mask = d->blk_off_mask;
   L->off_vk = d->blk_off_vk;
   L->off_u = d->blk_off_u;
@@ -117,6 +132,8 @@ int dkv_layout(dkv_desc* d) {
     return DKV_ERR_ARG;
   if (d->layout != DKV_LAYOUT_FRAGMENT && d->layout != DKV_LAYOUT_TC) return DKV_ERR_ARG;
   if (d->residual_bits != 0 && d->residual_bits != 8 && d->residual_bits != 4) return DKV_ERR_ARG;
+  if (d->rope_dims < 0 || d->rope_dims > d->head_dim || (d->rope_dims && !(d->rope_base > 1.f && d->rope_base < INFINITY)))
+    return DKV_ERR_ARG;
   if (d->n_q_heads % d->n_kv_heads != 0) return DKV_ERR_SHAPE;
   const int cap_b = d->block_capacity ? d->block_capacity : d->n_blocks;
   const int cap_w = d->window_capacity ? d->window_capacity : d->window;
@@ -133,6 +150,9 @@ int dkv_layout(dkv_desc* d) {
   const int r8 = (d->rank + 7) / 8 * 8;
   const int rq = d->residual_bits;
   if (rq && d->layout == DKV_LAYOUT_TC) return DKV_ERR_UNSUPPORTED;
+  // the un-rotated pool: RoPE pairs (j, j + rope_dims / 2) sit in k tiles 16 channels apart
+  if (d->rope_dims && (d->rope_dims % 32 != 0 || d->layout != DKV_LAYOUT_FRAGMENT || rq || r8 > 64))
+    return DKV_ERR_UNSUPPORTED;
   const int R8 = rq ? (d->n_residual + 15) / 16 * 16 : (d->n_residual + 7) / 8 * 8;
   const uint64_t res_bytes = rq ? (uint64_t)(R8 / 16) * qgroup_bytes(d->head_dim, rq) : 4ull * R8 * dd;
   const int W16 = (d->window + 15) / 16 * 16;
@@ -162,11 +182,16 @@ int dkv_layout(dkv_desc* d) {
   const uint64_t nb = (uint64_t)cap_b;
   const uint64_t W16cap = (uint64_t)(cap_w + 15) / 16 * 16;
   d->off_router = 0;
-  d->off_blocks = round_up(nb * 4 * dd, 128);
+  d->off_blocks = round_up(nb * (d->rope_dims ? 8 : 4) * dd, 128);  // fp32 boxes in an un-rotated pool
   d->off_cold = d->off_blocks + nb * d->block_stride;
   d->off_window = d->off_cold + round_up(nb * (uint64_t)R8 * 2, 128);
   d->unit_stride = round_up(d->off_window + W16cap * 4 * dd, 128);
   d->total_bytes = d->unit_stride * (uint64_t)d->n_units;
+  d->off_rope = 0;
+  if (d->rope_dims) {  // [pages][h] then [256][h] (cos, sin) fp32 pairs
+    d->off_rope = d->total_bytes;
+    d->total_bytes += (uint64_t)(rope_pages(d) + 256) * (uint64_t)(d->rope_dims / 2) * 8;
+  }
   return DKV_OK;
 }
 
@@ -251,7 +276,8 @@ int dkv_append(dkv_desc* d, const void* K_new, const void* V_new, int32_t n_new,
   uint32_t* err = reinterpret_cast<uint32_t*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int nb = d->n_blocks, w = d->window, i0 = 0;
-  cudaError_t e = cudaSuccess;
+  // an un-rotated pool that holds no token yet gets its RoPE tables with its first tokens
+  cudaError_t e = (L.rope && nb == 0 && w == 0) ? launch_rope_tables(L, cb, s) : cudaSuccess;
   while (i0 < n_new && e == cudaSuccess) {
     Layout S = L;  // the live state this step starts from
     S.NB = nb;

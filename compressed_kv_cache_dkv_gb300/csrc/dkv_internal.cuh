@@ -42,6 +42,10 @@ struct Layout {
   int tc;              // 1: tensor-core (core-matrix) layout, 0: mma.sync fragment layout
   int qbits;           // residual rows: 0 fp16, 8 or 4 group-quantised (fragment layout)
   int qgb;             // bytes of one 16-token group of quantised residual rows (0 for fp16)
+  int rope;            // 0: rotated pool; > 0: un-rotated pool, RoPE over the first `rope` channels at read
+  float rope_base;
+  int rope_pages;      // 256-token pages the RoPE page table covers
+  uint64_t off_rope;   // RoPE tables (after the units): [pages][rope/2] then [256][rope/2] float2 (cos, sin)
   uint64_t off_mask, off_vk, off_u, off_res, off_vv, block_bytes;
   uint64_t off_router, off_blocks, off_cold, off_window, block_stride, unit_stride, total;
 };
@@ -226,6 +230,20 @@ __host__ __device__ inline uint64_t win_v_off(const Layout& L, int t, int j) {
 }
 
 bool make_layout(const dkv_desc* d, Layout* L);  // from a desc filled by dkv_layout()
+
+// ---------------------------------------------------------------------------
+// Un-rotated pool (Layout.rope > 0): bytes of one block's router row ([kmin |
+// kmax] fp16, or fp32 over the rotated keys) and the RoPE tables at off_rope.
+// rope_cs gives (cos, sin) of the angle P theta_j as the page entry of P >> 8
+// turned by the in-page entry of P & 255 (one complex product in fp32).
+// ---------------------------------------------------------------------------
+__host__ __device__ inline uint64_t router_row_bytes(const Layout& L) { return (uint64_t)(L.rope ? 8 : 4) * L.d; }
+__device__ inline float2 rope_cs(const float2* __restrict__ tab, int pages, int h, int P, int j) {
+  const float2 a = __ldg(tab + (size_t)(P >> 8) * h + j);
+  const float2 b = __ldg(tab + (size_t)(pages + (P & 255)) * h + j);
+  return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.x, b.y, a.y * b.x));
+}
+cudaError_t launch_rope_tables(const Layout& L, uint8_t* cache, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Workspace header (first 256 bytes of every workspace)

@@ -35,12 +35,17 @@ __global__ void __launch_bounds__(256) pack_kernel(Layout L, dkv_factors f, uint
 
   const size_t base = (size_t)u * L.NB + b;
   uint8_t* blk = unit + L.off_blocks + (uint64_t)b * L.block_stride;
-  __half* router = reinterpret_cast<__half*>(unit + L.off_router + (uint64_t)b * 4 * d);
+  uint8_t* router = unit + L.off_router + (uint64_t)b * router_row_bytes(L);
   for (int j = tid; j < d; j += nt) {
     reinterpret_cast<__half*>(blk)[j] = ld_h(f.a_k, base * d + j);
     reinterpret_cast<__half*>(blk)[d + j] = ld_h(f.a_v, base * d + j);
-    router[j] = ld_h(f.kmin, base * d + j);
-    router[d + j] = ld_h(f.kmax, base * d + j);
+    if (L.rope) {  // un-rotated pool: fp32 box of the rotated keys
+      reinterpret_cast<float*>(router)[j] = static_cast<const float*>(f.kmin)[base * d + j];
+      reinterpret_cast<float*>(router)[d + j] = static_cast<const float*>(f.kmax)[base * d + j];
+    } else {
+      reinterpret_cast<__half*>(router)[j] = ld_h(f.kmin, base * d + j);
+      reinterpret_cast<__half*>(router)[d + j] = ld_h(f.kmax, base * d + j);
+    }
   }
   // residual mask + cold positions; positions must be strictly ascending in 1..255
   __shared__ uint32_t mask[8];
@@ -107,6 +112,8 @@ __global__ void __launch_bounds__(256) pack_kernel(Layout L, dkv_factors f, uint
 
 cudaError_t launch_pack(const Layout& L, const dkv_factors& f, uint8_t* cache, uint32_t* err, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(cache, 0, L.total, s);
+  if (e != cudaSuccess) return e;
+  e = launch_rope_tables(L, cache, s);
   if (e != cudaSuccess) return e;
   dim3 grid(L.NB + 1, L.units);
   pack_kernel<<<grid, 256, 0, s>>>(L, f, cache, err);

@@ -48,6 +48,8 @@ __device__ inline int bound_key(float v) {
 //
 // max(q kmax, q kmin) equals q kmax for q >= 0 and q kmin for q < 0 (rounding
 // is monotone), so every channel costs one select and one FMA.
+// F32: an un-rotated pool's fp32 router rows (8d bytes a block), 4 channels a piece.
+template <bool F32>
 __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteThreads)
     route_kernel(Layout L, int G, int Hq, int Hkv, int K_eff, float cq, const __half* __restrict__ q,
                  const uint8_t* __restrict__ cache, int32_t* __restrict__ routed, int32_t* __restrict__ routed_out) {
@@ -66,7 +68,9 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
   const uint8_t* router = cache + (uint64_t)u * L.unit_stride + L.off_router;
   const int per = (NB + kRouteCluster - 1) / kRouteCluster;
   const int b0 = min(NB, (int)crank * per), b1 = min(NB, b0 + per);
-  const int hp = d / 8;                  // 16-byte pieces per half row (kmin or kmax)
+  constexpr int cpp = F32 ? 4 : 8;       // channels per 16-byte piece
+  const int rb = (F32 ? 8 : 4) * d;      // router row bytes
+  const int hp = d / cpp;                // 16-byte pieces per half row (kmin or kmax)
   const int bpw = 32 / hp;               // blocks per warp and pass
   const int bpp = bpw * nw;              // blocks per pass
   const int piece = lane % hp;
@@ -78,9 +82,9 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
     const int blk = b0 + i * bpp + lb;
     mn[i] = mx[i] = make_uint4(0u, 0u, 0u, 0u);
     if (blk < b1) {
-      const uint8_t* row = router + (size_t)blk * 4 * d + (size_t)piece * 16;
+      const uint8_t* row = router + (size_t)blk * rb + (size_t)piece * 16;
       mn[i] = *reinterpret_cast<const uint4*>(row);
-      mx[i] = *reinterpret_cast<const uint4*>(row + 2 * d);
+      mx[i] = *reinterpret_cast<const uint4*>(row + rb / 2);
     }
   }
   for (int j = tid; j < d; j += kRouteThreads) {
@@ -100,7 +104,7 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
   float qv[8];
   uint32_t selm[4];  // per half: all ones where q_j >= 0 (take kmax), zero where q_j < 0 (take kmin)
 #pragma unroll
-  for (int e = 0; e < 8; ++e) qv[e] = qbar[8 * piece + e];
+  for (int e = 0; e < 8; ++e) qv[e] = e < cpp ? qbar[cpp * piece + e] : 0.f;
 #pragma unroll
   for (int w = 0; w < 4; ++w) selm[w] = (qv[2 * w] >= 0.f ? 0x0000ffffu : 0u) | (qv[2 * w + 1] >= 0.f ? 0xffff0000u : 0u);
   cluster_wait();  // every CTA of the cluster has started: peer shared memory may be written
@@ -111,9 +115,9 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
         const int blk = b0 + (p0 + i) * bpp + lb;
         mn[i] = mx[i] = make_uint4(0u, 0u, 0u, 0u);
         if (blk < b1) {
-          const uint8_t* row = router + (size_t)blk * 4 * d + (size_t)piece * 16;
+          const uint8_t* row = router + (size_t)blk * rb + (size_t)piece * 16;
           mn[i] = *reinterpret_cast<const uint4*>(row);
-          mx[i] = *reinterpret_cast<const uint4*>(row + 2 * d);
+          mx[i] = *reinterpret_cast<const uint4*>(row + rb / 2);
         }
       }
     }
@@ -123,12 +127,17 @@ __global__ void __cluster_dims__(kRouteCluster, 1, 1) __launch_bounds__(kRouteTh
       const uint32_t wn[4] = {mn[i].x, mn[i].y, mn[i].z, mn[i].w};
       const uint32_t wx[4] = {mx[i].x, mx[i].y, mx[i].z, mx[i].w};
       float acc = 0.f;
+      if constexpr (F32) {
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const uint32_t v = (wx[w] & selm[w]) | (wn[w] & ~selm[w]);
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
-        acc = fmaf(qv[2 * w], f.x, acc);
-        acc = fmaf(qv[2 * w + 1], f.y, acc);
+        for (int w = 0; w < 4; ++w) acc = fmaf(qv[w], __uint_as_float(qv[w] >= 0.f ? wx[w] : wn[w]), acc);
+      } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t v = (wx[w] & selm[w]) | (wn[w] & ~selm[w]);
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+          acc = fmaf(qv[2 * w], f.x, acc);
+          acc = fmaf(qv[2 * w + 1], f.y, acc);
+        }
       }
       for (int o = hp >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       if (blk < b1 && piece < kRouteCluster) st_cluster_s32(key + blk, (uint32_t)piece, bound_key(acc));
@@ -309,10 +318,11 @@ cudaError_t launch_route(const Layout& L, const DecodePlan& P, int n_q_heads, in
   const float cq = 1.f / (sqrtf((float)L.d) * (float)G);
   const size_t smem = ((size_t)L.NB + 3) / 4 * 16;  // at most 2048 blocks: 8 KB
   // an SM running a router CTA keeps room for attention CTAs of 108 KB
-  const cudaError_t e = ensure_max_carveout(reinterpret_cast<const void*>(route_kernel));
+  const auto kern = L.rope ? route_kernel<true> : route_kernel<false>;
+  const cudaError_t e = ensure_max_carveout(reinterpret_cast<const void*>(kern));
   if (e != cudaSuccess) return e;
-  route_kernel<<<L.units * kRouteCluster, kRouteThreads, smem, s>>>(L, G, n_q_heads, n_kv_heads, P.K_eff, cq, q, cache,
-                                                    reinterpret_cast<int32_t*>(ws + P.off_routed), routed_out);
+  kern<<<L.units * kRouteCluster, kRouteThreads, smem, s>>>(L, G, n_q_heads, n_kv_heads, P.K_eff, cq, q, cache,
+                                                            reinterpret_cast<int32_t*>(ws + P.off_routed), routed_out);
   return cudaGetLastError();
 }
 

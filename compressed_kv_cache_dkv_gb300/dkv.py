@@ -54,11 +54,13 @@ class DkvError(RuntimeError):
 class dkv_desc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "n_q_heads", "n_kv_heads", "head_dim", "block_size", "n_blocks", "window", "rank",
-        "n_residual", "layout", "block_capacity", "window_capacity", "residual_bits", "rank_pad", "res_pad",
-        "window_pad", "n_units")] + [
+        "n_residual", "layout", "block_capacity", "window_capacity", "residual_bits", "rope_dims")] + [
+        ("rope_base", ctypes.c_float)] + [(n, ctypes.c_int32) for n in ("rank_pad", "res_pad", "window_pad",
+                                                                         "n_units")] + [
         (n, ctypes.c_uint64) for n in (
             "blk_off_mask", "blk_off_vk", "blk_off_u", "blk_off_res", "blk_off_vv", "block_bytes",
-            "off_router", "off_blocks", "off_cold", "off_window", "block_stride", "unit_stride", "total_bytes")]
+            "off_router", "off_blocks", "off_cold", "off_window", "block_stride", "unit_stride", "total_bytes",
+            "off_rope")]
 
     @property
     def group(self) -> int:
@@ -146,15 +148,18 @@ def _stream(stream) -> int | None:
 def dkv_layout(batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int, n_blocks: int, window: int,
                rank: int, n_residual: int, block_size: int = BLOCK_SIZE,
                layout: int | None = None, block_capacity: int = 0, window_capacity: int = 0,
-               residual_bits: int = 0) -> dkv_desc:
+               residual_bits: int = 0, rope_dims: int = 0, rope_base: float = 0.0) -> dkv_desc:
     """Fill a descriptor.  `layout` is DKV_LAYOUT_FRAGMENT (mma.sync decode kernel, the
     default) or DKV_LAYOUT_TC (tcgen05 decode kernel; head_dim 128, rank <= 48, 1 <= R <= 128).
     `block_capacity` / `window_capacity` reserve room for dkv_append (0: the live counts).
-    `residual_bits` 0 keeps residual rows fp16; 8 or 4 stores them group-quantised."""
+    `residual_bits` 0 keeps residual rows fp16; 8 or 4 stores them group-quantised.
+    `rope_dims` > 0 makes an un-rotated pool: keys are given and stored before RoPE and the
+    decode rotates them to their absolute positions (RoPE base `rope_base`)."""
     d = dkv_desc(batch=batch, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, head_dim=head_dim,
                  block_size=block_size, n_blocks=n_blocks, window=window, rank=rank, n_residual=n_residual,
                  layout=DKV_LAYOUT_FRAGMENT if layout is None else layout,
-                 block_capacity=block_capacity, window_capacity=window_capacity, residual_bits=residual_bits)
+                 block_capacity=block_capacity, window_capacity=window_capacity, residual_bits=residual_bits,
+                 rope_dims=rope_dims, rope_base=rope_base)
     _check(lib().dkv_layout(ctypes.byref(d)), "dkv_layout")
     return d
 

@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define DKV_VERSION 4
+#define DKV_VERSION 5
 
 #if defined(__GNUC__)
 #define DKV_API __attribute__((visibility("default")))
@@ -107,6 +107,25 @@ extern "C" {
  * rows scale * code + bias, rounded to fp16 (the operand precision).  Only the
  * fragment layout, and head_dim 64 or 128, take quantised residuals; R is then
  * padded to a multiple of 16.
+ *
+ * rope_dims > 0 makes the cache an un-rotated pool ([README Knobs]
+ * DKV_ROTATED_POOL=0: keys are stored before RoPE and rotated to their absolute
+ * positions at read).  The keys given to dkv_compress_layout, dkv_append and
+ * dkv_import_factors are then keys BEFORE RoPE, stored as given; the decode
+ * rotates every key it attends to its absolute position (block b's token i
+ * at 256 b + i, window token w at 256 n_blocks + w) with the rotate-half
+ * RoPE: for j < h = rope_dims / 2 the channel pair (j, j + h) turns by the
+ * angle pos * rope_base^(-2j / rope_dims); channels from rope_dims on are not
+ * rotated.  q is the query as the model gives it, already rotated to its own
+ * position; values are never rotated.  The router section then holds each
+ * block's box over its exact keys AFTER rotation, in fp32 ([kmin | kmax], 8d
+ * bytes per block), and the cache ends with RoPE tables (cos, sin as fp32
+ * pairs of the angles 256 p theta_j for every 256-token page p the
+ * capacities reach, and i theta_j for i < 256), at off_rope, written by
+ * dkv_compress_layout, dkv_import_factors and the first dkv_append into an
+ * empty cache.  Supported with the fragment layout and fp16 residual rows,
+ * rope_dims a multiple of 32 up to head_dim, rope_base > 1 and finite.
+ * rope_dims 0 (the default) stores and attends keys as given (a rotated pool).
  */
 typedef struct dkv_desc {
   int32_t batch;        /* sequences B */
@@ -122,6 +141,8 @@ typedef struct dkv_desc {
   int32_t block_capacity;   /* blocks the cache has room for (0: n_blocks); >= n_blocks */
   int32_t window_capacity;  /* window token slots (0: window); >= window */
   int32_t residual_bits;    /* 0: fp16 residual rows; 8 or 4: group-quantised (see above) */
+  int32_t rope_dims;        /* 0: rotated pool; > 0: un-rotated pool, RoPE over this many channels at read */
+  float rope_base;          /* RoPE base (un-rotated pool only) */
   /* ---- filled by dkv_layout() ---- */
   int32_t rank_pad;     /* r rounded up to a multiple of 8 (zero-padded) */
   int32_t res_pad;      /* R rounded up to a multiple of 8 (16 when quantised; zero-padded) */
@@ -132,6 +153,7 @@ typedef struct dkv_desc {
   /* byte offsets inside one unit record */
   uint64_t off_router, off_blocks, off_cold, off_window;
   uint64_t block_stride, unit_stride, total_bytes;
+  uint64_t off_rope;    /* byte offset of the RoPE tables in the cache (un-rotated pool; else 0) */
 } dkv_desc;
 
 /*
@@ -149,8 +171,9 @@ typedef struct dkv_factors {
   const int32_t* res_pos; /* [U_][NB][R]      residual token positions, 1..255, strictly ascending */
   const void* K_res;      /* [U_][NB][R][d]   exact residual keys */
   const void* V_res;      /* [U_][NB][R][d]   exact residual values */
-  const void* kmin;       /* [U_][NB][d]      per-channel key minimum over the block */
-  const void* kmax;       /* [U_][NB][d]      per-channel key maximum */
+  const void* kmin;       /* [U_][NB][d]      per-channel key minimum over the block (an un-rotated
+                                              pool: fp32, over the keys rotated to their positions) */
+  const void* kmax;       /* [U_][NB][d]      per-channel key maximum (likewise) */
   const void* win_K;      /* [U_][W][d]       recency-window keys */
   const void* win_V;      /* [U_][W][d]       recency-window values */
 } dkv_factors;

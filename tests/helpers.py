@@ -31,24 +31,28 @@ def pool():
 
 
 def _compress_job(args):
-    w, layer, b, h, rank = args
+    w, layer, b, h, rank, rope = args
     K, V = synth.unit_kv(w, layer, b, h)
-    return O.compress_unit(K, V, w.n_blocks, rank, w.n_residual)
+    return O.compress_unit(K, V, w.n_blocks, rank, w.n_residual, rope=rope)
 
 
-def oracle_units(w: synth.Workload, layer: int, bh_list, parallel: bool = True):
-    jobs = [(w, layer, b, h, w.rank(layer)) for b, h in bh_list]
+def oracle_units(w: synth.Workload, layer: int, bh_list, parallel: bool = True, rope: O.Rope | None = None):
+    """Oracle-compressed units of `w` (an un-rotated pool when `rope` is given: the
+    synthetic keys are then read as keys before RoPE)."""
+    jobs = [(w, layer, b, h, w.rank(layer), rope) for b, h in bh_list]
     if parallel and len(jobs) > 1:
         return list(pool().map(_compress_job, jobs))
     return [_compress_job(j) for j in jobs]
 
 
 def round_unit(unit: O.Unit) -> O.Unit:
-    """The same compressed unit with every factor rounded to fp16 (the stored operands)."""
+    """The same compressed unit with every factor rounded to fp16 (the stored operands);
+    an un-rotated pool's boxes are stored as fp32."""
     h = lambda x: np.asarray(x, dtype=np.float16).astype(np.float64)
+    bx = (lambda x: np.asarray(x, dtype=np.float32).astype(np.float64)) if unit.rope is not None else h
     blocks = [O.Block(a_k=h(b.a_k), a_v=h(b.a_v), U=h(b.U), V_K=h(b.V_K), V_V=h(b.V_V), S=b.S.copy(),
-                      K_res=h(b.K_res), V_res=h(b.V_res), kmin=h(b.kmin), kmax=h(b.kmax)) for b in unit.blocks]
-    return O.Unit(blocks=blocks, win_K=h(unit.win_K), win_V=h(unit.win_V))
+                      K_res=h(b.K_res), V_res=h(b.V_res), kmin=bx(b.kmin), kmax=bx(b.kmax)) for b in unit.blocks]
+    return O.Unit(blocks=blocks, win_K=h(unit.win_K), win_V=h(unit.win_V), rope=unit.rope)
 
 
 def factor_arrays(units: list, d: int, r: int, R: int, W: int) -> dict:
@@ -56,11 +60,12 @@ def factor_arrays(units: list, d: int, r: int, R: int, W: int) -> dict:
     n = len(units)
     NB = len(units[0].blocks)
     f16 = np.float16
+    fb = np.float32 if units[0].rope is not None else f16  # an un-rotated pool's boxes are fp32
     out = {
         "a_k": np.zeros((n, NB, d), f16), "a_v": np.zeros((n, NB, d), f16),
         "U": np.zeros((n, NB, 255, r), f16), "V_K": np.zeros((n, NB, r, d), f16), "V_V": np.zeros((n, NB, r, d), f16),
         "res_pos": np.zeros((n, NB, R), np.int32), "K_res": np.zeros((n, NB, R, d), f16),
-        "V_res": np.zeros((n, NB, R, d), f16), "kmin": np.zeros((n, NB, d), f16), "kmax": np.zeros((n, NB, d), f16),
+        "V_res": np.zeros((n, NB, R, d), f16), "kmin": np.zeros((n, NB, d), fb), "kmax": np.zeros((n, NB, d), fb),
         "win_K": np.zeros((n, W, d), f16), "win_V": np.zeros((n, W, d), f16),
     }
     for i, un in enumerate(units):

@@ -145,7 +145,11 @@ def unpack_block(cache: np.ndarray, desc, u: int, b: int) -> dict:
         out["res_pad_zero"] = bool((res[ki][R:] == 0).all() and (res[vi][R:] == 0).all())
     vv = h(blk + desc.blk_off_vv, r8 * d)
     out["V_V"] = (vv[rd_index(r8, d)] if tc else vv[a_layout_index(d, r8)].T)[:r].copy()
-    router = h(unit + desc.off_router + b * 4 * d, 2 * d)
+    if desc.rope_dims:  # un-rotated pool: fp32 boxes of the rotated keys, 8d bytes a block
+        off = unit + desc.off_router + b * 8 * d
+        router = cache[off:off + 8 * d].view(np.float32)
+    else:
+        router = h(unit + desc.off_router + b * 4 * d, 2 * d)
     out["kmin"], out["kmax"] = router[:d].copy(), router[d:].copy()
     cold = cache[unit + desc.off_cold + b * R8 * 2: unit + desc.off_cold + (b + 1) * R8 * 2].view(np.uint16)
     out["S"] = cold[:R].astype(np.int64)
@@ -167,3 +171,12 @@ def unpack_window(cache: np.ndarray, desc, u: int) -> tuple[np.ndarray, np.ndarr
     else:
         ki, vi = exact_index(W16, d)
     return win[ki][:W].copy(), win[vi][:W].copy()
+
+
+def unpack_rope_tables(cache: np.ndarray, desc) -> tuple[np.ndarray, np.ndarray]:
+    """The un-rotated pool's RoPE tables: page entries [pages][h] and in-page entries
+    [256][h], each (cos, sin) as fp32."""
+    h = desc.rope_dims // 2
+    n = (desc.total_bytes - desc.off_rope) // (8 * h)
+    tab = cache[desc.off_rope:desc.off_rope + n * h * 8].view(np.float32).reshape(n, h, 2)
+    return tab[:n - 256], tab[n - 256:]

@@ -24,7 +24,7 @@ def test_library_exports_every_declared_symbol():
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(dkv.EXPORTED)
-    assert lib.dkv_version() == 4
+    assert lib.dkv_version() == 5
 
 
 def test_status_strings():
@@ -50,6 +50,15 @@ def test_layout_validation():
         # group-quantised residual rows: 8 or 4 bits, fragment layout only
         (dict(residual_bits=2), dkv.DKV_ERR_ARG), (dict(residual_bits=16), dkv.DKV_ERR_ARG),
         (dict(residual_bits=-8), dkv.DKV_ERR_ARG), (dict(layout=1, residual_bits=8), dkv.DKV_ERR_UNSUPPORTED),
+        # the un-rotated pool: rope_dims a multiple of 32 up to head_dim, base > 1, fragment layout,
+        # fp16 residual rows, rank up to 64
+        (dict(rope_dims=-32, rope_base=1e4), dkv.DKV_ERR_ARG), (dict(rope_dims=160, rope_base=1e4), dkv.DKV_ERR_ARG),
+        (dict(rope_dims=64, rope_base=1.0), dkv.DKV_ERR_ARG), (dict(rope_dims=64, rope_base=float("inf")), dkv.DKV_ERR_ARG),
+        (dict(rope_dims=64, rope_base=float("nan")), dkv.DKV_ERR_ARG),
+        (dict(rope_dims=48, rope_base=1e4), dkv.DKV_ERR_UNSUPPORTED),
+        (dict(rope_dims=64, rope_base=1e4, layout=1), dkv.DKV_ERR_UNSUPPORTED),
+        (dict(rope_dims=64, rope_base=1e4, residual_bits=8), dkv.DKV_ERR_UNSUPPORTED),
+        (dict(rope_dims=64, rope_base=1e4, rank=65), dkv.DKV_ERR_UNSUPPORTED),
     ]
     for change, status in bad:
         kw = dict(ok, **change)
@@ -191,3 +200,23 @@ def test_quantised_residual_layout_bytes(d, R, bits):
     for off in (desc.blk_off_vv, desc.block_stride, desc.off_window, desc.unit_stride):
         assert off % 16 == 0
     assert desc.block_bytes < plain.block_bytes or R == 0
+
+
+@pytest.mark.parametrize("d,dims,cap_b,cap_w", [(128, 128, 30, 512), (128, 32, 252, 1024), (64, 64, 3, 300),
+                                                (64, 32, 0, 100)])
+def test_unrotated_pool_layout_bytes(d, dims, cap_b, cap_w):
+    """An un-rotated pool stores fp32 router boxes (8d bytes a block) and ends with the
+    RoPE tables: a (cos, sin) fp32 pair per RoPE channel pair for every 256-token page
+    the capacities reach and for each of the 256 in-page offsets; the block records and
+    the window are those of the rotated pool."""
+    kw = dict(block_capacity=cap_b, window_capacity=cap_w)
+    desc = dkv.dkv_layout(2, 6, 2, d, min(cap_b, 2), min(cap_w, 50), 24, 40, rope_dims=dims, rope_base=1e6, **kw)
+    plain = dkv.dkv_layout(2, 6, 2, d, min(cap_b, 2), min(cap_w, 50), 24, 40, **kw)
+    assert desc.rope_dims == dims and desc.rope_base == 1e6
+    assert desc.block_bytes == plain.block_bytes and desc.blk_off_res == plain.blk_off_res
+    assert desc.off_blocks == -(-cap_b * 8 * d // 128) * 128
+    assert desc.off_window - desc.off_blocks == plain.off_window - plain.off_blocks
+    pages = max(1, -(-(cap_b * 256 + cap_w) // 256))
+    assert desc.off_rope == desc.unit_stride * desc.n_units and desc.off_rope % 16 == 0
+    assert desc.total_bytes == desc.off_rope + (pages + 256) * (dims // 2) * 8
+    assert plain.off_rope == 0 and plain.total_bytes == plain.unit_stride * plain.n_units

@@ -40,6 +40,17 @@ def test_append_equals_batch_compression(d, r, R, cap_b, cap_w, T0, chunks):
     _append_vs_batch(d, r, R, cap_b, cap_w, T0, chunks, 0)
 
 
+@pytest.mark.parametrize("d,r,R,cap_b,cap_w,T0,chunks,rope_dims", [
+    (128, 24, 40, 6, 600, 856, [1, 7, 36, 1, 300, 256, 5], 128),   # keys before RoPE, every channel rotated
+    (128, 16, 128, 5, 512, 0, [1, 255, 256, 1, 700], 64),           # starts empty: the first append writes the tables
+    (64, 8, 16, 4, 300, 300, [1, 1, 254, 300], 32),                  # partial RoPE at d = 64
+])
+def test_append_into_an_unrotated_pool_equals_batch_compression(d, r, R, cap_b, cap_w, T0, chunks, rope_dims):
+    """The same byte identity for an un-rotated pool: its blocks' boxes are taken over the
+    keys rotated to the positions the tokens keep when they leave the window."""
+    _append_vs_batch(d, r, R, cap_b, cap_w, T0, chunks, 0, rope_dims)
+
+
 @pytest.mark.parametrize("bits", [8, 4])
 def test_append_with_quantised_residuals_equals_batch_compression(bits):
     """The same byte identity when the residual rows are stored group-quantised."""
@@ -47,14 +58,15 @@ def test_append_with_quantised_residuals_equals_batch_compression(bits):
     _append_vs_batch(64, 8, 16, 4, 300, 300, [1, 1, 254, 300], bits)
 
 
-def _append_vs_batch(d, r, R, cap_b, cap_w, T0, chunks, bits):
+def _append_vs_batch(d, r, R, cap_b, cap_w, T0, chunks, bits, rope_dims=0):
     B, Hq, Hkv = 2, 6, 2
+    rope = dict(rope_dims=rope_dims, rope_base=10000.0 if rope_dims else 0.0)
     T = T0 + sum(chunks)
     K, V, _ = _tokens(B, Hq, Hkv, d, T, r, R, 321 + T)
     Kd, Vd = torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda()
     nb0, w0 = _expected_counts(T0, cap_w)
     desc = dkv.dkv_layout(B, Hq, Hkv, d, nb0, w0, r, R, block_capacity=cap_b, window_capacity=cap_w,
-                          residual_bits=bits)
+                          residual_bits=bits, **rope)
     ws = torch.zeros(max(dkv.dkv_append_workspace_bytes(desc), dkv.dkv_compress_workspace_bytes(desc), 256),
                      dtype=torch.uint8, device="cuda")
     cache = torch.empty(desc.total_bytes, dtype=torch.uint8, device="cuda")
@@ -72,7 +84,7 @@ def _append_vs_batch(d, r, R, cap_b, cap_w, T0, chunks, bits):
     st, word = dkv.dkv_get_error(ws)
     assert st == dkv.DKV_OK, f"device error word {word:#x}"
     ref_desc = dkv.dkv_layout(B, Hq, Hkv, d, desc.n_blocks, desc.window, r, R, block_capacity=cap_b,
-                              window_capacity=cap_w, residual_bits=bits)
+                              window_capacity=cap_w, residual_bits=bits, **rope)
     assert bytes(ref_desc) == bytes(desc)
     ref = dkv.dkv_compress_layout(ref_desc, Kd, Vd, workspace=ws)
     torch.cuda.synchronize()
