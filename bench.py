@@ -294,6 +294,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true", help="skip the block-sparse prefill measurement")
     ap.add_argument("--no-append", action="store_true", help="skip the streaming-append measurement")
     ap.add_argument("--no-unrotated", action="store_true", help="skip the un-rotated pool (RoPE at read) step")
+    ap.add_argument("--rope-dims", type=int, default=0,
+                    help="time the headline workload as an un-rotated pool with RoPE over this many channels")
     ap.add_argument("--prefill-tokens", type=int, default=32768, help="prompt length of the prefill measurement")
     ap.add_argument("--quant-bits", default="8,4",
                     help="also time the headline workload with residual rows group-quantised to these widths")
@@ -496,7 +498,9 @@ def main():
                f"{w.n_blocks} blocks of 256 + {w.window}-token window, r {sorted(set(w.ranks[i] for i in base_ids))}, "
                f"R {w.n_residual}, top-K {top_k}")
     t_setup = time.perf_counter()
-    S = Setup(w, base_ids, top_k, args.layout)
+    if args.rope_dims:
+        wl_name += f"; un-rotated pool (RoPE over {args.rope_dims} channels at read, base 1e6)"
+    S = Setup(w, base_ids, top_k, args.layout, rope=(args.rope_dims, 1e6 if args.rope_dims else 0.0))
     t_setup = time.perf_counter() - t_setup
     if S.n_rep > 1:
         wl_name += f"; each step {S.n_rep} calls over {S.n_rep} cache replicas"
@@ -540,7 +544,7 @@ def main():
         e1.record(stream)
         stream.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    step_bytes = sum(call_bytes(w, l, top_k) for l in S.layer_ids)
+    step_bytes = sum(call_bytes(w, l, top_k, 0, args.rope_dims > 0) for l in S.layer_ids)
     att_bytes_step = sum(attend_bytes(w, l, top_k) for l in S.layer_ids)
     S.free()
     del q_dev, o_dev, e_ws

@@ -285,11 +285,25 @@ __device__ inline bool raise_max(WarpState<D>& st, float mx0, float mx1, float& 
 
 // RoPE at read of an un-rotated pool, for one lane: the positions of its two
 // key rows (gq, gq + 8 of the 16-token tile) and the cache's RoPE tables.
+// float2 per in-page factor row: h <= 64 pairs, padded so that the 8-byte loads of a half
+// warp (rows gq, pairs 2t + e) fall in distinct bank pairs (row stride = 8 banks mod 32)
+constexpr int kRopeRow = 64 + 4;
 struct RopeRows {
-  const float2* tab;
-  int pages, h;  // h = rope channels / 2: channel j < h pairs with j + h
+  const float2* tab;       // the cache's page table [pages][h] (global)
+  const float2* s16;       // shared: (cos, sin)(16 m theta_j), [16][kRopeRow]
+  const float2* s1;        // shared: (cos, sin)(i theta_j), [16][kRopeRow]
+  int pages, h;            // h = rope channels / 2: channel j < h pairs with j + h
   int P0, P1;
 };
+__device__ inline float2 cmul(float2 a, float2 b) {
+  return make_float2(fmaf(a.x, b.x, -a.y * b.y), fmaf(a.x, b.y, a.y * b.x));
+}
+// (cos, sin) of P theta_j: page entry of P >> 8 (256 p theta_j) turned by 16 m theta_j and
+// i theta_j, P = 256 p + 16 m + i
+__device__ inline float2 rope_angle(const RopeRows& rr, int P, int j) {
+  const float2 a = __ldg(rr.tab + (size_t)(P >> 8) * rr.h + j);
+  return cmul(cmul(a, rr.s16[((P >> 4) & 15) * kRopeRow + j]), rr.s1[(P & 15) * kRopeRow + j]);
+}
 // turn the pair (x, y) = (channel j, channel j + h) by the angle whose (cos, sin) is cs
 __device__ inline void rot_pair(float& x, float& y, float2 cs) {
   const float xr = fmaf(x, cs.x, -y * cs.y);
@@ -301,8 +315,8 @@ __device__ inline void rot_pair(float& x, float& y, float2 cs) {
 __device__ inline void rot_regs(uint32_t ra, uint32_t rb, const RopeRows& rr, int P, int j, float2& xa, float2& xb) {
   xa = __half22float2(*reinterpret_cast<const __half2*>(&ra));
   xb = __half22float2(*reinterpret_cast<const __half2*>(&rb));
-  rot_pair(xa.x, xb.x, rope_cs(rr.tab, rr.pages, rr.h, P, j));
-  rot_pair(xa.y, xb.y, rope_cs(rr.tab, rr.pages, rr.h, P, j + 1));
+  rot_pair(xa.x, xb.x, rope_angle(rr, P, j));
+  rot_pair(xa.y, xb.y, rope_angle(rr, P, j + 1));
 }
 
 // One 16-token exact group (residual rows or window tokens) of one warp:
@@ -551,8 +565,12 @@ struct BlockState {
 
 // shared memory: [ring][full kNBar][empty kNBar][query barrier][ends kNBar]
 // [query rows 8 x (D + 8) fp16][a_v, one copy per consumer warp: 4 x D fp16]
-__host__ __device__ inline size_t smem_extra() {
-  return (size_t)kNBar * 8 * 2 + 16 + (size_t)kNBar * 4 + 8 * 136 * 2 + kConsumers * 128 * 2 + kNBar * 16 + 64;
+// [chunk descriptors kNBar] and, for an un-rotated pool, [RoPE in-page factors]:
+// (cos, sin) of 16 m theta_j and of i theta_j for m, i < 16 (rows of kRopeRow float2)
+constexpr size_t kRopeSmem = 2 * 16 * kRopeRow * 8;
+__host__ __device__ inline size_t smem_extra(bool rope) {
+  return (size_t)kNBar * 8 * 2 + 16 + (size_t)kNBar * 4 + 8 * 136 * 2 + kConsumers * 128 * 2 +
+         kNBar * sizeof(ChunkDesc) + 64 + (rope ? kRopeSmem : 0);
 }
 
 template <int D, int R8S, bool ROPE>
@@ -578,6 +596,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
   }
   // query rows past the group stay zero (the bulk copies fill rows 0 .. G-1)
   for (int e = threadIdx.x; e < (8 - a.G) * (D + 8); e += kThreads) qsm[a.G * (D + 8) + e] = __float2half(0.f);
+  float2* rsm = reinterpret_cast<float2*>(cdq + kNBar);  // ROPE: [16][kRopeRow] x 2
+  if constexpr (ROPE) {
+    // rows 16 m and i (m, i < 16) of the cache's in-page table
+    const int h = L.rope / 2;
+    const float2* inpage = reinterpret_cast<const float2*>(a.cache + L.off_rope) + (size_t)L.rope_pages * h;
+    for (int e = threadIdx.x; e < 32 * h; e += kThreads) {
+      const int row = e / h, j = e % h;
+      rsm[row * kRopeRow + j] = inpage[(size_t)(row < 16 ? 16 * row : row - 16) * h + j];
+    }
+  }
   __syncthreads();
   griddep_launch();  // the combine grid may be scheduled now; it waits for this grid's completion
 
@@ -689,6 +717,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
   const uint8_t* unit_g = a.cache + (uint64_t)u * L.unit_stride;
   if constexpr (ROPE) {
     rr.tab = reinterpret_cast<const float2*>(a.cache + L.off_rope);
+    rr.s16 = rsm;
+    rr.s1 = rsm + 16 * kRopeRow;
     rr.pages = L.rope_pages;
     rr.h = L.rope / 2;
   }
@@ -868,16 +898,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
             const int nts[4] = {2 * ka, 2 * ka + 1, 2 * kb, 2 * kb + 1};
             // V_K as B fragments (k = r, n = channel): its stored 8x8 blocks (r octet x
             // channel octet, lane L holding r 8o + L/4, channels 2(L%4)..) transposed in registers
+            // (n-tiles 2k, 2k + 1 sit in the same 16-byte lane word of their 32-channel group)
             uint32_t bf[4][RT][2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t col = (uint32_t)((nts[i] >> 2) * 512 + lane * 16 + (nts[i] & 3) * 4);
+            for (int p2 = 0; p2 < 2; ++p2) {
+              const int kx = p2 ? kb : ka;
+              const uint32_t col = (uint32_t)((kx >> 1) * 512 + lane * 16);
+              const bool hi = (kx & 1) != 0;  // n-tiles 2kx, 2kx + 1 are words 2, 3 (else 0, 1)
 #pragma unroll
               for (int kk = 0; kk < RT; ++kk) {
-                bf[i][kk][0] = bf[i][kk][1] = 0u;
+                bf[2 * p2][kk][0] = bf[2 * p2][kk][1] = bf[2 * p2 + 1][kk][0] = bf[2 * p2 + 1][kk][1] = 0u;
                 if (kk < nrt) {
-                  bf[i][kk][0] = movtrans(lds32(vk + (uint32_t)(2 * kk) * 16u * D + col));
-                  if (2 * kk + 1 < nro) bf[i][kk][1] = movtrans(lds32(vk + (uint32_t)(2 * kk + 1) * 16u * D + col));
+                  const uint4 w0 = lds128(vk + (uint32_t)(2 * kk) * 16u * D + col);
+                  bf[2 * p2][kk][0] = movtrans(hi ? w0.z : w0.x);
+                  bf[2 * p2 + 1][kk][0] = movtrans(hi ? w0.w : w0.y);
+                  if (2 * kk + 1 < nro) {
+                    const uint4 w1 = lds128(vk + (uint32_t)(2 * kk + 1) * 16u * D + col);
+                    bf[2 * p2][kk][1] = movtrans(hi ? w1.z : w1.x);
+                    bf[2 * p2 + 1][kk][1] = movtrans(hi ? w1.w : w1.y);
+                  }
                 }
               }
             }
@@ -910,19 +949,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attend_kernel(AttendArgs
                   if (kk < nrt) mma16816(kh[i], uv[kk].x, uv[kk].y, uv[kk].z, uv[kk].w, bf[i][kk][0], bf[i][kk][1]);
               }
               if (rot) {
+                // position 256 b + 16 m + i: m = 4 warp + mt, i = gq or gq + 8
+                const int m16 = ((P00 + 16 * mt) >> 4) & 15;
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                  const int ip = (P00 + 16 * mt + 8 * r) & 255;  // in-page index (the page is block b)
+                for (int i = 0; i < 2; ++i)
 #pragma unroll
-                  for (int i = 0; i < 2; ++i)
+                  for (int e = 0; e < 2; ++e) {
+                    const int j = 8 * nts[i] + 2 * t + e;
+                    const float2 pm = cmul(pg[i][e], rr.s16[m16 * kRopeRow + j]);
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                      const float2 bb = __ldg(rr.tab + (size_t)(rr.pages + ip) * rr.h + 8 * nts[i] + 2 * t + e);
-                      const float2 aa = pg[i][e];
-                      const float2 cs = make_float2(fmaf(aa.x, bb.x, -aa.y * bb.y), fmaf(aa.x, bb.y, aa.y * bb.x));
-                      rot_pair(kh[i][2 * r + e], kh[i + 2][2 * r + e], cs);
-                    }
-                }
+                    for (int r = 0; r < 2; ++r)
+                      rot_pair(kh[i][2 * r + e], kh[i + 2][2 * r + e], cmul(pm, rr.s1[(gq + 8 * r) * kRopeRow + j]));
+                  }
               }
               uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
               split_half2(kh[0][0], kh[0][1], h0, l0);  // a0: row gq, channels 16 ka + 2t..
@@ -1243,7 +1281,7 @@ AttendArgs make_args(const Layout& L, const DecodePlan& P, int n_q_heads, int n_
   a.n_wst = P.n_wchunks;
   a.mode = 0;
   if (a.n_r <= kMaxRanges) fill_ranges(L, a.K_eff, a.nres, a.n_wst, a.n_r, a.tab);
-  const size_t extra = smem_extra();
+  const size_t extra = smem_extra(L.rope != 0);
   a.ring = (int)((kSmemPerCta - extra) / 128 * 128);
   // 64 KB in flight per CTA (about 19 MB over the grid) covers the memory latency at full
   // bandwidth; measured on GB300 against 16, 24, 40 KB and the whole ring (about 103 KB)
