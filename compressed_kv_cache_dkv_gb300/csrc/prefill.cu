@@ -12,8 +12,9 @@
 //   stats:  per (unit, block) the channel min/max of its keys and its mean query (fp32)
 //   route:  per (unit, query block) the bounds of the earlier blocks, ranked on
 //           order-preserving integer keys; the selected blocks written ascending
-//   attend: one CTA of four warps per (64-query tile, query head), 16 queries a
-//           warp; the key tiles of the routed blocks, then those of its own block
+//   attend: head_dim 128 on the tcgen05 tensor cores (prefill_attend_tc_kernel,
+//           below); head_dim 64 on mma.sync: one CTA of four warps per (64-query
+//           tile, query head), 16 queries a warp; the key tiles of the routed blocks, then those of its own block
 //           up to the diagonal one (causal mask), stream through a three-stage
 //           cp.async pipeline of swizzled 64-token K and V tiles.  S = Q K^T and
 //           O += P V on mma.sync m16n8k16 (fp16 operands, fp32 accumulation); the
@@ -45,6 +46,7 @@ struct PfArgs {
   int32_t* routed;   // [units][nb][K_eff]  ascending, -1 past the block's count
   float* out;        // [B][Hq][T][d]
   float* lse;        // [B][Hq][T] or null
+  uint32_t* err;     // the workspace header's device error word
 };
 
 // ---------------------------------------------------------------- stats
@@ -305,6 +307,318 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_attend_kernel(PfArgs a)
   }
 }
 
+// ---------------------------------------------------------------- attend on tcgen05 (head_dim 128)
+// One CTA per (128-query tile, query head): warps w and w + 4 (w < 4) share the
+// query rows of tensor-memory lanes 32 w .. 32 w + 31, one row per thread, the
+// first taking S columns 0..31 and O columns 0..63, the second the rest (their
+// row maxima and sums meet in shared memory); warps 9 and 10 stream the 64-key K
+// and V tiles of the even and the odd tiles with cp.async into a four-stage ring
+// (each stage with a "loaded" and a "free" barrier), and lane 0 of warp 8 issues
+// the products, never waiting for one to complete:
+//   S_j = Q K_j^T   M = 128 queries, N = 64 keys, K = 128     (TMEM, two buffers)
+//   O  += P_j V_j   M = 128, N = 128 channels, K = 64 keys    (TMEM, P as fp16 hi + lo)
+// All operands sit in shared memory as 8x8 core matrices without swizzle: Q and
+// K_j K-major (rows = queries / keys, 16-byte rows of 8 channels), V_j the same
+// bytes read MN-major, P_j K-major (rows = queries, 8 keys a core-matrix row).
+// Online softmax in base 2 with a lazy rescale: the row maximum moves only when
+// a score exceeds it by kPtSlack, and O is rescaled in tensor memory then.  S_{j+1}
+// runs on the tensor cores while the rows work on S_j; P_j is written once O_{j-1}
+// has read P_{j-1}.
+constexpr int kPtThreads = 352;  // 8 softmax warps, the MMA warp, 2 load warps
+constexpr int kPtM = 128, kPtN = 64, kPtStages = 4;
+constexpr float kPtSlack = 8.f;
+constexpr uint32_t kPtTile = kPtN * 128 * 2;                    // one K or V tile: 16 KB
+constexpr uint32_t kPtOffQ = 0;                                  // Q [128 x 128]: 32 KB
+constexpr uint32_t kPtOffKV = kPtOffQ + kPtM * 128 * 2;          // [stage][K | V]
+constexpr uint32_t kPtPBuf = 2 * kPtM * kPtN * 2;                 // P: hi [128 x 64] | lo, 32 KB
+constexpr uint32_t kPtOffP = kPtOffKV + kPtStages * 2 * kPtTile;
+constexpr uint32_t kPtOffR = kPtOffP + kPtPBuf;                  // routed blocks [kPfMaxRouted]
+constexpr uint32_t kPtOffX = kPtOffR + kPfMaxRouted * 4;         // row maxima / sums of the two halves
+constexpr uint32_t kPtOffBar = kPtOffX + 2 * kPtM * 4;          // mbarriers, TMEM address
+constexpr uint32_t kPtSmem = kPtOffBar + 256;
+constexpr uint32_t kPtTmemCols = 256;  // S buffers at 0 and 64, O at 128
+constexpr uint32_t kPtColO = 128;
+
+__device__ inline uint64_t pt_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3fffu) | ((uint64_t)((lbo >> 4) & 0x3fffu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3fffu) << 32) | (1ull << 46);
+}
+// D f32, A and B f16, M = 128, N = n; a_mn / b_mn: MN-major operand
+__device__ inline uint32_t pt_idesc(bool a_mn, bool b_mn, uint32_t n) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((n >> 3) << 17) | ((128u >> 4) << 24);
+}
+__device__ inline void pt_mma(uint32_t dt, uint64_t ad, uint64_t bd, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dt),
+      "l"(ad), "l"(bd), "r"(id), "r"(acc)
+      : "memory");
+}
+__device__ inline void pt_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ inline void pt_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ inline void pt_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ inline void pt_fence_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// 16 consecutive fp32 columns of this thread's lane; the caller waits (pt_ld_wait)
+__device__ inline void pt_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ inline void pt_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ inline void pt_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ inline void pt_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ inline void pt_sts128(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+// byte offset of (row, 16-byte chunk cc) of a K-major [rows x 128] fp16 operand in core matrices
+__device__ inline uint32_t pt_core(int row, int cc) {
+  return (uint32_t)((row >> 3) * 2048 + cc * 128 + (row & 7) * 16);
+}
+
+__global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs a, int nq) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const uint32_t sb = smem_u32(smem);
+  int* rsm = reinterpret_cast<int*>(smem + kPtOffR);
+  uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + kPtOffBar);  // [2] S_j ready (commit)
+  uint64_t* bar_sf = bar_s + 2;                                      // [2] S_j read by the 256 row threads
+  uint64_t* bar_p = bar_s + 4;                                       // P_j written by the 256 row threads
+  uint64_t* bar_o = bar_s + 5;                                       // O += P_j V_j done (commit)
+  uint64_t* bar_kv = bar_s + 6;                                      // [4] stage loaded (32 loader lanes)
+  uint64_t* bar_fr = bar_s + 10;                                     // [4] stage free again (commit)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 14);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int qt = nq - 1 - (int)blockIdx.x;  // later tiles (more keys without routing) first
+  const int q0 = qt * kPtM, hq = blockIdx.y, b = blockIdx.z;
+  const int h = hq / a.G, u = b * a.Hkv + h, i = q0 / 256;
+  const int n_r = min(i, a.K_eff);
+  const int ntile = 4 * n_r + (q0 + kPtM - i * 256) / kPtN;
+  const __half* Kb = a.K + (size_t)u * a.T * 128;
+  const __half* Vb = a.V + (size_t)u * a.T * 128;
+  for (int x = tid; x < n_r; x += kPtThreads) rsm[x] = a.routed[((size_t)u * a.nb + i) * a.K_eff + x];
+  if (tid == 0) {
+    mbar_init(&bar_s[0], 1);
+    mbar_init(&bar_s[1], 1);
+    mbar_init(&bar_sf[0], 256);
+    mbar_init(&bar_sf[1], 256);
+    mbar_init(bar_p, 256);
+    mbar_init(bar_o, 1);
+    for (int x = 0; x < kPtStages; ++x) {
+      mbar_init(&bar_kv[x], 32);
+      mbar_init(&bar_fr[x], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "n"(kPtTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  pt_fence_before();
+  __syncthreads();
+  pt_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto key0 = [&](int p) -> int {
+    return p < 4 * n_r ? rsm[p >> 2] * 256 + (p & 3) * kPtN : i * 256 + (p - 4 * n_r) * kPtN;
+  };
+  bool ok = true;
+
+  if (warp >= 9) {
+    // =========================== loads: warp 9 the even tiles (and Q), warp 10 the odd ones
+    const int par = warp - 9;
+    auto load_kv = [&](int p) {
+      if (p < ntile) {
+        const int k0 = key0(p);
+        const uint32_t kd = sb + kPtOffKV + (uint32_t)(p % kPtStages) * 2u * kPtTile, vd = kd + kPtTile;
+        // one instruction fills 8 rows x 4 chunks: 512 contiguous bytes of core matrices (no bank conflict)
+#pragma unroll 4
+        for (int it = 0; it < kPtN * 16 / 32; ++it) {
+          const int r = 8 * (it >> 2) + (lane & 7), cc = 4 * (it & 3) + (lane >> 3), tok = k0 + r;
+          const bool valid = tok < a.T;
+          const size_t off = (size_t)(valid ? tok : 0) * 128 + cc * 8;  // rows past the prompt read zeros
+          pf_cp16(kd + pt_core(r, cc), Kb + off, valid ? 16u : 0u);
+          pf_cp16(vd + pt_core(r, cc), Vb + off, valid ? 16u : 0u);
+        }
+      }
+      pf_commit();
+    };
+    if (par == 0) {  // Q with tile 0
+      const __half* qp = a.q + ((size_t)b * a.Hq + hq) * a.T * 128;
+      for (int it = 0; it < kPtM * 16 / 32; ++it) {
+        const int r = 8 * (it >> 2) + (lane & 7), cc = 4 * (it & 3) + (lane >> 3), tok = q0 + r;
+        const bool valid = tok < a.T;
+        pf_cp16(sb + kPtOffQ + pt_core(r, cc), qp + (size_t)(valid ? tok : 0) * 128 + cc * 8, valid ? 16u : 0u);
+      }
+    }
+    load_kv(par);
+    load_kv(par + 2);
+    for (int p = par; p < ntile; p += 2) {
+      pf_wait<1>();  // tile p (this lane's copies); tile p + 2 may still be in flight
+      pt_fence_async();
+      mbar_arrive(&bar_kv[p % kPtStages]);
+      if (p + 4 < ntile) {  // stage p % 4 takes tile p + 4 once O_p has read it
+        if (ok) ok = mbar_wait(&bar_fr[p % kPtStages], (uint32_t)((p / kPtStages) & 1), a.err);
+        if (ok) load_kv(p + 4);
+        else pf_commit();
+      } else {
+        pf_commit();
+      }
+    }
+    pf_wait<0>();
+  } else if (warp == 8) {
+    // =========================== tensor-core issue (lane 0)
+    if (lane == 0 && ntile > 0) {
+      const uint64_t qdesc = pt_sdesc(sb + kPtOffQ, 128u, 2048u);
+      const uint32_t id_s = pt_idesc(false, false, kPtN), id_o = pt_idesc(false, true, 128);
+      auto issue_s = [&](int j) {  // S_j = Q K_j^T into buffer j % 2, once tile j has landed
+        if (ok) ok = mbar_wait(&bar_kv[j % kPtStages], (uint32_t)((j / kPtStages) & 1), a.err);
+        pt_fence_after();
+        const uint64_t kdesc = pt_sdesc(sb + kPtOffKV + (uint32_t)(j % kPtStages) * 2u * kPtTile, 128u, 2048u);
+        const uint32_t dt = tmem + (uint32_t)(j & 1) * kPtN;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          pt_mma(dt, qdesc + (uint64_t)(ks * 16), kdesc + (uint64_t)(ks * 16), id_s, ks > 0);
+        pt_commit(&bar_s[j & 1]);
+      };
+      issue_s(0);
+      const uint64_t ph = pt_sdesc(sb + kPtOffP, 128u, 1024u), pl = pt_sdesc(sb + kPtOffP + kPtM * kPtN * 2, 128u, 1024u);
+      for (int j = 0; j < ntile && ok; ++j) {
+        if (j + 1 < ntile) {
+          if (j >= 1) ok = mbar_wait(&bar_sf[(j + 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), a.err);  // S_{j-1} read
+          if (ok) issue_s(j + 1);
+        }
+        if (ok) ok = mbar_wait(bar_p, (uint32_t)(j & 1), a.err);  // P_j written
+        pt_fence_after();
+        if (!ok) break;
+        const uint64_t vdesc = pt_sdesc(sb + kPtOffKV + (uint32_t)(j % kPtStages) * 2u * kPtTile + kPtTile, 2048u, 128u);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          pt_mma(tmem + kPtColO, ph + (uint64_t)(ks * 16), vdesc + (uint64_t)(ks * 256), id_o, (j > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          pt_mma(tmem + kPtColO, pl + (uint64_t)(ks * 16), vdesc + (uint64_t)(ks * 256), id_o, 1u);
+        pt_commit(bar_o);
+        pt_commit(&bar_fr[j % kPtStages]);
+      }
+    }
+  } else {
+    // =========================== softmax: warps w and w + 4 share the rows of lane
+    // quarter w (query q0 + 32 w + lane), half 0 taking S columns 0..31, half 1 32..63
+    const int rw = warp & 3, half = warp >> 2, row = 32 * rw + lane, qrow = q0 + row;
+    const uint32_t tl = tmem + ((uint32_t)(rw * 32) << 16);
+    const float slog2 = a.scale_log2;
+    float* xch = reinterpret_cast<float*>(smem + kPtOffX);  // [2][128]: the halves' row maxima / sums
+    float m = -INFINITY, l = 0.f;
+    const uint32_t prow = sb + kPtOffP + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 16u + (uint32_t)half * 512u;
+    for (int j = 0; j < ntile; ++j) {
+      if (ok) ok = mbar_wait(&bar_s[j & 1], (uint32_t)((j >> 1) & 1), a.err);
+      pt_fence_after();
+      uint32_t r[2][16];
+      const uint32_t sc = tl + (uint32_t)(j & 1) * kPtN + 32u * (uint32_t)half;
+      pt_ld16(sc, r[0]);
+      pt_ld16(sc + 16, r[1]);
+      pt_ld_wait();
+      pt_fence_before();
+      mbar_arrive(&bar_sf[j & 1]);  // S_j may be overwritten by S_{j+2}
+      const int k0 = key0(j) + 32 * half;
+      // keys k0 + c valid for c < nv: before the prompt's end, and causal on the diagonal tiles
+      const int nv = min(a.T, qrow + 1) - k0;
+      float s[32], mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        s[c] = c < nv ? __uint_as_float(r[c >> 4][c & 15]) * slog2 : -INFINITY;
+        mxp[c & 3] = fmaxf(mxp[c & 3], s[c]);
+      }
+      float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
+      xch[half * 128 + row] = mx;
+      named_bar_sync(1, 256);
+      mx = fmaxf(mx, xch[(half ^ 1) * 128 + row]);
+      named_bar_sync(1, 256);  // both halves read before the next tile's store
+      // O_{j-1} done: P's buffer is free and O may be rescaled
+      const bool up = mx > m + kPtSlack;
+      const bool resc = __any_sync(0xffffffffu, up) && j > 0;  // the same rows in both halves' warps
+      if (j > 0 && ok) ok = mbar_wait(bar_o, (uint32_t)((j - 1) & 1), a.err);
+      pt_fence_after();
+      if (resc) {
+        const float nm = up ? mx : m;
+        const float al = fast_exp2(m - nm);
+        l *= al;
+        m = nm;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // this half's 64 of O's 128 columns
+          uint32_t o[16];
+          const uint32_t oc = tl + kPtColO + 64u * (uint32_t)half + 16u * (uint32_t)c;
+          pt_ld16(oc, o);
+          pt_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * al);
+          pt_st16(oc, o);
+        }
+        pt_st_wait();
+      } else if (up) {
+        m = mx;  // the first tile: no O yet
+      }
+      const float ms = m == -INFINITY ? 0.f : m;
+      const uint32_t pbase = prow;
+      float lp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {  // 8 keys per core-matrix row: hi at P, lo at P + 16 KB
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = fast_exp2(s[8 * g + 2 * e] - ms), p1 = fast_exp2(s[8 * g + 2 * e + 1] - ms);
+          lp[e] += p0 + p1;
+          split_half2(p0, p1, hi[e], lo[e]);
+        }
+        pt_sts128(pbase + (uint32_t)g * 128u, hi[0], hi[1], hi[2], hi[3]);
+        pt_sts128(pbase + kPtM * kPtN * 2 + (uint32_t)g * 128u, lo[0], lo[1], lo[2], lo[3]);
+      }
+      l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
+      pt_fence_async();
+      pt_fence_before();
+      mbar_arrive(bar_p);
+    }
+    // the row sum over both halves, then the last O: normalise and store this half's columns
+    xch[half * 128 + row] = l;
+    named_bar_sync(1, 256);
+    l += xch[(half ^ 1) * 128 + row];
+    if (ntile > 0 && ok) ok = mbar_wait(bar_o, (uint32_t)((ntile - 1) & 1), a.err);
+    pt_fence_after();
+    const float il = 1.f / l;
+    float* orow = a.out + (((size_t)b * a.Hq + hq) * a.T + (size_t)min(qrow, a.T - 1)) * 128 + 64 * half;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[16];
+      pt_ld16(tl + kPtColO + 64u * (uint32_t)half + 16u * (uint32_t)c, o);
+      pt_ld_wait();
+      if (qrow < a.T) {
+#pragma unroll
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<float4*>(orow + 16 * c + e) =
+              make_float4(__uint_as_float(o[e]) * il, __uint_as_float(o[e + 1]) * il, __uint_as_float(o[e + 2]) * il,
+                          __uint_as_float(o[e + 3]) * il);
+      }
+    }
+    if (half == 0 && a.lse && qrow < a.T) a.lse[((size_t)b * a.Hq + hq) * a.T + qrow] = (m + log2f(l)) * 0.6931471805599453f;
+  }
+  pt_fence_before();
+  __syncthreads();
+  pt_fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kPtTmemCols) : "memory");
+}
+
 template <int D>
 cudaError_t launch_prefill_d(const PfArgs& a, int batch, cudaStream_t s) {
   const int units = batch * a.Hkv;
@@ -314,6 +628,13 @@ cudaError_t launch_prefill_d(const PfArgs& a, int batch, cudaStream_t s) {
   prefill_route_kernel<D><<<dim3(a.nb, units), 256, (size_t)a.nb * 4, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (D == 128) {  // tensor cores with TMEM accumulators
+    e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_attend_tc_kernel), kPtSmem);
+    if (e != cudaSuccess) return e;
+    const int nq = (a.T + kPtM - 1) / kPtM;
+    prefill_attend_tc_kernel<<<dim3(nq, a.Hq, batch), kPtThreads, kPtSmem, s>>>(a, nq);
+    return cudaGetLastError();
+  }
   const size_t smem = (size_t)kPfStages * 2 * kPfKTile * D * 2 + (size_t)kPfMaxRouted * 4;
   e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_attend_kernel<D>), smem);
   if (e != cudaSuccess) return e;
@@ -356,6 +677,7 @@ cudaError_t launch_prefill(int batch, int n_q_heads, int n_kv_heads, int d, int 
   a.routed = routed_out ? routed_out : reinterpret_cast<int32_t*>(ws + P.off_routed);
   a.out = out;
   a.lse = lse;
+  a.err = reinterpret_cast<uint32_t*>(ws);
   return d == 128 ? launch_prefill_d<128>(a, batch, s) : launch_prefill_d<64>(a, batch, s);
 }
 
