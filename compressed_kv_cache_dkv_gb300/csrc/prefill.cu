@@ -308,35 +308,37 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_attend_kernel(PfArgs a)
 }
 
 // ---------------------------------------------------------------- attend on tcgen05 (head_dim 128)
-// One CTA per (128-query tile, query head): warps w and w + 4 (w < 4) share the
-// query rows of tensor-memory lanes 32 w .. 32 w + 31, one row per thread, the
-// first taking S columns 0..31 and O columns 0..63, the second the rest (their
-// row maxima and sums meet in shared memory); warps 9 and 10 stream the 64-key K
-// and V tiles of the even and the odd tiles with cp.async into a four-stage ring
-// (each stage with a "loaded" and a "free" barrier), and lane 0 of warp 8 issues
-// the products, never waiting for one to complete:
-//   S_j = Q K_j^T   M = 128 queries, N = 64 keys, K = 128     (TMEM, two buffers)
-//   O  += P_j V_j   M = 128, N = 128 channels, K = 64 keys    (TMEM, P as fp16 hi + lo)
+// One CTA per (256-token query block, query head), as two groups of 128 query rows
+// (A: the block's first 128 queries, B: the rest) that share every K and V tile, so
+// a tile crosses from L2 once for 256 rows.  Warps 0-3 own group A's rows and warps
+// 4-7 group B's, one row per thread in tensor-memory lane 32 (w % 4) + lane; warp 9
+// streams the 64-key K and V tiles with cp.async into a three-stage ring: a stage
+// takes tile t once the products of tile t - 3 have read it, and each lane's copies
+// arrive on the stage's "loaded" barrier by themselves when they land
+// (cp.async.mbarrier.arrive), so no arrival waits on a later product; lane 0 of
+// warp 8 issues the products of both groups, never waiting for one:
+//   S_gj = Q_g K_j^T   M = 128 queries, N = 64 keys, K = 128     (TMEM, two buffers per group)
+//   O_g += P_gj V_j    M = 128, N = 128 channels, K = 64 keys    (TMEM, P as fp16 hi + lo)
 // All operands sit in shared memory as 8x8 core matrices without swizzle: Q and
 // K_j K-major (rows = queries / keys, 16-byte rows of 8 channels), V_j the same
-// bytes read MN-major, P_j K-major (rows = queries, 8 keys a core-matrix row).
-// Online softmax in base 2 with a lazy rescale: the row maximum moves only when
-// a score exceeds it by kPtSlack, and O is rescaled in tensor memory then.  S_{j+1}
-// runs on the tensor cores while the rows work on S_j; P_j is written once O_{j-1}
-// has read P_{j-1}.
-constexpr int kPtThreads = 352;  // 8 softmax warps, the MMA warp, 2 load warps
-constexpr int kPtM = 128, kPtN = 64, kPtStages = 4;
+// bytes read MN-major, P_gj K-major (rows = queries, 8 keys a core-matrix row).
+// Group A stops after the block's second own tile (keys past its last query).
+// Online softmax in base 2 with a lazy rescale: the row maximum moves only when a
+// score exceeds it by kPtSlack, and O is rescaled in tensor memory then.  S_{j+1}
+// runs on the tensor cores while the rows work on S_j; P_gj is written once O_{g,j-1}
+// has read P_{g,j-1}.
+constexpr int kPtThreads = 320;  // 8 softmax warps (two groups), the MMA warp, the load warp
+constexpr int kPtM = 128, kPtN = 64, kPtStages = 3;
 constexpr float kPtSlack = 8.f;
 constexpr uint32_t kPtTile = kPtN * 128 * 2;                    // one K or V tile: 16 KB
-constexpr uint32_t kPtOffQ = 0;                                  // Q [128 x 128]: 32 KB
-constexpr uint32_t kPtOffKV = kPtOffQ + kPtM * 128 * 2;          // [stage][K | V]
-constexpr uint32_t kPtPBuf = 2 * kPtM * kPtN * 2;                 // P: hi [128 x 64] | lo, 32 KB
-constexpr uint32_t kPtOffP = kPtOffKV + kPtStages * 2 * kPtTile;
-constexpr uint32_t kPtOffR = kPtOffP + kPtPBuf;                  // routed blocks [kPfMaxRouted]
-constexpr uint32_t kPtOffX = kPtOffR + kPfMaxRouted * 4;         // row maxima / sums of the two halves
-constexpr uint32_t kPtOffBar = kPtOffX + 2 * kPtM * 4;          // mbarriers, TMEM address
+constexpr uint32_t kPtQ = kPtM * 128 * 2;                       // one group's Q: 32 KB
+constexpr uint32_t kPtPBuf = 2 * kPtM * kPtN * 2;               // one group's P: hi [128 x 64] | lo, 32 KB
+constexpr uint32_t kPtOffQ = 0;                                 // Q_A | Q_B
+constexpr uint32_t kPtOffKV = kPtOffQ + 2 * kPtQ;               // [stage][K | V]
+constexpr uint32_t kPtOffP = kPtOffKV + kPtStages * 2 * kPtTile; // P_A | P_B
+constexpr uint32_t kPtOffBar = kPtOffP + 2 * kPtPBuf;           // mbarriers, TMEM address
 constexpr uint32_t kPtSmem = kPtOffBar + 256;
-constexpr uint32_t kPtTmemCols = 256;  // S buffers at 0 and 64, O at 128
+constexpr uint32_t kPtTmemCols = 512;  // per group g: S buffers at 256 g + {0, 64}, O at 256 g + 128
 constexpr uint32_t kPtColO = 128;
 
 __device__ inline uint64_t pt_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -378,6 +380,11 @@ __device__ inline void pt_st16(uint32_t taddr, const uint32_t (&r)[16]) {
       : "memory");
 }
 __device__ inline void pt_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// arrive on `bar` once every cp.async this thread issued so far has landed (no count increment)
+__device__ inline void pt_cp_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ inline void pt_cp_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ inline void pt_sts128(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }
@@ -386,33 +393,38 @@ __device__ inline uint32_t pt_core(int row, int cc) {
   return (uint32_t)((row >> 3) * 2048 + cc * 128 + (row & 7) * 16);
 }
 
-__global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs a, int nq) {
+__global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs a, int nqb) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
-  int* rsm = reinterpret_cast<int*>(smem + kPtOffR);
-  uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + kPtOffBar);  // [2] S_j ready (commit)
-  uint64_t* bar_sf = bar_s + 2;                                      // [2] S_j read by the 256 row threads
-  uint64_t* bar_p = bar_s + 4;                                       // P_j written by the 256 row threads
-  uint64_t* bar_o = bar_s + 5;                                       // O += P_j V_j done (commit)
-  uint64_t* bar_kv = bar_s + 6;                                      // [4] stage loaded (32 loader lanes)
-  uint64_t* bar_fr = bar_s + 10;                                     // [4] stage free again (commit)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 14);
+  uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + kPtOffBar);  // [group][2] S_gj ready (commit)
+  uint64_t* bar_sf = bar_s + 4;                                      // [group][2] S_gj read by the group's rows
+  uint64_t* bar_p = bar_s + 8;                                       // [group] P_gj written by the group's rows
+  uint64_t* bar_o = bar_s + 10;                                      // [group] O_g += P_gj V_j done (commit)
+  uint64_t* bar_kv = bar_s + 12;                                     // [3] stage loaded (32 loader lanes)
+  uint64_t* bar_fr = bar_s + 15;                                     // [3] stage free again (commit)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 18);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  const int qt = nq - 1 - (int)blockIdx.x;  // later tiles (more keys without routing) first
-  const int q0 = qt * kPtM, hq = blockIdx.y, b = blockIdx.z;
-  const int h = hq / a.G, u = b * a.Hkv + h, i = q0 / 256;
+  const int i = nqb - 1 - (int)blockIdx.x;  // later query blocks (more keys without routing) first
+  const int q0 = i * 256, hq = blockIdx.y, b = blockIdx.z;
+  const int h = hq / a.G, u = b * a.Hkv + h;
   const int n_r = min(i, a.K_eff);
-  const int ntile = 4 * n_r + (q0 + kPtM - i * 256) / kPtN;
+  // query rows of the groups and the own-block tiles each needs (up to its last query)
+  const int rowsA = min(kPtM, a.T - q0), rowsB = max(0, min(kPtM, a.T - q0 - kPtM));
+  const int ownA = (rowsA + kPtN - 1) / kPtN, ownB = rowsB > 0 ? (kPtM + rowsB + kPtN - 1) / kPtN : 0;
+  const int ntA = 4 * n_r + ownA, ntB = rowsB > 0 ? 4 * n_r + ownB : 0;
+  const int ntile = max(ntA, ntB);
+  const int32_t* routed = a.routed + ((size_t)u * a.nb + i) * a.K_eff;
   const __half* Kb = a.K + (size_t)u * a.T * 128;
   const __half* Vb = a.V + (size_t)u * a.T * 128;
-  for (int x = tid; x < n_r; x += kPtThreads) rsm[x] = a.routed[((size_t)u * a.nb + i) * a.K_eff + x];
   if (tid == 0) {
-    mbar_init(&bar_s[0], 1);
-    mbar_init(&bar_s[1], 1);
-    mbar_init(&bar_sf[0], 256);
-    mbar_init(&bar_sf[1], 256);
-    mbar_init(bar_p, 256);
-    mbar_init(bar_o, 1);
+    for (int x = 0; x < 4; ++x) {
+      mbar_init(&bar_s[x], 1);
+      mbar_init(&bar_sf[x], 128);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar_p[x], 128);
+      mbar_init(&bar_o[x], 1);
+    }
     for (int x = 0; x < kPtStages; ++x) {
       mbar_init(&bar_kv[x], 32);
       mbar_init(&bar_fr[x], 1);
@@ -429,126 +441,115 @@ __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs
   __syncthreads();
   pt_fence_after();
   const uint32_t tmem = *tmem_slot;
-  auto key0 = [&](int p) -> int {
-    return p < 4 * n_r ? rsm[p >> 2] * 256 + (p & 3) * kPtN : i * 256 + (p - 4 * n_r) * kPtN;
-  };
   bool ok = true;
 
-  if (warp >= 9) {
-    // =========================== loads: warp 9 the even tiles (and Q), warp 10 the odd ones
-    const int par = warp - 9;
+  if (warp == 9) {
+    // =========================== loads (Q with tile 0)
     auto load_kv = [&](int p) {
-      if (p < ntile) {
-        const int k0 = key0(p);
-        const uint32_t kd = sb + kPtOffKV + (uint32_t)(p % kPtStages) * 2u * kPtTile, vd = kd + kPtTile;
-        // one instruction fills 8 rows x 4 chunks: 512 contiguous bytes of core matrices (no bank conflict)
+      const int k0 = p < 4 * n_r ? __ldg(routed + (p >> 2)) * 256 + (p & 3) * kPtN : q0 + (p - 4 * n_r) * kPtN;
+      const uint32_t kd = sb + kPtOffKV + (uint32_t)(p % kPtStages) * 2u * kPtTile, vd = kd + kPtTile;
+      // one instruction fills 8 rows x 4 chunks: 512 contiguous bytes of core matrices
 #pragma unroll 4
-        for (int it = 0; it < kPtN * 16 / 32; ++it) {
-          const int r = 8 * (it >> 2) + (lane & 7), cc = 4 * (it & 3) + (lane >> 3), tok = k0 + r;
-          const bool valid = tok < a.T;
-          const size_t off = (size_t)(valid ? tok : 0) * 128 + cc * 8;  // rows past the prompt read zeros
-          pf_cp16(kd + pt_core(r, cc), Kb + off, valid ? 16u : 0u);
-          pf_cp16(vd + pt_core(r, cc), Vb + off, valid ? 16u : 0u);
-        }
+      for (int it = 0; it < kPtN * 16 / 32; ++it) {
+        const int r = 8 * (it >> 2) + (lane & 7), cc = 4 * (it & 3) + (lane >> 3), tok = k0 + r;
+        const bool valid = tok < a.T;
+        const size_t off = (size_t)(valid ? tok : 0) * 128 + cc * 8;  // rows past the prompt read zeros
+        pf_cp16(kd + pt_core(r, cc), Kb + off, valid ? 16u : 0u);
+        pf_cp16(vd + pt_core(r, cc), Vb + off, valid ? 16u : 0u);
       }
-      pf_commit();
     };
-    if (par == 0) {  // Q with tile 0
+    {
       const __half* qp = a.q + ((size_t)b * a.Hq + hq) * a.T * 128;
-      for (int it = 0; it < kPtM * 16 / 32; ++it) {
+      for (int it = 0; it < 2 * kPtM * 16 / 32; ++it) {
         const int r = 8 * (it >> 2) + (lane & 7), cc = 4 * (it & 3) + (lane >> 3), tok = q0 + r;
         const bool valid = tok < a.T;
-        pf_cp16(sb + kPtOffQ + pt_core(r, cc), qp + (size_t)(valid ? tok : 0) * 128 + cc * 8, valid ? 16u : 0u);
+        pf_cp16(sb + kPtOffQ + (uint32_t)(r >> 7) * kPtQ + pt_core(r & 127, cc), qp + (size_t)(valid ? tok : 0) * 128 + cc * 8,
+                valid ? 16u : 0u);
       }
     }
-    load_kv(par);
-    load_kv(par + 2);
-    for (int p = par; p < ntile; p += 2) {
-      pf_wait<1>();  // tile p (this lane's copies); tile p + 2 may still be in flight
-      pt_fence_async();
-      mbar_arrive(&bar_kv[p % kPtStages]);
-      if (p + 4 < ntile) {  // stage p % 4 takes tile p + 4 once O_p has read it
-        if (ok) ok = mbar_wait(&bar_fr[p % kPtStages], (uint32_t)((p / kPtStages) & 1), a.err);
-        if (ok) load_kv(p + 4);
-        else pf_commit();
-      } else {
-        pf_commit();
-      }
+    for (int p = 0; p < ntile && ok; ++p) {
+      // stage p % 3 held tile p - 3: wait until every product that reads it is done
+      if (p >= kPtStages) ok = mbar_wait(&bar_fr[p % kPtStages], (uint32_t)(((p / kPtStages) - 1) & 1), a.err);
+      if (!ok) break;
+      load_kv(p);
+      pt_cp_arrive(&bar_kv[p % kPtStages]);
     }
-    pf_wait<0>();
+    pt_cp_wait_all();
   } else if (warp == 8) {
     // =========================== tensor-core issue (lane 0)
     if (lane == 0 && ntile > 0) {
-      const uint64_t qdesc = pt_sdesc(sb + kPtOffQ, 128u, 2048u);
       const uint32_t id_s = pt_idesc(false, false, kPtN), id_o = pt_idesc(false, true, 128);
-      auto issue_s = [&](int j) {  // S_j = Q K_j^T into buffer j % 2, once tile j has landed
+      auto issue_s = [&](int j) {  // S_gj = Q_g K_j^T into buffer j % 2 of each group that takes tile j
         if (ok) ok = mbar_wait(&bar_kv[j % kPtStages], (uint32_t)((j / kPtStages) & 1), a.err);
+        pt_fence_async();  // the landed cp.async bytes, seen through the barrier, for the tensor cores
         pt_fence_after();
         const uint64_t kdesc = pt_sdesc(sb + kPtOffKV + (uint32_t)(j % kPtStages) * 2u * kPtTile, 128u, 2048u);
-        const uint32_t dt = tmem + (uint32_t)(j & 1) * kPtN;
+        for (int g = 0; g < 2; ++g) {
+          if (j >= (g ? ntB : ntA)) continue;
+          if (j >= 2 && ok) ok = mbar_wait(&bar_sf[2 * g + (j & 1)], (uint32_t)(((j - 2) >> 1) & 1), a.err);  // S_{g,j-2} read
+          pt_fence_after();
+          const uint64_t qdesc = pt_sdesc(sb + kPtOffQ + (uint32_t)g * kPtQ, 128u, 2048u);
+          const uint32_t dt = tmem + 256u * (uint32_t)g + (uint32_t)(j & 1) * kPtN;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          pt_mma(dt, qdesc + (uint64_t)(ks * 16), kdesc + (uint64_t)(ks * 16), id_s, ks > 0);
-        pt_commit(&bar_s[j & 1]);
+          for (int ks = 0; ks < 8; ++ks)
+            pt_mma(dt, qdesc + (uint64_t)(ks * 16), kdesc + (uint64_t)(ks * 16), id_s, ks > 0);
+          pt_commit(&bar_s[2 * g + (j & 1)]);
+        }
       };
       issue_s(0);
-      const uint64_t ph = pt_sdesc(sb + kPtOffP, 128u, 1024u), pl = pt_sdesc(sb + kPtOffP + kPtM * kPtN * 2, 128u, 1024u);
       for (int j = 0; j < ntile && ok; ++j) {
-        if (j + 1 < ntile) {
-          if (j >= 1) ok = mbar_wait(&bar_sf[(j + 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), a.err);  // S_{j-1} read
-          if (ok) issue_s(j + 1);
-        }
-        if (ok) ok = mbar_wait(bar_p, (uint32_t)(j & 1), a.err);  // P_j written
-        pt_fence_after();
-        if (!ok) break;
+        if (j + 1 < ntile) issue_s(j + 1);
         const uint64_t vdesc = pt_sdesc(sb + kPtOffKV + (uint32_t)(j % kPtStages) * 2u * kPtTile + kPtTile, 2048u, 128u);
+        for (int g = 0; g < 2 && ok; ++g) {
+          if (j >= (g ? ntB : ntA)) continue;
+          ok = mbar_wait(&bar_p[g], (uint32_t)(j & 1), a.err);  // P_gj written
+          pt_fence_after();
+          if (!ok) break;
+          const uint32_t pb = sb + kPtOffP + (uint32_t)g * kPtPBuf;
+          const uint64_t ph = pt_sdesc(pb, 128u, 1024u), pl = pt_sdesc(pb + kPtM * kPtN * 2, 128u, 1024u);
+          const uint32_t dt = tmem + 256u * (uint32_t)g + kPtColO;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          pt_mma(tmem + kPtColO, ph + (uint64_t)(ks * 16), vdesc + (uint64_t)(ks * 256), id_o, (j > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < 4; ++ks)
+            pt_mma(dt, ph + (uint64_t)(ks * 16), vdesc + (uint64_t)(ks * 256), id_o, (j > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          pt_mma(tmem + kPtColO, pl + (uint64_t)(ks * 16), vdesc + (uint64_t)(ks * 256), id_o, 1u);
-        pt_commit(bar_o);
-        pt_commit(&bar_fr[j % kPtStages]);
+          for (int ks = 0; ks < 4; ++ks) pt_mma(dt, pl + (uint64_t)(ks * 16), vdesc + (uint64_t)(ks * 256), id_o, 1u);
+          pt_commit(&bar_o[g]);
+        }
+        pt_commit(&bar_fr[j % kPtStages]);  // every product that reads tile j is issued
       }
     }
   } else {
-    // =========================== softmax: warps w and w + 4 share the rows of lane
-    // quarter w (query q0 + 32 w + lane), half 0 taking S columns 0..31, half 1 32..63
-    const int rw = warp & 3, half = warp >> 2, row = 32 * rw + lane, qrow = q0 + row;
-    const uint32_t tl = tmem + ((uint32_t)(rw * 32) << 16);
+    // =========================== softmax: group g = warp / 4, one query row per thread
+    const int g = warp >> 2, rw = warp & 3, row = 32 * rw + lane, qrow = q0 + kPtM * g + row;
+    const int nt = g ? ntB : ntA;
+    const uint32_t tl = tmem + ((uint32_t)(rw * 32) << 16) + 256u * (uint32_t)g;
     const float slog2 = a.scale_log2;
-    float* xch = reinterpret_cast<float*>(smem + kPtOffX);  // [2][128]: the halves' row maxima / sums
     float m = -INFINITY, l = 0.f;
-    const uint32_t prow = sb + kPtOffP + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 16u + (uint32_t)half * 512u;
-    for (int j = 0; j < ntile; ++j) {
-      if (ok) ok = mbar_wait(&bar_s[j & 1], (uint32_t)((j >> 1) & 1), a.err);
+    const uint32_t pbase = sb + kPtOffP + (uint32_t)g * kPtPBuf + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 16u;
+    for (int j = 0; j < nt; ++j) {
+      if (ok) ok = mbar_wait(&bar_s[2 * g + (j & 1)], (uint32_t)((j >> 1) & 1), a.err);
       pt_fence_after();
-      uint32_t r[2][16];
-      const uint32_t sc = tl + (uint32_t)(j & 1) * kPtN + 32u * (uint32_t)half;
-      pt_ld16(sc, r[0]);
-      pt_ld16(sc + 16, r[1]);
+      uint32_t r[4][16];
+      const uint32_t sc = tl + (uint32_t)(j & 1) * kPtN;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) pt_ld16(sc + 16 * c, r[c]);
       pt_ld_wait();
       pt_fence_before();
-      mbar_arrive(&bar_sf[j & 1]);  // S_j may be overwritten by S_{j+2}
-      const int k0 = key0(j) + 32 * half;
-      // keys k0 + c valid for c < nv: before the prompt's end, and causal on the diagonal tiles
-      const int nv = min(a.T, qrow + 1) - k0;
-      float s[32], mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      mbar_arrive(&bar_sf[2 * g + (j & 1)]);  // S_gj may be overwritten by S_{g,j+2}
+      const int k0 = j < 4 * n_r ? 0 : q0 + (j - 4 * n_r) * kPtN;  // routed tiles: every key is earlier
+      // keys k0 + c valid for c < nv: before the prompt's end, and causal in the own block
+      const int nv = j < 4 * n_r ? kPtN : min(a.T, qrow + 1) - k0;
+      float s[64], mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < 64; ++c) {
         s[c] = c < nv ? __uint_as_float(r[c >> 4][c & 15]) * slog2 : -INFINITY;
         mxp[c & 3] = fmaxf(mxp[c & 3], s[c]);
       }
-      float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
-      xch[half * 128 + row] = mx;
-      named_bar_sync(1, 256);
-      mx = fmaxf(mx, xch[(half ^ 1) * 128 + row]);
-      named_bar_sync(1, 256);  // both halves read before the next tile's store
-      // O_{j-1} done: P's buffer is free and O may be rescaled
+      const float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
+      // O_{g,j-1} done: P_g's buffer is free and O_g may be rescaled
       const bool up = mx > m + kPtSlack;
-      const bool resc = __any_sync(0xffffffffu, up) && j > 0;  // the same rows in both halves' warps
-      if (j > 0 && ok) ok = mbar_wait(bar_o, (uint32_t)((j - 1) & 1), a.err);
+      const bool resc = __any_sync(0xffffffffu, up) && j > 0;
+      if (j > 0 && ok) ok = mbar_wait(&bar_o[g], (uint32_t)((j - 1) & 1), a.err);
       pt_fence_after();
       if (resc) {
         const float nm = up ? mx : m;
@@ -556,53 +557,49 @@ __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs
         l *= al;
         m = nm;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {  // this half's 64 of O's 128 columns
+        for (int c = 0; c < 8; ++c) {
           uint32_t o[16];
-          const uint32_t oc = tl + kPtColO + 64u * (uint32_t)half + 16u * (uint32_t)c;
-          pt_ld16(oc, o);
+          pt_ld16(tl + kPtColO + 16u * (uint32_t)c, o);
           pt_ld_wait();
 #pragma unroll
           for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * al);
-          pt_st16(oc, o);
+          pt_st16(tl + kPtColO + 16u * (uint32_t)c, o);
         }
         pt_st_wait();
       } else if (up) {
         m = mx;  // the first tile: no O yet
       }
       const float ms = m == -INFINITY ? 0.f : m;
-      const uint32_t pbase = prow;
       float lp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {  // 8 keys per core-matrix row: hi at P, lo at P + 16 KB
+      for (int gg = 0; gg < 8; ++gg) {  // 8 keys per core-matrix row: hi at P, lo at P + 16 KB
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(s[8 * g + 2 * e] - ms), p1 = fast_exp2(s[8 * g + 2 * e + 1] - ms);
+          const float p0 = fast_exp2(s[8 * gg + 2 * e] - ms), p1 = fast_exp2(s[8 * gg + 2 * e + 1] - ms);
           lp[e] += p0 + p1;
           split_half2(p0, p1, hi[e], lo[e]);
         }
-        pt_sts128(pbase + (uint32_t)g * 128u, hi[0], hi[1], hi[2], hi[3]);
-        pt_sts128(pbase + kPtM * kPtN * 2 + (uint32_t)g * 128u, lo[0], lo[1], lo[2], lo[3]);
+        pt_sts128(pbase + (uint32_t)gg * 128u, hi[0], hi[1], hi[2], hi[3]);
+        pt_sts128(pbase + kPtM * kPtN * 2 + (uint32_t)gg * 128u, lo[0], lo[1], lo[2], lo[3]);
       }
       l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
       pt_fence_async();
       pt_fence_before();
-      mbar_arrive(bar_p);
+      mbar_arrive(&bar_p[g]);
     }
-    // the row sum over both halves, then the last O: normalise and store this half's columns
-    xch[half * 128 + row] = l;
-    named_bar_sync(1, 256);
-    l += xch[(half ^ 1) * 128 + row];
-    if (ntile > 0 && ok) ok = mbar_wait(bar_o, (uint32_t)((ntile - 1) & 1), a.err);
+    // the last O_g: normalise and store this row
+    if (nt > 0 && ok) ok = mbar_wait(&bar_o[g], (uint32_t)((nt - 1) & 1), a.err);
     pt_fence_after();
     const float il = 1.f / l;
-    float* orow = a.out + (((size_t)b * a.Hq + hq) * a.T + (size_t)min(qrow, a.T - 1)) * 128 + 64 * half;
+    const bool live = (g ? rowsB : rowsA) > row;
+    float* orow = a.out + (((size_t)b * a.Hq + hq) * a.T + (size_t)min(qrow, a.T - 1)) * 128;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 8; ++c) {
       uint32_t o[16];
-      pt_ld16(tl + kPtColO + 64u * (uint32_t)half + 16u * (uint32_t)c, o);
+      pt_ld16(tl + kPtColO + 16u * (uint32_t)c, o);
       pt_ld_wait();
-      if (qrow < a.T) {
+      if (live && nt > 0) {
 #pragma unroll
         for (int e = 0; e < 16; e += 4)
           *reinterpret_cast<float4*>(orow + 16 * c + e) =
@@ -610,7 +607,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs
                           __uint_as_float(o[e + 3]) * il);
       }
     }
-    if (half == 0 && a.lse && qrow < a.T) a.lse[((size_t)b * a.Hq + hq) * a.T + qrow] = (m + log2f(l)) * 0.6931471805599453f;
+    if (live && nt > 0 && a.lse) a.lse[((size_t)b * a.Hq + hq) * a.T + qrow] = (m + log2f(l)) * 0.6931471805599453f;
   }
   pt_fence_before();
   __syncthreads();
@@ -631,8 +628,7 @@ cudaError_t launch_prefill_d(const PfArgs& a, int batch, cudaStream_t s) {
   if (D == 128) {  // tensor cores with TMEM accumulators
     e = ensure_smem_limit(reinterpret_cast<const void*>(prefill_attend_tc_kernel), kPtSmem);
     if (e != cudaSuccess) return e;
-    const int nq = (a.T + kPtM - 1) / kPtM;
-    prefill_attend_tc_kernel<<<dim3(nq, a.Hq, batch), kPtThreads, kPtSmem, s>>>(a, nq);
+    prefill_attend_tc_kernel<<<dim3(a.nb, a.Hq, batch), kPtThreads, kPtSmem, s>>>(a, a.nb);
     return cudaGetLastError();
   }
   const size_t smem = (size_t)kPfStages * 2 * kPfKTile * D * 2 + (size_t)kPfMaxRouted * 4;
