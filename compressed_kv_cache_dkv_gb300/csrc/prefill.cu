@@ -312,33 +312,34 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_attend_kernel(PfArgs a)
 // (A: the block's first 128 queries, B: the rest) that share every K and V tile, so
 // a tile crosses from L2 once for 256 rows.  Warps 0-3 own group A's rows and warps
 // 4-7 group B's, one row per thread in tensor-memory lane 32 (w % 4) + lane; warp 9
-// streams the 64-key K and V tiles with cp.async into a three-stage ring: a stage
-// takes tile t once the products of tile t - 3 have read it, and each lane's copies
+// streams the 64-key K and V tiles with cp.async into a four-stage ring: a stage
+// takes tile t once the products of tile t - 4 have read it, and each lane's copies
 // arrive on the stage's "loaded" barrier by themselves when they land
 // (cp.async.mbarrier.arrive), so no arrival waits on a later product; lane 0 of
-// warp 8 issues the products of both groups, never waiting for one:
+// warp 8 issues group A's products and lane 0 of warp 10 group B's:
 //   S_gj = Q_g K_j^T   M = 128 queries, N = 64 keys, K = 128     (TMEM, two buffers per group)
-//   O_g += P_gj V_j    M = 128, N = 128 channels, K = 64 keys    (TMEM, P as fp16 hi + lo)
-// All operands sit in shared memory as 8x8 core matrices without swizzle: Q and
-// K_j K-major (rows = queries / keys, 16-byte rows of 8 channels), V_j the same
-// bytes read MN-major, P_gj K-major (rows = queries, 8 keys a core-matrix row).
-// Group A stops after the block's second own tile (keys past its last query).
-// Online softmax in base 2 with a lazy rescale: the row maximum moves only when a
-// score exceeds it by kPtSlack, and O is rescaled in tensor memory then.  S_{j+1}
-// runs on the tensor cores while the rows work on S_j; P_gj is written once O_{g,j-1}
-// has read P_{g,j-1}.
-constexpr int kPtThreads = 320;  // 8 softmax warps (two groups), the MMA warp, the load warp
-constexpr int kPtM = 128, kPtN = 64, kPtStages = 3;
+//   O_g += P_gj V_j    M = 128, N = 128 channels, K = 64 keys    (P from TMEM, V from shared memory)
+// Q and K_j sit in shared memory as 8x8 core matrices without swizzle, K-major (rows
+// = queries / keys, 16-byte rows of 8 channels); V_j is the same bytes read MN-major.
+// The rows write P_gj (fp16 hi in columns 0-31, lo in 32-63, two keys a column) over
+// the S_gj they have just read, and the tensor cores take it from there as the A
+// operand.  Each issuing thread runs S_{g,j+1}, then O_{g,j}: while one group's rows
+// turn S into P, the tensor cores run the other group's products, and neither
+// issuing thread waits for the other group.  S_{g,j+1} overwrites P_{g,j-1}, so it is
+// issued once O_{g,j-1} is done.  Online softmax in base 2 with a lazy rescale: the row maximum
+// moves only when a score exceeds it by kPtSlack, and only then do the rows wait for
+// O_{g,j-1} and rescale O in tensor memory.  Group A stops after the block's second
+// own tile (keys past its last query).
+constexpr int kPtThreads = 352;  // 8 softmax warps (two groups), the load warp, one MMA-issuing warp per group
+constexpr int kPtM = 128, kPtN = 64, kPtStages = 4;
 constexpr float kPtSlack = 8.f;
-constexpr uint32_t kPtTile = kPtN * 128 * 2;                    // one K or V tile: 16 KB
-constexpr uint32_t kPtQ = kPtM * 128 * 2;                       // one group's Q: 32 KB
-constexpr uint32_t kPtPBuf = 2 * kPtM * kPtN * 2;               // one group's P: hi [128 x 64] | lo, 32 KB
-constexpr uint32_t kPtOffQ = 0;                                 // Q_A | Q_B
-constexpr uint32_t kPtOffKV = kPtOffQ + 2 * kPtQ;               // [stage][K | V]
-constexpr uint32_t kPtOffP = kPtOffKV + kPtStages * 2 * kPtTile; // P_A | P_B
-constexpr uint32_t kPtOffBar = kPtOffP + 2 * kPtPBuf;           // mbarriers, TMEM address
+constexpr uint32_t kPtTile = kPtN * 128 * 2;                      // one K or V tile: 16 KB
+constexpr uint32_t kPtQ = kPtM * 128 * 2;                         // one group's Q: 32 KB
+constexpr uint32_t kPtOffQ = 0;                                   // Q_A | Q_B
+constexpr uint32_t kPtOffKV = kPtOffQ + 2 * kPtQ;                 // [stage][K | V]
+constexpr uint32_t kPtOffBar = kPtOffKV + kPtStages * 2 * kPtTile; // mbarriers, TMEM address
 constexpr uint32_t kPtSmem = kPtOffBar + 256;
-constexpr uint32_t kPtTmemCols = 512;  // per group g: S buffers at 256 g + {0, 64}, O at 256 g + 128
+constexpr uint32_t kPtTmemCols = 512;  // per group g: S / P buffers at 256 g + {0, 64}, O at 256 g + 128
 constexpr uint32_t kPtColO = 128;
 
 __device__ inline uint64_t pt_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -349,11 +350,20 @@ __device__ inline uint64_t pt_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) 
 __device__ inline uint32_t pt_idesc(bool a_mn, bool b_mn, uint32_t n) {
   return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
+// A and B from shared-memory descriptors
 __device__ inline void pt_mma(uint32_t dt, uint64_t ad, uint64_t bd, uint32_t id, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dt),
       "l"(ad), "l"(bd), "r"(id), "r"(acc)
+      : "memory");
+}
+// A from tensor memory (row = lane, two 16-bit elements of K a column), B from a descriptor
+__device__ inline void pt_mma_ta(uint32_t dt, uint32_t at, uint64_t bd, uint32_t id, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(dt),
+      "r"(at), "l"(bd), "r"(id), "r"(acc)
       : "memory");
 }
 __device__ inline void pt_commit(uint64_t* bar) {
@@ -385,9 +395,6 @@ __device__ inline void pt_cp_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ inline void pt_cp_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ inline void pt_sts128(uint32_t addr, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
-  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
-}
 // byte offset of (row, 16-byte chunk cc) of a K-major [rows x 128] fp16 operand in core matrices
 __device__ inline uint32_t pt_core(int row, int cc) {
   return (uint32_t)((row >> 3) * 2048 + cc * 128 + (row & 7) * 16);
@@ -396,13 +403,13 @@ __device__ inline uint32_t pt_core(int row, int cc) {
 __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs a, int nqb) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
-  uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + kPtOffBar);  // [group][2] S_gj ready (commit)
-  uint64_t* bar_sf = bar_s + 4;                                      // [group][2] S_gj read by the group's rows
-  uint64_t* bar_p = bar_s + 8;                                       // [group] P_gj written by the group's rows
-  uint64_t* bar_o = bar_s + 10;                                      // [group] O_g += P_gj V_j done (commit)
-  uint64_t* bar_kv = bar_s + 12;                                     // [3] stage loaded (32 loader lanes)
-  uint64_t* bar_fr = bar_s + 15;                                     // [3] stage free again (commit)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_s + 18);
+  uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + kPtOffBar);  // [group][j % 2] S_gj ready (commit)
+  uint64_t* bar_p = bar_s + 4;                                       // [group][j % 2] P_gj written by the group's rows
+  uint64_t* bar_o = bar_s + 8;                                       // [group] O_g += P_gj V_j done (commit)
+  uint64_t* bar_end = bar_s + 10;                                    // [group] the group's last product done (commit)
+  uint64_t* bar_kv = bar_s + 12;                                     // [stage] loaded (32 loader lanes)
+  uint64_t* bar_fr = bar_kv + kPtStages;                             // [stage] free again (commit)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_fr + kPtStages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int i = nqb - 1 - (int)blockIdx.x;  // later query blocks (more keys without routing) first
   const int q0 = i * 256, hq = blockIdx.y, b = blockIdx.z;
@@ -419,15 +426,15 @@ __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs
   if (tid == 0) {
     for (int x = 0; x < 4; ++x) {
       mbar_init(&bar_s[x], 1);
-      mbar_init(&bar_sf[x], 128);
+      mbar_init(&bar_p[x], 128);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&bar_p[x], 128);
       mbar_init(&bar_o[x], 1);
+      mbar_init(&bar_end[x], 1);
     }
     for (int x = 0; x < kPtStages; ++x) {
       mbar_init(&bar_kv[x], 32);
-      mbar_init(&bar_fr[x], 1);
+      mbar_init(&bar_fr[x], 2);  // one commit from each group's issuing thread
     }
     fence_mbar_init();
   }
@@ -468,54 +475,56 @@ __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs
       }
     }
     for (int p = 0; p < ntile && ok; ++p) {
-      // stage p % 3 held tile p - 3: wait until every product that reads it is done
+      // stage p % 4 held tile p - 4: wait until every product that reads it is done
       if (p >= kPtStages) ok = mbar_wait(&bar_fr[p % kPtStages], (uint32_t)(((p / kPtStages) - 1) & 1), a.err);
       if (!ok) break;
       load_kv(p);
       pt_cp_arrive(&bar_kv[p % kPtStages]);
     }
     pt_cp_wait_all();
-  } else if (warp == 8) {
-    // =========================== tensor-core issue (lane 0)
-    if (lane == 0 && ntile > 0) {
+  } else if (warp == 8 || warp == 10) {
+    // =========================== tensor-core issue: lane 0 of warp 8 for group A, of warp 10 for group B
+    const int g = warp == 8 ? 0 : 1, nt = g ? ntB : ntA;
+    if (lane == 0) {
       const uint32_t id_s = pt_idesc(false, false, kPtN), id_o = pt_idesc(false, true, 128);
-      auto issue_s = [&](int j) {  // S_gj = Q_g K_j^T into buffer j % 2 of each group that takes tile j
+      const uint64_t qdesc = pt_sdesc(sb + kPtOffQ + (uint32_t)g * kPtQ, 128u, 2048u);
+      const uint32_t tg = tmem + 256u * (uint32_t)g;
+      auto issue_s = [&](int j) {  // S_gj = Q_g K_j^T into buffer j % 2
         if (ok) ok = mbar_wait(&bar_kv[j % kPtStages], (uint32_t)((j / kPtStages) & 1), a.err);
         pt_fence_async();  // the landed cp.async bytes, seen through the barrier, for the tensor cores
+        // the buffer holds P_{g,j-2}: O_{g,j-2} has to be done reading it
+        if (j >= 2 && ok) ok = mbar_wait(&bar_o[g], (uint32_t)((j - 2) & 1), a.err);
         pt_fence_after();
+        if (!ok) return;
         const uint64_t kdesc = pt_sdesc(sb + kPtOffKV + (uint32_t)(j % kPtStages) * 2u * kPtTile, 128u, 2048u);
-        for (int g = 0; g < 2; ++g) {
-          if (j >= (g ? ntB : ntA)) continue;
-          if (j >= 2 && ok) ok = mbar_wait(&bar_sf[2 * g + (j & 1)], (uint32_t)(((j - 2) >> 1) & 1), a.err);  // S_{g,j-2} read
-          pt_fence_after();
-          const uint64_t qdesc = pt_sdesc(sb + kPtOffQ + (uint32_t)g * kPtQ, 128u, 2048u);
-          const uint32_t dt = tmem + 256u * (uint32_t)g + (uint32_t)(j & 1) * kPtN;
+        const uint32_t dt = tg + (uint32_t)(j & 1) * kPtN;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            pt_mma(dt, qdesc + (uint64_t)(ks * 16), kdesc + (uint64_t)(ks * 16), id_s, ks > 0);
-          pt_commit(&bar_s[2 * g + (j & 1)]);
-        }
+        for (int ks = 0; ks < 8; ++ks) pt_mma(dt, qdesc + (uint64_t)(ks * 16), kdesc + (uint64_t)(ks * 16), id_s, ks > 0);
+        pt_commit(&bar_s[2 * g + (j & 1)]);
       };
-      issue_s(0);
-      for (int j = 0; j < ntile && ok; ++j) {
-        if (j + 1 < ntile) issue_s(j + 1);
+      auto issue_o = [&](int j) {  // O_g += P_gj V_j, P from S_gj's buffer
+        if (ok) ok = mbar_wait(&bar_p[2 * g + (j & 1)], (uint32_t)((j >> 1) & 1), a.err);
+        pt_fence_after();
+        if (!ok) return;
         const uint64_t vdesc = pt_sdesc(sb + kPtOffKV + (uint32_t)(j % kPtStages) * 2u * kPtTile + kPtTile, 2048u, 128u);
-        for (int g = 0; g < 2 && ok; ++g) {
-          if (j >= (g ? ntB : ntA)) continue;
-          ok = mbar_wait(&bar_p[g], (uint32_t)(j & 1), a.err);  // P_gj written
-          pt_fence_after();
-          if (!ok) break;
-          const uint32_t pb = sb + kPtOffP + (uint32_t)g * kPtPBuf;
-          const uint64_t ph = pt_sdesc(pb, 128u, 1024u), pl = pt_sdesc(pb + kPtM * kPtN * 2, 128u, 1024u);
-          const uint32_t dt = tmem + 256u * (uint32_t)g + kPtColO;
+        const uint32_t pt = tg + (uint32_t)(j & 1) * kPtN, dt = tg + kPtColO;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            pt_mma(dt, ph + (uint64_t)(ks * 16), vdesc + (uint64_t)(ks * 256), id_o, (j > 0 || ks > 0) ? 1u : 0u);
+        for (int ks = 0; ks < 4; ++ks)
+          pt_mma_ta(dt, pt + 8u * (uint32_t)ks, vdesc + (uint64_t)(ks * 256), id_o, (j > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) pt_mma(dt, pl + (uint64_t)(ks * 16), vdesc + (uint64_t)(ks * 256), id_o, 1u);
-          pt_commit(&bar_o[g]);
-        }
-        pt_commit(&bar_fr[j % kPtStages]);  // every product that reads tile j is issued
+        for (int ks = 0; ks < 4; ++ks) pt_mma_ta(dt, pt + 32u + 8u * (uint32_t)ks, vdesc + (uint64_t)(ks * 256), id_o, 1u);
+        pt_commit(&bar_o[g]);
+        if (j == nt - 1) pt_commit(&bar_end[g]);
+      };
+      // a stage is free once both groups' products of its tile are done: each thread commits once
+      // per tile it takes, and twice where the other group has no such tile
+      const int nt_other = g ? ntA : ntB;
+      if (nt > 0) issue_s(0);
+      for (int j = 0; j < nt && ok; ++j) {
+        if (j + 1 < nt) issue_s(j + 1);
+        issue_o(j);
+        pt_commit(&bar_fr[j % kPtStages]);
+        if (j >= nt_other) pt_commit(&bar_fr[j % kPtStages]);
       }
     }
   } else {
@@ -525,7 +534,6 @@ __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs
     const uint32_t tl = tmem + ((uint32_t)(rw * 32) << 16) + 256u * (uint32_t)g;
     const float slog2 = a.scale_log2;
     float m = -INFINITY, l = 0.f;
-    const uint32_t pbase = sb + kPtOffP + (uint32_t)g * kPtPBuf + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 16u;
     for (int j = 0; j < nt; ++j) {
       if (ok) ok = mbar_wait(&bar_s[2 * g + (j & 1)], (uint32_t)((j >> 1) & 1), a.err);
       pt_fence_after();
@@ -534,28 +542,43 @@ __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs
 #pragma unroll
       for (int c = 0; c < 4; ++c) pt_ld16(sc + 16 * c, r[c]);
       pt_ld_wait();
-      pt_fence_before();
-      mbar_arrive(&bar_sf[2 * g + (j & 1)]);  // S_gj may be overwritten by S_{g,j+2}
-      const int k0 = j < 4 * n_r ? 0 : q0 + (j - 4 * n_r) * kPtN;  // routed tiles: every key is earlier
-      // keys k0 + c valid for c < nv: before the prompt's end, and causal in the own block
-      const int nv = j < 4 * n_r ? kPtN : min(a.T, qrow + 1) - k0;
-      float s[64], mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (j >= 4 * n_r) {  // the own block: keys k0 + c valid for c < nv (causal, before the prompt's end)
+        const int k0 = q0 + (j - 4 * n_r) * kPtN, nv = min(a.T, qrow + 1) - k0;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        s[c] = c < nv ? __uint_as_float(r[c >> 4][c & 15]) * slog2 : -INFINITY;
-        mxp[c & 3] = fmaxf(mxp[c & 3], s[c]);
+        for (int c = 0; c < 64; ++c)
+          if (c >= nv) r[c >> 4][c & 15] = 0xff800000u;  // -inf
       }
-      const float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
-      // O_{g,j-1} done: P_g's buffer is free and O_g may be rescaled
+      float mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mxp[c & 3] = fmaxf(mxp[c & 3], __uint_as_float(r[c >> 4][c & 15]));
+      // scaling by slog2 > 0 keeps the order, so the scaled maximum is the maximum scaled
+      const float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])) * slog2;
       const bool up = mx > m + kPtSlack;
       const bool resc = __any_sync(0xffffffffu, up) && j > 0;
-      if (j > 0 && ok) ok = mbar_wait(&bar_o[g], (uint32_t)((j - 1) & 1), a.err);
-      pt_fence_after();
-      if (resc) {
-        const float nm = up ? mx : m;
-        const float al = fast_exp2(m - nm);
-        l *= al;
-        m = nm;
+      const float nm = up ? mx : m;
+      const float al = nm == -INFINITY ? 1.f : fast_exp2(m - nm);  // the factor on l and O (1 where m stays)
+      m = nm;
+      const float ms = m == -INFINITY ? 0.f : m;
+      // P_gj over S_gj: hi words in columns 0-31, lo words in 32-63 (keys 2w and 2w + 1 in word w)
+      float lp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int k = 32 * c + 2 * e;
+          const float p0 = fast_exp2(fmaf(__uint_as_float(r[k >> 4][k & 15]), slog2, -ms));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(r[k >> 4][(k & 15) + 1]), slog2, -ms));
+          lp[e & 3] += p0 + p1;
+          split_half2(p0, p1, hi[e], lo[e]);
+        }
+        pt_st16(sc + 16u * (uint32_t)c, hi);
+        pt_st16(sc + 32u + 16u * (uint32_t)c, lo);
+      }
+      l = fmaf(l, al, (lp[0] + lp[1]) + (lp[2] + lp[3]));
+      if (resc) {  // O_{g,j-1} done, then O *= al in tensor memory
+        if (ok) ok = mbar_wait(&bar_o[g], (uint32_t)((j - 1) & 1), a.err);
+        pt_fence_after();
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t o[16];
@@ -565,31 +588,13 @@ __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs
           for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * al);
           pt_st16(tl + kPtColO + 16u * (uint32_t)c, o);
         }
-        pt_st_wait();
-      } else if (up) {
-        m = mx;  // the first tile: no O yet
       }
-      const float ms = m == -INFINITY ? 0.f : m;
-      float lp[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int gg = 0; gg < 8; ++gg) {  // 8 keys per core-matrix row: hi at P, lo at P + 16 KB
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(s[8 * gg + 2 * e] - ms), p1 = fast_exp2(s[8 * gg + 2 * e + 1] - ms);
-          lp[e] += p0 + p1;
-          split_half2(p0, p1, hi[e], lo[e]);
-        }
-        pt_sts128(pbase + (uint32_t)gg * 128u, hi[0], hi[1], hi[2], hi[3]);
-        pt_sts128(pbase + kPtM * kPtN * 2 + (uint32_t)gg * 128u, lo[0], lo[1], lo[2], lo[3]);
-      }
-      l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
-      pt_fence_async();
+      pt_st_wait();
       pt_fence_before();
-      mbar_arrive(&bar_p[g]);
+      mbar_arrive(&bar_p[2 * g + (j & 1)]);
     }
-    // the last O_g: normalise and store this row
-    if (nt > 0 && ok) ok = mbar_wait(&bar_o[g], (uint32_t)((nt - 1) & 1), a.err);
+    // the group's last product: normalise and store this row
+    if (nt > 0 && ok) ok = mbar_wait(&bar_end[g], 0u, a.err);
     pt_fence_after();
     const float il = 1.f / l;
     const bool live = (g ? rowsB : rowsA) > row;
