@@ -315,22 +315,23 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_attend_kernel(PfArgs a)
 // streams the 64-key K and V tiles with cp.async into a four-stage ring: a stage
 // takes tile t once the products of tile t - 4 have read it, and each lane's copies
 // arrive on the stage's "loaded" barrier by themselves when they land
-// (cp.async.mbarrier.arrive), so no arrival waits on a later product; lane 0 of
-// warp 8 issues group A's products and lane 0 of warp 10 group B's:
+// (cp.async.mbarrier.arrive), so no arrival waits on a later product.  Each
+// tcgen05.mma holds its issuing thread for about 75 cycles, so four threads issue:
+// lane 0 of warps 8 and 11 the S products of groups A and B, of warps 10 and 12 their
+// O products:
 //   S_gj = Q_g K_j^T   M = 128 queries, N = 64 keys, K = 128     (TMEM, two buffers per group)
 //   O_g += P_gj V_j    M = 128, N = 128 channels, K = 64 keys    (P from TMEM, V from shared memory)
 // Q and K_j sit in shared memory as 8x8 core matrices without swizzle, K-major (rows
 // = queries / keys, 16-byte rows of 8 channels); V_j is the same bytes read MN-major.
 // The rows write P_gj (fp16 hi in columns 0-31, lo in 32-63, two keys a column) over
 // the S_gj they have just read, and the tensor cores take it from there as the A
-// operand.  Each issuing thread runs S_{g,j+1}, then O_{g,j}: while one group's rows
-// turn S into P, the tensor cores run the other group's products, and neither
-// issuing thread waits for the other group.  S_{g,j+1} overwrites P_{g,j-1}, so it is
-// issued once O_{g,j-1} is done.  Online softmax in base 2 with a lazy rescale: the row maximum
-// moves only when a score exceeds it by kPtSlack, and only then do the rows wait for
-// O_{g,j-1} and rescale O in tensor memory.  Group A stops after the block's second
-// own tile (keys past its last query).
-constexpr int kPtThreads = 352;  // 8 softmax warps (two groups), the load warp, one MMA-issuing warp per group
+// operand.  While one group's rows turn S into P, the tensor cores run the other
+// group's products, and no issuing thread waits for another.  S_{g,j} overwrites
+// P_{g,j-2}, so it is issued once O_{g,j-2} is done.  Online softmax in base 2 with a
+// lazy rescale: the row maximum moves only when a score exceeds it by kPtSlack, and
+// only then do the rows wait for O_{g,j-1} and rescale O in tensor memory.  Group A
+// stops after the block's second own tile (keys past its last query).
+constexpr int kPtThreads = 416;  // 8 softmax warps (two groups), the load warp, S- and O-issuing warps per group
 constexpr int kPtM = 128, kPtN = 64, kPtStages = 4;
 constexpr float kPtSlack = 8.f;
 constexpr uint32_t kPtTile = kPtN * 128 * 2;                      // one K or V tile: 16 KB
@@ -405,9 +406,9 @@ __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs
   const uint32_t sb = smem_u32(smem);
   uint64_t* bar_s = reinterpret_cast<uint64_t*>(smem + kPtOffBar);  // [group][j % 2] S_gj ready (commit)
   uint64_t* bar_p = bar_s + 4;                                       // [group][j % 2] P_gj written by the group's rows
-  uint64_t* bar_o = bar_s + 8;                                       // [group] O_g += P_gj V_j done (commit)
-  uint64_t* bar_end = bar_s + 10;                                    // [group] the group's last product done (commit)
-  uint64_t* bar_kv = bar_s + 12;                                     // [stage] loaded (32 loader lanes)
+  uint64_t* bar_o = bar_s + 8;                                       // [group][j % 2] O_g += P_gj V_j done (commit)
+  uint64_t* bar_end = bar_s + 12;                                    // [group] the group's last product done (commit)
+  uint64_t* bar_kv = bar_s + 14;                                     // [stage] loaded (32 loader lanes)
   uint64_t* bar_fr = bar_kv + kPtStages;                             // [stage] free again (commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_fr + kPtStages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
@@ -427,14 +428,12 @@ __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs
     for (int x = 0; x < 4; ++x) {
       mbar_init(&bar_s[x], 1);
       mbar_init(&bar_p[x], 128);
-    }
-    for (int x = 0; x < 2; ++x) {
       mbar_init(&bar_o[x], 1);
-      mbar_init(&bar_end[x], 1);
     }
+    for (int x = 0; x < 2; ++x) mbar_init(&bar_end[x], 1);
     for (int x = 0; x < kPtStages; ++x) {
       mbar_init(&bar_kv[x], 32);
-      mbar_init(&bar_fr[x], 2);  // one commit from each group's issuing thread
+      mbar_init(&bar_fr[x], 4);  // one commit from each issuing thread
     }
     fence_mbar_init();
   }
@@ -482,49 +481,52 @@ __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs
       pt_cp_arrive(&bar_kv[p % kPtStages]);
     }
     pt_cp_wait_all();
-  } else if (warp == 8 || warp == 10) {
-    // =========================== tensor-core issue: lane 0 of warp 8 for group A, of warp 10 for group B
-    const int g = warp == 8 ? 0 : 1, nt = g ? ntB : ntA;
+  } else if (warp == 8 || warp >= 10) {
+    // =========================== tensor-core issue, lane 0 of: warp 8 S_A, 10 O_A, 11 S_B, 12 O_B
+    const int g = warp >= 11 ? 1 : 0, nt = g ? ntB : ntA, nt_other = g ? ntA : ntB;
+    const bool o_side = warp == 10 || warp == 12;
     if (lane == 0) {
-      const uint32_t id_s = pt_idesc(false, false, kPtN), id_o = pt_idesc(false, true, 128);
-      const uint64_t qdesc = pt_sdesc(sb + kPtOffQ + (uint32_t)g * kPtQ, 128u, 2048u);
       const uint32_t tg = tmem + 256u * (uint32_t)g;
-      auto issue_s = [&](int j) {  // S_gj = Q_g K_j^T into buffer j % 2
-        if (ok) ok = mbar_wait(&bar_kv[j % kPtStages], (uint32_t)((j / kPtStages) & 1), a.err);
-        pt_fence_async();  // the landed cp.async bytes, seen through the barrier, for the tensor cores
-        // the buffer holds P_{g,j-2}: O_{g,j-2} has to be done reading it
-        if (j >= 2 && ok) ok = mbar_wait(&bar_o[g], (uint32_t)((j - 2) & 1), a.err);
-        pt_fence_after();
-        if (!ok) return;
-        const uint64_t kdesc = pt_sdesc(sb + kPtOffKV + (uint32_t)(j % kPtStages) * 2u * kPtTile, 128u, 2048u);
-        const uint32_t dt = tg + (uint32_t)(j & 1) * kPtN;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) pt_mma(dt, qdesc + (uint64_t)(ks * 16), kdesc + (uint64_t)(ks * 16), id_s, ks > 0);
-        pt_commit(&bar_s[2 * g + (j & 1)]);
-      };
-      auto issue_o = [&](int j) {  // O_g += P_gj V_j, P from S_gj's buffer
-        if (ok) ok = mbar_wait(&bar_p[2 * g + (j & 1)], (uint32_t)((j >> 1) & 1), a.err);
-        pt_fence_after();
-        if (!ok) return;
-        const uint64_t vdesc = pt_sdesc(sb + kPtOffKV + (uint32_t)(j % kPtStages) * 2u * kPtTile + kPtTile, 2048u, 128u);
-        const uint32_t pt = tg + (uint32_t)(j & 1) * kPtN, dt = tg + kPtColO;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          pt_mma_ta(dt, pt + 8u * (uint32_t)ks, vdesc + (uint64_t)(ks * 256), id_o, (j > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) pt_mma_ta(dt, pt + 32u + 8u * (uint32_t)ks, vdesc + (uint64_t)(ks * 256), id_o, 1u);
-        pt_commit(&bar_o[g]);
-        if (j == nt - 1) pt_commit(&bar_end[g]);
-      };
-      // a stage is free once both groups' products of its tile are done: each thread commits once
-      // per tile it takes, and twice where the other group has no such tile
-      const int nt_other = g ? ntA : ntB;
-      if (nt > 0) issue_s(0);
-      for (int j = 0; j < nt && ok; ++j) {
-        if (j + 1 < nt) issue_s(j + 1);
-        issue_o(j);
+      // a stage is free once every product of its tile is done: each thread commits once per
+      // tile its group takes, and twice where the other group has no such tile
+      auto release = [&](int j) {
         pt_commit(&bar_fr[j % kPtStages]);
         if (j >= nt_other) pt_commit(&bar_fr[j % kPtStages]);
+      };
+      if (!o_side) {
+        const uint32_t id_s = pt_idesc(false, false, kPtN);
+        const uint64_t qdesc = pt_sdesc(sb + kPtOffQ + (uint32_t)g * kPtQ, 128u, 2048u);
+        for (int j = 0; j < nt && ok; ++j) {  // S_gj = Q_g K_j^T into buffer j % 2
+          ok = mbar_wait(&bar_kv[j % kPtStages], (uint32_t)((j / kPtStages) & 1), a.err);
+          pt_fence_async();  // the landed cp.async bytes, seen through the barrier, for the tensor cores
+          // the buffer holds P_{g,j-2}: O_{g,j-2} has to be done reading it
+          if (j >= 2 && ok) ok = mbar_wait(&bar_o[2 * g + (j & 1)], (uint32_t)(((j - 2) >> 1) & 1), a.err);
+          pt_fence_after();
+          if (!ok) break;
+          const uint64_t kdesc = pt_sdesc(sb + kPtOffKV + (uint32_t)(j % kPtStages) * 2u * kPtTile, 128u, 2048u);
+          const uint32_t dt = tg + (uint32_t)(j & 1) * kPtN;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) pt_mma(dt, qdesc + (uint64_t)(ks * 16), kdesc + (uint64_t)(ks * 16), id_s, ks > 0);
+          pt_commit(&bar_s[2 * g + (j & 1)]);
+          release(j);
+        }
+      } else {
+        const uint32_t id_o = pt_idesc(false, true, 128);
+        for (int j = 0; j < nt && ok; ++j) {  // O_g += P_gj V_j, P from S_gj's buffer
+          ok = mbar_wait(&bar_p[2 * g + (j & 1)], (uint32_t)((j >> 1) & 1), a.err);
+          pt_fence_after();
+          if (!ok) break;
+          const uint64_t vdesc = pt_sdesc(sb + kPtOffKV + (uint32_t)(j % kPtStages) * 2u * kPtTile + kPtTile, 2048u, 128u);
+          const uint32_t pt = tg + (uint32_t)(j & 1) * kPtN, dt = tg + kPtColO;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            pt_mma_ta(dt, pt + 8u * (uint32_t)ks, vdesc + (uint64_t)(ks * 256), id_o, (j > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) pt_mma_ta(dt, pt + 32u + 8u * (uint32_t)ks, vdesc + (uint64_t)(ks * 256), id_o, 1u);
+          pt_commit(&bar_o[2 * g + (j & 1)]);
+          if (j == nt - 1) pt_commit(&bar_end[g]);
+          release(j);
+        }
       }
     }
   } else {
@@ -577,7 +579,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) prefill_attend_tc_kernel(PfArgs
       }
       l = fmaf(l, al, (lp[0] + lp[1]) + (lp[2] + lp[3]));
       if (resc) {  // O_{g,j-1} done, then O *= al in tensor memory
-        if (ok) ok = mbar_wait(&bar_o[g], (uint32_t)((j - 1) & 1), a.err);
+        if (ok) ok = mbar_wait(&bar_o[2 * g + ((j - 1) & 1)], (uint32_t)(((j - 1) >> 1) & 1), a.err);
         pt_fence_after();
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
