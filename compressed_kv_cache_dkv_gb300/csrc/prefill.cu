@@ -52,28 +52,72 @@ struct PfArgs {
 // ---------------------------------------------------------------- stats
 template <int D>
 __global__ void __launch_bounds__(256) prefill_stats_kernel(PfArgs a) {
+  // 16-byte loads: D / 8 threads cover a row, 256 / (D / 8) rows at a time; the per-row-slot
+  // partials meet in shared memory and are reduced in a fixed order
+  constexpr int kTpr = D / 8, kRows = 256 / kTpr;
+  __shared__ float red[2][kRows][D];
   const int j = blockIdx.x, u = blockIdx.y, b = u / a.Hkv, h = u % a.Hkv;
   const int t0 = j * 256, n = min(256, a.T - t0);
-  const int tid = threadIdx.x;
-  if (tid < D) {  // the block's key box, channel tid
-    const __half* k = a.K + ((size_t)u * a.T + t0) * D + tid;
-    float lo = INFINITY, hi = -INFINITY;
-    for (int t = 0; t < n; ++t) {
-      const float x = __half2float(k[(size_t)t * D]);
-      lo = fminf(lo, x);
-      hi = fmaxf(hi, x);
+  const int tid = threadIdx.x, rs = tid / kTpr, c0 = (tid % kTpr) * 8;
+  float lo[8], hi[8], sm[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    lo[e] = INFINITY;
+    hi[e] = -INFINITY;
+    sm[e] = 0.f;
+  }
+  const __half* kb = a.K + ((size_t)u * a.T + t0) * D + c0;
+#pragma unroll 4
+  for (int t = rs; t < n; t += kRows) {  // the block's key box
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(kb + (size_t)t * D));
+    const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(h2[e]);
+      lo[2 * e] = fminf(lo[2 * e], f.x);
+      hi[2 * e] = fmaxf(hi[2 * e], f.x);
+      lo[2 * e + 1] = fminf(lo[2 * e + 1], f.y);
+      hi[2 * e + 1] = fmaxf(hi[2 * e + 1], f.y);
+    }
+  }
+  for (int g = 0; g < a.G; ++g) {  // the sum of the group's queries over the block
+    const __half* qb = a.q + (((size_t)b * a.Hq + (size_t)h * a.G + g) * a.T + t0) * D + c0;
+#pragma unroll 4
+    for (int t = rs; t < n; t += kRows) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(qb + (size_t)t * D));
+      const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(h2[e]);
+        sm[2 * e] += f.x;
+        sm[2 * e + 1] += f.y;
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    red[0][rs][c0 + e] = lo[e];
+    red[1][rs][c0 + e] = hi[e];
+  }
+  __syncthreads();
+  if (tid < D) {
+    float l = INFINITY, m = -INFINITY;
+    for (int r = 0; r < kRows; ++r) {
+      l = fminf(l, red[0][r][tid]);
+      m = fmaxf(m, red[1][r][tid]);
     }
     float* box = a.kbox + ((size_t)u * a.nb + j) * 2 * D;
-    box[tid] = lo;
-    box[D + tid] = hi;
-  } else if (tid < 2 * D) {  // the block's mean query over the group, channel tid - D
-    const int c = tid - D;
-    float s = 0.f;
-    for (int g = 0; g < a.G; ++g) {
-      const __half* qp = a.q + (((size_t)b * a.Hq + (size_t)h * a.G + g) * a.T + t0) * D + c;
-      for (int t = 0; t < n; ++t) s += __half2float(qp[(size_t)t * D]);
-    }
-    a.qbar[((size_t)u * a.nb + j) * D + c] = s * (a.scale_log2 / 1.4426950408889634f) / (float)(a.G * n);
+    box[tid] = l;
+    box[D + tid] = m;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[0][rs][c0 + e] = sm[e];
+  __syncthreads();
+  if (tid < D) {  // the block's mean query over the group
+    float x = 0.f;
+    for (int r = 0; r < kRows; ++r) x += red[0][r][tid];
+    a.qbar[((size_t)u * a.nb + j) * D + tid] = x * (a.scale_log2 / 1.4426950408889634f) / (float)(a.G * n);
   }
 }
 
@@ -100,11 +144,20 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(PfArgs a) {
   }
   for (int c = tid; c < D; c += blockDim.x) qb[c] = a.qbar[((size_t)u * a.nb + i) * D + c];
   __syncthreads();
-  for (int j = tid; j < i; j += blockDim.x) {
-    const float* box = a.kbox + ((size_t)u * a.nb + j) * 2 * D;
-    float s = 0.f;
-    for (int c = 0; c < D; ++c) s += fmaxf(qb[c] * box[c], qb[c] * box[D + c]);
-    keys[j] = pf_key(s);
+  {  // one warp per earlier block: lanes over the channels, then a butterfly sum
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int j = warp; j < i; j += (int)(blockDim.x >> 5)) {
+      const float* box = a.kbox + ((size_t)u * a.nb + j) * 2 * D;
+      float s = 0.f;
+#pragma unroll
+      for (int x = 0; x < D / 32; ++x) {
+        const int c = lane + 32 * x;
+        s += fmaxf(qb[c] * __ldg(box + c), qb[c] * __ldg(box + D + c));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) keys[j] = pf_key(s);
+    }
   }
   __syncthreads();
   for (int j = tid; j < i; j += blockDim.x) {  // rank = blocks ahead by (bound desc, index asc)
