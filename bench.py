@@ -694,7 +694,7 @@ def main():
         configs["prefill32k"] = {
             "workload": f"block-sparse prefill, batch {Bp}, {Hq}q/{Hkv}kv x d{d}, {T} tokens, top-K {ktop} earlier "
                         f"256-token blocks per query block (random fp16 q, K, V)",
-            "kernel": "prefill_stats + prefill_route + prefill_attend (mma.sync, fp16 operands, fp32 accumulation)",
+            "kernel": "prefill_stats + prefill_route + prefill_attend_tc (tcgen05, fp16 operands, P as fp16 hi + lo, fp32 accumulation in tensor memory)",
             "ms_per_call": ms_s, "tokens_per_s": Bp * T / (ms_s / 1e3),
             "tflops": flops(ktop) / (ms_s / 1e3) / 1e12,
             "roofline": {"bound": "tensor", "achieved": flops(ktop) / (ms_s / 1e3) / 1e12, "peak": tf_peak,
