@@ -455,6 +455,8 @@ def main():
             res["ms"] = statistics.median(times)
             res["clocks"] = clk.summary()
             if stage_timing:
+                # (1) every attention launch between a pair of events of its own; the bracket itself
+                #     costs about 4 us of launch and event latency (measured in (3))
                 ev = [[(ext.new(), ext.new()) for _ in range(n)] for _ in range(steps)]
                 g2 = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g2, stream=stream):
@@ -466,9 +468,58 @@ def main():
                 stream.synchronize()
                 t2, clk2 = timed(g2, 1)
                 res["ms_ev"] = t2[0]
-                res["attend_ms"] = [ext.elapsed_ms(ev[k][i][0], ev[k][i][1]) for k in range(steps) for i in range(n)]
-                res["clocks_ev"] = clk2.summary()
+                res["attend_ms_bracketed"] = [ext.elapsed_ms(ev[k][i][0], ev[k][i][1])
+                                              for k in range(steps) for i in range(n)]
                 del g2
+                # (2) the same attention launches back to back: per step every call's router first
+                #     (each call keeps its routed list in a workspace of its own), then all the
+                #     attention grids in plain stream order (none overlaps the one before it) between
+                #     one pair of events, then the combines; time per launch = region / calls
+                wss = [torch.zeros_like(self.ws) for _ in range(n)]
+                evr = [(ext.new(), ext.new()) for _ in range(steps)]
+                g3 = torch.cuda.CUDAGraph()
+                dkv.dkv_debug_set_launch(False)
+                try:
+                    with torch.cuda.graph(g3, stream=stream):
+                        for k in range(steps):
+                            for i in range(n):
+                                dkv.dkv_decode_route(self.descs[i], self.qs[i], self.caches[i], top_k, wss[i],
+                                                     stream=sh)
+                            ext.record(evr[k][0], sh)
+                            for i in range(n):
+                                dkv.dkv_decode_blocks(self.descs[i], self.qs[i], self.caches[i], top_k, wss[i],
+                                                      stream=sh)
+                            ext.record(evr[k][1], sh)
+                            for i in range(n):
+                                dkv.dkv_decode_combine(self.descs[i], top_k, self.outs[i], wss[i],
+                                                       lse=self.lses[i], stream=sh)
+                finally:
+                    dkv.dkv_debug_set_launch(True)
+                with torch.cuda.stream(stream):
+                    g3.replay()
+                stream.synchronize()
+                _, clk3 = timed(g3, 1)
+                res["attend_ms"] = [ext.elapsed_ms(a, b) / n for a, b in evr]
+                res["clocks_ev"] = clk3.summary()
+                for x in wss:
+                    st_, word_ = dkv.dkv_get_error(x, stream=sh)
+                    if st_ != dkv.DKV_OK:
+                        raise RuntimeError(f"decode raised device error word {word_:#x}")
+                del g3, wss
+                # (3) the bracket of (1) around an empty kernel
+                evb = [(ext.new(), ext.new()) for _ in range(n)]
+                g4 = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g4, stream=stream):
+                    for i in range(n):
+                        ext.record(evb[i][0], sh)
+                        torch.cuda._sleep(0)
+                        ext.record(evb[i][1], sh)
+                with torch.cuda.stream(stream):
+                    g4.replay()
+                    g4.replay()
+                stream.synchronize()
+                res["bracket_ms"] = statistics.median(ext.elapsed_ms(a, b) for a, b in evb)
+                del g4
             if latency:
                 g1 = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g1, stream=stream):
@@ -599,7 +650,8 @@ def main():
             A.free()
             log(f"[bench] {alt_layout} layout timed: {AR['ms'] / K_steps:.3f} ms/step")
             alt = {"layout": alt_layout, "kernel": kernel_names[alt_layout], "ms": AR["ms"], "ms_ev": AR["ms_ev"],
-                   "attend_ms_mean": statistics.fmean(AR["attend_ms"]), "clocks": AR["clocks"]}
+                   "attend_ms_mean": statistics.fmean(AR["attend_ms"]),
+                   "attend_ms_bracketed": statistics.fmean(AR["attend_ms_bracketed"]), "clocks": AR["clocks"]}
 
     # ---------------- the other workloads: 32k, 8k and the 16k top-K sweep beside the dense fp16 kernel
     configs = {}
@@ -618,6 +670,7 @@ def main():
                     "frac_call": cb / (R_["ms"] / steps_c / 1e3) / 1e9 / peak,
                     "steps_per_replay": steps_c,
                     "attend_us_mean": att_us, "attend_bytes_per_launch": ab / S_.n_layers,
+                    "attend_us_bracketed": 1e3 * statistics.fmean(R_["attend_ms_bracketed"]),
                     "attend_frac": (ab / S_.n_layers) / (att_us / 1e6) / 1e9 / peak,
                     "latency_us": R_["latency_us"],
                     "replays": len(R_["ms_replays"]), "clocks": R_["clocks"]}
@@ -824,6 +877,7 @@ def main():
     e2e_serial_value = whole_job_rate(world, queries_per_step, e2e_steps, e2e_ms_serial)
 
     att_ms_mean = statistics.fmean(attend_ms)
+    att_ms_bracketed = statistics.fmean(R["attend_ms_bracketed"])
     achieved_gbs = (att_bytes_step / n_layers) / (att_ms_mean / 1e3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "attend_traffic.json")
@@ -853,8 +907,13 @@ def main():
                      "peak": peak, "unit": "GB/s", "frac": achieved_gbs / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback",
                      "bytes_per_launch": att_bytes_step / n_layers, "mean_launch_us": att_ms_mean * 1e3,
-                     "timed_in": "a second replay of the same K steps as stage calls, with events around "
-                                 "every attention launch", "launches_per_call": max(launches_per_call),
+                     "timed_in": "a replay of the same K steps as stage calls: per step every call's router, "
+                                 "then all the attention grids back to back in plain stream order between one "
+                                 "pair of events (time per launch = region / calls), then the combines",
+                     "mean_launch_us_bracketed": att_ms_bracketed * 1e3,
+                     "bracketed_in": "a replay with events around every attention launch",
+                     "bracket_overhead_us": R["bracket_ms"] * 1e3,
+                     "launches_per_call": max(launches_per_call),
                      "ms_per_step_with_events": ms_ev / K_steps,
                      "clocks": R["clocks_ev"]},
         "e2e": {"value": e2e_value, "unit": "queries/s", "steps": e2e_steps,
@@ -869,7 +928,7 @@ def main():
         "other_layout": None if alt is None else {
             "layout": alt["layout"], "kernel": alt["kernel"], "ms_per_step": alt["ms"] / K_steps,
             "value": whole_job_rate(world, queries_per_step, K_steps, alt["ms"]),
-            "mean_call_us": alt["attend_ms_mean"] * 1e3,
+            "mean_call_us": alt["attend_ms_mean"] * 1e3, "mean_call_us_bracketed": alt["attend_ms_bracketed"] * 1e3,
             "achieved_gbs": (att_bytes_step / n_layers) / (alt["attend_ms_mean"] / 1e3) / 1e9,
             "frac": (att_bytes_step / n_layers) / (alt["attend_ms_mean"] / 1e3) / 1e9 / peak,
             "ms_per_step_with_events": alt["ms_ev"] / K_steps, "clocks": alt["clocks"]},

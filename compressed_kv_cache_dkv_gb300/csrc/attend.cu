@@ -1238,7 +1238,7 @@ cudaError_t launch_one(const AttendArgs& a, int grid, size_t smem, cudaStream_t 
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap with the router's grid
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = programmatic_launch() ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, attend_kernel<D, R8S, ROPE>, a);
 }
 
@@ -1308,6 +1308,11 @@ void debug_limits(int* stop_after, uint32_t* wait_polls) {
   *stop_after = g_stop_after.load(std::memory_order_relaxed);
   *wait_polls = g_wait_polls.load(std::memory_order_relaxed);
 }
+namespace {
+std::atomic<int> g_programmatic{1};
+}  // namespace
+bool programmatic_launch() { return g_programmatic.load(std::memory_order_relaxed) != 0; }
+void set_programmatic_launch(bool on) { g_programmatic.store(on ? 1 : 0, std::memory_order_relaxed); }
 void set_debug_limits(int stop_after, uint32_t wait_polls) {
   g_stop_after.store(stop_after < 0 ? -1 : stop_after, std::memory_order_relaxed);
   g_wait_polls.store(wait_polls ? wait_polls : kWaitLimit, std::memory_order_relaxed);

@@ -785,7 +785,7 @@ cudaError_t launch_attend_tc(const Layout& L, const DecodePlan& P, int n_q_heads
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap with the router's grid
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = programmatic_launch() ? 1 : 0;
   cudaError_t e = cudaLaunchKernelEx(&cfg, attend_tc_kernel, a);
   if (e != cudaSuccess || out == nullptr) return e;
   return launch_combine(L, P, L.units / n_kv_heads, n_q_heads, n_kv_heads, a.partials, out, lse, s);

@@ -456,6 +456,11 @@ int dkv_debug_set_limits(int32_t stop_after_chunks, uint32_t wait_polls) {
   return DKV_OK;
 }
 
+int dkv_debug_set_launch(int32_t programmatic) {
+  set_programmatic_launch(programmatic != 0);
+  return DKV_OK;
+}
+
 int dkv_get_error(void* workspace, void* stream, uint32_t* word) {
   if (!workspace || !word) return DKV_ERR_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

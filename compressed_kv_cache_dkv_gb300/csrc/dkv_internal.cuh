@@ -459,6 +459,9 @@ int sm_count();  // multiprocessors of the current device
 // chunks a CTA's producer issues at most (negative: all) and polls of a bounded wait.
 void debug_limits(int* stop_after, uint32_t* wait_polls);
 void set_debug_limits(int stop_after, uint32_t wait_polls);
+// whether the decode grids (attention, combine) are launched as programmatic dependents
+bool programmatic_launch();
+void set_programmatic_launch(bool on);
 // Raise `func`'s dynamic shared-memory limit to at least `bytes` on the current
 // device: once per (kernel, device), again only when a larger size is asked for.
 // Thread-safe.

@@ -338,7 +338,7 @@ cudaError_t launch_combine_records(int units, int n_items, int n_q_heads, int n_
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = programmatic_launch() ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, combine_kernel, n_items, n_q_heads / n_kv_heads, n_q_heads, n_kv_heads, d,
                             partials, out, lse);
 }

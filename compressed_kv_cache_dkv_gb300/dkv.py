@@ -40,7 +40,7 @@ EXPORTED = (
     "dkv_decode_workspace_bytes", "dkv_decode_launches", "dkv_decode_attend", "dkv_decode_route", "dkv_decode_blocks",
     "dkv_decode_combine",
     "dkv_dense_workspace_bytes", "dkv_dense_decode", "dkv_get_error", "dkv_decode_attend_noalloc",
-    "dkv_append_workspace_bytes", "dkv_append", "dkv_debug_set_limits", "dkv_prefill_routed_slots",
+    "dkv_append_workspace_bytes", "dkv_append", "dkv_debug_set_limits", "dkv_debug_set_launch", "dkv_prefill_routed_slots",
     "dkv_prefill_workspace_bytes", "dkv_prefill_attend",
 )
 
@@ -111,6 +111,7 @@ def lib() -> ctypes.CDLL:
         L.dkv_append_workspace_bytes.argtypes = [pdesc]
         L.dkv_append.argtypes = [pdesc, vp, vp, i32, vp, vp, sz, vp]
         L.dkv_debug_set_limits.argtypes = [i32, ctypes.c_uint32]
+        L.dkv_debug_set_launch.argtypes = [i32]
         L.dkv_prefill_routed_slots.restype = i32
         L.dkv_prefill_routed_slots.argtypes = [i32, i32]
         L.dkv_prefill_workspace_bytes.restype = sz
@@ -344,6 +345,12 @@ def dkv_debug_set_limits(stop_after_chunks: int = -1, wait_polls: int = 0) -> No
     after `stop_after_chunks` chunks, bounded waits give up after `wait_polls` polls;
     (-1, 0) restores the defaults."""
     _check(lib().dkv_debug_set_limits(int(stop_after_chunks), int(wait_polls)), "dkv_debug_set_limits")
+
+
+def dkv_debug_set_launch(programmatic: bool = True) -> None:
+    """Timing aid: False launches the decode grids in plain stream order (no programmatic
+    overlap with the grid before them); True restores the default."""
+    _check(lib().dkv_debug_set_launch(1 if programmatic else 0), "dkv_debug_set_launch")
 
 
 def dkv_get_error(workspace: torch.Tensor, stream=None) -> tuple[int, int]:

@@ -375,7 +375,8 @@ DKV_API int dkv_dense_decode(int32_t batch, int32_t n_q_heads, int32_t n_kv_head
  *           blocks ascending, -1 in the unused slots
  *   workspace / ws_bytes  device scratch of dkv_prefill_workspace_bytes(...)
  * Supported: head_dim 64 or 128, n_q_heads / n_kv_heads <= 8, 1 <= T <= 262400.
- * The products run on the tensor cores (mma.sync, fp16 operands, fp32 accumulation).
+ * The products run on the tensor cores with fp16 operands and fp32 accumulation:
+ * tcgen05 with tensor-memory accumulators at head_dim 128, mma.sync at head_dim 64.
  */
 DKV_API int32_t dkv_prefill_routed_slots(int32_t T, int32_t top_k);
 DKV_API size_t dkv_prefill_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
@@ -398,6 +399,18 @@ DKV_API int dkv_prefill_attend(int32_t batch, int32_t n_q_heads, int32_t n_kv_he
  * DKV_OK.
  */
 DKV_API int dkv_debug_set_limits(int32_t stop_after_chunks, uint32_t wait_polls);
+
+/*
+ * Timing aid (no counterpart in the pages): with programmatic = 0 the decode
+ * grids that are normally programmatic dependents of the grid before them (the
+ * attention grid of both layouts, and the combine grid) are launched in plain
+ * stream order from the next launch on: each starts once the previous grid on
+ * the stream has finished, so that consecutive attention grids of a timing loop
+ * cannot overlap.  Results are unchanged.  programmatic = 1 restores the
+ * default.  The setting is process-wide and read when a grid is launched (or
+ * captured into a CUDA graph).  Returns DKV_OK.
+ */
+DKV_API int dkv_debug_set_launch(int32_t programmatic);
 
 /*
  * Synchronise `stream`, read the device error word kept in the header of
