@@ -137,9 +137,6 @@ __device__ void jacobi(float* A, float* Z, int m, int ld, float* red, float2* cs
   }
 }
 
-// packed upper-triangular index of (i, j), i <= j, for an n x n symmetric matrix
-__device__ inline int pk_base(int i, int n) { return i * n - (i * (i - 1)) / 2 - i; }
-
 template <int D>
 __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
   extern __shared__ __align__(16) uint8_t sm[];
@@ -285,18 +282,15 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
     __syncthreads();
     jacobi(H, Z, n, ldh, red, cs, pr);
   } else {
-    // packed Gram
+    // the Gram's upper triangle as 8x8 tiles: tile (TI, TJ), TI <= TJ, is the owner's, at
+    // 64 tid floats (rows of the tile contiguous)
     if (owner) {
 #pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const int i = 8 * TI + x;
-        const int bi = pk_base(i, n);
+      for (int x = 0; x < 8; ++x)
 #pragma unroll
-        for (int y = 0; y < 8; ++y) {
-          const int j = 8 * TJ + y;
-          if (i <= j) R1[bi + j] = acc[x][y];
-        }
-      }
+        for (int y = 0; y < 8; y += 4)
+          *reinterpret_cast<float4*>(R1 + tid * 64 + 8 * x + y) =
+              make_float4(acc[x][y], acc[x][y + 1], acc[x][y + 2], acc[x][y + 3]);
     }
     // start block: fixed +-1 pattern
     const int ldq = n + 1;
@@ -306,23 +300,52 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
     }
     __syncthreads();
     for (int it = 0; it <= kIters + 1; ++it) {
-      // ---- Y = G Q (warps 0..15 own rows w + 16 ii; lanes own columns lane, lane + 32)
-      float y[n / 16][2];
+      // ---- Y = G Q: warps 0..15 own the 8-row blocks w and w + 16, lanes the columns lane and
+      // lane + 32; per 8-row block J of Q one Gram tile (a broadcast to the warp), read
+      // transposed below the diagonal
+      float y[2][8][2];
 #pragma unroll
-      for (int ii = 0; ii < n / 16; ++ii) y[ii][0] = y[ii][1] = 0.f;
+      for (int bb = 0; bb < 2; ++bb)
+#pragma unroll
+        for (int x = 0; x < 8; ++x) y[bb][x][0] = y[bb][x][1] = 0.f;
       const bool gw = warp < 16;
       const int c0 = lane, c1 = lane + 32;
       if (gw) {
-        for (int j = 0; j < n; ++j) {
-          const float q0 = c0 < p ? Qb[c0 * ldq + j] : 0.f;
-          const float q1 = c1 < p ? Qb[c1 * ldq + j] : 0.f;
-          const int bj = pk_base(j, n);
 #pragma unroll
-          for (int ii = 0; ii < n / 16; ++ii) {
-            const int i = warp + 16 * ii;
-            const float g = i <= j ? R1[pk_base(i, n) + j] : R1[bj + i];
-            y[ii][0] = fmaf(g, q0, y[ii][0]);
-            y[ii][1] = fmaf(g, q1, y[ii][1]);
+        for (int bb = 0; bb < 2; ++bb) {
+          const int I = warp + 16 * bb;
+          for (int J = 0; J < n8; ++J) {
+            float q0[8], q1[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              q0[e] = c0 < p ? Qb[c0 * ldq + 8 * J + e] : 0.f;
+              q1[e] = c1 < p ? Qb[c1 * ldq + 8 * J + e] : 0.f;
+            }
+            const int lo = I < J ? I : J, hi = I < J ? J : I;
+            const float4* T4 = reinterpret_cast<const float4*>(R1 + (lo * n8 - (lo * (lo - 1)) / 2 + (hi - lo)) * 64);
+            if (I <= J) {  // G[8I + x][8J + e] = T[x][e]
+#pragma unroll
+              for (int x = 0; x < 8; ++x) {
+                const float4 ga = T4[2 * x], gb = T4[2 * x + 1];
+                const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  y[bb][x][0] = fmaf(g[e], q0[e], y[bb][x][0]);
+                  y[bb][x][1] = fmaf(g[e], q1[e], y[bb][x][1]);
+                }
+              }
+            } else {  // G[8I + x][8J + e] = T[e][x] of tile (J, I)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float4 ga = T4[2 * e], gb = T4[2 * e + 1];
+                const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                  y[bb][x][0] = fmaf(g[x], q0[e], y[bb][x][0]);
+                  y[bb][x][1] = fmaf(g[x], q1[e], y[bb][x][1]);
+                }
+              }
+            }
           }
         }
       }
@@ -331,11 +354,13 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
         // Q <- orth(Y): classical Gram-Schmidt, twice, column by column
         if (gw) {
 #pragma unroll
-          for (int ii = 0; ii < n / 16; ++ii) {
-            const int i = warp + 16 * ii;
-            if (c0 < p) Qb[c0 * ldq + i] = y[ii][0];
-            if (c1 < p) Qb[c1 * ldq + i] = y[ii][1];
-          }
+          for (int bb = 0; bb < 2; ++bb)
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              const int i = 8 * (warp + 16 * bb) + x;
+              if (c0 < p) Qb[c0 * ldq + i] = y[bb][x][0];
+              if (c1 < p) Qb[c1 * ldq + i] = y[bb][x][1];
+            }
         }
         __syncthreads();
         for (int c = 0; c < p; ++c) {
@@ -384,11 +409,13 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
         // ---- Rayleigh-Ritz: Y into R1 (the Gram is no longer needed), H = Q^T Y
         if (gw) {
 #pragma unroll
-          for (int ii = 0; ii < n / 16; ++ii) {
-            const int i = warp + 16 * ii;
-            if (c0 < p) R1[c0 * ldq + i] = y[ii][0];
-            if (c1 < p) R1[c1 * ldq + i] = y[ii][1];
-          }
+          for (int bb = 0; bb < 2; ++bb)
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              const int i = 8 * (warp + 16 * bb) + x;
+              if (c0 < p) R1[c0 * ldq + i] = y[bb][x][0];
+              if (c1 < p) R1[c1 * ldq + i] = y[bb][x][1];
+            }
         }
         __syncthreads();
         H = R1 + p * ldq;
@@ -554,7 +581,7 @@ CPlan plan(const Layout& L) {
   if (c.full) {
     r1 = (uint32_t)(2 * c.n * (c.n + 1) * 4);
   } else {
-    const uint32_t gram = (uint32_t)(c.n * (c.n + 1) / 2 * 4);
+    const uint32_t gram = (uint32_t)((c.n / 8) * (c.n / 8 + 1) / 2 * 64 * 4);  // 8x8 tiles of the upper triangle
     const uint32_t rr = (uint32_t)((c.p * (c.n + 1) + 2 * c.p * (c.p + 1)) * 4);
     r1 = gram > rr ? gram : rr;
   }
