@@ -93,7 +93,9 @@ __device__ void jacobi(float* A, float* Z, int m, int ld, float* red, float2* cs
     }
     off = block_sum(off, red);
     dia = block_sum(dia, red + 32);
-    if (!(off > 1e-13f * dia) || dia == 0.f) break;
+    // converged for fp32 (and far below the fp16 the factors are stored in): the
+    // off-diagonal norm is at most 1e-5 of the diagonal's
+    if (!(off > 1e-10f * dia) || dia == 0.f) break;
     for (int round = 0; round < m - 1; ++round) {
       for (int k = tid; k < half; k += nt) {
         int p, q;
@@ -135,6 +137,89 @@ __device__ void jacobi(float* A, float* Z, int m, int ld, float* red, float2* cs
       __syncthreads();
     }
   }
+}
+
+// Orthonormalises columns b0 .. b0 + nb - 1 (nb <= 8) of Q (column c at Q + c ldq, RPL
+// rows a lane: row lane + 32 k) inside one warp, one column after the other, each
+// projected twice against the block's earlier columns (classical Gram-Schmidt, twice);
+// the columns before the block are already projected out.  A column that is numerically
+// in the span of the earlier ones (its norm falls below 1e-5 of what it was) restarts
+// from a fixed +-1 pattern projected against every earlier column, and is zero if that
+// fails too.
+template <int RPL>
+__device__ __noinline__ void orth_block_warp(float* Q, int ldq, int b0, int nb, int lane) {
+  float x[8][RPL];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) x[j][k] = j < nb ? Q[(b0 + j) * ldq + lane + 32 * k] : 0.f;
+  auto warp_sum = [](float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+  };
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j >= nb) break;
+    float n0 = 0.f;
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) n0 = fmaf(x[j][k], x[j][k], n0);
+    const float nrm0 = sqrtf(warp_sum(n0));
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      for (int pass = 0; pass < 2; ++pass) {
+        if (attempt == 1) {  // a restarted column: the columns before the block as well
+          for (int cc = 0; cc < b0; ++cc) {
+            float sd = 0.f;
+#pragma unroll
+            for (int k = 0; k < RPL; ++k) sd = fmaf(Q[cc * ldq + lane + 32 * k], x[j][k], sd);
+            sd = warp_sum(sd);
+#pragma unroll
+            for (int k = 0; k < RPL; ++k) x[j][k] = fmaf(-sd, Q[cc * ldq + lane + 32 * k], x[j][k]);
+          }
+        }
+        float sd[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          sd[jj] = 0.f;
+          if (jj < j) {
+#pragma unroll
+            for (int k = 0; k < RPL; ++k) sd[jj] = fmaf(x[jj][k], x[j][k], sd[jj]);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj)
+            if (jj < j) sd[jj] += __shfl_xor_sync(0xffffffffu, sd[jj], o);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+          if (jj < j) {
+#pragma unroll
+            for (int k = 0; k < RPL; ++k) x[j][k] = fmaf(-sd[jj], x[jj][k], x[j][k]);
+          }
+      }
+      float n1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < RPL; ++k) n1 = fmaf(x[j][k], x[j][k], n1);
+      const float nrm = sqrtf(warp_sum(n1));
+      if (nrm > 1e-5f * nrm0 && nrm > 1e-30f) {
+        const float inv = 1.f / nrm;
+#pragma unroll
+        for (int k = 0; k < RPL; ++k) x[j][k] *= inv;
+        break;
+      }
+#pragma unroll
+      for (int k = 0; k < RPL; ++k)
+        x[j][k] = attempt == 0 ? ((hash32((uint32_t)((lane + 32 * k) * 7 + (b0 + j) * 104729 + 99991)) & 1u) ? 1.f : -1.f)
+                               : 0.f;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j < nb) {
+#pragma unroll
+      for (int k = 0; k < RPL; ++k) Q[(b0 + j) * ldq + lane + 32 * k] = x[j][k];
+    }
 }
 
 template <int D>
@@ -351,7 +436,7 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
       }
       __syncthreads();
       if (it <= kIters) {
-        // Q <- orth(Y): classical Gram-Schmidt, twice, column by column
+        // Q <- orth(Y): classical Gram-Schmidt, twice
         if (gw) {
 #pragma unroll
           for (int bb = 0; bb < 2; ++bb)
@@ -363,47 +448,36 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
             }
         }
         __syncthreads();
-        for (int c = 0; c < p; ++c) {
-          float* qc = Qb + c * ldq;
-          float v0 = 0.f;
-          for (int i = tid; i < n; i += nt) v0 += qc[i] * qc[i];
-          const float nrm0 = sqrtf(block_sum(v0, red));
-          for (int attempt = 0; attempt < 2; ++attempt) {
+        // 8 columns at a time: the block is projected twice against the columns before it
+        // (every warp shares the dot products and the update), then warp 0 orthonormalises
+        // the block's columns one after the other, twice against each earlier one
+        float* coef = ubuf;  // [64][8] projection coefficients (ubuf is idle until the U phase)
+        for (int b0 = 0; b0 < p; b0 += 8) {
+          const int nb = min(8, p - b0);
+          if (b0 > 0) {
             for (int pass = 0; pass < 2; ++pass) {
-              for (int cc = warp; cc < c; cc += nw) {
+              for (int e = warp; e < b0 * nb; e += nw) {
+                const int cc = e / nb, j = e % nb;
                 const float* qp = Qb + cc * ldq;
-                float s = 0.f;
-                for (int i = lane; i < n; i += 32) s = fmaf(qp[i], qc[i], s);
+                const float* qj = Qb + (b0 + j) * ldq;
+                float sd = 0.f;
+                for (int i = lane; i < n; i += 32) sd = fmaf(qp[i], qj[i], sd);
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == 0) vec[cc] = s;
+                for (int o = 16; o > 0; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
+                if (lane == 0) coef[cc * 8 + j] = sd;
               }
               __syncthreads();
-              for (int i = tid; i < n; i += nt) {
-                float v = qc[i];
-                for (int cc = 0; cc < c; ++cc) v = fmaf(-vec[cc], Qb[cc * ldq + i], v);
-                qc[i] = v;
+              for (int e = tid; e < nb * n; e += nt) {
+                const int j = e / n, i = e % n;
+                float v = Qb[(b0 + j) * ldq + i];
+                for (int cc = 0; cc < b0; ++cc) v = fmaf(-coef[cc * 8 + j], Qb[cc * ldq + i], v);
+                Qb[(b0 + j) * ldq + i] = v;
               }
               __syncthreads();
             }
-            float v1 = 0.f;
-            for (int i = tid; i < n; i += nt) v1 += qc[i] * qc[i];
-            const float nrm = sqrtf(block_sum(v1, red));
-            if (nrm > 1e-5f * nrm0 && nrm > 1e-30f) {
-              const float inv = 1.f / nrm;
-              for (int i = tid; i < n; i += nt) qc[i] *= inv;
-              __syncthreads();
-              break;
-            }
-            // numerically in the span of the previous columns: restart from a fixed pattern
-            if (attempt == 0) {
-              for (int i = tid; i < n; i += nt)
-                qc[i] = (hash32((uint32_t)(i * 7 + c * 104729 + 99991)) & 1u) ? 1.f : -1.f;
-            } else {
-              for (int i = tid; i < n; i += nt) qc[i] = 0.f;
-            }
-            __syncthreads();
           }
+          if (warp == 0) orth_block_warp<n / 32>(Qb, ldq, b0, nb, lane);
+          __syncthreads();
         }
       } else {
         // ---- Rayleigh-Ritz: Y into R1 (the Gram is no longer needed), H = Q^T Y
