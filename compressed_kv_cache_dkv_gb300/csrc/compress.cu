@@ -448,30 +448,64 @@ __global__ void __launch_bounds__(kCThreads, 1) compress_kernel(CArgs a) {
             }
         }
         __syncthreads();
-        // 8 columns at a time: the block is projected twice against the columns before it
-        // (every warp shares the dot products and the update), then warp 0 orthonormalises
-        // the block's columns one after the other, twice against each earlier one
-        float* coef = ubuf;  // [64][8] projection coefficients (ubuf is idle until the U phase)
+        // 8 columns at a time: the block is projected twice against the columns before it,
+        // then warp 0 orthonormalises the block's columns one after the other, twice against
+        // each earlier one.  For the projection the block also sits row-major in Yt (the
+        // staging area of X, idle here): a dot-product thread (earlier column cc, half of the
+        // rows) reads Q's column once and the block's row as two broadcast 16-byte loads,
+        // and an update thread (row i) takes every earlier column's 8 coefficients the same way.
+        float* Yt = reinterpret_cast<float*>(Xc);  // [n][8]
+        float* part = ubuf;                         // [2 halves][64][8] partial coefficients
         for (int b0 = 0; b0 < p; b0 += 8) {
           const int nb = min(8, p - b0);
           if (b0 > 0) {
-            for (int pass = 0; pass < 2; ++pass) {
-              for (int e = warp; e < b0 * nb; e += nw) {
-                const int cc = e / nb, j = e % nb;
-                const float* qp = Qb + cc * ldq;
-                const float* qj = Qb + (b0 + j) * ldq;
-                float sd = 0.f;
-                for (int i = lane; i < n; i += 32) sd = fmaf(qp[i], qj[i], sd);
+            for (int i = tid; i < n; i += nt) {
+              float v[8];
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
-                if (lane == 0) coef[cc * 8 + j] = sd;
+              for (int j = 0; j < 8; ++j) v[j] = j < nb ? Qb[(b0 + j) * ldq + i] : 0.f;
+              *reinterpret_cast<float4*>(Yt + 8 * i) = make_float4(v[0], v[1], v[2], v[3]);
+              *reinterpret_cast<float4*>(Yt + 8 * i + 4) = make_float4(v[4], v[5], v[6], v[7]);
+            }
+            __syncthreads();
+            for (int pass = 0; pass < 2; ++pass) {
+              if (tid < 2 * b0) {  // coefficients of column cc over one half of the rows
+                const int cc = tid % b0, hh = tid / b0;
+                const float* qp = Qb + cc * ldq;
+                float c8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int i = hh * (n / 2); i < (hh + 1) * (n / 2); ++i) {
+                  const float qv = qp[i];
+                  const float4 ya = *reinterpret_cast<const float4*>(Yt + 8 * i);
+                  const float4 yb = *reinterpret_cast<const float4*>(Yt + 8 * i + 4);
+                  c8[0] = fmaf(qv, ya.x, c8[0]); c8[1] = fmaf(qv, ya.y, c8[1]);
+                  c8[2] = fmaf(qv, ya.z, c8[2]); c8[3] = fmaf(qv, ya.w, c8[3]);
+                  c8[4] = fmaf(qv, yb.x, c8[4]); c8[5] = fmaf(qv, yb.y, c8[5]);
+                  c8[6] = fmaf(qv, yb.z, c8[6]); c8[7] = fmaf(qv, yb.w, c8[7]);
+                }
+                float* pc = part + (hh * 64 + cc) * 8;
+                *reinterpret_cast<float4*>(pc) = make_float4(c8[0], c8[1], c8[2], c8[3]);
+                *reinterpret_cast<float4*>(pc + 4) = make_float4(c8[4], c8[5], c8[6], c8[7]);
               }
               __syncthreads();
-              for (int e = tid; e < nb * n; e += nt) {
-                const int j = e / n, i = e % n;
-                float v = Qb[(b0 + j) * ldq + i];
-                for (int cc = 0; cc < b0; ++cc) v = fmaf(-coef[cc * 8 + j], Qb[cc * ldq + i], v);
-                Qb[(b0 + j) * ldq + i] = v;
+              for (int i = tid; i < n; i += nt) {  // row i of the block minus its projection
+                const float4 ya = *reinterpret_cast<const float4*>(Yt + 8 * i);
+                const float4 yb = *reinterpret_cast<const float4*>(Yt + 8 * i + 4);
+                float v[8] = {ya.x, ya.y, ya.z, ya.w, yb.x, yb.y, yb.z, yb.w};
+                for (int cc = 0; cc < b0; ++cc) {
+                  const float qv = Qb[cc * ldq + i];
+                  const float4 a0 = *reinterpret_cast<const float4*>(part + cc * 8);
+                  const float4 a1 = *reinterpret_cast<const float4*>(part + cc * 8 + 4);
+                  const float4 b0v = *reinterpret_cast<const float4*>(part + (64 + cc) * 8);
+                  const float4 b1v = *reinterpret_cast<const float4*>(part + (64 + cc) * 8 + 4);
+                  v[0] = fmaf(-(a0.x + b0v.x), qv, v[0]); v[1] = fmaf(-(a0.y + b0v.y), qv, v[1]);
+                  v[2] = fmaf(-(a0.z + b0v.z), qv, v[2]); v[3] = fmaf(-(a0.w + b0v.w), qv, v[3]);
+                  v[4] = fmaf(-(a1.x + b1v.x), qv, v[4]); v[5] = fmaf(-(a1.y + b1v.y), qv, v[5]);
+                  v[6] = fmaf(-(a1.z + b1v.z), qv, v[6]); v[7] = fmaf(-(a1.w + b1v.w), qv, v[7]);
+                }
+                *reinterpret_cast<float4*>(Yt + 8 * i) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(Yt + 8 * i + 4) = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  if (j < nb) Qb[(b0 + j) * ldq + i] = v[j];
               }
               __syncthreads();
             }
